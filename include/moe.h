@@ -1,0 +1,227 @@
+/*
+ * moe.h -- C ABI of libmoe: one routed mixture-of-experts feed-forward layer over
+ * block-quantised expert weights, hand-written CUDA for sm_103a (GB300).
+ *
+ * The layer (x[T,d], router W[d,E], expert gate/up [E,2f,d], down [E,d,f], top-k, an
+ * activation) is the one the pages keep returning to:
+ *   - "Running Gemma 4 26B at 5 tokens/s on a 13-year-old Xeon without a GPU"
+ *     (amuse.peoplentools.com), section "A three-step fix" / "Runtime graph fallback":
+ *     per-expert gate/up matmuls over a fused [n_embd, 2*n_ff, n_experts] tensor, gate
+ *     first and up second, then SiLU(gate)*up, over Q8_0 weights;
+ *   - "Running NVIDIA's new 120B Nemotron-3.5-Super on an 8GB GPU" (molayo1419.me),
+ *     sections "The single most important number: bytes per token" and "How the engine
+ *     works", steps 1 and 4: gateless latent experts (up 2688x1024, down 1024x2688,
+ *     ReLU^2) in NVFP4, a down matrix relaid out neuron-contiguous, and a down
+ *     projection that skips 16-neuron groups that are all zero; section "How we check
+ *     correctness": per-(token, expert) buffers combined in a fixed order.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device memory owned by the caller; the library
+ *     allocates nothing (the caller provides the workspace) and keeps no state besides
+ *     per-device kernel attributes set once.
+ *   - Calls are asynchronous and ordered on the given stream (NULL = legacy default).
+ *   - Arguments are validated on the host before anything is launched.  On an error
+ *     nothing is launched, outputs are untouched, and the status says why.  No C++
+ *     exception crosses this interface.
+ *   - Faults found inside a kernel (an expert index out of range in caller-supplied
+ *     routing) never trap: the kernel clamps, records a code in the workspace's error
+ *     word, and moe_get_device_status() reports it.
+ *   - Shapes: row counts and column counts must be multiples of 32 (Q8_0) or 64
+ *     (NVFP4); the layer needs d a multiple of 256 and f a multiple of 32 (Q8_0) or 64
+ *     (NVFP4).  Pointers must be 16-byte aligned.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t.  Declared here so that this header needs no CUDA header. */
+struct CUstream_st;
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* NULL pointer, k out of range, unknown enum value */
+    MOE_ERR_SHAPE = 2,         /* a dimension is not a supported multiple / too large */
+    MOE_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned */
+    MOE_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than the size query says */
+    MOE_ERR_UNSUPPORTED = 5,   /* combination not built (e.g. a layout for a format) */
+    MOE_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, attribute, copy) */
+    MOE_ERR_DEVICE_CHECK = 7   /* a kernel recorded an error in the workspace (see below) */
+} moe_status;
+
+typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_RELU2 = 1 } moe_act;
+typedef enum { MOE_W_Q8_0 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/*
+ * Byte layouts of one quantised matrix [rows, cols] (cols = the reduction dimension K).
+ *
+ * MOE_LAYOUT_CANONICAL
+ *   Q8_0 : blocks of 32 consecutive values along a row, row-major; each block is the
+ *          fp16 scale (little endian) then 32 int8 codes: 34 bytes per 32 values.
+ *   NVFP4: all E2M1 codes row-major, two per byte (even element in the low nibble),
+ *          then all E4M3 block scales row-major (one per 16 values).
+ * MOE_LAYOUT_DEVICE  (what moe_layer_forward reads for gate/up matrices, and for the
+ *                     down matrix in Q8_0)
+ *   Q8_0 : panel b = columns 32b..32b+31: the 32 codes of every row (rows in order),
+ *          then the fp16 scale of every row.  Panel size rows*34 bytes.
+ *   NVFP4: panel P = columns 64P..64P+63: the 32 code bytes of every row, then the 4
+ *          scale bytes of every row.  Panel size rows*36 bytes.
+ * MOE_LAYOUT_NEURON  (NVFP4 down matrices [d, f] only; what moe_layer_forward reads)
+ *   Nemotron page, "How the engine works", step 4: for each group g of 16 neurons
+ *   (columns), each neuron's codes for rows 0..rows-1 contiguous (rows/2 bytes, row r
+ *   in the low nibble of byte r/2 when r is even), then the rows scale bytes of the
+ *   group.  A pure byte permutation of the canonical layout, same size.
+ * Every layout of a matrix has the same size (moe_q8_0_bytes / moe_nvfp4_bytes); a
+ * stack of n_mat matrices is the matrices back to back.
+ */
+typedef enum { MOE_LAYOUT_CANONICAL = 0, MOE_LAYOUT_DEVICE = 1, MOE_LAYOUT_NEURON = 2 } moe_layout;
+
+/* Which expert kernels moe_layer_forward uses.  AUTO picks by tokens per expert. */
+typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GEMM = 2 } moe_path;
+
+/* Bytes of one quantised matrix: rows*cols/32*34 (Q8_0), rows*cols/2 + rows*cols/16
+ * (NVFP4).  Returns 0 for non-positive or non-multiple sizes. */
+size_t moe_q8_0_bytes(int64_t rows, int64_t cols);
+size_t moe_nvfp4_bytes(int64_t rows, int64_t cols);
+
+/*
+ * moe_quantize_q8_0 -- Q8_0 weight packer (the Xeon page's Q8_0 experts; block of 32
+ * int8 codes and one fp16 scale).  For every row and block of 32 along cols:
+ *   d = amax/127 (fp32), id = 1/d (0 when d = 0), q = round-half-away(x*id);
+ *   stored scale = fp16(d) rounded to nearest even; codes use the fp32 d.
+ * src   device, fp32 [n_mat][rows][cols] row-major.
+ * dst   device, n_mat * moe_q8_0_bytes(rows, cols) bytes, written in `layout`
+ *       (CANONICAL or DEVICE).
+ * Errors: INVALID_ARG (NULL, n_mat < 0, bad layout), SHAPE (rows or cols not a
+ * positive multiple of 32), ALIGNMENT, CUDA.
+ */
+moe_status moe_quantize_q8_0(const float* src, int64_t n_mat, int64_t rows, int64_t cols, moe_layout layout,
+                             void* dst, moe_stream_t stream);
+
+/*
+ * moe_pack_nvfp4 -- NVFP4 weight packer (Nemotron page: E2M1 values, one FP8 E4M3
+ * scale per 16 consecutive values, plus one fp32 scale per tensor).  Per matrix:
+ *   s_t = amax/(6*448) (1 when the matrix is all zero);
+ *   per 16 along cols: sb = E4M3(amax_b/(6*s_t)), round to nearest even, saturating;
+ *   per value: q = E2M1(x/(dec(sb)*s_t)), nearest even, saturating; zero codes +0.
+ * src           device, fp32 [n_mat][rows][cols].
+ * dst           device, n_mat * moe_nvfp4_bytes(rows, cols) bytes in `layout`
+ *               (CANONICAL, DEVICE or NEURON).
+ * tensor_scale  device, fp32 [n_mat]: s_t of each matrix (written).
+ * Errors: INVALID_ARG, SHAPE (rows a positive multiple of 32, cols of 64), ALIGNMENT,
+ * CUDA.
+ */
+moe_status moe_pack_nvfp4(const float* src, int64_t n_mat, int64_t rows, int64_t cols, moe_layout layout,
+                          void* dst, float* tensor_scale, moe_stream_t stream);
+
+/*
+ * moe_router_topk -- router projection, top-k and softmax over the selected logits
+ * (Inferentia page, "Wall 1": top-8 of 128 experts per token; the Nemotron page:
+ * top-22 of 512).
+ *   logit[t][e] = fp32 dot of x[t] and W[:, e] in one canonical order: 256 partial
+ *   sums (partial l takes i = l, l+256, ... in increasing i with fused multiply-add),
+ *   then a halving tree (h = 128..1: s_l += s_{l+h}).
+ *   Top-k: k rounds of "largest remaining logit, lower index on ties"; slot j holds the
+ *   j-th selection.  w[t][j] = exp(l_j - l_0) / sum_j' exp(l_j' - l_0), sum in slot order.
+ * x         device, [T][d], fp32 or bf16 (xt).
+ * W         device, fp32 [d][E] row-major.
+ * idx, w    device outputs, int32 [T][k] and fp32 [T][k].
+ * logits    device output, fp32 [T][E], or NULL.
+ * workspace device, moe_router_workspace_bytes(T, E) bytes (may be NULL when that is 0).
+ * Errors: INVALID_ARG (k < 1, k > E, k > 32, E > 1024), SHAPE (d not a multiple of
+ * 256), ALIGNMENT, WORKSPACE, CUDA.
+ */
+size_t moe_router_workspace_bytes(int64_t T, int64_t E);
+moe_status moe_router_topk(const void* x, moe_dtype xt, const float* W, int64_t T, int64_t d, int64_t E, int k,
+                           int32_t* idx, float* w, float* logits, void* workspace, size_t ws_bytes,
+                           moe_stream_t stream);
+
+/* Weights and shape of one layer.  All pointers are device memory. */
+typedef struct {
+    int64_t d;                    /* model width (K of gate/up, rows of down) */
+    int64_t f;                    /* expert width (neurons) */
+    int64_t E;                    /* experts */
+    int32_t k;                    /* experts per token */
+    int32_t act;                  /* moe_act: SWIGLU (gate/up 2f rows) or RELU2 (up f rows) */
+    int32_t wfmt;                 /* moe_wfmt */
+    int32_t path;                 /* moe_path */
+    const float* router_w;        /* fp32 [d][E] */
+    const void* w_gate_up;        /* E matrices [rows_gu][d], MOE_LAYOUT_DEVICE, back to back;
+                                     SwiGLU: rows 0..f-1 gate, f..2f-1 up */
+    const void* w_down;           /* E matrices [d][f]: Q8_0 MOE_LAYOUT_DEVICE, NVFP4 MOE_LAYOUT_NEURON */
+    const float* gate_up_tscale;  /* NVFP4: fp32 [E] tensor scales of the gate/up matrices */
+    const float* down_tscale;     /* NVFP4: fp32 [E] tensor scales of the down matrices */
+} moe_layer_desc;
+
+/* Optional copies of intermediate results (device pointers, each may be NULL). */
+typedef struct {
+    float* logits;     /* [T][E] fp32 (not written when routing is supplied) */
+    int32_t* idx;      /* [T][k] */
+    float* w;          /* [T][k] */
+    int32_t* offsets;  /* [E+1]: expert e owns sorted rows offsets[e]..offsets[e+1]-1 */
+    int32_t* perm;     /* [T*k]: pair id (t*k+j) at each sorted row */
+    int32_t* pos;      /* [T*k]: sorted row of each pair */
+    float* h;          /* [T*k][f] activations in sorted-row order */
+} moe_trace;
+
+/* Workspace bytes moe_layer_forward needs for up to T_max tokens; 0 on a bad desc. */
+size_t moe_layer_workspace_bytes(const moe_layer_desc* desc, int64_t T_max);
+
+/*
+ * moe_layer_forward -- one routed MoE layer:
+ *   out[t] = sum_{j<k} w[t][j] * Expert_{idx[t][j]}(x[t]), the sum in slot order j.
+ * Steps, all in this library's kernels: router + top-k + softmax (skipped when idx_in
+ * is given), histogram / prefix scan / stable scatter of the T*k pairs by expert
+ * (within an expert, pairs keep increasing t*k+j), grouped gate.up with the activation
+ * fused (SwiGLU: SiLU(gate)*up; ReLU^2: max(z,0)^2) and a mask of 16-neuron groups
+ * that hold a non-zero activation, a down projection that reads only those groups,
+ * and a fixed-order combine (no atomics: bitwise deterministic run to run).
+ * x          device [T][d], fp32 or bf16 (xt).
+ * idx_in     device int32 [T][k] precomputed routing, or NULL; w_in device fp32 [T][k]
+ *            (both or neither).  Entries outside [0, E) are clamped to a valid expert
+ *            and recorded as device error 1 (see moe_get_device_status).
+ * out        device fp32 [T][d] (written).
+ * workspace  device, at least moe_layer_workspace_bytes(desc, T) bytes, 256-byte
+ *            aligned, zero-filled before its first use (the library leaves its control
+ *            words zero again after every call).
+ * trace      optional copies of intermediates, or NULL.
+ * T = 0 returns MOE_OK and launches nothing.
+ * Errors: INVALID_ARG, SHAPE (d a multiple of 256 up to 65536; f a multiple of 32 (Q8_0) or
+ * 64 (NVFP4) up to 32768; E a multiple of 4 up to 1024), ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtype xt, int64_t T,
+                             const int32_t* idx_in, const float* w_in, float* out, void* workspace,
+                             size_t ws_bytes, const moe_trace* trace, moe_stream_t stream);
+
+/*
+ * moe_rmsnorm_bf16 -- glue between stacked layers: xo[t] = bf16(x[t] / sqrt(mean(x[t]^2)
+ * + eps)), no gain; the sum of squares uses a fixed reduction order.
+ * x device fp32 [T][d]; xo device bf16 bits [T][d].  Errors: INVALID_ARG, ALIGNMENT, CUDA.
+ */
+moe_status moe_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uint16_t* xo, moe_stream_t stream);
+
+/*
+ * moe_get_device_status -- synchronises `stream`, reads the error word of a layer
+ * workspace, clears it, and returns MOE_OK or MOE_ERR_DEVICE_CHECK (the device code in
+ * *device_code, may be NULL): 1 = an expert index outside [0, E) was clamped.
+ */
+moe_status moe_get_device_status(void* workspace, moe_stream_t stream, int32_t* device_code);
+
+/* A static string naming a status. */
+const char* moe_status_string(moe_status status);
+
+/* Version of this interface (major*10000 + minor*100 + patch). */
+int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

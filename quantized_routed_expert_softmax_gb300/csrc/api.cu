@@ -1,0 +1,369 @@
+// api.cu -- the C ABI of libmoe (include/moe.h): host-side validation, workspace layout
+// and the launch sequence of one MoE layer.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+
+// launchers (pack.cu, route.cu, gemv.cu)
+cudaError_t launch_q8_0_quantize(const float*, int64_t, int64_t, int64_t, int, void*, cudaStream_t);
+cudaError_t launch_nvfp4_pack(const float*, int64_t, int64_t, int64_t, int, void*, float*, cudaStream_t);
+cudaError_t launch_router_logits(const void*, int, const float*, int64_t, int64_t, int64_t, float*, cudaStream_t);
+cudaError_t launch_topk_softmax(const float*, int64_t, int64_t, int, int32_t*, float*, cudaStream_t);
+cudaError_t launch_route_small(const float*, const int32_t*, const float*, int64_t, int64_t, int, int,
+                               const Workspace&, cudaStream_t);
+cudaError_t launch_permute_large(const int32_t*, const float*, int64_t, int64_t, int, int, const Workspace&,
+                                 cudaStream_t);
+cudaError_t configure_gemv_kernels();
+cudaError_t launch_gate_up_gemv(const ExpertArgs&, int, int, int, cudaStream_t);
+cudaError_t launch_down_gemv(const ExpertArgs&, int, int, cudaStream_t);
+cudaError_t launch_combine(const float*, const int32_t*, const float*, int64_t, int, int64_t, int, int64_t, float*,
+                           cudaStream_t);
+cudaError_t launch_rmsnorm_bf16(const float*, int64_t, int64_t, float, uint16_t*, cudaStream_t);
+
+
+namespace {
+
+constexpr int64_t kMaxDim = 1 << 16;
+constexpr int64_t kMaxTokens = 1 << 20;
+constexpr int64_t kMaxF = 32768;     // group-mask words per slot fit the kernels' 64-word array
+constexpr int kSmallT = 32;          // route_small handles up to 32 tokens
+constexpr int kSmallPairs = 1024;    // ... and up to 1024 pairs
+constexpr size_t kSmemBudget = 96 * 1024;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Per-device one-time kernel attribute setup (dynamic shared memory above 48 KB).
+cudaError_t ensure_configured() {
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    e = configure_gemv_kernels();
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct Plan {
+    int64_t T, P;
+    int slot_cap;       // min(E, P)
+    int nchunk;
+    int gwords;
+    int tt_gu, tt_dn;
+    int ksplit;
+    int64_t y_rows;     // rows of the y partial buffer per split stride (P)
+    bool small_route;
+};
+
+int down_ksplit(const moe_layer_desc* d, int64_t P) {
+    if (P > 64) return 1;
+    const int64_t units = (d->wfmt == MOE_W_Q8_0) ? d->f / 32 : d->f / 16;
+    const int64_t want = (d->wfmt == MOE_W_Q8_0) ? 4 : 8;
+    return static_cast<int>(std::max<int64_t>(1, std::min(want, units)));
+}
+
+Plan make_plan(const moe_layer_desc* d, int64_t T) {
+    Plan p{};
+    p.T = T;
+    p.P = T * d->k;
+    p.slot_cap = static_cast<int>(std::min<int64_t>(d->E, p.P));
+    p.nchunk = static_cast<int>((p.P + 1023) / 1024);
+    p.gwords = static_cast<int>((d->f / 16 + 31) / 32);
+    const int64_t tmax = std::max<int64_t>(1, std::min<int64_t>(8, T));
+    p.tt_gu = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tmax, kSmemBudget / (4 * d->d))));
+    const int64_t dn_cap = (d->wfmt == MOE_W_NVFP4) ? 4 : 8;
+    p.tt_dn = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(std::min(tmax, dn_cap), kSmemBudget / (4 * d->f))));
+    // the tile counts are powers of two up to 8 (the kernels specialise 1, 2, 4, 8)
+    auto pow2 = [](int v) { return v >= 8 ? 8 : (v >= 4 ? 4 : (v >= 2 ? 2 : 1)); };
+    p.tt_gu = pow2(p.tt_gu);
+    p.tt_dn = pow2(p.tt_dn);
+    p.ksplit = down_ksplit(d, p.P);
+    p.small_route = (T <= kSmallT && p.P <= kSmallPairs);
+    return p;
+}
+
+struct Layout {
+    size_t err, n_active, logits, idx, w, offsets, perm, pos, act_e, chunk_cnt, local_rank, gmask, h, y, total;
+};
+
+// Workspace regions for T tokens (each 256-byte aligned).  The y region is sized for the
+// largest split count any T <= T_max can use.
+Layout layout_for(const moe_layer_desc* d, int64_t T) {
+    const Plan p = make_plan(d, T);
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = round_up(off + bytes, 256);
+        return at;
+    };
+    L.err = take(4);
+    L.n_active = take(4);
+    L.logits = take(sizeof(float) * T * d->E);
+    L.idx = take(sizeof(int32_t) * p.P);
+    L.w = take(sizeof(float) * p.P);
+    L.offsets = take(sizeof(int32_t) * (d->E + 1));
+    L.perm = take(sizeof(int32_t) * p.P);
+    L.pos = take(sizeof(int32_t) * p.P);
+    L.act_e = take(sizeof(int32_t) * p.slot_cap);
+    L.chunk_cnt = take(sizeof(int32_t) * p.nchunk * d->E);
+    L.local_rank = take(sizeof(int32_t) * p.P);
+    L.gmask = take(sizeof(uint32_t) * p.slot_cap * p.gwords);
+    L.h = take(sizeof(float) * p.P * d->f);
+    // splits are used only while P <= 64 (at most 8 of them)
+    const int64_t y_rows = std::max<int64_t>(p.P, std::min<int64_t>(p.P, 64) * 8);
+    L.y = take(sizeof(float) * y_rows * d->d);
+    L.total = off;
+    return L;
+}
+
+Workspace bind(void* base, const Layout& L) {
+    char* b = static_cast<char*>(base);
+    Workspace w;
+    w.err = reinterpret_cast<int32_t*>(b + L.err);
+    w.n_active = reinterpret_cast<int32_t*>(b + L.n_active);
+    w.logits = reinterpret_cast<float*>(b + L.logits);
+    w.idx = reinterpret_cast<int32_t*>(b + L.idx);
+    w.w = reinterpret_cast<float*>(b + L.w);
+    w.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+    w.perm = reinterpret_cast<int32_t*>(b + L.perm);
+    w.pos = reinterpret_cast<int32_t*>(b + L.pos);
+    w.act_e = reinterpret_cast<int32_t*>(b + L.act_e);
+    w.chunk_cnt = reinterpret_cast<int32_t*>(b + L.chunk_cnt);
+    w.local_rank = reinterpret_cast<int32_t*>(b + L.local_rank);
+    w.gmask = reinterpret_cast<uint32_t*>(b + L.gmask);
+    w.h = reinterpret_cast<float*>(b + L.h);
+    w.y = reinterpret_cast<float*>(b + L.y);
+    return w;
+}
+
+moe_status validate_desc(const moe_layer_desc* d) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->act != MOE_ACT_SWIGLU && d->act != MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
+    if (d->wfmt != MOE_W_Q8_0 && d->wfmt != MOE_W_NVFP4) return MOE_ERR_INVALID_ARG;
+    if (d->path != MOE_PATH_AUTO && d->path != MOE_PATH_GEMV && d->path != MOE_PATH_GEMM) return MOE_ERR_INVALID_ARG;
+    if (d->E < 1 || d->E > kMaxE || d->E % 4 != 0) return MOE_ERR_SHAPE;
+    if (d->k < 1 || d->k > kMaxK || d->k > d->E) return MOE_ERR_INVALID_ARG;
+    if (d->d < 256 || d->d > kMaxDim || d->d % 256 != 0) return MOE_ERR_SHAPE;
+    const int64_t fq = (d->wfmt == MOE_W_Q8_0) ? 32 : 64;
+    if (d->f < fq || d->f > kMaxF || d->f % fq != 0) return MOE_ERR_SHAPE;
+    if (d->act == MOE_ACT_RELU2 && d->f % 32 != 0) return MOE_ERR_SHAPE;
+    if (!d->router_w || !d->w_gate_up || !d->w_down) return MOE_ERR_INVALID_ARG;
+    if (d->wfmt == MOE_W_NVFP4 && (!d->gate_up_tscale || !d->down_tscale)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(d->router_w) || !aligned16(d->w_gate_up) || !aligned16(d->w_down)) return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return 10000; }
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: a pointer is NULL or an argument is out of range";
+        case MOE_ERR_SHAPE: return "MOE_ERR_SHAPE: a dimension is not a supported multiple or is too large";
+        case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT: a pointer is not 16-byte aligned";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: this combination is not built";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA runtime call failed";
+        case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK: a kernel recorded an error";
+    }
+    return "unknown moe_status";
+}
+
+size_t moe_q8_0_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0 || cols % 32 != 0) return 0;
+    return static_cast<size_t>(rows) * static_cast<size_t>(cols / 32) * 34;
+}
+
+size_t moe_nvfp4_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0 || cols % 16 != 0) return 0;
+    return static_cast<size_t>(rows) * static_cast<size_t>(cols) / 2 + static_cast<size_t>(rows) * cols / 16;
+}
+
+moe_status moe_quantize_q8_0(const float* src, int64_t n_mat, int64_t rows, int64_t cols, moe_layout layout,
+                             void* dst, moe_stream_t stream) {
+    if (!src || !dst || n_mat < 0) return MOE_ERR_INVALID_ARG;
+    if (layout != MOE_LAYOUT_CANONICAL && layout != MOE_LAYOUT_DEVICE) return MOE_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 32 != 0 || rows > kMaxTokens || cols > kMaxDim)
+        return MOE_ERR_SHAPE;
+    if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_ALIGNMENT;
+    if (n_mat == 0) return MOE_OK;
+    return cuda_status(launch_q8_0_quantize(src, n_mat, rows, cols, layout, dst, stream));
+}
+
+moe_status moe_pack_nvfp4(const float* src, int64_t n_mat, int64_t rows, int64_t cols, moe_layout layout, void* dst,
+                          float* tensor_scale, moe_stream_t stream) {
+    if (!src || !dst || !tensor_scale || n_mat < 0) return MOE_ERR_INVALID_ARG;
+    if (layout != MOE_LAYOUT_CANONICAL && layout != MOE_LAYOUT_DEVICE && layout != MOE_LAYOUT_NEURON)
+        return MOE_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 64 != 0 || rows > kMaxTokens || cols > kMaxDim)
+        return MOE_ERR_SHAPE;
+    if (n_mat > 65535) return MOE_ERR_SHAPE;
+    if (!aligned16(src) || !aligned16(dst) || (reinterpret_cast<uintptr_t>(tensor_scale) & 3u)) return MOE_ERR_ALIGNMENT;
+    if (n_mat == 0) return MOE_OK;
+    return cuda_status(launch_nvfp4_pack(src, n_mat, rows, cols, layout, dst, tensor_scale, stream));
+}
+
+size_t moe_router_workspace_bytes(int64_t T, int64_t E) {
+    if (T < 0 || E < 1) return 0;
+    return round_up(sizeof(float) * static_cast<size_t>(T) * static_cast<size_t>(E), 256);
+}
+
+moe_status moe_router_topk(const void* x, moe_dtype xt, const float* W, int64_t T, int64_t d, int64_t E, int k,
+                           int32_t* idx, float* w, float* logits, void* workspace, size_t ws_bytes,
+                           moe_stream_t stream) {
+    if (!x || !W || !idx || !w) return MOE_ERR_INVALID_ARG;
+    if (xt != MOE_F32 && xt != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || T > kMaxTokens) return MOE_ERR_SHAPE;
+    if (E < 4 || E > kMaxE || E % 4 != 0) return MOE_ERR_SHAPE;
+    if (k < 1 || k > kMaxK || k > E) return MOE_ERR_INVALID_ARG;
+    if (d < 256 || d > kMaxDim || d % 256 != 0) return MOE_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(idx) || !aligned16(w) || (logits && !aligned16(logits)))
+        return MOE_ERR_ALIGNMENT;
+    float* lg = logits;
+    if (!lg) {
+        if (!workspace || ws_bytes < moe_router_workspace_bytes(T, E)) return MOE_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return MOE_ERR_ALIGNMENT;
+        lg = static_cast<float*>(workspace);
+    }
+    if (T == 0) return MOE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_router_logits(x, xt, W, T, d, E, lg, s);
+    if (e == cudaSuccess) e = launch_topk_softmax(lg, T, E, k, idx, w, s);
+    return cuda_status(e);
+}
+
+size_t moe_layer_workspace_bytes(const moe_layer_desc* desc, int64_t T_max) {
+    if (validate_desc(desc) != MOE_OK || T_max < 1 || T_max > kMaxTokens) return 0;
+    // The largest layout over T <= T_max: every region grows with T except the split y
+    // region, which is bounded by the P <= 64 case; take the max of both ends.
+    const size_t a = layout_for(desc, T_max).total;
+    const int64_t t_small = std::min<int64_t>(T_max, std::max<int64_t>(1, 64 / desc->k));
+    const size_t b = layout_for(desc, t_small).total;
+    return std::max(a, b);
+}
+
+moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtype xt, int64_t T,
+                             const int32_t* idx_in, const float* w_in, float* out, void* workspace,
+                             size_t ws_bytes, const moe_trace* trace, moe_stream_t stream) {
+    moe_status st = validate_desc(desc);
+    if (st != MOE_OK) return st;
+    if (!x || !out) return MOE_ERR_INVALID_ARG;
+    if (xt != MOE_F32 && xt != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if ((idx_in == nullptr) != (w_in == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || T > kMaxTokens) return MOE_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
+    if (idx_in && (!aligned16(idx_in) || !aligned16(w_in))) return MOE_ERR_ALIGNMENT;
+    if (T == 0) return MOE_OK;
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_ALIGNMENT;
+    const Layout L = layout_for(desc, T);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (desc->path == MOE_PATH_GEMM) return MOE_ERR_UNSUPPORTED;
+
+    cudaError_t e = ensure_configured();
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Plan p = make_plan(desc, T);
+    const Workspace ws = bind(workspace, L);
+    const int k = desc->k;
+
+    // 1. router + top-k + softmax, 2. permutation by expert
+    if (!idx_in) {
+        e = launch_router_logits(x, xt, desc->router_w, T, desc->d, desc->E, ws.logits, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (p.small_route) {
+        e = launch_route_small(idx_in ? nullptr : ws.logits, idx_in, w_in, T, desc->E, k, p.gwords, ws, s);
+    } else {
+        if (!idx_in) {
+            e = launch_topk_softmax(ws.logits, T, desc->E, k, ws.idx, ws.w, s);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+        }
+        e = launch_permute_large(idx_in, w_in, T, desc->E, k, p.gwords, ws, s);
+    }
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 3. gate.up + activation + group mask, 4. sparse down, 5. combine
+    ExpertArgs a{};
+    a.x = x;
+    a.xt = xt;
+    a.d = static_cast<int>(desc->d);
+    a.f = static_cast<int>(desc->f);
+    a.k = k;
+    a.rows_gu = static_cast<int>(desc->act == MOE_ACT_SWIGLU ? 2 * desc->f : desc->f);
+    a.tt_gu = p.tt_gu;
+    a.tt_dn = p.tt_dn;
+    a.ksplit = p.ksplit;
+    a.gwords = p.gwords;
+    a.P = static_cast<int>(p.P);
+    a.w_gu = static_cast<const uint8_t*>(desc->w_gate_up);
+    a.w_dn = static_cast<const uint8_t*>(desc->w_down);
+    if (desc->wfmt == MOE_W_Q8_0) {
+        a.gu_bytes = static_cast<int64_t>(moe_q8_0_bytes(a.rows_gu, desc->d));
+        a.dn_bytes = static_cast<int64_t>(moe_q8_0_bytes(desc->d, desc->f));
+    } else {
+        a.gu_bytes = static_cast<int64_t>(moe_nvfp4_bytes(a.rows_gu, desc->d));
+        a.dn_bytes = static_cast<int64_t>(moe_nvfp4_bytes(desc->d, desc->f));
+    }
+    a.gu_ts = desc->gate_up_tscale;
+    a.dn_ts = desc->down_tscale;
+    a.ws = ws;
+    if ((e = launch_gate_up_gemv(a, desc->wfmt, desc->act, p.slot_cap, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((e = launch_down_gemv(a, desc->wfmt, p.slot_cap, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((e = launch_combine(ws.w, ws.pos, ws.y, T, k, desc->d, p.ksplit, p.P * desc->d, out, s)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    if (trace) {
+        auto cp = [&](void* dst, const void* src, size_t bytes) {
+            if (dst && e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+        };
+        if (!idx_in) cp(trace->logits, ws.logits, sizeof(float) * T * desc->E);
+        cp(trace->idx, ws.idx, sizeof(int32_t) * p.P);
+        cp(trace->w, ws.w, sizeof(float) * p.P);
+        cp(trace->offsets, ws.offsets, sizeof(int32_t) * (desc->E + 1));
+        cp(trace->perm, ws.perm, sizeof(int32_t) * p.P);
+        cp(trace->pos, ws.pos, sizeof(int32_t) * p.P);
+        cp(trace->h, ws.h, sizeof(float) * p.P * desc->f);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uint16_t* xo, moe_stream_t stream) {
+    if (!x || !xo || T < 0 || d < 1 || d > kMaxDim) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    return cuda_status(launch_rmsnorm_bf16(x, T, d, eps, xo, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_get_device_status(void* workspace, moe_stream_t stream, int32_t* device_code) {
+    if (!workspace) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t code = 0;
+    cudaError_t e = cudaMemcpyAsync(&code, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && code != 0) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (device_code) *device_code = code;
+    return code == 0 ? MOE_OK : MOE_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

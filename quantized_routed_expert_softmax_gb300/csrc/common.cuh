@@ -1,0 +1,97 @@
+// common.cuh -- device helpers shared by libmoe's kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Device error codes recorded in the workspace error word.
+constexpr int kDevErrBadExpert = 1;
+
+constexpr int kRouterPartials = 256;   // partial sums of the router's canonical order
+constexpr int kMaxK = 32;              // top-k fits one warp
+constexpr int kMaxE = 1024;
+
+// Pointers into one layer workspace (see layout_workspace in api.cu).
+struct Workspace {
+    int32_t* err;          // [1] sticky first error
+    int32_t* n_active;     // [1] number of experts with at least one pair
+    float* logits;         // [T][E]
+    int32_t* idx;          // [T][k]
+    float* w;              // [T][k]
+    int32_t* offsets;      // [E+1]
+    int32_t* perm;         // [P] sorted row -> pair
+    int32_t* pos;          // [P] pair -> sorted row
+    int32_t* act_e;        // [min(E,P)] expert id of each active slot, increasing
+    int32_t* chunk_cnt;    // [nchunk][E] pairs of each expert per chunk (large-T permute)
+    int32_t* local_rank;   // [P] rank of a pair among its expert's pairs in its chunk
+    uint32_t* gmask;       // [min(E,P)][ceil(f/16/32)] active 16-neuron groups per slot
+    float* h;              // [P][f] activations, sorted rows
+    float* y;              // [ksplit][P][d] down partials, sorted rows
+};
+
+// Arguments of the expert kernels (gate.up, down) of one layer call.
+struct ExpertArgs {
+    const void* x;
+    int xt;
+    int d, f, k, rows_gu;
+    int tt_gu, tt_dn;            // tokens per shared-memory tile
+    int ksplit;                  // K splits of the down projection (partials summed in combine)
+    int gwords;                  // 32-bit words of group mask per slot
+    int P;                       // pairs T*k
+    const uint8_t* w_gu;
+    int64_t gu_bytes;            // bytes of one expert's gate/up matrix
+    const uint8_t* w_dn;
+    int64_t dn_bytes;
+    const float* gu_ts;          // NVFP4 tensor scales [E] (or null)
+    const float* dn_ts;
+    Workspace ws;
+};
+
+__device__ __forceinline__ void set_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// x row element as fp32 (exact for bf16).
+__device__ __forceinline__ float load_x(const void* x, int xt, int64_t off) {
+    if (xt == MOE_F32) return static_cast<const float*>(x)[off];
+    return bf16_bits_to_f32(static_cast<const uint16_t*>(x)[off]);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Signed int8 byte b of a 32-bit word as float, exact.
+__device__ __forceinline__ float s8_to_f32(uint32_t word, int b) {
+    return static_cast<float>(static_cast<int8_t>((word >> (8 * b)) & 0xffu));
+}
+
+// Two E2M1 codes (one byte, low nibble first) -> two floats, exact.
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
+    __half2 hh = *reinterpret_cast<__half2*>(&h2);
+    return __half22float2(hh);   // .x = low half = the low nibble's code
+}
+
+// One E4M3 byte -> float, exact.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+    uint32_t h2;
+    uint16_t in = static_cast<uint16_t>(byte & 0xffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    return __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xffffu)));
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+}  // namespace moe

@@ -1,0 +1,274 @@
+"""GPU parity: libmoe's CUDA path against the CPU oracle, through the C ABI.
+
+Bit-exact: quantised bytes (every layout), tensor scales, router logits, top-k indices,
+expert offsets and the permutation.  Floating point: combine weights to 1e-6 relative,
+layer outputs to max|err| <= 2e-3 * rms(out).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle_bridge import TOL, assert_close, oracle_layer, to_numpy_x
+from quantized_routed_expert_softmax_gb300 import layers, native, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_routed_expert_softmax_gb300 import build
+    build.build()
+    native.lib()
+
+
+def _f32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def _edge_matrix(rows, cols, seed):
+    g = np.random.default_rng(seed)
+    m = (g.standard_normal((rows, cols)) * 0.02).astype(np.float32)
+    m[0, :32] = 0.0                                    # an all-zero block
+    m[1, :32] = 0.3                                    # a constant block
+    m[2, :8] = [127.0, 2.5, -2.5, 0.5, -0.5, 1.5, 126.5, -0.49]    # half-way codes
+    m[3, :3] = [1.0, 0.49997, -0.49997]                # fp32-vs-fp16 scale sensitivity
+    m[4, :64] = g.standard_normal(64).astype(np.float32) * 1e3      # large values
+    m[5, :64] = g.standard_normal(64).astype(np.float32) * 1e-30    # tiny (subnormal scales)
+    return m
+
+
+# ------------------------------------------------------------------ packers
+@pytest.mark.parametrize("rows,cols", [(64, 256), (96, 2816)])
+def test_q8_0_packer_bitexact(rows, cols):
+    mats = np.stack([_edge_matrix(rows, cols, s) for s in range(3)])
+    canon = np.stack([oracle.q8_0_quantize(m) for m in mats])
+    got_c = native.quantize_q8_0(_f32(mats), "canonical").cpu().numpy()
+    got_d = native.quantize_q8_0(_f32(mats), "device").cpu().numpy()
+    assert np.array_equal(got_c, canon)
+    for i in range(3):
+        assert np.array_equal(got_d[i], oracle.q8_0_to_device(canon[i], rows, cols))
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 256), (64, 2688), (2688, 1024)])
+def test_nvfp4_packer_bitexact(rows, cols):
+    g = np.random.default_rng(rows + cols)
+    mats = [(g.standard_normal((rows, cols)) * 0.02).astype(np.float32) for _ in range(3)]
+    mats[1] = _edge_matrix(rows, cols, 7)
+    mats[2][:] = 0.0                                  # an all-zero matrix: s_t = 1
+    src = _f32(np.stack(mats))
+    ref = [oracle.nvfp4_quantize(m) for m in mats]
+    for layout in ("canonical", "device", "neuron"):
+        got, ts = native.pack_nvfp4(src, layout)
+        got, ts = got.cpu().numpy(), ts.cpu().numpy()
+        for i, (q, st) in enumerate(ref):
+            assert ts[i] == np.float32(st)
+            want = {"canonical": q, "device": oracle.nvfp4_to_panels(q, rows, cols),
+                    "neuron": oracle.nvfp4_to_neuron(q, rows, cols)}[layout]
+            assert np.array_equal(got[i], want), (layout, i, int((got[i] != want).sum()))
+
+
+# ------------------------------------------------------------------ router
+@pytest.mark.parametrize("name", ["tiny", "gemma", "nemotron"])
+@pytest.mark.parametrize("T", [1, 3, 16, 37])
+def test_router_topk_bitexact(name, T):
+    w = synth.WORKLOADS[name]
+    x = synth.tokens(w, T, tag="router")
+    W = synth.router_weight(w)
+    xt = torch.from_numpy(x).cuda()
+    if x.dtype == np.uint16:
+        xt = xt.view(torch.bfloat16)
+    idx, wt, lg = native.router_topk(xt, _f32(W), w.k, return_logits=True)
+    ref_lg = oracle.router_logits(x, W)
+    assert np.array_equal(lg.cpu().numpy().view(np.uint32), ref_lg.view(np.uint32))
+    ref_idx, ref_w = oracle.topk_softmax(ref_lg, w.k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.allclose(wt.cpu().numpy(), ref_w, rtol=1e-6, atol=0)
+
+
+def test_router_ties_take_lowest_index():
+    w = synth.WORKLOADS["gemma"]
+    x = torch.zeros((4, w.d), dtype=torch.bfloat16, device="cuda")
+    idx, wt = native.router_topk(x, _f32(synth.router_weight(w)), w.k)
+    assert (idx.cpu().numpy() == np.arange(w.k)).all()
+    assert (wt.cpu().numpy() == np.float32(1.0 / w.k)).all()
+
+
+# ------------------------------------------------------------------ the layer, small shapes
+SMALL = {
+    "tiny_q8_swiglu": synth.WORKLOADS["tiny"],
+    "small_nvfp4_relu2": synth.Workload("small_nvfp4_relu2", d=256, f=512, E=16, k=4, act="relu2", wfmt="nvfp4",
+                                        x_dtype="bf16", layers=1, zero_fraction=0.925),
+    "small_q8_relu2": synth.Workload("small_q8_relu2", d=512, f=256, E=12, k=3, act="relu2", wfmt="q8_0",
+                                     x_dtype="bf16", layers=1, zero_fraction=0.8),
+    "small_nvfp4_swiglu": synth.Workload("small_nvfp4_swiglu", d=512, f=320, E=8, k=2, act="swiglu", wfmt="nvfp4",
+                                         x_dtype="f32", layers=1),
+}
+
+
+def _run_small(w, T, idx_in=None, w_in=None):
+    L = layers.build_layer(w, source="numpy")
+    x = synth.tokens(w, T, tag="parity")
+    xt = torch.from_numpy(x).cuda()
+    if x.dtype == np.uint16:
+        xt = xt.view(torch.bfloat16)
+    tr = {}
+    ii = None if idx_in is None else torch.from_numpy(idx_in).cuda()
+    ww = None if w_in is None else torch.from_numpy(w_in).cuda()
+    out = L.forward(xt, idx_in=ii, w_in=ww, trace=tr).cpu().numpy()
+    ol = oracle_layer(w, synth.router_weight(w), lambda e: synth.expert_weights(w, 0, e)[0],
+                      lambda e: synth.expert_weights(w, 0, e)[1], range(w.E))
+    ref = ol.forward(x, idx_in=idx_in, w_in=w_in)
+    return L, out, tr, ref
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("T", [1, 3, 16, 33, 100])
+def test_layer_small_parity(name, T):
+    w = SMALL[name]
+    L, out, tr, ref = _run_small(w, T)
+    assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
+    assert np.allclose(tr["w"].cpu().numpy(), ref["w"], rtol=1e-6, atol=0)
+    assert np.array_equal(tr["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(tr["pos"].cpu().numpy(), ref["pos"])
+    assert np.array_equal(tr["logits"].cpu().numpy().view(np.uint32), ref["logits"].view(np.uint32))
+    # activations in sorted-row order
+    h_ref = ref["h"][ref["perm"]]
+    assert_close(tr["h"].cpu().numpy(), h_ref, what="h")
+    assert_close(out, ref["out"])
+
+
+@pytest.mark.parametrize("T", [5, 64])
+def test_layer_supplied_routing(T):
+    w = SMALL["tiny_q8_swiglu"]
+    idx, wts = synth.zipf_routing(T, w.E, w.k, seed_tag="parity")
+    L, out, tr, ref = _run_small(w, T, idx_in=idx, w_in=wts)
+    assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
+    assert_close(out, ref["out"])
+
+
+def test_bad_expert_index_is_clamped_and_reported():
+    w = SMALL["tiny_q8_swiglu"]
+    L = layers.build_layer(w, source="numpy")
+    x = torch.from_numpy(synth.tokens(w, 4, tag="bad")).cuda()
+    idx = torch.tensor([[0, 1], [2, 999], [3, -5], [4, 5]], dtype=torch.int32, device="cuda")
+    wts = torch.full((4, 2), 0.5, dtype=torch.float32, device="cuda")
+    out = L.forward(x, idx_in=idx, w_in=wts)
+    assert torch.isfinite(out).all()
+    assert L.device_status() == 1
+    assert L.device_status() == 0          # reading clears the word
+
+
+def test_output_is_fully_written_and_deterministic():
+    w = SMALL["small_nvfp4_relu2"]
+    L = layers.build_layer(w, source="numpy")
+    x = torch.from_numpy(synth.tokens(w, 33, tag="det")).cuda().view(torch.bfloat16)
+    outs = []
+    for _ in range(3):
+        o = torch.full((33, w.d), float("nan"), device="cuda")
+        L.forward(x, out=o)
+        outs.append(o.cpu().numpy())
+    assert np.isfinite(outs[0]).all()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert np.array_equal(outs[0].view(np.uint32), outs[2].view(np.uint32))
+
+
+def test_zero_input_gives_zero_output():
+    for name in ("tiny_q8_swiglu", "small_nvfp4_swiglu"):
+        w = SMALL[name]
+        L = layers.build_layer(w, source="numpy")
+        x = torch.zeros((3, w.d), dtype=torch.float32, device="cuda")
+        assert (L.forward(x) == 0).all()
+
+
+def test_empty_batch_is_a_no_op():
+    w = SMALL["tiny_q8_swiglu"]
+    L = layers.build_layer(w, source="numpy")
+    out = torch.full((1, w.d), 7.0, device="cuda")
+    L.forward(torch.zeros((0, w.d), device="cuda"), out=out[:0])
+    assert (out == 7.0).all()
+
+
+def test_rmsnorm_bf16():
+    g = np.random.default_rng(3)
+    x = (g.standard_normal((5, 2816)) * 3).astype(np.float32)
+    got = native.rmsnorm_bf16(_f32(x)).float().cpu().numpy()
+    ref = x / np.sqrt((x.astype(np.float64) ** 2).mean(axis=1, keepdims=True) + 1e-6)
+    assert np.abs(got - ref).max() <= 2 ** -8 * np.abs(ref).max()
+
+
+# ------------------------------------------------------------------ the layer, full shapes
+def _full_case(name, T, sample=None, idx_in=None, w_in=None):
+    w = synth.WORKLOADS[name]
+    L = layers.build_layer(w, keep_fp32=True)
+    x = synth.tokens_cuda(w, T, tag="parity")
+    tr = {}
+    ii = None if idx_in is None else torch.from_numpy(idx_in).cuda()
+    ww = None if w_in is None else torch.from_numpy(w_in).cuda()
+    out = L.forward(x, idx_in=ii, w_in=ww, trace=tr).cpu().numpy()
+    rows = np.arange(T) if sample is None else np.asarray(sample)
+    xs = to_numpy_x(x)[rows]
+    W = L.router_w.cpu().numpy()
+    if idx_in is None:
+        lg = oracle.router_logits(xs, W)
+        need, _ = oracle.topk_softmax(lg, w.k)
+    else:
+        need = idx_in[rows]
+    ol = oracle_layer(w, W, lambda e: L.gate_up_f32[e].cpu().numpy(), lambda e: L.down_f32[e].cpu().numpy(),
+                      need.ravel())
+    ref = ol.forward(xs, idx_in=None if idx_in is None else idx_in[rows],
+                     w_in=None if w_in is None else w_in[rows])
+    # the packed bytes of the experts used, bit for bit
+    for e in sorted(set(int(v) for v in need.ravel()))[:3]:
+        if w.wfmt == "q8_0":
+            assert np.array_equal(L.gate_up[e].cpu().numpy(), oracle.q8_0_to_device(ol.gate_up[e], w.rows_gu, w.d))
+            assert np.array_equal(L.down[e].cpu().numpy(), oracle.q8_0_to_device(ol.down[e], w.d, w.f))
+        else:
+            assert np.array_equal(L.gate_up[e].cpu().numpy(), oracle.nvfp4_to_panels(ol.gate_up[e], w.rows_gu, w.d))
+            assert np.array_equal(L.down[e].cpu().numpy(), oracle.nvfp4_to_neuron(ol.down[e], w.d, w.f))
+    if idx_in is None:
+        assert np.array_equal(tr["logits"].cpu().numpy()[rows].view(np.uint32), ref["logits"].view(np.uint32))
+    assert np.array_equal(tr["idx"].cpu().numpy()[rows], ref["idx"])
+    assert np.allclose(tr["w"].cpu().numpy()[rows], ref["w"], rtol=1e-6, atol=0)
+    ratio = assert_close(out[rows], ref["out"])
+    # invariants of the full-size permutation
+    off = tr["offsets"].cpu().numpy()
+    perm = tr["perm"].cpu().numpy()
+    pos = tr["pos"].cpu().numpy()
+    assert off[0] == 0 and off[-1] == T * w.k
+    assert np.array_equal(perm[pos], np.arange(T * w.k))
+    idx_all = tr["idx"].cpu().numpy().ravel()
+    assert np.array_equal(np.diff(off), np.bincount(idx_all, minlength=w.E))
+    assert np.array_equal(perm, np.argsort(idx_all, kind="stable"))
+    del L
+    torch.cuda.empty_cache()
+    return ratio
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_gemma_layer_full_size(T):
+    _full_case("gemma", T)
+
+
+def test_gemma_layer_prefill_512_sampled():
+    _full_case("gemma", 512, sample=[0, 1, 255, 511])
+
+
+@pytest.mark.parametrize("T,sample", [(1, None), (32, [0, 31])])
+def test_nemotron_layer_full_size(T, sample):
+    _full_case("nemotron", T, sample=sample)
+
+
+@pytest.mark.parametrize("T,sample", [(1, None), (8, [0, 7])])
+def test_minimax_layer_full_size(T, sample):
+    _full_case("minimax", T, sample=sample)
+
+
+@pytest.mark.parametrize("T", [64])
+def test_zipf_routing_full_size(T):
+    w = synth.WORKLOADS["zipf"]
+    idx, wts = synth.zipf_routing(T, w.E, w.k)
+    _full_case("zipf", T, sample=[0, 17, 63], idx_in=idx, w_in=wts)
