@@ -1,0 +1,502 @@
+"""Benchmark: routed MoE layer stack on GB300 (libmoe) or the CPU oracle.
+
+Default workload: the Gemma-4-26B-A4B-shaped stack (30 MoE layers, d=2816, E=128, top-8,
+f=704, SwiGLU, Q8_0 experts, bf16 activations), decode, one token per step.  A step is one
+pass of the whole hot path over every layer of the stack: router, top-k, permutation,
+gate.up + SwiGLU, sparse down, combine, and the RMS-norm glue that feeds the next layer.
+The 30 layers are captured once into CUDA graphs; weights, inputs and workspaces are
+resident in HBM before timing starts.
+
+One JSON line on rank 0:  metric / value / unit (tokens per second through the stack), the
+roofline of the dominant kernel (gate.up, live CUDA-event timing inside the graphs against
+the measured HBM copy bandwidth), the oracle timed on the host cores (cpu_baseline), an
+end-to-end figure with host<->device copies inside the timed region, clocks sampled during
+the timed region and the number of libmoe kernels launched.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload gemma|nemotron|minimax] [--tokens T]
+Under torchrun (N > 1) every rank runs its own replica (the layer needs no exchange on
+one GPU); value = tokens of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; decode active-expert GB/s vs GB300 HBM roofline"
+N_ROTATE = 8          # distinct token inputs, replayed round robin (no step reuses the last one's experts)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gemma")
+    ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = the workload's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def hbm_peak():
+    p = peaks()
+    if p and p.get("hbm_gbs"):
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+    return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def workload_config(w, T, layers):
+    return {
+        "workload": f"{w.name}-shaped MoE stack: {layers} layers, d={w.d}, E={w.E}, top-{w.k}, f={w.f}, "
+                    f"{'SwiGLU' if w.act == 'swiglu' else 'ReLU^2'}, {w.wfmt.upper()} experts, "
+                    f"{w.x_dtype} activations, {'decode' if T <= 32 else 'prefill'} T={T}",
+        "layers": layers, "tokens_per_step": T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "act": w.act,
+        "weights": w.wfmt, "activations": w.x_dtype,
+    }
+
+
+# ====================================================================== oracle timing
+def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0):
+    """Time the CPU oracle on a bounded sample of the workload.
+
+    A unit is the oracle's forward of one layer of the stack (router, top-k, softmax,
+    permutation, every routed expert: dequantise + gate.up + activation + down, combine;
+    fp64) on up to 8 of the step's tokens.  Units cycle through the stack's layers; the
+    experts a layer routes to are drawn and quantised once (untimed) and cached.
+    Returns (seconds per stack step, units timed, threads, description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from quantized_routed_expert_softmax_gb300 import synth
+
+    have_cuda = torch.cuda.is_available()
+    act = oracle.ACT_SWIGLU if w.act == "swiglu" else oracle.ACT_RELU2
+    fmt = oracle.W_Q8_0 if w.wfmt == "q8_0" else oracle.W_NVFP4
+    tu = min(T, 8)
+    cache = {}
+
+    def layer_obj(layer):
+        if layer in cache:
+            return cache[layer]
+        x = synth.tokens(w, tu, layer, tag="cpu")
+        W = synth.router_weight(w, layer)
+        idx, _ = oracle.topk_softmax(oracle.router_logits(x, W), w.k)
+        gu, dn = [None] * w.E, [None] * w.E
+        gts, dts = np.ones(w.E, np.float32), np.ones(w.E, np.float32)
+        for e in sorted(set(int(v) for v in idx.ravel())):
+            if have_cuda:
+                a = synth.expert_stack_cuda(w, layer, "gate_up", [e])[0].cpu().numpy()
+                b = synth.expert_stack_cuda(w, layer, "down", [e])[0].cpu().numpy()
+            else:
+                a, b = synth.expert_weights(w, layer, e)
+            if w.wfmt == "q8_0":
+                gu[e], dn[e] = oracle.q8_0_quantize(a), oracle.q8_0_quantize(b)
+            else:
+                gu[e], gts[e] = oracle.nvfp4_quantize(a)
+                dn[e], dts[e] = oracle.nvfp4_quantize(b)
+        L = oracle.Layer(w.d, w.f, w.E, w.k, act, fmt, W, gu, dn,
+                         gts if w.wfmt == "nvfp4" else None, dts if w.wfmt == "nvfp4" else None)
+        cache[layer] = (L, x)
+        return cache[layer]
+
+    times = []
+    units = 0
+    spent = 0.0
+    while units < max_units + warmup_units and (spent < time_budget_s or units < warmup_units + 1):
+        L, x = layer_obj(units % layers)
+        t0 = time.perf_counter()
+        L.forward(x)
+        dt = time.perf_counter() - t0
+        if units >= warmup_units:
+            times.append(dt)
+            spent += dt
+        units += 1
+    per_token_layer = statistics.mean(times) / tu
+    step_s = per_token_layer * T * layers
+    desc = (f"{len(times)} oracle forwards of single layers of the stack on {tu} token(s) each (router, top-k, "
+            f"softmax, permutation, every routed expert dequantised and evaluated in fp64, combine), cycling over "
+            f"the {layers} layers; per-step time = mean per token-layer x {T} token(s) x {layers} layers")
+    return step_s, len(times), oracle.num_threads(), desc
+
+
+# ====================================================================== GPU arm
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = str(gpu_index)
+        try:
+            import torch
+            self.gpu = "GPU-" + str(torch.cuda.get_device_properties(gpu_index).uuid)
+        except Exception:
+            pass
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.fh = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def build_stack(w, T, layers, local_rank):
+    import torch
+
+    from quantized_routed_expert_softmax_gb300 import layers as L
+    from quantized_routed_expert_softmax_gb300 import synth
+    stack = [L.build_layer(w, layer=l) for l in range(layers)]
+    inputs = [synth.tokens_cuda(w, T, layer=0, tag=f"bench{r}") for r in range(N_ROTATE)]
+    torch.cuda.synchronize()
+    return stack, inputs
+
+
+def capture_graphs(stack, inputs, T, w, stage_events=None):
+    """One CUDA graph per rotated input; each runs the whole stack."""
+    import torch
+
+    from quantized_routed_expert_softmax_gb300 import native
+    dev = torch.device("cuda")
+    outs = [torch.empty((T, w.d), dtype=torch.float32, device=dev) for _ in stack]
+    nxt = [torch.empty((T, w.d), dtype=torch.bfloat16, device=dev) for _ in stack]
+    wss = [layer.workspace(T) for layer in stack]
+    graphs = []
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        # warm the kernels once outside capture (per-device attribute setup happens here)
+        x = inputs[0]
+        for li, layer in enumerate(stack):
+            layer.forward(x, out=outs[li], workspace=wss[li])
+            native.rmsnorm_bf16(outs[li], out=nxt[li])
+            x = nxt[li]
+        torch.cuda.current_stream().synchronize()
+        for g_i, x0 in enumerate(inputs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                x = x0
+                for li, layer in enumerate(stack):
+                    ev = None if stage_events is None else stage_events[g_i][li]
+                    layer.forward(x, out=outs[li], workspace=wss[li], stage_events=ev)
+                    native.rmsnorm_bf16(outs[li], out=nxt[li])
+                    x = nxt[li]
+            graphs.append(g)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return graphs, outs
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_routed_expert_softmax_gb300 import native, synth
+    from quantized_routed_expert_softmax_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(local_rank)
+    w = synth.WORKLOADS[args.workload]
+    T = args.tokens
+    layers = args.layers or w.layers
+    stack, inputs = build_stack(w, T, layers, local_rank)
+    graphs, outs = capture_graphs(stack, inputs, T, w)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- headline: K graph replays, round robin over the rotated inputs
+    for i in range(args.warmup):
+        graphs[i % N_ROTATE].replay()
+    barrier()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.15)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        graphs[i % N_ROTATE].replay()
+    e1.record()
+    barrier()
+    clk = clocks.stop()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    tokens_per_s = world * T * args.steps / (ms_total / 1e3)
+
+    # ---- active-expert bytes of one step (from the routing the stack actually took)
+    tr_bytes = active_expert_bytes(stack, inputs, T, w)
+
+    # ---- dominant kernel (gate.up): live CUDA events recorded inside the graphs
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in stack] for _ in inputs]
+    for g in evs:
+        for lay in g:
+            for ev in lay:
+                ev.record()
+    torch.cuda.synchronize()
+    n_ev_steps = max(N_ROTATE, min(args.steps, 400))
+    gu_ms, dn_ms, rt_ms, cb_ms = [], [], [], []
+    timing_how = "CUDA events recorded as graph nodes at the stage boundaries of every layer"
+    try:
+        graphs_ev, _ = capture_graphs(stack, inputs, T, w, stage_events=evs)
+        for i in range(args.warmup):
+            graphs_ev[i % N_ROTATE].replay()
+        torch.cuda.synchronize()
+        for i in range(n_ev_steps):
+            graphs_ev[i % N_ROTATE].replay()
+        torch.cuda.synchronize()
+        for g in evs:
+            for lay in g:
+                rt_ms.append(lay[0].elapsed_time(lay[1]))
+                gu_ms.append(lay[1].elapsed_time(lay[2]))
+                dn_ms.append(lay[2].elapsed_time(lay[3]))
+                cb_ms.append(lay[3].elapsed_time(lay[4]))
+    except Exception as exc:   # graph event nodes refused: time the same launches eagerly
+        timing_how = f"CUDA events around eager launches of the stack (graph events unavailable: {exc})"
+        gu_ms, dn_ms, rt_ms, cb_ms = [], [], [], []
+        outs_e = [torch.empty((T, w.d), dtype=torch.float32, device="cuda") for _ in stack]
+        for r in range(N_ROTATE):
+            x = inputs[r]
+            for li, layer in enumerate(stack):
+                lay = evs[r][li]
+                layer.forward(x, out=outs_e[li], workspace=layer.workspace(T), stage_events=lay)
+                x = native.rmsnorm_bf16(outs_e[li])
+            torch.cuda.synchronize()
+            for lay in evs[r]:
+                rt_ms.append(lay[0].elapsed_time(lay[1]))
+                gu_ms.append(lay[1].elapsed_time(lay[2]))
+                dn_ms.append(lay[2].elapsed_time(lay[3]))
+                cb_ms.append(lay[3].elapsed_time(lay[4]))
+    gu_us = statistics.mean(gu_ms) * 1e3
+    gu_bytes = tr_bytes["gate_up_per_layer"]
+    peak, peak_src = hbm_peak()
+    achieved = gu_bytes / (gu_us * 1e-6) / 1e9
+    traffic = measured_traffic(args.workload, T)
+
+    # ---- end to end: host x in pinned memory -> device, the stack, out -> host
+    x_host = [inp.cpu().pin_memory() for inp in inputs]
+    out_host = torch.empty((T, w.d), dtype=torch.float32).pin_memory()
+    e2e_steps = max(N_ROTATE, min(args.steps, 500))
+    for i in range(min(args.warmup, 10)):
+        inputs[i % N_ROTATE].copy_(x_host[i % N_ROTATE], non_blocking=True)
+        graphs[i % N_ROTATE].replay()
+        out_host.copy_(outs[-1], non_blocking=True)
+    barrier()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for i in range(e2e_steps):
+        inputs[i % N_ROTATE].copy_(x_host[i % N_ROTATE], non_blocking=True)
+        graphs[i % N_ROTATE].replay()
+        out_host.copy_(outs[-1], non_blocking=True)
+    a1.record()
+    barrier()
+    e2e_ms = a0.elapsed_time(a1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * T * e2e_steps / (e2e_ms / 1e3)
+
+    launches_per_step = sum(layer.launches(T) + 1 for layer in stack)   # + the RMS-norm glue
+    result = None
+    if rank == 0:
+        step_bytes = tr_bytes["step"]
+        cfg = workload_config(w, T, layers)
+        cfg.update({
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": f"per-step weight working set {step_bytes / 1e9:.2f} GB > 129 MB L2; {N_ROTATE} token inputs "
+                  f"rotate so consecutive steps route to different experts",
+            "graph": "one CUDA graph per rotated input covers the whole stack",
+            "layer_us": round(ms_step * 1e3 / layers, 3),
+            "layer_tokens_per_s": round(tokens_per_s * layers, 1),
+            "active_expert_bytes_per_step": step_bytes,
+            "active_expert_gbs": round(step_bytes * world / (ms_step * 1e-3) / 1e9, 1),
+            "active_expert_frac_of_measured_hbm": round(step_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
+            "active_expert_frac_of_8tbs": round(step_bytes / (ms_step * 1e-3) / 1e9 / 8000.0, 4),
+            "stage_us_mean": {"routing": round(statistics.mean(rt_ms) * 1e3, 2), "gate_up": round(gu_us, 2),
+                              "down": round(statistics.mean(dn_ms) * 1e3, 2),
+                              "combine": round(statistics.mean(cb_ms) * 1e3, 2)},
+        })
+        result = {
+            "metric": METRIC, "value": round(tokens_per_s, 2), "unit": f"tokens/s through the {layers}-layer stack",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; random-init weights of the workload's shapes)",
+            "config": cfg,
+            "roofline": {"bound": "hbm", "kernel": "gate_up_gemv (gate.up + SwiGLU + group mask)",
+                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes_per_launch": gu_bytes, "launch_us_mean": round(gu_us, 3),
+                         "launches_timed": len(gu_ms), "timing": timing_how, "peak_source": peak_src},
+            "e2e": {"value": round(e2e_value, 2), "unit": f"tokens/s through the {layers}-layer stack",
+                    "h2d_bytes_per_step": int(x_host[0].numel() * x_host[0].element_size()),
+                    "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()),
+                    "how": "pinned host x -> device copy, graph replay of the stack, out -> pinned host, "
+                           "all on the stream inside the timed region"},
+            "clocks": clk,
+            "gpu_launches": launches_per_step * args.steps,
+        }
+    return result, (w, T, layers)
+
+
+def active_expert_bytes(stack, inputs, T, w):
+    """Unique active-expert bytes of one step, from the routing each layer took
+    (gate.up bytes of every selected expert + down bytes of its active groups)."""
+    import torch
+
+    from quantized_routed_expert_softmax_gb300 import native
+    gu_b = stack[0].gate_up.shape[1]
+    dn_b = stack[0].down.shape[1]
+    x = inputs[0]
+    step = 0
+    gu_layer = []
+    for layer in stack:
+        tr = {}
+        out = layer.forward(x, trace=tr)
+        experts = torch.unique(tr["idx"]).numel()
+        gu_layer.append(experts * gu_b)
+        if w.act == "relu2":
+            h = tr["h"]
+            off = tr["offsets"].cpu().numpy()
+            act_groups = 0
+            for e in range(w.E):
+                if off[e + 1] > off[e]:
+                    hh = h[off[e]:off[e + 1]].reshape(off[e + 1] - off[e], -1, 16)
+                    act_groups += int((hh != 0).any(dim=2).any(dim=0).sum().item())
+            step += experts * gu_b + act_groups * (dn_b // (w.f // 16))
+        else:
+            step += experts * (gu_b + dn_b)
+        x = native.rmsnorm_bf16(out)
+    torch.cuda.synchronize()
+    return {"step": int(step), "gate_up_per_layer": int(statistics.mean(gu_layer))}
+
+
+def measured_traffic(workload, T):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if one
+    exists for this kernel build and workload; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        data = json.load(open(p))
+        return data.get(f"{workload}_T{T}")
+    except (OSError, ValueError):
+        return None
+
+
+# ====================================================================== reference arm
+def run_reference(args, rank, world):
+    from quantized_routed_expert_softmax_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    T = args.tokens
+    layers = args.layers or w.layers
+    budget = 120.0
+    t0 = time.perf_counter()
+    step_s, n, threads, desc = oracle_sample(w, T, layers, max_units=max(1, args.steps),
+                                             time_budget_s=budget, warmup_units=min(args.warmup, 1))
+    wall = time.perf_counter() - t0
+    value = T / step_s
+    cfg = workload_config(w, T, layers)
+    cfg["parallelism"] = "host cores"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6),
+        "unit": f"tokens/s through the {layers}-layer stack", "n_gpus": world, "steps": n, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded; random-init weights of the workload's shapes)", "config": cfg,
+        "cpu_baseline": {"value": round(value, 6), "unit": f"tokens/s through the {layers}-layer stack",
+                         "cores": threads, "kind": "oracle", "sample": desc, "wall_s": round(wall, 1)},
+        "e2e": {"value": round(value, 6), "unit": f"tokens/s through the {layers}-layer stack",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            import torch
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    result, (w, T, layers) = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            step_s, n, threads, desc = oracle_sample(w, T, layers, max_units=10 * layers, time_budget_s=15.0,
+                                                     warmup_units=1)
+            result["cpu_baseline"] = {"value": round(T / step_s, 6), "unit": result["unit"], "cores": threads,
+                                      "kind": "oracle", "sample": desc}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

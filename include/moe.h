@@ -160,7 +160,11 @@ typedef struct {
     const float* down_tscale;     /* NVFP4: fp32 [E] tensor scales of the down matrices */
 } moe_layer_desc;
 
-/* Optional copies of intermediate results (device pointers, each may be NULL). */
+/* Optional copies of intermediate results (device pointers, each may be NULL), and
+ * optional stage-boundary events for timing: each non-NULL stage_events[i] must be a
+ * cudaEvent_t created by the caller; it is recorded on the stream at boundary i:
+ * 0 before routing, 1 after routing and the permutation, 2 after gate.up, 3 after the
+ * down projection, 4 after the combine.  Recording works inside stream capture too. */
 typedef struct {
     float* logits;     /* [T][E] fp32 (not written when routing is supplied) */
     int32_t* idx;      /* [T][k] */
@@ -169,6 +173,7 @@ typedef struct {
     int32_t* perm;     /* [T*k]: pair id (t*k+j) at each sorted row */
     int32_t* pos;      /* [T*k]: sorted row of each pair */
     float* h;          /* [T*k][f] activations in sorted-row order */
+    void* stage_events[5];
 } moe_trace;
 
 /* Workspace bytes moe_layer_forward needs for up to T_max tokens; 0 on a bad desc. */
@@ -199,6 +204,10 @@ size_t moe_layer_workspace_bytes(const moe_layer_desc* desc, int64_t T_max);
 moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtype xt, int64_t T,
                              const int32_t* idx_in, const float* w_in, float* out, void* workspace,
                              size_t ws_bytes, const moe_trace* trace, moe_stream_t stream);
+
+/* Number of kernels one moe_layer_forward call launches for this desc, T and routing
+ * (routing_supplied != 0 when idx_in/w_in are given); -1 on a bad desc or T. */
+int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_t routing_supplied);
 
 /*
  * moe_rmsnorm_bf16 -- glue between stacked layers: xo[t] = bf16(x[t] / sqrt(mean(x[t]^2)

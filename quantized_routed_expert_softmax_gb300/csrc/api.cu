@@ -285,6 +285,13 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     const Workspace ws = bind(workspace, L);
     const int k = desc->k;
 
+    auto mark = [&](int i) {
+        if (trace && trace->stage_events[i] && e == cudaSuccess)
+            e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(trace->stage_events[i]), s,
+                                         cudaEventRecordExternal);   // a real record node under capture
+    };
+    mark(0);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
     // 1. router + top-k + softmax, 2. permutation by expert
     if (!idx_in) {
         e = launch_router_logits(x, xt, desc->router_w, T, desc->d, desc->E, ws.logits, s);
@@ -326,10 +333,18 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.gu_ts = desc->gate_up_tscale;
     a.dn_ts = desc->down_tscale;
     a.ws = ws;
+    mark(1);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
     if ((e = launch_gate_up_gemv(a, desc->wfmt, desc->act, p.slot_cap, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(2);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
     if ((e = launch_down_gemv(a, desc->wfmt, p.slot_cap, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(3);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
     if ((e = launch_combine(ws.w, ws.pos, ws.y, T, k, desc->d, p.ksplit, p.P * desc->d, out, s)) != cudaSuccess)
         return MOE_ERR_CUDA;
+    mark(4);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     if (trace) {
         auto cp = [&](void* dst, const void* src, size_t bytes) {
@@ -345,6 +360,18 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     return MOE_OK;
+}
+
+int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_t routing_supplied) {
+    if (validate_desc(desc) != MOE_OK || T < 0 || T > kMaxTokens) return -1;
+    if (T == 0) return 0;
+    const Plan p = make_plan(desc, T);
+    int n = 0;
+    if (!routing_supplied) n += 1;                          // router logits
+    if (p.small_route) n += 1;                              // top-k + permutation in one block
+    else n += (routing_supplied ? 0 : 1) + 3;               // top-k, rank, scan, scatter
+    n += 3;                                                 // gate.up, down, combine
+    return n;
 }
 
 moe_status moe_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uint16_t* xo, moe_stream_t stream) {

@@ -25,7 +25,7 @@ PATH = {"auto": 0, "gemv": 1, "gemm": 2}
 # Every symbol include/moe.h declares.
 EXPORTS = ["moe_q8_0_bytes", "moe_nvfp4_bytes", "moe_quantize_q8_0", "moe_pack_nvfp4", "moe_router_workspace_bytes",
            "moe_router_topk", "moe_layer_workspace_bytes", "moe_layer_forward", "moe_rmsnorm_bf16",
-           "moe_get_device_status", "moe_status_string", "moe_abi_version"]
+           "moe_get_device_status", "moe_status_string", "moe_abi_version", "moe_layer_forward_launches"]
 
 
 class MoeError(RuntimeError):
@@ -44,7 +44,8 @@ class LayerDesc(ctypes.Structure):
 
 
 class Trace(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("logits", "idx", "w", "offsets", "perm", "pos", "h")]
+    _fields_ = [(n, ctypes.c_void_p) for n in ("logits", "idx", "w", "offsets", "perm", "pos", "h")] + [
+        ("stage_events", ctypes.c_void_p * 5)]
 
 
 _lib = None
@@ -72,6 +73,7 @@ def lib() -> ctypes.CDLL:
             "moe_get_device_status": (I32, [P, P, ctypes.POINTER(I32)]),
             "moe_status_string": (ctypes.c_char_p, [I32]),
             "moe_abi_version": (I32, []),
+            "moe_layer_forward_launches": (I32, [ctypes.POINTER(LayerDesc), I64, I32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -198,7 +200,15 @@ class MoELayer:
             self._ws_tokens = T
         return self._ws
 
-    def forward(self, x, idx_in=None, w_in=None, out=None, trace: dict | None = None, workspace=None, stream=None):
+    def launches(self, T: int, routing_supplied: bool = False) -> int:
+        """Kernels one forward launches (moe_layer_forward_launches)."""
+        return int(lib().moe_layer_forward_launches(ctypes.byref(self.desc), T, int(routing_supplied)))
+
+    def forward(self, x, idx_in=None, w_in=None, out=None, trace: dict | None = None, workspace=None, stream=None,
+                stage_events=None):
+        """moe_layer_forward.  trace: a dict filled with device copies of the intermediates.
+        stage_events: up to 5 torch.cuda.Event (timing enabled, already recorded once so
+        that the handle exists) recorded at the stage boundaries."""
         import torch
         T = x.shape[0]
         if out is None:
@@ -222,6 +232,11 @@ class MoELayer:
                 pos=torch.empty(P, dtype=torch.int32, device=dev),
                 h=torch.empty((P, self.f), dtype=torch.float32, device=dev))
             tr = Trace(*[_ptr(trace[n]) for n in ("logits", "idx", "w", "offsets", "perm", "pos", "h")])
+        if stage_events is not None:
+            if tr is None:
+                tr = Trace()
+            for i, ev in enumerate(stage_events):
+                tr.stage_events[i] = None if ev is None else ev.cuda_event
         st = lib().moe_layer_forward(ctypes.byref(self.desc), _ptr(x), _x_dtype(x), T, _ptr(idx_in), _ptr(w_in),
                                      _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(),
                                      ctypes.byref(tr) if tr is not None else None,
