@@ -197,7 +197,7 @@ size_t moe_layer_workspace_bytes(const moe_layer_desc* desc, int64_t T_max);
  *            aligned, zero-filled before its first use (the library leaves its control
  *            words zero again after every call).
  * trace      optional copies of intermediates, or NULL.
- * T = 0 returns MOE_OK and launches nothing.
+ * T = 0 returns MOE_OK, launches nothing and touches no buffer (they may be NULL).
  * Errors: INVALID_ARG, SHAPE (d a multiple of 256 up to 65536; f a multiple of 32 (Q8_0) or
  * 64 (NVFP4) up to 32768; E a multiple of 4 up to 1024), ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
  */

@@ -265,13 +265,13 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
                              size_t ws_bytes, const moe_trace* trace, moe_stream_t stream) {
     moe_status st = validate_desc(desc);
     if (st != MOE_OK) return st;
-    if (!x || !out) return MOE_ERR_INVALID_ARG;
     if (xt != MOE_F32 && xt != MOE_BF16) return MOE_ERR_INVALID_ARG;
-    if ((idx_in == nullptr) != (w_in == nullptr)) return MOE_ERR_INVALID_ARG;
     if (T < 0 || T > kMaxTokens) return MOE_ERR_SHAPE;
+    if (T == 0) return MOE_OK;                 // an empty batch: its (possibly NULL) buffers are not touched
+    if (!x || !out) return MOE_ERR_INVALID_ARG;
+    if ((idx_in == nullptr) != (w_in == nullptr)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
     if (idx_in && (!aligned16(idx_in) || !aligned16(w_in))) return MOE_ERR_ALIGNMENT;
-    if (T == 0) return MOE_OK;
     if (!workspace) return MOE_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_ALIGNMENT;
     const Layout L = layout_for(desc, T);
