@@ -217,6 +217,36 @@ int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_
 moe_status moe_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uint16_t* xo, moe_stream_t stream);
 
 /*
+ * Bytes of the fixed device scratch behind moe_layer_forward_noalloc (16 MiB).
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * moe_layer_forward_noalloc -- moe_layer_forward for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this call: it exists for callers that are
+ * handed only input and output buffers and a stream (a plugin inside an engine that owns
+ * every allocation), or that must not allocate while serving (an allocation can
+ * synchronise the device, and allocation is not allowed while a stream is being
+ * captured).  It computes exactly what moe_layer_forward computes, with the same
+ * arguments minus the workspace and trace, and allocates nothing: its scratch is a
+ * 16 MiB array inside the library (MOE_NOALLOC_SCRATCH_BYTES), which every GPU that loads
+ * libmoe holds until the process exits.
+ *   - The first call on a device looks up that array's device address (with the device
+ *     current); make that first call before any stream capture.
+ *   - Problems whose moe_layer_workspace_bytes(desc, T) exceeds the scratch are rejected
+ *     with MOE_ERR_WORKSPACE (decode-sized T fits: e.g. the 512-expert, top-22 latent
+ *     layer at T = 32 needs about 11 MB); use moe_layer_forward for larger T.
+ *   - Every call shares the one array, so calls that may overlap on the GPU (different
+ *     streams without ordering between them) race and corrupt each other's results;
+ *     order them on one stream.
+ *   - Each call clears the array's device-error word first; out-of-range supplied expert
+ *     indices are still clamped, but there is no workspace to query afterwards.
+ * Errors: as moe_layer_forward, plus WORKSPACE when the problem does not fit.
+ */
+moe_status moe_layer_forward_noalloc(const moe_layer_desc* desc, const void* x, moe_dtype xt, int64_t T,
+                                     const int32_t* idx_in, const float* w_in, float* out, moe_stream_t stream);
+
+/*
  * moe_get_device_status -- synchronises `stream`, reads the error word of a layer
  * workspace, clears it, and returns MOE_OK or MOE_ERR_DEVICE_CHECK (the device code in
  * *device_code, may be NULL): 1 = an expert index outside [0, E) was clamped.

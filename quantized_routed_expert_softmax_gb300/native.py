@@ -25,7 +25,8 @@ PATH = {"auto": 0, "gemv": 1, "gemm": 2}
 # Every symbol include/moe.h declares.
 EXPORTS = ["moe_q8_0_bytes", "moe_nvfp4_bytes", "moe_quantize_q8_0", "moe_pack_nvfp4", "moe_router_workspace_bytes",
            "moe_router_topk", "moe_layer_workspace_bytes", "moe_layer_forward", "moe_rmsnorm_bf16",
-           "moe_get_device_status", "moe_status_string", "moe_abi_version", "moe_layer_forward_launches"]
+           "moe_get_device_status", "moe_status_string", "moe_abi_version", "moe_layer_forward_launches",
+           "moe_layer_forward_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -74,6 +75,7 @@ def lib() -> ctypes.CDLL:
             "moe_status_string": (ctypes.c_char_p, [I32]),
             "moe_abi_version": (I32, []),
             "moe_layer_forward_launches": (I32, [ctypes.POINTER(LayerDesc), I64, I32]),
+            "moe_layer_forward_noalloc": (I32, [ctypes.POINTER(LayerDesc), P, I32, I64, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -242,6 +244,18 @@ class MoELayer:
                                      ctypes.byref(tr) if tr is not None else None,
                                      _stream(stream))
         _check("moe_layer_forward", st)
+        return out
+
+    def forward_noalloc(self, x, idx_in=None, w_in=None, out=None, stream=None):
+        """moe_layer_forward_noalloc: the same forward with the library's fixed scratch
+        instead of a workspace (for callers that cannot allocate device memory)."""
+        import torch
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.d), dtype=torch.float32, device=x.device)
+        _check("moe_layer_forward_noalloc",
+               lib().moe_layer_forward_noalloc(ctypes.byref(self.desc), _ptr(x), _x_dtype(x), T, _ptr(idx_in),
+                                               _ptr(w_in), _ptr(out), _stream(stream)))
         return out
 
     def device_status(self, stream=None) -> int:
