@@ -432,15 +432,24 @@ def active_expert_bytes(stack, inputs, T, w):
     return {"step": int(step), "gate_up_per_layer": int(statistics.mean(gu_layer))}
 
 
+def kernel_source_sha():
+    import hashlib
+    csrc = os.path.join(ROOT, "quantized_routed_expert_softmax_gb300", "csrc")
+    blob = open(os.path.join(csrc, "gemv.cu"), "rb").read() + open(os.path.join(csrc, "common.cuh"), "rb").read()
+    return hashlib.sha1(blob).hexdigest()[:12]
+
+
 def measured_traffic(workload, T):
-    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if one
-    exists for this kernel build and workload; else None."""
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, when it
+    was taken on this kernel source (gemv.cu + common.cuh) and workload; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        data = json.load(open(p))
-        return data.get(f"{workload}_T{T}")
+        entry = json.load(open(p)).get(f"{workload}_T{T}")
     except (OSError, ValueError):
         return None
+    if not entry or entry.get("source_sha1_12") != kernel_source_sha():
+        return None
+    return entry.get("bytes")
 
 
 # ====================================================================== reference arm

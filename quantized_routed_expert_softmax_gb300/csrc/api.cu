@@ -16,11 +16,12 @@ cudaError_t launch_route_small(const float*, const int32_t*, const float*, int64
                                const Workspace&, cudaStream_t);
 cudaError_t launch_permute_large(const int32_t*, const float*, int64_t, int64_t, int, int, const Workspace&,
                                  cudaStream_t);
+cudaError_t launch_route_decode(const void*, int, const float*, int64_t, int64_t, int64_t, int, int, const Workspace&,
+                                cudaStream_t);
 cudaError_t configure_gemv_kernels();
 cudaError_t launch_gate_up_gemv(const ExpertArgs&, int, int, int, cudaStream_t);
 cudaError_t launch_down_gemv(const ExpertArgs&, int, int, cudaStream_t);
-cudaError_t launch_combine(const float*, const int32_t*, const float*, int64_t, int, int64_t, int, int64_t, float*,
-                           cudaStream_t);
+cudaError_t launch_combine(const float*, const int32_t*, const float*, int64_t, int, int64_t, float*, cudaStream_t);
 cudaError_t launch_rmsnorm_bf16(const float*, int64_t, int64_t, float, uint16_t*, cudaStream_t);
 
 
@@ -31,7 +32,9 @@ constexpr int64_t kMaxTokens = 1 << 20;
 constexpr int64_t kMaxF = 32768;     // group-mask words per slot fit the kernels' 64-word array
 constexpr int kSmallT = 32;          // route_small handles up to 32 tokens
 constexpr int kSmallPairs = 1024;    // ... and up to 1024 pairs
-constexpr size_t kSmemBudget = 96 * 1024;
+constexpr int64_t kFusedRouteLogits = 4096;   // ... and up to 4096 logits (the routing CTA keeps them on chip)
+constexpr size_t kSmemBudget = 96 * 1024;        // token rows staged per expert CTA (plus the 55 KB ring)
+constexpr int64_t kPrefetchBudget = 64ll << 20;   // down weights prefetched into L2 (of 126 MB)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -60,19 +63,12 @@ struct Plan {
     int nchunk;
     int gwords;
     int tt_gu, tt_dn;
-    int ksplit;
-    int64_t y_rows;     // rows of the y partial buffer per split stride (P)
-    bool small_route;
+    bool small_route;   // T <= 32 and P <= 1024: routing and permutation in one CTA
+    bool fuse_combine;  // the down kernel's last CTA per row tile combines (one item per thread)
+    bool prefetch_down; // gate.up CTAs prefetch the routed experts' down weights into L2
 };
 
-int down_ksplit(const moe_layer_desc* d, int64_t P) {
-    if (P > 64) return 1;
-    const int64_t units = (d->wfmt == MOE_W_Q8_0) ? d->f / 32 : d->f / 16;
-    const int64_t want = (d->wfmt == MOE_W_Q8_0) ? 4 : 8;
-    return static_cast<int>(std::max<int64_t>(1, std::min(want, units)));
-}
-
-Plan make_plan(const moe_layer_desc* d, int64_t T) {
+Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     Plan p{};
     p.T = T;
     p.P = T * d->k;
@@ -80,24 +76,31 @@ Plan make_plan(const moe_layer_desc* d, int64_t T) {
     p.nchunk = static_cast<int>((p.P + 1023) / 1024);
     p.gwords = static_cast<int>((d->f / 16 + 31) / 32);
     const int64_t tmax = std::max<int64_t>(1, std::min<int64_t>(8, T));
-    p.tt_gu = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tmax, kSmemBudget / (4 * d->d))));
+    // staged activations: f16 (bf16 inputs) or f16 hi + lo (fp32 inputs; h always) per element
+    const int64_t x_bytes = (xt == MOE_F32) ? 4 : 2;
+    p.tt_gu = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tmax, kSmemBudget / (x_bytes * d->d))));
     const int64_t dn_cap = (d->wfmt == MOE_W_NVFP4) ? 4 : 8;
     p.tt_dn = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(std::min(tmax, dn_cap), kSmemBudget / (4 * d->f))));
     // the tile counts are powers of two up to 8 (the kernels specialise 1, 2, 4, 8)
     auto pow2 = [](int v) { return v >= 8 ? 8 : (v >= 4 ? 4 : (v >= 2 ? 2 : 1)); };
     p.tt_gu = pow2(p.tt_gu);
     p.tt_dn = pow2(p.tt_dn);
-    p.ksplit = down_ksplit(d, p.P);
-    p.small_route = (T <= kSmallT && p.P <= kSmallPairs);
+    p.small_route = (T <= kSmallT && p.P <= kSmallPairs && T * d->E <= kFusedRouteLogits);
+    const int64_t rows_per_tile = (d->wfmt == MOE_W_Q8_0) ? 32 : 256;
+    p.fuse_combine = T * rows_per_tile <= 256;
+    const int64_t dn_bytes = static_cast<int64_t>(d->wfmt == MOE_W_Q8_0 ? moe_q8_0_bytes(d->d, d->f)
+                                                                          : moe_nvfp4_bytes(d->d, d->f));
+    p.prefetch_down = static_cast<int64_t>(p.slot_cap) * dn_bytes <= kPrefetchBudget;
     return p;
 }
 
 struct Layout {
-    size_t err, n_active, logits, idx, w, offsets, perm, pos, act_e, chunk_cnt, local_rank, gmask, h, y, total;
+    size_t err, route_ctr, n_active, row_ctr, logits, rpart, idx, w, offsets, perm, pos, act_e, slot_info, chunk_cnt,
+        local_rank, gmask, h, y, total;
 };
 
-// Workspace regions for T tokens (each 256-byte aligned).  The y region is sized for the
-// largest split count any T <= T_max can use.
+// Workspace regions for T tokens (each 256-byte aligned).  The control words (err,
+// route_ctr, row_ctr) come first; they must be zero before a call and are left zero.
 Layout layout_for(const moe_layer_desc* d, int64_t T) {
     const Plan p = make_plan(d, T);
     Layout L{};
@@ -107,38 +110,45 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
         off = round_up(off + bytes, 256);
         return at;
     };
-    L.err = take(4);
-    L.n_active = take(4);
+    L.err = 0;
+    L.route_ctr = 4;
+    L.n_active = 8;
+    off = 256;
+    L.row_ctr = take(sizeof(int32_t) * (d->d / 32));
     L.logits = take(sizeof(float) * T * d->E);
+    L.rpart = take(p.small_route ? sizeof(float) * T * d->E * 32 : 0);
     L.idx = take(sizeof(int32_t) * p.P);
     L.w = take(sizeof(float) * p.P);
     L.offsets = take(sizeof(int32_t) * (d->E + 1));
     L.perm = take(sizeof(int32_t) * p.P);
     L.pos = take(sizeof(int32_t) * p.P);
     L.act_e = take(sizeof(int32_t) * p.slot_cap);
+    L.slot_info = take(sizeof(int4) * p.slot_cap);
     L.chunk_cnt = take(sizeof(int32_t) * p.nchunk * d->E);
     L.local_rank = take(sizeof(int32_t) * p.P);
     L.gmask = take(sizeof(uint32_t) * p.slot_cap * p.gwords);
     L.h = take(sizeof(float) * p.P * d->f);
-    // splits are used only while P <= 64 (at most 8 of them)
-    const int64_t y_rows = std::max<int64_t>(p.P, std::min<int64_t>(p.P, 64) * 8);
-    L.y = take(sizeof(float) * y_rows * d->d);
+    L.y = take(sizeof(float) * p.P * d->d);
     L.total = off;
     return L;
 }
 
 Workspace bind(void* base, const Layout& L) {
     char* b = static_cast<char*>(base);
-    Workspace w;
+    Workspace w{};
     w.err = reinterpret_cast<int32_t*>(b + L.err);
+    w.route_ctr = reinterpret_cast<int32_t*>(b + L.route_ctr);
+    w.row_ctr = reinterpret_cast<int32_t*>(b + L.row_ctr);
     w.n_active = reinterpret_cast<int32_t*>(b + L.n_active);
     w.logits = reinterpret_cast<float*>(b + L.logits);
+    w.rpart = reinterpret_cast<float*>(b + L.rpart);
     w.idx = reinterpret_cast<int32_t*>(b + L.idx);
     w.w = reinterpret_cast<float*>(b + L.w);
     w.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
     w.perm = reinterpret_cast<int32_t*>(b + L.perm);
     w.pos = reinterpret_cast<int32_t*>(b + L.pos);
     w.act_e = reinterpret_cast<int32_t*>(b + L.act_e);
+    w.slot_info = reinterpret_cast<int4*>(b + L.slot_info);
     w.chunk_cnt = reinterpret_cast<int32_t*>(b + L.chunk_cnt);
     w.local_rank = reinterpret_cast<int32_t*>(b + L.local_rank);
     w.gmask = reinterpret_cast<uint32_t*>(b + L.gmask);
@@ -252,12 +262,14 @@ moe_status moe_router_topk(const void* x, moe_dtype xt, const float* W, int64_t 
 
 size_t moe_layer_workspace_bytes(const moe_layer_desc* desc, int64_t T_max) {
     if (validate_desc(desc) != MOE_OK || T_max < 1 || T_max > kMaxTokens) return 0;
-    // The largest layout over T <= T_max: every region grows with T except the split y
-    // region, which is bounded by the P <= 64 case; take the max of both ends.
-    const size_t a = layout_for(desc, T_max).total;
-    const int64_t t_small = std::min<int64_t>(T_max, std::max<int64_t>(1, 64 / desc->k));
-    const size_t b = layout_for(desc, t_small).total;
-    return std::max(a, b);
+    // Regions grow with T inside each routing regime; the fused small-batch routing also
+    // needs a partial-sum buffer, so take the larger of the two regimes' layouts.
+    int64_t t_small = std::min<int64_t>(T_max, kSmallT);
+    t_small = std::min<int64_t>(t_small, kSmallPairs / desc->k);
+    t_small = std::min<int64_t>(t_small, kFusedRouteLogits / desc->E);
+    size_t n = layout_for(desc, T_max).total;
+    if (t_small >= 1) n = std::max(n, layout_for(desc, t_small).total);
+    return n;
 }
 
 moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtype xt, int64_t T,
@@ -281,7 +293,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     cudaError_t e = ensure_configured();
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const Plan p = make_plan(desc, T);
+    const Plan p = make_plan(desc, T, xt);
     const Workspace ws = bind(workspace, L);
     const int k = desc->k;
 
@@ -293,22 +305,20 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     mark(0);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     // 1. router + top-k + softmax, 2. permutation by expert
-    if (!idx_in) {
-        e = launch_router_logits(x, xt, desc->router_w, T, desc->d, desc->E, ws.logits, s);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-    }
-    if (p.small_route) {
-        e = launch_route_small(idx_in ? nullptr : ws.logits, idx_in, w_in, T, desc->E, k, p.gwords, ws, s);
+    if (p.small_route && !idx_in) {
+        e = launch_route_decode(x, xt, desc->router_w, T, desc->d, desc->E, k, p.gwords, ws, s);
+    } else if (p.small_route) {
+        e = launch_route_small(nullptr, idx_in, w_in, T, desc->E, k, p.gwords, ws, s);
     } else {
         if (!idx_in) {
-            e = launch_topk_softmax(ws.logits, T, desc->E, k, ws.idx, ws.w, s);
-            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            e = launch_router_logits(x, xt, desc->router_w, T, desc->d, desc->E, ws.logits, s);
+            if (e == cudaSuccess) e = launch_topk_softmax(ws.logits, T, desc->E, k, ws.idx, ws.w, s);
         }
-        e = launch_permute_large(idx_in, w_in, T, desc->E, k, p.gwords, ws, s);
+        if (e == cudaSuccess) e = launch_permute_large(idx_in, w_in, T, desc->E, k, p.gwords, ws, s);
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    // 3. gate.up + activation + group mask, 4. sparse down, 5. combine
+    // 3. gate.up + activation + group mask, 4. sparse down (+ combine), 5. combine
     ExpertArgs a{};
     a.x = x;
     a.xt = xt;
@@ -318,9 +328,12 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.rows_gu = static_cast<int>(desc->act == MOE_ACT_SWIGLU ? 2 * desc->f : desc->f);
     a.tt_gu = p.tt_gu;
     a.tt_dn = p.tt_dn;
-    a.ksplit = p.ksplit;
     a.gwords = p.gwords;
+    a.T = static_cast<int>(T);
     a.P = static_cast<int>(p.P);
+    a.fuse_combine = p.fuse_combine ? 1 : 0;
+    a.prefetch_down = p.prefetch_down ? 1 : 0;
+    a.out = out;
     a.w_gu = static_cast<const uint8_t*>(desc->w_gate_up);
     a.w_dn = static_cast<const uint8_t*>(desc->w_down);
     if (desc->wfmt == MOE_W_Q8_0) {
@@ -341,8 +354,9 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     if ((e = launch_down_gemv(a, desc->wfmt, p.slot_cap, s)) != cudaSuccess) return MOE_ERR_CUDA;
     mark(3);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if ((e = launch_combine(ws.w, ws.pos, ws.y, T, k, desc->d, p.ksplit, p.P * desc->d, out, s)) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (!p.fuse_combine) {
+        if ((e = launch_combine(ws.w, ws.pos, ws.y, T, k, desc->d, out, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    }
     mark(4);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -367,10 +381,10 @@ int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_
     if (T == 0) return 0;
     const Plan p = make_plan(desc, T);
     int n = 0;
-    if (!routing_supplied) n += 1;                          // router logits
-    if (p.small_route) n += 1;                              // top-k + permutation in one block
-    else n += (routing_supplied ? 0 : 1) + 3;               // top-k, rank, scan, scatter
-    n += 3;                                                 // gate.up, down, combine
+    if (p.small_route) n += 1;                              // routing + permutation in one launch
+    else n += (routing_supplied ? 0 : 2) + 3;               // router, top-k; rank, scan, scatter
+    n += 2;                                                 // gate.up, down
+    if (!p.fuse_combine) n += 1;                            // combine
     return n;
 }
 

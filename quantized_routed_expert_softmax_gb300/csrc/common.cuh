@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -17,22 +19,29 @@ constexpr int kRouterPartials = 256;   // partial sums of the router's canonical
 constexpr int kMaxK = 32;              // top-k fits one warp
 constexpr int kMaxE = 1024;
 
-// Pointers into one layer workspace (see layout_workspace in api.cu).
+// Pointers into one layer workspace (see layout_for in api.cu).  The control words
+// (err, route_ctr, row_ctr) must be zero before a call; the kernels leave the counters
+// zero again when they finish.
 struct Workspace {
     int32_t* err;          // [1] sticky first error
+    int32_t* route_ctr;    // [1] CTAs of the routing kernel that have finished their logits
+    int32_t* row_ctr;      // [d/32] down CTAs finished per row tile (fused combine)
     int32_t* n_active;     // [1] number of experts with at least one pair
     float* logits;         // [T][E]
+    float* rpart;          // [T][E][32] router partial sums by residue class (fused decode routing)
     int32_t* idx;          // [T][k]
     float* w;              // [T][k]
     int32_t* offsets;      // [E+1]
     int32_t* perm;         // [P] sorted row -> pair
     int32_t* pos;          // [P] pair -> sorted row
     int32_t* act_e;        // [min(E,P)] expert id of each active slot, increasing
+    int4* slot_info;       // [min(E,P)] per slot: expert, first sorted row, pair count (0 = idle slot),
+                           //   and the tokens of its first four rows packed 8 bits each (-1: read perm)
     int32_t* chunk_cnt;    // [nchunk][E] pairs of each expert per chunk (large-T permute)
     int32_t* local_rank;   // [P] rank of a pair among its expert's pairs in its chunk
     uint32_t* gmask;       // [min(E,P)][ceil(f/16/32)] active 16-neuron groups per slot
     float* h;              // [P][f] activations, sorted rows
-    float* y;              // [ksplit][P][d] down partials, sorted rows
+    float* y;              // [P][d] down projections, sorted rows
 };
 
 // Arguments of the expert kernels (gate.up, down) of one layer call.
@@ -41,9 +50,12 @@ struct ExpertArgs {
     int xt;
     int d, f, k, rows_gu;
     int tt_gu, tt_dn;            // tokens per shared-memory tile
-    int ksplit;                  // K splits of the down projection (partials summed in combine)
     int gwords;                  // 32-bit words of group mask per slot
+    int T;                       // tokens
     int P;                       // pairs T*k
+    int fuse_combine;            // the down kernel's last CTA per row tile also combines
+    int prefetch_down;           // gate.up CTAs prefetch the routed experts' down weights into L2
+    float* out;                  // [T][d] layer output (fused combine)
     const uint8_t* w_gu;
     int64_t gu_bytes;            // bytes of one expert's gate/up matrix
     const uint8_t* w_dn;
@@ -52,6 +64,37 @@ struct ExpertArgs {
     const float* dn_ts;
     Workspace ws;
 };
+
+// Programmatic dependent launch: wait for the preceding kernel's memory, and allow the
+// next kernel to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with programmatic stream serialization allowed (the kernel calls pdl_wait()
+// before touching global memory, so overlap with the previous kernel is safe).
+template <typename... Exp, typename... Act>
+inline cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Act&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
+}
+
+constexpr int kNoPackedTokens = -1;
+
+// Token of sorted row r0 + i of a slot, from the packed field when present.
+__device__ __forceinline__ int slot_token(const int4& si, int i, const int32_t* perm, int k) {
+    if (si.w != kNoPackedTokens && i < 4) return (si.w >> (8 * i)) & 0xff;
+    return perm[si.y + i] / k;
+}
 
 __device__ __forceinline__ void set_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
 

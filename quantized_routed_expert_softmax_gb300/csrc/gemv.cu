@@ -10,23 +10,39 @@
 // combine: same page, "How we check correctness": per-(token, expert) results summed in
 //   a fixed order instead of scatter-add atomics.
 //
-// Layout in HBM (see include/moe.h): weights in K panels, so that lane l of a warp owns
-// one weight row and streams it 32 bytes per panel; a warp reads 1 KB contiguous per
-// panel (fully coalesced) and no cross-lane reduction is needed.  The tokens of one
-// expert sit in shared memory as fp32; dequantisation is exact (int8 or e2m1 codes
-// times the block scale) and accumulation is fp32.  One CTA's 8 warps split the K
-// panels of its rows and reduce through shared memory in a fixed order, so results are
-// bitwise reproducible.
+// Layout in HBM (include/moe.h): weights in K panels, so that lane l of a warp owns one
+// weight row and streams it 32 bytes per panel; a warp reads 1 KB contiguous per panel
+// and no cross-lane reduction is needed.  The 8 warps of a CTA split the K panels of its
+// rows; each warp issues the loads of all its panels (up to a batch of 12) before it
+// waits on any of them, so a CTA keeps its whole weight slice in flight.  Partial sums
+// meet in shared memory in a fixed warp order: results are bitwise reproducible.
+// Dequantisation is exact (int8 or e2m1 codes times the block scale); accumulation is
+// fp32; the tokens of one expert sit in shared memory as fp32.
 #include "common.cuh"
 
 namespace moe {
 
-
 __device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
     uint4 v;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// Same, with an L2 evict-first policy: weights read once should not push out data that
+// is still wanted (the down weights prefetched into L2 while gate.up streams).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint4 ldg_stream16_ef(const uint8_t* p, uint64_t pol) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(pol));
     return v;
 }
 
@@ -42,10 +58,44 @@ __device__ __forceinline__ uint2 ldg_stream8(const uint8_t* p) {
     return v;
 }
 
-__device__ __forceinline__ float ldg_half(const uint8_t* p) {
+__device__ __forceinline__ uint32_t ldg_u16(const uint8_t* p) {
     unsigned short v;
     asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
-    return __half2float(__ushort_as_half(v));
+    return v;
+}
+
+__device__ __forceinline__ float half_bits_to_f32(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// Bring `bytes` (a multiple of 16, 16-byte aligned) into L2 without loading registers.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Per-thread asynchronous copies global -> shared (no registers held while in flight).
+__device__ __forceinline__ void cp_async16_ef(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& a, const uint4& b, int i) {
@@ -66,12 +116,11 @@ __device__ __forceinline__ float f4get(const float4& v, int j) {
 }
 
 // Load the x rows of `nt` tokens (sorted rows r0+t0 ...) into shared memory as fp32.
-__device__ __forceinline__ void load_token_rows(const ExpertArgs& a, int r0, int t0, int nt, float* xs) {
+__device__ __forceinline__ void load_token_rows(const ExpertArgs& a, const int4& si, int t0, int nt, float* xs) {
     const int d4 = a.d / 4;
     for (int i = threadIdx.x; i < nt * d4; i += blockDim.x) {
         const int t = i / d4, c = (i % d4) * 4;
-        const int pair = a.ws.perm[r0 + t0 + t];
-        const int64_t off = static_cast<int64_t>(pair / a.k) * a.d + c;
+        const int64_t off = static_cast<int64_t>(slot_token(si, t0 + t, a.ws.perm, a.k)) * a.d + c;
         float4 v;
         if (a.xt == MOE_F32) {
             v = *reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + off);
@@ -84,372 +133,619 @@ __device__ __forceinline__ void load_token_rows(const ExpertArgs& a, int r0, int
     }
 }
 
-// ------------------------------------------------------------------------------ gate.up
-// Partial dot products of this lane's weight row with N tokens over panels [pb, pe).
-template <int FMT, int N>
-__device__ __forceinline__ void gu_dot(const ExpertArgs& a, const uint8_t* W, int row, int pb, int pe,
-                                       const float* xs, float acc[N]) {
-    const int rows = a.rows_gu;
-    const int d = a.d;
-    constexpr int U = 4;
+__device__ __forceinline__ void load_h_rows(const ExpertArgs& a, int r0, int t0, int nt, float* hs) {
+    const int f4 = a.f / 4;
+    const float4* src = reinterpret_cast<const float4*>(a.ws.h + static_cast<int64_t>(r0 + t0) * a.f);
+    for (int i = threadIdx.x; i < nt * f4; i += blockDim.x) reinterpret_cast<float4*>(hs)[i] = __ldcg(src + i);
+}
+
+// ------------------------------------------------------------------------------ tensor-core GEMV core
+// The multiply-adds run on the tensor cores (mma.sync m16n8k16, f16 inputs, f32
+// accumulation) so the only per-weight ALU work is the exact conversion of the code to f16:
+//   Q8_0 : byte-insert the (sign-flipped) int8 into the mantissa of 1024.0h and subtract
+//          1152.0h: exact integers -128..127; the fp16 block scale is applied to the f32
+//          result of each 32-column panel;
+//   NVFP4: cvt.rn.f16x2.e2m1x2, times the E4M3 block scale (exact: 2 x 4 significant bits).
+// A warp computes two 16-row blocks (A, B) of a 32-row tile over its share of the K panels;
+// up to 8 tokens ride in the MMA's N = 8 columns for free.  In the K order of the MMA,
+// thread t of a quad owns 8 (Q8_0) or 16 (NVFP4) consecutive columns of a panel, the same
+// columns for the weights (A) and the activations (B), so any assignment is a valid dot
+// product order.
+//
+// A warp streams its panels through a ring of kStages slots in shared memory: per slot the
+// 2 x 512 code bytes of its 32 rows and their scales (64 or 128 bytes), copied with
+// cp.async by all 32 lanes; cp.async.wait_group + __syncwarp make a slot readable.
+constexpr int kStages = 6;
+constexpr int kSlotBytes = 1024 + 128;
+
+__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four signed int8 in a word -> two f16x2 (bytes 0,1 and bytes 2,3), exact.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;                       // int8 + 128 as unsigned bytes
+    const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140);   // halves 0x64 u0, 0x64 u1 = 1024 + u
+    const uint32_t h = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+    const __half2 lv = __hsub2(*reinterpret_cast<const __half2*>(&l), off);
+    const __half2 hv = __hsub2(*reinterpret_cast<const __half2*>(&h), off);
+    lo = *reinterpret_cast<const uint32_t*>(&lv);
+    hi = *reinterpret_cast<const uint32_t*>(&hv);
+}
+
+// One byte of two E2M1 codes times an f16 scale -> f16x2, exact.
+__device__ __forceinline__ uint32_t e2m1x2_scaled(uint32_t byte, __half2 sc) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
+    const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), sc);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ __half2 e4m3_to_h2(uint32_t byte) {
+    uint32_t h2;
+    const uint16_t in = static_cast<uint16_t>(byte & 0xffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    const __half h = __ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu));
+    return __halves2half2(h, h);
+}
+
+// Copy one panel's codes of rows [rowA, rowA+16) and [rowB, rowB+16) and their scales into
+// a slot.  Chunk c (16 bytes) of a 512-byte block is row c/2, columns 16*(c%2)..; `skip`
+// bit 0 / 1 drops the first / second 16 columns (inactive neuron groups, Q8_0 down).
+template <int FMT>
+__device__ __forceinline__ void issue_panel_block(uint32_t slot, const uint8_t* W, int rows, int rowA, int rowB,
+                                                  int b, uint64_t pol, int skip) {
+    const int lane = threadIdx.x & 31;
+    const int64_t pbytes = static_cast<int64_t>(rows) * (FMT == MOE_W_Q8_0 ? 34 : 36);
+    const uint8_t* P = W + b * pbytes;
+    const bool keep = !((skip >> (lane & 1)) & 1);
+    if (keep) {
+        cp_async16_ef(slot + lane * 16, P + rowA * 32 + lane * 16, pol);
+        cp_async16_ef(slot + 512 + lane * 16, P + rowB * 32 + lane * 16, pol);
+    }
+    const uint8_t* S = P + rows * 32;
+    if (FMT == MOE_W_Q8_0) {   // 2 bytes per row: 32 bytes per block
+        if (lane < 2) cp_async16(slot + 1024 + lane * 16, S + rowA * 2 + lane * 16);
+        else if (lane < 4) cp_async16(slot + 1024 + 32 + (lane - 2) * 16, S + rowB * 2 + (lane - 2) * 16);
+    } else {                   // 4 bytes per row: 64 bytes per block
+        if (lane < 4) cp_async16(slot + 1024 + lane * 16, S + rowA * 4 + lane * 16);
+        else if (lane < 8) cp_async16(slot + 1024 + 64 + (lane - 4) * 16, S + rowB * 4 + (lane - 4) * 16);
+    }
+}
+
+// acc[blk][i] += this panel's contribution; xs: f16 activations [8 tokens][ld] (rows >= nt
+// are never read: their B fragments are zero).  `skip`: inactive 16-column halves.
+// With `split`, the activations are fp32 values carried as two f16 terms (hi at xs, lo at
+// xs + lo_off, v ~= hi + lo to ~22 bits): each weight fragment meets both.
+template <int FMT>
+__device__ __forceinline__ void panel_mma(const unsigned char* slot, const __half* xs, int ld, int b, int nt,
+                                          int skip, float acc[2][4], bool split, int lo_off) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const bool has_tok = g < nt;
     if (FMT == MOE_W_Q8_0) {
-        const int64_t pbytes = static_cast<int64_t>(rows) * 34;
-        for (int b = pb; b < pe; b += U) {
-            uint4 q0[U], q1[U];
-            float sc[U];
+        uint4 xv = make_uint4(0, 0, 0, 0), xl = make_uint4(0, 0, 0, 0);
+        if (has_tok) {
+            xv = *reinterpret_cast<const uint4*>(xs + g * ld + b * 32 + 8 * t);
+            if (split) xl = *reinterpret_cast<const uint4*>(xs + lo_off + g * ld + b * 32 + 8 * t);
+        }
+        const bool dead = (skip >> (t >> 1)) & 1;   // thread t covers columns 8t..8t+7
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (b + u < pe) {
-                    const uint8_t* P = W + (b + u) * pbytes;
-                    q0[u] = ldg_stream16(P + row * 32);
-                    q1[u] = ldg_stream16(P + row * 32 + 16);
-                    sc[u] = ldg_half(P + rows * 32 + row * 2);
-                }
+        for (int blk = 0; blk < 2; ++blk) {
+            const unsigned char* cb = slot + blk * 512;
+            uint2 r0 = *reinterpret_cast<const uint2*>(cb + g * 32 + 8 * t);
+            uint2 r8 = *reinterpret_cast<const uint2*>(cb + (g + 8) * 32 + 8 * t);
+            if (dead) r0 = r8 = make_uint2(0u, 0u);   // a skipped group: its bytes were not copied
+            const unsigned short* sc = reinterpret_cast<const unsigned short*>(slot + 1024 + blk * 32);
+            const float s0 = __half2float(__ushort_as_half(sc[g]));
+            const float s8 = __half2float(__ushort_as_half(sc[g + 8]));
+            uint32_t a0, a2, a1, a3, c0, c2, c1, c3;
+            s8x4_to_f16x2x2(r0.x, a0, a2);
+            s8x4_to_f16x2x2(r8.x, a1, a3);
+            s8x4_to_f16x2x2(r0.y, c0, c2);
+            s8x4_to_f16x2x2(r8.y, c1, c3);
+            float dd[4] = {0.f, 0.f, 0.f, 0.f};
+            mma16816(dd, a0, a1, a2, a3, xv.x, xv.y);
+            mma16816(dd, c0, c1, c2, c3, xv.z, xv.w);
+            if (split) {
+                mma16816(dd, a0, a1, a2, a3, xl.x, xl.y);
+                mma16816(dd, c0, c1, c2, c3, xl.z, xl.w);
             }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (b + u < pe) {
-                    float part[N];
-#pragma unroll
-                    for (int t = 0; t < N; ++t) part[t] = 0.0f;
-                    const float* xb = xs + (b + u) * 32;
-#pragma unroll
-                    for (int wi = 0; wi < 8; ++wi) {
-                        const uint32_t word = word_of(q0[u], q1[u], wi);
-                        float4 xv[N];
-#pragma unroll
-                        for (int t = 0; t < N; ++t) xv[t] = *reinterpret_cast<const float4*>(xb + t * d + wi * 4);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float v = s8_to_f32(word, j);
-#pragma unroll
-                            for (int t = 0; t < N; ++t) part[t] = fmaf(v, f4get(xv[t], j), part[t]);
-                        }
-                    }
-#pragma unroll
-                    for (int t = 0; t < N; ++t) acc[t] = fmaf(sc[u], part[t], acc[t]);
-                }
+            acc[blk][0] = fmaf(s0, dd[0], acc[blk][0]);
+            acc[blk][1] = fmaf(s0, dd[1], acc[blk][1]);
+            acc[blk][2] = fmaf(s8, dd[2], acc[blk][2]);
+            acc[blk][3] = fmaf(s8, dd[3], acc[blk][3]);
+        }
+    } else {
+        uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
+        uint4 l0 = make_uint4(0, 0, 0, 0), l1 = make_uint4(0, 0, 0, 0);
+        if (has_tok) {
+            x0 = *reinterpret_cast<const uint4*>(xs + g * ld + b * 64 + 16 * t);
+            x1 = *reinterpret_cast<const uint4*>(xs + g * ld + b * 64 + 16 * t + 8);
+            if (split) {
+                l0 = *reinterpret_cast<const uint4*>(xs + lo_off + g * ld + b * 64 + 16 * t);
+                l1 = *reinterpret_cast<const uint4*>(xs + lo_off + g * ld + b * 64 + 16 * t + 8);
             }
         }
-    } else {   // NVFP4, panels of 64 columns: 32 code bytes + 4 scale bytes per row
-        const int64_t pbytes = static_cast<int64_t>(rows) * 36;
-        for (int b = pb; b < pe; b += U) {
-            uint4 q0[U], q1[U];
-            uint32_t sw[U];
+        const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t xlw[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (b + u < pe) {
-                    const uint8_t* P = W + (b + u) * pbytes;
-                    q0[u] = ldg_stream16(P + row * 32);
-                    q1[u] = ldg_stream16(P + row * 32 + 16);
-                    sw[u] = ldg_stream4(P + rows * 32 + row * 4);
-                }
-            }
+        for (int blk = 0; blk < 2; ++blk) {
+            const unsigned char* cb = slot + blk * 512;
+            const uint2 r0 = *reinterpret_cast<const uint2*>(cb + g * 32 + 8 * t);
+            const uint2 r8 = *reinterpret_cast<const uint2*>(cb + (g + 8) * 32 + 8 * t);
+            const unsigned char* sc = slot + 1024 + blk * 64;   // 4 scale bytes per row
+            const __half2 s0 = e4m3_to_h2(sc[g * 4 + t]);         // columns 16t.. are sub-block t
+            const __half2 s8 = e4m3_to_h2(sc[(g + 8) * 4 + t]);
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (b + u < pe) {
-                    const float* xb = xs + (b + u) * 64;
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {      // 4 sub-blocks of 16 values
-                        float part[N];
-#pragma unroll
-                        for (int t = 0; t < N; ++t) part[t] = 0.0f;
-#pragma unroll
-                        for (int wi = 0; wi < 2; ++wi) {
-                            const uint32_t word = word_of(q0[u], q1[u], 2 * s + wi);
-#pragma unroll
-                            for (int by = 0; by < 4; ++by) {
-                                const float2 v = e2m1x2_to_f32x2((word >> (8 * by)) & 0xffu);
-                                const int c = 16 * s + 8 * wi + 2 * by;
-#pragma unroll
-                                for (int t = 0; t < N; ++t) {
-                                    const float2 xv = *reinterpret_cast<const float2*>(xb + t * d + c);
-                                    part[t] = fmaf(v.x, xv.x, part[t]);
-                                    part[t] = fmaf(v.y, xv.y, part[t]);
-                                }
-                            }
-                        }
-                        const float sb = e4m3_to_f32((sw[u] >> (8 * s)) & 0xffu);
-#pragma unroll
-                        for (int t = 0; t < N; ++t) acc[t] = fmaf(sb, part[t], acc[t]);
-                    }
-                }
+            for (int m = 0; m < 4; ++m) {   // 4 MMAs of 16 columns: bytes 2m, 2m+1 of the 8
+                const uint32_t w0 = (m < 2) ? r0.x : r0.y;
+                const uint32_t w8 = (m < 2) ? r8.x : r8.y;
+                const int sh = (m & 1) * 16;
+                const uint32_t a0 = e2m1x2_scaled((w0 >> sh) & 0xffu, s0);
+                const uint32_t a2 = e2m1x2_scaled((w0 >> (sh + 8)) & 0xffu, s0);
+                const uint32_t a1 = e2m1x2_scaled((w8 >> sh) & 0xffu, s8);
+                const uint32_t a3 = e2m1x2_scaled((w8 >> (sh + 8)) & 0xffu, s8);
+                mma16816(acc[blk], a0, a1, a2, a3, xw[2 * m], xw[2 * m + 1]);
+                if (split) mma16816(acc[blk], a0, a1, a2, a3, xlw[2 * m], xlw[2 * m + 1]);
             }
         }
     }
 }
 
-template <int FMT, int ACT, int N>
-__device__ __forceinline__ void gu_tile(const ExpertArgs& a, const uint8_t* W, int row, int pb, int pe,
-                                        const float* xs, float (*red)[8][32], int e, int r0, int t0, int nt,
-                                        int tile, uint32_t* act_bits) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float acc[N];
+// Stream panels [pb, pe) (restricted to `active` ones when gm != nullptr) through the
+// warp's ring and accumulate.
+template <int FMT, typename Between>
+__device__ __forceinline__ void stream_panels(const uint8_t* W, int rows, int rowA, int rowB, int pb, int pe,
+                                              unsigned char* ring, const __half* xs, int ld, int nt,
+                                              const uint32_t* gm, float acc[2][4], bool split, int lo_off,
+                                              Between&& between) {
+    const uint64_t pol = l2_evict_first_policy();
+    auto skip_of = [&](int b) -> int {
+        if (!gm) return 0;
+        const int g = 2 * b;
+        return (((gm[g >> 5] >> (g & 31)) & 1u) ? 0 : 1) | (((gm[(g + 1) >> 5] >> ((g + 1) & 31)) & 1u) ? 0 : 2);
+    };
+    auto next = [&](int b) {
+        while (b < pe && skip_of(b) == 3) ++b;
+        return b;
+    };
+    int bi = next(pb);
 #pragma unroll
-    for (int t = 0; t < N; ++t) acc[t] = 0.0f;
-    gu_dot<FMT, N>(a, W, row, pb, pe, xs, acc);
-#pragma unroll
-    for (int t = 0; t < N; ++t) red[warp][t][lane] = acc[t];
-    __syncthreads();
-    if (warp < nt) {
-        const int t = warp;
-        float z = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) z += red[w][t][lane];
-        if (FMT == MOE_W_NVFP4) z *= a.gu_ts[e];
-        float* hrow = a.ws.h + static_cast<int64_t>(r0 + t0 + t) * a.f;
-        if (ACT == MOE_ACT_SWIGLU) {
-            const float u = __shfl_down_sync(0xffffffffu, z, 16);
-            const float h = silu(z) * u;
-            if (lane < 16) hrow[tile * 16 + lane] = h;
-            const uint32_t nz = __ballot_sync(0xffffffffu, lane < 16 && h != 0.0f);
-            if (lane == 0 && nz) atomicOr(act_bits, 1u);
+    for (int s = 0; s < kStages; ++s) {
+        if (bi < pe) {
+            issue_panel_block<FMT>(smem_addr(ring + s * kSlotBytes), W, rows, rowA, rowB, bi, pol, skip_of(bi));
+            bi = next(bi + 1);
+        }
+        cp_async_commit();
+    }
+    between();   // block-wide: stage the activations while the first copies are in flight
+    int bc = next(pb);
+    for (int i = 0; bc < pe; ++i) {
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const int s = i % kStages;
+        panel_mma<FMT>(ring + s * kSlotBytes, xs, ld, bc, nt, skip_of(bc), acc, split, lo_off);
+        __syncwarp();   // every lane is done with the slot before it is refilled
+        if (bi < pe) {
+            issue_panel_block<FMT>(smem_addr(ring + s * kSlotBytes), W, rows, rowA, rowB, bi, pol, skip_of(bi));
+            bi = next(bi + 1);
+        }
+        cp_async_commit();
+        bc = next(bc + 1);
+    }
+}
+
+// v ~= hi + lo with both terms f16 (lo = f16(v - hi)).
+__device__ __forceinline__ void split_f16(float v0, float v1, __half2& hi, __half2& lo) {
+    hi = __floats2half2_rn(v0, v1);
+    const float2 h = __half22float2(hi);
+    lo = __floats2half2_rn(v0 - h.x, v1 - h.y);
+}
+
+// Stage the f16 activations of `nt` tokens: x rows (gate.up) or h rows (down).  fp32
+// sources also write the lo terms at + lo_off (bf16 sources are exact in one f16).
+__device__ __forceinline__ void stage_x_f16(const ExpertArgs& a, const int4& si, int t0, int nt, __half* xs,
+                                            int lo_off) {
+    const int d4 = a.d / 4;
+    for (int i = threadIdx.x; i < nt * d4; i += blockDim.x) {
+        const int t = i / d4, c = (i % d4) * 4;
+        const int64_t off = static_cast<int64_t>(slot_token(si, t0 + t, a.ws.perm, a.k)) * a.d + c;
+        float4 v;
+        if (a.xt == MOE_F32) {
+            v = *reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + off);
         } else {
-            const float h = z > 0.0f ? z * z : 0.0f;
-            hrow[tile * 32 + lane] = h;
-            const uint32_t nz = __ballot_sync(0xffffffffu, h != 0.0f);
-            if (lane == 0 && nz) atomicOr(act_bits, ((nz & 0xffffu) ? 1u : 0u) | ((nz >> 16) ? 2u : 0u));
+            const uint2 b = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.x) + off);
+            v = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xffff0000u),
+                            __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xffff0000u));
+        }
+        __half2 h01, h23, l01, l23;
+        split_f16(v.x, v.y, h01, l01);
+        split_f16(v.z, v.w, h23, l23);
+        *reinterpret_cast<__half2*>(xs + t * a.d + c) = h01;
+        *reinterpret_cast<__half2*>(xs + t * a.d + c + 2) = h23;
+        if (a.xt == MOE_F32) {
+            *reinterpret_cast<__half2*>(xs + lo_off + t * a.d + c) = l01;
+            *reinterpret_cast<__half2*>(xs + lo_off + t * a.d + c + 2) = l23;
         }
     }
 }
 
-// grid: (f/16 tiles for SwiGLU or f/32 for ReLU^2, active-slot capacity); block 256.
-// TT: the largest token tile this launch needs (1, 2, 4 or 8); smaller tiles of the same
-// launch use the narrower bodies, so a one-token launch carries no wide accumulators.
-template <int FMT, int ACT, int TT>
-__global__ void __launch_bounds__(256) gate_up_gemv_kernel(ExpertArgs a) {
-    const int slot = blockIdx.y;
-    if (slot >= *a.ws.n_active) return;
-    const int e = a.ws.act_e[slot];
-    const int r0 = a.ws.offsets[e];
-    const int cnt = a.ws.offsets[e + 1] - r0;
-    extern __shared__ __align__(16) float xs[];
-    __shared__ float red[8][8][32];
-    __shared__ uint32_t act_bits;
+__device__ __forceinline__ void stage_h_f16(const ExpertArgs& a, int r0, int t0, int nt, __half* hs, int lo_off) {
+    const int f4 = a.f / 4;
+    const float4* src = reinterpret_cast<const float4*>(a.ws.h + static_cast<int64_t>(r0 + t0) * a.f);
+    __half2* hi = reinterpret_cast<__half2*>(hs);
+    __half2* lo = reinterpret_cast<__half2*>(hs + lo_off);
+    for (int i = threadIdx.x; i < nt * f4; i += blockDim.x) {
+        const float4 v = __ldcg(src + i);
+        split_f16(v.x, v.y, hi[2 * i], lo[2 * i]);
+        split_f16(v.z, v.w, hi[2 * i + 1], lo[2 * i + 1]);
+    }
+}
+
+// Per-warp partial sums of a 32-row x 8-token tile into red[warp][blk][row][token].
+__device__ __forceinline__ void store_partials(float* red, const float acc[2][4]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    float* r = red + warp * 256;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        r[blk * 128 + g * 8 + 2 * t] = acc[blk][0];
+        r[blk * 128 + g * 8 + 2 * t + 1] = acc[blk][1];
+        r[blk * 128 + (g + 8) * 8 + 2 * t] = acc[blk][2];
+        r[blk * 128 + (g + 8) * 8 + 2 * t + 1] = acc[blk][3];
+    }
+}
+
+// ------------------------------------------------------------------------------ gate.up
+// grid: (f/16 tiles for SwiGLU: 16 gate rows and the 16 matching up rows; f/32 for ReLU^2:
+// 32 up rows;  slot capacity); block 256 = 8 warps splitting the K panels.  Tokens of the
+// slot's expert go 8 at a time through the MMA's N columns.
+template <int FMT, int ACT>
+__global__ void __launch_bounds__(256, 3) gate_up_gemv_kernel(ExpertArgs a) {
+    pdl_wait();
+    pdl_trigger();   // let the down kernel start filling its weight ring now
+    const int slot = blockIdx.y;
+    const int4 si = __ldcg(a.ws.slot_info + slot);
+    const int e = si.x, r0 = si.y, cnt = si.z;
+    if (cnt == 0) return;   // idle slot
+    const int warp = threadIdx.x >> 5;
+    extern __shared__ __align__(16) unsigned char dsm[];
+    unsigned char* ring = dsm + warp * kStages * kSlotBytes;
+    __half* xs = reinterpret_cast<__half*>(dsm + 8 * kStages * kSlotBytes);   // [tt][d]
+    __shared__ float red[8 * 256];
+    __shared__ uint32_t act_bits;
     const int tile = blockIdx.x;
-    const int row = (ACT == MOE_ACT_SWIGLU) ? (lane < 16 ? tile * 16 + lane : a.f + tile * 16 + lane - 16)
-                                            : tile * 32 + lane;
+    const int rowA = (ACT == MOE_ACT_SWIGLU) ? tile * 16 : tile * 32;
+    const int rowB = (ACT == MOE_ACT_SWIGLU) ? a.f + tile * 16 : tile * 32 + 16;
     const uint8_t* W = a.w_gu + static_cast<int64_t>(e) * a.gu_bytes;
     const int npan = (FMT == MOE_W_Q8_0) ? a.d / 32 : a.d / 64;
     const int pb = warp * npan / 8, pe = (warp + 1) * npan / 8;
-    if (threadIdx.x == 0) act_bits = 0;
+    if (threadIdx.x == 0) {
+        act_bits = 0;
+        if (a.prefetch_down) {   // this CTA's share of the expert's down matrix, into L2
+            const int64_t share = ((a.dn_bytes + gridDim.x - 1) / gridDim.x + 127) / 128 * 128;
+            const int64_t off = static_cast<int64_t>(tile) * share;
+            if (off < a.dn_bytes) {
+                const int64_t n = min(share, a.dn_bytes - off);
+                prefetch_l2(a.w_dn + static_cast<int64_t>(e) * a.dn_bytes + off, static_cast<uint32_t>(n));
+            }
+        }
+    }
+    const float ts = (FMT == MOE_W_NVFP4) ? a.gu_ts[e] : 1.0f;
     for (int t0 = 0; t0 < cnt; t0 += a.tt_gu) {
         const int nt = min(a.tt_gu, cnt - t0);
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const bool split = a.xt == MOE_F32;
+        const int lo_off = a.tt_gu * a.d;
+        stream_panels<FMT>(W, a.rows_gu, rowA, rowB, pb, pe, ring, xs, a.d, nt, nullptr, acc, split, lo_off, [&] {
+            stage_x_f16(a, si, t0, nt, xs, lo_off);
+            __syncthreads();
+        });
+        store_partials(red, acc);
         __syncthreads();
-        load_token_rows(a, r0, t0, nt, xs);
-        __syncthreads();
-        if (TT == 1 || nt == 1) gu_tile<FMT, ACT, 1>(a, W, row, pb, pe, xs, red, e, r0, t0, nt, tile, &act_bits);
-        else if (TT == 2 || nt == 2) gu_tile<FMT, ACT, (TT < 2 ? TT : 2)>(a, W, row, pb, pe, xs, red, e, r0, t0, nt, tile, &act_bits);
-        else if (TT == 4 || nt <= 4) gu_tile<FMT, ACT, (TT < 4 ? TT : 4)>(a, W, row, pb, pe, xs, red, e, r0, t0, nt, tile, &act_bits);
-        else gu_tile<FMT, ACT, TT>(a, W, row, pb, pe, xs, red, e, r0, t0, nt, tile, &act_bits);
+        for (int it = threadIdx.x; it < 16 * 8; it += blockDim.x) {
+            const int row = it >> 3, tok = it & 7;
+            if (tok >= nt) continue;
+            float zA = 0.0f, zB = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                zA += red[w * 256 + row * 8 + tok];
+                zB += red[w * 256 + 128 + row * 8 + tok];
+            }
+            zA *= ts;
+            zB *= ts;
+            float* hrow = a.ws.h + static_cast<int64_t>(r0 + t0 + tok) * a.f;
+            if (ACT == MOE_ACT_SWIGLU) {
+                const float h = silu(zA) * zB;
+                hrow[tile * 16 + row] = h;
+                if (h != 0.0f) atomicOr(&act_bits, 1u);
+            } else {
+                const float hA = zA > 0.0f ? zA * zA : 0.0f;
+                const float hB = zB > 0.0f ? zB * zB : 0.0f;
+                hrow[tile * 32 + row] = hA;
+                hrow[tile * 32 + 16 + row] = hB;
+                if (hA != 0.0f) atomicOr(&act_bits, 1u);
+                if (hB != 0.0f) atomicOr(&act_bits, 2u);
+            }
+        }
+        __syncthreads();   // red and xs are reused by the next token tile
     }
-    __syncthreads();
     if (threadIdx.x == 0 && act_bits) {
         const int g0 = (ACT == MOE_ACT_SWIGLU) ? tile : 2 * tile;
-        uint32_t bits = (ACT == MOE_ACT_SWIGLU) ? 1u : act_bits;
+        const uint32_t bits = (ACT == MOE_ACT_SWIGLU) ? 1u : act_bits;
         atomicOr(a.ws.gmask + slot * a.gwords + g0 / 32, bits << (g0 % 32));
     }
 }
 
-// ------------------------------------------------------------------------------ down, Q8_0
-// Q8_0 down matrices [d][f] in K panels of 32 neurons.  Lane = one output row; a panel
-// holds neuron groups 2b and 2b+1 and each 16-byte half is read only if its group is
-// active.  grid: (d/256, slot capacity, ksplit); block 256 (8 warps x 32 rows).
-template <int N>
-__device__ __forceinline__ void dn_q8_tile(const ExpertArgs& a, const uint8_t* W, int row, int pb, int pe,
-                                           const float* hs, const uint32_t* gm, float acc[N]) {
-    const int d = a.d, f = a.f;
-    const int64_t pbytes = static_cast<int64_t>(d) * 34;
-    constexpr int U = 4;
-    for (int b = pb; b < pe; b += U) {
-        uint4 q0[U], q1[U];
-        float sc[U];
-        bool a0[U], a1[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            a0[u] = a1[u] = false;
-            if (b + u < pe) {
-                const int g = 2 * (b + u);
-                a0[u] = (gm[g >> 5] >> (g & 31)) & 1u;
-                a1[u] = (gm[(g + 1) >> 5] >> ((g + 1) & 31)) & 1u;
-                const uint8_t* P = W + (b + u) * pbytes;
-                q0[u] = a0[u] ? ldg_stream16(P + row * 32) : make_uint4(0, 0, 0, 0);
-                q1[u] = a1[u] ? ldg_stream16(P + row * 32 + 16) : make_uint4(0, 0, 0, 0);
-                sc[u] = (a0[u] || a1[u]) ? ldg_half(P + d * 32 + row * 2) : 0.0f;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (b + u < pe && (a0[u] || a1[u])) {
-                float part[N];
-#pragma unroll
-                for (int t = 0; t < N; ++t) part[t] = 0.0f;
-                const float* hb = hs + (b + u) * 32;
-#pragma unroll
-                for (int wi = 0; wi < 8; ++wi) {
-                    if ((wi < 4 && !a0[u]) || (wi >= 4 && !a1[u])) continue;
-                    const uint32_t word = word_of(q0[u], q1[u], wi);
-                    float4 hv[N];
-#pragma unroll
-                    for (int t = 0; t < N; ++t) hv[t] = *reinterpret_cast<const float4*>(hb + t * f + wi * 4);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float v = s8_to_f32(word, j);
-#pragma unroll
-                        for (int t = 0; t < N; ++t) part[t] = fmaf(v, f4get(hv[t], j), part[t]);
-                    }
-                }
-#pragma unroll
-                for (int t = 0; t < N; ++t) acc[t] = fmaf(sc[u], part[t], acc[t]);
-            }
-        }
+// ------------------------------------------------------------------------------ fused combine
+// pos / w of every pair in shared memory (the down kernels load them in their prologue).
+constexpr int kMaxFusedPairs = 256;
+
+__device__ __forceinline__ void preload_pairs(const ExpertArgs& a, int* spos, float* sw) {
+    for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
+        spos[p] = __ldcg(a.ws.pos + p);
+        sw[p] = __ldcg(a.ws.w + p);
     }
 }
 
-__device__ __forceinline__ void load_h_rows(const ExpertArgs& a, int r0, int t0, int nt, float* hs) {
-    const int f4 = a.f / 4;
-    const float4* src = reinterpret_cast<const float4*>(a.ws.h + static_cast<int64_t>(r0 + t0) * a.f);
-    for (int i = threadIdx.x; i < nt * f4; i += blockDim.x) reinterpret_cast<float4*>(hs)[i] = src[i];
+// Every CTA of the down grid (one per slot, idle slots included) arrives once per row tile;
+// the last one of row tile [row0, row0+nrows) combines those rows for every token:
+// out[t][r] = sum_{j<k} w[t][j] * y[pos(t,j)][r], in slot order.
+__device__ __forceinline__ void combine_rows_if_last(const ExpertArgs& a, int tile, int row0, int nrows,
+                                                     const int* spos, const float* sw) {
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(a.ws.row_ctr + tile, 1) == static_cast<int>(gridDim.y) - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int k = a.k;
+    for (int it = threadIdx.x; it < a.T * nrows; it += blockDim.x) {
+        const int t = it / nrows, r = row0 + it % nrows;
+        float yj[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j)     // every load of the item in flight at once
+            if (j < k) yj[j] = __ldcg(a.ws.y + static_cast<int64_t>(spos[t * k + j]) * a.d + r);
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j)
+            if (j < k) acc = fmaf(sw[t * k + j], yj[j], acc);
+        a.out[static_cast<int64_t>(t) * a.d + r] = acc;
+    }
+    if (threadIdx.x == 0) a.ws.row_ctr[tile] = 0;
 }
 
-template <int TT>
-__global__ void __launch_bounds__(256) down_q8_gemv_kernel(ExpertArgs a) {
+// ------------------------------------------------------------------------------ down, Q8_0
+// Q8_0 down matrices [d][f] in K panels of 32 neurons.  A CTA = 32 output rows (two MMA
+// blocks of 16); its 4 warps split the panels.  A panel holds neuron groups 2b and 2b+1;
+// the 16 columns of an inactive group are neither copied nor used, and panels whose two
+// groups are inactive are skipped.  grid: (d/32, slot capacity).
+constexpr int kDnWarps = 4;
+
+__global__ void __launch_bounds__(kDnWarps * 32, 6) down_q8_gemv_kernel(ExpertArgs a) {
     const int slot = blockIdx.y;
-    if (slot >= *a.ws.n_active) return;
-    const int e = a.ws.act_e[slot];
-    const int r0 = a.ws.offsets[e];
-    const int cnt = a.ws.offsets[e + 1] - r0;
-    extern __shared__ __align__(16) float hs[];
+    const int warp = threadIdx.x >> 5;
+    extern __shared__ __align__(16) unsigned char dsm[];
+    unsigned char* ring = dsm + warp * kStages * kSlotBytes;
+    __half* hs = reinterpret_cast<__half*>(dsm + kDnWarps * kStages * kSlotBytes);   // [tt][f] hi, then lo
     __shared__ uint32_t gm[64];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 256 + warp * 32 + lane;
+    __shared__ float red[kDnWarps * 256];
+    __shared__ int spos[kMaxFusedPairs];
+    __shared__ float sw[kMaxFusedPairs];
+    // The slot records come from the routing kernel, which completed before the gate.up grid
+    // this launch depends on could start: they and the weights may be read before waiting,
+    // so the first panels stream in while gate.up is still running.
+    const int4 si = __ldcg(a.ws.slot_info + slot);
+    const int e = si.x, r0 = si.y, cnt = si.z;
+    const int rt = blockIdx.x;
     const int npan = a.f / 32;
-    const int z = blockIdx.z;
-    const int pb = z * npan / a.ksplit, pe = (z + 1) * npan / a.ksplit;
+    const int pb = warp * npan / kDnWarps, pe = (warp + 1) * npan / kDnWarps;
     const uint8_t* W = a.w_dn + static_cast<int64_t>(e) * a.dn_bytes;
-    for (int i = threadIdx.x; i < a.gwords; i += blockDim.x) gm[i] = a.ws.gmask[slot * a.gwords + i];
-    float* ybase = a.ws.y + static_cast<int64_t>(z) * a.P * a.d;
+    const uint64_t pol = l2_evict_first_policy();
+    const int rowA = rt * 32, rowB = rt * 32 + 16;
+    const int npre = cnt > 0 ? min(kStages, pe - pb) : 0;
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+        if (s < npre) issue_panel_block<MOE_W_Q8_0>(smem_addr(ring + s * kSlotBytes), W, a.d, rowA, rowB, pb + s, pol, 0);
+        cp_async_commit();
+    }
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i < a.gwords; i += blockDim.x) gm[i] = __ldcg(a.ws.gmask + slot * a.gwords + i);
+    if (a.fuse_combine) preload_pairs(a, spos, sw);
+    __syncthreads();
+    // halves of inactive neuron groups: not copied (after the first panels) and not used
+    auto skip_of = [&](int b) -> int {
+        const int g = 2 * b;
+        return (((gm[g >> 5] >> (g & 31)) & 1u) ? 0 : 1) | (((gm[(g + 1) >> 5] >> ((g + 1) & 31)) & 1u) ? 0 : 2);
+    };
+    const int lo_off = a.tt_dn * a.f;
     for (int t0 = 0; t0 < cnt; t0 += a.tt_dn) {
         const int nt = min(a.tt_dn, cnt - t0);
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        if (t0 > 0) {   // later token tiles refill the ring
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) {
+                if (s < npre)
+                    issue_panel_block<MOE_W_Q8_0>(smem_addr(ring + s * kSlotBytes), W, a.d, rowA, rowB, pb + s, pol,
+                                                  skip_of(pb + s));
+                cp_async_commit();
+            }
+        }
+        stage_h_f16(a, r0, t0, nt, hs, lo_off);
         __syncthreads();
-        load_h_rows(a, r0, t0, nt, hs);
+        for (int i = 0; pb + i < pe; ++i) {
+            cp_async_wait<kStages - 1>();
+            __syncwarp();
+            const int s = i % kStages;
+            panel_mma<MOE_W_Q8_0>(ring + s * kSlotBytes, hs, a.f, pb + i, nt, skip_of(pb + i), acc, true, lo_off);
+            __syncwarp();
+            const int bn = pb + i + kStages;
+            if (bn < pe)
+                issue_panel_block<MOE_W_Q8_0>(smem_addr(ring + s * kSlotBytes), W, a.d, rowA, rowB, bn, pol, skip_of(bn));
+            cp_async_commit();
+        }
+        store_partials(red, acc);
         __syncthreads();
-#define MOE_DN_Q8_CASE(NN)                                                              \
-    {                                                                                   \
-        float acc[NN];                                                                  \
-        _Pragma("unroll") for (int t = 0; t < NN; ++t) acc[t] = 0.0f;                   \
-        dn_q8_tile<NN>(a, W, row, pb, pe, hs, gm, acc);                                 \
-        _Pragma("unroll") for (int t = 0; t < NN; ++t) if (t < nt)                      \
-            ybase[static_cast<int64_t>(r0 + t0 + t) * a.d + row] = acc[t];              \
+        for (int it = threadIdx.x; it < 32 * 8; it += blockDim.x) {
+            const int blk = it >> 7, row = (it >> 3) & 15, tok = it & 7;
+            if (tok >= nt) continue;
+            float yv = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kDnWarps; ++w) yv += red[w * 256 + blk * 128 + row * 8 + tok];
+            a.ws.y[static_cast<int64_t>(r0 + t0 + tok) * a.d + rt * 32 + blk * 16 + row] = yv;
+        }
+        __syncthreads();
     }
-        if (TT == 1 || nt == 1) MOE_DN_Q8_CASE(1)
-        else if (TT == 2 || nt == 2) MOE_DN_Q8_CASE((TT < 2 ? TT : 2))
-        else if (TT == 4 || nt <= 4) MOE_DN_Q8_CASE((TT < 4 ? TT : 4))
-        else MOE_DN_Q8_CASE(TT)
-#undef MOE_DN_Q8_CASE
-    }
+    cp_async_wait<0>();
+    if (a.fuse_combine) combine_rows_if_last(a, rt, rt * 32, 32, spos, sw);
 }
 
 // ------------------------------------------------------------------------------ down, NVFP4
 // NVFP4 down matrices in the neuron layout: per group of 16 neurons, each neuron's codes
-// for all d rows (d/2 bytes), then the d scale bytes.  A warp covers 256 rows: lane l
-// rows 256*rt + 8l .. +7 (4 code bytes per neuron, 8 scale bytes).  Inactive groups are
-// not read at all.  grid: (ceil(d/1024), slot capacity, ksplit); block 128 (4 row tiles).
+// for all d rows (d/2 bytes), then the d scale bytes.  A CTA covers 256 rows (lane l:
+// rows 8l .. 8l+7, 4 code bytes per neuron, 8 scale bytes); its 8 warps split the groups
+// and meet in shared memory.  Inactive groups are not read at all.  grid: (d/256, slots).
+constexpr int kMaxGroupsInFlight = 2;
+
 template <int N>
 __device__ __forceinline__ void dn_nv_tile(const ExpertArgs& a, const uint8_t* W, int rt, int gb, int ge,
-                                           const float* hs, const uint32_t* gm, float acc[N][8]) {
+                                           const uint32_t* gm, float* hs, int r0, int t0, int nt,
+                                           float acc[N][8]) {
     const int d = a.d, f = a.f;
     const int lane = threadIdx.x & 31;
     const int64_t rec = 16 * (d / 2) + d;
-    for (int g = gb; g < ge; ++g) {
-        if (!((gm[g >> 5] >> (g & 31)) & 1u)) continue;
-        const uint8_t* base = W + g * rec;
-        uint32_t codes[16];
+    uint32_t codes[kMaxGroupsInFlight][16];
+    uint2 sc[kMaxGroupsInFlight];
+    int gid[kMaxGroupsInFlight];
+    int g = gb;
+    // gather the next batch of active groups and issue their loads
+    auto issue = [&]() {
+        int n = 0;
+        while (g < ge && n < kMaxGroupsInFlight) {
+            if ((gm[g >> 5] >> (g & 31)) & 1u) {
+                gid[n] = g;
+                ++n;
+            }
+            ++g;
+        }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) codes[j] = ldg_stream4(base + j * (d / 2) + rt * 128 + lane * 4);
-        const uint2 sc = ldg_stream8(base + 16 * (d / 2) + rt * 256 + lane * 8);
-        float part[N][8];
+        for (int u = 0; u < kMaxGroupsInFlight; ++u) {
+            if (u < n) {
+                const uint8_t* base = W + gid[u] * rec;
 #pragma unroll
-        for (int t = 0; t < N; ++t)
+                for (int j = 0; j < 16; ++j) codes[u][j] = ldg_stream4(base + j * (d / 2) + rt * 128 + lane * 4);
+                sc[u] = ldg_stream8(base + 16 * (d / 2) + rt * 256 + lane * 8);
+            }
+        }
+        return n;
+    };
+    int n = issue();
+    load_h_rows(a, r0, t0, nt, hs);
+    __syncthreads();
+    while (n > 0) {
 #pragma unroll
-            for (int r = 0; r < 8; ++r) part[t][r] = 0.0f;
+        for (int u = 0; u < kMaxGroupsInFlight; ++u) {
+            if (u < n) {
+                float part[N][8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            float hv[N];
+                for (int t = 0; t < N; ++t)
 #pragma unroll
-            for (int t = 0; t < N; ++t) hv[t] = hs[t * f + 16 * g + j];
+                    for (int r = 0; r < 8; ++r) part[t][r] = 0.0f;
 #pragma unroll
-            for (int by = 0; by < 4; ++by) {
-                const float2 v = e2m1x2_to_f32x2((codes[j] >> (8 * by)) & 0xffu);   // rows 2by, 2by+1
+                for (int j = 0; j < 16; ++j) {
+                    float hv[N];
 #pragma unroll
-                for (int t = 0; t < N; ++t) {
-                    part[t][2 * by] = fmaf(v.x, hv[t], part[t][2 * by]);
-                    part[t][2 * by + 1] = fmaf(v.y, hv[t], part[t][2 * by + 1]);
+                    for (int t = 0; t < N; ++t) hv[t] = hs[t * f + 16 * gid[u] + j];
+#pragma unroll
+                    for (int by = 0; by < 4; ++by) {
+                        const float2 v = e2m1x2_to_f32x2((codes[u][j] >> (8 * by)) & 0xffu);   // rows 2by, 2by+1
+#pragma unroll
+                        for (int t = 0; t < N; ++t) {
+                            part[t][2 * by] = fmaf(v.x, hv[t], part[t][2 * by]);
+                            part[t][2 * by + 1] = fmaf(v.y, hv[t], part[t][2 * by + 1]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const float sb = e4m3_to_f32(((r < 4 ? sc[u].x : sc[u].y) >> (8 * (r & 3))) & 0xffu);
+#pragma unroll
+                    for (int t = 0; t < N; ++t) acc[t][r] = fmaf(sb, part[t][r], acc[t][r]);
                 }
             }
         }
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const float sb = e4m3_to_f32(((r < 4 ? sc.x : sc.y) >> (8 * (r & 3))) & 0xffu);
-#pragma unroll
-            for (int t = 0; t < N; ++t) acc[t][r] = fmaf(sb, part[t][r], acc[t][r]);
-        }
+        n = issue();
     }
 }
 
 template <int TT>
-__global__ void __launch_bounds__(128) down_nv_gemv_kernel(ExpertArgs a) {
+__global__ void __launch_bounds__(256) down_nv_gemv_kernel(ExpertArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const int slot = blockIdx.y;
-    if (slot >= *a.ws.n_active) return;
-    const int e = a.ws.act_e[slot];
-    const int r0 = a.ws.offsets[e];
-    const int cnt = a.ws.offsets[e + 1] - r0;
-    extern __shared__ __align__(16) float hs[];
+    extern __shared__ __align__(16) float dyn[];
+    float* hs = dyn;                                   // [TT][f]
+    float* red = dyn + static_cast<size_t>(TT) * a.f;  // [8 warps][TT][256 rows]
     __shared__ uint32_t gm[64];
+    __shared__ int spos[kMaxFusedPairs];
+    __shared__ float sw[kMaxFusedPairs];
+    const int4 si = __ldcg(a.ws.slot_info + slot);
+    for (int i = threadIdx.x; i < a.gwords; i += blockDim.x) gm[i] = __ldcg(a.ws.gmask + slot * a.gwords + i);
+    if (a.fuse_combine) preload_pairs(a, spos, sw);
+    __syncthreads();
+    const int e = si.x, r0 = si.y, cnt = si.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rt = blockIdx.x * 4 + warp;            // row tile of this warp
-    const bool has_rows = rt < a.d / 256;
+    const int rt = blockIdx.x;
     const int ng = a.f / 16;
-    const int z = blockIdx.z;
-    const int gb = z * ng / a.ksplit, ge = (z + 1) * ng / a.ksplit;
+    const int gb = warp * ng / 8, ge = (warp + 1) * ng / 8;
     const uint8_t* W = a.w_dn + static_cast<int64_t>(e) * a.dn_bytes;
-    const float ts = a.dn_ts[e];
-    for (int i = threadIdx.x; i < a.gwords; i += blockDim.x) gm[i] = a.ws.gmask[slot * a.gwords + i];
-    float* ybase = a.ws.y + static_cast<int64_t>(z) * a.P * a.d;
-    const int row0 = rt * 256 + lane * 8;
-    for (int t0 = 0; t0 < cnt; t0 += a.tt_dn) {
-        const int nt = min(a.tt_dn, cnt - t0);
-        __syncthreads();
-        load_h_rows(a, r0, t0, nt, hs);
-        __syncthreads();
-        if (!has_rows) continue;
-#define MOE_DN_NV_CASE(NN)                                                                      \
-    {                                                                                           \
-        float acc[NN][8];                                                                       \
+    const float ts = cnt > 0 ? a.dn_ts[e] : 0.0f;
+    for (int t0 = 0; t0 < cnt; t0 += TT) {
+        const int nt = min(TT, cnt - t0);
+#define MOE_DN_NV_CASE(NN)                                                                          \
+    {                                                                                               \
+        float acc[NN][8];                                                                           \
         _Pragma("unroll") for (int t = 0; t < NN; ++t) _Pragma("unroll") for (int r = 0; r < 8; ++r) \
-            acc[t][r] = 0.0f;                                                                   \
-        dn_nv_tile<NN>(a, W, rt, gb, ge, hs, gm, acc);                                          \
-        _Pragma("unroll") for (int t = 0; t < NN; ++t) if (t < nt) {                            \
-            float* yr = ybase + static_cast<int64_t>(r0 + t0 + t) * a.d + row0;                 \
-            *reinterpret_cast<float4*>(yr) =                                                    \
-                make_float4(acc[t][0] * ts, acc[t][1] * ts, acc[t][2] * ts, acc[t][3] * ts);    \
-            *reinterpret_cast<float4*>(yr + 4) =                                                \
-                make_float4(acc[t][4] * ts, acc[t][5] * ts, acc[t][6] * ts, acc[t][7] * ts);    \
-        }                                                                                       \
+            acc[t][r] = 0.0f;                                                                       \
+        dn_nv_tile<NN>(a, W, rt, gb, ge, gm, hs, r0, t0, nt, acc);                                  \
+        _Pragma("unroll") for (int t = 0; t < NN; ++t) {                                            \
+            float* rr = red + (warp * TT + t) * 256 + lane * 8;                                     \
+            *reinterpret_cast<float4*>(rr) = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]); \
+            *reinterpret_cast<float4*>(rr + 4) = make_float4(acc[t][4], acc[t][5], acc[t][6], acc[t][7]); \
+        }                                                                                           \
     }
         if (TT == 1 || nt == 1) MOE_DN_NV_CASE(1)
         else if (TT == 2 || nt == 2) MOE_DN_NV_CASE((TT < 2 ? TT : 2))
         else MOE_DN_NV_CASE((TT < 4 ? TT : 4))
 #undef MOE_DN_NV_CASE
+        __syncthreads();
+        for (int it = threadIdx.x; it < nt * 256; it += blockDim.x) {
+            const int t = it / 256, r = it % 256;
+            float yv = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) yv += red[(w * TT + t) * 256 + r];
+            a.ws.y[static_cast<int64_t>(r0 + t0 + t) * a.d + rt * 256 + r] = yv * ts;
+        }
+        __syncthreads();
     }
+    if (a.fuse_combine) combine_rows_if_last(a, rt, rt * 256, 256, spos, sw);
 }
 
 // ------------------------------------------------------------------------------ combine
-// out[t] = sum_{j<k} w[t][j] * sum_{z<ksplit} y[z][pos(t,j)], both sums in index order.
+// out[t] = sum_{j<k} w[t][j] * y[pos(t,j)], in slot order.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pos,
-                                                       const float* __restrict__ y, int k, int d, int ksplit,
-                                                       int64_t zstride, float* __restrict__ out) {
+                                                       const float* __restrict__ y, int k, int d,
+                                                       float* __restrict__ out) {
+    pdl_wait();
     const int t = blockIdx.y;
     const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (c >= d) return;
@@ -457,90 +753,96 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     for (int j = 0; j < k; ++j) {
         const int r = pos[t * k + j];
         const float wt = w[t * k + j];
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int z = 0; z < ksplit; ++z) {
-            const float4 v = *reinterpret_cast<const float4*>(y + z * zstride + static_cast<int64_t>(r) * d + c);
-            s.x += v.x, s.y += v.y, s.z += v.z, s.w += v.w;
-        }
-        acc.x = fmaf(wt, s.x, acc.x);
-        acc.y = fmaf(wt, s.y, acc.y);
-        acc.z = fmaf(wt, s.z, acc.z);
-        acc.w = fmaf(wt, s.w, acc.w);
+        const float4 v = *reinterpret_cast<const float4*>(y + static_cast<int64_t>(r) * d + c);
+        acc.x = fmaf(wt, v.x, acc.x);
+        acc.y = fmaf(wt, v.y, acc.y);
+        acc.z = fmaf(wt, v.z, acc.z);
+        acc.w = fmaf(wt, v.w, acc.w);
     }
     *reinterpret_cast<float4*>(out + static_cast<int64_t>(t) * d + c) = acc;
 }
 
 // ------------------------------------------------------------------------------ rmsnorm glue
+// One CTA per token: every thread loads its elements first, then a fixed-order reduction.
+constexpr int kNormMaxPerThread = 32;
+
 __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restrict__ x, int d, float eps,
                                                             uint16_t* __restrict__ xo) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     const float* xr = x + static_cast<int64_t>(t) * d;
+    float v[kNormMaxPerThread];
     float ss = 0.0f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+    for (int base = 0; base < d; base += 256 * kNormMaxPerThread) {
+#pragma unroll
+        for (int u = 0; u < kNormMaxPerThread; ++u) {
+            const int i = base + u * 256 + threadIdx.x;
+            v[u] = (i < d) ? xr[i] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < kNormMaxPerThread; ++u) ss = fmaf(v[u], v[u], ss);
+    }
     ss = warp_sum(ss);
-    __shared__ float ws[8];
-    if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = ss;
+    __shared__ float wsum[8];
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
     __syncthreads();
     float tot = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) tot += ws[i];
+    for (int i = 0; i < 8; ++i) tot += wsum[i];
     const float inv = rsqrtf(tot / static_cast<float>(d) + eps);
-    for (int i = threadIdx.x; i < d; i += blockDim.x)
-        xo[static_cast<int64_t>(t) * d + i] = __bfloat16_as_ushort(__float2bfloat16_rn(xr[i] * inv));
+    if (d <= 256 * kNormMaxPerThread) {
+#pragma unroll
+        for (int u = 0; u < kNormMaxPerThread; ++u) {
+            const int i = u * 256 + threadIdx.x;
+            if (i < d) xo[static_cast<int64_t>(t) * d + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v[u] * inv));
+        }
+    } else {
+        for (int i = threadIdx.x; i < d; i += 256)
+            xo[static_cast<int64_t>(t) * d + i] = __bfloat16_as_ushort(__float2bfloat16_rn(xr[i] * inv));
+    }
 }
 
 // ------------------------------------------------------------------------------ launchers
+// Raise the kernel's dynamic shared-memory limit and ask for the largest shared-memory
+// carveout, so that as many CTAs fit per SM as registers allow.
 template <typename K>
 static cudaError_t allow_smem(K kernel, int bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
-
-template <int FMT, int ACT, int TT>
-static cudaError_t gu_launch(const ExpertArgs& a, dim3 grid, size_t smem, cudaStream_t s, bool configure) {
-    if (configure) return allow_smem(gate_up_gemv_kernel<FMT, ACT, TT>, 200 * 1024);
-    gate_up_gemv_kernel<FMT, ACT, TT><<<grid, 256, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }
 
 template <int FMT, int ACT>
-static cudaError_t gu_dispatch_tt(const ExpertArgs& a, dim3 grid, size_t smem, cudaStream_t s, bool configure) {
-    switch (a.tt_gu) {
-        case 1: return gu_launch<FMT, ACT, 1>(a, grid, smem, s, configure);
-        case 2: return gu_launch<FMT, ACT, 2>(a, grid, smem, s, configure);
-        case 4: return gu_launch<FMT, ACT, 4>(a, grid, smem, s, configure);
-        default: return gu_launch<FMT, ACT, 8>(a, grid, smem, s, configure);
-    }
+static cudaError_t gu_launch(const ExpertArgs& a, dim3 grid, size_t smem, cudaStream_t s, bool configure) {
+    if (configure) return allow_smem(gate_up_gemv_kernel<FMT, ACT>, 200 * 1024);
+    return launch_pdl(gate_up_gemv_kernel<FMT, ACT>, grid, dim3(256), smem, s, a);
 }
 
 static cudaError_t gu_dispatch(const ExpertArgs& a, int wfmt, int act, dim3 grid, size_t smem, cudaStream_t s,
                                bool configure) {
-    if (wfmt == MOE_W_Q8_0 && act == MOE_ACT_SWIGLU)
-        return gu_dispatch_tt<MOE_W_Q8_0, MOE_ACT_SWIGLU>(a, grid, smem, s, configure);
-    if (wfmt == MOE_W_Q8_0) return gu_dispatch_tt<MOE_W_Q8_0, MOE_ACT_RELU2>(a, grid, smem, s, configure);
-    if (act == MOE_ACT_SWIGLU) return gu_dispatch_tt<MOE_W_NVFP4, MOE_ACT_SWIGLU>(a, grid, smem, s, configure);
-    return gu_dispatch_tt<MOE_W_NVFP4, MOE_ACT_RELU2>(a, grid, smem, s, configure);
+    if (wfmt == MOE_W_Q8_0 && act == MOE_ACT_SWIGLU) return gu_launch<MOE_W_Q8_0, MOE_ACT_SWIGLU>(a, grid, smem, s, configure);
+    if (wfmt == MOE_W_Q8_0) return gu_launch<MOE_W_Q8_0, MOE_ACT_RELU2>(a, grid, smem, s, configure);
+    if (act == MOE_ACT_SWIGLU) return gu_launch<MOE_W_NVFP4, MOE_ACT_SWIGLU>(a, grid, smem, s, configure);
+    return gu_launch<MOE_W_NVFP4, MOE_ACT_RELU2>(a, grid, smem, s, configure);
 }
 
 template <int TT>
-static cudaError_t dn_launch(const ExpertArgs& a, int wfmt, int slot_cap, size_t smem, cudaStream_t s,
-                             bool configure) {
-    if (wfmt == MOE_W_Q8_0) {
-        if (configure) return allow_smem(down_q8_gemv_kernel<TT>, 200 * 1024);
-        down_q8_gemv_kernel<TT><<<dim3(a.d / 256, slot_cap, a.ksplit), 256, smem, s>>>(a);
-    } else {
-        if (configure) return allow_smem(down_nv_gemv_kernel<(TT < 4 ? TT : 4)>, 200 * 1024);
-        down_nv_gemv_kernel<(TT < 4 ? TT : 4)><<<dim3((a.d / 256 + 3) / 4, slot_cap, a.ksplit), 128, smem, s>>>(a);
-    }
-    return cudaGetLastError();
+static cudaError_t dn_nv_launch(const ExpertArgs& a, int slot_cap, size_t smem, cudaStream_t s, bool configure) {
+    if (configure) return allow_smem(down_nv_gemv_kernel<TT>, 200 * 1024);
+    return launch_pdl(down_nv_gemv_kernel<TT>, dim3(a.d / 256, slot_cap), dim3(256), smem, s, a);
 }
 
 static cudaError_t dn_dispatch(const ExpertArgs& a, int wfmt, int slot_cap, size_t smem, cudaStream_t s,
                                bool configure) {
+    if (wfmt == MOE_W_Q8_0) {
+        if (configure) return allow_smem(down_q8_gemv_kernel, 200 * 1024);
+        return launch_pdl(down_q8_gemv_kernel, dim3(a.d / 32, slot_cap), dim3(kDnWarps * 32), smem, s, a);
+    }
     switch (a.tt_dn) {
-        case 1: return dn_launch<1>(a, wfmt, slot_cap, smem, s, configure);
-        case 2: return dn_launch<2>(a, wfmt, slot_cap, smem, s, configure);
-        case 4: return dn_launch<4>(a, wfmt, slot_cap, smem, s, configure);
-        default: return dn_launch<8>(a, wfmt, slot_cap, smem, s, configure);
+        case 1: return dn_nv_launch<1>(a, slot_cap, smem, s, configure);
+        case 2: return dn_nv_launch<2>(a, slot_cap, smem, s, configure);
+        default: return dn_nv_launch<4>(a, slot_cap, smem, s, configure);
     }
 }
 
@@ -550,14 +852,15 @@ cudaError_t configure_gemv_kernels() {
     ExpertArgs a{};
     const int wf[2] = {MOE_W_Q8_0, MOE_W_NVFP4};
     const int ac[2] = {MOE_ACT_SWIGLU, MOE_ACT_RELU2};
-    const int tts[4] = {1, 2, 4, 8};
+    for (int w : wf)
+        for (int c : ac) {
+            cudaError_t e = gu_dispatch(a, w, c, dim3(1), 0, nullptr, true);
+            if (e != cudaSuccess) return e;
+        }
+    const int tts[3] = {1, 2, 4};
     for (int tt : tts) {
-        a.tt_gu = a.tt_dn = tt;
+        a.tt_dn = tt;
         for (int w : wf) {
-            for (int c : ac) {
-                cudaError_t e = gu_dispatch(a, w, c, dim3(1), 0, nullptr, true);
-                if (e != cudaSuccess) return e;
-            }
             cudaError_t e = dn_dispatch(a, w, 1, 0, nullptr, true);
             if (e != cudaSuccess) return e;
         }
@@ -567,26 +870,33 @@ cudaError_t configure_gemv_kernels() {
 
 cudaError_t launch_gate_up_gemv(const ExpertArgs& a, int wfmt, int act, int slot_cap, cudaStream_t s) {
     const int tiles = (act == MOE_ACT_SWIGLU) ? a.f / 16 : a.f / 32;
-    const size_t smem = static_cast<size_t>(a.tt_gu) * a.d * sizeof(float);
+    const size_t smem = static_cast<size_t>(8) * kStages * kSlotBytes +
+                        static_cast<size_t>(a.tt_gu) * a.d * 2 * (a.xt == MOE_F32 ? 2 : 1);
     return gu_dispatch(a, wfmt, act, dim3(tiles, slot_cap), smem, s, false);
 }
 
+size_t down_gemv_smem(int wfmt, int tt_dn, int f) {
+    if (wfmt == MOE_W_NVFP4) {
+        const int t4 = tt_dn < 4 ? tt_dn : 4;
+        return static_cast<size_t>(t4) * f * sizeof(float) + static_cast<size_t>(8) * t4 * 256 * sizeof(float);
+    }
+    return static_cast<size_t>(kDnWarps) * kStages * kSlotBytes + static_cast<size_t>(tt_dn) * f * 2 * 2;
+}
+
 cudaError_t launch_down_gemv(const ExpertArgs& a, int wfmt, int slot_cap, cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(a.tt_dn) * a.f * sizeof(float);
-    return dn_dispatch(a, wfmt, slot_cap, smem, s, false);
+    return dn_dispatch(a, wfmt, slot_cap, down_gemv_smem(wfmt, a.tt_dn, a.f), s, false);
 }
 
 cudaError_t launch_combine(const float* w, const int32_t* pos, const float* y, int64_t T, int k, int64_t d,
-                           int ksplit, int64_t zstride, float* out, cudaStream_t s) {
+                           float* out, cudaStream_t s) {
     const int64_t cols4 = d / 4;
     const dim3 grid(static_cast<unsigned>((cols4 + 255) / 256), static_cast<unsigned>(T));
-    combine_kernel<<<grid, 256, 0, s>>>(w, pos, y, k, (int)d, ksplit, zstride, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(256), 0, s, w, pos, y, k, static_cast<int>(d), out);
 }
 
 cudaError_t launch_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uint16_t* xo, cudaStream_t s) {
-    rmsnorm_bf16_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(x, (int)d, eps, xo);
-    return cudaGetLastError();
+    return launch_pdl(rmsnorm_bf16_kernel, dim3(static_cast<unsigned>(T)), dim3(256), 0, s, x, static_cast<int>(d),
+                      eps, xo);
 }
 
 }  // namespace moe

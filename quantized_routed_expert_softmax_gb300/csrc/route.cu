@@ -20,6 +20,7 @@ template <int TT>
 __global__ void __launch_bounds__(256) router_logits_kernel(const void* __restrict__ x, int xt,
                                                              const float* __restrict__ W, int T, int d, int E,
                                                              float* __restrict__ logits) {
+    pdl_wait();
     const int l = threadIdx.x;
     const int e0 = blockIdx.x * 4;
     const int t0 = blockIdx.y * TT;
@@ -72,28 +73,25 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const void* __restri
 cudaError_t launch_router_logits(const void* x, int xt, const float* W, int64_t T, int64_t d, int64_t E,
                                  float* logits, cudaStream_t s) {
     const dim3 block(256);
-    if (T <= 1) {
-        router_logits_kernel<1><<<dim3(E / 4, T), block, 0, s>>>(x, xt, W, (int)T, (int)d, (int)E, logits);
-    } else if (T <= 2) {
-        router_logits_kernel<2><<<dim3(E / 4, 1), block, 0, s>>>(x, xt, W, (int)T, (int)d, (int)E, logits);
-    } else if (T <= 4) {
-        router_logits_kernel<4><<<dim3(E / 4, 1), block, 0, s>>>(x, xt, W, (int)T, (int)d, (int)E, logits);
-    } else {
-        router_logits_kernel<8><<<dim3(E / 4, (unsigned)((T + 7) / 8)), block, 0, s>>>(x, xt, W, (int)T, (int)d,
-                                                                                        (int)E, logits);
-    }
-    return cudaGetLastError();
+    // (the generic router is also launched with PDL through the helper below)
+    const int Ti = (int)T, di = (int)d, Ei = (int)E;
+    if (T <= 1) return launch_pdl(router_logits_kernel<1>, dim3(E / 4, 1), block, 0, s, x, xt, W, Ti, di, Ei, logits);
+    if (T <= 2) return launch_pdl(router_logits_kernel<2>, dim3(E / 4, 1), block, 0, s, x, xt, W, Ti, di, Ei, logits);
+    if (T <= 4) return launch_pdl(router_logits_kernel<4>, dim3(E / 4, 1), block, 0, s, x, xt, W, Ti, di, Ei, logits);
+    return launch_pdl(router_logits_kernel<8>, dim3(E / 4, (unsigned)((T + 7) / 8)), block, 0, s, x, xt, W, Ti, di, Ei,
+                      logits);
 }
 
 // ----------------------------------------------------------------------------- top-k
 // Warp-wide selection of the best remaining (value, index): larger value, lower index on
 // equal values.  Every lane ends with the same winner.
+template <int NM>   // E <= 32 * NM
 __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ lt, int E, int k, int lane,
                                                   int32_t* my_e, float* my_w) {
-    float v[kMaxE / 32];
+    float v[NM];
     uint32_t avail = 0;
 #pragma unroll
-    for (int m = 0; m < kMaxE / 32; ++m) {
+    for (int m = 0; m < NM; ++m) {
         const int e = lane + 32 * m;
         v[m] = (e < E) ? lt[e] : 0.0f;
         if (e < E) avail |= 1u << m;
@@ -104,7 +102,7 @@ __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ lt, 
         float bv = 0.0f;
         int be = 0x7fffffff;
 #pragma unroll
-        for (int m = 0; m < kMaxE / 32; ++m) {
+        for (int m = 0; m < NM; ++m) {
             if ((avail >> m) & 1u) {
                 const int e = lane + 32 * m;
                 if (be == 0x7fffffff || v[m] > bv || (v[m] == bv && e < be)) {
@@ -136,14 +134,26 @@ __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ lt, 
     *my_w = (lane < k) ? ex / sum : 0.0f;
 }
 
+// Calls f<NM>() with the smallest chunk count NM in {1, 4, 16, 32} that covers E.
+template <typename F>
+__device__ __forceinline__ void with_chunks(int E, F&& f) {
+    if (E <= 32) f(std::integral_constant<int, 1>());
+    else if (E <= 128) f(std::integral_constant<int, 4>());
+    else if (E <= 512) f(std::integral_constant<int, 16>());
+    else f(std::integral_constant<int, 32>());
+}
+
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                             int32_t* __restrict__ idx, float* __restrict__ w) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
     int32_t e;
     float wt;
-    warp_topk_softmax(logits + static_cast<int64_t>(t) * E, E, k, lane, &e, &wt);
+    with_chunks(E, [&](auto nm) {
+        warp_topk_softmax<decltype(nm)::value>(logits + static_cast<int64_t>(t) * E, E, k, lane, &e, &wt);
+    });
     if (lane < k) {
         idx[static_cast<int64_t>(t) * k + lane] = e;
         w[static_cast<int64_t>(t) * k + lane] = wt;
@@ -153,11 +163,32 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
 cudaError_t launch_topk_softmax(const float* logits, int64_t T, int64_t E, int k, int32_t* idx, float* w,
                                 cudaStream_t s) {
     const int64_t grid = (T * 32 + 255) / 256;
-    topk_softmax_kernel<<<(unsigned)grid, 256, 0, s>>>(logits, (int)T, (int)E, k, idx, w);
-    return cudaGetLastError();
+    return launch_pdl(topk_softmax_kernel, dim3((unsigned)grid), dim3(256), 0, s, logits, (int)T, (int)E, k, idx, w);
 }
 
 // ----------------------------------------------------------------------------- permute
+// One record per slot once this CTA has written offsets, act_e, perm and n_active (call
+// after a __syncthreads): expert, first sorted row, pair count (0 for idle slots), and the
+// tokens of its first four rows packed 8 bits each when `pack` (T <= 254).
+__device__ void write_slot_infos(int slot_cap, int k, int T, const Workspace& ws, bool pack) {
+    const int n_act = *ws.n_active;
+    for (int s = threadIdx.x; s < slot_cap; s += blockDim.x) {
+        int4 si = make_int4(0, 0, 0, kNoPackedTokens);
+        if (s < n_act) {
+            const int e = ws.act_e[s];
+            const int r0 = ws.offsets[e];
+            const int cnt = ws.offsets[e + 1] - r0;
+            int packed = kNoPackedTokens;
+            if (pack && T <= 254) {
+                packed = 0;
+                for (int i = 0; i < 4 && i < cnt; ++i) packed |= (ws.perm[r0 + i] / k) << (8 * i);
+            }
+            si = make_int4(e, r0, cnt, packed);
+        }
+        ws.slot_info[s] = si;
+    }
+}
+
 // Exclusive prefix sum over n <= 1024 values held one per thread (blockDim 1024).
 __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* warp_tot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -216,6 +247,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
                                                             const int32_t* __restrict__ idx_in,
                                                             const float* __restrict__ w_in, int T, int E, int k,
                                                             int gwords, Workspace ws) {
+    pdl_wait();
     extern __shared__ int smem[];
     int* wcnt = smem;                    // [32][E]
     int* sidx = smem + 32 * E;           // [1024]
@@ -227,7 +259,9 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
         if (warp < T) {
             int32_t e;
             float wt;
-            warp_topk_softmax(logits + static_cast<int64_t>(warp) * E, E, k, lane, &e, &wt);
+            with_chunks(E, [&](auto nm) {
+                warp_topk_softmax<decltype(nm)::value>(logits + static_cast<int64_t>(warp) * E, E, k, lane, &e, &wt);
+            });
             if (lane < k) {
                 sidx[warp * k + lane] = e;
                 ws.idx[warp * k + lane] = e;
@@ -278,6 +312,8 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
     }
     const int max_slots = min(E, P);
     for (int i = threadIdx.x; i < max_slots * gwords; i += blockDim.x) ws.gmask[i] = 0;
+    __syncthreads();
+    write_slot_infos(max_slots, k, T, ws, true);
 }
 
 cudaError_t launch_route_small(const float* logits, const int32_t* idx_in, const float* w_in, int64_t T,
@@ -292,8 +328,8 @@ cudaError_t launch_route_small(const float* logits, const int32_t* idx_in, const
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    route_small_kernel<<<1, 1024, smem, s>>>(logits, idx_in, w_in, (int)T, (int)E, k, gwords, ws);
-    return cudaGetLastError();
+    return launch_pdl(route_small_kernel, dim3(1), dim3(1024), smem, s, logits, idx_in, w_in, (int)T, (int)E, k, gwords,
+                      ws);
 }
 
 // Large problems: three kernels over chunks of 1024 pairs.
@@ -301,6 +337,7 @@ cudaError_t launch_route_small(const float* logits, const int32_t* idx_in, const
 __global__ void __launch_bounds__(1024) perm_rank_kernel(const int32_t* __restrict__ idx_src,
                                                           const float* __restrict__ w_in, int P, int E,
                                                           Workspace ws) {
+    pdl_wait();
     extern __shared__ int wcnt[];   // [32][E]
     const int p = blockIdx.x * 1024 + threadIdx.x;
     int e = -1;
@@ -329,6 +366,7 @@ __global__ void __launch_bounds__(1024) perm_rank_kernel(const int32_t* __restri
 
 // (2) one block: chunk bases, offsets, active list, group-mask clear.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int nchunk, int E, int P, int gwords, Workspace ws) {
+    pdl_wait();
     __shared__ int warp_tot[32];
     int total = 0;
     if ((int)threadIdx.x < E) {
@@ -353,10 +391,13 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int nchunk, int E, int 
     }
     const int max_slots = min(E, P);
     for (int i = threadIdx.x; i < max_slots * gwords; i += blockDim.x) ws.gmask[i] = 0;
+    __syncthreads();
+    write_slot_infos(max_slots, 0, 0, ws, false);
 }
 
 // (3) scatter.
 __global__ void __launch_bounds__(256) perm_scatter_kernel(int P, int E, Workspace ws) {
+    pdl_wait();
     const int p = blockIdx.x * blockDim.x + threadIdx.x;
     if (p >= P) return;
     const int e = ws.idx[p];
@@ -379,14 +420,320 @@ cudaError_t launch_permute_large(const int32_t* idx_in, const float* w_in, int64
         configured_device = dev;
     }
     const int32_t* src = idx_in ? idx_in : ws.idx;
-    perm_rank_kernel<<<nchunk, 1024, 32 * (size_t)E * sizeof(int), s>>>(src, idx_in ? w_in : nullptr, P, (int)E,
-                                                                        ws);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(perm_rank_kernel, dim3(nchunk), dim3(1024), 32 * (size_t)E * sizeof(int), s, src,
+                               idx_in ? w_in : nullptr, P, (int)E, ws);
     if (e != cudaSuccess) return e;
-    perm_scan_kernel<<<1, 1024, 0, s>>>(nchunk, (int)E, P, gwords, ws);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    perm_scatter_kernel<<<(P + 255) / 256, 256, 0, s>>>(P, (int)E, ws);
-    return cudaGetLastError();
+    if ((e = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, nchunk, (int)E, P, gwords, ws)) != cudaSuccess)
+        return e;
+    return launch_pdl(perm_scatter_kernel, dim3((P + 255) / 256), dim3(256), 0, s, P, (int)E, ws);
+}
+
+// ----------------------------------------------------------------------------- fused decode routing
+// Block-wide exclusive scan (256 threads) over v[0..n), n <= 1024, in place; returns the total.
+__device__ __forceinline__ int block_scan_256(int* v, int n, int* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per = (n + 255) / 256;
+    const int b0 = threadIdx.x * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i)
+        if (b0 + i < n) local += v[b0 + i];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int w = 0; w < 8; ++w) {
+            const int c = warp_tot[w];
+            warp_tot[w] = run;
+            run += c;
+        }
+        warp_tot[8] = run;
+    }
+    __syncthreads();
+    int run = warp_tot[warp] + incl - local;
+    for (int i = 0; i < per; ++i) {
+        if (b0 + i < n) {
+            const int c = v[b0 + i];
+            v[b0 + i] = run;
+            run += c;
+        }
+    }
+    const int total = warp_tot[8];
+    __syncthreads();
+    return total;
+}
+
+// Stable permutation of P <= 1024 pairs (expert ids in sidx) by one CTA of 256 threads.
+// Writes offsets[E+1], perm, pos, the active-expert list, n_active and the slot records,
+// all from values held in shared memory (no read-back of its own global writes).
+__device__ void permute_block_256(const int* sidx, int T, int k, int E, int gwords, Workspace ws) {
+    const int P = T * k;
+    const int slot_cap = min(E, P);
+    const bool pack = T <= 254;
+    __shared__ int cnt[kMaxE + 1];
+    __shared__ int act[kMaxE];
+    __shared__ int sperm[1024];
+    __shared__ int warp_tot[9];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (P <= 32) {
+        // one warp: ranks by direct comparison
+        if (warp == 0) {
+            const int e = lane < P ? sidx[lane] : 0x7fffffff;
+            int before = 0, same_before = 0;
+            for (int q = 0; q < P; ++q) {
+                const int eq = __shfl_sync(0xffffffffu, e, q);
+                before += (eq < e);
+                same_before += (eq == e && q < lane);
+            }
+            const int r = before + same_before;
+            if (lane < P) {
+                ws.perm[r] = lane;
+                ws.pos[lane] = r;
+            }
+            // lane r takes the expert and the pair at sorted row r
+            int se = 0x7fffffff, sp = 0;
+            for (int q = 0; q < P; ++q) {
+                const int rq = __shfl_sync(0xffffffffu, r, q);
+                const int eq = __shfl_sync(0xffffffffu, e, q);
+                if (rq == lane) {
+                    se = eq;
+                    sp = q;
+                }
+            }
+            const int prev = __shfl_up_sync(0xffffffffu, se, 1);
+            const bool first = lane < P && (lane == 0 || prev != se);
+            const uint32_t fm = __ballot_sync(0xffffffffu, first);
+            const int n_act = __popc(fm);
+            int packed = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int src = min(lane + i, 31);
+                const int tok = __shfl_sync(0xffffffffu, sp, src) / k;
+                const int tse = __shfl_sync(0xffffffffu, se, src);
+                if (lane + i < P && tse == se) packed |= tok << (8 * i);
+            }
+            if (first) {
+                const int slot = __popc(fm & ((1u << lane) - 1u));
+                const uint32_t above = fm & ~((2u << lane) - 1u);
+                const int next = above ? (__ffs(above) - 1) : P;
+                ws.act_e[slot] = se;
+                ws.slot_info[slot] = make_int4(se, lane, next - lane, pack ? packed : kNoPackedTokens);
+            }
+            for (int sl = n_act + lane; sl < slot_cap; sl += 32) ws.slot_info[sl] = make_int4(0, 0, 0, kNoPackedTokens);
+            if (lane == 0) *ws.n_active = n_act;
+        }
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+            int c = 0;
+            for (int q = 0; q < P; ++q) c += (sidx[q] < e);
+            ws.offsets[e] = c;
+        }
+    } else {
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) cnt[e] = 0;
+        __syncthreads();
+        for (int p = threadIdx.x; p < P; p += blockDim.x) atomicAdd(&cnt[sidx[p]], 1);
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x) act[e] = cnt[e] > 0 ? 1 : 0;
+        __syncthreads();
+        block_scan_256(cnt, E, warp_tot);           // cnt -> offsets
+        const int n_act = block_scan_256(act, E, warp_tot);
+        __shared__ int s_act_e[kMaxE];
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            ws.offsets[e] = cnt[e];
+            const int c = ((e + 1 < E) ? cnt[e + 1] : P) - cnt[e];
+            if (c > 0) {
+                ws.act_e[act[e]] = e;
+                s_act_e[act[e]] = e;
+            }
+        }
+        if (threadIdx.x == 0) {
+            ws.offsets[E] = P;
+            *ws.n_active = n_act;
+        }
+        __syncthreads();
+        // stable ranks: pairs in order, one expert-run counter per expert
+        for (int e = threadIdx.x; e < E; e += blockDim.x) act[e] = cnt[e];   // next free row of each expert
+        __syncthreads();
+        for (int c0 = 0; c0 < P; c0 += 256) {
+            const int p = c0 + threadIdx.x;
+            const int e = p < P ? sidx[p] : -1;
+            const uint32_t peers = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            // warps take their turn in order so that rows follow pair order
+            for (int w = 0; w < 8; ++w) {
+                if (warp == w && e >= 0) {
+                    const int r = act[e] + rank;
+                    ws.perm[r] = p;
+                    ws.pos[p] = r;
+                    sperm[r] = p;
+                    __syncwarp(peers);
+                    if (rank == 0) act[e] += __popc(peers);
+                }
+                __syncthreads();
+            }
+        }
+        for (int sl = threadIdx.x; sl < slot_cap; sl += blockDim.x) {
+            int4 si = make_int4(0, 0, 0, kNoPackedTokens);
+            if (sl < n_act) {
+                const int e = s_act_e[sl];
+                const int r0 = cnt[e];
+                const int c = ((e + 1 < E) ? cnt[e + 1] : P) - r0;
+                int packed = kNoPackedTokens;
+                if (pack) {
+                    packed = 0;
+                    for (int i = 0; i < 4 && i < c; ++i) packed |= (sperm[r0 + i] / k) << (8 * i);
+                }
+                si = make_int4(e, r0, c, packed);
+            }
+            ws.slot_info[sl] = si;
+        }
+    }
+    for (int i = threadIdx.x; i < slot_cap * gwords; i += blockDim.x) ws.gmask[i] = 0;
+}
+
+// Router + top-k + softmax + permutation for small batches (T * E <= 4096, T * k <= 1024)
+// in one launch.  grid: (32 residue classes, ceil(E/128) expert chunks) x 256 threads.
+// Warp j of CTA (c, chunk) owns the canonical partial sum l = c + 32 j for the chunk's 128
+// experts (lane = 4 experts): it reads whole 512-byte rows i = l, l + 256, ... of W, fully
+// coalesced.  Tree levels h = 128, 64, 32 combine partials of the same residue c, inside the
+// CTA; the CTA writes its result to part[t][e][c].  The last CTA to finish (atomic counter,
+// no waiting) applies levels h = 16 .. 1 across the 32 residues, then selects, weights and
+// permutes, and resets the counter.
+constexpr int kResidues = 32;
+constexpr int kRouteChunk = 128;
+constexpr int kChainBatch = 12;
+constexpr int kFusedRouteLogits = 4096;
+
+__global__ void __launch_bounds__(256) route_decode_kernel(const void* __restrict__ x, int xt,
+                                                            const float* __restrict__ W, int T, int d, int E, int k,
+                                                            int gwords, Workspace ws) {
+    const int c = blockIdx.x, chunk = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int l = c + kResidues * warp;
+    const int e0 = chunk * kRouteChunk + lane * 4;
+    const bool on = e0 < E;
+    const int nchain = d / kRouterPartials;     // d is a multiple of 256
+    // phase 1 uses the buffer as red[8 warps][4 tokens][128 experts], the last CTA as the
+    // logits slog[T * E] (both 16 KB)
+    __shared__ __align__(16) float buf[8 * 4 * kRouteChunk];
+    static_assert(8 * 4 * kRouteChunk == kFusedRouteLogits, "shared buffer reuse");
+    float (*red)[4][kRouteChunk] = reinterpret_cast<float (*)[4][kRouteChunk]>(buf);
+    float* slog = buf;
+    __shared__ int s_last;
+    __shared__ int sidx[1024];
+    // The router weights do not depend on the previous kernel: the first batch of rows is
+    // loaded before waiting for it.
+    float4 w0[kChainBatch];
+#pragma unroll
+    for (int u = 0; u < kChainBatch; ++u)
+        if (on && u < nchain)
+            w0[u] = __ldg(reinterpret_cast<const float4*>(W + static_cast<int64_t>(l + u * kRouterPartials) * E + e0));
+    pdl_wait();
+    pdl_trigger();
+    for (int t0 = 0; t0 < T; t0 += 4) {
+        const int nt = min(4, T - t0);
+        float acc[4][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+        for (int m0 = 0; m0 < nchain; m0 += kChainBatch) {
+            float4 wv[kChainBatch];
+            float xv[4][kChainBatch];
+#pragma unroll
+            for (int u = 0; u < kChainBatch; ++u) {
+                if (m0 + u < nchain) {
+                    const int i = l + (m0 + u) * kRouterPartials;
+                    if (on) wv[u] = (m0 == 0) ? w0[u]
+                                              : __ldg(reinterpret_cast<const float4*>(W + static_cast<int64_t>(i) * E + e0));
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        xv[t][u] = (t < nt) ? load_x(x, xt, static_cast<int64_t>(t0 + t) * d + i) : 0.0f;
+                }
+            }
+            if (on) {
+#pragma unroll
+                for (int u = 0; u < kChainBatch; ++u) {
+                    if (m0 + u < nchain) {
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            acc[t][0] = fmaf(xv[t][u], wv[u].x, acc[t][0]);
+                            acc[t][1] = fmaf(xv[t][u], wv[u].y, acc[t][1]);
+                            acc[t][2] = fmaf(xv[t][u], wv[u].z, acc[t][2]);
+                            acc[t][3] = fmaf(xv[t][u], wv[u].w, acc[t][3]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            *reinterpret_cast<float4*>(&red[warp][t][lane * 4]) = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+        __syncthreads();
+        // levels h = 128, 64, 32: warp j += warp j + h/32 (same residue c)
+        for (int it = threadIdx.x; it < 4 * kRouteChunk; it += blockDim.x) {
+            const int t = it / kRouteChunk, ee = it % kRouteChunk;
+            float s[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s[j] = red[j][t][ee];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[j] = s[j] + s[j + 4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) s[j] = s[j] + s[j + 2];
+            s[0] = s[0] + s[1];
+            const int e = chunk * kRouteChunk + ee;
+            if (t < nt && e < E) ws.rpart[(static_cast<int64_t>(t0 + t) * E + e) * kResidues + c] = s[0];
+        }
+        __syncthreads();
+    }
+    // the last CTA to finish does the rest
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = (atomicAdd(ws.route_ctr, 1) == static_cast<int>(gridDim.x * gridDim.y) - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // levels h = 16 .. 1 across the 32 residues
+    for (int it = threadIdx.x; it < T * E; it += blockDim.x) {
+        const float4* pp = reinterpret_cast<const float4*>(ws.rpart + static_cast<int64_t>(it) * kResidues);
+        float s[kResidues];
+#pragma unroll
+        for (int q = 0; q < kResidues / 4; ++q) {
+            const float4 v = __ldcg(pp + q);
+            s[4 * q] = v.x, s[4 * q + 1] = v.y, s[4 * q + 2] = v.z, s[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int h = kResidues / 2; h >= 1; h >>= 1)
+#pragma unroll
+            for (int j = 0; j < h; ++j) s[j] = s[j] + s[j + h];
+        slog[it] = s[0];
+        ws.logits[it] = s[0];
+    }
+    __syncthreads();
+    for (int t = warp; t < T; t += 8) {
+        int32_t e;
+        float wt;
+        with_chunks(E, [&](auto nm) {
+            warp_topk_softmax<decltype(nm)::value>(slog + t * E, E, k, lane, &e, &wt);
+        });
+        if (lane < k) {
+            sidx[t * k + lane] = e;
+            ws.idx[t * k + lane] = e;
+            ws.w[t * k + lane] = wt;
+        }
+    }
+    __syncthreads();
+    permute_block_256(sidx, T, k, E, gwords, ws);
+    if (threadIdx.x == 0) *ws.route_ctr = 0;
+}
+
+cudaError_t launch_route_decode(const void* x, int xt, const float* W, int64_t T, int64_t d, int64_t E, int k,
+                                int gwords, const Workspace& ws, cudaStream_t s) {
+    const dim3 grid(kResidues, (unsigned)((E + kRouteChunk - 1) / kRouteChunk));
+    return launch_pdl(route_decode_kernel, grid, dim3(256), 0, s, x, xt, W, (int)T, (int)d, (int)E, k, gwords, ws);
 }
 
 }  // namespace moe
