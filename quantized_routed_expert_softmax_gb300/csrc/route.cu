@@ -713,17 +713,35 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
         ws.logits[it] = s[0];
     }
     __syncthreads();
-    for (int t = warp; t < T; t += 8) {
-        int32_t e;
-        float wt;
-        with_chunks(E, [&](auto nm) {
-            warp_topk_softmax<decltype(nm)::value>(slog + t * E, E, k, lane, &e, &wt);
-        });
-        if (lane < k) {
-            sidx[t * k + lane] = e;
-            ws.idx[t * k + lane] = e;
-            ws.w[t * k + lane] = wt;
+    // Top-k by rank: expert e's slot is the number of experts that beat it (larger logit, or
+    // equal logit and lower index) -- the order repeated selection would produce, computed
+    // for all (token, expert) at once.
+    __shared__ float stop[1024];
+    for (int it = threadIdx.x; it < T * E; it += blockDim.x) {
+        const int t = it / E, e = it % E;
+        const float v = slog[it];
+        const float4* row = reinterpret_cast<const float4*>(slog + t * E);
+        int rank = 0;
+        for (int q = 0; q < E / 4; ++q) {
+            const float4 o = row[q];
+            const int b = 4 * q;
+            rank += (o.x > v || (o.x == v && b < e)) + (o.y > v || (o.y == v && b + 1 < e)) +
+                    (o.z > v || (o.z == v && b + 2 < e)) + (o.w > v || (o.w == v && b + 3 < e));
         }
+        if (rank < k) {
+            sidx[t * k + rank] = e;
+            stop[t * k + rank] = v;
+        }
+    }
+    __syncthreads();
+    // softmax over the k selected logits, the maximum (slot 0) subtracted, sum in slot order
+    for (int p = threadIdx.x; p < T * k; p += blockDim.x) {
+        const int t = p / k;
+        const float m0 = stop[t * k];
+        float sum = 0.0f;
+        for (int j = 0; j < k; ++j) sum += expf(stop[t * k + j] - m0);
+        ws.idx[p] = sidx[p];
+        ws.w[p] = expf(stop[p] - m0) / sum;
     }
     __syncthreads();
     permute_block_256(sidx, T, k, E, gwords, ws);
