@@ -24,8 +24,9 @@
  *     nothing is launched, outputs are untouched, and the status says why.  No C++
  *     exception crosses this interface.
  *   - Faults found inside a kernel (an expert index out of range in caller-supplied
- *     routing) never trap: the kernel clamps, records a code in the workspace's error
- *     word, and moe_get_device_status() reports it.
+ *     routing, a tensor-core wait that ran past its time limit) never trap: the kernel
+ *     clamps or stops, records a code in the workspace's error word, and
+ *     moe_get_device_status() reports it.
  *   - Shapes: row counts and column counts must be multiples of 32 (Q8_0) or 64
  *     (NVFP4); the layer needs d a multiple of 256 and f a multiple of 32 (Q8_0) or 64
  *     (NVFP4).  Pointers must be 16-byte aligned.
@@ -83,7 +84,10 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  */
 typedef enum { MOE_LAYOUT_CANONICAL = 0, MOE_LAYOUT_DEVICE = 1, MOE_LAYOUT_NEURON = 2 } moe_layout;
 
-/* Which expert kernels moe_layer_forward uses.  AUTO picks by tokens per expert. */
+/* Which expert kernels moe_layer_forward uses.  GEMV: weight-streaming matrix-vector
+ * kernels (a few tokens per expert).  GEMM: grouped GEMMs on the tensor cores (tcgen05),
+ * which need f a multiple of 64 (128 for ReLU^2); forcing GEMM on another shape returns
+ * MOE_ERR_UNSUPPORTED.  AUTO takes GEMM when T*k >= 8*E and the shape allows it. */
 typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GEMM = 2 } moe_path;
 
 /* Bytes of one quantised matrix: rows*cols/32*34 (Q8_0), rows*cols/2 + rows*cols/16
@@ -249,7 +253,9 @@ moe_status moe_layer_forward_noalloc(const moe_layer_desc* desc, const void* x, 
 /*
  * moe_get_device_status -- synchronises `stream`, reads the error word of a layer
  * workspace, clears it, and returns MOE_OK or MOE_ERR_DEVICE_CHECK (the device code in
- * *device_code, may be NULL): 1 = an expert index outside [0, E) was clamped.
+ * *device_code, may be NULL): 1 = an expert index outside [0, E) was clamped; 2 = a
+ * tensor-core (GEMM path) wait passed its one-second limit and the kernel stopped early
+ * (the output is then not valid).
  */
 moe_status moe_get_device_status(void* workspace, moe_stream_t stream, int32_t* device_code);
 

@@ -23,6 +23,8 @@ cudaError_t launch_gate_up_gemv(const ExpertArgs&, int, int, int, cudaStream_t);
 cudaError_t launch_down_gemv(const ExpertArgs&, int, int, cudaStream_t);
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int64_t, int, int64_t, float*, cudaStream_t);
 cudaError_t launch_rmsnorm_bf16(const float*, int64_t, int64_t, float, uint16_t*, cudaStream_t);
+cudaError_t configure_gemm_kernels();
+cudaError_t launch_expert_gemm(const ExpertArgs&, int, int, int, int, int, cudaStream_t);
 
 
 namespace {
@@ -40,8 +42,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Per-device one-time kernel attribute setup (dynamic shared memory above 48 KB).
-cudaError_t ensure_configured() {
+// Per-device one-time kernel attribute setup (dynamic shared memory above 48 KB) and the
+// device's SM count.
+int g_num_sms[64] = {};
+
+cudaError_t ensure_configured(int* num_sms) {
     static std::mutex mu;
     static bool done[64] = {};
     int dev = 0;
@@ -49,10 +54,15 @@ cudaError_t ensure_configured() {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
-    if (done[dev]) return cudaSuccess;
-    e = configure_gemv_kernels();
-    if (e == cudaSuccess) done[dev] = true;
-    return e;
+    if (!done[dev]) {
+        e = configure_gemv_kernels();
+        if (e == cudaSuccess) e = configure_gemm_kernels();
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    *num_sms = g_num_sms[dev];
+    return cudaSuccess;
 }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -66,7 +76,15 @@ struct Plan {
     bool small_route;   // T <= 32 and P <= 1024: routing and permutation in one CTA
     bool fuse_combine;  // the down kernel's last CTA per row tile combines (one item per thread)
     bool prefetch_down; // gate.up CTAs prefetch the routed experts' down weights into L2
+    bool gemm;          // expert GEMMs on the tensor cores instead of the GEMVs
 };
+
+// The GEMM path tiles rows by 128 (SwiGLU gate.up: 64 neurons' gate and up rows) and K by 64.
+bool gemm_shape_ok(const moe_layer_desc* d) {
+    if (d->f % 64 != 0 || d->d % 64 != 0) return false;
+    if (d->act == MOE_ACT_RELU2 && d->f % 128 != 0) return false;
+    return true;
+}
 
 Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     Plan p{};
@@ -91,6 +109,9 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     const int64_t dn_bytes = static_cast<int64_t>(d->wfmt == MOE_W_Q8_0 ? moe_q8_0_bytes(d->d, d->f)
                                                                           : moe_nvfp4_bytes(d->d, d->f));
     p.prefetch_down = static_cast<int64_t>(p.slot_cap) * dn_bytes <= kPrefetchBudget;
+    // many tokens per expert (at least 8 on average): tensor-core GEMMs
+    p.gemm = gemm_shape_ok(d) && (d->path == MOE_PATH_GEMM || (d->path == MOE_PATH_AUTO && p.P >= 8 * d->E));
+    if (p.gemm) p.fuse_combine = false;
     return p;
 }
 
@@ -288,9 +309,10 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_ALIGNMENT;
     const Layout L = layout_for(desc, T);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-    if (desc->path == MOE_PATH_GEMM) return MOE_ERR_UNSUPPORTED;
+    if (desc->path == MOE_PATH_GEMM && !gemm_shape_ok(desc)) return MOE_ERR_UNSUPPORTED;
 
-    cudaError_t e = ensure_configured();
+    int num_sms = 0;
+    cudaError_t e = ensure_configured(&num_sms);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const Plan p = make_plan(desc, T, xt);
@@ -348,10 +370,14 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.ws = ws;
     mark(1);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if ((e = launch_gate_up_gemv(a, desc->wfmt, desc->act, p.slot_cap, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (p.gemm) e = launch_expert_gemm(a, 0, desc->wfmt, desc->act, p.slot_cap, num_sms, s);
+    else e = launch_gate_up_gemv(a, desc->wfmt, desc->act, p.slot_cap, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
     mark(2);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if ((e = launch_down_gemv(a, desc->wfmt, p.slot_cap, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (p.gemm) e = launch_expert_gemm(a, 1, desc->wfmt, desc->act, p.slot_cap, num_sms, s);
+    else e = launch_down_gemv(a, desc->wfmt, p.slot_cap, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
     mark(3);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (!p.fuse_combine) {

@@ -108,8 +108,8 @@ SMALL = {
 }
 
 
-def _run_small(w, T, idx_in=None, w_in=None):
-    L = layers.build_layer(w, source="numpy")
+def _run_small(w, T, idx_in=None, w_in=None, path="auto"):
+    L = layers.build_layer(w, source="numpy", path=path)
     x = synth.tokens(w, T, tag="parity")
     xt = torch.from_numpy(x).cuda()
     if x.dtype == np.uint16:
@@ -138,6 +138,34 @@ def test_layer_small_parity(name, T):
     # activations in sorted-row order
     h_ref = ref["h"][ref["perm"]]
     assert_close(tr["h"].cpu().numpy(), h_ref, what="h")
+    assert_close(out, ref["out"])
+
+
+# The tensor-core GEMM path forced on the same layers: token tiles of 128 with ragged tails
+# (T=700 puts about 175 rows on each expert of the 8-expert layers), fp32 inputs split hi/lo.
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("T", [1, 16, 100, 700])
+def test_layer_small_gemm_parity(name, T):
+    w = SMALL[name]
+    L, out, tr, ref = _run_small(w, T, path="gemm")
+    assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
+    assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
+    assert_close(tr["h"].cpu().numpy(), ref["h"][ref["perm"]], what="h")
+    assert_close(out, ref["out"])
+    # no atomics on this path either: a second call is bit-identical
+    out2 = L.forward(torch.from_numpy(synth.tokens(w, T, tag="parity")).cuda().view(
+        torch.bfloat16 if w.x_dtype == "bf16" else torch.float32)).cpu().numpy()
+    assert np.array_equal(out.view(np.uint32), out2.view(np.uint32))
+
+
+def test_layer_gemm_skewed_routing():
+    # Zipf-skewed supplied routing: the hottest experts get several token tiles, some none
+    w = SMALL["small_nvfp4_relu2"]
+    T = 900
+    idx, wts = synth.zipf_routing(T, w.E, w.k, seed_tag="gemm-skew")
+    L, out, tr, ref = _run_small(w, T, idx_in=idx, w_in=wts, path="gemm")
+    assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
+    assert np.bincount(idx.ravel(), minlength=w.E).max() > 2 * 128
     assert_close(out, ref["out"])
 
 
@@ -201,9 +229,9 @@ def test_rmsnorm_bf16():
 
 
 # ------------------------------------------------------------------ the layer, full shapes
-def _full_case(name, T, sample=None, idx_in=None, w_in=None):
+def _full_case(name, T, sample=None, idx_in=None, w_in=None, path="auto"):
     w = synth.WORKLOADS[name]
-    L = layers.build_layer(w, keep_fp32=True)
+    L = layers.build_layer(w, keep_fp32=True, path=path)
     x = synth.tokens_cuda(w, T, tag="parity")
     tr = {}
     ii = None if idx_in is None else torch.from_numpy(idx_in).cuda()
@@ -253,8 +281,9 @@ def test_gemma_layer_full_size(T):
     _full_case("gemma", T)
 
 
-def test_gemma_layer_prefill_512_sampled():
-    _full_case("gemma", 512, sample=[0, 1, 255, 511])
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+def test_gemma_layer_prefill_512_sampled(path):
+    _full_case("gemma", 512, sample=[0, 1, 255, 511], path=path)
 
 
 @pytest.mark.parametrize("T,sample", [(1, None), (32, [0, 31])])
@@ -267,8 +296,12 @@ def test_minimax_layer_full_size(T, sample):
     _full_case("minimax", T, sample=sample)
 
 
-@pytest.mark.parametrize("T", [64])
-def test_zipf_routing_full_size(T):
-    w = synth.WORKLOADS["zipf"]
+def test_minimax_layer_prefill_4096_sampled():
+    _full_case("minimax", 4096, sample=[0, 2047, 4095])
+
+
+@pytest.mark.parametrize("name,T", [("zipf", 64), ("zipf", 2048), ("zipf_nvfp4", 2048)])
+def test_zipf_routing_full_size(name, T):
+    w = synth.WORKLOADS[name]
     idx, wts = synth.zipf_routing(T, w.E, w.k)
-    _full_case("zipf", T, sample=[0, 17, 63], idx_in=idx, w_in=wts)
+    _full_case(name, T, sample=[0, 17, T - 1], idx_in=idx, w_in=wts)
