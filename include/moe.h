@@ -255,7 +255,8 @@ moe_status moe_layer_forward_noalloc(const moe_layer_desc* desc, const void* x, 
  * workspace, clears it, and returns MOE_OK or MOE_ERR_DEVICE_CHECK (the device code in
  * *device_code, may be NULL): 1 = an expert index outside [0, E) was clamped; 2 = a
  * tensor-core (GEMM path) wait passed its one-second limit and the kernel stopped early
- * (the output is then not valid).
+ * (the output is then not valid); 3 = the GEMM path met an activation (x or h) beyond the
+ * f16 range +-65504 that its tensor-core operands use (the output then holds inf).
  */
 moe_status moe_get_device_status(void* workspace, moe_stream_t stream, int32_t* device_code);
 

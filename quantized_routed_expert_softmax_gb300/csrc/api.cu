@@ -25,6 +25,7 @@ cudaError_t launch_combine(const float*, const int32_t*, const float*, int64_t, 
 cudaError_t launch_rmsnorm_bf16(const float*, int64_t, int64_t, float, uint16_t*, cudaStream_t);
 cudaError_t configure_gemm_kernels();
 cudaError_t launch_expert_gemm(const ExpertArgs&, int, int, int, int, int, cudaStream_t);
+cudaError_t launch_gather_x_f16(const ExpertArgs&, int, cudaStream_t);
 
 
 namespace {
@@ -117,7 +118,7 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
 
 struct Layout {
     size_t err, route_ctr, n_active, row_ctr, logits, rpart, idx, w, offsets, perm, pos, act_e, slot_info, chunk_cnt,
-        local_rank, gmask, h, y, total;
+        local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, total;
 };
 
 // Workspace regions for T tokens (each 256-byte aligned).  The control words (err,
@@ -150,6 +151,13 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     L.gmask = take(sizeof(uint32_t) * p.slot_cap * p.gwords);
     L.h = take(sizeof(float) * p.P * d->f);
     L.y = take(sizeof(float) * p.P * d->d);
+    // f16 planes of the tensor-core path (the lo plane of x is used by fp32 inputs only)
+    const size_t xs = p.gemm ? sizeof(uint16_t) * p.P * d->d : 0;
+    const size_t hs = p.gemm ? sizeof(uint16_t) * p.P * d->f : 0;
+    L.xs_hi = take(xs);
+    L.xs_lo = take(xs);
+    L.h_hi = take(hs);
+    L.h_lo = take(hs);
     L.total = off;
     return L;
 }
@@ -175,6 +183,10 @@ Workspace bind(void* base, const Layout& L) {
     w.gmask = reinterpret_cast<uint32_t*>(b + L.gmask);
     w.h = reinterpret_cast<float*>(b + L.h);
     w.y = reinterpret_cast<float*>(b + L.y);
+    w.xs_hi = reinterpret_cast<uint16_t*>(b + L.xs_hi);
+    w.xs_lo = reinterpret_cast<uint16_t*>(b + L.xs_lo);
+    w.h_hi = reinterpret_cast<uint16_t*>(b + L.h_hi);
+    w.h_lo = reinterpret_cast<uint16_t*>(b + L.h_lo);
     return w;
 }
 
@@ -370,8 +382,12 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.ws = ws;
     mark(1);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if (p.gemm) e = launch_expert_gemm(a, 0, desc->wfmt, desc->act, p.slot_cap, num_sms, s);
-    else e = launch_gate_up_gemv(a, desc->wfmt, desc->act, p.slot_cap, s);
+    if (p.gemm) {
+        e = launch_gather_x_f16(a, num_sms, s);
+        if (e == cudaSuccess) e = launch_expert_gemm(a, 0, desc->wfmt, desc->act, p.slot_cap, num_sms, s);
+    } else {
+        e = launch_gate_up_gemv(a, desc->wfmt, desc->act, p.slot_cap, s);
+    }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mark(2);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -410,6 +426,7 @@ int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_
     if (p.small_route) n += 1;                              // routing + permutation in one launch
     else n += (routing_supplied ? 0 : 2) + 3;               // router, top-k; rank, scan, scatter
     n += 2;                                                 // gate.up, down
+    if (p.gemm) n += 1;                                     // sorted f16 copy of x
     if (!p.fuse_combine) n += 1;                            // combine
     return n;
 }

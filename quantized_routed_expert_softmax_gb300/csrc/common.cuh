@@ -42,6 +42,10 @@ struct Workspace {
     uint32_t* gmask;       // [min(E,P)][ceil(f/16/32)] active 16-neuron groups per slot
     float* h;              // [P][f] activations, sorted rows
     float* y;              // [P][d] down projections, sorted rows
+    uint16_t* xs_hi;       // [P][d] f16 x in sorted-row order (tensor-core path), hi part
+    uint16_t* xs_lo;       // [P][d] ... lo part (fp32 inputs)
+    uint16_t* h_hi;        // [P][f] f16 hi part of h (tensor-core path)
+    uint16_t* h_lo;        // [P][f] f16 lo part of h
 };
 
 // Arguments of the expert kernels (gate.up, down) of one layer call.

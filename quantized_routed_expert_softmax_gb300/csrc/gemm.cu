@@ -7,36 +7,63 @@
 // tensor; "Running NVIDIA's new 120B Nemotron-3.5-Super on an 8GB GPU", "bytes per token":
 // the gateless ReLU^2 latent experts), for batches where each expert sees many tokens.
 //
-// Swap-AB: D[128 weight rows][N tokens] = W_e[rows][K] * X^T, so the weight rows fill the
-// MMA's M = 128 and the expert's tokens (often few) fill N (16..128).  A persistent grid walks
-// a device-built list of (expert slot, token tile, row tile) work items.  Per K step of 64:
-//   1. raw weight bytes (Q8_0 / NVFP4 panels) and the activation rows stream through a
-//      cp.async ring in shared memory (kRaw steps ahead);
-//   2. all threads dequantise into f16 tiles in the 128-byte-swizzled K-major layout the
-//      tensor core reads and convert the activations to f16.  NVFP4 weights e2m1 * e4m3
-//      are exact in f16.  A Q8_0 weight q * d needs up to 18 significant bits, so it is
-//      split into hi = f16(q * d) and lo = fma(q, d, -hi) (the exact residual, rounded).
-//      bf16 activations in f16's normal range convert exactly; fp32 inputs and the fp32
-//      hidden activations are split the same way into hi + lo;
-//   3. one thread issues the tcgen05.mma (K = 16 each: A.hi*B.hi, A.lo*B.hi for Q8_0,
-//      A.hi*B.lo for fp32 activations; the lo*lo term is below fp32 rounding) into the
-//      tensor-memory accumulator and commits them to an mbarrier that frees the stage.
-// SwiGLU tiles interleave gate row n and up row n on adjacent accumulator lanes (2i, 2i+1),
-// so the epilogue pairs them with one shuffle.  Every wait on an mbarrier is bounded (about
-// a second); on timeout the kernel records MOE device error 2, releases its tensor memory
-// and returns.
+// Swap-AB: D[128 weight rows][N tokens] = W_e[rows][K] * B^T, so the weight rows fill the
+// MMA's M = 128 and the expert's tokens fill N (16..256).  B is an f16 "plane" of
+// activations in sorted-row order ([P][K]; written by gather_x_f16_kernel for gate.up and by
+// the gate.up epilogue for down), so a token tile is a plain 2-D box that TMA copies straight
+// into the 128-byte-swizzled K-major layout the tensor core reads.  fp32 activations (fp32
+// inputs, and always the hidden activations h) come as two planes hi + lo.
+//
+// A persistent grid walks a device-built list of (expert slot, token tile, row tile) work
+// items.  The warps of a CTA have fixed roles, linked by mbarriers:
+//   warp 0       weight producer: 1-D bulk copies of each K step's raw Q8_0 / NVFP4 bytes
+//                into a ring of kRawSlots slots (several K steps of HBM reads in flight);
+//   warp 1       activation producer: TMA 2-D loads of the token tile's B planes;
+//   warp 2       MMA issuer (one thread): per K step of 64, four K = 16 slices of
+//                tcgen05.mma (A.hi*B.hi, A.lo*B.hi for Q8_0, A.hi*B.lo for two planes; the
+//                lo*lo term is below fp32 rounding), committed to the stage's "empty"
+//                barrier, and at the end of an item to the accumulator's "full" barrier;
+//   warps 4..7   epilogue: tensor memory -> registers (lane quadrant = warp % 4), the
+//                activation (SwiGLU pairs gate row i and up row i on accumulator lanes 2i
+//                and 2i+1, one shuffle), stores; two accumulators alternate, so the
+//                epilogue of one item overlaps the main loop of the next;
+//   warps 8..15  dequantisers: raw slot -> f16 A tiles.  NVFP4 weights e2m1 * e4m3 are
+//                exact in f16.  A Q8_0 weight q * d needs up to 18 significant bits, so it
+//                is split into hi = f16(q * d) and lo = fma(q, d, -hi), the exact residual
+//                rounded once.
+// Every wait on an mbarrier is bounded (about a second); on timeout the kernel records MOE
+// device error 2, waits (bounded) for its copies and MMAs in flight, releases its tensor
+// memory and returns.
+#include <cuda.h>   // CUtensorMap and its enums; the encoder is looked up in the driver at run time
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int kGemmThreads = 256;
-constexpr int kTileM = 128;
-constexpr int kTileN = 128;          // tokens per work item (tensor-memory columns)
-constexpr int kStepK = 64;           // one 128-byte swizzle row of f16
-constexpr int kRaw = 2;              // raw ring depth (K steps in flight)
-constexpr int kStagesMma = 2;        // f16 operand stages
 constexpr int kDevErrTimeout = 2;
+constexpr int kDevErrF16Range = 3;
 constexpr long long kWaitLimitNs = 1000000000ll;
+
+constexpr int kGemmThreads = 512;
+constexpr int kTileM = 128;
+constexpr int kStepK = 64;                          // one 128-byte swizzle row of f16
+constexpr int kBRows = 256;                         // B rows per stage: token tile x planes
+constexpr int kBoxRows = 32;                        // rows per TMA box
+constexpr int kRawSlots = 8;
+constexpr int kStages = 2;
+constexpr int kRawSlot = 9216;                      // >= 8704 (Q8_0: 2 panels x (4096 + 256))
+constexpr int kATile = kTileM * kStepK * 2;         // 16 KB
+constexpr int kBTile = kBRows * kStepK * 2;         // 32 KB
+constexpr int kStageBytes = 2 * kATile + kBTile;    // A hi, A lo, B planes
+constexpr size_t kGemmSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
+                             static_cast<size_t>(kRawSlots) * kRawSlot;
+constexpr int kWarpLoadA = 0, kWarpLoadB = 1, kWarpMma = 2, kWarpEpi0 = 4, kWarpConv0 = 8;
+constexpr int kConvWarps = 8, kConvThreads = kConvWarps * 32;
 
 // ------------------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t s_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -47,17 +74,18 @@ __device__ __forceinline__ long long global_ns() {
     return t;
 }
 
-__device__ __forceinline__ void g_cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void g_cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void g_cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(s_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(s_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -70,13 +98,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for completion number n (0-based) of a barrier's phases, for at most kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t n) {
+    const uint32_t parity = n & 1u;
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
         if (global_ns() - t0 > kWaitLimitNs) return false;
     return true;
+}
+
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(s_addr(bar))
+                 : "memory");
+}
+
+// TMA 2-D tile load (coordinates: x = column, y = row), completion on `bar`.
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(s_addr(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -129,125 +174,147 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// ------------------------------------------------------------------------------ operands
+// f16 hi + lo of an fp32 value (hi + lo carries about 22 significant bits).
+__device__ __forceinline__ void split_f16(float v, __half* hi, __half* lo) {
+    *hi = __float2half_rn(v);
+    *lo = __float2half_rn(v - __half2float(*hi));
+}
+
+// ------------------------------------------------------------------------------ work items
 enum GemmKind { kGateUp = 0, kDown = 1 };
 
 struct GemmArgs {
+    CUtensorMap tb[2];   // B planes, f16 [P][K] (hi, lo), boxes of 64 columns x kBoxRows rows
     ExpertArgs a;
-    int kind;          // GemmKind
-    int fmt;           // MOE_W_Q8_0 / MOE_W_NVFP4
-    int act;           // MOE_ACT_* (gate.up)
+    int kind;            // GemmKind
+    int fmt;             // MOE_W_Q8_0 / MOE_W_NVFP4
+    int act;             // MOE_ACT_* (gate.up)
     int slot_cap;
+    int planes;          // 1 or 2
+    int nt_max;          // token tile: kBRows / planes
 };
 
-// Shared-memory plan of one CTA.  Raw slot: A raw bytes (<= 9 KB), then B raw rows
-// (<= 128 rows x 256 bytes).  MMA stage: A hi, A lo, B hi, B lo f16 tiles of 16 KB.
-constexpr int kRawA = 9216;
-constexpr int kRawB = kTileN * kStepK * 4;
-constexpr int kRawSlot = kRawA + kRawB;
-constexpr int kTileBytes = kTileM * kStepK * 2;     // 16 KB (A, or B with 128 rows)
-constexpr int kMmaStage = 4 * kTileBytes;
-constexpr size_t kGemmSmem = 1024 + static_cast<size_t>(kRaw) * kRawSlot + static_cast<size_t>(kStagesMma) * kMmaStage;
-
-// The rows of W one work item reads: SwiGLU gate.up tiles take 64 gate rows and the same 64
-// neurons' up rows (interleaved in the tile), everything else 128 consecutive rows.
-struct RowMap {
-    int gate0, up0;    // SwiGLU gate.up
-    int row0;          // others
-    bool swiglu;
+struct Item {
+    int e;               // expert
+    int r_first;         // first sorted row of the token tile
+    int nt;              // tokens in the tile (1..nt_max)
+    int mtile;           // row tile
 };
 
-// Copy the raw operands of K step `ks` into a raw slot (every thread issues its share).
-__device__ __forceinline__ void issue_raw(const GemmArgs& g, unsigned char* raw, const uint8_t* W, int rows_w,
-                                          const RowMap& rm, int ks, const int* tok, int nt, int r_first) {
-    const ExpertArgs& a = g.a;
-    const int tid = threadIdx.x;
-    unsigned char* ra = raw;
-    unsigned char* rb = raw + kRawA;
-    if (g.kind == kDown && g.fmt == MOE_W_NVFP4) {
-        // neuron layout: 4 groups of 16 neurons; per group 16 x (64 rows' 32 bytes) then 128 scale bytes
-        const int64_t rec = 16 * (a.d / 2) + a.d;
-        for (int c = tid; c < 4 * (16 * 4 + 8); c += kGemmThreads) {   // 16-byte chunks
-            const int grp = c / 72, rem = c % 72;
-            const uint8_t* base = W + (static_cast<int64_t>(ks) * 4 + grp) * rec;
-            if (rem < 64) {
-                const int n = rem / 4, q = rem % 4;                 // neuron n, rows 32q .. 32q+31 of the tile
-                g_cp_async16(s_addr(ra + grp * 1152 + n * 64 + q * 16), base + n * (a.d / 2) + rm.row0 / 2 + q * 16);
-            } else {
-                const int q = rem - 64;                             // 8 chunks = 128 scale bytes
-                g_cp_async16(s_addr(ra + grp * 1152 + 1024 + q * 16), base + 16 * (a.d / 2) + rm.row0 + q * 16);
-            }
-        }
-    } else {
-        // K panels: Q8_0 two panels of 32 columns, NVFP4 one panel of 64 columns
-        const int npanel = (g.fmt == MOE_W_Q8_0) ? 2 : 1;
-        const int64_t pbytes = static_cast<int64_t>(rows_w) * (g.fmt == MOE_W_Q8_0 ? 34 : 36);
-        const int scb = (g.fmt == MOE_W_Q8_0) ? 2 : 4;             // scale bytes per row per panel
-        const int per_panel = 128 * 32 / 16 + 128 * scb / 16;       // 16-byte chunks
-        for (int c = tid; c < npanel * per_panel; c += kGemmThreads) {
-            const int p = c / per_panel, rem = c % per_panel;
-            const uint8_t* P = W + (static_cast<int64_t>(ks) * npanel + p) * pbytes;
-            unsigned char* dst = ra + p * (128 * 32 + 128 * 4);
-            if (rem < 256) {       // codes: 128 rows x 32 bytes, 2 chunks per row
-                const int r = rem / 2, h = rem % 2;
-                const int src_row = rm.swiglu ? ((r < 64) ? rm.gate0 + r : rm.up0 + r - 64) : rm.row0 + r;
-                g_cp_async16(s_addr(dst + r * 32 + h * 16), P + static_cast<int64_t>(src_row) * 32 + h * 16);
-            } else {               // scales of the same 128 rows (two runs of 64 for SwiGLU)
-                const int q = rem - 256;
-                const int run_chunks = 64 * scb / 16;
-                const int half = q / run_chunks, qi = q % run_chunks;
-                const int src_row = rm.swiglu ? (half == 0 ? rm.gate0 : rm.up0) : rm.row0 + 64 * half;
-                g_cp_async16(s_addr(dst + 128 * 32 + half * 64 * scb + qi * 16),
-                             P + static_cast<int64_t>(rows_w) * 32 + static_cast<int64_t>(src_row) * scb + qi * 16);
-            }
-        }
+__device__ __forceinline__ Item decode_item(const GemmArgs& g, const int* tile_prefix, int mtiles, int item) {
+    int lo = 0, hi = g.slot_cap - 1;
+    while (lo < hi) {   // last slot whose first item is <= item
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_prefix[mid] <= item) lo = mid;
+        else hi = mid - 1;
     }
-    // activations: gate.up reads x rows (bf16: 128 B per step, fp32: 256 B), down reads h rows (fp32)
-    const bool f32 = (g.kind == kDown) || a.xt == MOE_F32;
-    const int rowbytes = f32 ? 256 : 128;
-    const int cpr = rowbytes / 16;
-    for (int c = tid; c < nt * cpr; c += kGemmThreads) {
-        const int n = c / cpr, q = c % cpr;
-        const unsigned char* src;
-        if (g.kind == kDown) {
-            src = reinterpret_cast<const unsigned char*>(a.ws.h + static_cast<int64_t>(r_first + n) * a.f + ks * kStepK) + q * 16;
-        } else if (a.xt == MOE_F32) {
-            src = reinterpret_cast<const unsigned char*>(static_cast<const float*>(a.x) + static_cast<int64_t>(tok[n]) * a.d + ks * kStepK) + q * 16;
-        } else {
-            src = reinterpret_cast<const unsigned char*>(static_cast<const uint16_t*>(a.x) + static_cast<int64_t>(tok[n]) * a.d + ks * kStepK) + q * 16;
+    const int4 si = __ldcg(g.a.ws.slot_info + lo);
+    const int local = item - tile_prefix[lo];
+    const int ntile = local / mtiles;
+    Item it;
+    it.e = si.x;
+    it.mtile = local - ntile * mtiles;
+    it.r_first = si.y + ntile * g.nt_max;
+    it.nt = min(g.nt_max, si.z - ntile * g.nt_max);
+    return it;
+}
+
+// Raw bytes of one K step of the weights.
+__device__ __forceinline__ uint32_t raw_step_bytes(const GemmArgs& g) {
+    return (g.fmt == MOE_W_Q8_0) ? 2u * (4096u + 256u) : 4096u + 512u;
+}
+
+// The weight producer's copies of K step ks for row tile `mtile` of expert matrix W
+// (lane-strided).  Raw slot layout: Q8_0 two panels of 32 columns, each [128 rows][32 codes]
+// then [128][2-byte scale] at 4608-byte spacing; NVFP4 one panel of 64 columns, [128][32
+// code bytes] then [128][4 scale bytes]; NVFP4 down (neuron layout) four 16-neuron groups
+// at 1152-byte spacing, each [16 neurons][64 bytes = 128 rows' nibbles] then [128 scales].
+// SwiGLU gate.up tiles stage gate rows in rows 0..63 and the same neurons' up rows in 64..127.
+__device__ __forceinline__ void issue_weights(const GemmArgs& g, uint32_t slot_addr, const uint8_t* W, int rows_w,
+                                              int mtile, int ks, uint64_t* bar, int lane) {
+    const ExpertArgs& a = g.a;
+    const bool swiglu = (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU);
+    if (g.kind == kDown && g.fmt == MOE_W_NVFP4) {
+        const int64_t rec = 16 * static_cast<int64_t>(a.d / 2) + a.d;   // one 16-neuron group record
+        const int row0 = mtile * kTileM;
+        for (int c = lane; c < 4 * 17; c += 32) {
+            const int grp = c / 17, n = c % 17;
+            const uint8_t* base = W + (static_cast<int64_t>(ks) * 4 + grp) * rec;
+            if (n < 16)
+                bulk_g2s(slot_addr + grp * 1152 + n * 64, base + static_cast<int64_t>(n) * (a.d / 2) + row0 / 2, 64, bar);
+            else
+                bulk_g2s(slot_addr + grp * 1152 + 1024, base + 16 * static_cast<int64_t>(a.d / 2) + row0, 128, bar);
         }
-        g_cp_async16(s_addr(rb + n * rowbytes + q * 16), src);
+        return;
+    }
+    const bool q8 = (g.fmt == MOE_W_Q8_0);
+    const int npanel = q8 ? 2 : 1;
+    const int scb = q8 ? 2 : 4;                                  // scale bytes per row per panel
+    const int64_t pbytes = static_cast<int64_t>(rows_w) * (q8 ? 34 : 36);
+    const int runs = swiglu ? 2 : 1;                             // row runs per panel
+    const int run_rows = kTileM / runs;
+    const int ncopies = npanel * runs * 2;
+    for (int c = lane; c < ncopies; c += 32) {
+        const int p = c / (runs * 2), rem = c % (runs * 2);
+        const int run = rem >> 1, is_scale = rem & 1;
+        const int src_row = swiglu ? (run == 0 ? mtile * 64 : a.f + mtile * 64) : mtile * kTileM;
+        const uint8_t* P = W + (static_cast<int64_t>(ks) * npanel + p) * pbytes;
+        const uint32_t dst = slot_addr + p * 4608;
+        if (!is_scale)
+            bulk_g2s(dst + run * run_rows * 32, P + static_cast<int64_t>(src_row) * 32, run_rows * 32, bar);
+        else
+            bulk_g2s(dst + 4096 + run * run_rows * scb, P + static_cast<int64_t>(rows_w) * 32 + src_row * scb,
+                     run_rows * scb, bar);
     }
 }
 
-// Dequantise / convert one K step from a raw slot into an MMA stage.
-__device__ __forceinline__ void convert_step(const GemmArgs& g, const unsigned char* raw, unsigned char* st, int nt,
-                                             int n16, bool split) {
-    const ExpertArgs& a = g.a;
-    const int tid = threadIdx.x;
-    const unsigned char* ra = raw;
-    const unsigned char* rb = raw + kRawA;
-    unsigned char* ta = st;
-    unsigned char* tal = st + kTileBytes;
-    unsigned char* tb = st + 2 * kTileBytes;
-    unsigned char* tl = st + 3 * kTileBytes;
-    // A: 128 tile rows x 4 chunks of 16 columns
-    for (int u = tid; u < kTileM * 4; u += kGemmThreads) {
-        const int r = u >> 2, c16 = u & 3;
-        // tile row r <- staged row: SwiGLU interleaves gate (staged 0..63) and up (staged 64..127)
-        const int sr = (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU) ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
-        uint32_t h[8], hl[8];
-        if (g.kind == kDown && g.fmt == MOE_W_NVFP4) {
-            // columns 16*c16 .. +15 are group c16 (16 neurons) of this step; row sr
-            const unsigned char* gb = ra + c16 * 1152;
-            const uint32_t sbyte = gb[1024 + sr];
+// Dequantise one K step from a raw slot into the A hi (and, for Q8_0, lo) tiles.
+__device__ __forceinline__ void dequant_step(const GemmArgs& g, const unsigned char* raw, unsigned char* ta,
+                                             unsigned char* tal, int ct) {
+    const bool swiglu = (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU);
+#pragma unroll
+    for (int i = 0; i < (kTileM * 4) / kConvThreads; ++i) {
+        const int u = ct + i * kConvThreads;
+        const int r = u >> 2, c16 = u & 3;              // tile row, 16-column chunk
+        const int sr = swiglu ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;   // staged row
+        uint32_t h[8];
+        if (g.fmt == MOE_W_Q8_0) {
+            const int p = c16 >> 1, hh = c16 & 1;       // panel of 32 columns, half
+            const unsigned char* pan = raw + p * 4608;
+            const uint4 q = *reinterpret_cast<const uint4*>(pan + sr * 32 + hh * 16);
+            const unsigned short sbits = *reinterpret_cast<const unsigned short*>(pan + 4096 + sr * 2);
+            const __half2 s2 = __halves2half2(__ushort_as_half(sbits), __ushort_as_half(sbits));
+            const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+            uint32_t hl[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // int8 codes -> exact f16: bytes XOR 0x80 placed under exponent 0x64 give
+                // 1024 + 128 + q; subtracting 1152 (0x6480) leaves q
+                const uint32_t u8 = w4[j] ^ 0x80808080u;
+                const uint32_t b01 = __byte_perm(u8, 0x64646464u, 0x4140);
+                const uint32_t b23 = __byte_perm(u8, 0x64646464u, 0x4342);
+                const __half2 q01 = __hsub2(*reinterpret_cast<const __half2*>(&b01), off);
+                const __half2 q23 = __hsub2(*reinterpret_cast<const __half2*>(&b23), off);
+                const __half2 v01 = __hmul2(q01, s2), v23 = __hmul2(q23, s2);
+                const __half2 l01 = __hfma2(q01, s2, __hneg2(v01)), l23 = __hfma2(q23, s2, __hneg2(v23));
+                h[2 * j] = *reinterpret_cast<const uint32_t*>(&v01);
+                h[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&v23);
+                hl[2 * j] = *reinterpret_cast<const uint32_t*>(&l01);
+                hl[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&l23);
+            }
+            *reinterpret_cast<uint4*>(tal + swz(r, 2 * c16)) = make_uint4(hl[0], hl[1], hl[2], hl[3]);
+            *reinterpret_cast<uint4*>(tal + swz(r, 2 * c16 + 1)) = make_uint4(hl[4], hl[5], hl[6], hl[7]);
+        } else if (g.kind == kDown) {
+            // NVFP4 neuron layout: columns 16*c16 .. +15 are group c16; row sr is nibble
+            // (sr & 1) of byte sr/2 in each neuron's run
+            const unsigned char* gb = raw + c16 * 1152;
             uint32_t s16;
-            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(static_cast<uint16_t>(sbyte)));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(static_cast<uint16_t>(gb[1024 + sr])));
             const __half sh = __ushort_as_half(static_cast<unsigned short>(s16 & 0xffffu));
             const __half2 s2 = __halves2half2(sh, sh);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                // neurons 2j, 2j+1: nibble (sr & 1) of byte sr/2 in each neuron's row run
                 const uint32_t b0 = gb[(2 * j) * 64 + (sr >> 1)];
                 const uint32_t b1 = gb[(2 * j + 1) * 64 + (sr >> 1)];
                 const uint32_t n0 = (sr & 1) ? (b0 >> 4) : (b0 & 0xfu);
@@ -257,35 +324,11 @@ __device__ __forceinline__ void convert_step(const GemmArgs& g, const unsigned c
                 const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), s2);
                 h[j] = *reinterpret_cast<const uint32_t*>(&v);
             }
-        } else if (g.fmt == MOE_W_Q8_0) {
-            const int p = c16 >> 1, hh = c16 & 1;              // panel of 32 columns, half
-            const unsigned char* pan = ra + p * (128 * 32 + 128 * 4);
-            const uint4 q = *reinterpret_cast<const uint4*>(pan + sr * 32 + hh * 16);
-            const unsigned short sbits = *reinterpret_cast<const unsigned short*>(pan + 128 * 32 + sr * 2);
-            const __half2 s2 = __halves2half2(__ushort_as_half(sbits), __ushort_as_half(sbits));
-            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t u8 = w4[i] ^ 0x80808080u;
-                const uint32_t lo = __byte_perm(u8, 0x64646464u, 0x4140);
-                const uint32_t hi = __byte_perm(u8, 0x64646464u, 0x4342);
-                const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-                const __half2 ql = __hsub2(*reinterpret_cast<const __half2*>(&lo), off);   // exact codes
-                const __half2 qh = __hsub2(*reinterpret_cast<const __half2*>(&hi), off);
-                const __half2 lv = __hmul2(ql, s2), hv = __hmul2(qh, s2);
-                const __half2 lr = __hfma2(ql, s2, __hneg2(lv)), hr = __hfma2(qh, s2, __hneg2(hv));
-                h[2 * i] = *reinterpret_cast<const uint32_t*>(&lv);
-                h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hv);
-                hl[2 * i] = *reinterpret_cast<const uint32_t*>(&lr);
-                hl[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hr);
-            }
-            *reinterpret_cast<uint4*>(tal + swz(r, 2 * c16)) = make_uint4(hl[0], hl[1], hl[2], hl[3]);
-            *reinterpret_cast<uint4*>(tal + swz(r, 2 * c16 + 1)) = make_uint4(hl[4], hl[5], hl[6], hl[7]);
-        } else {   // NVFP4 K panel of 64 columns: 32 code bytes, 4 scale bytes per row
-            const uint2 cw = *reinterpret_cast<const uint2*>(ra + sr * 32 + c16 * 8);
-            const uint32_t sbyte = ra[128 * 32 + sr * 4 + c16];
+        } else {
+            // NVFP4 panel of 64 columns: 32 code bytes, 4 scale bytes per row
+            const uint2 cw = *reinterpret_cast<const uint2*>(raw + sr * 32 + c16 * 8);
             uint32_t s16;
-            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(static_cast<uint16_t>(sbyte)));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(static_cast<uint16_t>(raw[4096 + sr * 4 + c16])));
             const __half sh = __ushort_as_half(static_cast<unsigned short>(s16 & 0xffffu));
             const __half2 s2 = __halves2half2(sh, sh);
             const uint32_t w2[2] = {cw.x, cw.y};
@@ -301,69 +344,50 @@ __device__ __forceinline__ void convert_step(const GemmArgs& g, const unsigned c
         *reinterpret_cast<uint4*>(ta + swz(r, 2 * c16)) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4*>(ta + swz(r, 2 * c16 + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
     }
-    // B: n16 rows (tokens) x 8 chunks of 8 columns; rows >= nt are zero
-    const bool f32 = (g.kind == kDown) || a.xt == MOE_F32;
-    for (int u = tid; u < n16 * 8; u += kGemmThreads) {
-        const int n = u >> 3, c = u & 7;
-        uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-        if (n < nt) {
-            if (f32) {
-                const float4 v0 = *reinterpret_cast<const float4*>(rb + n * 256 + c * 32);
-                const float4 v1 = *reinterpret_cast<const float4*>(rb + n * 256 + c * 32 + 16);
-                const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const __half2 hh = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-                    const float2 hf = __half22float2(hh);
-                    const __half2 ll = __floats2half2_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
-                    hw[i] = *reinterpret_cast<const uint32_t*>(&hh);
-                    lw[i] = *reinterpret_cast<const uint32_t*>(&ll);
-                }
-                hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            } else {
-                const uint4 b = *reinterpret_cast<const uint4*>(rb + n * 128 + c * 16);
-                const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-                uint32_t hw[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float f0 = __uint_as_float(bw[i] << 16), f1 = __uint_as_float(bw[i] & 0xffff0000u);
-                    const __half2 hh = __floats2half2_rn(f0, f1);
-                    hw[i] = *reinterpret_cast<const uint32_t*>(&hh);
-                }
-                hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            }
-        }
-        *reinterpret_cast<uint4*>(tb + swz(n, c)) = hi;
-        if (split) *reinterpret_cast<uint4*>(tl + swz(n, c)) = lo;
-    }
 }
 
 // ------------------------------------------------------------------------------ the kernel
-__global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(GemmArgs g) {
+__global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __grid_constant__ GemmArgs g) {
     pdl_wait();
     const ExpertArgs& a = g.a;
     extern __shared__ __align__(16) unsigned char dsm_raw[];
-    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char* rawring = base;
-    unsigned char* stages = base + kRaw * kRawSlot;     // kRawSlot is a multiple of 1024
-    __shared__ uint64_t bar[kStagesMma];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    unsigned char* stages = base;                               // kStages x (A hi, A lo, B)
+    unsigned char* raws = base + kStages * kStageBytes;         // kRawSlots x kRawSlot
+    __shared__ uint64_t raw_full[kRawSlots], raw_empty[kRawSlots];
+    __shared__ uint64_t a_full[kStages], b_full[kStages], st_empty[kStages];
+    __shared__ uint64_t acc_full[2], acc_empty[2];
+    __shared__ uint32_t raw_issued[kRawSlots], b_issued[kStages], mma_commits[kStages];
     __shared__ uint32_t tmem_base;
     __shared__ int tile_prefix[kMaxE + 1];
-    __shared__ int tok[kTileN];
-    __shared__ int warp_sum[kGemmThreads / 32];
-    __shared__ int s_fail;
+    __shared__ int warp_tot[kGemmThreads / 32];
+    __shared__ volatile int s_fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t tmem_cols = static_cast<uint32_t>(2 * g.nt_max);   // two accumulators
 
-    // tensor memory: 128 columns (kTileN fp32 accumulators per lane)
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s_addr(&tmem_base)),
-                     "r"(kTileN));
+                     "r"(tmem_cols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) {
-        for (int s = 0; s < kStagesMma; ++s) mbar_init(&bar[s], 1);
+        for (int s = 0; s < kRawSlots; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], kConvWarps);
+            raw_issued[s] = 0;
+        }
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&a_full[s], kConvWarps);
+            mbar_init(&b_full[s], 1);
+            mbar_init(&st_empty[s], 1);
+            b_issued[s] = 0;
+            mma_commits[s] = 0;
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], 4);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_fail = 0;
     }
@@ -371,16 +395,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(GemmArgs g
     const int rows_out = (g.kind == kGateUp) ? a.rows_gu : a.d;
     const int mtiles = rows_out / kTileM;
     {
-        const int per = (g.slot_cap + kGemmThreads - 1) / kGemmThreads;   // consecutive slots per thread
+        const int per = (g.slot_cap + kGemmThreads - 1) / kGemmThreads;   // <= 2 (slot_cap <= 1024)
         const int s0 = tid * per;
-        int cnts[4];   // slot_cap <= 1024 = 4 * 256
+        int cnts[2] = {0, 0};
         int local = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            cnts[i] = 0;
+        for (int i = 0; i < 2; ++i) {
             if (i < per && s0 + i < g.slot_cap) {
                 const int c = __ldcg(&a.ws.slot_info[s0 + i].z);
-                cnts[i] = ((c + kTileN - 1) / kTileN) * mtiles;
+                cnts[i] = ((c + g.nt_max - 1) / g.nt_max) * mtiles;
             }
             local += cnts[i];
         }
@@ -390,13 +413,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(GemmArgs g
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        if (lane == 31) warp_sum[warp] = incl;
+        if (lane == 31) warp_tot[warp] = incl;
         __syncthreads();
-        int before = 0;
-        for (int w = 0; w < warp; ++w) before += warp_sum[w];
-        int run = before + incl - local;
+        int run = incl - local;
+        for (int w = 0; w < warp; ++w) run += warp_tot[w];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             if (i < per && s0 + i < g.slot_cap) tile_prefix[s0 + i] = run;
             run += cnts[i];
         }
@@ -408,147 +430,352 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(GemmArgs g
     const uint32_t tmem = tmem_base;
     const int total = tile_prefix[g.slot_cap];
     const int ksteps = ((g.kind == kGateUp) ? a.d : a.f) / kStepK;
-    const bool split = (g.kind == kDown) || a.xt == MOE_F32;   // fp32 operands: hi + lo
-    const bool alo = (g.fmt == MOE_W_Q8_0);                      // Q8_0 weights: hi + lo
-    uint32_t mma_count = 0;   // commits issued by this CTA (stage = count % kStagesMma)
+    const int rows_w = (g.kind == kGateUp) ? a.rows_gu : a.d;
 
-    for (int item = blockIdx.x; item < total && !s_fail; item += gridDim.x) {
-        // decode (slot, token tile, row tile)
-        int lo = 0, hi = g.slot_cap - 1;
-        while (lo < hi) {   // last slot with prefix <= item
-            const int mid = (lo + hi + 1) >> 1;
-            if (tile_prefix[mid] <= item) lo = mid;
-            else hi = mid - 1;
-        }
-        const int slot = lo;
-        const int4 si = __ldcg(a.ws.slot_info + slot);
-        const int local = item - tile_prefix[slot];
-        const int ntile = local / mtiles, mtile = local % mtiles;
-        const int e = si.x, r0 = si.y;
-        const int t0 = ntile * kTileN;
-        const int nt = min(kTileN, si.z - t0);
-        const int n16 = (nt + 15) & ~15;
-        const int r_first = r0 + t0;
-        RowMap rm;
-        rm.swiglu = (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU);
-        rm.gate0 = mtile * 64;
-        rm.up0 = a.f + mtile * 64;
-        rm.row0 = mtile * kTileM;
-        const uint8_t* W = (g.kind == kGateUp) ? a.w_gu + static_cast<int64_t>(e) * a.gu_bytes
-                                               : a.w_dn + static_cast<int64_t>(e) * a.dn_bytes;
-        const int rows_w = (g.kind == kGateUp) ? a.rows_gu : a.d;
-        if (g.kind == kGateUp)
-            for (int n = tid; n < nt; n += kGemmThreads) tok[n] = slot_token(si, t0 + n, a.ws.perm, a.k);
-        __syncthreads();
-        // prologue of the raw ring
-#pragma unroll
-        for (int s = 0; s < kRaw; ++s) {
-            if (s < ksteps) issue_raw(g, rawring + s * kRawSlot, W, rows_w, rm, s, tok, nt, r_first);
-            g_cp_async_commit();
-        }
-        const uint32_t idesc = idesc_f16(n16);
-        for (int ks = 0; ks < ksteps; ++ks) {
-            g_cp_async_wait<kRaw - 1>();
-            __syncthreads();
-            const uint32_t c = mma_count + ks;
-            const int st = c % kStagesMma;
-            unsigned char* stg = stages + st * kMmaStage;
-            if (c >= kStagesMma) {   // the MMAs that last read this stage are done
-                if (!mbar_wait_bounded(&bar[st], ((c / kStagesMma) - 1) & 1)) s_fail = 1;
-            }
-            convert_step(g, rawring + (ks % kRaw) * kRawSlot, stg, nt, n16, split);
-            proxy_fence_smem();
-            __syncthreads();
-            if (s_fail) break;
-            if (ks + kRaw < ksteps)
-                issue_raw(g, rawring + (ks % kRaw) * kRawSlot, W, rows_w, rm, ks + kRaw, tok, nt, r_first);
-            g_cp_async_commit();
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t sa = s_addr(stg), sal = s_addr(stg + kTileBytes);
-                const uint32_t sb = s_addr(stg + 2 * kTileBytes), sl = s_addr(stg + 3 * kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < kStepK / 16; ++kk) {
-                    umma_f16(tmem, sdesc_k128(sa + kk * 32), sdesc_k128(sb + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-                    if (alo) umma_f16(tmem, sdesc_k128(sal + kk * 32), sdesc_k128(sb + kk * 32), idesc, 1u);
-                    if (split) umma_f16(tmem, sdesc_k128(sa + kk * 32), sdesc_k128(sl + kk * 32), idesc, 1u);
+    if (warp == kWarpLoadA) {
+        // ---------------------------------------------------------------- weight producer
+        const uint32_t bytes = raw_step_bytes(g);
+        uint32_t gs = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            const Item it = decode_item(g, tile_prefix, mtiles, item);
+            const uint8_t* W = (g.kind == kGateUp) ? a.w_gu + static_cast<int64_t>(it.e) * a.gu_bytes
+                                                   : a.w_dn + static_cast<int64_t>(it.e) * a.dn_bytes;
+            for (int ks = 0; ks < ksteps; ++ks, ++gs) {
+                const int slot = gs % kRawSlots;
+                const uint32_t use = gs / kRawSlots;
+                bool w_ok = (use == 0) || mbar_wait(&raw_empty[slot], use - 1);
+                w_ok = __all_sync(0xffffffffu, w_ok) && !s_fail;
+                if (!w_ok) {
+                    ok = false;
+                    break;
                 }
-                umma_commit(&bar[st]);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&raw_full[slot], bytes);
+                    raw_issued[slot] = use + 1;
+                }
+                __syncwarp();
+                issue_weights(g, s_addr(raws + slot * kRawSlot), W, rows_w, it.mtile, ks, &raw_full[slot], lane);
             }
         }
-        g_cp_async_wait<0>();
-        __syncthreads();
-        if (s_fail) break;
-        // wait for the item's last commit: every MMA of the item has completed
-        {
-            const uint32_t c = mma_count + ksteps - 1;
-            if (!mbar_wait_bounded(&bar[c % kStagesMma], (c / kStagesMma) & 1)) s_fail = 1;
+        if (!ok && lane == 0) {
+            s_fail = 1;
+            atomicCAS(a.ws.err, 0, kDevErrTimeout);
         }
-        mma_count += ksteps;
-        tc_fence_after();
-        __syncthreads();
-        if (s_fail) break;
-        // epilogue: warp w reads lanes 32*(w%4).. and columns [(w/4)*64, +64) of the accumulator
-        const int q = warp & 3, half = warp >> 2;
-        const int row = q * 32 + lane;   // accumulator row = tile row
-        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-            if (c0 >= n16) break;
-            float v[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c0), v);
-            if (g.kind == kGateUp) {
-                const float ts = (g.fmt == MOE_W_NVFP4) ? a.gu_ts[e] : 1.0f;
+    } else if (warp == kWarpLoadB) {
+        // ---------------------------------------------------------------- activation producer
+        if (lane == 0) {
+            uint32_t gs = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                const Item it = decode_item(g, tile_prefix, mtiles, item);
+                const int nbox = (it.nt + kBoxRows - 1) / kBoxRows;
+                const uint32_t bytes = static_cast<uint32_t>(nbox * kBoxRows * 128 * g.planes);
+                for (int ks = 0; ks < ksteps; ++ks, ++gs) {
+                    const int st = gs % kStages;
+                    const uint32_t use = gs / kStages;
+                    if ((use > 0 && !mbar_wait(&st_empty[st], use - 1)) || s_fail) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&b_full[st], bytes);
+                    b_issued[st] = use + 1;
+                    const uint32_t bdst = s_addr(stages + st * kStageBytes + 2 * kATile);
+                    for (int p = 0; p < g.planes; ++p)
+                        for (int j = 0; j < nbox; ++j)
+                            tma_2d(bdst + p * g.nt_max * 128 + j * kBoxRows * 128, &g.tb[p], ks * kStepK,
+                                   it.r_first + j * kBoxRows, &b_full[st]);
+                }
+            }
+            if (!ok) {
+                s_fail = 1;
+                atomicCAS(a.ws.err, 0, kDevErrTimeout);
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const bool alo = (g.fmt == MOE_W_Q8_0);
+            uint32_t gs = 0, n_item = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++n_item) {
+                const Item it = decode_item(g, tile_prefix, mtiles, item);
+                const int n16 = (it.nt + 15) & ~15;
+                const uint32_t idesc = idesc_f16(n16);
+                const int buf = n_item & 1;
+                const uint32_t ub = n_item >> 1;
+                if ((ub > 0 && !mbar_wait(&acc_empty[buf], ub - 1)) || s_fail) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dt = tmem + static_cast<uint32_t>(buf * g.nt_max);
+                for (int ks = 0; ks < ksteps; ++ks, ++gs) {
+                    const int st = gs % kStages;
+                    const uint32_t use = gs / kStages;
+                    if (!mbar_wait(&a_full[st], use) || !mbar_wait(&b_full[st], use) || s_fail) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = s_addr(stages + st * kStageBytes);
+                    const uint32_t sal = sa + kATile;
+                    const uint32_t sb = sa + 2 * kATile;
+                    const uint32_t sbl = sb + g.nt_max * 128;
+#pragma unroll
+                    for (int kk = 0; kk < kStepK / 16; ++kk) {
+                        umma_f16(dt, sdesc_k128(sa + kk * 32), sdesc_k128(sb + kk * 32), idesc, (ks | kk) ? 1u : 0u);
+                        if (alo) umma_f16(dt, sdesc_k128(sal + kk * 32), sdesc_k128(sb + kk * 32), idesc, 1u);
+                        if (g.planes == 2) umma_f16(dt, sdesc_k128(sa + kk * 32), sdesc_k128(sbl + kk * 32), idesc, 1u);
+                    }
+                    umma_commit(&st_empty[st]);
+                    mma_commits[st] = use + 1;
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[buf]);
+            }
+            if (!ok) {
+                s_fail = 1;
+                atomicCAS(a.ws.err, 0, kDevErrTimeout);
+            }
+        }
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+        // ---------------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;                 // accumulator lane = tile row
+        const float* ts_arr = (g.kind == kGateUp) ? a.gu_ts : a.dn_ts;
+        uint32_t n_item = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total; item += gridDim.x, ++n_item) {
+            const Item it = decode_item(g, tile_prefix, mtiles, item);
+            const int n16 = (it.nt + 15) & ~15;
+            const int buf = n_item & 1;
+            bool w_ok = mbar_wait(&acc_full[buf], n_item >> 1);
+            w_ok = __all_sync(0xffffffffu, w_ok) && !s_fail;
+            if (!w_ok) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float ts = (g.fmt == MOE_W_NVFP4) ? ts_arr[it.e] : 1.0f;
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * g.nt_max);
+            bool range_ok = true;
+            for (int c0 = 0; c0 < n16; c0 += 16) {
+                float v[16];
+                tmem_ld16(tbase + static_cast<uint32_t>(c0), v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int n = c0 + j;
-                    float z = v[j] * ts;
-                    if (g.act == MOE_ACT_SWIGLU) {
-                        const float u = __shfl_xor_sync(0xffffffffu, z, 1);   // odd lane holds the up row
-                        if (!(lane & 1) && n < nt)
-                            a.ws.h[static_cast<int64_t>(r_first + n) * a.f + mtile * 64 + (row >> 1)] = silu(z) * u;
-                    } else if (n < nt) {
-                        a.ws.h[static_cast<int64_t>(r_first + n) * a.f + mtile * kTileM + row] = z > 0.0f ? z * z : 0.0f;
+                    const int64_t prow = static_cast<int64_t>(it.r_first + n);
+                    const float z = v[j] * ts;
+                    if (g.kind == kGateUp) {
+                        float hv;
+                        int64_t col;
+                        bool store;
+                        if (g.act == MOE_ACT_SWIGLU) {
+                            const float u = __shfl_xor_sync(0xffffffffu, z, 1);   // odd lanes hold the up rows
+                            hv = silu(z) * u;
+                            col = it.mtile * 64 + (row >> 1);
+                            store = !(lane & 1) && n < it.nt;
+                        } else {
+                            hv = z > 0.0f ? z * z : 0.0f;
+                            col = it.mtile * kTileM + row;
+                            store = n < it.nt;
+                        }
+                        if (store) {
+                            const int64_t o = prow * a.f + col;
+                            a.ws.h[o] = hv;
+                            __half hh, hl;
+                            split_f16(hv, &hh, &hl);
+                            range_ok &= fabsf(hv) <= 65504.0f;
+                            a.ws.h_hi[o] = __half_as_ushort(hh);
+                            a.ws.h_lo[o] = __half_as_ushort(hl);
+                        }
+                    } else if (n < it.nt) {
+                        a.ws.y[prow * a.d + it.mtile * kTileM + row] = z;
                     }
                 }
-            } else {
-                const float ts = (g.fmt == MOE_W_NVFP4) ? a.dn_ts[e] : 1.0f;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int n = c0 + j;
-                    if (n < nt) a.ws.y[static_cast<int64_t>(r_first + n) * a.d + mtile * kTileM + row] = v[j] * ts;
-                }
+            }
+            if (!range_ok) atomicCAS(a.ws.err, 0, kDevErrF16Range);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        if (!ok && lane == 0) {
+            s_fail = 1;
+            atomicCAS(a.ws.err, 0, kDevErrTimeout);
+        }
+    } else if (warp >= kWarpConv0) {
+        // ---------------------------------------------------------------- dequantisers
+        const int ct = tid - kWarpConv0 * 32;
+        int my_items = 0;
+        for (int item = blockIdx.x; item < total; item += gridDim.x) ++my_items;
+        const uint32_t nsteps = static_cast<uint32_t>(my_items) * ksteps;
+        bool ok = true;
+        for (uint32_t gs = 0; gs < nsteps; ++gs) {
+            const int slot = gs % kRawSlots;
+            const int st = gs % kStages;
+            const uint32_t use = gs / kStages;
+            bool w_ok = mbar_wait(&raw_full[slot], gs / kRawSlots);
+            w_ok = w_ok && (use == 0 || mbar_wait(&st_empty[st], use - 1));
+            w_ok = __all_sync(0xffffffffu, w_ok) && !s_fail;
+            if (!w_ok) {
+                ok = false;
+                break;
+            }
+            unsigned char* sa = stages + st * kStageBytes;
+            dequant_step(g, raws + slot * kRawSlot, sa, sa + kATile, ct);
+            proxy_fence_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&a_full[st]);
+                mbar_arrive(&raw_empty[slot]);
             }
         }
-        tc_fence_before();
-        __syncthreads();   // accumulator reads finished before the next item's MMAs
+        if (!ok && lane == 0) {
+            s_fail = 1;
+            atomicCAS(a.ws.err, 0, kDevErrTimeout);
+        }
     }
-    if (s_fail && tid == 0) atomicCAS(a.ws.err, 0, kDevErrTimeout);
-    g_cp_async_wait<0>();
+
+    // drain: every copy and MMA this CTA issued has landed before shared and tensor memory
+    // are given back (immediate on the normal path; bounded after a timeout)
+    __syncthreads();
+    if (tid == 0) {
+        bool ok = true;
+        for (int s = 0; s < kRawSlots; ++s)
+            if (raw_issued[s]) ok &= mbar_wait(&raw_full[s], raw_issued[s] - 1);
+        for (int s = 0; s < kStages; ++s) {
+            if (b_issued[s]) ok &= mbar_wait(&b_full[s], b_issued[s] - 1);
+            if (mma_commits[s]) ok &= mbar_wait(&st_empty[s], mma_commits[s] - 1);
+        }
+        if (!ok) atomicCAS(a.ws.err, 0, kDevErrTimeout);
+    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTileN));
+    tc_fence_after();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols));
 }
 
-// ------------------------------------------------------------------------------ launchers
+// f16 B planes of the gate.up GEMM: x rows in sorted-row order (hi = f16(x); for fp32 x
+// also lo = f16(x - hi)).  One thread per 8 elements, grid-stride.
+__global__ void __launch_bounds__(256) gather_x_f16_kernel(const void* __restrict__ x, int xt, int d, int k,
+                                                           int64_t P, const int32_t* __restrict__ perm,
+                                                           uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
+                                                           int32_t* err) {
+    pdl_wait();
+    pdl_trigger();
+    const int cpr = d / 8;
+    const int64_t total = P * cpr;
+    bool range_ok = true;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t p = i / cpr;
+        const int c = static_cast<int>(i - p * cpr);
+        const int64_t t = __ldg(perm + p) / k;
+        float v[8];
+        if (xt == MOE_F32) {
+            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + t * d) + 2 * c;
+            const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+            v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+            v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+        } else {
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + t * d) + c);
+            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[2 * j] = __uint_as_float(bw[j] << 16);
+                v[2 * j + 1] = __uint_as_float(bw[j] & 0xffff0000u);
+            }
+        }
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __half h0, l0, h1, l1;
+            split_f16(v[2 * j], &h0, &l0);
+            split_f16(v[2 * j + 1], &h1, &l1);
+            range_ok &= fabsf(v[2 * j]) <= 65504.0f && fabsf(v[2 * j + 1]) <= 65504.0f;
+            hw[j] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+            lw[j] = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+        }
+        reinterpret_cast<uint4*>(hi + p * d)[c] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (xt == MOE_F32) reinterpret_cast<uint4*>(lo + p * d)[c] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    if (!range_ok) atomicCAS(err, 0, kDevErrF16Range);
+}
+
+// ------------------------------------------------------------------------------ host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encoder() {
+    static std::once_flag once;
+    static cudaError_t status = cudaSuccess;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (status == cudaSuccess && (q != cudaDriverEntryPointSuccess || fn == nullptr)) status = cudaErrorNotSupported;
+        if (status == cudaSuccess) g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return status;
+}
+
+// Tensor map of an f16 plane [rows][cols] (row stride cols*2 bytes), boxes of 64 columns x
+// kBoxRows rows, 128-byte swizzle; rows past the end read as zero.
+cudaError_t plane_map(CUtensorMap* m, const uint16_t* base, int64_t rows, int64_t cols) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStepK), static_cast<cuuint32_t>(kBoxRows)};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box,
+                                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t configure_gemm_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kGemmSmem));
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kGemmSmem));
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }
 
 size_t gemm_smem_bytes() { return kGemmSmem; }
 
+cudaError_t launch_gather_x_f16(const ExpertArgs& a, int num_sms, cudaStream_t s) {
+    const int64_t total = static_cast<int64_t>(a.P) * (a.d / 8);
+    const int64_t want = (total + 255) / 256;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(num_sms) * 8)));
+    return launch_pdl(gather_x_f16_kernel, dim3(grid), dim3(256), 0, s, a.x, a.xt, a.d, a.k,
+                      static_cast<int64_t>(a.P), static_cast<const int32_t*>(a.ws.perm), a.ws.xs_hi, a.ws.xs_lo,
+                      a.ws.err);
+}
+
 cudaError_t launch_expert_gemm(const ExpertArgs& a, int kind, int wfmt, int act, int slot_cap, int num_sms,
                                cudaStream_t s) {
     GemmArgs g;
+    std::memset(&g, 0, sizeof(g));
     g.a = a;
     g.kind = kind;
     g.fmt = wfmt;
     g.act = act;
     g.slot_cap = slot_cap;
+    g.planes = (kind == kDown || a.xt == MOE_F32) ? 2 : 1;
+    g.nt_max = kBRows / g.planes;
+    const int64_t K = (kind == kGateUp) ? a.d : a.f;
+    const uint16_t* hi = (kind == kGateUp) ? a.ws.xs_hi : a.ws.h_hi;
+    const uint16_t* lo = (kind == kGateUp) ? a.ws.xs_lo : a.ws.h_lo;
+    cudaError_t e = plane_map(&g.tb[0], hi, a.P, K);
+    if (e == cudaSuccess && g.planes == 2) e = plane_map(&g.tb[1], lo, a.P, K);
+    if (e != cudaSuccess) return e;
     const int rows_out = (kind == kGateUp) ? a.rows_gu : a.d;
-    const int64_t bound = static_cast<int64_t>(rows_out / kTileM) * (slot_cap + (a.P + kTileN - 1) / kTileN);
+    const int64_t bound = static_cast<int64_t>(rows_out / kTileM) * (slot_cap + (a.P + g.nt_max - 1) / g.nt_max);
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms, bound)));
     return launch_pdl(expert_gemm_kernel, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, g);
 }
