@@ -24,7 +24,7 @@ cudaError_t launch_down_gemv(const ExpertArgs&, int, int, cudaStream_t);
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int64_t, int, int64_t, float*, cudaStream_t);
 cudaError_t launch_rmsnorm_bf16(const float*, int64_t, int64_t, float, uint16_t*, cudaStream_t);
 cudaError_t configure_gemm_kernels();
-cudaError_t launch_expert_gemm(const ExpertArgs&, int, int, int, int, int, cudaStream_t);
+cudaError_t launch_expert_gemm(const ExpertArgs&, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_gather_x_f16(const ExpertArgs&, int, cudaStream_t);
 
 
@@ -384,14 +384,14 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (p.gemm) {
         e = launch_gather_x_f16(a, num_sms, s);
-        if (e == cudaSuccess) e = launch_expert_gemm(a, 0, desc->wfmt, desc->act, p.slot_cap, num_sms, s);
+        if (e == cudaSuccess) e = launch_expert_gemm(a, 0, desc->wfmt, desc->act, p.slot_cap, static_cast<int>(desc->E), num_sms, s);
     } else {
         e = launch_gate_up_gemv(a, desc->wfmt, desc->act, p.slot_cap, s);
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mark(2);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if (p.gemm) e = launch_expert_gemm(a, 1, desc->wfmt, desc->act, p.slot_cap, num_sms, s);
+    if (p.gemm) e = launch_expert_gemm(a, 1, desc->wfmt, desc->act, p.slot_cap, static_cast<int>(desc->E), num_sms, s);
     else e = launch_down_gemv(a, desc->wfmt, p.slot_cap, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mark(3);

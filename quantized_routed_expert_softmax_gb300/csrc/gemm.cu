@@ -16,18 +16,28 @@
 //
 // A persistent grid walks a device-built list of (expert slot, token tile, row tile) work
 // items.  The warps of a CTA have fixed roles, linked by mbarriers:
-//   warp 0       weight producer: 1-D bulk copies of each K step's raw Q8_0 / NVFP4 bytes
-//                into a ring of kRawSlots slots (several K steps of HBM reads in flight);
-//   warp 1       activation producer: TMA 2-D loads of the token tile's B planes;
+//   warp 0       weight producer: TMA loads of the raw Q8_0 / NVFP4 bytes of two K steps
+//                at a time into a ring of kRawSlots slots.  Tensor maps over the whole expert
+//                stack (up to 5-D: byte, row, gate/up half, K panel, expert) make one load
+//                of codes and one of scales cover a slot, since every TMA operation has a
+//                fixed issue cost of the order of a hundred cycles;
+//   warp 1       activation producer: TMA 2-D loads of the token tile's B planes into a
+//                ring of kBStages stages of their own, one box per plane whose height is
+//                the smallest of kBoxHeights that covers the tile's tokens;
 //   warp 2       MMA issuer (one thread): per K step of 64, four K = 16 slices of
-//                tcgen05.mma (A.hi*B.hi, A.lo*B.hi for Q8_0, A.hi*B.lo for two planes; the
-//                lo*lo term is below fp32 rounding), committed to the stage's "empty"
-//                barrier, and at the end of an item to the accumulator's "full" barrier;
+//                tcgen05.mma with A read from tensor memory and B from shared memory
+//                (A.hi*B.hi, A.lo*B.hi for Q8_0, A.hi*B.lo for two planes; the lo*lo term is
+//                below fp32 rounding), committed to the A and B stages' "empty" barriers,
+//                and at the end of an item to the accumulator's "full" barrier;
 //   warps 4..7   epilogue: tensor memory -> registers (lane quadrant = warp % 4), the
 //                activation (SwiGLU pairs gate row i and up row i on accumulator lanes 2i
 //                and 2i+1, one shuffle), stores; two accumulators alternate, so the
 //                epilogue of one item overlaps the main loop of the next;
-//   warps 8..15  dequantisers: raw slot -> f16 A tiles.  NVFP4 weights e2m1 * e4m3 are
+//   warps 8..23  dequantisers: raw slot -> f16 A tiles written straight into tensor
+//                memory (tcgen05.st; warp w writes lane quadrant w % 4, so it converts
+//                rows 32*(w%4).. of one 16-column chunk), which keeps the A operand out of
+//                shared memory: shared-memory bandwidth, not the tensor core, bounded the
+//                kernel when A went through it.  NVFP4 weights e2m1 * e4m3 are
 //                exact in f16.  A Q8_0 weight q * d needs up to 18 significant bits, so it
 //                is split into hi = f16(q * d) and lo = fma(q, d, -hi), the exact residual
 //                rounded once.
@@ -49,21 +59,33 @@ constexpr int kDevErrTimeout = 2;
 constexpr int kDevErrF16Range = 3;
 constexpr long long kWaitLimitNs = 1000000000ll;
 
-constexpr int kGemmThreads = 512;
+constexpr int kGemmThreads = 768;
 constexpr int kTileM = 128;
 constexpr int kStepK = 64;                          // one 128-byte swizzle row of f16
-constexpr int kBRows = 256;                         // B rows per stage: token tile x planes
-constexpr int kBoxRows = 32;                        // rows per TMA box
-constexpr int kRawSlots = 8;
-constexpr int kStages = 2;
-constexpr int kRawSlot = 9216;                      // >= 8704 (Q8_0: 2 panels x (4096 + 256))
-constexpr int kATile = kTileM * kStepK * 2;         // 16 KB
-constexpr int kBTile = kBRows * kStepK * 2;         // 32 KB
-constexpr int kStageBytes = 2 * kATile + kBTile;    // A hi, A lo, B planes
-constexpr size_t kGemmSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
+constexpr int kBRows = 192;                         // B rows per stage: token tile x planes
+constexpr int kSmallTile = 64;                      // tokens per work item, few tokens per expert
+constexpr int kLargeTile = 192;                     // ... many tokens per expert (capped by kBRows / planes)
+constexpr int kLargeAverage = 96;                   // average tokens per expert that selects large tiles
+constexpr int kNumBoxHeights = 3;
+constexpr int kBoxHeights[kNumBoxHeights] = {32, 64, 128};   // B box rows (below the tile height)
+constexpr int kStepsPerSlot = 2;                    // K steps per raw slot
+constexpr int kRawSlots = 4;
+constexpr int kMaxAStages = 4;                      // in tensor memory: 64 columns each (hi, lo)
+constexpr int kBStages = 6;
+constexpr int kRawSlot = 17408;                     // Q8_0: 4 panels x 4096 code bytes + 4 x 256 scale bytes
+constexpr int kBStageBytes = kBRows * kStepK * 2;   // 24 KB: B planes
+constexpr size_t kGemmSmem = 1024 + static_cast<size_t>(kBStages) * kBStageBytes +
                              static_cast<size_t>(kRawSlots) * kRawSlot;
+// Tensor memory: 512 columns of 128 lanes x 32 bits.  A stage s: columns 64*s .. 64*s+31 hold
+// the hi part of the K step (two f16 K values per column), 64*s+32 .. the lo part.  Then
+// acc_bufs buffers (alternate items) x two issuers' accumulators of acc_stride columns each.
+// Two shapes fit: small tiles (4 A stages, 64 tokens, 2 buffers, so the epilogue of one item
+// overlaps the next) and large tiles (2 A stages, up to 192 tokens, 1 buffer).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAColsPerStage = 64;
+
 constexpr int kWarpLoadA = 0, kWarpLoadB = 1, kWarpMma = 2, kWarpEpi0 = 4, kWarpConv0 = 8;
-constexpr int kConvWarps = 8, kConvThreads = kConvWarps * 32;
+constexpr int kConvWarps = 16, kConvThreads = kConvWarps * 32;
 
 // ------------------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t s_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -80,6 +102,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(s_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(s_addr(bar)), "r"(n)
+                 : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -103,9 +130,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t n) {
     const uint32_t parity = n & 1u;
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    return true;
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
@@ -113,6 +141,31 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(s_addr(bar))
                  : "memory");
+}
+
+// TMA tile loads of 3, 4 and 5 dimensions (coordinates innermost first), completion on `bar`.
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(s_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                       uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(s_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
+                                       uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(s_addr(bar))
+        : "memory");
 }
 
 // TMA 2-D tile load (coordinates: x = column, y = row), completion on `bar`.
@@ -152,6 +205,21 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// The same with A in tensor memory (row i in lane i, two K values per 32-bit column).
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t v[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s_addr(bar))
                  : "memory");
@@ -169,6 +237,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float v[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
@@ -184,7 +262,8 @@ __device__ __forceinline__ void split_f16(float v, __half* hi, __half* lo) {
 enum GemmKind { kGateUp = 0, kDown = 1 };
 
 struct GemmArgs {
-    CUtensorMap tb[2];   // B planes, f16 [P][K] (hi, lo), boxes of 64 columns x kBoxRows rows
+    CUtensorMap tb[2][kNumBoxHeights + 1];   // B planes, f16 [P][K] (hi, lo); box 64 columns x bh[i] rows
+    CUtensorMap tw_codes, tw_scales;     // the weight stack's codes and scales (see raw_slot_layout)
     ExpertArgs a;
     int kind;            // GemmKind
     int fmt;             // MOE_W_Q8_0 / MOE_W_NVFP4
@@ -192,6 +271,12 @@ struct GemmArgs {
     int slot_cap;
     int planes;          // 1 or 2
     int nt_max;          // token tile: kBRows / planes
+    int acc_stride;      // tensor-memory columns per accumulator (nt_max rounded up to 32)
+    int a_stages;        // A stages in tensor memory (2 or 4)
+    int acc_bufs;        // accumulator buffers (1 or 2)
+    int nbh;             // box heights in use (kBoxHeights[i] < nt_max, then nt_max itself)
+    int bh[kNumBoxHeights + 1];
+    uint32_t slot_bytes; // bytes one raw slot receives
 };
 
 struct Item {
@@ -219,70 +304,45 @@ __device__ __forceinline__ Item decode_item(const GemmArgs& g, const int* tile_p
     return it;
 }
 
-// Raw bytes of one K step of the weights.
-__device__ __forceinline__ uint32_t raw_step_bytes(const GemmArgs& g) {
-    return (g.fmt == MOE_W_Q8_0) ? 2u * (4096u + 256u) : 4096u + 512u;
-}
-
-// The weight producer's copies of K step ks for row tile `mtile` of expert matrix W
-// (lane-strided).  Raw slot layout: Q8_0 two panels of 32 columns, each [128 rows][32 codes]
-// then [128][2-byte scale] at 4608-byte spacing; NVFP4 one panel of 64 columns, [128][32
-// code bytes] then [128][4 scale bytes]; NVFP4 down (neuron layout) four 16-neuron groups
-// at 1152-byte spacing, each [16 neurons][64 bytes = 128 rows' nibbles] then [128 scales].
-// SwiGLU gate.up tiles stage gate rows in rows 0..63 and the same neurons' up rows in 64..127.
-__device__ __forceinline__ void issue_weights(const GemmArgs& g, uint32_t slot_addr, const uint8_t* W, int rows_w,
-                                              int mtile, int ks, uint64_t* bar, int lane) {
-    const ExpertArgs& a = g.a;
-    const bool swiglu = (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU);
-    if (g.kind == kDown && g.fmt == MOE_W_NVFP4) {
-        const int64_t rec = 16 * static_cast<int64_t>(a.d / 2) + a.d;   // one 16-neuron group record
-        const int row0 = mtile * kTileM;
-        for (int c = lane; c < 4 * 17; c += 32) {
-            const int grp = c / 17, n = c % 17;
-            const uint8_t* base = W + (static_cast<int64_t>(ks) * 4 + grp) * rec;
-            if (n < 16)
-                bulk_g2s(slot_addr + grp * 1152 + n * 64, base + static_cast<int64_t>(n) * (a.d / 2) + row0 / 2, 64, bar);
-            else
-                bulk_g2s(slot_addr + grp * 1152 + 1024, base + 16 * static_cast<int64_t>(a.d / 2) + row0, 128, bar);
-        }
+// raw_slot_layout: what one raw slot (two K steps = 128 columns) holds.
+//   Q8_0, K panels of 32 columns: codes [4 panels][128 staged rows][32 B], then scales
+//     [4 panels][128][2 B] at byte 16384.
+//   NVFP4 K panels of 64 columns: codes [2 panels][128][32 B], then scales [2][128][4 B] at
+//     byte 8192.
+//   NVFP4 down, neuron layout: codes [8 groups of 16 neurons][16][64 B = the tile's 128 rows,
+//     two per byte], then scales [8 groups][128 B] at byte 8192.
+// SwiGLU gate.up tiles stage gate rows of 64 neurons as rows 0..63 and the same neurons' up
+// rows as 64..127 (the gate/up half is a dimension of the tensor maps).
+__device__ __forceinline__ void load_slot(const GemmArgs& g, uint32_t dst, int e, int mtile, int ks0, uint64_t* bar) {
+    const bool q8 = (g.fmt == MOE_W_Q8_0);
+    const uint32_t scales_at = q8 ? 16384u : 8192u;
+    if (g.kind == kDown && !q8) {
+        tma_4d(dst, &g.tw_codes, mtile * 64, 0, ks0 * 4, e, bar);
+        tma_3d(dst + scales_at, &g.tw_scales, mtile * kTileM, ks0 * 4, e, bar);
         return;
     }
-    const bool q8 = (g.fmt == MOE_W_Q8_0);
-    const int npanel = q8 ? 2 : 1;
-    const int scb = q8 ? 2 : 4;                                  // scale bytes per row per panel
-    const int64_t pbytes = static_cast<int64_t>(rows_w) * (q8 ? 34 : 36);
-    const int runs = swiglu ? 2 : 1;                             // row runs per panel
-    const int run_rows = kTileM / runs;
-    const int ncopies = npanel * runs * 2;
-    for (int c = lane; c < ncopies; c += 32) {
-        const int p = c / (runs * 2), rem = c % (runs * 2);
-        const int run = rem >> 1, is_scale = rem & 1;
-        const int src_row = swiglu ? (run == 0 ? mtile * 64 : a.f + mtile * 64) : mtile * kTileM;
-        const uint8_t* P = W + (static_cast<int64_t>(ks) * npanel + p) * pbytes;
-        const uint32_t dst = slot_addr + p * 4608;
-        if (!is_scale)
-            bulk_g2s(dst + run * run_rows * 32, P + static_cast<int64_t>(src_row) * 32, run_rows * 32, bar);
-        else
-            bulk_g2s(dst + 4096 + run * run_rows * scb, P + static_cast<int64_t>(rows_w) * 32 + src_row * scb,
-                     run_rows * scb, bar);
+    const int p0 = ks0 * (q8 ? 2 : 1);   // first K panel
+    if (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU) {
+        tma_5d(dst, &g.tw_codes, 0, mtile * 64, 0, p0, e, bar);
+        tma_4d(dst + scales_at, &g.tw_scales, mtile * 64, 0, p0, e, bar);
+    } else {
+        tma_4d(dst, &g.tw_codes, 0, mtile * kTileM, p0, e, bar);
+        tma_3d(dst + scales_at, &g.tw_scales, mtile * kTileM, p0, e, bar);
     }
 }
 
-// Dequantise one K step from a raw slot into the A hi (and, for Q8_0, lo) tiles.
-__device__ __forceinline__ void dequant_step(const GemmArgs& g, const unsigned char* raw, unsigned char* ta,
-                                             unsigned char* tal, int ct) {
+// Dequantise 16 columns (chunk c16 of K step js of a raw slot) of tile row r into the A hi
+// (and, for Q8_0, lo) columns of tensor memory at ta (this warp's lane quadrant).
+__device__ __forceinline__ void dequant_step(const GemmArgs& g, const unsigned char* raw, int js, uint32_t ta, int r,
+                                             int c16) {
     const bool swiglu = (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU);
-#pragma unroll
-    for (int i = 0; i < (kTileM * 4) / kConvThreads; ++i) {
-        const int u = ct + i * kConvThreads;
-        const int r = u >> 2, c16 = u & 3;              // tile row, 16-column chunk
+    {
         const int sr = swiglu ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;   // staged row
         uint32_t h[8];
         if (g.fmt == MOE_W_Q8_0) {
-            const int p = c16 >> 1, hh = c16 & 1;       // panel of 32 columns, half
-            const unsigned char* pan = raw + p * 4608;
-            const uint4 q = *reinterpret_cast<const uint4*>(pan + sr * 32 + hh * 16);
-            const unsigned short sbits = *reinterpret_cast<const unsigned short*>(pan + 4096 + sr * 2);
+            const int pp = 2 * js + (c16 >> 1), hh = c16 & 1;   // panel of 32 columns, half
+            const uint4 q = *reinterpret_cast<const uint4*>(raw + pp * 4096 + sr * 32 + hh * 16);
+            const unsigned short sbits = *reinterpret_cast<const unsigned short*>(raw + 16384 + pp * 256 + sr * 2);
             const __half2 s2 = __halves2half2(__ushort_as_half(sbits), __ushort_as_half(sbits));
             const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
             const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
@@ -303,14 +363,14 @@ __device__ __forceinline__ void dequant_step(const GemmArgs& g, const unsigned c
                 hl[2 * j] = *reinterpret_cast<const uint32_t*>(&l01);
                 hl[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&l23);
             }
-            *reinterpret_cast<uint4*>(tal + swz(r, 2 * c16)) = make_uint4(hl[0], hl[1], hl[2], hl[3]);
-            *reinterpret_cast<uint4*>(tal + swz(r, 2 * c16 + 1)) = make_uint4(hl[4], hl[5], hl[6], hl[7]);
+            tmem_st8(ta + 32 + c16 * 8, hl);
         } else if (g.kind == kDown) {
             // NVFP4 neuron layout: columns 16*c16 .. +15 are group c16; row sr is nibble
             // (sr & 1) of byte sr/2 in each neuron's run
-            const unsigned char* gb = raw + c16 * 1152;
+            const int gg = 4 * js + c16;
+            const unsigned char* gb = raw + gg * 1024;
             uint32_t s16;
-            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(static_cast<uint16_t>(gb[1024 + sr])));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(static_cast<uint16_t>(raw[8192 + gg * 128 + sr])));
             const __half sh = __ushort_as_half(static_cast<unsigned short>(s16 & 0xffffu));
             const __half2 s2 = __halves2half2(sh, sh);
 #pragma unroll
@@ -326,9 +386,9 @@ __device__ __forceinline__ void dequant_step(const GemmArgs& g, const unsigned c
             }
         } else {
             // NVFP4 panel of 64 columns: 32 code bytes, 4 scale bytes per row
-            const uint2 cw = *reinterpret_cast<const uint2*>(raw + sr * 32 + c16 * 8);
+            const uint2 cw = *reinterpret_cast<const uint2*>(raw + js * 4096 + sr * 32 + c16 * 8);
             uint32_t s16;
-            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(static_cast<uint16_t>(raw[4096 + sr * 4 + c16])));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(static_cast<uint16_t>(raw[8192 + js * 512 + sr * 4 + c16])));
             const __half sh = __ushort_as_half(static_cast<unsigned short>(s16 & 0xffffu));
             const __half2 s2 = __halves2half2(sh, sh);
             const uint32_t w2[2] = {cw.x, cw.y};
@@ -341,8 +401,7 @@ __device__ __forceinline__ void dequant_step(const GemmArgs& g, const unsigned c
                 h[j] = *reinterpret_cast<const uint32_t*>(&v);
             }
         }
-        *reinterpret_cast<uint4*>(ta + swz(r, 2 * c16)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(ta + swz(r, 2 * c16 + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+        tmem_st8(ta + c16 * 8, h);
     }
 }
 
@@ -353,18 +412,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
     extern __shared__ __align__(16) unsigned char dsm_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    unsigned char* stages = base;                               // kStages x (A hi, A lo, B)
-    unsigned char* raws = base + kStages * kStageBytes;         // kRawSlots x kRawSlot
+    unsigned char* bstages = base;                                    // kBStages x B planes
+    unsigned char* raws = bstages + kBStages * kBStageBytes;          // kRawSlots x kRawSlot
     __shared__ uint64_t raw_full[kRawSlots], raw_empty[kRawSlots];
-    __shared__ uint64_t a_full[kStages], b_full[kStages], st_empty[kStages];
+    __shared__ uint64_t a_full[kMaxAStages], a_empty[kMaxAStages], b_full[kBStages], b_empty[kBStages];
     __shared__ uint64_t acc_full[2], acc_empty[2];
-    __shared__ uint32_t raw_issued[kRawSlots], b_issued[kStages], mma_commits[kStages];
+    __shared__ uint32_t raw_issued[kRawSlots], b_issued[kBStages], a_commits[kMaxAStages], b_commits[kBStages];
     __shared__ uint32_t tmem_base;
     __shared__ int tile_prefix[kMaxE + 1];
     __shared__ int warp_tot[kGemmThreads / 32];
     __shared__ volatile int s_fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t tmem_cols = static_cast<uint32_t>(2 * g.nt_max);   // two accumulators
+    const uint32_t tmem_cols = kTmemCols;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s_addr(&tmem_base)),
@@ -374,18 +433,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
     if (tid == 0) {
         for (int s = 0; s < kRawSlots; ++s) {
             mbar_init(&raw_full[s], 1);
-            mbar_init(&raw_empty[s], kConvWarps);
+            mbar_init(&raw_empty[s], (kConvWarps / 2) * kStepsPerSlot);   // 8 warps per K step
             raw_issued[s] = 0;
         }
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&a_full[s], kConvWarps);
+        for (int s = 0; s < kMaxAStages; ++s) {
+            mbar_init(&a_full[s], kConvWarps / 2);   // one converter group
+            mbar_init(&a_empty[s], 1);
+            a_commits[s] = 0;
+        }
+        for (int s = 0; s < kBStages; ++s) {
             mbar_init(&b_full[s], 1);
-            mbar_init(&st_empty[s], 1);
+            mbar_init(&b_empty[s], 1);
             b_issued[s] = 0;
-            mma_commits[s] = 0;
+            b_commits[s] = 0;
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_full[s], 2);   // one commit per issuer
             mbar_init(&acc_empty[s], 4);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -431,36 +494,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
     const int total = tile_prefix[g.slot_cap];
     const int ksteps = ((g.kind == kGateUp) ? a.d : a.f) / kStepK;
     const int rows_w = (g.kind == kGateUp) ? a.rows_gu : a.d;
+    // a_stages (2 or 4) and acc_bufs (1 or 2) are powers of two: shifts and masks
+    const uint32_t a_shift = (g.a_stages == 4) ? 2u : 1u, a_mask = (1u << a_shift) - 1u;
+    const uint32_t b_shift = (g.acc_bufs == 2) ? 1u : 0u, b_mask = (1u << b_shift) - 1u;
+    const uint32_t acc_col0 = static_cast<uint32_t>(g.a_stages) * kAColsPerStage;
 
     if (warp == kWarpLoadA) {
         // ---------------------------------------------------------------- weight producer
-        const uint32_t bytes = raw_step_bytes(g);
-        uint32_t gs = 0;
-        bool ok = true;
-        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-            const Item it = decode_item(g, tile_prefix, mtiles, item);
-            const uint8_t* W = (g.kind == kGateUp) ? a.w_gu + static_cast<int64_t>(it.e) * a.gu_bytes
-                                                   : a.w_dn + static_cast<int64_t>(it.e) * a.dn_bytes;
-            for (int ks = 0; ks < ksteps; ++ks, ++gs) {
-                const int slot = gs % kRawSlots;
-                const uint32_t use = gs / kRawSlots;
-                bool w_ok = (use == 0) || mbar_wait(&raw_empty[slot], use - 1);
-                w_ok = __all_sync(0xffffffffu, w_ok) && !s_fail;
-                if (!w_ok) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&raw_full[slot], bytes);
+        if (lane == 0) {
+            uint32_t sn = 0;   // slots issued
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                const Item it = decode_item(g, tile_prefix, mtiles, item);
+                for (int ks0 = 0; ks0 < ksteps; ks0 += kStepsPerSlot, ++sn) {
+                    const int slot = sn % kRawSlots;
+                    const uint32_t use = sn / kRawSlots;
+                    if ((use > 0 && !mbar_wait(&raw_empty[slot], use - 1)) || s_fail) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&raw_full[slot], g.slot_bytes);
                     raw_issued[slot] = use + 1;
+                    load_slot(g, s_addr(raws + slot * kRawSlot), it.e, it.mtile, ks0, &raw_full[slot]);
                 }
-                __syncwarp();
-                issue_weights(g, s_addr(raws + slot * kRawSlot), W, rows_w, it.mtile, ks, &raw_full[slot], lane);
             }
-        }
-        if (!ok && lane == 0) {
-            s_fail = 1;
-            atomicCAS(a.ws.err, 0, kDevErrTimeout);
+            if (!ok) {
+                s_fail = 1;
+                atomicCAS(a.ws.err, 0, kDevErrTimeout);
+            }
         }
     } else if (warp == kWarpLoadB) {
         // ---------------------------------------------------------------- activation producer
@@ -469,22 +530,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
             bool ok = true;
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
                 const Item it = decode_item(g, tile_prefix, mtiles, item);
-                const int nbox = (it.nt + kBoxRows - 1) / kBoxRows;
-                const uint32_t bytes = static_cast<uint32_t>(nbox * kBoxRows * 128 * g.planes);
+                int bi = 0;
+                while (bi + 1 < g.nbh && g.bh[bi] < it.nt) ++bi;   // smallest box covering the tile
+                const uint32_t bytes = static_cast<uint32_t>(g.bh[bi] * 128 * g.planes);
                 for (int ks = 0; ks < ksteps; ++ks, ++gs) {
-                    const int st = gs % kStages;
-                    const uint32_t use = gs / kStages;
-                    if ((use > 0 && !mbar_wait(&st_empty[st], use - 1)) || s_fail) {
+                    const int st = gs % kBStages;
+                    const uint32_t use = gs / kBStages;
+                    if ((use > 0 && !mbar_wait(&b_empty[st], use - 1)) || s_fail) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&b_full[st], bytes);
                     b_issued[st] = use + 1;
-                    const uint32_t bdst = s_addr(stages + st * kStageBytes + 2 * kATile);
+                    const uint32_t bdst = s_addr(bstages + st * kBStageBytes);
                     for (int p = 0; p < g.planes; ++p)
-                        for (int j = 0; j < nbox; ++j)
-                            tma_2d(bdst + p * g.nt_max * 128 + j * kBoxRows * 128, &g.tb[p], ks * kStepK,
-                                   it.r_first + j * kBoxRows, &b_full[st]);
+                        tma_2d(bdst + p * g.nt_max * 128, &g.tb[p][bi], ks * kStepK, it.r_first, &b_full[st]);
                 }
             }
             if (!ok) {
@@ -492,47 +552,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
                 atomicCAS(a.ws.err, 0, kDevErrTimeout);
             }
         }
-    } else if (warp == kWarpMma) {
-        // ---------------------------------------------------------------- MMA issuer
+    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+        // ---------------------------------------------------------------- MMA issuers
+        // Issuer iss takes the K steps whose global index has parity iss (so it always uses A
+        // stage iss) and accumulates them into its own accumulator of the item's buffer.
         if (lane == 0) {
+            const int iss = warp - kWarpMma;
             const bool alo = (g.fmt == MOE_W_Q8_0);
+            const bool two = (g.planes == 2);
+            // B descriptors of stage 0; the encoded start address (bits 0..13, bytes / 16) is
+            // linear in the address, so stage s adds s * stage bytes / 16 and a K = 16 slice
+            // adds 32 bytes (2).  A in tensor memory: a K = 16 slice is 8 columns.
+            const uint64_t dB0 = sdesc_k128(s_addr(bstages));
+            const uint64_t dBl0 = sdesc_k128(s_addr(bstages + g.nt_max * 128));
             uint32_t gs = 0, n_item = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++n_item) {
                 const Item it = decode_item(g, tile_prefix, mtiles, item);
-                const int n16 = (it.nt + 15) & ~15;
-                const uint32_t idesc = idesc_f16(n16);
-                const int buf = n_item & 1;
-                const uint32_t ub = n_item >> 1;
+                const uint32_t idesc = idesc_f16((it.nt + 15) & ~15);
+                const int buf = static_cast<int>(n_item & b_mask);
+                const uint32_t ub = n_item >> b_shift;
                 if ((ub > 0 && !mbar_wait(&acc_empty[buf], ub - 1)) || s_fail) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dt = tmem + static_cast<uint32_t>(buf * g.nt_max);
+                const uint32_t dt = tmem + acc_col0 + static_cast<uint32_t>((2 * buf + iss) * g.acc_stride);
+                bool first = true;
                 for (int ks = 0; ks < ksteps; ++ks, ++gs) {
-                    const int st = gs % kStages;
-                    const uint32_t use = gs / kStages;
-                    if (!mbar_wait(&a_full[st], use) || !mbar_wait(&b_full[st], use) || s_fail) {
+                    if ((gs & 1u) != static_cast<uint32_t>(iss)) continue;
+                    const int sa = static_cast<int>(gs & a_mask), sb = gs % kBStages;
+                    const uint32_t ua = gs >> a_shift, ubb = gs / kBStages;
+                    if (!mbar_wait(&a_full[sa], ua) || !mbar_wait(&b_full[sb], ubb) || s_fail) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = s_addr(stages + st * kStageBytes);
-                    const uint32_t sal = sa + kATile;
-                    const uint32_t sb = sa + 2 * kATile;
-                    const uint32_t sbl = sb + g.nt_max * 128;
+                    const uint32_t ta = tmem + static_cast<uint32_t>(sa) * kAColsPerStage;
+                    const uint64_t ob = static_cast<uint64_t>(sb * (kBStageBytes >> 4));
 #pragma unroll
                     for (int kk = 0; kk < kStepK / 16; ++kk) {
-                        umma_f16(dt, sdesc_k128(sa + kk * 32), sdesc_k128(sb + kk * 32), idesc, (ks | kk) ? 1u : 0u);
-                        if (alo) umma_f16(dt, sdesc_k128(sal + kk * 32), sdesc_k128(sb + kk * 32), idesc, 1u);
-                        if (g.planes == 2) umma_f16(dt, sdesc_k128(sa + kk * 32), sdesc_k128(sbl + kk * 32), idesc, 1u);
+                        const uint64_t o = static_cast<uint64_t>(2 * kk);
+                        const uint32_t tk = ta + 8 * kk;
+                        umma_f16_ta(dt, tk, dB0 + ob + o, idesc, (first && kk == 0) ? 0u : 1u);
+                        if (alo) umma_f16_ta(dt, tk + 32, dB0 + ob + o, idesc, 1u);
+                        if (two) umma_f16_ta(dt, tk, dBl0 + ob + o, idesc, 1u);
                     }
-                    umma_commit(&st_empty[st]);
-                    mma_commits[st] = use + 1;
+                    first = false;
+                    umma_commit(&a_empty[sa]);
+                    umma_commit(&b_empty[sb]);
+                    a_commits[sa] = ua + 1;
+                    b_commits[sb] = ubb + 1;
                 }
                 if (!ok) break;
-                umma_commit(&acc_full[buf]);
+                umma_commit(&acc_full[buf]);   // arrives at once when this issuer had no step
             }
             if (!ok) {
                 s_fail = 1;
@@ -544,13 +617,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
         const int q = warp & 3;
         const int row = q * 32 + lane;                 // accumulator lane = tile row
         const float* ts_arr = (g.kind == kGateUp) ? a.gu_ts : a.dn_ts;
-        uint32_t n_item = 0;
+        uint32_t n_item = 0, gs0 = 0;   // gs0: global index of the item's first K step
         bool ok = true;
-        for (int item = blockIdx.x; item < total; item += gridDim.x, ++n_item) {
+        for (int item = blockIdx.x; item < total; item += gridDim.x, ++n_item, gs0 += ksteps) {
             const Item it = decode_item(g, tile_prefix, mtiles, item);
             const int n16 = (it.nt + 15) & ~15;
-            const int buf = n_item & 1;
-            bool w_ok = mbar_wait(&acc_full[buf], n_item >> 1);
+            // issuers with at least one K step of this item (both unless it has one step)
+            const bool has0 = ksteps >= 2 || (gs0 & 1u) == 0, has1 = ksteps >= 2 || (gs0 & 1u) == 1;
+            const int buf = static_cast<int>(n_item & b_mask);
+            bool w_ok = mbar_wait(&acc_full[buf], n_item >> b_shift);
             w_ok = __all_sync(0xffffffffu, w_ok) && !s_fail;
             if (!w_ok) {
                 ok = false;
@@ -558,13 +633,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
             }
             tc_fence_after();
             const float ts = (g.fmt == MOE_W_NVFP4) ? ts_arr[it.e] : 1.0f;
-            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * g.nt_max);
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(q * 32) << 16) + acc_col0 + static_cast<uint32_t>(2 * buf * g.acc_stride);
             bool range_ok = true;
-            for (int c0 = 0; c0 < n16; c0 += 16) {
-                float v[16];
-                tmem_ld16(tbase + static_cast<uint32_t>(c0), v);
+            for (int c0 = 0; c0 < n16; c0 += 8) {
+                float v[8], v1[8];
+                if (has0) tmem_ld8(tbase + static_cast<uint32_t>(c0), v);
+                if (has1) tmem_ld8(tbase + static_cast<uint32_t>(g.acc_stride + c0), v1);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int jj = 0; jj < 8; ++jj) v[jj] = has0 ? (has1 ? v[jj] + v1[jj] : v[jj]) : v1[jj];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
                     const int n = c0 + j;
                     const int64_t prow = static_cast<int64_t>(it.r_first + n);
                     const float z = v[j] * ts;
@@ -607,29 +686,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
         }
     } else if (warp >= kWarpConv0) {
         // ---------------------------------------------------------------- dequantisers
-        const int ct = tid - kWarpConv0 * 32;
-        int my_items = 0;
-        for (int item = blockIdx.x; item < total; item += gridDim.x) ++my_items;
-        const uint32_t nsteps = static_cast<uint32_t>(my_items) * ksteps;
+        // Group grp (8 warps) converts the K steps whose global index has parity grp, so a
+        // group's latency (waits, conversion, tensor-memory stores, fences) overlaps the other
+        // group's.  Warp w converts lane quadrant w % 4 of two 16-column chunks.
+        const int cw = warp - kWarpConv0;
+        const int grp = cw / 8;
+        const int q = warp & 3;                          // lane quadrant of tensor memory
+        const int cpair = (cw % 8) >> 2;                 // chunks 2*cpair, 2*cpair + 1
+        const int r = q * 32 + lane;                     // tile row
+        const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        uint32_t gs = 0, sn = 0;   // K steps seen, slots seen
         bool ok = true;
-        for (uint32_t gs = 0; gs < nsteps; ++gs) {
-            const int slot = gs % kRawSlots;
-            const int st = gs % kStages;
-            const uint32_t use = gs / kStages;
-            bool w_ok = mbar_wait(&raw_full[slot], gs / kRawSlots);
-            w_ok = w_ok && (use == 0 || mbar_wait(&st_empty[st], use - 1));
-            w_ok = __all_sync(0xffffffffu, w_ok) && !s_fail;
-            if (!w_ok) {
-                ok = false;
-                break;
-            }
-            unsigned char* sa = stages + st * kStageBytes;
-            dequant_step(g, raws + slot * kRawSlot, sa, sa + kATile, ct);
-            proxy_fence_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&a_full[st]);
-                mbar_arrive(&raw_empty[slot]);
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            for (int ks = 0; ks < ksteps; ++ks, ++gs) {
+                const int j = ks % kStepsPerSlot;
+                const bool single = (j == 0) && (ks == ksteps - 1);       // a slot holding one K step
+                const bool slot_last = (j == kStepsPerSlot - 1) || (ks == ksteps - 1);
+                const int slot = sn % kRawSlots;
+                const uint32_t slot_use = sn / kRawSlots;
+                if (slot_last) ++sn;
+                if ((gs & 1u) != static_cast<uint32_t>(grp)) continue;
+                const int sa = static_cast<int>(gs & a_mask);
+                const uint32_t ua = gs >> a_shift;
+                bool w_ok = mbar_wait(&raw_full[slot], slot_use);
+                w_ok = w_ok && (ua == 0 || mbar_wait(&a_empty[sa], ua - 1));
+                w_ok = __all_sync(0xffffffffu, w_ok) && !s_fail;
+                if (!w_ok) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const unsigned char* raw = raws + slot * kRawSlot;
+                const uint32_t ta = tq + static_cast<uint32_t>(sa) * kAColsPerStage;
+                dequant_step(g, raw, j, ta, r, 2 * cpair);
+                dequant_step(g, raw, j, ta, r, 2 * cpair + 1);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&a_full[sa]);
+                    mbar_arrive_n(&raw_empty[slot], single ? kStepsPerSlot : 1);
+                }
             }
         }
         if (!ok && lane == 0) {
@@ -645,10 +742,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
         bool ok = true;
         for (int s = 0; s < kRawSlots; ++s)
             if (raw_issued[s]) ok &= mbar_wait(&raw_full[s], raw_issued[s] - 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kBStages; ++s) {
             if (b_issued[s]) ok &= mbar_wait(&b_full[s], b_issued[s] - 1);
-            if (mma_commits[s]) ok &= mbar_wait(&st_empty[s], mma_commits[s] - 1);
+            if (b_commits[s]) ok &= mbar_wait(&b_empty[s], b_commits[s] - 1);
         }
+        for (int s = 0; s < kMaxAStages; ++s)
+            if (a_commits[s]) ok &= mbar_wait(&a_empty[s], a_commits[s] - 1);
         if (!ok) atomicCAS(a.ws.err, 0, kDevErrTimeout);
     }
     tc_fence_before();
@@ -722,17 +821,71 @@ cudaError_t get_encoder() {
     return status;
 }
 
+cudaError_t encode(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    const CUresult r = g_encode(m, type, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Tensor map of an f16 plane [rows][cols] (row stride cols*2 bytes), boxes of 64 columns x
-// kBoxRows rows, 128-byte swizzle; rows past the end read as zero.
-cudaError_t plane_map(CUtensorMap* m, const uint16_t* base, int64_t rows, int64_t cols) {
+// box_rows rows, 128-byte swizzle; rows past the end read as zero.
+cudaError_t plane_map(CUtensorMap* m, const uint16_t* base, int64_t rows, int64_t cols, int box_rows) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStepK), static_cast<cuuint32_t>(kBoxRows)};
-    const cuuint32_t es[2] = {1, 1};
-    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box,
-                                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStepK), static_cast<cuuint32_t>(box_rows)};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Tensor maps of a stack of E quantised matrices for raw_slot_layout (strides in bytes).
+cudaError_t weight_maps(GemmArgs* g, const uint8_t* W, int64_t E, int64_t mat_bytes, int64_t rows_w, int64_t K) {
+    const bool q8 = (g->fmt == MOE_W_Q8_0);
+    const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
+    const cuuint64_t e64 = static_cast<cuuint64_t>(E), mb = static_cast<cuuint64_t>(mat_bytes);
+    if (g->kind == kDown && !q8) {
+        // neuron layout: per 16-neuron group, [16 neurons][rows/2 bytes] then [rows] scales
+        const int64_t d = rows_w, groups = K / 16, rec = 9 * d;
+        const cuuint64_t cd[4] = {static_cast<cuuint64_t>(d / 2), 16, static_cast<cuuint64_t>(groups), e64};
+        const cuuint64_t cs[3] = {static_cast<cuuint64_t>(d / 2), static_cast<cuuint64_t>(rec), mb};
+        const cuuint32_t cb[4] = {64, 16, 4 * kStepsPerSlot, 1};
+        cudaError_t e = encode(&g->tw_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, W, cd, cs, cb, none);
+        if (e != cudaSuccess) return e;
+        const cuuint64_t sd[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(groups), e64};
+        const cuuint64_t ss[2] = {static_cast<cuuint64_t>(rec), mb};
+        const cuuint32_t sb[3] = {kTileM, 4 * kStepsPerSlot, 1};
+        g->slot_bytes = 64 * 16 * 4 * kStepsPerSlot + kTileM * 4 * kStepsPerSlot;
+        return encode(&g->tw_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, W + 8 * d, sd, ss, sb, none);
+    }
+    // K panels: [rows][32 code bytes] then [rows] scales of 2 (Q8_0) or 4 (NVFP4) bytes
+    const int64_t panel_cols = q8 ? 32 : 64, panels = K / panel_cols;
+    const int64_t scb = q8 ? 2 : 4, pbytes = rows_w * (32 + scb);
+    const cuuint32_t npan = static_cast<cuuint32_t>((q8 ? 2 : 1) * kStepsPerSlot);
+    const CUtensorMapDataType st = q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32;
+    g->slot_bytes = npan * (kTileM * 32 + kTileM * static_cast<uint32_t>(scb));
+    cudaError_t e;
+    if (g->kind == kGateUp && g->act == MOE_ACT_SWIGLU) {
+        const int64_t f = rows_w / 2;   // gate rows 0..f-1, up rows f..2f-1
+        const cuuint64_t cd[5] = {32, static_cast<cuuint64_t>(f), 2, static_cast<cuuint64_t>(panels), e64};
+        const cuuint64_t cs[4] = {32, static_cast<cuuint64_t>(f * 32), static_cast<cuuint64_t>(pbytes), mb};
+        const cuuint32_t cb[5] = {32, 64, 2, npan, 1};
+        e = encode(&g->tw_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, W, cd, cs, cb, none);
+        if (e != cudaSuccess) return e;
+        const cuuint64_t sd[4] = {static_cast<cuuint64_t>(f), 2, static_cast<cuuint64_t>(panels), e64};
+        const cuuint64_t ss[3] = {static_cast<cuuint64_t>(f * scb), static_cast<cuuint64_t>(pbytes), mb};
+        const cuuint32_t sb[4] = {64, 2, npan, 1};
+        return encode(&g->tw_scales, st, 4, W + rows_w * 32, sd, ss, sb, none);
+    }
+    const cuuint64_t cd[4] = {32, static_cast<cuuint64_t>(rows_w), static_cast<cuuint64_t>(panels), e64};
+    const cuuint64_t cs[3] = {32, static_cast<cuuint64_t>(pbytes), mb};
+    const cuuint32_t cb[4] = {32, kTileM, npan, 1};
+    e = encode(&g->tw_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, W, cd, cs, cb, none);
+    if (e != cudaSuccess) return e;
+    const cuuint64_t sd[3] = {static_cast<cuuint64_t>(rows_w), static_cast<cuuint64_t>(panels), e64};
+    const cuuint64_t ss[2] = {static_cast<cuuint64_t>(pbytes), mb};
+    const cuuint32_t sb[3] = {kTileM, npan, 1};
+    return encode(&g->tw_scales, st, 3, W + rows_w * 32, sd, ss, sb, none);
 }
 
 }  // namespace
@@ -757,7 +910,7 @@ cudaError_t launch_gather_x_f16(const ExpertArgs& a, int num_sms, cudaStream_t s
                       a.ws.err);
 }
 
-cudaError_t launch_expert_gemm(const ExpertArgs& a, int kind, int wfmt, int act, int slot_cap, int num_sms,
+cudaError_t launch_expert_gemm(const ExpertArgs& a, int kind, int wfmt, int act, int slot_cap, int E, int num_sms,
                                cudaStream_t s) {
     GemmArgs g;
     std::memset(&g, 0, sizeof(g));
@@ -767,12 +920,27 @@ cudaError_t launch_expert_gemm(const ExpertArgs& a, int kind, int wfmt, int act,
     g.act = act;
     g.slot_cap = slot_cap;
     g.planes = (kind == kDown || a.xt == MOE_F32) ? 2 : 1;
-    g.nt_max = kBRows / g.planes;
+    // tile shape by the average tokens per active expert
+    const bool large = a.P >= static_cast<int64_t>(kLargeAverage) * slot_cap;
+    g.nt_max = std::min(large ? kLargeTile : kSmallTile, kBRows / g.planes);
+    g.acc_stride = (g.nt_max + 31) & ~31;
+    g.a_stages = large ? 2 : 4;
+    g.acc_bufs = large ? 1 : 2;
+    g.nbh = 0;
+    for (int i = 0; i < kNumBoxHeights && kBoxHeights[i] < g.nt_max; ++i) g.bh[g.nbh++] = kBoxHeights[i];
+    static_assert(kNumBoxHeights + 1 <= 4, "box height table");
+    g.bh[g.nbh++] = g.nt_max;
     const int64_t K = (kind == kGateUp) ? a.d : a.f;
     const uint16_t* hi = (kind == kGateUp) ? a.ws.xs_hi : a.ws.h_hi;
     const uint16_t* lo = (kind == kGateUp) ? a.ws.xs_lo : a.ws.h_lo;
-    cudaError_t e = plane_map(&g.tb[0], hi, a.P, K);
-    if (e == cudaSuccess && g.planes == 2) e = plane_map(&g.tb[1], lo, a.P, K);
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < g.nbh && e == cudaSuccess; ++i) {
+        e = plane_map(&g.tb[0][i], hi, a.P, K, g.bh[i]);
+        if (e == cudaSuccess && g.planes == 2) e = plane_map(&g.tb[1][i], lo, a.P, K, g.bh[i]);
+    }
+    if (e == cudaSuccess)
+        e = (kind == kGateUp) ? weight_maps(&g, a.w_gu, E, a.gu_bytes, a.rows_gu, a.d)
+                              : weight_maps(&g, a.w_dn, E, a.dn_bytes, a.d, a.f);
     if (e != cudaSuccess) return e;
     const int rows_out = (kind == kGateUp) ? a.rows_gu : a.d;
     const int64_t bound = static_cast<int64_t>(rows_out / kTileM) * (slot_cap + (a.P + g.nt_max - 1) / g.nt_max);
