@@ -333,6 +333,15 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_src = hbm_peak()
     achieved = gu_bytes / (gu_us * 1e-6) / 1e9
     traffic = measured_traffic(args.workload, T)
+    # Which expert kernels run (the library's AUTO rule): the tensor-core GEMMs when an expert
+    # sees at least 8 tokens on average and the shape allows them, else the GEMVs.
+    gemm = (T * w.k >= 8 * w.E and w.f % 64 == 0 and (w.act == "swiglu" or w.f % 128 == 0))
+    gu_flops = 2 * T * w.k * w.rows_gu * w.d                    # useful gate.up FLOP per layer
+    pk = peaks() or {}
+    tc_peak = float(pk.get("bf16_tflops_sustained") or 1700.0)
+    tc_src = ("measured (MEASURED_PEAKS.json bf16_tflops_sustained: cuBLAS bf16, seconds-long loop; "
+              "f16 kind::f16 runs at the bf16 rate)" if pk.get("bf16_tflops_sustained") else "fallback 1.7 PFLOP/s")
+    tc_achieved = gu_flops / (gu_us * 1e-6) / 1e12
 
     # ---- end to end: host x in pinned memory -> device, the stack, out -> host
     x_host = [inp.cpu().pin_memory() for inp in inputs]
@@ -384,11 +393,21 @@ def run_ours(args, rank, world, local_rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; random-init weights of the workload's shapes)",
             "config": cfg,
-            "roofline": {"bound": "hbm", "kernel": "gate_up_gemv (gate.up + SwiGLU + group mask)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("expert_gemm_kernel (gate.up + activation, tcgen05)" if gemm
+                                    else "gate_up_gemv (gate.up + activation + group mask)"),
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes_per_launch": gu_bytes, "launch_us_mean": round(gu_us, 3),
-                         "launches_timed": len(gu_ms), "timing": timing_how, "peak_source": peak_src},
+                         "launches_timed": len(gu_ms), "timing": timing_how, "peak_source": peak_src,
+                         "tensor": {"useful_flop_per_launch": gu_flops, "achieved": round(tc_achieved, 2),
+                                    "peak": tc_peak, "unit": "TFLOP/s", "frac": round(tc_achieved / tc_peak, 4),
+                                    "peak_source": tc_src,
+                                    "note": ("useful FLOP only (2*T*k*rows*d); the Q8_0 path issues a second "
+                                             "MMA per weight for the exact lo part" if gemm else
+                                             "GEMV path: CUDA-core dequant, mma.sync for the dot products")},
+                         "bytes_time_us": round(gu_bytes / (peak * 1e9) * 1e6, 2),
+                         "flop_time_us": round(gu_flops / (tc_peak * 1e12) * 1e6, 2)},
             "e2e": {"value": round(e2e_value, 2), "unit": f"tokens/s through the {layers}-layer stack",
                     "h2d_bytes_per_step": int(x_host[0].numel() * x_host[0].element_size()),
                     "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()),
@@ -435,7 +454,7 @@ def active_expert_bytes(stack, inputs, T, w):
 def kernel_source_sha():
     import hashlib
     csrc = os.path.join(ROOT, "quantized_routed_expert_softmax_gb300", "csrc")
-    blob = open(os.path.join(csrc, "gemv.cu"), "rb").read() + open(os.path.join(csrc, "common.cuh"), "rb").read()
+    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("gemv.cu", "gemm.cu", "common.cuh"))
     return hashlib.sha1(blob).hexdigest()[:12]
 
 

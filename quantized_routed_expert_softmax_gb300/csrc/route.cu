@@ -596,58 +596,85 @@ __device__ void permute_block_256(const int* sidx, int T, int k, int E, int gwor
 }
 
 // Router + top-k + softmax + permutation for small batches (T * E <= 4096, T * k <= 1024)
-// in one launch.  grid: (32 residue classes, ceil(E/128) expert chunks) x 256 threads.
-// Warp j of CTA (c, chunk) owns the canonical partial sum l = c + 32 j for the chunk's 128
-// experts (lane = 4 experts): it reads whole 512-byte rows i = l, l + 256, ... of W, fully
-// coalesced.  Tree levels h = 128, 64, 32 combine partials of the same residue c, inside the
-// CTA; the CTA writes its result to part[t][e][c].  The last CTA to finish (atomic counter,
-// no waiting) applies levels h = 16 .. 1 across the 32 residues, then selects, weights and
-// permutes, and resets the counter.
+// in one launch.  grid: (32 residue classes, E / (32 * EPL) expert chunks) x 256 threads.
+// Warp j of CTA (c, chunk) owns the canonical partial sum l = c + 32 j for the chunk's
+// 32 * EPL experts (lane = EPL experts): it reads rows i = l, l + 256, ... of W, coalesced
+// across the warp.  Narrow chunks spread the router weights over 128-256 CTAs: a CTA can keep
+// only so many loads in flight, and the weights come from HBM.  Tree levels h = 128, 64, 32
+// combine partials of the same residue c, inside the CTA; the CTA writes its result to
+// part[t][e][c].  The last CTA to finish (atomic counter, no waiting) applies levels
+// h = 16 .. 1 across the 32 residues, then selects, weights and permutes, and resets the
+// counter.
 constexpr int kResidues = 32;
-constexpr int kRouteChunk = 128;
 constexpr int kChainBatch = 12;
 constexpr int kFusedRouteLogits = 4096;
+constexpr int kRankTopkMaxE = 256;   // above this, top-k goes through segment candidates
 
+template <int EPL>
+__device__ __forceinline__ void load_w_row(const float* __restrict__ W, int64_t off, float (&w)[EPL]) {
+    if constexpr (EPL == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(W + off));
+        w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+    } else if constexpr (EPL == 2) {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(W + off));
+        w[0] = v.x, w[1] = v.y;
+    } else {
+        w[0] = __ldg(W + off);
+    }
+}
+
+// a beats b: larger logit, or equal logit and lower expert index
+__device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) { return va > vb || (va == vb && ea < eb); }
+
+template <int EPL>
 __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restrict__ x, int xt,
                                                             const float* __restrict__ W, int T, int d, int E, int k,
                                                             int gwords, Workspace ws) {
+    constexpr int kChunk = 32 * EPL;
     const int c = blockIdx.x, chunk = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int l = c + kResidues * warp;
-    const int e0 = chunk * kRouteChunk + lane * 4;
+    const int e0 = chunk * kChunk + lane * EPL;
     const bool on = e0 < E;
     const int nchain = d / kRouterPartials;     // d is a multiple of 256
-    // phase 1 uses the buffer as red[8 warps][4 tokens][128 experts], the last CTA as the
-    // logits slog[T * E] (both 16 KB)
-    __shared__ __align__(16) float buf[8 * 4 * kRouteChunk];
-    static_assert(8 * 4 * kRouteChunk == kFusedRouteLogits, "shared buffer reuse");
-    float (*red)[4][kRouteChunk] = reinterpret_cast<float (*)[4][kRouteChunk]>(buf);
+    // phase 1 uses the buffer as red[8 warps][4 tokens][kChunk experts], the last CTA as the
+    // logits slog[T * E]
+    __shared__ __align__(16) float buf[kFusedRouteLogits];
+    static_assert(8 * 4 * kChunk <= kFusedRouteLogits, "shared buffer reuse");
+    float (*red)[4][kChunk] = reinterpret_cast<float (*)[4][kChunk]>(buf);
     float* slog = buf;
     __shared__ int s_last;
     __shared__ int sidx[1024];
     // The router weights do not depend on the previous kernel: the first batch of rows is
     // loaded before waiting for it.
-    float4 w0[kChainBatch];
+    float w0[kChainBatch][EPL];
 #pragma unroll
     for (int u = 0; u < kChainBatch; ++u)
-        if (on && u < nchain)
-            w0[u] = __ldg(reinterpret_cast<const float4*>(W + static_cast<int64_t>(l + u * kRouterPartials) * E + e0));
+        if (on && u < nchain) load_w_row<EPL>(W, static_cast<int64_t>(l + u * kRouterPartials) * E + e0, w0[u]);
     pdl_wait();
     pdl_trigger();
     for (int t0 = 0; t0 < T; t0 += 4) {
         const int nt = min(4, T - t0);
-        float acc[4][4];
+        float acc[4][EPL];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int q = 0; q < EPL; ++q) acc[t][q] = 0.0f;
         for (int m0 = 0; m0 < nchain; m0 += kChainBatch) {
-            float4 wv[kChainBatch];
+            float wv[kChainBatch][EPL];
             float xv[4][kChainBatch];
 #pragma unroll
             for (int u = 0; u < kChainBatch; ++u) {
                 if (m0 + u < nchain) {
                     const int i = l + (m0 + u) * kRouterPartials;
-                    if (on) wv[u] = (m0 == 0) ? w0[u]
-                                              : __ldg(reinterpret_cast<const float4*>(W + static_cast<int64_t>(i) * E + e0));
+                    if (on) {
+                        if (m0 == 0) {
+#pragma unroll
+                            for (int q = 0; q < EPL; ++q) wv[u][q] = w0[u][q];
+                        } else {
+                            load_w_row<EPL>(W, static_cast<int64_t>(i) * E + e0, wv[u]);
+                        }
+                    }
 #pragma unroll
                     for (int t = 0; t < 4; ++t)
                         xv[t][u] = (t < nt) ? load_x(x, xt, static_cast<int64_t>(t0 + t) * d + i) : 0.0f;
@@ -658,33 +685,31 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
                 for (int u = 0; u < kChainBatch; ++u) {
                     if (m0 + u < nchain) {
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            acc[t][0] = fmaf(xv[t][u], wv[u].x, acc[t][0]);
-                            acc[t][1] = fmaf(xv[t][u], wv[u].y, acc[t][1]);
-                            acc[t][2] = fmaf(xv[t][u], wv[u].z, acc[t][2]);
-                            acc[t][3] = fmaf(xv[t][u], wv[u].w, acc[t][3]);
-                        }
+                        for (int t = 0; t < 4; ++t)
+#pragma unroll
+                            for (int q = 0; q < EPL; ++q) acc[t][q] = fmaf(xv[t][u], wv[u][q], acc[t][q]);
                     }
                 }
             }
         }
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-            *reinterpret_cast<float4*>(&red[warp][t][lane * 4]) = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+#pragma unroll
+            for (int q = 0; q < EPL; ++q) red[warp][t][lane * EPL + q] = acc[t][q];
         __syncthreads();
         // levels h = 128, 64, 32: warp j += warp j + h/32 (same residue c)
-        for (int it = threadIdx.x; it < 4 * kRouteChunk; it += blockDim.x) {
-            const int t = it / kRouteChunk, ee = it % kRouteChunk;
-            float s[8];
+        for (int it = threadIdx.x; it < 4 * kChunk; it += blockDim.x) {
+            const int t = it / kChunk, ee = it % kChunk;
+            float sv[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s[j] = red[j][t][ee];
+            for (int j = 0; j < 8; ++j) sv[j] = red[j][t][ee];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) s[j] = s[j] + s[j + 4];
+            for (int j = 0; j < 4; ++j) sv[j] = sv[j] + sv[j + 4];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) s[j] = s[j] + s[j + 2];
-            s[0] = s[0] + s[1];
-            const int e = chunk * kRouteChunk + ee;
-            if (t < nt && e < E) ws.rpart[(static_cast<int64_t>(t0 + t) * E + e) * kResidues + c] = s[0];
+            for (int j = 0; j < 2; ++j) sv[j] = sv[j] + sv[j + 2];
+            sv[0] = sv[0] + sv[1];
+            const int e = chunk * kChunk + ee;
+            if (t < nt && e < E) ws.rpart[(static_cast<int64_t>(t0 + t) * E + e) * kResidues + c] = sv[0];
         }
         __syncthreads();
     }
@@ -699,38 +724,74 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
     // levels h = 16 .. 1 across the 32 residues
     for (int it = threadIdx.x; it < T * E; it += blockDim.x) {
         const float4* pp = reinterpret_cast<const float4*>(ws.rpart + static_cast<int64_t>(it) * kResidues);
-        float s[kResidues];
+        float sv[kResidues];
 #pragma unroll
         for (int q = 0; q < kResidues / 4; ++q) {
             const float4 v = __ldcg(pp + q);
-            s[4 * q] = v.x, s[4 * q + 1] = v.y, s[4 * q + 2] = v.z, s[4 * q + 3] = v.w;
+            sv[4 * q] = v.x, sv[4 * q + 1] = v.y, sv[4 * q + 2] = v.z, sv[4 * q + 3] = v.w;
         }
 #pragma unroll
         for (int h = kResidues / 2; h >= 1; h >>= 1)
 #pragma unroll
-            for (int j = 0; j < h; ++j) s[j] = s[j] + s[j + h];
-        slog[it] = s[0];
-        ws.logits[it] = s[0];
+            for (int j = 0; j < h; ++j) sv[j] = sv[j] + sv[j + h];
+        slog[it] = sv[0];
+        ws.logits[it] = sv[0];
     }
     __syncthreads();
-    // Top-k by rank: expert e's slot is the number of experts that beat it (larger logit, or
-    // equal logit and lower index) -- the order repeated selection would produce, computed
-    // for all (token, expert) at once.
+    // Top-k: expert e's slot is the number of experts that beat it -- the order repeated
+    // selection would produce, computed for all (token, expert) at once.
     __shared__ float stop[1024];
-    for (int it = threadIdx.x; it < T * E; it += blockDim.x) {
-        const int t = it / E, e = it % E;
-        const float v = slog[it];
-        const float4* row = reinterpret_cast<const float4*>(slog + t * E);
-        int rank = 0;
-        for (int q = 0; q < E / 4; ++q) {
-            const float4 o = row[q];
-            const int b = 4 * q;
-            rank += (o.x > v || (o.x == v && b < e)) + (o.y > v || (o.y == v && b + 1 < e)) +
-                    (o.z > v || (o.z == v && b + 2 < e)) + (o.w > v || (o.w == v && b + 3 < e));
+    if (E <= kRankTopkMaxE) {
+        for (int it = threadIdx.x; it < T * E; it += blockDim.x) {
+            const int t = it / E, e = it % E;
+            const float v = slog[it];
+            const float4* row = reinterpret_cast<const float4*>(slog + t * E);
+            int rank = 0;
+            for (int q = 0; q < E / 4; ++q) {
+                const float4 o = row[q];
+                const int b = 4 * q;
+                rank += beats(o.x, b, v, e) + beats(o.y, b + 1, v, e) + beats(o.z, b + 2, v, e) + beats(o.w, b + 3, v, e);
+            }
+            if (rank < k) {
+                sidx[t * k + rank] = e;
+                stop[t * k + rank] = v;
+            }
         }
-        if (rank < k) {
-            sidx[t * k + rank] = e;
-            stop[t * k + rank] = v;
+    } else {
+        // Many experts (then T <= 4096 / E is small): per token, an expert can be among the k
+        // best only if fewer than k experts of its own segment (E split into 8) beat it; the
+        // experts that beat a top-k member are top-k members themselves, so ranks counted
+        // among these candidates are exact for the k best.
+        __shared__ int s_ncand;
+        __shared__ int cand_e[8 * kMaxK];
+        const int seg = (E + 7) / 8;
+        for (int t = 0; t < T; ++t) {
+            if (threadIdx.x == 0) s_ncand = 0;
+            __syncthreads();
+            const float* row = slog + t * E;
+            for (int e = threadIdx.x; e < E; e += blockDim.x) {
+                const float v = row[e];
+                const int s0 = (e / seg) * seg, s1 = min(E, s0 + seg);
+                int rank = 0;
+                for (int o = s0; o < s1 && rank < k; ++o) rank += beats(row[o], o, v, e);
+                if (rank < k) cand_e[atomicAdd(&s_ncand, 1)] = e;
+            }
+            __syncthreads();
+            const int nc = s_ncand;
+            for (int i = threadIdx.x; i < nc; i += blockDim.x) {
+                const int e = cand_e[i];
+                const float v = row[e];
+                int rank = 0;
+                for (int j = 0; j < nc; ++j) {
+                    const int o = cand_e[j];
+                    rank += beats(row[o], o, v, e);
+                }
+                if (rank < k) {
+                    sidx[t * k + rank] = e;
+                    stop[t * k + rank] = v;
+                }
+            }
+            __syncthreads();
         }
     }
     __syncthreads();
@@ -750,8 +811,13 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
 
 cudaError_t launch_route_decode(const void* x, int xt, const float* W, int64_t T, int64_t d, int64_t E, int k,
                                 int gwords, const Workspace& ws, cudaStream_t s) {
-    const dim3 grid(kResidues, (unsigned)((E + kRouteChunk - 1) / kRouteChunk));
-    return launch_pdl(route_decode_kernel, grid, dim3(256), 0, s, x, xt, W, (int)T, (int)d, (int)E, k, gwords, ws);
+    // experts per lane: chunks narrow enough that the router weights spread over >= 128 CTAs
+    const int epl = (E <= 128) ? 1 : (E <= 512 ? 2 : 4);
+    const dim3 grid(kResidues, static_cast<unsigned>((E + 32 * epl - 1) / (32 * epl)));
+    const int Ti = static_cast<int>(T), di = static_cast<int>(d), Ei = static_cast<int>(E);
+    if (epl == 1) return launch_pdl(route_decode_kernel<1>, grid, dim3(256), 0, s, x, xt, W, Ti, di, Ei, k, gwords, ws);
+    if (epl == 2) return launch_pdl(route_decode_kernel<2>, grid, dim3(256), 0, s, x, xt, W, Ti, di, Ei, k, gwords, ws);
+    return launch_pdl(route_decode_kernel<4>, grid, dim3(256), 0, s, x, xt, W, Ti, di, Ei, k, gwords, ws);
 }
 
 }  // namespace moe

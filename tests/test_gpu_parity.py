@@ -106,6 +106,30 @@ SMALL = {
     "small_nvfp4_swiglu": synth.Workload("small_nvfp4_swiglu", d=512, f=320, E=8, k=2, act="swiglu", wfmt="nvfp4",
                                          x_dtype="f32", layers=1),
 }
+# Many experts: up to 4096 logits the one-launch routing selects the top-k through segment
+# candidates once E > 256 (T = 1, 3, 8 here); T = 16 goes through the separate kernels.
+WIDE = synth.Workload("wide_e512", d=256, f=128, E=512, k=6, act="relu2", wfmt="q8_0", x_dtype="bf16", layers=1,
+                      zero_fraction=0.8)
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 16])
+def test_layer_many_experts_parity(T):
+    L, out, tr, ref = _run_small(WIDE, T)
+    assert np.array_equal(tr["logits"].cpu().numpy().view(np.uint32), ref["logits"].view(np.uint32))
+    assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
+    assert np.allclose(tr["w"].cpu().numpy(), ref["w"], rtol=1e-6, atol=0)
+    assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
+    assert_close(out, ref["out"])
+
+
+def test_many_experts_ties_take_lowest_indices():
+    # all logits equal (x = 0): the k lowest expert indices, uniform weights
+    L = layers.build_layer(WIDE, source="numpy")
+    x = torch.zeros((3, WIDE.d), dtype=torch.bfloat16, device="cuda")
+    tr = {}
+    L.forward(x, trace=tr)
+    assert (tr["idx"].cpu().numpy() == np.arange(WIDE.k)).all()
+    assert (tr["w"].cpu().numpy() == np.float32(1.0 / WIDE.k)).all()
 
 
 def _run_small(w, T, idx_in=None, w_in=None, path="auto"):
