@@ -460,7 +460,7 @@ def kernel_source_sha():
 
 def measured_traffic(workload, T):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, when it
-    was taken on this kernel source (gemv.cu + common.cuh) and workload; else None."""
+    was taken on this kernel source (gemv.cu + gemm.cu + common.cuh) and workload; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         entry = json.load(open(p)).get(f"{workload}_T{T}")
