@@ -764,6 +764,7 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
         // among these candidates are exact for the k best.
         __shared__ int s_ncand;
         __shared__ int cand_e[8 * kMaxK];
+        __shared__ float cand_v[8 * kMaxK];
         const int seg = (E + 7) / 8;
         for (int t = 0; t < T; ++t) {
             if (threadIdx.x == 0) s_ncand = 0;
@@ -773,19 +774,22 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
                 const float v = row[e];
                 const int s0 = (e / seg) * seg, s1 = min(E, s0 + seg);
                 int rank = 0;
-                for (int o = s0; o < s1 && rank < k; ++o) rank += beats(row[o], o, v, e);
-                if (rank < k) cand_e[atomicAdd(&s_ncand, 1)] = e;
+#pragma unroll 4
+                for (int o = s0; o < s1; ++o) rank += beats(row[o], o, v, e);
+                if (rank < k) {
+                    const int at = atomicAdd(&s_ncand, 1);
+                    cand_e[at] = e;
+                    cand_v[at] = v;
+                }
             }
             __syncthreads();
             const int nc = s_ncand;
             for (int i = threadIdx.x; i < nc; i += blockDim.x) {
                 const int e = cand_e[i];
-                const float v = row[e];
+                const float v = cand_v[i];
                 int rank = 0;
-                for (int j = 0; j < nc; ++j) {
-                    const int o = cand_e[j];
-                    rank += beats(row[o], o, v, e);
-                }
+#pragma unroll 4
+                for (int j = 0; j < nc; ++j) rank += beats(cand_v[j], cand_e[j], v, e);
                 if (rank < k) {
                     sidx[t * k + rank] = e;
                     stop[t * k + rank] = v;
