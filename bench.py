@@ -55,6 +55,23 @@ def dist_info():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device="cuda") -> float:
+    """The largest of every rank's value, returned on all ranks (the job's time is its
+    slowest replica's); the value itself when there is one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Units per second of the whole job: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -277,13 +294,9 @@ def run_ours(args, rank, world, local_rank):
     e1.record()
     barrier()
     clk = clocks.stop()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world)
     ms_step = ms_total / args.steps
-    tokens_per_s = world * T * args.steps / (ms_total / 1e3)
+    tokens_per_s = job_throughput(T * args.steps, world, ms_total)
 
     # ---- active-expert bytes of one step (from the routing the stack actually took)
     tr_bytes = active_expert_bytes(stack, inputs, T, w)
@@ -360,12 +373,8 @@ def run_ours(args, rank, world, local_rank):
         out_host.copy_(outs[-1], non_blocking=True)
     a1.record()
     barrier()
-    e2e_ms = a0.elapsed_time(a1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * T * e2e_steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1), world)
+    e2e_value = job_throughput(T * e2e_steps, world, e2e_ms)
 
     launches_per_step = sum(layer.launches(T) + 1 for layer in stack)   # + the RMS-norm glue
     result = None
