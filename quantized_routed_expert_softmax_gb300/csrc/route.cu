@@ -652,7 +652,9 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
     for (int u = 0; u < kChainBatch; ++u)
         if (on && u < nchain) load_w_row<EPL>(W, static_cast<int64_t>(l + u * kRouterPartials) * E + e0, w0[u]);
     pdl_wait();
-    pdl_trigger();
+    // No early trigger: the expert kernel that follows is launched once the partial-sum CTAs
+    // have exited (and the last one triggers below), so its CTAs spread over every SM
+    // instead of piling onto the few SMs the routing CTAs leave free.
     for (int t0 = 0; t0 < T; t0 += 4) {
         const int nt = min(4, T - t0);
         float acc[4][EPL];
@@ -720,6 +722,7 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
         s_last = (atomicAdd(ws.route_ctr, 1) == static_cast<int>(gridDim.x * gridDim.y) - 1);
     __syncthreads();
     if (!s_last) return;
+    pdl_trigger();   // the expert kernel's launch overlaps this CTA's selection and permutation
     __threadfence();
     // levels h = 16 .. 1 across the 32 residues
     for (int it = threadIdx.x; it < T * E; it += blockDim.x) {
