@@ -221,6 +221,8 @@ def build_stack(w, T, layers, local_rank):
     from quantized_routed_expert_softmax_gb300 import layers as L
     from quantized_routed_expert_softmax_gb300 import synth
     stack = [L.build_layer(w, layer=l) for l in range(layers)]
+    for l, layer in enumerate(stack):   # each layer warms L2 with the next one's router weights
+        layer.set_l2_prefetch(stack[(l + 1) % layers].router_w)
     inputs = [synth.tokens_cuda(w, T, layer=0, tag=f"bench{r}") for r in range(N_ROTATE)]
     torch.cuda.synchronize()
     return stack, inputs

@@ -162,6 +162,11 @@ typedef struct {
     const void* w_down;           /* E matrices [d][f]: Q8_0 MOE_LAYOUT_DEVICE, NVFP4 MOE_LAYOUT_NEURON */
     const float* gate_up_tscale;  /* NVFP4: fp32 [E] tensor scales of the gate/up matrices */
     const float* down_tscale;     /* NVFP4: fp32 [E] tensor scales of the down matrices */
+    const void* l2_prefetch;      /* optional, may be NULL: device bytes to pull into L2 while this
+                                     layer's expert weights stream -- in a stack, the next layer's
+                                     router weights, so its routing does not wait on HBM.  A hint:
+                                     never read by the layer's arithmetic; 16-byte aligned */
+    int64_t l2_prefetch_bytes;    /* bytes at l2_prefetch (rounded down to a multiple of 16) */
 } moe_layer_desc;
 
 /* Optional copies of intermediate results (device pointers, each may be NULL), and

@@ -21,6 +21,7 @@ cudaError_t launch_route_decode(const void*, int, const float*, int64_t, int64_t
 cudaError_t configure_gemv_kernels();
 cudaError_t launch_gate_up_gemv(const ExpertArgs&, int, int, int, cudaStream_t);
 cudaError_t launch_down_gemv(const ExpertArgs&, int, int, cudaStream_t);
+cudaError_t launch_down_q8_t1(const ExpertArgs&, cudaStream_t);
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int64_t, int, int64_t, float*, cudaStream_t);
 cudaError_t launch_rmsnorm_bf16(const float*, int64_t, int64_t, float, uint16_t*, cudaStream_t);
 cudaError_t configure_gemm_kernels();
@@ -78,6 +79,7 @@ struct Plan {
     bool fuse_combine;  // the down kernel's last CTA per row tile combines (one item per thread)
     bool prefetch_down; // gate.up CTAs prefetch the routed experts' down weights into L2
     bool gemm;          // expert GEMMs on the tensor cores instead of the GEMVs
+    bool down_t1;       // one token, Q8_0 SwiGLU, k in {1,2,4,8}: the row-tile down kernel combines
 };
 
 // The GEMM path tiles rows by 128 (SwiGLU gate.up: 64 neurons' gate and up rows) and K by 64.
@@ -113,6 +115,9 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     // many tokens per expert (at least 8 on average): tensor-core GEMMs
     p.gemm = gemm_shape_ok(d) && (d->path == MOE_PATH_GEMM || (d->path == MOE_PATH_AUTO && p.P >= 8 * d->E));
     if (p.gemm) p.fuse_combine = false;
+    p.down_t1 = !p.gemm && T == 1 && d->wfmt == MOE_W_Q8_0 && d->act == MOE_ACT_SWIGLU &&
+                (d->k == 1 || d->k == 2 || d->k == 4 || d->k == 8) && d->f / 32 >= 8 / d->k && d->d % 16 == 0;
+    if (p.down_t1) p.fuse_combine = true;   // the down kernel writes the output rows
     return p;
 }
 
@@ -204,6 +209,7 @@ moe_status validate_desc(const moe_layer_desc* d) {
     if (!d->router_w || !d->w_gate_up || !d->w_down) return MOE_ERR_INVALID_ARG;
     if (d->wfmt == MOE_W_NVFP4 && (!d->gate_up_tscale || !d->down_tscale)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(d->router_w) || !aligned16(d->w_gate_up) || !aligned16(d->w_down)) return MOE_ERR_ALIGNMENT;
+    if (d->l2_prefetch && (d->l2_prefetch_bytes < 0 || !aligned16(d->l2_prefetch))) return MOE_ERR_ALIGNMENT;
     return MOE_OK;
 }
 
@@ -214,7 +220,7 @@ using namespace moe;
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 10000; }
+int32_t moe_abi_version(void) { return 10100; }
 
 const char* moe_status_string(moe_status s) {
     switch (s) {
@@ -377,6 +383,8 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
         a.gu_bytes = static_cast<int64_t>(moe_nvfp4_bytes(a.rows_gu, desc->d));
         a.dn_bytes = static_cast<int64_t>(moe_nvfp4_bytes(desc->d, desc->f));
     }
+    a.pf = static_cast<const uint8_t*>(desc->l2_prefetch);
+    a.pf_bytes = desc->l2_prefetch ? (desc->l2_prefetch_bytes & ~static_cast<int64_t>(15)) : 0;
     a.gu_ts = desc->gate_up_tscale;
     a.dn_ts = desc->down_tscale;
     a.ws = ws;
@@ -392,6 +400,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     mark(2);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (p.gemm) e = launch_expert_gemm(a, 1, desc->wfmt, desc->act, p.slot_cap, static_cast<int>(desc->E), num_sms, s);
+    else if (p.down_t1 && !idx_in) e = launch_down_q8_t1(a, s);   // supplied routing may repeat an expert
     else e = launch_down_gemv(a, desc->wfmt, p.slot_cap, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mark(3);

@@ -64,6 +64,8 @@ struct ExpertArgs {
     int64_t gu_bytes;            // bytes of one expert's gate/up matrix
     const uint8_t* w_dn;
     int64_t dn_bytes;
+    const uint8_t* pf;           // bytes to pull into L2 during the gate.up kernel (a hint), or null
+    int64_t pf_bytes;
     const float* gu_ts;          // NVFP4 tensor scales [E] (or null)
     const float* dn_ts;
     Workspace ws;

@@ -491,6 +491,12 @@ __global__ void __launch_bounds__(256, 3) gate_up_gemv_kernel(ExpertArgs a) {
                 prefetch_l2(a.w_dn + static_cast<int64_t>(e) * a.dn_bytes + off, static_cast<uint32_t>(n));
             }
         }
+        if (a.pf_bytes > 0) {   // this CTA's share of the caller's L2 hint (the next layer's router)
+            const int64_t nct = static_cast<int64_t>(gridDim.x) * gridDim.y;
+            const int64_t share = ((a.pf_bytes + nct - 1) / nct + 127) / 128 * 128;
+            const int64_t off = (static_cast<int64_t>(blockIdx.y) * gridDim.x + tile) * share;
+            if (off < a.pf_bytes) prefetch_l2(a.pf + off, static_cast<uint32_t>(min(share, a.pf_bytes - off)));
+        }
     }
     const float ts = (FMT == MOE_W_NVFP4) ? a.gu_ts[e] : 1.0f;
     for (int t0 = 0; t0 < cnt; t0 += a.tt_gu) {
@@ -661,6 +667,131 @@ __global__ void __launch_bounds__(kDnWarps * 32, 6) down_q8_gemv_kernel(ExpertAr
     }
     cp_async_wait<0>();
     if (a.fuse_combine) combine_rows_if_last(a, rt, rt * 32, 32, spos, sw);
+}
+
+// ------------------------------------------------------------------------------ down, Q8_0, one token
+// One token, SwiGLU (no group skips), k in {1, 2, 4, 8}: a CTA owns 16 output rows for every
+// routed expert and combines them itself, so the expert outputs y never leave the CTA: no
+// global round trip, atomic counter or last-CTA step.  Warp w works on slot w / wps (wps =
+// 8 / k warps per slot, each a contiguous share of the K panels) through a ring of 16-row
+// panel blocks (512 code bytes, then 16 fp16 scales).  grid: d/16 x 256 threads.
+constexpr int kT1SlotBytes = 512 + 64;
+constexpr int kT1Stages = 12;   // each warp walks a slot's whole K: a deeper ring than the other kernels
+
+__global__ void __launch_bounds__(256, 2) down_q8_t1_kernel(ExpertArgs a, int wps) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int row0 = blockIdx.x * 16;
+    const int slot = warp / wps, part = warp % wps;
+    extern __shared__ __align__(16) unsigned char dsm[];
+    unsigned char* ring = dsm + warp * kT1Stages * kT1SlotBytes;
+    __half* hs = reinterpret_cast<__half*>(dsm + 8 * kT1Stages * kT1SlotBytes);   // [k][f] hi, then lo
+    __shared__ float red[8][16];
+    __shared__ int s_pos[8];
+    __shared__ float s_w[8];
+    // Slot records come from the routing kernel, complete before the gate.up grid this
+    // launch depends on started: the weights stream in while gate.up still runs.
+    const int4 si = __ldcg(a.ws.slot_info + slot);
+    const int e = si.x, hrow = si.y;
+    const int npan = a.f / 32;
+    const int pb = part * npan / wps, pe = (part + 1) * npan / wps;
+    const int n = pe - pb;
+    const int64_t stride = static_cast<int64_t>(a.d) * 34;
+    const uint8_t* P = a.w_dn + static_cast<int64_t>(e) * a.dn_bytes + static_cast<int64_t>(pb) * stride;
+    const uint8_t* srcC = P + static_cast<int64_t>(row0) * 32 + lane * 16;       // 16 rows x 32 codes = 32 x 16 B
+    const uint8_t* srcS = P + static_cast<int64_t>(a.d) * 32 + row0 * 2 + lane * 16;   // 32 scale bytes, lanes 0-1
+    const uint64_t pol = l2_evict_first_policy();
+    const uint32_t ring_addr = smem_addr(ring);
+    auto issue = [&](int s) {
+        const uint32_t sl = ring_addr + s * kT1SlotBytes;
+        cp_async16_ef(sl + lane * 16, srcC, pol);
+        if (lane < 2) cp_async16(sl + 512 + lane * 16, srcS);
+        srcC += stride;
+        srcS += stride;
+    };
+#pragma unroll
+    for (int s = 0; s < kT1Stages; ++s) {
+        if (s < n) issue(s);
+        cp_async_commit();
+    }
+    pdl_wait();
+    pdl_trigger();
+    const int k = a.k;
+    if (threadIdx.x < k) {   // the token's pairs: sorted row (= slot, one token) and weight
+        s_pos[threadIdx.x] = __ldcg(a.ws.pos + threadIdx.x);
+        s_w[threadIdx.x] = __ldcg(a.ws.w + threadIdx.x);
+    }
+    // h of the k pairs (sorted rows 0..k-1) as f16 hi + lo
+    const int lo_off = k * a.f;
+    {
+        const float4* src = reinterpret_cast<const float4*>(a.ws.h);
+        __half2* hi = reinterpret_cast<__half2*>(hs);
+        __half2* lo = reinterpret_cast<__half2*>(hs + lo_off);
+        for (int i = threadIdx.x; i < k * a.f / 4; i += blockDim.x) {
+            const float4 v = __ldcg(src + i);
+            split_f16(v.x, v.y, hi[2 * i], lo[2 * i]);
+            split_f16(v.z, v.w, hi[2 * i + 1], lo[2 * i + 1]);
+        }
+    }
+    __syncthreads();
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const __half* xrow = hs + hrow * a.f;            // this slot's token (lane group g == 0)
+    for (int i0 = 0; i0 < n; i0 += kT1Stages) {
+#pragma unroll
+        for (int s = 0; s < kT1Stages; ++s) {
+            const int i = i0 + s;
+            if (i < n) {
+                cp_async_wait<kT1Stages - 1>();
+                __syncwarp();
+                const unsigned char* cb = ring + s * kT1SlotBytes;
+                const int b = pb + i;
+                uint4 xv = make_uint4(0, 0, 0, 0), xl = make_uint4(0, 0, 0, 0);
+                if (g == 0) {
+                    xv = *reinterpret_cast<const uint4*>(xrow + b * 32 + 8 * t);
+                    xl = *reinterpret_cast<const uint4*>(xrow + lo_off + b * 32 + 8 * t);
+                }
+                const uint2 r0 = *reinterpret_cast<const uint2*>(cb + g * 32 + 8 * t);
+                const uint2 r8 = *reinterpret_cast<const uint2*>(cb + (g + 8) * 32 + 8 * t);
+                const unsigned short* sc = reinterpret_cast<const unsigned short*>(cb + 512);
+                const float s0 = __half2float(__ushort_as_half(sc[g]));
+                const float s8 = __half2float(__ushort_as_half(sc[g + 8]));
+                uint32_t a0, a2, a1, a3, c0, c2, c1, c3;
+                s8x4_to_f16x2x2(r0.x, a0, a2);
+                s8x4_to_f16x2x2(r8.x, a1, a3);
+                s8x4_to_f16x2x2(r0.y, c0, c2);
+                s8x4_to_f16x2x2(r8.y, c1, c3);
+                float dd[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(dd, a0, a1, a2, a3, xv.x, xv.y);
+                mma16816(dd, c0, c1, c2, c3, xv.z, xv.w);
+                mma16816(dd, a0, a1, a2, a3, xl.x, xl.y);
+                mma16816(dd, c0, c1, c2, c3, xl.z, xl.w);
+                acc[0] = fmaf(s0, dd[0], acc[0]);
+                acc[2] = fmaf(s8, dd[2], acc[2]);
+                __syncwarp();   // every lane is done with the slot before it is refilled
+                if (i + kT1Stages < n) issue(s);
+                cp_async_commit();
+            }
+        }
+    }
+    cp_async_wait<0>();
+    // token column 0 of the accumulator: rows g (acc[0]) and g + 8 (acc[2]) on lanes t == 0
+    if (t == 0) {
+        red[warp][g] = acc[0];
+        red[warp][g + 8] = acc[2];
+    }
+    __syncthreads();
+    // y[slot][r]: the slot's warps in order; out[r] = sum over the token's pairs j in order
+    if (threadIdx.x < 16) {
+        const int r = threadIdx.x;
+        float o = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int sj = s_pos[j];                  // sorted row of pair j = its slot (one token)
+            float y = 0.0f;
+            for (int q = 0; q < wps; ++q) y += red[sj * wps + q][r];
+            o = fmaf(s_w[j], y, o);
+        }
+        a.out[row0 + r] = o;
+    }
 }
 
 // ------------------------------------------------------------------------------ down, NVFP4
@@ -911,6 +1042,8 @@ cudaError_t configure_gemv_kernels() {
             cudaError_t e = gu_dispatch(a, w, c, dim3(1), 0, nullptr, true);
             if (e != cudaSuccess) return e;
         }
+    cudaError_t e0 = allow_smem(down_q8_t1_kernel, 200 * 1024);
+    if (e0 != cudaSuccess) return e0;
     const int tts[3] = {1, 2, 4};
     for (int tt : tts) {
         a.tt_dn = tt;
@@ -935,6 +1068,15 @@ size_t down_gemv_smem(int wfmt, int tt_dn, int f) {
         return static_cast<size_t>(t4) * f * sizeof(float) + static_cast<size_t>(8) * t4 * 256 * sizeof(float);
     }
     return static_cast<size_t>(kDnWarps) * kStages * kSlotBytes + static_cast<size_t>(tt_dn) * f * 2 * 2;
+}
+
+size_t down_t1_smem(int k, int f) {
+    return static_cast<size_t>(8) * kT1Stages * kT1SlotBytes + static_cast<size_t>(k) * f * 2 * 2;
+}
+
+cudaError_t launch_down_q8_t1(const ExpertArgs& a, cudaStream_t s) {
+    const int wps = 8 / a.k;
+    return launch_pdl(down_q8_t1_kernel, dim3(a.d / 16), dim3(256), down_t1_smem(a.k, a.f), s, a, wps);
 }
 
 cudaError_t launch_down_gemv(const ExpertArgs& a, int wfmt, int slot_cap, cudaStream_t s) {

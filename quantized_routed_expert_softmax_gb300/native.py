@@ -41,6 +41,7 @@ class LayerDesc(ctypes.Structure):
         ("k", ctypes.c_int32), ("act", ctypes.c_int32), ("wfmt", ctypes.c_int32), ("path", ctypes.c_int32),
         ("router_w", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
         ("gate_up_tscale", ctypes.c_void_p), ("down_tscale", ctypes.c_void_p),
+        ("l2_prefetch", ctypes.c_void_p), ("l2_prefetch_bytes", ctypes.c_int64),
     ]
 
 
@@ -184,6 +185,13 @@ class MoELayer:
                               _ptr(gate_up_tscale), _ptr(down_tscale))
         self._ws = None
         self._ws_tokens = 0
+
+    def set_l2_prefetch(self, t) -> None:
+        """Bytes (a device tensor, or None) that this layer pulls into L2 while its experts
+        stream: in a stack, the next layer's router weights."""
+        self._l2_prefetch = t
+        self.desc.l2_prefetch = _ptr(t) if t is not None else None
+        self.desc.l2_prefetch_bytes = 0 if t is None else t.numel() * t.element_size()
 
     def set_path(self, path: str) -> None:
         self.desc.path = PATH[path]

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.moe_abi_version() == 10000
+    assert L.moe_abi_version() == 10100
     for s in range(8):
         assert L.moe_status_string(s).decode().startswith(native.STATUS_NAMES[s])
 

@@ -193,6 +193,25 @@ def test_layer_gemm_skewed_routing():
     assert_close(out, ref["out"])
 
 
+# One token, Q8_0 SwiGLU, k in {1, 2, 4, 8}: the down kernel owns 16 output rows for every
+# routed expert and combines in place.  k = 1 gives eight warps per expert; a supplied routing
+# that names one expert twice must take the general path (two rows in one slot).
+@pytest.mark.parametrize("k", [1, 4])
+def test_one_token_row_tile_down(k):
+    w = synth.Workload(f"t1_k{k}", d=512, f=256, E=8, k=k, act="swiglu", wfmt="q8_0", x_dtype="bf16", layers=1)
+    L, out, tr, ref = _run_small(w, 1)
+    assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
+    assert_close(out, ref["out"])
+
+
+def test_one_token_repeated_expert_in_supplied_routing():
+    w = SMALL["tiny_q8_swiglu"]
+    idx = np.array([[3, 3]], dtype=np.int32)
+    wts = np.array([[0.25, 0.75]], dtype=np.float32)
+    L, out, tr, ref = _run_small(w, 1, idx_in=idx, w_in=wts)
+    assert_close(out, ref["out"])
+
+
 @pytest.mark.parametrize("T", [5, 64])
 def test_layer_supplied_routing(T):
     w = SMALL["tiny_q8_swiglu"]
