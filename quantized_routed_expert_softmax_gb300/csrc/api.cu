@@ -80,6 +80,7 @@ struct Plan {
     bool prefetch_down; // gate.up CTAs prefetch the routed experts' down weights into L2
     bool gemm;          // expert GEMMs on the tensor cores instead of the GEMVs
     bool down_t1;       // one token, Q8_0 SwiGLU, k in {1,2,4,8}: the row-tile down kernel combines
+    int nv_split;       // NVFP4 down with fused combine: group splits per (row tile, slot)
 };
 
 // The GEMM path tiles rows by 128 (SwiGLU gate.up: 64 neurons' gate and up rows) and K by 64.
@@ -118,6 +119,7 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     p.down_t1 = !p.gemm && T == 1 && d->wfmt == MOE_W_Q8_0 && d->act == MOE_ACT_SWIGLU &&
                 (d->k == 1 || d->k == 2 || d->k == 4 || d->k == 8) && d->f / 32 >= 8 / d->k && d->d % 16 == 0;
     if (p.down_t1) p.fuse_combine = true;   // the down kernel writes the output rows
+    p.nv_split = (!p.gemm && d->wfmt == MOE_W_NVFP4 && p.fuse_combine && T == 1 && (d->f / 16) >= 4 * 8) ? 4 : 1;
     return p;
 }
 
@@ -155,7 +157,7 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     L.local_rank = take(sizeof(int32_t) * p.P);
     L.gmask = take(sizeof(uint32_t) * p.slot_cap * p.gwords);
     L.h = take(sizeof(float) * p.P * d->f);
-    L.y = take(sizeof(float) * p.P * d->d);
+    L.y = take(sizeof(float) * p.P * d->d * p.nv_split);   // NVFP4 split partials
     // f16 planes of the tensor-core path (the lo plane of x is used by fp32 inputs only)
     const size_t xs = p.gemm ? sizeof(uint16_t) * p.P * d->d : 0;
     const size_t hs = p.gemm ? sizeof(uint16_t) * p.P * d->f : 0;
@@ -373,6 +375,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.P = static_cast<int>(p.P);
     a.fuse_combine = p.fuse_combine ? 1 : 0;
     a.prefetch_down = p.prefetch_down ? 1 : 0;
+    a.nv_split = p.nv_split;
     a.out = out;
     a.w_gu = static_cast<const uint8_t*>(desc->w_gate_up);
     a.w_dn = static_cast<const uint8_t*>(desc->w_down);

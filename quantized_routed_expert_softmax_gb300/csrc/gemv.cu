@@ -559,11 +559,12 @@ __device__ __forceinline__ void preload_pairs(const ExpertArgs& a, int* spos, fl
 // the last one of row tile [row0, row0+nrows) combines those rows for every token:
 // out[t][r] = sum_{j<k} w[t][j] * y[pos(t,j)][r], in slot order.
 __device__ __forceinline__ void combine_rows_if_last(const ExpertArgs& a, int tile, int row0, int nrows,
-                                                     const int* spos, const float* sw) {
+                                                     const int* spos, const float* sw, int nsplit = 1) {
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(a.ws.row_ctr + tile, 1) == static_cast<int>(gridDim.y) - 1);
+    if (threadIdx.x == 0)
+        s_last = (atomicAdd(a.ws.row_ctr + tile, 1) == static_cast<int>(gridDim.y) * nsplit - 1);
     __syncthreads();
     if (!s_last) return;
     __threadfence();
@@ -574,6 +575,12 @@ __device__ __forceinline__ void combine_rows_if_last(const ExpertArgs& a, int ti
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j)     // every load of the item in flight at once
             if (j < k) yj[j] = __ldcg(a.ws.y + static_cast<int64_t>(spos[t * k + j]) * a.d + r);
+        for (int z = 1; z < nsplit; ++z) {  // partial sums of the other group splits, in order
+            const float* yz = a.ws.y + static_cast<int64_t>(z) * a.P * a.d;
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j)
+                if (j < k) yj[j] += __ldcg(yz + static_cast<int64_t>(spos[t * k + j]) * a.d + r);
+        }
         float acc = 0.0f;
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j)
@@ -798,8 +805,13 @@ __global__ void __launch_bounds__(256, 2) down_q8_t1_kernel(ExpertArgs a, int wp
 // NVFP4 down matrices in the neuron layout: per group of 16 neurons, each neuron's codes
 // for all d rows (d/2 bytes), then the d scale bytes.  A CTA covers 256 rows (lane l:
 // rows 8l .. 8l+7, 4 code bytes per neuron, 8 scale bytes); its 8 warps split the groups
-// and meet in shared memory.  Inactive groups are not read at all.  grid: (d/256, slots).
-constexpr int kMaxGroupsInFlight = 2;
+// and meet in shared memory.  Inactive groups are not read at all.  grid: (d/256, slots,
+// splits): with several splits (one token, fused combine) each CTA takes a share of the
+// groups and writes a partial y; the combining CTA adds the splits in order.
+// groups whose loads are in flight per warp (more costs registers, and with them the
+// CTAs per SM that the split grid of the one-token case relies on)
+template <int N>
+constexpr int groups_in_flight() { return 2; }
 
 template <int N>
 __device__ __forceinline__ void dn_nv_tile(const ExpertArgs& a, const uint8_t* W, int rt, int gb, int ge,
@@ -808,14 +820,15 @@ __device__ __forceinline__ void dn_nv_tile(const ExpertArgs& a, const uint8_t* W
     const int d = a.d, f = a.f;
     const int lane = threadIdx.x & 31;
     const int64_t rec = 16 * (d / 2) + d;
-    uint32_t codes[kMaxGroupsInFlight][16];
-    uint2 sc[kMaxGroupsInFlight];
-    int gid[kMaxGroupsInFlight];
+    constexpr int kGif = groups_in_flight<N>();
+    uint32_t codes[kGif][16];
+    uint2 sc[kGif];
+    int gid[kGif];
     int g = gb;
     // gather the next batch of active groups and issue their loads
     auto issue = [&]() {
         int n = 0;
-        while (g < ge && n < kMaxGroupsInFlight) {
+        while (g < ge && n < kGif) {
             if ((gm[g >> 5] >> (g & 31)) & 1u) {
                 gid[n] = g;
                 ++n;
@@ -823,7 +836,7 @@ __device__ __forceinline__ void dn_nv_tile(const ExpertArgs& a, const uint8_t* W
             ++g;
         }
 #pragma unroll
-        for (int u = 0; u < kMaxGroupsInFlight; ++u) {
+        for (int u = 0; u < kGif; ++u) {
             if (u < n) {
                 const uint8_t* base = W + gid[u] * rec;
 #pragma unroll
@@ -838,7 +851,7 @@ __device__ __forceinline__ void dn_nv_tile(const ExpertArgs& a, const uint8_t* W
     __syncthreads();
     while (n > 0) {
 #pragma unroll
-        for (int u = 0; u < kMaxGroupsInFlight; ++u) {
+        for (int u = 0; u < kGif; ++u) {
             if (u < n) {
                 float part[N][8];
 #pragma unroll
@@ -873,7 +886,7 @@ __device__ __forceinline__ void dn_nv_tile(const ExpertArgs& a, const uint8_t* W
 }
 
 template <int TT>
-__global__ void __launch_bounds__(256) down_nv_gemv_kernel(ExpertArgs a) {
+__global__ void __launch_bounds__(256, TT == 1 ? 3 : 1) down_nv_gemv_kernel(ExpertArgs a) {
     pdl_wait();
     pdl_trigger();
     const int slot = blockIdx.y;
@@ -891,9 +904,12 @@ __global__ void __launch_bounds__(256) down_nv_gemv_kernel(ExpertArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rt = blockIdx.x;
     const int ng = a.f / 16;
-    const int gb = warp * ng / 8, ge = (warp + 1) * ng / 8;
+    const int z = blockIdx.z, nz = gridDim.z;
+    const int zb = z * ng / nz, ze = (z + 1) * ng / nz;      // this split's groups
+    const int gb = zb + warp * (ze - zb) / 8, ge = zb + (warp + 1) * (ze - zb) / 8;
     const uint8_t* W = a.w_dn + static_cast<int64_t>(e) * a.dn_bytes;
     const float ts = cnt > 0 ? a.dn_ts[e] : 0.0f;
+    float* ydst = a.ws.y + static_cast<int64_t>(z) * a.P * a.d;
     for (int t0 = 0; t0 < cnt; t0 += TT) {
         const int nt = min(TT, cnt - t0);
 #define MOE_DN_NV_CASE(NN)                                                                          \
@@ -918,11 +934,11 @@ __global__ void __launch_bounds__(256) down_nv_gemv_kernel(ExpertArgs a) {
             float yv = 0.0f;
 #pragma unroll
             for (int w = 0; w < 8; ++w) yv += red[(w * TT + t) * 256 + r];
-            a.ws.y[static_cast<int64_t>(r0 + t0 + t) * a.d + rt * 256 + r] = yv * ts;
+            ydst[static_cast<int64_t>(r0 + t0 + t) * a.d + rt * 256 + r] = yv * ts;
         }
         __syncthreads();
     }
-    if (a.fuse_combine) combine_rows_if_last(a, rt, rt * 256, 256, spos, sw);
+    if (a.fuse_combine) combine_rows_if_last(a, rt, rt * 256, 256, spos, sw, nz);
 }
 
 // ------------------------------------------------------------------------------ combine
@@ -1015,7 +1031,7 @@ static cudaError_t gu_dispatch(const ExpertArgs& a, int wfmt, int act, dim3 grid
 template <int TT>
 static cudaError_t dn_nv_launch(const ExpertArgs& a, int slot_cap, size_t smem, cudaStream_t s, bool configure) {
     if (configure) return allow_smem(down_nv_gemv_kernel<TT>, 200 * 1024);
-    return launch_pdl(down_nv_gemv_kernel<TT>, dim3(a.d / 256, slot_cap), dim3(256), smem, s, a);
+    return launch_pdl(down_nv_gemv_kernel<TT>, dim3(a.d / 256, slot_cap, a.nv_split), dim3(256), smem, s, a);
 }
 
 static cudaError_t dn_dispatch(const ExpertArgs& a, int wfmt, int slot_cap, size_t smem, cudaStream_t s,
