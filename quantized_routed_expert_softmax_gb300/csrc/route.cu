@@ -724,21 +724,34 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
     if (!s_last) return;
     pdl_trigger();   // the expert kernel's launch overlaps this CTA's selection and permutation
     __threadfence();
-    // levels h = 16 .. 1 across the 32 residues
-    for (int it = threadIdx.x; it < T * E; it += blockDim.x) {
-        const float4* pp = reinterpret_cast<const float4*>(ws.rpart + static_cast<int64_t>(it) * kResidues);
-        float sv[kResidues];
+    // levels h = 16 .. 1 across the 32 residues; two logits per thread with all their loads
+    // issued before either tree
+    for (int it0 = threadIdx.x; it0 < T * E; it0 += 2 * blockDim.x) {
+        float sv[2][kResidues];
 #pragma unroll
-        for (int q = 0; q < kResidues / 4; ++q) {
-            const float4 v = __ldcg(pp + q);
-            sv[4 * q] = v.x, sv[4 * q + 1] = v.y, sv[4 * q + 2] = v.z, sv[4 * q + 3] = v.w;
+        for (int u = 0; u < 2; ++u) {
+            const int it = it0 + u * blockDim.x;
+            if (it < T * E) {
+                const float4* pp = reinterpret_cast<const float4*>(ws.rpart + static_cast<int64_t>(it) * kResidues);
+#pragma unroll
+                for (int q = 0; q < kResidues / 4; ++q) {
+                    const float4 v = __ldcg(pp + q);
+                    sv[u][4 * q] = v.x, sv[u][4 * q + 1] = v.y, sv[u][4 * q + 2] = v.z, sv[u][4 * q + 3] = v.w;
+                }
+            }
         }
 #pragma unroll
-        for (int h = kResidues / 2; h >= 1; h >>= 1)
+        for (int u = 0; u < 2; ++u) {
+            const int it = it0 + u * blockDim.x;
+            if (it < T * E) {
 #pragma unroll
-            for (int j = 0; j < h; ++j) sv[j] = sv[j] + sv[j + h];
-        slog[it] = sv[0];
-        ws.logits[it] = sv[0];
+                for (int h = kResidues / 2; h >= 1; h >>= 1)
+#pragma unroll
+                    for (int j = 0; j < h; ++j) sv[u][j] = sv[u][j] + sv[u][j + h];
+                slog[it] = sv[u][0];
+                ws.logits[it] = sv[u][0];
+            }
+        }
     }
     __syncthreads();
     // Top-k: expert e's slot is the number of experts that beat it -- the order repeated
@@ -765,34 +778,38 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
         // best only if fewer than k experts of its own segment (E split into 8) beat it; the
         // experts that beat a top-k member are top-k members themselves, so ranks counted
         // among these candidates are exact for the k best.
-        __shared__ int s_ncand;
+        // Each segment's candidates go to fixed slots seg * k + (rank in the segment), so
+        // no atomic counter is needed; empty slots hold -1.
         __shared__ int cand_e[8 * kMaxK];
         __shared__ float cand_v[8 * kMaxK];
         const int seg = (E + 7) / 8;
+        const int ncs = 8 * k;
         for (int t = 0; t < T; ++t) {
-            if (threadIdx.x == 0) s_ncand = 0;
+            for (int i = threadIdx.x; i < ncs; i += blockDim.x) cand_e[i] = -1;
             __syncthreads();
             const float* row = slog + t * E;
             for (int e = threadIdx.x; e < E; e += blockDim.x) {
                 const float v = row[e];
-                const int s0 = (e / seg) * seg, s1 = min(E, s0 + seg);
+                const int sg = e / seg, s0 = sg * seg, s1 = min(E, s0 + seg);
                 int rank = 0;
 #pragma unroll 4
                 for (int o = s0; o < s1; ++o) rank += beats(row[o], o, v, e);
                 if (rank < k) {
-                    const int at = atomicAdd(&s_ncand, 1);
-                    cand_e[at] = e;
-                    cand_v[at] = v;
+                    cand_e[sg * k + rank] = e;
+                    cand_v[sg * k + rank] = v;
                 }
             }
             __syncthreads();
-            const int nc = s_ncand;
-            for (int i = threadIdx.x; i < nc; i += blockDim.x) {
+            for (int i = threadIdx.x; i < ncs; i += blockDim.x) {
                 const int e = cand_e[i];
+                if (e < 0) continue;
                 const float v = cand_v[i];
                 int rank = 0;
 #pragma unroll 4
-                for (int j = 0; j < nc; ++j) rank += beats(cand_v[j], cand_e[j], v, e);
+                for (int j = 0; j < ncs; ++j) {
+                    const int o = cand_e[j];
+                    rank += (o >= 0) && beats(cand_v[j], o, v, e);
+                }
                 if (rank < k) {
                     sidx[t * k + rank] = e;
                     stop[t * k + rank] = v;
@@ -812,7 +829,28 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
         ws.w[p] = expf(stop[p] - m0) / sum;
     }
     __syncthreads();
-    permute_block_256(sidx, T, k, E, gwords, ws);
+    if (T == 1) {
+        // One token, k distinct experts: pair j's sorted row (= its slot) is the number of
+        // selected experts with a lower index.
+        for (int j = threadIdx.x; j < k; j += blockDim.x) {
+            const int e = sidx[j];
+            int r = 0;
+            for (int i = 0; i < k; ++i) r += sidx[i] < e;
+            ws.perm[r] = j;
+            ws.pos[j] = r;
+            ws.act_e[r] = e;
+            ws.slot_info[r] = make_int4(e, r, 1, 0);   // one row: token 0
+        }
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+            int c = 0;
+            for (int i = 0; i < k; ++i) c += sidx[i] < e;
+            ws.offsets[e] = c;
+        }
+        if (threadIdx.x == 0) *ws.n_active = k;
+        for (int i = threadIdx.x; i < k * gwords; i += blockDim.x) ws.gmask[i] = 0;
+    } else {
+        permute_block_256(sidx, T, k, E, gwords, ws);
+    }
     if (threadIdx.x == 0) *ws.route_ctr = 0;
 }
 
