@@ -25,6 +25,7 @@ cudaError_t launch_down_q8_t1(const ExpertArgs&, cudaStream_t);
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int64_t, int, int64_t, float*, cudaStream_t);
 cudaError_t launch_rmsnorm_bf16(const float*, int64_t, int64_t, float, uint16_t*, cudaStream_t);
 cudaError_t configure_gemm_kernels();
+cudaError_t configure_route_kernels();
 cudaError_t launch_expert_gemm(const ExpertArgs&, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_gather_x_f16(const ExpertArgs&, int, cudaStream_t);
 
@@ -59,6 +60,7 @@ cudaError_t ensure_configured(int* num_sms) {
     if (!done[dev]) {
         e = configure_gemv_kernels();
         if (e == cudaSuccess) e = configure_gemm_kernels();
+        if (e == cudaSuccess) e = configure_route_kernels();
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         done[dev] = true;

@@ -323,10 +323,10 @@ __device__ __forceinline__ void load_slot(const GemmArgs& g, uint32_t dst, int e
     }
     const int p0 = ks0 * (q8 ? 2 : 1);   // first K panel
     if (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU) {
-        tma_5d(dst, &g.tw_codes, 0, mtile * 64, 0, p0, e, bar);
+        tma_5d(dst, &g.tw_codes, 0, mtile * 8, 0, p0, e, bar);
         tma_4d(dst + scales_at, &g.tw_scales, mtile * 64, 0, p0, e, bar);
     } else {
-        tma_4d(dst, &g.tw_codes, 0, mtile * kTileM, p0, e, bar);
+        tma_4d(dst, &g.tw_codes, 0, mtile * (kTileM / 8), p0, e, bar);
         tma_3d(dst + scales_at, &g.tw_scales, mtile * kTileM, p0, e, bar);
     }
 }
@@ -858,7 +858,10 @@ cudaError_t weight_maps(GemmArgs* g, const uint8_t* W, int64_t E, int64_t mat_by
         g->slot_bytes = 64 * 16 * 4 * kStepsPerSlot + kTileM * 4 * kStepsPerSlot;
         return encode(&g->tw_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, W + 8 * d, sd, ss, sb, none);
     }
-    // K panels: [rows][32 code bytes] then [rows] scales of 2 (Q8_0) or 4 (NVFP4) bytes
+    // K panels: [rows][32 code bytes] then [rows] scales of 2 (Q8_0) or 4 (NVFP4) bytes.  The
+    // codes of 8 consecutive rows are 256 contiguous bytes: that is the innermost box extent,
+    // since a copy engine handles a box one innermost run at a time and 32-byte runs left it
+    // issuing eight times as many requests for the same bytes.
     const int64_t panel_cols = q8 ? 32 : 64, panels = K / panel_cols;
     const int64_t scb = q8 ? 2 : 4, pbytes = rows_w * (32 + scb);
     const cuuint32_t npan = static_cast<cuuint32_t>((q8 ? 2 : 1) * kStepsPerSlot);
@@ -867,9 +870,9 @@ cudaError_t weight_maps(GemmArgs* g, const uint8_t* W, int64_t E, int64_t mat_by
     cudaError_t e;
     if (g->kind == kGateUp && g->act == MOE_ACT_SWIGLU) {
         const int64_t f = rows_w / 2;   // gate rows 0..f-1, up rows f..2f-1
-        const cuuint64_t cd[5] = {32, static_cast<cuuint64_t>(f), 2, static_cast<cuuint64_t>(panels), e64};
-        const cuuint64_t cs[4] = {32, static_cast<cuuint64_t>(f * 32), static_cast<cuuint64_t>(pbytes), mb};
-        const cuuint32_t cb[5] = {32, 64, 2, npan, 1};
+        const cuuint64_t cd[5] = {256, static_cast<cuuint64_t>(f / 8), 2, static_cast<cuuint64_t>(panels), e64};
+        const cuuint64_t cs[4] = {256, static_cast<cuuint64_t>(f * 32), static_cast<cuuint64_t>(pbytes), mb};
+        const cuuint32_t cb[5] = {256, 8, 2, npan, 1};
         e = encode(&g->tw_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, W, cd, cs, cb, none);
         if (e != cudaSuccess) return e;
         const cuuint64_t sd[4] = {static_cast<cuuint64_t>(f), 2, static_cast<cuuint64_t>(panels), e64};
@@ -877,9 +880,9 @@ cudaError_t weight_maps(GemmArgs* g, const uint8_t* W, int64_t E, int64_t mat_by
         const cuuint32_t sb[4] = {64, 2, npan, 1};
         return encode(&g->tw_scales, st, 4, W + rows_w * 32, sd, ss, sb, none);
     }
-    const cuuint64_t cd[4] = {32, static_cast<cuuint64_t>(rows_w), static_cast<cuuint64_t>(panels), e64};
-    const cuuint64_t cs[3] = {32, static_cast<cuuint64_t>(pbytes), mb};
-    const cuuint32_t cb[4] = {32, kTileM, npan, 1};
+    const cuuint64_t cd[4] = {256, static_cast<cuuint64_t>(rows_w / 8), static_cast<cuuint64_t>(panels), e64};
+    const cuuint64_t cs[3] = {256, static_cast<cuuint64_t>(pbytes), mb};
+    const cuuint32_t cb[4] = {256, kTileM / 8, npan, 1};
     e = encode(&g->tw_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, W, cd, cs, cb, none);
     if (e != cudaSuccess) return e;
     const cuuint64_t sd[3] = {static_cast<cuuint64_t>(rows_w), static_cast<cuuint64_t>(panels), e64};

@@ -10,6 +10,8 @@
 // top-22 of 512 in the Nemotron page).  The permutation is a stable counting sort of
 // the T*k pairs by expert, the grouping an expert-indexed matmul presupposes ("Running
 // Gemma 4 26B ... on a 13-year-old Xeon", section "A three-step fix").
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -739,6 +741,138 @@ __device__ __forceinline__ void load_w_row(const float* __restrict__ W, int64_t 
 // a beats b: larger logit, or equal logit and lower expert index
 __device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) { return va > vb || (va == vb && ea < eb); }
 
+// Selection, weights and permutation from the logits slog[T][E] in shared memory (every
+// thread of the block): top-k with larger first and the lower index on ties, softmax over the
+// k selected logits, then the permutation by expert.
+__device__ __forceinline__ void route_select(const float* slog, int T, int E, int k, int gwords, const Workspace& ws) {
+    // Top-k: expert e's slot is the number of experts that beat it -- the order repeated
+    // selection would produce, computed for all (token, expert) at once.
+    __shared__ int sidx[1024];
+    __shared__ float stop[1024];
+    if (E <= kRankTopkMaxE && 2 * T * E <= static_cast<int>(blockDim.x) && E % 8 == 0) {
+        // two threads per (token, expert), each counting over half the experts
+        const int it = threadIdx.x >> 1, half = threadIdx.x & 1;
+        const bool live = it < T * E;
+        const int t = live ? it / E : 0, e = live ? it % E : 0;
+        const float v = live ? slog[it] : 0.0f;
+        int r[4] = {0, 0, 0, 0};
+        if (live) {
+            const float4* row = reinterpret_cast<const float4*>(slog + t * E) + half * (E / 8);
+            for (int q = 0; q < E / 8; ++q) {
+                const float4 o = row[q];
+                const int b = 4 * (q + half * (E / 8));
+                r[0] += beats(o.x, b, v, e);
+                r[1] += beats(o.y, b + 1, v, e);
+                r[2] += beats(o.z, b + 2, v, e);
+                r[3] += beats(o.w, b + 3, v, e);
+            }
+        }
+        int rank = r[0] + r[1] + r[2] + r[3];
+        rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+        if (live && half == 0 && rank < k) {
+            sidx[t * k + rank] = e;
+            stop[t * k + rank] = v;
+        }
+    } else if (E <= kRankTopkMaxE) {
+        for (int it = threadIdx.x; it < T * E; it += blockDim.x) {
+            const int t = it / E, e = it % E;
+            const float v = slog[it];
+            const float4* row = reinterpret_cast<const float4*>(slog + t * E);
+            int r[4] = {0, 0, 0, 0};
+            for (int q = 0; q < E / 4; ++q) {
+                const float4 o = row[q];
+                const int b = 4 * q;
+                r[0] += beats(o.x, b, v, e);
+                r[1] += beats(o.y, b + 1, v, e);
+                r[2] += beats(o.z, b + 2, v, e);
+                r[3] += beats(o.w, b + 3, v, e);
+            }
+            const int rank = r[0] + r[1] + r[2] + r[3];
+            if (rank < k) {
+                sidx[t * k + rank] = e;
+                stop[t * k + rank] = v;
+            }
+        }
+    } else {
+        // Many experts (then T <= 4096 / E is small): per token, an expert can be among the k
+        // best only if fewer than k experts of its own segment (E split into 8) beat it; the
+        // experts that beat a top-k member are top-k members themselves, so ranks counted
+        // among these candidates are exact for the k best.
+        // Each segment's candidates go to fixed slots seg * k + (rank in the segment), so
+        // no atomic counter is needed; empty slots hold -1.
+        __shared__ int cand_e[8 * kMaxK];
+        __shared__ float cand_v[8 * kMaxK];
+        const int seg = (E + 7) / 8;
+        const int ncs = 8 * k;
+        for (int t = 0; t < T; ++t) {
+            for (int i = threadIdx.x; i < ncs; i += blockDim.x) cand_e[i] = -1;
+            __syncthreads();
+            const float* row = slog + t * E;
+            for (int e = threadIdx.x; e < E; e += blockDim.x) {
+                const float v = row[e];
+                const int sg = e / seg, s0 = sg * seg, s1 = min(E, s0 + seg);
+                int rank = 0;
+#pragma unroll 4
+                for (int o = s0; o < s1; ++o) rank += beats(row[o], o, v, e);
+                if (rank < k) {
+                    cand_e[sg * k + rank] = e;
+                    cand_v[sg * k + rank] = v;
+                }
+            }
+            __syncthreads();
+            for (int i = threadIdx.x; i < ncs; i += blockDim.x) {
+                const int e = cand_e[i];
+                if (e < 0) continue;
+                const float v = cand_v[i];
+                int rank = 0;
+#pragma unroll 4
+                for (int j = 0; j < ncs; ++j) {
+                    const int o = cand_e[j];
+                    rank += (o >= 0) && beats(cand_v[j], o, v, e);
+                }
+                if (rank < k) {
+                    sidx[t * k + rank] = e;
+                    stop[t * k + rank] = v;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    __syncthreads();
+    // softmax over the k selected logits, the maximum (slot 0) subtracted, sum in slot order
+    for (int p = threadIdx.x; p < T * k; p += blockDim.x) {
+        const int t = p / k;
+        const float m0 = stop[t * k];
+        float sum = 0.0f;
+        for (int j = 0; j < k; ++j) sum += expf(stop[t * k + j] - m0);
+        ws.idx[p] = sidx[p];
+        ws.w[p] = expf(stop[p] - m0) / sum;
+    }
+    __syncthreads();
+    if (T == 1) {
+        // One token, k distinct experts: pair j's sorted row (= its slot) is the number of
+        // selected experts with a lower index.
+        for (int j = threadIdx.x; j < k; j += blockDim.x) {
+            const int e = sidx[j];
+            int r = 0;
+            for (int i = 0; i < k; ++i) r += sidx[i] < e;
+            ws.perm[r] = j;
+            ws.pos[j] = r;
+            ws.act_e[r] = e;
+            ws.slot_info[r] = make_int4(e, r, 1, 0);   // one row: token 0
+        }
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+            int c = 0;
+            for (int i = 0; i < k; ++i) c += sidx[i] < e;
+            ws.offsets[e] = c;
+        }
+        if (threadIdx.x == 0) *ws.n_active = k;
+        for (int i = threadIdx.x; i < k * gwords; i += blockDim.x) ws.gmask[i] = 0;
+    } else {
+        permute_block_256(sidx, T, k, E, gwords, ws);
+    }
+}
+
 template <int EPL>
 __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restrict__ x, int xt,
                                                             const float* __restrict__ W, int T, int d, int E, int k,
@@ -757,7 +891,6 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
     float (*red)[4][kChunk] = reinterpret_cast<float (*)[4][kChunk]>(buf);
     float* slog = buf;
     __shared__ int s_last;
-    __shared__ int sidx[1024];
     // The router weights do not depend on the previous kernel: the first batch of rows is
     // loaded before waiting for it.
     float w0[kChainBatch][EPL];
@@ -867,108 +1000,268 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
         }
     }
     __syncthreads();
-    // Top-k: expert e's slot is the number of experts that beat it -- the order repeated
-    // selection would produce, computed for all (token, expert) at once.
-    __shared__ float stop[1024];
-    if (E <= kRankTopkMaxE) {
-        for (int it = threadIdx.x; it < T * E; it += blockDim.x) {
-            const int t = it / E, e = it % E;
-            const float v = slog[it];
-            const float4* row = reinterpret_cast<const float4*>(slog + t * E);
-            int rank = 0;
-            for (int q = 0; q < E / 4; ++q) {
-                const float4 o = row[q];
-                const int b = 4 * q;
-                rank += beats(o.x, b, v, e) + beats(o.y, b + 1, v, e) + beats(o.z, b + 2, v, e) + beats(o.w, b + 3, v, e);
-            }
-            if (rank < k) {
-                sidx[t * k + rank] = e;
-                stop[t * k + rank] = v;
-            }
-        }
-    } else {
-        // Many experts (then T <= 4096 / E is small): per token, an expert can be among the k
-        // best only if fewer than k experts of its own segment (E split into 8) beat it; the
-        // experts that beat a top-k member are top-k members themselves, so ranks counted
-        // among these candidates are exact for the k best.
-        // Each segment's candidates go to fixed slots seg * k + (rank in the segment), so
-        // no atomic counter is needed; empty slots hold -1.
-        __shared__ int cand_e[8 * kMaxK];
-        __shared__ float cand_v[8 * kMaxK];
-        const int seg = (E + 7) / 8;
-        const int ncs = 8 * k;
-        for (int t = 0; t < T; ++t) {
-            for (int i = threadIdx.x; i < ncs; i += blockDim.x) cand_e[i] = -1;
-            __syncthreads();
-            const float* row = slog + t * E;
-            for (int e = threadIdx.x; e < E; e += blockDim.x) {
-                const float v = row[e];
-                const int sg = e / seg, s0 = sg * seg, s1 = min(E, s0 + seg);
-                int rank = 0;
-#pragma unroll 4
-                for (int o = s0; o < s1; ++o) rank += beats(row[o], o, v, e);
-                if (rank < k) {
-                    cand_e[sg * k + rank] = e;
-                    cand_v[sg * k + rank] = v;
-                }
-            }
-            __syncthreads();
-            for (int i = threadIdx.x; i < ncs; i += blockDim.x) {
-                const int e = cand_e[i];
-                if (e < 0) continue;
-                const float v = cand_v[i];
-                int rank = 0;
-#pragma unroll 4
-                for (int j = 0; j < ncs; ++j) {
-                    const int o = cand_e[j];
-                    rank += (o >= 0) && beats(cand_v[j], o, v, e);
-                }
-                if (rank < k) {
-                    sidx[t * k + rank] = e;
-                    stop[t * k + rank] = v;
-                }
-            }
-            __syncthreads();
-        }
-    }
-    __syncthreads();
-    // softmax over the k selected logits, the maximum (slot 0) subtracted, sum in slot order
-    for (int p = threadIdx.x; p < T * k; p += blockDim.x) {
-        const int t = p / k;
-        const float m0 = stop[t * k];
-        float sum = 0.0f;
-        for (int j = 0; j < k; ++j) sum += expf(stop[t * k + j] - m0);
-        ws.idx[p] = sidx[p];
-        ws.w[p] = expf(stop[p] - m0) / sum;
-    }
-    __syncthreads();
-    if (T == 1) {
-        // One token, k distinct experts: pair j's sorted row (= its slot) is the number of
-        // selected experts with a lower index.
-        for (int j = threadIdx.x; j < k; j += blockDim.x) {
-            const int e = sidx[j];
-            int r = 0;
-            for (int i = 0; i < k; ++i) r += sidx[i] < e;
-            ws.perm[r] = j;
-            ws.pos[j] = r;
-            ws.act_e[r] = e;
-            ws.slot_info[r] = make_int4(e, r, 1, 0);   // one row: token 0
-        }
-        for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-            int c = 0;
-            for (int i = 0; i < k; ++i) c += sidx[i] < e;
-            ws.offsets[e] = c;
-        }
-        if (threadIdx.x == 0) *ws.n_active = k;
-        for (int i = threadIdx.x; i < k * gwords; i += blockDim.x) ws.gmask[i] = 0;
-    } else {
-        permute_block_256(sidx, T, k, E, gwords, ws);
-    }
+    route_select(slog, T, E, k, gwords, ws);
     if (threadIdx.x == 0) *ws.route_ctr = 0;
+}
+
+// The same computation for one to a few tokens as ONE thread-block cluster of E / EPC CTAs
+// (at most 16): CTA g owns experts [g * EPC, (g + 1) * EPC) and thread l the canonical
+// partial sum l (i = l, l + 256, ...).  The CTA's slice of the router weights does not
+// depend on the previous kernel, so it is copied into shared memory before waiting for it.
+// After the fixed halving tree (h = 128, 64, 32 through shared memory, 16 .. 1 by warp
+// shuffles) the CTA writes its logits straight into the shared memory of CTA 0 of the
+// cluster (distributed shared memory); one cluster barrier later CTA 0 has every logit and
+// selects, weights and permutes.  Compared with per-CTA partials in global memory and a
+// "last CTA" counter, this takes a global round trip, an atomic and a grid-wide fence off the
+// serial path of every decode step.
+constexpr int kClusterMaxAcc = 32;   // T * EPC accumulators per thread
+constexpr int kClusterMaxCtas = 16;
+constexpr size_t kClusterMaxDynSmem = 200 * 1024;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared-memory address of the same variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(r)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_st_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// 16-byte chunk q of weight row i sits at chunk q ^ wsw<EPC>(i): the rows that the 8 lanes
+// of one shared-memory wavefront read then fall on distinct banks.
+template <int EPC>
+__device__ __forceinline__ int wsw(int i) {
+    constexpr int cpr = EPC / 4;
+    return (i / (8 / cpr)) & (cpr - 1);
+}
+
+template <int EPC>
+__global__ void __launch_bounds__(256, 1) route_cluster_kernel(const void* __restrict__ x, int xt,
+                                                               const float* __restrict__ W, int T, int d, int E,
+                                                               int k, int gwords, Workspace ws) {
+    constexpr int TT = kClusterMaxAcc / EPC;   // tokens at most
+    constexpr int cpr = EPC / 4;                // 16-byte chunks per weight row
+    extern __shared__ __align__(16) float csm[];
+    float* wsl = csm;                                             // [d][EPC], chunk-swizzled
+    float* red = csm;                                             // after the products: tree
+    float* slog = csm + ((d * EPC > 192 * kClusterMaxAcc) ? d * EPC : 192 * kClusterMaxAcc);   // [T][E]
+    float* xs = slog + T * E;                                     // [T][d]
+    const uint32_t g = cluster_ctarank();
+    const int l = threadIdx.x;
+    cluster_arrive_relaxed();   // every CTA of the cluster has started before any remote store
+    {
+        const uint32_t wb = static_cast<uint32_t>(__cvta_generic_to_shared(wsl));
+        const float* src = W + static_cast<int64_t>(g) * EPC;
+        for (int c = l; c < d * cpr; c += 256) {
+            const int i = c / cpr, q = c % cpr;
+            rt_cp16(wb + static_cast<uint32_t>((i * cpr + (q ^ wsw<EPC>(i))) * 16), src + static_cast<int64_t>(i) * E + 4 * q);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    pdl_wait();
+    // x rows into shared memory as fp32: one round trip for all of them
+    if (xt == MOE_F32) {
+        const float4* src = static_cast<const float4*>(x);
+        for (int i = l; i < T * d / 4; i += 256) reinterpret_cast<float4*>(xs)[i] = __ldg(src + i);
+    } else {
+        const uint4* src = static_cast<const uint4*>(x);   // 8 bf16
+        for (int i = l; i < T * d / 8; i += 256) {
+            const uint4 v = __ldg(src + i);
+            float4* o = reinterpret_cast<float4*>(xs) + 2 * i;
+            o[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                               __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+            o[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
+                               __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+        }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const int nchain = d / kRouterPartials;
+    float acc[TT][EPC];
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) acc[t][e] = 0.0f;
+#pragma unroll 4
+    for (int m = 0; m < nchain; ++m) {
+        const int i = l + m * kRouterPartials;
+        const float4* row = reinterpret_cast<const float4*>(wsl) + i * cpr;
+        float wv[EPC];
+#pragma unroll
+        for (int q = 0; q < cpr; ++q) {
+            const float4 v = row[q ^ wsw<EPC>(i)];
+            wv[4 * q] = v.x, wv[4 * q + 1] = v.y, wv[4 * q + 2] = v.z, wv[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+            if (t < T) {
+                const float xv = xs[t * d + i];
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc[t][e] = fmaf(xv, wv[e], acc[t][e]);
+            }
+    }
+    // levels h = 128, 64, 32: s_l += s_{l+h} through shared memory (the weight slice is dead);
+    // red[j][0..h) for accumulator j, two regions so that one barrier separates the levels
+    __syncthreads();
+    {
+        float* r0 = red;                              // [32][128]
+        float* r1 = red + 128 * kClusterMaxAcc;       // [32][64]
+#pragma unroll
+        for (int lev = 0; lev < 3; ++lev) {
+            const int h = 128 >> lev;
+            float* rb = (lev == 1) ? r1 : r0;
+            if (l >= h && l < 2 * h) {
+#pragma unroll
+                for (int t = 0; t < TT; ++t)
+                    if (t < T)
+#pragma unroll
+                        for (int e = 0; e < EPC; ++e) rb[(t * EPC + e) * h + (l - h)] = acc[t][e];
+            }
+            __syncthreads();
+            if (l < h) {
+#pragma unroll
+                for (int t = 0; t < TT; ++t)
+                    if (t < T)
+#pragma unroll
+                        for (int e = 0; e < EPC; ++e) acc[t][e] = acc[t][e] + rb[(t * EPC + e) * h + l];
+            }
+        }
+    }
+    cluster_wait_acquire();   // (the barrier armed at entry): CTA 0's shared memory is live
+    if (l < 32) {
+        // levels h = 16 .. 1 across the lanes; lane 0 ends with s_0 of every accumulator
+#pragma unroll
+        for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+                if (t < T)
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e)
+                        acc[t][e] = acc[t][e] + __shfl_down_sync(0xffffffffu, acc[t][e], h);
+        if (l == 0) {
+            const uint32_t dst = cluster_map(slog, 0);
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+                if (t < T)
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e)
+                        cluster_st_f32(dst + static_cast<uint32_t>((t * E + static_cast<int>(g) * EPC + e) * 4), acc[t][e]);
+        }
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (g != 0) return;
+    pdl_trigger();   // the expert kernel's launch overlaps the selection and permutation
+    for (int it = l; it < T * E; it += blockDim.x) ws.logits[it] = slog[it];
+    route_select(slog, T, E, k, gwords, ws);
+}
+
+// Experts per CTA of the cluster kernel for E experts (0: not eligible).
+int route_cluster_epc(int64_t E) {
+    for (int epc : {4, 8, 16, 32})
+        if (E % epc == 0 && E / epc <= kClusterMaxCtas) return epc;
+    return 0;
+}
+
+size_t route_cluster_smem(int64_t T, int64_t d, int64_t E, int epc) {
+    const int64_t tree = 192 * kClusterMaxAcc;
+    return static_cast<size_t>(std::max<int64_t>(d * epc, tree) + T * E + T * d) * sizeof(float);
+}
+
+bool g_route_cluster_ok = false;
+
+template <int EPC>
+cudaError_t configure_route_cluster() {
+    cudaError_t e = cudaFuncSetAttribute(route_cluster_kernel<EPC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(route_cluster_kernel<EPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kClusterMaxDynSmem));
+    return e;
+}
+
+// Enables the cluster router when a 16-CTA cluster with the largest shared-memory request
+// can be resident; otherwise every shape keeps the partial-sum router.
+cudaError_t configure_route_kernels() {
+    cudaError_t e = configure_route_cluster<4>();
+    if (e == cudaSuccess) e = configure_route_cluster<8>();
+    if (e == cudaSuccess) e = configure_route_cluster<16>();
+    if (e == cudaSuccess) e = configure_route_cluster<32>();
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        g_route_cluster_ok = false;
+        return cudaSuccess;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterMaxCtas);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = kClusterMaxDynSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterMaxCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<8>, &cfg);
+    g_route_cluster_ok = (e == cudaSuccess && n >= 1);
+    (void)cudaGetLastError();
+    return cudaSuccess;
+}
+
+template <int EPC>
+cudaError_t launch_route_cluster(const void* x, int xt, const float* W, int T, int d, int E, int k, int gwords,
+                                 const Workspace& ws, size_t smem, cudaStream_t s) {
+    const unsigned ctas = static_cast<unsigned>(E / EPC);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, route_cluster_kernel<EPC>, x, xt, W, T, d, E, k, gwords, ws);
 }
 
 cudaError_t launch_route_decode(const void* x, int xt, const float* W, int64_t T, int64_t d, int64_t E, int k,
                                 int gwords, const Workspace& ws, cudaStream_t s) {
+    const int epc = route_cluster_epc(E);
+    if (g_route_cluster_ok && epc > 0 && T * epc <= kClusterMaxAcc) {
+        const size_t smem = route_cluster_smem(T, d, E, epc);
+        if (smem <= kClusterMaxDynSmem) {
+            const int Tc = static_cast<int>(T), dc = static_cast<int>(d), Ec = static_cast<int>(E);
+            switch (epc) {
+                case 4: return launch_route_cluster<4>(x, xt, W, Tc, dc, Ec, k, gwords, ws, smem, s);
+                case 8: return launch_route_cluster<8>(x, xt, W, Tc, dc, Ec, k, gwords, ws, smem, s);
+                case 16: return launch_route_cluster<16>(x, xt, W, Tc, dc, Ec, k, gwords, ws, smem, s);
+                default: return launch_route_cluster<32>(x, xt, W, Tc, dc, Ec, k, gwords, ws, smem, s);
+            }
+        }
+    }
     // experts per lane: chunks narrow enough that the router weights spread over >= 128 CTAs
     const int epl = (E <= 128) ? 1 : (E <= 512 ? 2 : 4);
     const dim3 grid(kResidues, static_cast<unsigned>((E + 32 * epl - 1) / (32 * epl)));
