@@ -87,7 +87,11 @@ typedef enum { MOE_LAYOUT_CANONICAL = 0, MOE_LAYOUT_DEVICE = 1, MOE_LAYOUT_NEURO
 /* Which expert kernels moe_layer_forward uses.  GEMV: weight-streaming matrix-vector
  * kernels (a few tokens per expert).  GEMM: grouped GEMMs on the tensor cores (tcgen05),
  * which need f a multiple of 64 (128 for ReLU^2); forcing GEMM on another shape returns
- * MOE_ERR_UNSUPPORTED.  AUTO takes GEMM when T*k >= 8*E and the shape allows it. */
+ * MOE_ERR_UNSUPPORTED.  AUTO takes GEMM when T*k >= 8*E and the shape allows it; for ONE
+ * token with Q8_0 SwiGLU experts and routing computed by the call (d <= 8192, k*f <= 16384)
+ * it runs the whole layer as a single cooperative kernel, one CTA per SM, when the device
+ * supports cooperative launches (the same results within the output tolerance; routing,
+ * weights and the permutation bit-identical).  GEMV keeps the separate kernels. */
 typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GEMM = 2 } moe_path;
 
 /* Bytes of one quantised matrix: rows*cols/32*34 (Q8_0), rows*cols/2 + rows*cols/16
@@ -215,7 +219,8 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
                              size_t ws_bytes, const moe_trace* trace, moe_stream_t stream);
 
 /* Number of kernels one moe_layer_forward call launches for this desc, T and routing
- * (routing_supplied != 0 when idx_in/w_in are given); -1 on a bad desc or T. */
+ * (routing_supplied != 0 when idx_in/w_in are given), for bf16 inputs on the current
+ * device (1 when the one-kernel decode layer applies); -1 on a bad desc or T. */
 int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_t routing_supplied);
 
 /*

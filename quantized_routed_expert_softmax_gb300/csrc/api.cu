@@ -28,6 +28,11 @@ cudaError_t configure_gemm_kernels();
 cudaError_t configure_route_kernels();
 cudaError_t launch_expert_gemm(const ExpertArgs&, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_gather_x_f16(const ExpertArgs&, int, cudaStream_t);
+cudaError_t configure_decode_kernel(int, int);
+int decode_ctas(int);
+size_t decode_smem_bytes(int, int, int, int, int);
+size_t decode_max_smem();
+cudaError_t launch_decode_layer(const DecodeArgs&, int, cudaStream_t);
 
 
 namespace {
@@ -62,6 +67,7 @@ cudaError_t ensure_configured(int* num_sms) {
         if (e == cudaSuccess) e = configure_gemm_kernels();
         if (e == cudaSuccess) e = configure_route_kernels();
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = configure_decode_kernel(dev, g_num_sms[dev]);
         if (e != cudaSuccess) return e;
         done[dev] = true;
     }
@@ -83,7 +89,66 @@ struct Plan {
     bool gemm;          // expert GEMMs on the tensor cores instead of the GEMVs
     bool down_t1;       // one token, Q8_0 SwiGLU, k in {1,2,4,8}: the row-tile down kernel combines
     int nv_split;       // NVFP4 down with fused combine: group splits per (row tile, slot)
+    bool decode1;       // one token, Q8_0 SwiGLU: the shape fits the one-kernel decode layer
 };
+
+// Router experts per routing CTA of the one-kernel decode layer (0: E too large for `ctas`).
+int decode_epc(int64_t E, int ctas) {
+    for (int epc : {1, 2, 4, 8})
+        if (E % epc == 0 && E / epc <= ctas) return epc;
+    return 0;
+}
+
+// The one-kernel decode layer splits U_g = k * f/16 * d/32 gate.up panel units and
+// U_d = d/32 * k * f/32 down units evenly over the warps of `ctas` CTAs (16 each).
+struct DecodeSplit {
+    int64_t U_g, U_d, warps_g, warps_d;
+    int64_t cov_g;       // CTAs whose ranges can touch one gate.up item (records per item)
+    int64_t cov_d;       // warps whose ranges can touch one down item
+    int64_t cta_items;   // gate.up items one CTA's range can touch
+};
+
+DecodeSplit decode_split(const moe_layer_desc* d, int64_t ctas) {
+    DecodeSplit sp{};
+    const int64_t npan_g = d->d / 32, npan_d = d->f / 32;
+    sp.U_g = static_cast<int64_t>(d->k) * (d->f / 16) * npan_g;
+    sp.U_d = (d->d / 32) * d->k * npan_d;
+    sp.warps_g = std::min<int64_t>(16 * ctas, sp.U_g);
+    sp.warps_d = std::min<int64_t>(16 * ctas, sp.U_d);
+    // a range of at least Lmin units meets at most ceil((npan - 2) / Lmin) + 2 of them
+    const int64_t lcta = std::max<int64_t>(1, sp.U_g / ((sp.warps_g + 15) / 16));   // units per CTA, at least
+    sp.cov_g = (npan_g + lcta - 1) / lcta + 2;
+    const int64_t lwd = std::max<int64_t>(1, sp.U_d / sp.warps_d);
+    sp.cov_d = (npan_d + lwd - 1) / lwd + 2;
+    // the most gate.up items one CTA's range touches (exact, from the same split)
+    sp.cta_items = 0;
+    for (int64_t c = 0; 16 * c < sp.warps_g; ++c) {
+        const int64_t w0 = 16 * c, w1 = std::min(16 * c + 16, sp.warps_g);
+        const int64_t u0 = w0 * sp.U_g / sp.warps_g, u1 = w1 * sp.U_g / sp.warps_g;
+        if (u1 > u0) sp.cta_items = std::max(sp.cta_items, (u1 - 1) / npan_g - u0 / npan_g + 1);
+    }
+    return sp;
+}
+
+// The one-kernel decode layer's shape limits (any device): one token, Q8_0 SwiGLU, the
+// router-weight slice of a routing CTA, the staged rows and the CTA's gate.up partials within
+// its shared memory, and 32-bit unit arithmetic.
+bool decode_shape_ok(const moe_layer_desc* d, int64_t T, int xt) {
+    if (T != 1 || d->wfmt != MOE_W_Q8_0 || d->act != MOE_ACT_SWIGLU || d->path != MOE_PATH_AUTO) return false;
+    if (d->d > 8192 || d->k * d->f > 16384 || d->f % 16 != 0) return false;
+    if (decode_smem_bytes(static_cast<int>(d->d), static_cast<int>(d->f), d->k, xt, 1) > decode_max_smem()) return false;
+    const int epc = decode_epc(d->E, kMaxDecodeCtas);
+    if (epc == 0 || d->d * epc * 4 + epc * 1024 > 16 * 6 * 1152) return false;
+    const DecodeSplit sp = decode_split(d, kMaxDecodeCtas);   // the most warps: the largest products
+    return (sp.U_g + 1) * sp.warps_g < (int64_t(1) << 32) && (sp.U_d + 1) * sp.warps_d < (int64_t(1) << 32);
+}
+
+// With `ctas` CTAs on this device: the kernel's shared memory, including the per-warp
+// gate.up partials of one CTA's items, within what the kernel is configured for.
+bool decode_split_fits(const moe_layer_desc* d, const DecodeSplit& sp, int xt) {
+    return decode_smem_bytes(static_cast<int>(d->d), static_cast<int>(d->f), d->k, xt,
+                             static_cast<int>(sp.cta_items)) <= decode_max_smem();
+}
 
 // The GEMM path tiles rows by 128 (SwiGLU gate.up: 64 neurons' gate and up rows) and K by 64.
 bool gemm_shape_ok(const moe_layer_desc* d) {
@@ -122,12 +187,13 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
                 (d->k == 1 || d->k == 2 || d->k == 4 || d->k == 8) && d->f / 32 >= 8 / d->k && d->d % 16 == 0;
     if (p.down_t1) p.fuse_combine = true;   // the down kernel writes the output rows
     p.nv_split = (!p.gemm && d->wfmt == MOE_W_NVFP4 && p.fuse_combine && T == 1 && (d->f / 16) >= 4 * 8) ? 4 : 1;
+    p.decode1 = !p.gemm && decode_shape_ok(d, T, xt);
     return p;
 }
 
 struct Layout {
     size_t err, route_ctr, n_active, row_ctr, logits, rpart, idx, w, offsets, perm, pos, act_e, slot_info, chunk_cnt,
-        local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, total;
+        local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, dec_bar, dec_grec, dec_drec, total;
 };
 
 // Workspace regions for T tokens (each 256-byte aligned).  The control words (err,
@@ -167,6 +233,13 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     L.xs_lo = take(xs);
     L.h_hi = take(hs);
     L.h_lo = take(hs);
+    // the one-kernel decode layer's counters (zero between calls) and partial sums
+    const bool dec = p.decode1;
+    // (sized for the most CTAs any device can give the kernel: more CTAs, more records per item)
+    const DecodeSplit sp = decode_split(d, kMaxDecodeCtas);
+    L.dec_bar = take(dec ? sizeof(int32_t) * 2 : 0);
+    L.dec_grec = take(dec ? sizeof(float) * 32 * d->k * (d->f / 16) * sp.cov_g : 0);
+    L.dec_drec = take(dec ? sizeof(float) * 32 * (d->d / 32) * d->k * sp.cov_d : 0);
     L.total = off;
     return L;
 }
@@ -312,6 +385,7 @@ size_t moe_layer_workspace_bytes(const moe_layer_desc* desc, int64_t T_max) {
     t_small = std::min<int64_t>(t_small, kFusedRouteLogits / desc->E);
     size_t n = layout_for(desc, T_max).total;
     if (t_small >= 1) n = std::max(n, layout_for(desc, t_small).total);
+    n = std::max(n, layout_for(desc, 1).total);   // one token may take the one-kernel decode layer
     return n;
 }
 
@@ -346,8 +420,68 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
             e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(trace->stage_events[i]), s,
                                          cudaEventRecordExternal);   // a real record node under capture
     };
+    // optional copies of the intermediates (device to device, on the stream)
+    auto copy_trace = [&]() -> moe_status {
+        if (!trace) return MOE_OK;
+        auto cp = [&](void* dst, const void* src, size_t bytes) {
+            if (dst && e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+        };
+        if (!idx_in) cp(trace->logits, ws.logits, sizeof(float) * T * desc->E);
+        cp(trace->idx, ws.idx, sizeof(int32_t) * p.P);
+        cp(trace->w, ws.w, sizeof(float) * p.P);
+        cp(trace->offsets, ws.offsets, sizeof(int32_t) * (desc->E + 1));
+        cp(trace->perm, ws.perm, sizeof(int32_t) * p.P);
+        cp(trace->pos, ws.pos, sizeof(int32_t) * p.P);
+        cp(trace->h, ws.h, sizeof(float) * p.P * desc->f);
+        return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    };
+
     mark(0);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    // One token, routing computed here: the whole layer as one cooperative kernel when the
+    // device and the shape allow it.
+    if (p.decode1 && !idx_in) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+        const int ctas = decode_ctas(dev);
+        const int epc = decode_epc(desc->E, ctas);
+        const DecodeSplit sp = decode_split(desc, std::max(1, ctas));
+        if (ctas > 0 && epc > 0 && decode_split_fits(desc, sp, xt)) {
+            char* base = static_cast<char*>(workspace);
+            DecodeArgs a{};
+            a.x = x;
+            a.xt = xt;
+            a.W = desc->router_w;
+            a.d = static_cast<int>(desc->d);
+            a.f = static_cast<int>(desc->f);
+            a.E = static_cast<int>(desc->E);
+            a.k = k;
+            a.epc = epc;
+            a.prefetch_down = p.prefetch_down ? 1 : 0;
+            // warps that share each phase's panel range: all of them, or one per unit
+            a.warps_g = static_cast<int>(sp.warps_g);
+            a.warps_d = static_cast<int>(sp.warps_d);
+            a.cov_g = static_cast<int>(sp.cov_g);
+            a.cov_d = static_cast<int>(sp.cov_d);
+            a.cta_items = static_cast<int>(sp.cta_items);
+            a.w_gu = static_cast<const uint8_t*>(desc->w_gate_up);
+            a.gu_bytes = static_cast<int64_t>(moe_q8_0_bytes(2 * desc->f, desc->d));
+            a.w_dn = static_cast<const uint8_t*>(desc->w_down);
+            a.dn_bytes = static_cast<int64_t>(moe_q8_0_bytes(desc->d, desc->f));
+            a.pf = static_cast<const uint8_t*>(desc->l2_prefetch);
+            a.pf_bytes = desc->l2_prefetch ? (desc->l2_prefetch_bytes & ~static_cast<int64_t>(15)) : 0;
+            a.out = out;
+            a.ws = ws;
+            a.bar = reinterpret_cast<int32_t*>(base + L.dec_bar);
+            a.grec = reinterpret_cast<float*>(base + L.dec_grec);
+            a.drec = reinterpret_cast<float*>(base + L.dec_drec);
+            e = launch_decode_layer(a, ctas, s);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            for (int i = 1; i <= 4; ++i) mark(i);   // one kernel: the inner boundaries coincide
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            return copy_trace();
+        }
+    }
     // 1. router + top-k + softmax, 2. permutation by expert
     if (p.small_route && !idx_in) {
         e = launch_route_decode(x, xt, desc->router_w, T, desc->d, desc->E, k, p.gwords, ws, s);
@@ -416,19 +550,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     mark(4);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    if (trace) {
-        auto cp = [&](void* dst, const void* src, size_t bytes) {
-            if (dst && e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
-        };
-        if (!idx_in) cp(trace->logits, ws.logits, sizeof(float) * T * desc->E);
-        cp(trace->idx, ws.idx, sizeof(int32_t) * p.P);
-        cp(trace->w, ws.w, sizeof(float) * p.P);
-        cp(trace->offsets, ws.offsets, sizeof(int32_t) * (desc->E + 1));
-        cp(trace->perm, ws.perm, sizeof(int32_t) * p.P);
-        cp(trace->pos, ws.pos, sizeof(int32_t) * p.P);
-        cp(trace->h, ws.h, sizeof(float) * p.P * desc->f);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-    }
+    return copy_trace();
     return MOE_OK;
 }
 
@@ -436,6 +558,13 @@ int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_
     if (validate_desc(desc) != MOE_OK || T < 0 || T > kMaxTokens) return -1;
     if (T == 0) return 0;
     const Plan p = make_plan(desc, T);
+    if (p.decode1 && !routing_supplied) {   // the one-kernel decode layer, when this device runs it
+        int num_sms = 0, dev = 0;
+        if (ensure_configured(&num_sms) == cudaSuccess && cudaGetDevice(&dev) == cudaSuccess &&
+            decode_epc(desc->E, decode_ctas(dev)) > 0 &&
+            decode_split_fits(desc, decode_split(desc, std::max(1, decode_ctas(dev))), MOE_BF16))
+            return 1;
+    }
     int n = 0;
     if (p.small_route) n += 1;                              // routing + permutation in one launch
     else n += (routing_supplied ? 0 : 2) + 3;               // router, top-k; rank, scan, scatter

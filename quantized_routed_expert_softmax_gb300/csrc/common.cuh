@@ -18,6 +18,7 @@ constexpr int kDevErrBadExpert = 1;
 constexpr int kRouterPartials = 256;   // partial sums of the router's canonical order
 constexpr int kMaxK = 32;              // top-k fits one warp
 constexpr int kMaxE = 1024;
+constexpr int kMaxDecodeCtas = 256;   // CTAs of the one-kernel decode layer at most (one per SM)
 
 // Pointers into one layer workspace (see layout_for in api.cu).  The control words
 // (err, route_ctr, row_ctr) must be zero before a call; the kernels leave the counters
@@ -70,6 +71,31 @@ struct ExpertArgs {
     const float* gu_ts;          // NVFP4 tensor scales [E] (or null)
     const float* dn_ts;
     Workspace ws;
+};
+
+// Arguments of the one-kernel decode layer (decode.cu): one token, Q8_0 SwiGLU experts.
+// The kernel's own control words and partial sums sit in the layer workspace too.
+struct DecodeArgs {
+    const void* x;
+    int xt;
+    const float* W;              // router [d][E]
+    int d, f, E, k;
+    int epc;                     // router experts per routing CTA (E / epc CTAs compute logits)
+    int prefetch_down;           // the routed experts' down matrices are pulled into L2 during gate.up
+    int warps_g, warps_d;        // warps that share the gate.up / down panel ranges
+    int cov_g, cov_d;            // partial records per item at most (CTAs / warps that can share one item)
+    int cta_items;               // gate.up items one CTA's range touches at most
+    const uint8_t* w_gu;
+    int64_t gu_bytes;
+    const uint8_t* w_dn;
+    int64_t dn_bytes;
+    const uint8_t* pf;           // L2 hint (the next layer's router weights), or null
+    int64_t pf_bytes;
+    float* out;                  // [d]
+    Workspace ws;
+    int32_t* bar;                // [2] grid-barrier arrivals, CTAs finished (zero between calls)
+    float* grec;                 // [k * f/16][cov_g][32] gate.up partial sums per item and contributor
+    float* drec;                 // [k * d/32][cov_d][32] down partial sums per item and contributor
 };
 
 // Programmatic dependent launch: wait for the preceding kernel's memory, and allow the

@@ -1,0 +1,621 @@
+// decode.cu -- one routed MoE layer for ONE token as a single persistent kernel.
+//
+// The same layer as route.cu + gemv.cu (router, top-k, softmax over the selected logits,
+// gate.up with SiLU(gate)*up, down projection, fixed-order combine), for the case that
+// decides decode speed: one token, where the layer moves only the routed experts' weights
+// (a few tens of MB) and the separate launches' start-up, ramp and tail cost more than the
+// bytes.  Sources of the computation:
+//   router / top-k / softmax: "Squeezing a 26B MoE onto the cheapest Inferentia instance"
+//     (128 experts, top-8 per token), with the canonical fp32 summation order of the oracle;
+//   gate.up + SwiGLU: "Running Gemma 4 26B at 5 tokens/s on a 13-year-old Xeon", sections
+//     "A three-step fix" / "Runtime graph fallback" (fused [n_embd, 2*n_ff, n_experts]
+//     tensor, gate rows first, then SiLU(gate)*up);
+//   combine: "Running NVIDIA's new 120B Nemotron-3.5-Super on an 8GB GPU", section "How we
+//     check correctness" (per-(token, expert) results summed in a fixed order, no atomics
+//     on the values).
+//
+// One CTA per SM (a cooperative launch: every CTA is resident, so the grid barriers below
+// cannot wait on a CTA that never runs), 16 warps each.  Three grid barriers:
+//   R  CTA c < E/epc computes the logits of experts [c*epc, (c+1)*epc) in the canonical
+//      order (256 fma chains i = l (mod 256), then the halving tree); its slice of the
+//      router weights is copied into shared memory before the kernel waits for the
+//      previous one.  Barrier 1.  Every CTA then ranks all E logits itself (top-k with the
+//      lower index on ties), so no CTA waits for a selection made elsewhere.
+//   G  gate.up: the panel products of all k experts (k * f/16 items of 16 gate + 16 up
+//      rows, d/32 panels each) are one flattened range split evenly over the warps of the
+//      grid, so every warp streams the same number of panels (within one) whatever the
+//      shapes.  A CTA's warps cover a contiguous stretch of items: their partials meet in
+//      shared memory and the CTA writes one record per item it touched.  Each CTA also
+//      asks L2 for its share of the routed experts' down matrices.  Barrier 2.
+//   H  every CTA sums each item's records (in CTA order) and applies SwiGLU into its own
+//      f16 copy of h.
+//   D  down: (slot, row tile of 32, panel) units flattened the same way (the first ring
+//      stages are requested before H); each warp writes one record per item it touched.
+//      Barrier 3.
+//   C  row tile rt is combined by CTA rt mod G: y per slot (records in warp order), then the
+//      pairs in order j: out[r] = sum_j w_j * y_{slot(j)}[r].
+// Every per-warp quantity that depends only on the shapes is worked out before the kernel
+// waits for the previous one.  All waits are bounded (about one second, then device error 2
+// and the kernel goes on), so a barrier can never hang the GPU.  Results are bitwise
+// reproducible run to run: every sum has a fixed order.
+#include "gemv_core.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kDecWarps = 16;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kDevErrTimeout = 2;
+constexpr long long kWaitLimitNs = 1000000000ll;   // bounded waits: one second
+constexpr size_t kRingBytes = static_cast<size_t>(kDecWarps) * kStages * kSlotBytes;
+
+__device__ __forceinline__ long long globaltimer() {
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier over a monotonically growing counter (target = n * gridDim.x for the
+// n-th barrier of a call).  Bounded: after ~1 s it records device error 2 and returns.
+__device__ __forceinline__ void grid_barrier(int32_t* ctr, int target, int32_t* err) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // release: the CTA's writes (ordered before this by the barrier above) are visible to
+        // every CTA that acquires the counter at or past the target
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
+        if (ld_acquire(ctr) < target) {
+            const long long t0 = globaltimer();
+            while (ld_acquire(ctr) < target) {
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    set_error(err, kDevErrTimeout);
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+
+// An even split of U units over W warps: warp w owns [begin(w), begin(w+1)).  The host
+// admits only shapes with (U + 1) * W < 2^32, so the arithmetic stays 32-bit.
+__device__ __forceinline__ uint32_t split_begin(uint32_t U, uint32_t W, uint32_t w) { return w * U / W; }
+// The warp that owns unit u: the largest w with begin(w) <= u.
+__device__ __forceinline__ uint32_t split_owner(uint32_t U, uint32_t W, uint32_t u) { return ((u + 1) * W + U - 1) / U - 1; }
+// Warps that own units of item i (units [i * npan, (i + 1) * npan)).
+__device__ __forceinline__ int item_contributors(uint32_t U, uint32_t W, uint32_t npan, uint32_t i) {
+    return static_cast<int>(split_owner(U, W, (i + 1) * npan - 1) - split_owner(U, W, i * npan)) + 1;
+}
+
+__device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) { return va > vb || (va == vb && ea < eb); }
+
+// A warp's share of one phase: units [u0, u0 + n) starting at panel b0 of item item0, whose
+// first record goes to contributor slot c0 of that item (later items: slot 0).
+struct WarpRange {
+    int n, item0, b0, c0;
+};
+
+__device__ __forceinline__ WarpRange warp_range(uint32_t U, uint32_t W, uint32_t npan, uint32_t gw) {
+    WarpRange r{0, 0, 0, 0};
+    if (gw >= W) return r;
+    const uint32_t u0 = split_begin(U, W, gw), u1 = split_begin(U, W, gw + 1);
+    r.n = static_cast<int>(u1 - u0);
+    r.item0 = static_cast<int>(u0 / npan);
+    r.b0 = static_cast<int>(u0 % npan);
+    r.c0 = static_cast<int>(gw - split_owner(U, W, static_cast<uint32_t>(r.item0) * npan));
+    return r;
+}
+
+}  // namespace
+
+// Shared-memory plan (dynamic): [ring | B | C | P]
+//   ring : per-warp rings of panel blocks (16 x 6 x 1152 B), gate.up then down; during
+//          routing, the CTA's router-weight slice [d][epc] and the tree buffer [epc][256]
+//   B    : x as fp32 [d] (routing), then h of the k slots as f16 hi [k][f] + lo [k][f] (down)
+//   C    : x as f16 hi [d] (+ lo [d] for fp32 inputs) (gate.up)
+//   P    : the per-warp gate.up partials of the CTA's items [cta_items][16 warps][32]
+__host__ __device__ size_t decode_region_b(int d, int f, int k) {
+    const size_t xb = static_cast<size_t>(d) * 4, hb = static_cast<size_t>(k) * f * 4;
+    return xb > hb ? xb : hb;
+}
+
+__host__ __device__ size_t decode_region_c(int d, int xt) { return static_cast<size_t>(d) * 2 * (xt == MOE_F32 ? 2 : 1); }
+
+size_t decode_smem_bytes(int d, int f, int k, int xt, int cta_items) {
+    return kRingBytes + decode_region_b(d, f, k) + decode_region_c(d, xt) +
+           static_cast<size_t>(cta_items) * kDecWarps * 32 * sizeof(float);
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs a) {
+    extern __shared__ __align__(16) unsigned char dsm[];
+    __shared__ __align__(16) float slog[kMaxE];   // logits; later the contributor counts of the gate.up items
+    __shared__ int s_sel[kMaxK];     // expert of selection slot j (larger logit first)
+    __shared__ float s_val[kMaxK];   // its logit
+    __shared__ int s_e[kMaxK];       // expert of sorted slot s (increasing expert index)
+    __shared__ int s_pos[kMaxK];     // sorted slot of pair j
+    __shared__ float s_w[kMaxK];     // combine weight of pair j
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int d = a.d, f = a.f, E = a.E, k = a.k;
+    const uint32_t gw = static_cast<uint32_t>(c * kDecWarps + warp);   // warp index in the grid
+    unsigned char* ring = dsm;
+    float* xf = reinterpret_cast<float*>(dsm + kRingBytes);
+    __half* xh = reinterpret_cast<__half*>(dsm + kRingBytes + decode_region_b(d, f, k));
+    const bool split = a.xt == MOE_F32;
+    // the two streaming phases: items, panels per item, units
+    const int nt_g = f / 16, npan_g = d / 32, npan_d = f / 32;
+    const int nrt = d / 32;   // 32-row tiles of the down projection
+    const uint32_t items_g = static_cast<uint32_t>(k * nt_g), items_d = static_cast<uint32_t>(nrt * k);
+    const uint32_t U_g = items_g * npan_g, U_d = items_d * npan_d;
+    // shape-only bookkeeping, done before waiting for the previous kernel
+    const WarpRange rg = warp_range(U_g, a.warps_g, npan_g, gw);
+    const WarpRange rd = warp_range(U_d, a.warps_d, npan_d, gw);
+
+    // ---------------------------------------------------------------- R: router logits
+    const int epc = a.epc;
+    const bool router = c < E / epc;
+    float* wsl = reinterpret_cast<float*>(ring);   // [d][epc]
+    float* red = wsl + d * epc;                     // [epc][256]
+    if (router) {   // the weights do not depend on the previous kernel: copied before waiting
+        const float* src = a.W + c * epc;
+        const uint32_t wb = smem_addr(wsl);
+        for (int it = tid; it < d * epc; it += kDecThreads) {
+            const int i = it / epc, e = it % epc;
+            cp_async4(wb + static_cast<uint32_t>(it) * 4, src + static_cast<int64_t>(i) * E + e);
+        }
+        cp_async_commit();
+    }
+    pdl_wait();
+    for (int i = tid; i < d / 4; i += kDecThreads) {
+        float4 v;
+        if (split) {
+            v = __ldcg(reinterpret_cast<const float4*>(a.x) + i);
+        } else {
+            const uint2 b = __ldcg(reinterpret_cast<const uint2*>(a.x) + i);
+            v = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xffff0000u), __uint_as_float(b.y << 16),
+                            __uint_as_float(b.y & 0xffff0000u));
+        }
+        reinterpret_cast<float4*>(xf)[i] = v;
+        __half2 h01, h23, l01, l23;
+        split_f16(v.x, v.y, h01, l01);
+        split_f16(v.z, v.w, h23, l23);
+        reinterpret_cast<__half2*>(xh)[2 * i] = h01;
+        reinterpret_cast<__half2*>(xh)[2 * i + 1] = h23;
+        if (split) {
+            reinterpret_cast<__half2*>(xh + d)[2 * i] = l01;
+            reinterpret_cast<__half2*>(xh + d)[2 * i + 1] = l23;
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    if (router) {
+        if (tid < kRouterPartials) {   // chain l: fmaf over i = l, l + 256, ... in increasing i
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+            const int nchain = d / kRouterPartials;
+            for (int m = 0; m < nchain; ++m) {
+                const int i = tid + m * kRouterPartials;
+                const float xv = xf[i];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (e < epc) acc[e] = fmaf(xv, wsl[i * epc + e], acc[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (e < epc) red[e * kRouterPartials + tid] = acc[e];
+        }
+        __syncthreads();
+        for (int h = kRouterPartials / 2; h >= 32; h >>= 1) {   // s_l += s_{l+h}, h = 128, 64, 32
+            for (int it = tid; it < epc * h; it += kDecThreads) {
+                const int e = it / h, l = it % h;
+                red[e * kRouterPartials + l] = red[e * kRouterPartials + l] + red[e * kRouterPartials + l + h];
+            }
+            __syncthreads();
+        }
+        if (warp < epc) {   // h = 16 .. 1 across the lanes; lane 0 ends with s_0
+            float v = red[warp * kRouterPartials + lane];
+#pragma unroll
+            for (int h = 16; h >= 1; h >>= 1) v = v + __shfl_down_sync(0xffffffffu, v, h);
+            if (lane == 0) a.ws.logits[c * epc + warp] = v;
+        }
+    }
+    grid_barrier(a.bar, G, a.ws.err);
+    pdl_trigger();   // every CTA is resident: the next kernel may be scheduled
+
+    // ---------------------------------------------------------------- R: top-k, weights, slots
+    for (int e = tid; e < E; e += kDecThreads) slog[e] = __ldcg(a.ws.logits + e);
+    // gate.up items this CTA's warps touch, and their per-warp partials [items][16 warps][32]
+    const uint32_t wc0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_g));
+    const uint32_t wc1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_g));
+    const uint32_t cu0 = split_begin(U_g, a.warps_g, wc0), cu1 = split_begin(U_g, a.warps_g, wc1);
+    const int cta_item0 = static_cast<int>(cu0 / npan_g);
+    const int cta_items = cu1 > cu0 ? static_cast<int>((cu1 - 1) / npan_g) - cta_item0 + 1 : 0;
+    float* cred = reinterpret_cast<float*>(dsm + kRingBytes + decode_region_b(d, f, k) + decode_region_c(d, a.xt));
+    for (int i = tid; i < cta_items * kDecWarps * 32; i += kDecThreads) cred[i] = 0.0f;
+    if (tid < kMaxK) {   // every slot holds a valid expert even if the logits were not finite
+        s_sel[tid] = 0;
+        s_val[tid] = 0.0f;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kDecThreads) {   // slot = number of experts that beat e
+        const float v = slog[e];
+        const float4* row = reinterpret_cast<const float4*>(slog);
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        for (int q = 0; q < E / 4; ++q) {
+            const float4 o = row[q];
+            r0 += beats(o.x, 4 * q, v, e);
+            r1 += beats(o.y, 4 * q + 1, v, e);
+            r2 += beats(o.z, 4 * q + 2, v, e);
+            r3 += beats(o.w, 4 * q + 3, v, e);
+        }
+        const int r = r0 + r1 + r2 + r3;
+        if (r < k) {
+            s_sel[r] = e;
+            s_val[r] = v;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {   // softmax over the k selected logits (slot 0's subtracted, sum in slot order)
+        const int j = lane;
+        const bool live = j < k;
+        const int ej = live ? s_sel[j] : 0;
+        float wj = 0.0f;
+        if (live) {
+            const float m0 = s_val[0];
+            float sum = 0.0f;
+            for (int i = 0; i < k; ++i) sum += expf(s_val[i] - m0);
+            wj = expf(s_val[j] - m0) / sum;
+        }
+        int r = 0;   // sorted slot: selected experts with a lower index
+        for (int i = 0; i < k; ++i) r += s_sel[i] < ej;
+        if (live) {
+            s_e[r] = ej;
+            s_pos[j] = r;
+            s_w[j] = wj;
+            if (c == 0) {
+                a.ws.idx[j] = ej;
+                a.ws.w[j] = wj;
+                a.ws.perm[r] = j;
+                a.ws.pos[j] = r;
+                a.ws.act_e[r] = ej;
+                a.ws.slot_info[r] = make_int4(ej, r, 1, 0);
+            }
+        }
+    }
+    if (c == 0) {
+        for (int e = tid; e <= E; e += kDecThreads) {
+            int n = 0;
+            for (int i = 0; i < k; ++i) n += s_sel[i] < e;
+            a.ws.offsets[e] = n;
+        }
+        if (tid == 0) *a.ws.n_active = k;
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- G: gate.up partial sums
+    const uint64_t pol = l2_evict_first_policy();
+    if (tid == 0 && a.pf_bytes > 0) {   // this CTA's share of the caller's L2 hint
+        const int64_t share = ((a.pf_bytes + G - 1) / G + 127) / 128 * 128;
+        const int64_t off = static_cast<int64_t>(c) * share;
+        if (off < a.pf_bytes) prefetch_l2(a.pf + off, static_cast<uint32_t>(min(share, a.pf_bytes - off)));
+    }
+    // The routed experts' down matrices, asked of L2 while gate.up streams (a hint): CTA c
+    // takes a contiguous 1/G of the k matrices' bytes, in a few large bulk requests (each
+    // bulk request costs the copy engine about the same whatever its size).
+    auto prefetch_down = [&]() {
+        if (tid != 0 || !a.prefetch_down) return;
+        const int64_t total = static_cast<int64_t>(k) * a.dn_bytes;
+        const int64_t share = ((total + G - 1) / G + 15) / 16 * 16;
+        int64_t off = static_cast<int64_t>(c) * share;
+        const int64_t end = min(total, off + share);
+        while (off < end) {
+            const int s = static_cast<int>(off / a.dn_bytes);
+            const int64_t within = off - static_cast<int64_t>(s) * a.dn_bytes;
+            const int64_t n = min(end - off, a.dn_bytes - within);
+            prefetch_l2(a.w_dn + static_cast<int64_t>(s_e[s]) * a.dn_bytes + within, static_cast<uint32_t>(n));
+            off += n;
+        }
+    };
+    if (rg.n > 0) {
+        const int n = rg.n;
+        unsigned char* wring = ring + warp * kStages * kSlotBytes;
+        const uint32_t ring_addr = smem_addr(wring);
+        // the issue pointer as (slot, tile, panel), advanced by increments
+        int iss_s = rg.item0 / nt_g, iss_t = rg.item0 % nt_g, iss_b = rg.b0;
+        const uint8_t* iss_w = a.w_gu + static_cast<int64_t>(s_e[iss_s]) * a.gu_bytes;
+        auto issue = [&](int st) {
+            issue_panel_block<MOE_W_Q8_0>(ring_addr + st * kSlotBytes, iss_w, 2 * f, iss_t * 16, f + iss_t * 16, iss_b,
+                                          pol, 0);
+            if (++iss_b == npan_g) {
+                iss_b = 0;
+                if (++iss_t == nt_g) {
+                    iss_t = 0;
+                    if (++iss_s < k) iss_w = a.w_gu + static_cast<int64_t>(s_e[iss_s]) * a.gu_bytes;
+                }
+            }
+        };
+#pragma unroll
+        for (int st = 0; st < kStages; ++st) {
+            if (st < n) issue(st);
+            cp_async_commit();
+        }
+        prefetch_down();   // after this warp's first gate.up requests
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        int cur_item = rg.item0, cur_b = rg.b0;
+        for (int i0 = 0; i0 < n; i0 += kStages) {
+#pragma unroll
+            for (int st = 0; st < kStages; ++st) {
+                const int i = i0 + st;
+                if (i < n) {
+                    cp_async_wait<kStages - 1>();
+                    __syncwarp();
+                    panel_mma<MOE_W_Q8_0>(wring + st * kSlotBytes, xh, d, cur_b, 1, 0, acc, split, d);
+                    __syncwarp();   // every lane is done with the slot before it is refilled
+                    if (i + kStages < n) issue(st);
+                    cp_async_commit();
+                    if (++cur_b == npan_g || i == n - 1) {
+                        // this warp's share of the item, token column 0: lanes t == 0 hold rows
+                        // g and g + 8 of the gate block and of the up block
+                        if ((lane & 3) == 0) {
+                            float* rr = cred + ((cur_item - cta_item0) * kDecWarps + warp) * 32;
+                            const int g = lane >> 2;
+                            rr[g] = acc[0][0];
+                            rr[g + 8] = acc[0][2];
+                            rr[16 + g] = acc[1][0];
+                            rr[24 + g] = acc[1][2];
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
+                        cur_b = 0;
+                        ++cur_item;
+                    }
+                }
+            }
+        }
+        cp_async_wait<0>();
+    } else {
+        prefetch_down();
+    }
+    // The CTA's record of each item it touched: its warps' partials in warp order (a warp
+    // that did not touch the item adds zero), at the CTA's contributor slot of the item.
+    __syncthreads();
+    for (int i = tid; i < cta_items * 32; i += kDecThreads) {
+        const int it = i >> 5, j = i & 31;
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) v += cred[(it * kDecWarps + w) * 32 + j];
+        const uint32_t item = static_cast<uint32_t>(cta_item0 + it);
+        const int cidx = c - static_cast<int>(split_owner(U_g, a.warps_g, item * npan_g) / kDecWarps);
+        a.grec[(static_cast<int64_t>(item) * a.cov_g + cidx) * 32 + j] = v;
+    }
+    grid_barrier(a.bar, 2 * G, a.ws.err);
+
+    // ---------------------------------------------------------------- D ring, then H
+    // The down panel blocks do not depend on h: this warp's first ones are requested before
+    // the activations are reduced.
+    const int kf = k * f;
+    __half* hs = reinterpret_cast<__half*>(xf);   // [k][f] hi, then [k][f] lo
+    unsigned char* dring = ring + warp * kStages * kSlotBytes;
+    const uint32_t dring_addr = smem_addr(dring);
+    // the issue pointer as (slot, row tile, panel), advanced by increments: slot-major, so
+    // that a CTA's units read the activations of one or two slots only
+    int dss = rd.item0 / nrt, dsrt = rd.item0 % nrt, dsb = rd.b0;
+    const uint8_t* dsw = a.w_dn + static_cast<int64_t>(s_e[dss < k ? dss : 0]) * a.dn_bytes;
+    auto issue_d = [&](int st) {
+        issue_panel_block<MOE_W_Q8_0>(dring_addr + st * kSlotBytes, dsw, d, dsrt * 32, dsrt * 32 + 16, dsb, pol, 0);
+        if (++dsb == npan_d) {
+            dsb = 0;
+            if (++dsrt == nrt) {
+                dsrt = 0;
+                if (++dss < k) dsw = a.w_dn + static_cast<int64_t>(s_e[dss]) * a.dn_bytes;
+            }
+        }
+    };
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) {
+        if (st < rd.n) issue_d(st);
+        cp_async_commit();
+    }
+    // H: h = SiLU(gate) * up.  Each CTA sums the records (in contributor order) of the slots
+    // its down units read, into its own f16 hi + lo copy of h, and writes them as fp32 too
+    // (every slot is read by some CTA; CTAs that share a slot write the same values).
+    int h_lo_q = 0, h_hi_q = 0;   // neurons [h_lo_q, h_hi_q) of the flattened [k][f]
+    {
+        const uint32_t w0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_d));
+        const uint32_t w1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_d));
+        const uint32_t v0 = split_begin(U_d, a.warps_d, w0), v1 = split_begin(U_d, a.warps_d, w1);
+        const uint32_t per_slot = static_cast<uint32_t>(nrt * npan_d);
+        if (v1 > v0) {
+            h_lo_q = static_cast<int>(v0 / per_slot) * f;
+            h_hi_q = (static_cast<int>((v1 - 1) / per_slot) + 1) * f;
+        }
+    }
+    int* gcov = reinterpret_cast<int*>(slog);     // CTAs that recorded each gate.up item (items_g <= 1024)
+    for (int i = tid; i < static_cast<int>(items_g); i += kDecThreads) {
+        const uint32_t u0 = static_cast<uint32_t>(i) * npan_g, u1 = u0 + npan_g - 1;
+        gcov[i] = static_cast<int>(split_owner(U_g, a.warps_g, u1) / kDecWarps -
+                                   split_owner(U_g, a.warps_g, u0) / kDecWarps) + 1;
+    }
+    __syncthreads();
+    constexpr int kHB = 4;   // neurons per thread per batch: their first two records load together
+    for (int q0 = h_lo_q + tid; q0 < h_hi_q; q0 += kHB * kDecThreads) {   // neuron q = item * 16 + j
+        float g0[kHB], g1[kHB], u0[kHB], u1[kHB];
+#pragma unroll
+        for (int u = 0; u < kHB; ++u) {
+            const int q = q0 + u * kDecThreads;
+            g0[u] = g1[u] = u0[u] = u1[u] = 0.0f;
+            if (q < h_hi_q) {
+                const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
+                g0[u] = __ldcg(rec);
+                u0[u] = __ldcg(rec + 16);
+                if (gcov[q >> 4] > 1) {
+                    g1[u] = __ldcg(rec + 32);
+                    u1[u] = __ldcg(rec + 48);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kHB; ++u) {
+            const int q = q0 + u * kDecThreads;
+            if (q < h_hi_q) {
+                float zg = g0[u] + g1[u], zu = u0[u] + u1[u];   // records in contributor order
+                const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
+                for (int cc = 2; cc < gcov[q >> 4]; ++cc) {
+                    zg += __ldcg(rec + cc * 32);
+                    zu += __ldcg(rec + cc * 32 + 16);
+                }
+                const float h = silu(zg) * zu;
+                const __half hi = __float2half_rn(h);
+                hs[q] = hi;
+                hs[kf + q] = __float2half_rn(h - __half2float(hi));
+                a.ws.h[q] = h;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- D: down partial sums
+    // A unit is one 32-neuron panel of a 32-row tile of one slot's down matrix (two 16-row
+    // MMA blocks, the gate.up panel product with h as the activations).
+    if (rd.n > 0) {
+        const int n = rd.n;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        int cur_item = rd.item0, cur_s = rd.item0 / nrt, cur_rt = rd.item0 % nrt, cur_b = rd.b0, cur_c = rd.c0;
+        for (int i0 = 0; i0 < n; i0 += kStages) {
+#pragma unroll
+            for (int st = 0; st < kStages; ++st) {
+                const int i = i0 + st;
+                if (i < n) {
+                    cp_async_wait<kStages - 1>();
+                    __syncwarp();
+                    panel_mma<MOE_W_Q8_0>(dring + st * kSlotBytes, hs + cur_s * f, f, cur_b, 1, 0, acc, true, kf);
+                    __syncwarp();   // every lane is done with the slot before it is refilled
+                    if (i + kStages < n) issue_d(st);
+                    cp_async_commit();
+                    if (++cur_b == npan_d || i == n - 1) {
+                        if ((lane & 3) == 0) {   // rows g, g + 8 of both blocks, token column 0
+                            float* rec = a.drec + (static_cast<int64_t>(cur_item) * a.cov_d + cur_c) * 32;
+                            const int g = lane >> 2;
+                            rec[g] = acc[0][0];
+                            rec[g + 8] = acc[0][2];
+                            rec[16 + g] = acc[1][0];
+                            rec[24 + g] = acc[1][2];
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
+                        cur_b = 0;
+                        cur_c = 0;
+                        ++cur_item;
+                        if (++cur_rt == nrt) {
+                            cur_rt = 0;
+                            ++cur_s;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    grid_barrier(a.bar, 3 * G, a.ws.err);
+
+    // ---------------------------------------------------------------- C: combine
+    // Row tile rt (32 outputs) is combined by CTA rt mod G: y of each slot (its records in
+    // contributor order), then out[r] = sum over the pairs j in order of w_j * y_{slot(j)}[r].
+    float* s_y = slog;   // [k][32] (kMaxK * 32 == kMaxE floats)
+    static_assert(kMaxK * 32 <= kMaxE, "combine buffer");
+    for (int rt = c; rt < nrt; rt += G) {
+        for (int task = tid; task < k * 32; task += kDecThreads) {
+            const int s = task >> 5, r = task & 31;
+            const uint32_t item = static_cast<uint32_t>(s * nrt + rt);
+            const int nc = item_contributors(U_d, a.warps_d, npan_d, item);
+            const float* rec = a.drec + static_cast<int64_t>(item) * a.cov_d * 32 + r;
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = q < nc ? __ldcg(rec + q * 32) : 0.0f;
+            float y = ((v[0] + v[1]) + v[2]) + v[3];   // records in contributor order
+            for (int cc = 4; cc < nc; ++cc) y += __ldcg(rec + cc * 32);
+            s_y[s * 32 + r] = y;
+        }
+        __syncthreads();
+        if (tid < 32) {
+            float o = 0.0f;
+            for (int j = 0; j < k; ++j) o = fmaf(s_w[j], s_y[s_pos[j] * 32 + tid], o);
+            a.out[rt * 32 + tid] = o;
+        }
+        __syncthreads();
+    }
+    // The last CTA to finish resets the barrier counters for the next call (every CTA has
+    // passed all three barriers by now).
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(a.bar + 1, 1) == G - 1) {
+            a.bar[0] = 0;
+            a.bar[1] = 0;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------ host side
+// Largest dynamic shared memory the kernel is configured for: region B up to 64 KB
+// (k*f <= 16384, d <= 16384), region C up to 32 KB (d <= 8192, or 4096 for fp32 x), region P
+// up to 16 KB (8 items); with the static arrays, within the 227 KB of one CTA.
+size_t decode_max_smem() { return kRingBytes + 2 * 32768 + 2 * 16384 + 16384; }
+
+namespace {
+bool g_decode_ok[64] = {};
+int g_decode_ctas[64] = {};
+}  // namespace
+
+// Dynamic shared memory limit, cooperative-launch support and one-CTA-per-SM residency
+// (once per device, with that device current).
+cudaError_t configure_decode_kernel(int dev, int num_sms) {
+    g_decode_ok[dev] = false;
+    int coop = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (e != cudaSuccess) return e;
+    if (!coop) return cudaSuccess;
+    const int max_smem = static_cast<int>(decode_max_smem());
+    e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return cudaSuccess;   // the separate kernels serve every shape
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel, kDecThreads, max_smem);
+    if (e != cudaSuccess || per_sm < 1) {
+        (void)cudaGetLastError();
+        return cudaSuccess;
+    }
+    g_decode_ok[dev] = true;
+    g_decode_ctas[dev] = num_sms < kMaxDecodeCtas ? num_sms : kMaxDecodeCtas;
+    return cudaSuccess;
+}
+
+// CTAs of the decode kernel on this device (0: not available).
+int decode_ctas(int dev) { return (dev >= 0 && dev < 64 && g_decode_ok[dev]) ? g_decode_ctas[dev] : 0; }
+
+cudaError_t launch_decode_layer(const DecodeArgs& a, int ctas, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = decode_smem_bytes(a.d, a.f, a.k, a.xt, a.cta_items);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
+}
+
+}  // namespace moe

@@ -104,7 +104,8 @@ def test_layer_validation(L):
     # workspace: missing, misaligned, too small
     assert F(ctypes.byref(ok), FAKE, 0, 16, None, None, FAKE, None, need, None, None) == 4
     assert F(ctypes.byref(ok), FAKE, 0, 16, None, None, FAKE, FAKE + 16, need, None, None) == 3
-    assert F(ctypes.byref(ok), FAKE, 0, 16, None, None, FAKE, FAKE, need - 1, None, None) == 4
+    need1 = L.moe_layer_workspace_bytes(ctypes.byref(ok), 1)   # the exact need of one token
+    assert F(ctypes.byref(ok), FAKE, 0, 1, None, None, FAKE, FAKE, need1 - 1, None, None) == 4
     # an empty batch returns OK without touching anything
     assert F(ctypes.byref(ok), FAKE, 0, 0, None, None, FAKE, None, 0, None, None) == 0
 

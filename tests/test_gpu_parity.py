@@ -199,9 +199,58 @@ def test_layer_gemm_skewed_routing():
 @pytest.mark.parametrize("k", [1, 4])
 def test_one_token_row_tile_down(k):
     w = synth.Workload(f"t1_k{k}", d=512, f=256, E=8, k=k, act="swiglu", wfmt="q8_0", x_dtype="bf16", layers=1)
-    L, out, tr, ref = _run_small(w, 1)
+    L, out, tr, ref = _run_small(w, 1, path="gemv")
+    assert L.launches(1) == 3
     assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
     assert_close(out, ref["out"])
+
+
+# One token, Q8_0 SwiGLU, routing computed: the whole layer as one cooperative kernel
+# (router, top-k, softmax, gate.up, down, combine; two grid barriers).  The shapes cover
+# k = 1 .. 8 and 32, E from 4 to 1024 (1024 experts: 8 per routing CTA), fp32 and bf16 inputs,
+# panel ranges that split items across warps and warps that span several items; every case
+# is checked against the oracle and against the separate-kernel path, and the output must
+# be completely written and bitwise identical over three calls.
+ONE_KERNEL = {
+    "tiny_f32": synth.WORKLOADS["tiny"],
+    "k1": synth.Workload("ok_k1", d=512, f=256, E=8, k=1, act="swiglu", wfmt="q8_0", x_dtype="bf16", layers=1),
+    "k8_e64": synth.Workload("ok_k8", d=1024, f=192, E=64, k=8, act="swiglu", wfmt="q8_0", x_dtype="bf16", layers=1),
+    "k3_e12_f32": synth.Workload("ok_k3", d=768, f=96, E=12, k=3, act="swiglu", wfmt="q8_0", x_dtype="f32",
+                                 layers=1),
+    "k32_e1024": synth.Workload("ok_k32", d=256, f=64, E=1024, k=32, act="swiglu", wfmt="q8_0", x_dtype="bf16",
+                                layers=1),
+    "e4_k4": synth.Workload("ok_e4", d=256, f=32, E=4, k=4, act="swiglu", wfmt="q8_0", x_dtype="bf16", layers=1),
+}
+
+
+@pytest.mark.parametrize("name", list(ONE_KERNEL))
+def test_one_token_one_kernel(name):
+    w = ONE_KERNEL[name]
+    L, out, tr, ref = _run_small(w, 1)
+    assert L.launches(1) == 1
+    assert np.array_equal(tr["logits"].cpu().numpy().view(np.uint32), ref["logits"].view(np.uint32))
+    assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
+    assert np.allclose(tr["w"].cpu().numpy(), ref["w"], rtol=1e-6, atol=0)
+    assert np.array_equal(tr["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(tr["pos"].cpu().numpy(), ref["pos"])
+    assert_close(tr["h"].cpu().numpy(), ref["h"][ref["perm"]], what="h")
+    assert_close(out, ref["out"])
+    x = torch.from_numpy(synth.tokens(w, 1, tag="parity")).cuda()
+    if w.x_dtype == "bf16":
+        x = x.view(torch.bfloat16)
+    outs = []
+    for _ in range(3):
+        o = torch.full((1, w.d), float("nan"), device="cuda")
+        L.forward(x, out=o)
+        outs.append(o.cpu().numpy())
+    assert np.isfinite(outs[0]).all()
+    for o in outs:
+        assert np.array_equal(o.view(np.uint32), out.view(np.uint32))
+    assert L.device_status() == 0
+    L.set_path("gemv")
+    assert L.launches(1) > 1
+    assert_close(L.forward(x).cpu().numpy(), ref["out"])
 
 
 def test_one_token_repeated_expert_in_supplied_routing():
