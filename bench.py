@@ -228,12 +228,35 @@ def build_stack(w, T, layers, local_rank):
     return stack, inputs
 
 
-def capture_graphs(stack, inputs, T, w, stage_events=None):
-    """One CUDA graph per rotated input; each runs the whole stack."""
+def capture_graphs(stack, inputs, T, w, stage_events=None, stack_obj=None):
+    """One CUDA graph per rotated input; each runs the whole stack (with stack_obj: one
+    moe_stack_forward call; stage_events then holds two events per input, around it)."""
     import torch
 
     from quantized_routed_expert_softmax_gb300 import native
     dev = torch.device("cuda")
+    if stack_obj is not None:
+        outs_all = torch.empty((len(stack), w.d), dtype=torch.float32, device=dev)
+        ws = stack_obj.workspace()
+        graphs = []
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            stack_obj.forward(inputs[0], outs=outs_all, workspace=ws)   # warm outside capture
+            torch.cuda.current_stream().synchronize()
+            for g_i, x0 in enumerate(inputs):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    ev = None if stage_events is None else stage_events[g_i]
+                    if ev is not None:
+                        ev[0].record()
+                    stack_obj.forward(x0, outs=outs_all, workspace=ws)
+                    if ev is not None:
+                        ev[1].record()
+                graphs.append(g)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return graphs, [outs_all[l:l + 1] for l in range(len(stack))]
     outs = [torch.empty((T, w.d), dtype=torch.float32, device=dev) for _ in stack]
     nxt = [torch.empty((T, w.d), dtype=torch.bfloat16, device=dev) for _ in stack]
     wss = [layer.workspace(T) for layer in stack]
@@ -275,7 +298,12 @@ def run_ours(args, rank, world, local_rank):
     T = args.tokens
     layers = args.layers or w.layers
     stack, inputs = build_stack(w, T, layers, local_rank)
-    graphs, outs = capture_graphs(stack, inputs, T, w)
+    # One token on layers the library runs as one kernel per layer: the whole stack as ONE
+    # kernel (moe_stack_forward), the RMS-norm between layers inside it.
+    stack_obj = native.MoEStack(stack) if T == 1 else None
+    if stack_obj is not None and stack_obj.launches() != 1:
+        stack_obj = None
+    graphs, outs = capture_graphs(stack, inputs, T, w, stack_obj=stack_obj)
 
     def barrier():
         if world > 1:
@@ -313,7 +341,42 @@ def run_ours(args, rank, world, local_rank):
     n_ev_steps = max(N_ROTATE, min(args.steps, 400))
     gu_ms, dn_ms, rt_ms, cb_ms = [], [], [], []
     timing_how = "CUDA events recorded as graph nodes at the stage boundaries of every layer"
+    if stack_obj is not None:   # one kernel per step: events around it
+        try:   # events that are real record nodes under capture
+            sev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in inputs]
+        except TypeError:
+            sev = None
+        if sev is not None:
+            timing_how = "CUDA events recorded as graph nodes around the one-kernel stack"
+            for pair in sev:
+                for ev in pair:
+                    ev.record()
+            torch.cuda.synchronize()
+            graphs_ev, _ = capture_graphs(stack, inputs, T, w, stage_events=sev, stack_obj=stack_obj)
+            for i in range(args.warmup):
+                graphs_ev[i % N_ROTATE].replay()
+            torch.cuda.synchronize()
+            for i in range(n_ev_steps):
+                graphs_ev[i % N_ROTATE].replay()
+                if i % N_ROTATE == N_ROTATE - 1:
+                    torch.cuda.synchronize()
+                    rt_ms.extend(pair[0].elapsed_time(pair[1]) for pair in sev)
+        else:   # this torch cannot record external events under capture: time eager launches
+            timing_how = "CUDA events around eager launches of the one-kernel stack"
+            e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            outs_e = torch.empty((layers, w.d), dtype=torch.float32, device="cuda")
+            for i in range(max(args.warmup, 3)):
+                stack_obj.forward(inputs[i % N_ROTATE], outs=outs_e)
+            for i in range(n_ev_steps):
+                e_a.record()
+                stack_obj.forward(inputs[i % N_ROTATE], outs=outs_e)
+                e_b.record()
+                e_b.synchronize()
+                rt_ms.append(e_a.elapsed_time(e_b))
+        torch.cuda.synchronize()
     try:
+        if stack_obj is not None:
+            raise StopIteration
         graphs_ev, _ = capture_graphs(stack, inputs, T, w, stage_events=evs)
         for i in range(args.warmup):
             graphs_ev[i % N_ROTATE].replay()
@@ -327,6 +390,8 @@ def run_ours(args, rank, world, local_rank):
                 gu_ms.append(lay[1].elapsed_time(lay[2]))
                 dn_ms.append(lay[2].elapsed_time(lay[3]))
                 cb_ms.append(lay[3].elapsed_time(lay[4]))
+    except StopIteration:
+        pass
     except Exception as exc:   # graph event nodes refused: time the same launches eagerly
         timing_how = f"CUDA events around eager launches of the stack (graph events unavailable: {exc})"
         gu_ms, dn_ms, rt_ms, cb_ms = [], [], [], []
@@ -348,7 +413,12 @@ def run_ours(args, rank, world, local_rank):
     # later boundaries coincide with the second), with all the layer's bytes as its work.
     one_kernel = stack[0].launches(T) == 1
     peak, peak_src = hbm_peak()
-    if one_kernel:
+    if stack_obj is not None:   # the one-kernel stack: a launch processes every layer
+        gu_ms = list(rt_ms)
+        gu_us = statistics.mean(gu_ms) * 1e3
+        gu_bytes = tr_bytes["layer_per_launch"] * layers
+        gu_flops = 2 * T * w.k * (w.rows_gu * w.d + w.d * w.f) * layers
+    elif one_kernel:
         gu_ms = list(rt_ms)
         gu_us = statistics.mean(gu_ms) * 1e3
         gu_bytes = tr_bytes["layer_per_launch"]
@@ -388,7 +458,8 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(a0.elapsed_time(a1), world)
     e2e_value = job_throughput(T * e2e_steps, world, e2e_ms)
 
-    launches_per_step = sum(layer.launches(T) + 1 for layer in stack)   # + the RMS-norm glue
+    launches_per_step = (1 if stack_obj is not None else
+                         sum(layer.launches(T) + 1 for layer in stack))   # + the RMS-norm glue
     result = None
     if rank == 0:
         step_bytes = tr_bytes["step"]
@@ -404,12 +475,18 @@ def run_ours(args, rank, world, local_rank):
             "active_expert_gbs": round(step_bytes * world / (ms_step * 1e-3) / 1e9, 1),
             "active_expert_frac_of_measured_hbm": round(step_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
             "active_expert_frac_of_8tbs": round(step_bytes / (ms_step * 1e-3) / 1e9 / 8000.0, 4),
-            "stage_us_mean": ({"layer_kernel": round(gu_us, 2)} if one_kernel else
+            "stage_us_mean": ({"stack_kernel": round(gu_us, 2), "per_layer": round(gu_us / layers, 3)}
+                              if stack_obj is not None else {"layer_kernel": round(gu_us, 2)} if one_kernel else
                               {"routing": round(statistics.mean(rt_ms) * 1e3, 2), "gate_up": round(gu_us, 2),
                                "down": round(statistics.mean(dn_ms) * 1e3, 2),
                                "combine": round(statistics.mean(cb_ms) * 1e3, 2)}),
         })
-        if one_kernel:
+        if stack_obj is not None:
+            cfg["layer_kernel"] = ("decode_layer_kernel over the whole stack (moe_stack_forward): router, top-k, "
+                                   "softmax, gate.up + SwiGLU, down, combine and the RMS-norm glue of every layer in "
+                                   "one cooperative launch per step (one CTA per SM)")
+            cfg["graph"] = "one CUDA graph per rotated input holds the single stack launch"
+        elif one_kernel:
             cfg["layer_kernel"] = ("decode_layer_kernel: router, top-k, softmax, gate.up + SwiGLU, down and combine "
                                    "in one cooperative launch per layer (one CTA per SM)")
         result = {
@@ -419,7 +496,9 @@ def run_ours(args, rank, world, local_rank):
             "data": "synthetic (seeded; random-init weights of the workload's shapes)",
             "config": cfg,
             "roofline": {"bound": "hbm",
-                         "kernel": ("decode_layer_kernel (the whole layer: routed experts' gate.up + down "
+                         "kernel": ("decode_layer_kernel (the whole stack in one launch: every layer's routed "
+                                    "experts' gate.up + down bytes and router weights)" if stack_obj is not None else
+                                    "decode_layer_kernel (the whole layer: routed experts' gate.up + down "
                                     "bytes and the router weights)" if one_kernel else
                                     "expert_gemm_kernel (gate.up + activation, tcgen05)" if gemm
                                     else "gate_up_gemv (gate.up + activation + group mask)"),

@@ -231,6 +231,34 @@ int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_
 moe_status moe_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uint16_t* xo, moe_stream_t stream);
 
 /*
+ * moe_stack_forward -- a stack of routed MoE layers for ONE token, the layers glued by the
+ * RMS-norm of moe_rmsnorm_bf16:
+ *   x_0 = x;  out_l = layer_l(x_l);  x_{l+1} = bf16(out_l / sqrt(mean(out_l^2) + eps)).
+ * (The pages' models run their MoE layers as such a stack: Gemma-4 26B-A4B has 30, the
+ * MiniMax model of "Why can super-large MoE be distributed for inference" 57.)
+ * descs    n_layers layer descriptors of one shape (d, f, E, k, act, wfmt, path equal;
+ *          the weights, router and L2 hint per layer).
+ * x        device [1][d], fp32 or bf16 (xt): the first layer's input.
+ * outs     device fp32 [n_layers][d] (written): every layer's output.
+ * x_next   optional device bf16 [n_layers][d]: x_{l+1} for every l (the last one too), or NULL.
+ * idx, w   optional device int32 / fp32 [n_layers][k]: each layer's routing, or both NULL.
+ * workspace at least moe_layer_workspace_bytes(descs, 1) bytes, zero-filled before its first
+ *          use (as for moe_layer_forward).
+ * With Q8_0 SwiGLU layers, path AUTO, at most 64 layers and a device that supports
+ * cooperative launches, the whole stack is ONE kernel launch (one CTA per SM, the RMS-norm
+ * between layers inside it, bitwise equal to the layer-by-layer result); otherwise each
+ * layer is a moe_layer_forward call followed by the RMS-norm.
+ * Errors: those of moe_layer_forward, and SHAPE when the descriptors differ in shape.
+ */
+moe_status moe_stack_forward(const moe_layer_desc* descs, int32_t n_layers, const void* x, moe_dtype xt, float eps,
+                             float* outs, uint16_t* x_next, int32_t* idx, float* w, void* workspace, size_t ws_bytes,
+                             moe_stream_t stream);
+
+/* Kernels one moe_stack_forward call launches (bf16 or fp32 x, current device); -1 on bad
+ * descriptors. */
+int32_t moe_stack_forward_launches(const moe_layer_desc* descs, int32_t n_layers, int32_t with_x_next);
+
+/*
  * Bytes of the fixed device scratch behind moe_layer_forward_noalloc (16 MiB).
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)

@@ -193,7 +193,7 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
 
 struct Layout {
     size_t err, route_ctr, n_active, row_ctr, logits, rpart, idx, w, offsets, perm, pos, act_e, slot_info, chunk_cnt,
-        local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, dec_bar, dec_grec, dec_drec, total;
+        local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, dec_bar, dec_grec, dec_drec, xnext, total;
 };
 
 // Workspace regions for T tokens (each 256-byte aligned).  The control words (err,
@@ -240,6 +240,7 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     L.dec_bar = take(dec ? sizeof(int32_t) * 2 : 0);
     L.dec_grec = take(dec ? sizeof(float) * 32 * d->k * (d->f / 16) * sp.cov_g : 0);
     L.dec_drec = take(dec ? sizeof(float) * 32 * (d->d / 32) * d->k * sp.cov_d : 0);
+    L.xnext = take(T == 1 ? sizeof(uint16_t) * d->d : 0);   // a stack's next input (one token)
     L.total = off;
     return L;
 }
@@ -290,6 +291,53 @@ moe_status validate_desc(const moe_layer_desc* d) {
     return MOE_OK;
 }
 
+// The one-kernel decode arguments for n layers of descs[0]'s shape (pointers per layer), on
+// the current device; false when the device or the shape cannot run it.
+bool fill_decode_args(const moe_layer_desc* descs, int n, const void* x, int xt, void* workspace, const Layout& L,
+                      const Workspace& ws, DecodeArgs* a, int* ctas_out) {
+    const moe_layer_desc* desc = descs;
+    const Plan p = make_plan(desc, 1, xt);
+    if (!p.decode1 || n < 1 || n > kMaxStackLayers) return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const int ctas = decode_ctas(dev);
+    const int epc = decode_epc(desc->E, ctas);
+    const DecodeSplit sp = decode_split(desc, std::max(1, ctas));
+    if (ctas <= 0 || epc <= 0 || !decode_split_fits(desc, sp, xt)) return false;
+    char* base = static_cast<char*>(workspace);
+    *a = DecodeArgs{};
+    a->x = x;
+    a->xt = xt;
+    a->d = static_cast<int>(desc->d);
+    a->f = static_cast<int>(desc->f);
+    a->E = static_cast<int>(desc->E);
+    a->k = desc->k;
+    a->epc = epc;
+    a->prefetch_down = p.prefetch_down ? 1 : 0;
+    // warps that share each phase's panel range: all of them, or one per unit
+    a->warps_g = static_cast<int>(sp.warps_g);
+    a->warps_d = static_cast<int>(sp.warps_d);
+    a->cov_g = static_cast<int>(sp.cov_g);
+    a->cov_d = static_cast<int>(sp.cov_d);
+    a->cta_items = static_cast<int>(sp.cta_items);
+    a->gu_bytes = static_cast<int64_t>(moe_q8_0_bytes(2 * desc->f, desc->d));
+    a->dn_bytes = static_cast<int64_t>(moe_q8_0_bytes(desc->d, desc->f));
+    a->n_layers = n;
+    for (int l = 0; l < n; ++l) {
+        a->lp[l].W = descs[l].router_w;
+        a->lp[l].w_gu = static_cast<const uint8_t*>(descs[l].w_gate_up);
+        a->lp[l].w_dn = static_cast<const uint8_t*>(descs[l].w_down);
+        a->lp[l].pf = static_cast<const uint8_t*>(descs[l].l2_prefetch);
+        a->lp[l].pf_bytes = descs[l].l2_prefetch ? (descs[l].l2_prefetch_bytes & ~static_cast<int64_t>(15)) : 0;
+    }
+    a->ws = ws;
+    a->bar = reinterpret_cast<int32_t*>(base + L.dec_bar);
+    a->grec = reinterpret_cast<float*>(base + L.dec_grec);
+    a->drec = reinterpret_cast<float*>(base + L.dec_drec);
+    *ctas_out = ctas;
+    return true;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -297,7 +345,7 @@ using namespace moe;
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 10100; }
+int32_t moe_abi_version(void) { return 10200; }
 
 const char* moe_status_string(moe_status s) {
     switch (s) {
@@ -441,40 +489,10 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     // One token, routing computed here: the whole layer as one cooperative kernel when the
     // device and the shape allow it.
     if (p.decode1 && !idx_in) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-        const int ctas = decode_ctas(dev);
-        const int epc = decode_epc(desc->E, ctas);
-        const DecodeSplit sp = decode_split(desc, std::max(1, ctas));
-        if (ctas > 0 && epc > 0 && decode_split_fits(desc, sp, xt)) {
-            char* base = static_cast<char*>(workspace);
-            DecodeArgs a{};
-            a.x = x;
-            a.xt = xt;
-            a.W = desc->router_w;
-            a.d = static_cast<int>(desc->d);
-            a.f = static_cast<int>(desc->f);
-            a.E = static_cast<int>(desc->E);
-            a.k = k;
-            a.epc = epc;
-            a.prefetch_down = p.prefetch_down ? 1 : 0;
-            // warps that share each phase's panel range: all of them, or one per unit
-            a.warps_g = static_cast<int>(sp.warps_g);
-            a.warps_d = static_cast<int>(sp.warps_d);
-            a.cov_g = static_cast<int>(sp.cov_g);
-            a.cov_d = static_cast<int>(sp.cov_d);
-            a.cta_items = static_cast<int>(sp.cta_items);
-            a.w_gu = static_cast<const uint8_t*>(desc->w_gate_up);
-            a.gu_bytes = static_cast<int64_t>(moe_q8_0_bytes(2 * desc->f, desc->d));
-            a.w_dn = static_cast<const uint8_t*>(desc->w_down);
-            a.dn_bytes = static_cast<int64_t>(moe_q8_0_bytes(desc->d, desc->f));
-            a.pf = static_cast<const uint8_t*>(desc->l2_prefetch);
-            a.pf_bytes = desc->l2_prefetch ? (desc->l2_prefetch_bytes & ~static_cast<int64_t>(15)) : 0;
+        DecodeArgs a{};
+        int ctas = 0;
+        if (fill_decode_args(desc, 1, x, xt, workspace, L, ws, &a, &ctas)) {
             a.out = out;
-            a.ws = ws;
-            a.bar = reinterpret_cast<int32_t*>(base + L.dec_bar);
-            a.grec = reinterpret_cast<float*>(base + L.dec_grec);
-            a.drec = reinterpret_cast<float*>(base + L.dec_drec);
             e = launch_decode_layer(a, ctas, s);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
             for (int i = 1; i <= 4; ++i) mark(i);   // one kernel: the inner boundaries coincide
@@ -572,6 +590,80 @@ int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_
     if (p.gemm) n += 1;                                     // sorted f16 copy of x
     if (!p.fuse_combine) n += 1;                            // combine
     return n;
+}
+
+// Layers of one shape (the first descriptor's d, f, E, k, activation and format).
+static moe_status validate_stack(const moe_layer_desc* descs, int32_t n_layers) {
+    if (!descs || n_layers < 1) return MOE_ERR_INVALID_ARG;
+    for (int32_t l = 0; l < n_layers; ++l) {
+        const moe_status st = validate_desc(descs + l);
+        if (st != MOE_OK) return st;
+        const moe_layer_desc& a = descs[0];
+        const moe_layer_desc& b = descs[l];
+        if (a.d != b.d || a.f != b.f || a.E != b.E || a.k != b.k || a.act != b.act || a.wfmt != b.wfmt ||
+            a.path != b.path)
+            return MOE_ERR_SHAPE;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_stack_forward(const moe_layer_desc* descs, int32_t n_layers, const void* x, moe_dtype xt, float eps,
+                             float* outs, uint16_t* x_next, int32_t* idx, float* w, void* workspace, size_t ws_bytes,
+                             moe_stream_t stream) {
+    moe_status st = validate_stack(descs, n_layers);
+    if (st != MOE_OK) return st;
+    if (xt != MOE_F32 && xt != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (!x || !outs || (idx == nullptr) != (w == nullptr) || !(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(outs) || (x_next && !aligned16(x_next))) return MOE_ERR_ALIGNMENT;
+    if ((idx && (reinterpret_cast<uintptr_t>(idx) & 3u)) || (w && (reinterpret_cast<uintptr_t>(w) & 3u)))
+        return MOE_ERR_ALIGNMENT;
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_ALIGNMENT;
+    const Layout L = layout_for(descs, 1);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    int num_sms = 0;
+    if (ensure_configured(&num_sms) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t d = descs[0].d, k = descs[0].k;
+    // the whole stack as one cooperative kernel
+    {
+        DecodeArgs a{};
+        int ctas = 0;
+        if (fill_decode_args(descs, n_layers, x, xt, workspace, L, bind(workspace, L), &a, &ctas)) {
+            a.out = outs;
+            a.eps = eps;
+            a.x_next = x_next;
+            a.idx_out = idx;
+            a.w_out = w;
+            return cuda_status(launch_decode_layer(a, ctas, s));
+        }
+    }
+    // otherwise layer by layer, the RMS-norm glue between them
+    uint16_t* scratch = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + L.xnext);
+    const void* xl = x;
+    moe_dtype xtl = xt;
+    for (int32_t l = 0; l < n_layers; ++l) {
+        moe_trace tr{};
+        tr.idx = idx ? idx + l * k : nullptr;
+        tr.w = w ? w + l * k : nullptr;
+        st = moe_layer_forward(descs + l, xl, xtl, 1, nullptr, nullptr, outs + l * d, workspace, ws_bytes,
+                               idx ? &tr : nullptr, stream);
+        if (st != MOE_OK) return st;
+        const bool last = l + 1 == n_layers;
+        if (last && !x_next) break;
+        uint16_t* xn = x_next ? x_next + l * d : scratch;
+        if (launch_rmsnorm_bf16(outs + l * d, 1, d, eps, xn, s) != cudaSuccess) return MOE_ERR_CUDA;
+        xl = xn;
+        xtl = MOE_BF16;
+    }
+    return MOE_OK;
+}
+
+int32_t moe_stack_forward_launches(const moe_layer_desc* descs, int32_t n_layers, int32_t with_x_next) {
+    if (validate_stack(descs, n_layers) != MOE_OK) return -1;
+    int32_t one = moe_layer_forward_launches(descs, 1, 0);
+    if (one == 1 && n_layers <= kMaxStackLayers) return 1;
+    return n_layers * (one + 1) - (with_x_next ? 0 : 1);
 }
 
 moe_status moe_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uint16_t* xo, moe_stream_t stream) {

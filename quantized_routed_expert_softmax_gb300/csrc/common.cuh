@@ -73,29 +73,41 @@ struct ExpertArgs {
     Workspace ws;
 };
 
-// Arguments of the one-kernel decode layer (decode.cu): one token, Q8_0 SwiGLU experts.
-// The kernel's own control words and partial sums sit in the layer workspace too.
-struct DecodeArgs {
-    const void* x;
-    int xt;
+// Arguments of the one-kernel decode layer (decode.cu): one token, Q8_0 SwiGLU experts, one
+// layer or a stack of layers of the same shape (the next layer's input is the RMS-normalised
+// output of the previous one).  The kernel's own control words and partial sums sit in the
+// layer workspace too.
+constexpr int kMaxStackLayers = 64;
+
+struct DecodeLayerPtrs {
     const float* W;              // router [d][E]
+    const uint8_t* w_gu;         // gate/up matrices of the E experts (Q8_0, device layout)
+    const uint8_t* w_dn;         // down matrices
+    const uint8_t* pf;           // L2 hint (the next layer's router weights), or null
+    int64_t pf_bytes;
+};
+
+struct DecodeArgs {
+    const void* x;               // the first layer's input [d]
+    int xt;
     int d, f, E, k;
     int epc;                     // router experts per routing CTA (E / epc CTAs compute logits)
     int prefetch_down;           // the routed experts' down matrices are pulled into L2 during gate.up
     int warps_g, warps_d;        // warps that share the gate.up / down panel ranges
     int cov_g, cov_d;            // partial records per item at most (CTAs / warps that can share one item)
     int cta_items;               // gate.up items one CTA's range touches at most
-    const uint8_t* w_gu;
-    int64_t gu_bytes;
-    const uint8_t* w_dn;
-    int64_t dn_bytes;
-    const uint8_t* pf;           // L2 hint (the next layer's router weights), or null
-    int64_t pf_bytes;
-    float* out;                  // [d]
+    int64_t gu_bytes, dn_bytes;  // bytes of one expert's gate/up and down matrices
+    int n_layers;                // 1: moe_layer_forward; more: moe_stack_forward
+    float eps;                   // RMS-norm between stacked layers
+    float* out;                  // [n_layers][d] every layer's output
+    uint16_t* x_next;            // [n_layers][d] bf16 RMS-normalised outputs (stacks; may be null)
+    int32_t* idx_out;            // [n_layers][k] routing of each layer (stacks; may be null)
+    float* w_out;                // [n_layers][k]
     Workspace ws;
     int32_t* bar;                // [2] grid-barrier arrivals, CTAs finished (zero between calls)
     float* grec;                 // [k * f/16][cov_g][32] gate.up partial sums per item and contributor
     float* drec;                 // [k * d/32][cov_d][32] down partial sums per item and contributor
+    DecodeLayerPtrs lp[kMaxStackLayers];
 };
 
 // Programmatic dependent launch: wait for the preceding kernel's memory, and allow the

@@ -163,15 +163,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     const bool router = c < E / epc;
     float* wsl = reinterpret_cast<float*>(ring);   // [d][epc]
     float* red = wsl + d * epc;                     // [epc][256]
-    if (router) {   // the weights do not depend on the previous kernel: copied before waiting
-        const float* src = a.W + c * epc;
+    // this CTA's slice of a layer's router weights, copied asynchronously into the ring region
+    auto request_router = [&](const float* W) {
+        if (!router) return;
+        const float* src = W + c * epc;
         const uint32_t wb = smem_addr(wsl);
         for (int it = tid; it < d * epc; it += kDecThreads) {
             const int i = it / epc, e = it % epc;
             cp_async4(wb + static_cast<uint32_t>(it) * 4, src + static_cast<int64_t>(i) * E + e);
         }
         cp_async_commit();
-    }
+    };
+    request_router(a.lp[0].W);   // does not depend on the previous kernel: before waiting for it
     pdl_wait();
     for (int i = tid; i < d / 4; i += kDecThreads) {
         float4 v;
@@ -193,364 +196,406 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             reinterpret_cast<__half2*>(xh + d)[2 * i + 1] = l23;
         }
     }
-    cp_async_wait<0>();
-    __syncthreads();
-    if (router) {
-        if (tid < kRouterPartials) {   // chain l: fmaf over i = l, l + 256, ... in increasing i
-            float acc[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-            const int nchain = d / kRouterPartials;
-            for (int m = 0; m < nchain; ++m) {
-                const int i = tid + m * kRouterPartials;
-                const float xv = xf[i];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (e < epc) acc[e] = fmaf(xv, wsl[i * epc + e], acc[e]);
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if (e < epc) red[e * kRouterPartials + tid] = acc[e];
-        }
+    int nbar = 0;   // grid barriers passed (the counter target of the next is (nbar + 1) * G)
+    for (int l = 0; l < a.n_layers; ++l) {
+        const DecodeLayerPtrs P = a.lp[l];
+        const bool split_l = l == 0 && split;   // later layers read bf16 inputs: one f16 term
+        cp_async_wait<0>();
         __syncthreads();
-        for (int h = kRouterPartials / 2; h >= 32; h >>= 1) {   // s_l += s_{l+h}, h = 128, 64, 32
-            for (int it = tid; it < epc * h; it += kDecThreads) {
-                const int e = it / h, l = it % h;
-                red[e * kRouterPartials + l] = red[e * kRouterPartials + l] + red[e * kRouterPartials + l + h];
+        if (router) {
+            if (tid < kRouterPartials) {   // chain l: fmaf over i = l, l + 256, ... in increasing i
+                float acc[8];
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+                const int nchain = d / kRouterPartials;
+                for (int m = 0; m < nchain; ++m) {
+                    const int i = tid + m * kRouterPartials;
+                    const float xv = xf[i];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (e < epc) acc[e] = fmaf(xv, wsl[i * epc + e], acc[e]);
+                }
+    #pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (e < epc) red[e * kRouterPartials + tid] = acc[e];
             }
             __syncthreads();
-        }
-        if (warp < epc) {   // h = 16 .. 1 across the lanes; lane 0 ends with s_0
-            float v = red[warp * kRouterPartials + lane];
-#pragma unroll
-            for (int h = 16; h >= 1; h >>= 1) v = v + __shfl_down_sync(0xffffffffu, v, h);
-            if (lane == 0) a.ws.logits[c * epc + warp] = v;
-        }
-    }
-    grid_barrier(a.bar, G, a.ws.err);
-    pdl_trigger();   // every CTA is resident: the next kernel may be scheduled
-
-    // ---------------------------------------------------------------- R: top-k, weights, slots
-    for (int e = tid; e < E; e += kDecThreads) slog[e] = __ldcg(a.ws.logits + e);
-    // gate.up items this CTA's warps touch, and their per-warp partials [items][16 warps][32]
-    const uint32_t wc0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_g));
-    const uint32_t wc1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_g));
-    const uint32_t cu0 = split_begin(U_g, a.warps_g, wc0), cu1 = split_begin(U_g, a.warps_g, wc1);
-    const int cta_item0 = static_cast<int>(cu0 / npan_g);
-    const int cta_items = cu1 > cu0 ? static_cast<int>((cu1 - 1) / npan_g) - cta_item0 + 1 : 0;
-    float* cred = reinterpret_cast<float*>(dsm + kRingBytes + decode_region_b(d, f, k) + decode_region_c(d, a.xt));
-    for (int i = tid; i < cta_items * kDecWarps * 32; i += kDecThreads) cred[i] = 0.0f;
-    if (tid < kMaxK) {   // every slot holds a valid expert even if the logits were not finite
-        s_sel[tid] = 0;
-        s_val[tid] = 0.0f;
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += kDecThreads) {   // slot = number of experts that beat e
-        const float v = slog[e];
-        const float4* row = reinterpret_cast<const float4*>(slog);
-        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-        for (int q = 0; q < E / 4; ++q) {
-            const float4 o = row[q];
-            r0 += beats(o.x, 4 * q, v, e);
-            r1 += beats(o.y, 4 * q + 1, v, e);
-            r2 += beats(o.z, 4 * q + 2, v, e);
-            r3 += beats(o.w, 4 * q + 3, v, e);
-        }
-        const int r = r0 + r1 + r2 + r3;
-        if (r < k) {
-            s_sel[r] = e;
-            s_val[r] = v;
-        }
-    }
-    __syncthreads();
-    if (warp == 0) {   // softmax over the k selected logits (slot 0's subtracted, sum in slot order)
-        const int j = lane;
-        const bool live = j < k;
-        const int ej = live ? s_sel[j] : 0;
-        float wj = 0.0f;
-        if (live) {
-            const float m0 = s_val[0];
-            float sum = 0.0f;
-            for (int i = 0; i < k; ++i) sum += expf(s_val[i] - m0);
-            wj = expf(s_val[j] - m0) / sum;
-        }
-        int r = 0;   // sorted slot: selected experts with a lower index
-        for (int i = 0; i < k; ++i) r += s_sel[i] < ej;
-        if (live) {
-            s_e[r] = ej;
-            s_pos[j] = r;
-            s_w[j] = wj;
-            if (c == 0) {
-                a.ws.idx[j] = ej;
-                a.ws.w[j] = wj;
-                a.ws.perm[r] = j;
-                a.ws.pos[j] = r;
-                a.ws.act_e[r] = ej;
-                a.ws.slot_info[r] = make_int4(ej, r, 1, 0);
+            for (int h = kRouterPartials / 2; h >= 32; h >>= 1) {   // s_l += s_{l+h}, h = 128, 64, 32
+                for (int it = tid; it < epc * h; it += kDecThreads) {
+                    const int e = it / h, l = it % h;
+                    red[e * kRouterPartials + l] = red[e * kRouterPartials + l] + red[e * kRouterPartials + l + h];
+                }
+                __syncthreads();
+            }
+            if (warp < epc) {   // h = 16 .. 1 across the lanes; lane 0 ends with s_0
+                float v = red[warp * kRouterPartials + lane];
+    #pragma unroll
+                for (int h = 16; h >= 1; h >>= 1) v = v + __shfl_down_sync(0xffffffffu, v, h);
+                if (lane == 0) a.ws.logits[c * epc + warp] = v;
             }
         }
-    }
-    if (c == 0) {
-        for (int e = tid; e <= E; e += kDecThreads) {
-            int n = 0;
-            for (int i = 0; i < k; ++i) n += s_sel[i] < e;
-            a.ws.offsets[e] = n;
-        }
-        if (tid == 0) *a.ws.n_active = k;
-    }
-    __syncthreads();
+        grid_barrier(a.bar, ++nbar * G, a.ws.err);
+        if (l == 0) pdl_trigger();   // every CTA is resident: the next kernel may be scheduled
 
-    // ---------------------------------------------------------------- G: gate.up partial sums
-    const uint64_t pol = l2_evict_first_policy();
-    if (tid == 0 && a.pf_bytes > 0) {   // this CTA's share of the caller's L2 hint
-        const int64_t share = ((a.pf_bytes + G - 1) / G + 127) / 128 * 128;
-        const int64_t off = static_cast<int64_t>(c) * share;
-        if (off < a.pf_bytes) prefetch_l2(a.pf + off, static_cast<uint32_t>(min(share, a.pf_bytes - off)));
-    }
-    // The routed experts' down matrices, asked of L2 while gate.up streams (a hint): CTA c
-    // takes a contiguous 1/G of the k matrices' bytes, in a few large bulk requests (each
-    // bulk request costs the copy engine about the same whatever its size).
-    auto prefetch_down = [&]() {
-        if (tid != 0 || !a.prefetch_down) return;
-        const int64_t total = static_cast<int64_t>(k) * a.dn_bytes;
-        const int64_t share = ((total + G - 1) / G + 15) / 16 * 16;
-        int64_t off = static_cast<int64_t>(c) * share;
-        const int64_t end = min(total, off + share);
-        while (off < end) {
-            const int s = static_cast<int>(off / a.dn_bytes);
-            const int64_t within = off - static_cast<int64_t>(s) * a.dn_bytes;
-            const int64_t n = min(end - off, a.dn_bytes - within);
-            prefetch_l2(a.w_dn + static_cast<int64_t>(s_e[s]) * a.dn_bytes + within, static_cast<uint32_t>(n));
-            off += n;
+        // ---------------------------------------------------------------- R: top-k, weights, slots
+        for (int e = tid; e < E; e += kDecThreads) slog[e] = __ldcg(a.ws.logits + e);
+        // gate.up items this CTA's warps touch, and their per-warp partials [items][16 warps][32]
+        const uint32_t wc0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_g));
+        const uint32_t wc1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_g));
+        const uint32_t cu0 = split_begin(U_g, a.warps_g, wc0), cu1 = split_begin(U_g, a.warps_g, wc1);
+        const int cta_item0 = static_cast<int>(cu0 / npan_g);
+        const int cta_items = cu1 > cu0 ? static_cast<int>((cu1 - 1) / npan_g) - cta_item0 + 1 : 0;
+        float* cred = reinterpret_cast<float*>(dsm + kRingBytes + decode_region_b(d, f, k) + decode_region_c(d, a.xt));
+        for (int i = tid; i < cta_items * kDecWarps * 32; i += kDecThreads) cred[i] = 0.0f;
+        if (tid < kMaxK) {   // every slot holds a valid expert even if the logits were not finite
+            s_sel[tid] = 0;
+            s_val[tid] = 0.0f;
         }
-    };
-    if (rg.n > 0) {
-        const int n = rg.n;
-        unsigned char* wring = ring + warp * kStages * kSlotBytes;
-        const uint32_t ring_addr = smem_addr(wring);
-        // the issue pointer as (slot, tile, panel), advanced by increments
-        int iss_s = rg.item0 / nt_g, iss_t = rg.item0 % nt_g, iss_b = rg.b0;
-        const uint8_t* iss_w = a.w_gu + static_cast<int64_t>(s_e[iss_s]) * a.gu_bytes;
-        auto issue = [&](int st) {
-            issue_panel_block<MOE_W_Q8_0>(ring_addr + st * kSlotBytes, iss_w, 2 * f, iss_t * 16, f + iss_t * 16, iss_b,
-                                          pol, 0);
-            if (++iss_b == npan_g) {
-                iss_b = 0;
-                if (++iss_t == nt_g) {
-                    iss_t = 0;
-                    if (++iss_s < k) iss_w = a.w_gu + static_cast<int64_t>(s_e[iss_s]) * a.gu_bytes;
+        __syncthreads();
+        for (int e = tid; e < E; e += kDecThreads) {   // slot = number of experts that beat e
+            const float v = slog[e];
+            const float4* row = reinterpret_cast<const float4*>(slog);
+            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+            for (int q = 0; q < E / 4; ++q) {
+                const float4 o = row[q];
+                r0 += beats(o.x, 4 * q, v, e);
+                r1 += beats(o.y, 4 * q + 1, v, e);
+                r2 += beats(o.z, 4 * q + 2, v, e);
+                r3 += beats(o.w, 4 * q + 3, v, e);
+            }
+            const int r = r0 + r1 + r2 + r3;
+            if (r < k) {
+                s_sel[r] = e;
+                s_val[r] = v;
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {   // softmax over the k selected logits (slot 0's subtracted, sum in slot order)
+            const int j = lane;
+            const bool live = j < k;
+            const int ej = live ? s_sel[j] : 0;
+            float wj = 0.0f;
+            if (live) {
+                const float m0 = s_val[0];
+                float sum = 0.0f;
+                for (int i = 0; i < k; ++i) sum += expf(s_val[i] - m0);
+                wj = expf(s_val[j] - m0) / sum;
+            }
+            int r = 0;   // sorted slot: selected experts with a lower index
+            for (int i = 0; i < k; ++i) r += s_sel[i] < ej;
+            if (live) {
+                s_e[r] = ej;
+                s_pos[j] = r;
+                s_w[j] = wj;
+                if (c == 0 && a.idx_out) {
+                    a.idx_out[l * k + j] = ej;
+                    a.w_out[l * k + j] = wj;
+                }
+                if (c == 0) {
+                    a.ws.idx[j] = ej;
+                    a.ws.w[j] = wj;
+                    a.ws.perm[r] = j;
+                    a.ws.pos[j] = r;
+                    a.ws.act_e[r] = ej;
+                    a.ws.slot_info[r] = make_int4(ej, r, 1, 0);
+                }
+            }
+        }
+        if (c == 0) {
+            for (int e = tid; e <= E; e += kDecThreads) {
+                int n = 0;
+                for (int i = 0; i < k; ++i) n += s_sel[i] < e;
+                a.ws.offsets[e] = n;
+            }
+            if (tid == 0) *a.ws.n_active = k;
+        }
+        __syncthreads();
+
+        // ---------------------------------------------------------------- G: gate.up partial sums
+        const uint64_t pol = l2_evict_first_policy();
+        if (tid == 0 && P.pf_bytes > 0) {   // this CTA's share of the caller's L2 hint
+            const int64_t share = ((P.pf_bytes + G - 1) / G + 127) / 128 * 128;
+            const int64_t off = static_cast<int64_t>(c) * share;
+            if (off < P.pf_bytes) prefetch_l2(P.pf + off, static_cast<uint32_t>(min(share, P.pf_bytes - off)));
+        }
+        // The routed experts' down matrices, asked of L2 while gate.up streams (a hint): CTA c
+        // takes a contiguous 1/G of the k matrices' bytes, in a few large bulk requests (each
+        // bulk request costs the copy engine about the same whatever its size).
+        auto prefetch_down = [&]() {
+            if (tid != 0 || !a.prefetch_down) return;
+            const int64_t total = static_cast<int64_t>(k) * a.dn_bytes;
+            const int64_t share = ((total + G - 1) / G + 15) / 16 * 16;
+            int64_t off = static_cast<int64_t>(c) * share;
+            const int64_t end = min(total, off + share);
+            while (off < end) {
+                const int s = static_cast<int>(off / a.dn_bytes);
+                const int64_t within = off - static_cast<int64_t>(s) * a.dn_bytes;
+                const int64_t n = min(end - off, a.dn_bytes - within);
+                prefetch_l2(P.w_dn + static_cast<int64_t>(s_e[s]) * a.dn_bytes + within, static_cast<uint32_t>(n));
+                off += n;
+            }
+        };
+        if (rg.n > 0) {
+            const int n = rg.n;
+            unsigned char* wring = ring + warp * kStages * kSlotBytes;
+            const uint32_t ring_addr = smem_addr(wring);
+            // the issue pointer as (slot, tile, panel), advanced by increments
+            int iss_s = rg.item0 / nt_g, iss_t = rg.item0 % nt_g, iss_b = rg.b0;
+            const uint8_t* iss_w = P.w_gu + static_cast<int64_t>(s_e[iss_s]) * a.gu_bytes;
+            auto issue = [&](int st) {
+                issue_panel_block<MOE_W_Q8_0>(ring_addr + st * kSlotBytes, iss_w, 2 * f, iss_t * 16, f + iss_t * 16, iss_b,
+                                              pol, 0);
+                if (++iss_b == npan_g) {
+                    iss_b = 0;
+                    if (++iss_t == nt_g) {
+                        iss_t = 0;
+                        if (++iss_s < k) iss_w = P.w_gu + static_cast<int64_t>(s_e[iss_s]) * a.gu_bytes;
+                    }
+                }
+            };
+    #pragma unroll
+            for (int st = 0; st < kStages; ++st) {
+                if (st < n) issue(st);
+                cp_async_commit();
+            }
+            prefetch_down();   // after this warp's first gate.up requests
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            int cur_item = rg.item0, cur_b = rg.b0;
+            for (int i0 = 0; i0 < n; i0 += kStages) {
+    #pragma unroll
+                for (int st = 0; st < kStages; ++st) {
+                    const int i = i0 + st;
+                    if (i < n) {
+                        cp_async_wait<kStages - 1>();
+                        __syncwarp();
+                        panel_mma<MOE_W_Q8_0>(wring + st * kSlotBytes, xh, d, cur_b, 1, 0, acc, split_l, d);
+                        __syncwarp();   // every lane is done with the slot before it is refilled
+                        if (i + kStages < n) issue(st);
+                        cp_async_commit();
+                        if (++cur_b == npan_g || i == n - 1) {
+                            // this warp's share of the item, token column 0: lanes t == 0 hold rows
+                            // g and g + 8 of the gate block and of the up block
+                            if ((lane & 3) == 0) {
+                                float* rr = cred + ((cur_item - cta_item0) * kDecWarps + warp) * 32;
+                                const int g = lane >> 2;
+                                rr[g] = acc[0][0];
+                                rr[g + 8] = acc[0][2];
+                                rr[16 + g] = acc[1][0];
+                                rr[24 + g] = acc[1][2];
+                            }
+    #pragma unroll
+                            for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
+                            cur_b = 0;
+                            ++cur_item;
+                        }
+                    }
+                }
+            }
+            cp_async_wait<0>();
+        } else {
+            prefetch_down();
+        }
+        // The CTA's record of each item it touched: its warps' partials in warp order (a warp
+        // that did not touch the item adds zero), at the CTA's contributor slot of the item.
+        __syncthreads();
+        for (int i = tid; i < cta_items * 32; i += kDecThreads) {
+            const int it = i >> 5, j = i & 31;
+            float v = 0.0f;
+    #pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) v += cred[(it * kDecWarps + w) * 32 + j];
+            const uint32_t item = static_cast<uint32_t>(cta_item0 + it);
+            const int cidx = c - static_cast<int>(split_owner(U_g, a.warps_g, item * npan_g) / kDecWarps);
+            a.grec[(static_cast<int64_t>(item) * a.cov_g + cidx) * 32 + j] = v;
+        }
+        grid_barrier(a.bar, ++nbar * G, a.ws.err);
+
+        // ---------------------------------------------------------------- D ring, then H
+        // The down panel blocks do not depend on h: this warp's first ones are requested before
+        // the activations are reduced.
+        const int kf = k * f;
+        __half* hs = reinterpret_cast<__half*>(xf);   // [k][f] hi, then [k][f] lo
+        unsigned char* dring = ring + warp * kStages * kSlotBytes;
+        const uint32_t dring_addr = smem_addr(dring);
+        // the issue pointer as (slot, row tile, panel), advanced by increments: slot-major, so
+        // that a CTA's units read the activations of one or two slots only
+        int dss = rd.item0 / nrt, dsrt = rd.item0 % nrt, dsb = rd.b0;
+        const uint8_t* dsw = P.w_dn + static_cast<int64_t>(s_e[dss < k ? dss : 0]) * a.dn_bytes;
+        auto issue_d = [&](int st) {
+            issue_panel_block<MOE_W_Q8_0>(dring_addr + st * kSlotBytes, dsw, d, dsrt * 32, dsrt * 32 + 16, dsb, pol, 0);
+            if (++dsb == npan_d) {
+                dsb = 0;
+                if (++dsrt == nrt) {
+                    dsrt = 0;
+                    if (++dss < k) dsw = P.w_dn + static_cast<int64_t>(s_e[dss]) * a.dn_bytes;
                 }
             }
         };
-#pragma unroll
+    #pragma unroll
         for (int st = 0; st < kStages; ++st) {
-            if (st < n) issue(st);
+            if (st < rd.n) issue_d(st);
             cp_async_commit();
         }
-        prefetch_down();   // after this warp's first gate.up requests
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        int cur_item = rg.item0, cur_b = rg.b0;
-        for (int i0 = 0; i0 < n; i0 += kStages) {
-#pragma unroll
-            for (int st = 0; st < kStages; ++st) {
-                const int i = i0 + st;
-                if (i < n) {
-                    cp_async_wait<kStages - 1>();
-                    __syncwarp();
-                    panel_mma<MOE_W_Q8_0>(wring + st * kSlotBytes, xh, d, cur_b, 1, 0, acc, split, d);
-                    __syncwarp();   // every lane is done with the slot before it is refilled
-                    if (i + kStages < n) issue(st);
-                    cp_async_commit();
-                    if (++cur_b == npan_g || i == n - 1) {
-                        // this warp's share of the item, token column 0: lanes t == 0 hold rows
-                        // g and g + 8 of the gate block and of the up block
-                        if ((lane & 3) == 0) {
-                            float* rr = cred + ((cur_item - cta_item0) * kDecWarps + warp) * 32;
-                            const int g = lane >> 2;
-                            rr[g] = acc[0][0];
-                            rr[g + 8] = acc[0][2];
-                            rr[16 + g] = acc[1][0];
-                            rr[24 + g] = acc[1][2];
+        // H: h = SiLU(gate) * up.  Each CTA sums the records (in contributor order) of the slots
+        // its down units read, into its own f16 hi + lo copy of h, and writes them as fp32 too
+        // (every slot is read by some CTA; CTAs that share a slot write the same values).
+        int h_lo_q = 0, h_hi_q = 0;   // neurons [h_lo_q, h_hi_q) of the flattened [k][f]
+        {
+            const uint32_t w0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_d));
+            const uint32_t w1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_d));
+            const uint32_t v0 = split_begin(U_d, a.warps_d, w0), v1 = split_begin(U_d, a.warps_d, w1);
+            const uint32_t per_slot = static_cast<uint32_t>(nrt * npan_d);
+            if (v1 > v0) {
+                h_lo_q = static_cast<int>(v0 / per_slot) * f;
+                h_hi_q = (static_cast<int>((v1 - 1) / per_slot) + 1) * f;
+            }
+        }
+        int* gcov = reinterpret_cast<int*>(slog);     // CTAs that recorded each gate.up item (items_g <= 1024)
+        for (int i = tid; i < static_cast<int>(items_g); i += kDecThreads) {
+            const uint32_t u0 = static_cast<uint32_t>(i) * npan_g, u1 = u0 + npan_g - 1;
+            gcov[i] = static_cast<int>(split_owner(U_g, a.warps_g, u1) / kDecWarps -
+                                       split_owner(U_g, a.warps_g, u0) / kDecWarps) + 1;
+        }
+        __syncthreads();
+        constexpr int kHB = 4;   // neurons per thread per batch: their first two records load together
+        for (int q0 = h_lo_q + tid; q0 < h_hi_q; q0 += kHB * kDecThreads) {   // neuron q = item * 16 + j
+            float g0[kHB], g1[kHB], u0[kHB], u1[kHB];
+    #pragma unroll
+            for (int u = 0; u < kHB; ++u) {
+                const int q = q0 + u * kDecThreads;
+                g0[u] = g1[u] = u0[u] = u1[u] = 0.0f;
+                if (q < h_hi_q) {
+                    const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
+                    g0[u] = __ldcg(rec);
+                    u0[u] = __ldcg(rec + 16);
+                    if (gcov[q >> 4] > 1) {
+                        g1[u] = __ldcg(rec + 32);
+                        u1[u] = __ldcg(rec + 48);
+                    }
+                }
+            }
+    #pragma unroll
+            for (int u = 0; u < kHB; ++u) {
+                const int q = q0 + u * kDecThreads;
+                if (q < h_hi_q) {
+                    float zg = g0[u] + g1[u], zu = u0[u] + u1[u];   // records in contributor order
+                    const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
+                    for (int cc = 2; cc < gcov[q >> 4]; ++cc) {
+                        zg += __ldcg(rec + cc * 32);
+                        zu += __ldcg(rec + cc * 32 + 16);
+                    }
+                    const float h = silu(zg) * zu;
+                    const __half hi = __float2half_rn(h);
+                    hs[q] = hi;
+                    hs[kf + q] = __float2half_rn(h - __half2float(hi));
+                    a.ws.h[q] = h;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---------------------------------------------------------------- D: down partial sums
+        // A unit is one 32-neuron panel of a 32-row tile of one slot's down matrix (two 16-row
+        // MMA blocks, the gate.up panel product with h as the activations).
+        if (rd.n > 0) {
+            const int n = rd.n;
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            int cur_item = rd.item0, cur_s = rd.item0 / nrt, cur_rt = rd.item0 % nrt, cur_b = rd.b0, cur_c = rd.c0;
+            for (int i0 = 0; i0 < n; i0 += kStages) {
+    #pragma unroll
+                for (int st = 0; st < kStages; ++st) {
+                    const int i = i0 + st;
+                    if (i < n) {
+                        cp_async_wait<kStages - 1>();
+                        __syncwarp();
+                        panel_mma<MOE_W_Q8_0>(dring + st * kSlotBytes, hs + cur_s * f, f, cur_b, 1, 0, acc, true, kf);
+                        __syncwarp();   // every lane is done with the slot before it is refilled
+                        if (i + kStages < n) issue_d(st);
+                        cp_async_commit();
+                        if (++cur_b == npan_d || i == n - 1) {
+                            if ((lane & 3) == 0) {   // rows g, g + 8 of both blocks, token column 0
+                                float* rec = a.drec + (static_cast<int64_t>(cur_item) * a.cov_d + cur_c) * 32;
+                                const int g = lane >> 2;
+                                rec[g] = acc[0][0];
+                                rec[g + 8] = acc[0][2];
+                                rec[16 + g] = acc[1][0];
+                                rec[24 + g] = acc[1][2];
+                            }
+    #pragma unroll
+                            for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
+                            cur_b = 0;
+                            cur_c = 0;
+                            ++cur_item;
+                            if (++cur_rt == nrt) {
+                                cur_rt = 0;
+                                ++cur_s;
+                            }
                         }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
-                        cur_b = 0;
-                        ++cur_item;
                     }
                 }
             }
         }
         cp_async_wait<0>();
-    } else {
-        prefetch_down();
-    }
-    // The CTA's record of each item it touched: its warps' partials in warp order (a warp
-    // that did not touch the item adds zero), at the CTA's contributor slot of the item.
-    __syncthreads();
-    for (int i = tid; i < cta_items * 32; i += kDecThreads) {
-        const int it = i >> 5, j = i & 31;
-        float v = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) v += cred[(it * kDecWarps + w) * 32 + j];
-        const uint32_t item = static_cast<uint32_t>(cta_item0 + it);
-        const int cidx = c - static_cast<int>(split_owner(U_g, a.warps_g, item * npan_g) / kDecWarps);
-        a.grec[(static_cast<int64_t>(item) * a.cov_g + cidx) * 32 + j] = v;
-    }
-    grid_barrier(a.bar, 2 * G, a.ws.err);
+        grid_barrier(a.bar, ++nbar * G, a.ws.err);
+        if (l + 1 < a.n_layers) request_router(a.lp[l + 1].W);   // the ring is free until the next gate.up
 
-    // ---------------------------------------------------------------- D ring, then H
-    // The down panel blocks do not depend on h: this warp's first ones are requested before
-    // the activations are reduced.
-    const int kf = k * f;
-    __half* hs = reinterpret_cast<__half*>(xf);   // [k][f] hi, then [k][f] lo
-    unsigned char* dring = ring + warp * kStages * kSlotBytes;
-    const uint32_t dring_addr = smem_addr(dring);
-    // the issue pointer as (slot, row tile, panel), advanced by increments: slot-major, so
-    // that a CTA's units read the activations of one or two slots only
-    int dss = rd.item0 / nrt, dsrt = rd.item0 % nrt, dsb = rd.b0;
-    const uint8_t* dsw = a.w_dn + static_cast<int64_t>(s_e[dss < k ? dss : 0]) * a.dn_bytes;
-    auto issue_d = [&](int st) {
-        issue_panel_block<MOE_W_Q8_0>(dring_addr + st * kSlotBytes, dsw, d, dsrt * 32, dsrt * 32 + 16, dsb, pol, 0);
-        if (++dsb == npan_d) {
-            dsb = 0;
-            if (++dsrt == nrt) {
-                dsrt = 0;
-                if (++dss < k) dsw = a.w_dn + static_cast<int64_t>(s_e[dss]) * a.dn_bytes;
+        // ---------------------------------------------------------------- C: combine
+        // Row tile rt (32 outputs) is combined by CTA rt mod G: y of each slot (its records in
+        // contributor order), then out[r] = sum over the pairs j in order of w_j * y_{slot(j)}[r].
+        float* s_y = slog;   // [k][32] (kMaxK * 32 == kMaxE floats)
+        static_assert(kMaxK * 32 <= kMaxE, "combine buffer");
+        for (int rt = c; rt < nrt; rt += G) {
+            for (int task = tid; task < k * 32; task += kDecThreads) {
+                const int s = task >> 5, r = task & 31;
+                const uint32_t item = static_cast<uint32_t>(s * nrt + rt);
+                const int nc = item_contributors(U_d, a.warps_d, npan_d, item);
+                const float* rec = a.drec + static_cast<int64_t>(item) * a.cov_d * 32 + r;
+                float v[4];
+    #pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = q < nc ? __ldcg(rec + q * 32) : 0.0f;
+                float y = ((v[0] + v[1]) + v[2]) + v[3];   // records in contributor order
+                for (int cc = 4; cc < nc; ++cc) y += __ldcg(rec + cc * 32);
+                s_y[s * 32 + r] = y;
             }
-        }
-    };
-#pragma unroll
-    for (int st = 0; st < kStages; ++st) {
-        if (st < rd.n) issue_d(st);
-        cp_async_commit();
-    }
-    // H: h = SiLU(gate) * up.  Each CTA sums the records (in contributor order) of the slots
-    // its down units read, into its own f16 hi + lo copy of h, and writes them as fp32 too
-    // (every slot is read by some CTA; CTAs that share a slot write the same values).
-    int h_lo_q = 0, h_hi_q = 0;   // neurons [h_lo_q, h_hi_q) of the flattened [k][f]
-    {
-        const uint32_t w0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_d));
-        const uint32_t w1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_d));
-        const uint32_t v0 = split_begin(U_d, a.warps_d, w0), v1 = split_begin(U_d, a.warps_d, w1);
-        const uint32_t per_slot = static_cast<uint32_t>(nrt * npan_d);
-        if (v1 > v0) {
-            h_lo_q = static_cast<int>(v0 / per_slot) * f;
-            h_hi_q = (static_cast<int>((v1 - 1) / per_slot) + 1) * f;
-        }
-    }
-    int* gcov = reinterpret_cast<int*>(slog);     // CTAs that recorded each gate.up item (items_g <= 1024)
-    for (int i = tid; i < static_cast<int>(items_g); i += kDecThreads) {
-        const uint32_t u0 = static_cast<uint32_t>(i) * npan_g, u1 = u0 + npan_g - 1;
-        gcov[i] = static_cast<int>(split_owner(U_g, a.warps_g, u1) / kDecWarps -
-                                   split_owner(U_g, a.warps_g, u0) / kDecWarps) + 1;
-    }
-    __syncthreads();
-    constexpr int kHB = 4;   // neurons per thread per batch: their first two records load together
-    for (int q0 = h_lo_q + tid; q0 < h_hi_q; q0 += kHB * kDecThreads) {   // neuron q = item * 16 + j
-        float g0[kHB], g1[kHB], u0[kHB], u1[kHB];
-#pragma unroll
-        for (int u = 0; u < kHB; ++u) {
-            const int q = q0 + u * kDecThreads;
-            g0[u] = g1[u] = u0[u] = u1[u] = 0.0f;
-            if (q < h_hi_q) {
-                const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
-                g0[u] = __ldcg(rec);
-                u0[u] = __ldcg(rec + 16);
-                if (gcov[q >> 4] > 1) {
-                    g1[u] = __ldcg(rec + 32);
-                    u1[u] = __ldcg(rec + 48);
-                }
+            __syncthreads();
+            if (tid < 32) {
+                float o = 0.0f;
+                for (int j = 0; j < k; ++j) o = fmaf(s_w[j], s_y[s_pos[j] * 32 + tid], o);
+                a.out[static_cast<int64_t>(l) * d + rt * 32 + tid] = o;
             }
+            __syncthreads();
         }
-#pragma unroll
-        for (int u = 0; u < kHB; ++u) {
-            const int q = q0 + u * kDecThreads;
-            if (q < h_hi_q) {
-                float zg = g0[u] + g1[u], zu = u0[u] + u1[u];   // records in contributor order
-                const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
-                for (int cc = 2; cc < gcov[q >> 4]; ++cc) {
-                    zg += __ldcg(rec + cc * 32);
-                    zu += __ldcg(rec + cc * 32 + 16);
-                }
-                const float h = silu(zg) * zu;
-                const __half hi = __float2half_rn(h);
-                hs[q] = hi;
-                hs[kf + q] = __float2half_rn(h - __half2float(hi));
-                a.ws.h[q] = h;
-            }
-        }
-    }
-    __syncthreads();
 
-    // ---------------------------------------------------------------- D: down partial sums
-    // A unit is one 32-neuron panel of a 32-row tile of one slot's down matrix (two 16-row
-    // MMA blocks, the gate.up panel product with h as the activations).
-    if (rd.n > 0) {
-        const int n = rd.n;
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        int cur_item = rd.item0, cur_s = rd.item0 / nrt, cur_rt = rd.item0 % nrt, cur_b = rd.b0, cur_c = rd.c0;
-        for (int i0 = 0; i0 < n; i0 += kStages) {
-#pragma unroll
-            for (int st = 0; st < kStages; ++st) {
-                const int i = i0 + st;
-                if (i < n) {
-                    cp_async_wait<kStages - 1>();
-                    __syncwarp();
-                    panel_mma<MOE_W_Q8_0>(dring + st * kSlotBytes, hs + cur_s * f, f, cur_b, 1, 0, acc, true, kf);
-                    __syncwarp();   // every lane is done with the slot before it is refilled
-                    if (i + kStages < n) issue_d(st);
-                    cp_async_commit();
-                    if (++cur_b == npan_d || i == n - 1) {
-                        if ((lane & 3) == 0) {   // rows g, g + 8 of both blocks, token column 0
-                            float* rec = a.drec + (static_cast<int64_t>(cur_item) * a.cov_d + cur_c) * 32;
-                            const int g = lane >> 2;
-                            rec[g] = acc[0][0];
-                            rec[g + 8] = acc[0][2];
-                            rec[16 + g] = acc[1][0];
-                            rec[24 + g] = acc[1][2];
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
-                        cur_b = 0;
-                        cur_c = 0;
-                        ++cur_item;
-                        if (++cur_rt == nrt) {
-                            cur_rt = 0;
-                            ++cur_s;
-                        }
-                    }
+        // ---------------------------------------------------------------- N: the next layer's input
+        // x_{l+1} = bf16(out_l / sqrt(mean(out_l^2) + eps)), the sum of squares in the order of the
+        // stand-alone RMS-norm kernel (threads t < 256 take elements t, t + 256, ...; warp sums;
+        // the 8 warp sums in order), so a stack equals its layers glued by that kernel bitwise.
+        if (l + 1 < a.n_layers || a.x_next) {
+            grid_barrier(a.bar, ++nbar * G, a.ws.err);
+            const float* ol = a.out + static_cast<int64_t>(l) * d;
+            float* wsum = slog;
+            if (tid < 256) {
+                float ss = 0.0f;
+                for (int i = tid; i < 32 * 256; i += 256) {
+                    const float v = i < d ? __ldcg(ol + i) : 0.0f;
+                    ss = fmaf(v, v, ss);
                 }
+                ss = warp_sum(ss);
+                if (lane == 0) wsum[warp] = ss;
             }
+            __syncthreads();
+            float tot = 0.0f;
+    #pragma unroll
+            for (int i = 0; i < 8; ++i) tot += wsum[i];
+            const float inv = rsqrtf(tot / static_cast<float>(d) + a.eps);
+            for (int i = tid; i < d; i += kDecThreads) {
+                const __nv_bfloat16 xb = __float2bfloat16_rn(__ldcg(ol + i) * inv);
+                const float xv = __bfloat162float(xb);
+                xf[i] = xv;
+                xh[i] = __float2half_rn(xv);
+                if (c == 0 && a.x_next) a.x_next[static_cast<int64_t>(l) * d + i] = __bfloat16_as_ushort(xb);
+            }
+            __syncthreads();   // (slog is read again by the next layer's selection)
         }
-    }
-    cp_async_wait<0>();
-    grid_barrier(a.bar, 3 * G, a.ws.err);
-
-    // ---------------------------------------------------------------- C: combine
-    // Row tile rt (32 outputs) is combined by CTA rt mod G: y of each slot (its records in
-    // contributor order), then out[r] = sum over the pairs j in order of w_j * y_{slot(j)}[r].
-    float* s_y = slog;   // [k][32] (kMaxK * 32 == kMaxE floats)
-    static_assert(kMaxK * 32 <= kMaxE, "combine buffer");
-    for (int rt = c; rt < nrt; rt += G) {
-        for (int task = tid; task < k * 32; task += kDecThreads) {
-            const int s = task >> 5, r = task & 31;
-            const uint32_t item = static_cast<uint32_t>(s * nrt + rt);
-            const int nc = item_contributors(U_d, a.warps_d, npan_d, item);
-            const float* rec = a.drec + static_cast<int64_t>(item) * a.cov_d * 32 + r;
-            float v[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = q < nc ? __ldcg(rec + q * 32) : 0.0f;
-            float y = ((v[0] + v[1]) + v[2]) + v[3];   // records in contributor order
-            for (int cc = 4; cc < nc; ++cc) y += __ldcg(rec + cc * 32);
-            s_y[s * 32 + r] = y;
-        }
-        __syncthreads();
-        if (tid < 32) {
-            float o = 0.0f;
-            for (int j = 0; j < k; ++j) o = fmaf(s_w[j], s_y[s_pos[j] * 32 + tid], o);
-            a.out[rt * 32 + tid] = o;
-        }
-        __syncthreads();
     }
     // The last CTA to finish resets the barrier counters for the next call (every CTA has
     // passed all three barriers by now).

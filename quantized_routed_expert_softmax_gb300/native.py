@@ -26,7 +26,7 @@ PATH = {"auto": 0, "gemv": 1, "gemm": 2}
 EXPORTS = ["moe_q8_0_bytes", "moe_nvfp4_bytes", "moe_quantize_q8_0", "moe_pack_nvfp4", "moe_router_workspace_bytes",
            "moe_router_topk", "moe_layer_workspace_bytes", "moe_layer_forward", "moe_rmsnorm_bf16",
            "moe_get_device_status", "moe_status_string", "moe_abi_version", "moe_layer_forward_launches",
-           "moe_layer_forward_noalloc"]
+           "moe_layer_forward_noalloc", "moe_stack_forward", "moe_stack_forward_launches"]
 
 
 class MoeError(RuntimeError):
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
             "moe_abi_version": (I32, []),
             "moe_layer_forward_launches": (I32, [ctypes.POINTER(LayerDesc), I64, I32]),
             "moe_layer_forward_noalloc": (I32, [ctypes.POINTER(LayerDesc), P, I32, I64, P, P, P, P]),
+            "moe_stack_forward": (I32, [ctypes.POINTER(LayerDesc), I32, P, I32, ctypes.c_float, P, P, P, P, P, SZ, P]),
+            "moe_stack_forward_launches": (I32, [ctypes.POINTER(LayerDesc), I32, I32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -271,3 +273,47 @@ class MoELayer:
         code = ctypes.c_int32(0)
         lib().moe_get_device_status(_ptr(self._ws), _stream(stream), ctypes.byref(code))
         return int(code.value)
+
+
+class MoEStack:
+    """Layers of one shape called as a stack for one token (moe_stack_forward): each layer's
+    input is the RMS-normalised (bf16) output of the previous one."""
+
+    def __init__(self, layers, eps: float = 1e-6):
+        self.layers = list(layers)
+        self.eps = eps
+        self.descs = (LayerDesc * len(self.layers))(*[l.desc for l in self.layers])
+        self._ws = None
+
+    def refresh(self) -> None:
+        """Copy the layers' descriptors again (after set_path / set_l2_prefetch)."""
+        self.descs = (LayerDesc * len(self.layers))(*[l.desc for l in self.layers])
+
+    def workspace(self):
+        import torch
+        if self._ws is None:
+            self._ws = torch.zeros(self.layers[0].workspace_bytes(1), dtype=torch.uint8,
+                                   device=self.layers[0].router_w.device)
+        return self._ws
+
+    def launches(self, with_x_next: bool = False) -> int:
+        return int(lib().moe_stack_forward_launches(self.descs, len(self.layers), int(with_x_next)))
+
+    def forward(self, x, outs=None, x_next=None, routing: dict | None = None, workspace=None, stream=None):
+        """x: [1, d] fp32 or bf16 on the device.  Returns outs fp32 [n_layers, d]; x_next
+        (bf16 [n_layers, d]) and routing (dict with idx int32 / w fp32 [n_layers, k]) are
+        filled when given."""
+        import torch
+        n, l0 = len(self.layers), self.layers[0]
+        if outs is None:
+            outs = torch.empty((n, l0.d), dtype=torch.float32, device=x.device)
+        idx = w = None
+        if routing is not None:
+            idx = torch.empty((n, l0.k), dtype=torch.int32, device=x.device)
+            w = torch.empty((n, l0.k), dtype=torch.float32, device=x.device)
+            routing.update(idx=idx, w=w)
+        ws = workspace if workspace is not None else self.workspace()
+        _check("moe_stack_forward",
+               lib().moe_stack_forward(self.descs, n, _ptr(x), _x_dtype(x), ctypes.c_float(self.eps), _ptr(outs),
+                                       _ptr(x_next), _ptr(idx), _ptr(w), _ptr(ws), ws.numel(), _stream(stream)))
+        return outs

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.moe_abi_version() == 10100
+    assert L.moe_abi_version() == 10200
     for s in range(8):
         assert L.moe_status_string(s).decode().startswith(native.STATUS_NAMES[s])
 
@@ -124,3 +124,20 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "from oracle" not in text, fn
                 assert "moe_oracle" not in text and "liboracle" not in text, fn
+
+
+def test_stack_validation(L):
+    two = (native.LayerDesc * 2)(_desc(), _desc())
+    mixed = (native.LayerDesc * 2)(_desc(), _desc(f=256))
+    need1 = L.moe_layer_workspace_bytes(ctypes.byref(_desc()), 1)
+    eps = ctypes.c_float(1e-6)
+    def call(descs, n, x=FAKE, xt=0, outs=FAKE, idx=None, w=None, ws=FAKE, nbytes=need1):
+        return L.moe_stack_forward(descs, n, x or None, xt, eps, outs, None, idx, w, ws or None, nbytes, None)
+    assert call(two, 0) == 1                       # no layers
+    assert call(mixed, 2) == 2                     # layers of different shapes
+    assert call(two, 2, x=0) == 1                  # NULL x
+    assert call(two, 2, idx=FAKE) == 1             # idx without w
+    assert call(two, 2, xt=3) == 1                 # bad dtype
+    assert call(two, 2, x=FAKE + 2) == 3           # misaligned x
+    assert call(two, 2, ws=0) == 4                 # no workspace
+    assert call(two, 2, nbytes=need1 - 1) == 4     # workspace too small

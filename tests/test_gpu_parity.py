@@ -397,3 +397,57 @@ def test_zipf_routing_full_size(name, T):
     w = synth.WORKLOADS[name]
     idx, wts = synth.zipf_routing(T, w.E, w.k)
     _full_case(name, T, sample=[0, 17, T - 1], idx_in=idx, w_in=wts)
+
+
+# ------------------------------------------------------------------ a stack of layers, one token
+# moe_stack_forward: x_{l+1} = bf16(RMSNorm(out_l)).  On Q8_0 SwiGLU layers the whole stack is
+# one kernel; it must equal the layers called one by one with moe_rmsnorm_bf16 between them bit
+# for bit (the same arithmetic per layer, the same reduction order in the norm), and every layer
+# must match the oracle on the input that layer consumed.  path GEMV takes the layer-by-layer
+# fallback inside the library.
+STACKS = {
+    "k8_e64_bf16": (synth.Workload("st_k8", d=1024, f=192, E=64, k=8, act="swiglu", wfmt="q8_0", x_dtype="bf16",
+                                   layers=4), 4),
+    "tiny_f32_input": (synth.WORKLOADS["tiny"], 3),
+}
+
+
+@pytest.mark.parametrize("name", list(STACKS))
+@pytest.mark.parametrize("path", ["auto", "gemv"])
+def test_stack_one_token(name, path):
+    w, n = STACKS[name]
+    layers_ = [layers.build_layer(w, layer=l, source="numpy", path=path) for l in range(n)]
+    stack = native.MoEStack(layers_)
+    if path == "auto":
+        assert stack.launches(True) == 1
+    else:   # each layer's own launches, then the norm
+        assert stack.launches(True) == n * (layers_[0].launches(1) + 1)
+    x0 = torch.from_numpy(synth.tokens(w, 1, tag="stack")).cuda()
+    if w.x_dtype == "bf16":
+        x0 = x0.view(torch.bfloat16)
+    xn = torch.full((n, w.d), 0, dtype=torch.bfloat16, device="cuda")
+    outs = torch.full((n, w.d), float("nan"), device="cuda")
+    routing = {}
+    stack.forward(x0, outs=outs, x_next=xn, routing=routing)
+    # layer by layer through the single-layer calls and the stand-alone norm
+    x = x0
+    for l, L in enumerate(layers_):
+        tr = {}
+        o = L.forward(x, trace=tr)
+        assert np.array_equal(o.cpu().numpy().view(np.uint32), outs[l:l + 1].cpu().numpy().view(np.uint32)), l
+        assert np.array_equal(tr["idx"].cpu().numpy(), routing["idx"][l:l + 1].cpu().numpy())
+        assert np.array_equal(tr["w"].cpu().numpy().view(np.uint32), routing["w"][l:l + 1].cpu().numpy().view(np.uint32))
+        x = native.rmsnorm_bf16(o)
+        assert torch.equal(x.view(torch.int16), xn[l:l + 1].view(torch.int16)), l
+    # each layer against the oracle on its own input
+    for l in range(n):
+        xl = x0 if l == 0 else xn[l - 1:l]
+        xs = to_numpy_x(xl)
+        ol = oracle_layer(w, synth.router_weight(w, l), lambda e: synth.expert_weights(w, l, e)[0],
+                          lambda e: synth.expert_weights(w, l, e)[1], range(w.E))
+        ref = ol.forward(xs)
+        assert np.array_equal(routing["idx"][l:l + 1].cpu().numpy(), ref["idx"])
+        assert_close(outs[l:l + 1].cpu().numpy(), ref["out"])
+    # run to run: bitwise identical
+    outs2 = stack.forward(x0)
+    assert torch.equal(outs.view(torch.int32), outs2.view(torch.int32))
