@@ -205,17 +205,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         if (router) {
             if (tid < kRouterPartials) {   // chain l: fmaf over i = l, l + 256, ... in increasing i
                 float acc[8];
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
                 const int nchain = d / kRouterPartials;
                 for (int m = 0; m < nchain; ++m) {
                     const int i = tid + m * kRouterPartials;
                     const float xv = xf[i];
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 8; ++e)
                         if (e < epc) acc[e] = fmaf(xv, wsl[i * epc + e], acc[e]);
                 }
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 8; ++e)
                     if (e < epc) red[e * kRouterPartials + tid] = acc[e];
             }
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             }
             if (warp < epc) {   // h = 16 .. 1 across the lanes; lane 0 ends with s_0
                 float v = red[warp * kRouterPartials + lane];
-    #pragma unroll
+#pragma unroll
                 for (int h = 16; h >= 1; h >>= 1) v = v + __shfl_down_sync(0xffffffffu, v, h);
                 if (lane == 0) a.ws.logits[c * epc + warp] = v;
             }
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                     }
                 }
             };
-    #pragma unroll
+#pragma unroll
             for (int st = 0; st < kStages; ++st) {
                 if (st < n) issue(st);
                 cp_async_commit();
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             int cur_item = rg.item0, cur_b = rg.b0;
             for (int i0 = 0; i0 < n; i0 += kStages) {
-    #pragma unroll
+#pragma unroll 1   // rolled: the kernel's code stays small (no faster unrolled on GB300)
                 for (int st = 0; st < kStages; ++st) {
                     const int i = i0 + st;
                     if (i < n) {
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                                 rr[16 + g] = acc[1][0];
                                 rr[24 + g] = acc[1][2];
                             }
-    #pragma unroll
+#pragma unroll
                             for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
                             cur_b = 0;
                             ++cur_item;
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         for (int i = tid; i < cta_items * 32; i += kDecThreads) {
             const int it = i >> 5, j = i & 31;
             float v = 0.0f;
-    #pragma unroll
+#pragma unroll
             for (int w = 0; w < kDecWarps; ++w) v += cred[(it * kDecWarps + w) * 32 + j];
             const uint32_t item = static_cast<uint32_t>(cta_item0 + it);
             const int cidx = c - static_cast<int>(split_owner(U_g, a.warps_g, item * npan_g) / kDecWarps);
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 }
             }
         };
-    #pragma unroll
+#pragma unroll
         for (int st = 0; st < kStages; ++st) {
             if (st < rd.n) issue_d(st);
             cp_async_commit();
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         constexpr int kHB = 4;   // neurons per thread per batch: their first two records load together
         for (int q0 = h_lo_q + tid; q0 < h_hi_q; q0 += kHB * kDecThreads) {   // neuron q = item * 16 + j
             float g0[kHB], g1[kHB], u0[kHB], u1[kHB];
-    #pragma unroll
+#pragma unroll
             for (int u = 0; u < kHB; ++u) {
                 const int q = q0 + u * kDecThreads;
                 g0[u] = g1[u] = u0[u] = u1[u] = 0.0f;
@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                     }
                 }
             }
-    #pragma unroll
+#pragma unroll
             for (int u = 0; u < kHB; ++u) {
                 const int q = q0 + u * kDecThreads;
                 if (q < h_hi_q) {
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             int cur_item = rd.item0, cur_s = rd.item0 / nrt, cur_rt = rd.item0 % nrt, cur_b = rd.b0, cur_c = rd.c0;
             for (int i0 = 0; i0 < n; i0 += kStages) {
-    #pragma unroll
+#pragma unroll 1   // rolled: the kernel's code stays small (no faster unrolled on GB300)
                 for (int st = 0; st < kStages; ++st) {
                     const int i = i0 + st;
                     if (i < n) {
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                                 rec[16 + g] = acc[1][0];
                                 rec[24 + g] = acc[1][2];
                             }
-    #pragma unroll
+#pragma unroll
                             for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
                             cur_b = 0;
                             cur_c = 0;
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 const int nc = item_contributors(U_d, a.warps_d, npan_d, item);
                 const float* rec = a.drec + static_cast<int64_t>(item) * a.cov_d * 32 + r;
                 float v[4];
-    #pragma unroll
+#pragma unroll
                 for (int q = 0; q < 4; ++q) v[q] = q < nc ? __ldcg(rec + q * 32) : 0.0f;
                 float y = ((v[0] + v[1]) + v[2]) + v[3];   // records in contributor order
                 for (int cc = 4; cc < nc; ++cc) y += __ldcg(rec + cc * 32);
@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             }
             __syncthreads();
             float tot = 0.0f;
-    #pragma unroll
+#pragma unroll
             for (int i = 0; i < 8; ++i) tot += wsum[i];
             const float inv = rsqrtf(tot / static_cast<float>(d) + a.eps);
             for (int i = tid; i < d; i += kDecThreads) {
