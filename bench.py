@@ -560,23 +560,22 @@ def active_expert_bytes(stack, inputs, T, w):
             "layer_per_launch": int(statistics.mean(layer_bytes))}
 
 
-def kernel_source_sha():
+def kernel_source_sha(files=("gemv.cu", "gemm.cu", "common.cuh", "decode.cu", "gemv_core.cuh")):
     import hashlib
     csrc = os.path.join(ROOT, "quantized_routed_expert_softmax_gb300", "csrc")
-    blob = b"".join(open(os.path.join(csrc, f), "rb").read()
-                    for f in ("gemv.cu", "gemm.cu", "common.cuh", "decode.cu", "gemv_core.cuh"))
+    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in files)
     return hashlib.sha1(blob).hexdigest()[:12]
 
 
 def measured_traffic(workload, T):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, when it
-    was taken on this kernel source (the expert and decode kernels) and workload; else None."""
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, while the
+    kernel's own source files (the entry's "sources") are unchanged since the capture; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         entry = json.load(open(p)).get(f"{workload}_T{T}")
     except (OSError, ValueError):
         return None
-    if not entry or entry.get("source_sha1_12") != kernel_source_sha():
+    if not entry or entry.get("source_sha1_12") != kernel_source_sha(tuple(entry.get("sources", ()))):
         return None
     return entry.get("bytes")
 
