@@ -30,9 +30,10 @@ cudaError_t launch_expert_gemm(const ExpertArgs&, int, int, int, int, int, int, 
 cudaError_t launch_gather_x_f16(const ExpertArgs&, int, cudaStream_t);
 cudaError_t configure_decode_kernel(int, int);
 int decode_ctas(int);
-size_t decode_smem_bytes(int, int, int, int, int);
+size_t decode_smem_plan(int, int, int, int, int, int, int, int*, int*, int*);
+size_t decode_ring_bytes();
 size_t decode_max_smem();
-cudaError_t launch_decode_layer(const DecodeArgs&, int, cudaStream_t);
+cudaError_t launch_decode_layer(const DecodeArgs&, int, size_t, int, cudaStream_t);
 
 
 namespace {
@@ -103,42 +104,69 @@ int decode_epc(int64_t E, int ctas) {
 // U_d = d/32 * k * f/32 down units evenly over the warps of `ctas` CTAs (16 each).
 struct DecodeSplit {
     int64_t U_g, U_d, warps_g, warps_d;
+    int64_t npan_g, npan_d;  // panels per gate.up item, units per down item
     int64_t cov_g;       // CTAs whose ranges can touch one gate.up item (records per item)
-    int64_t cov_d;       // warps whose ranges can touch one down item
+    int64_t cov_d;       // Q8_0: warps, NVFP4: CTAs whose ranges can touch one down item
     int64_t cta_items;   // gate.up items one CTA's range can touch
+    int64_t cta_items_d; // NVFP4: down items one CTA's range can touch
+    int64_t cta_slots;   // NVFP4: slots whose activations one CTA's down units read
+    int64_t items_d;     // down items
+    int64_t rec_d;       // floats per down record (32 rows, or 256 rows for NVFP4)
 };
 
+// The most items of npan units that one CTA's range (16 warps of an even split of U over W)
+// touches.
+int64_t cta_max_items(int64_t U, int64_t W, int64_t npan) {
+    int64_t m = 0;
+    for (int64_t c = 0; 16 * c < W; ++c) {
+        const int64_t w0 = 16 * c, w1 = std::min(16 * c + 16, W);
+        const int64_t u0 = w0 * U / W, u1 = w1 * U / W;
+        if (u1 > u0) m = std::max(m, (u1 - 1) / npan - u0 / npan + 1);
+    }
+    return m;
+}
+
+// Q8_0 SwiGLU: gate.up units (slot, 16-neuron tile, 32-column panel), down units (slot,
+// 32-row tile, 32-neuron panel).  NVFP4 ReLU^2: gate.up units (slot, 32-neuron tile,
+// 64-column panel), down units (slot, 256-row tile, 16-neuron group).
 DecodeSplit decode_split(const moe_layer_desc* d, int64_t ctas) {
     DecodeSplit sp{};
-    const int64_t npan_g = d->d / 32, npan_d = d->f / 32;
-    sp.U_g = static_cast<int64_t>(d->k) * (d->f / 16) * npan_g;
-    sp.U_d = (d->d / 32) * d->k * npan_d;
+    const bool q8 = d->wfmt == MOE_W_Q8_0;
+    sp.npan_g = q8 ? d->d / 32 : d->d / 64;
+    sp.npan_d = q8 ? d->f / 32 : d->f / 16;
+    const int64_t items_g = static_cast<int64_t>(d->k) * (q8 ? d->f / 16 : d->f / 32);
+    sp.items_d = static_cast<int64_t>(d->k) * (q8 ? d->d / 32 : d->d / 256);
+    sp.rec_d = q8 ? 32 : 256;
+    sp.U_g = items_g * sp.npan_g;
+    sp.U_d = sp.items_d * sp.npan_d;
     sp.warps_g = std::min<int64_t>(16 * ctas, sp.U_g);
     sp.warps_d = std::min<int64_t>(16 * ctas, sp.U_d);
-    // a range of at least Lmin units meets at most ceil((npan - 2) / Lmin) + 2 of them
+    // a range of at least Lmin units meets at most ceil(npan / Lmin) + 1 items; +2 for margin
     const int64_t lcta = std::max<int64_t>(1, sp.U_g / ((sp.warps_g + 15) / 16));   // units per CTA, at least
-    sp.cov_g = (npan_g + lcta - 1) / lcta + 2;
-    const int64_t lwd = std::max<int64_t>(1, sp.U_d / sp.warps_d);
-    sp.cov_d = (npan_d + lwd - 1) / lwd + 2;
-    // the most gate.up items one CTA's range touches (exact, from the same split)
-    sp.cta_items = 0;
-    for (int64_t c = 0; 16 * c < sp.warps_g; ++c) {
-        const int64_t w0 = 16 * c, w1 = std::min(16 * c + 16, sp.warps_g);
-        const int64_t u0 = w0 * sp.U_g / sp.warps_g, u1 = w1 * sp.U_g / sp.warps_g;
-        if (u1 > u0) sp.cta_items = std::max(sp.cta_items, (u1 - 1) / npan_g - u0 / npan_g + 1);
-    }
+    sp.cov_g = (sp.npan_g + lcta - 1) / lcta + 2;
+    const int64_t lwd = std::max<int64_t>(1, q8 ? sp.U_d / sp.warps_d : sp.U_d / ((sp.warps_d + 15) / 16));
+    sp.cov_d = (sp.npan_d + lwd - 1) / lwd + 2;
+    sp.cta_items = cta_max_items(sp.U_g, sp.warps_g, sp.npan_g);
+    sp.cta_items_d = q8 ? 0 : cta_max_items(sp.U_d, sp.warps_d, sp.npan_d);
+    sp.cta_slots = q8 ? 0 : cta_max_items(sp.U_d, sp.warps_d, sp.npan_d * (d->d / 256));
     return sp;
 }
 
-// The one-kernel decode layer's shape limits (any device): one token, Q8_0 SwiGLU, the
-// router-weight slice of a routing CTA, the staged rows and the CTA's gate.up partials within
-// its shared memory, and 32-bit unit arithmetic.
+// The one-kernel decode layer's shape limits (any device): one token, Q8_0 SwiGLU or NVFP4
+// ReLU^2, the router-weight slice of a routing CTA and x within its shared memory, and 32-bit
+// unit arithmetic.
 bool decode_shape_ok(const moe_layer_desc* d, int64_t T, int xt) {
-    if (T != 1 || d->wfmt != MOE_W_Q8_0 || d->act != MOE_ACT_SWIGLU || d->path != MOE_PATH_AUTO) return false;
-    if (d->d > 8192 || d->k * d->f > 16384 || d->f % 16 != 0) return false;
-    if (decode_smem_bytes(static_cast<int>(d->d), static_cast<int>(d->f), d->k, xt, 1) > decode_max_smem()) return false;
+    if (T != 1 || d->path != MOE_PATH_AUTO) return false;
+    const bool q8 = d->wfmt == MOE_W_Q8_0 && d->act == MOE_ACT_SWIGLU;
+    const bool nv = d->wfmt == MOE_W_NVFP4 && d->act == MOE_ACT_RELU2;
+    if (!q8 && !nv) return false;
+    if (d->d > 8192 || d->f % 32 != 0) return false;
+    if (q8 && d->k * d->f > 16384) return false;   // h of every slot in shared memory
+    if (decode_smem_plan(d->wfmt, static_cast<int>(d->d), static_cast<int>(d->f), d->k, xt, 1, 1, nullptr, nullptr,
+                         nullptr) > decode_max_smem())
+        return false;
     const int epc = decode_epc(d->E, kMaxDecodeCtas);
-    if (epc == 0 || d->d * epc * 4 + epc * 1024 > 16 * 6 * 1152) return false;
+    if (epc == 0 || static_cast<size_t>(d->d * epc * 4 + epc * 1024) > decode_ring_bytes()) return false;
     const DecodeSplit sp = decode_split(d, kMaxDecodeCtas);   // the most warps: the largest products
     return (sp.U_g + 1) * sp.warps_g < (int64_t(1) << 32) && (sp.U_d + 1) * sp.warps_d < (int64_t(1) << 32);
 }
@@ -146,8 +174,18 @@ bool decode_shape_ok(const moe_layer_desc* d, int64_t T, int xt) {
 // With `ctas` CTAs on this device: the kernel's shared memory, including the per-warp
 // gate.up partials of one CTA's items, within what the kernel is configured for.
 bool decode_split_fits(const moe_layer_desc* d, const DecodeSplit& sp, int xt) {
-    return decode_smem_bytes(static_cast<int>(d->d), static_cast<int>(d->f), d->k, xt,
-                             static_cast<int>(sp.cta_items)) <= decode_max_smem();
+    if (decode_smem_plan(d->wfmt, static_cast<int>(d->d), static_cast<int>(d->f), d->k, xt,
+                         static_cast<int>(sp.cta_items), static_cast<int>(sp.cta_slots), nullptr, nullptr,
+                         nullptr) > decode_max_smem())
+        return false;
+    if (d->wfmt == MOE_W_NVFP4) {
+        // the down partials of the CTA's items fit the ring; its slots' group flags fit 1024 words
+        if (static_cast<size_t>(sp.cta_items_d) * 16 * 256 * sizeof(float) > decode_ring_bytes()) return false;
+        if (sp.cta_slots * (d->f / 16) > 1024) return false;
+    } else if (static_cast<int64_t>(d->k) * (d->f / 16) > 1024) {
+        return false;   // contributor counts of the gate.up items fit 1024 words
+    }
+    return true;
 }
 
 // The GEMM path tiles rows by 128 (SwiGLU gate.up: 64 neurons' gate and up rows) and K by 64.
@@ -193,7 +231,7 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
 
 struct Layout {
     size_t err, route_ctr, n_active, row_ctr, logits, rpart, idx, w, offsets, perm, pos, act_e, slot_info, chunk_cnt,
-        local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, dec_bar, dec_grec, dec_drec, xnext, total;
+        local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, dec_bar, dec_sel, dec_grec, dec_drec, xnext, total;
 };
 
 // Workspace regions for T tokens (each 256-byte aligned).  The control words (err,
@@ -238,8 +276,9 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     // (sized for the most CTAs any device can give the kernel: more CTAs, more records per item)
     const DecodeSplit sp = decode_split(d, kMaxDecodeCtas);
     L.dec_bar = take(dec ? sizeof(int32_t) * 2 : 0);
-    L.dec_grec = take(dec ? sizeof(float) * 32 * d->k * (d->f / 16) * sp.cov_g : 0);
-    L.dec_drec = take(dec ? sizeof(float) * 32 * (d->d / 32) * d->k * sp.cov_d : 0);
+    L.dec_sel = take(dec ? sizeof(int32_t) * 2 * kMaxK : 0);
+    L.dec_grec = take(dec ? sizeof(float) * 32 * (sp.U_g / sp.npan_g) * sp.cov_g : 0);
+    L.dec_drec = take(dec ? sizeof(float) * sp.rec_d * sp.items_d * sp.cov_d : 0);
     L.xnext = take(T == 1 ? sizeof(uint16_t) * d->d : 0);   // a stack's next input (one token)
     L.total = off;
     return L;
@@ -294,7 +333,7 @@ moe_status validate_desc(const moe_layer_desc* d) {
 // The one-kernel decode arguments for n layers of descs[0]'s shape (pointers per layer), on
 // the current device; false when the device or the shape cannot run it.
 bool fill_decode_args(const moe_layer_desc* descs, int n, const void* x, int xt, void* workspace, const Layout& L,
-                      const Workspace& ws, DecodeArgs* a, int* ctas_out) {
+                      const Workspace& ws, DecodeArgs* a, int* ctas_out, size_t* smem_out) {
     const moe_layer_desc* desc = descs;
     const Plan p = make_plan(desc, 1, xt);
     if (!p.decode1 || n < 1 || n > kMaxStackLayers) return false;
@@ -313,15 +352,26 @@ bool fill_decode_args(const moe_layer_desc* descs, int n, const void* x, int xt,
     a->E = static_cast<int>(desc->E);
     a->k = desc->k;
     a->epc = epc;
-    a->prefetch_down = p.prefetch_down ? 1 : 0;
+    // the routed experts' whole down matrices into L2 (Q8_0: every byte is read; NVFP4 reads
+    // only the active groups, so a whole-matrix prefetch would fetch bytes that are skipped)
+    a->prefetch_down = (p.prefetch_down && desc->wfmt == MOE_W_Q8_0) ? 1 : 0;
     // warps that share each phase's panel range: all of them, or one per unit
     a->warps_g = static_cast<int>(sp.warps_g);
     a->warps_d = static_cast<int>(sp.warps_d);
     a->cov_g = static_cast<int>(sp.cov_g);
     a->cov_d = static_cast<int>(sp.cov_d);
     a->cta_items = static_cast<int>(sp.cta_items);
-    a->gu_bytes = static_cast<int64_t>(moe_q8_0_bytes(2 * desc->f, desc->d));
-    a->dn_bytes = static_cast<int64_t>(moe_q8_0_bytes(desc->d, desc->f));
+    a->cta_items_d = static_cast<int>(sp.cta_items_d);
+    const int64_t rows_gu = desc->act == MOE_ACT_SWIGLU ? 2 * desc->f : desc->f;
+    if (desc->wfmt == MOE_W_Q8_0) {
+        a->gu_bytes = static_cast<int64_t>(moe_q8_0_bytes(rows_gu, desc->d));
+        a->dn_bytes = static_cast<int64_t>(moe_q8_0_bytes(desc->d, desc->f));
+    } else {
+        a->gu_bytes = static_cast<int64_t>(moe_nvfp4_bytes(rows_gu, desc->d));
+        a->dn_bytes = static_cast<int64_t>(moe_nvfp4_bytes(desc->d, desc->f));
+    }
+    *smem_out = decode_smem_plan(desc->wfmt, a->d, a->f, a->k, xt, a->cta_items, static_cast<int>(sp.cta_slots),
+                                 &a->off_b, &a->off_c, &a->off_p);
     a->n_layers = n;
     for (int l = 0; l < n; ++l) {
         a->lp[l].W = descs[l].router_w;
@@ -329,9 +379,13 @@ bool fill_decode_args(const moe_layer_desc* descs, int n, const void* x, int xt,
         a->lp[l].w_dn = static_cast<const uint8_t*>(descs[l].w_down);
         a->lp[l].pf = static_cast<const uint8_t*>(descs[l].l2_prefetch);
         a->lp[l].pf_bytes = descs[l].l2_prefetch ? (descs[l].l2_prefetch_bytes & ~static_cast<int64_t>(15)) : 0;
+        a->lp[l].gu_ts = descs[l].gate_up_tscale;
+        a->lp[l].dn_ts = descs[l].down_tscale;
     }
     a->ws = ws;
     a->bar = reinterpret_cast<int32_t*>(base + L.dec_bar);
+    a->sel = reinterpret_cast<int32_t*>(base + L.dec_sel);
+    a->selv = reinterpret_cast<float*>(base + L.dec_sel + sizeof(int32_t) * kMaxK);
     a->grec = reinterpret_cast<float*>(base + L.dec_grec);
     a->drec = reinterpret_cast<float*>(base + L.dec_drec);
     *ctas_out = ctas;
@@ -491,9 +545,10 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     if (p.decode1 && !idx_in) {
         DecodeArgs a{};
         int ctas = 0;
-        if (fill_decode_args(desc, 1, x, xt, workspace, L, ws, &a, &ctas)) {
+        size_t smem = 0;
+        if (fill_decode_args(desc, 1, x, xt, workspace, L, ws, &a, &ctas, &smem)) {
             a.out = out;
-            e = launch_decode_layer(a, ctas, s);
+            e = launch_decode_layer(a, desc->wfmt, smem, ctas, s);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
             for (int i = 1; i <= 4; ++i) mark(i);   // one kernel: the inner boundaries coincide
             if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -629,13 +684,14 @@ moe_status moe_stack_forward(const moe_layer_desc* descs, int32_t n_layers, cons
     {
         DecodeArgs a{};
         int ctas = 0;
-        if (fill_decode_args(descs, n_layers, x, xt, workspace, L, bind(workspace, L), &a, &ctas)) {
+        size_t smem = 0;
+        if (fill_decode_args(descs, n_layers, x, xt, workspace, L, bind(workspace, L), &a, &ctas, &smem)) {
             a.out = outs;
             a.eps = eps;
             a.x_next = x_next;
             a.idx_out = idx;
             a.w_out = w;
-            return cuda_status(launch_decode_layer(a, ctas, s));
+            return cuda_status(launch_decode_layer(a, descs->wfmt, smem, ctas, s));
         }
     }
     // otherwise layer by layer, the RMS-norm glue between them

@@ -85,6 +85,8 @@ struct DecodeLayerPtrs {
     const uint8_t* w_dn;         // down matrices
     const uint8_t* pf;           // L2 hint (the next layer's router weights), or null
     int64_t pf_bytes;
+    const float* gu_ts;          // NVFP4 tensor scales [E] of the gate/up and down matrices
+    const float* dn_ts;
 };
 
 struct DecodeArgs {
@@ -96,6 +98,8 @@ struct DecodeArgs {
     int warps_g, warps_d;        // warps that share the gate.up / down panel ranges
     int cov_g, cov_d;            // partial records per item at most (CTAs / warps that can share one item)
     int cta_items;               // gate.up items one CTA's range touches at most
+    int cta_items_d;             // NVFP4: down items (slot, 256-row tile) one CTA's range touches at most
+    int off_b, off_c, off_p;     // dynamic shared memory: x fp32 / h, x f16, gate.up partials (bytes)
     int64_t gu_bytes, dn_bytes;  // bytes of one expert's gate/up and down matrices
     int n_layers;                // 1: moe_layer_forward; more: moe_stack_forward
     float eps;                   // RMS-norm between stacked layers
@@ -105,8 +109,11 @@ struct DecodeArgs {
     float* w_out;                // [n_layers][k]
     Workspace ws;
     int32_t* bar;                // [2] grid-barrier arrivals, CTAs finished (zero between calls)
+    int32_t* sel;                // [k] experts selected by rank (more than 256 experts)
+    float* selv;                 // [k] their logits
     float* grec;                 // [k * f/16][cov_g][32] gate.up partial sums per item and contributor
-    float* drec;                 // [k * d/32][cov_d][32] down partial sums per item and contributor
+    float* drec;                 // [k * d/32][cov_d][32] (Q8_0) or [k * d/256][cov_d][256] (NVFP4) down
+                                 //   partial sums per item and contributor
     DecodeLayerPtrs lp[kMaxStackLayers];
 };
 

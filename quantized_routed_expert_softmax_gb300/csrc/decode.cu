@@ -49,6 +49,7 @@ constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDevErrTimeout = 2;
 constexpr long long kWaitLimitNs = 1000000000ll;   // bounded waits: one second
 constexpr size_t kRingBytes = static_cast<size_t>(kDecWarps) * kStages * kSlotBytes;
+constexpr int kLocalRankMaxE = 256;   // up to this many experts every CTA ranks all logits itself
 
 __device__ __forceinline__ long long globaltimer() {
     long long t;
@@ -115,25 +116,35 @@ __device__ __forceinline__ WarpRange warp_range(uint32_t U, uint32_t W, uint32_t
 
 }  // namespace
 
-// Shared-memory plan (dynamic): [ring | B | C | P]
-//   ring : per-warp rings of panel blocks (16 x 6 x 1152 B), gate.up then down; during
-//          routing, the CTA's router-weight slice [d][epc] and the tree buffer [epc][256]
-//   B    : x as fp32 [d] (routing), then h of the k slots as f16 hi [k][f] + lo [k][f] (down)
+// Shared-memory plan (dynamic): [ring | B | C | P], offsets computed on the host
+//   ring : per-warp rings of panel blocks (16 x 6 x 1152 B), gate.up then down (Q8_0); during
+//          routing, the CTA's router-weight slice [d][epc] and the tree buffer [epc][256];
+//          NVFP4 down: the CTA's per-warp partials [items][16 warps][256]
+//   B    : x as fp32 [d] (routing), then h: Q8_0 f16 hi [k][f] + lo [k][f], NVFP4 fp32 for the
+//          CTA's slots [slots][f]
 //   C    : x as f16 hi [d] (+ lo [d] for fp32 inputs) (gate.up)
 //   P    : the per-warp gate.up partials of the CTA's items [cta_items][16 warps][32]
-__host__ __device__ size_t decode_region_b(int d, int f, int k) {
-    const size_t xb = static_cast<size_t>(d) * 4, hb = static_cast<size_t>(k) * f * 4;
-    return xb > hb ? xb : hb;
+size_t decode_smem_plan(int wfmt, int d, int f, int k, int xt, int cta_items, int cta_slots, int* off_b, int* off_c,
+                        int* off_p) {
+    const size_t xb = static_cast<size_t>(d) * 4;
+    const size_t hb = (wfmt == MOE_W_Q8_0) ? static_cast<size_t>(k) * f * 4 : static_cast<size_t>(cta_slots) * f * 4;
+    const size_t b = xb > hb ? xb : hb;
+    const size_t cbytes = static_cast<size_t>(d) * 2 * (xt == MOE_F32 ? 2 : 1);
+    const size_t pb = static_cast<size_t>(cta_items) * kDecWarps * 32 * sizeof(float);
+    if (off_b) *off_b = static_cast<int>(kRingBytes);
+    if (off_c) *off_c = static_cast<int>(kRingBytes + b);
+    if (off_p) *off_p = static_cast<int>(kRingBytes + b + cbytes);
+    return kRingBytes + b + cbytes + pb;
 }
 
-__host__ __device__ size_t decode_region_c(int d, int xt) { return static_cast<size_t>(d) * 2 * (xt == MOE_F32 ? 2 : 1); }
+size_t decode_ring_bytes() { return kRingBytes; }
 
-size_t decode_smem_bytes(int d, int f, int k, int xt, int cta_items) {
-    return kRingBytes + decode_region_b(d, f, k) + decode_region_c(d, xt) +
-           static_cast<size_t>(cta_items) * kDecWarps * 32 * sizeof(float);
-}
-
+template <int FMT, int ACT>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs a) {
+    // Q8_0 with SwiGLU, or NVFP4 with ReLU^2 (gateless latent experts)
+    constexpr bool kQ8 = FMT == MOE_W_Q8_0;
+    constexpr bool kSwiglu = ACT == MOE_ACT_SWIGLU;
+    constexpr int kNeur = kSwiglu ? 16 : 32;   // neurons per gate.up item (16 gate + 16 up rows, or 32 rows)
     extern __shared__ __align__(16) unsigned char dsm[];
     __shared__ __align__(16) float slog[kMaxE];   // logits; later the contributor counts of the gate.up items
     __shared__ int s_sel[kMaxK];     // expert of selection slot j (larger logit first)
@@ -141,17 +152,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     __shared__ int s_e[kMaxK];       // expert of sorted slot s (increasing expert index)
     __shared__ int s_pos[kMaxK];     // sorted slot of pair j
     __shared__ float s_w[kMaxK];     // combine weight of pair j
+    __shared__ int s_cnt[kDecWarps]; // per-warp counts (ranking over many experts)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
     const int d = a.d, f = a.f, E = a.E, k = a.k;
     const uint32_t gw = static_cast<uint32_t>(c * kDecWarps + warp);   // warp index in the grid
     unsigned char* ring = dsm;
-    float* xf = reinterpret_cast<float*>(dsm + kRingBytes);
-    __half* xh = reinterpret_cast<__half*>(dsm + kRingBytes + decode_region_b(d, f, k));
+    float* xf = reinterpret_cast<float*>(dsm + a.off_b);
+    __half* xh = reinterpret_cast<__half*>(dsm + a.off_c);
     const bool split = a.xt == MOE_F32;
     // the two streaming phases: items, panels per item, units
-    const int nt_g = f / 16, npan_g = d / 32, npan_d = f / 32;
-    const int nrt = d / 32;   // 32-row tiles of the down projection
+    // gate.up: items (slot, tile of kNeur neurons), panels of 32 (Q8_0) or 64 (NVFP4) columns
+    const int nt_g = f / kNeur, npan_g = kQ8 ? d / 32 : d / 64;
+    // down: Q8_0 items (slot, 32-row tile), units 32-neuron panels; NVFP4 items (slot, 256-row
+    // tile), units 16-neuron groups of the neuron-contiguous layout
+    const int npan_d = kQ8 ? f / 32 : f / 16;
+    const int nrt = kQ8 ? d / 32 : d / 256;
     const uint32_t items_g = static_cast<uint32_t>(k * nt_g), items_d = static_cast<uint32_t>(nrt * k);
     const uint32_t U_g = items_g * npan_g, U_d = items_d * npan_d;
     // shape-only bookkeeping, done before waiting for the previous kernel
@@ -238,35 +254,69 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         if (l == 0) pdl_trigger();   // every CTA is resident: the next kernel may be scheduled
 
         // ---------------------------------------------------------------- R: top-k, weights, slots
-        for (int e = tid; e < E; e += kDecThreads) slog[e] = __ldcg(a.ws.logits + e);
+        // Up to 256 experts every CTA ranks all the logits itself.  With more, the O(E^2)
+        // comparisons would cost a CTA microseconds: each routing CTA ranks only its own
+        // experts among all E logits and publishes the winners, and after one more grid barrier
+        // every CTA reads the k winners.
+        const bool wide = E > kLocalRankMaxE;
+        if (!wide || router)
+            for (int e = tid; e < E; e += kDecThreads) slog[e] = __ldcg(a.ws.logits + e);
         // gate.up items this CTA's warps touch, and their per-warp partials [items][16 warps][32]
         const uint32_t wc0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_g));
         const uint32_t wc1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_g));
         const uint32_t cu0 = split_begin(U_g, a.warps_g, wc0), cu1 = split_begin(U_g, a.warps_g, wc1);
         const int cta_item0 = static_cast<int>(cu0 / npan_g);
         const int cta_items = cu1 > cu0 ? static_cast<int>((cu1 - 1) / npan_g) - cta_item0 + 1 : 0;
-        float* cred = reinterpret_cast<float*>(dsm + kRingBytes + decode_region_b(d, f, k) + decode_region_c(d, a.xt));
+        float* cred = reinterpret_cast<float*>(dsm + a.off_p);
         for (int i = tid; i < cta_items * kDecWarps * 32; i += kDecThreads) cred[i] = 0.0f;
         if (tid < kMaxK) {   // every slot holds a valid expert even if the logits were not finite
             s_sel[tid] = 0;
             s_val[tid] = 0.0f;
         }
         __syncthreads();
-        for (int e = tid; e < E; e += kDecThreads) {   // slot = number of experts that beat e
-            const float v = slog[e];
-            const float4* row = reinterpret_cast<const float4*>(slog);
-            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-            for (int q = 0; q < E / 4; ++q) {
-                const float4 o = row[q];
-                r0 += beats(o.x, 4 * q, v, e);
-                r1 += beats(o.y, 4 * q + 1, v, e);
-                r2 += beats(o.z, 4 * q + 2, v, e);
-                r3 += beats(o.w, 4 * q + 3, v, e);
+        if (!wide) {
+            for (int e = tid; e < E; e += kDecThreads) {   // slot = number of experts that beat e
+                const float v = slog[e];
+                const float4* row = reinterpret_cast<const float4*>(slog);
+                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+                for (int q = 0; q < E / 4; ++q) {
+                    const float4 o = row[q];
+                    r0 += beats(o.x, 4 * q, v, e);
+                    r1 += beats(o.y, 4 * q + 1, v, e);
+                    r2 += beats(o.z, 4 * q + 2, v, e);
+                    r3 += beats(o.w, 4 * q + 3, v, e);
+                }
+                const int r = r0 + r1 + r2 + r3;
+                if (r < k) {
+                    s_sel[r] = e;
+                    s_val[r] = v;
+                }
             }
-            const int r = r0 + r1 + r2 + r3;
-            if (r < k) {
-                s_sel[r] = e;
-                s_val[r] = v;
+        } else {
+            if (router) {   // tpx threads per own expert, each counting over a share of the E logits
+                const int tpx = kDecThreads / epc;
+                const int j = tid / tpx, part = tid % tpx;
+                const int e = c * epc + j;
+                const float v = slog[e];
+                int r = 0;
+                for (int o = part * E / tpx; o < (part + 1) * E / tpx; ++o) r += beats(slog[o], o, v, e);
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
+                if (lane == 0) s_cnt[warp] = r;
+                __syncthreads();
+                if (part == 0) {
+                    int rank = 0;
+                    for (int w = j * tpx / 32; w < (j + 1) * tpx / 32; ++w) rank += s_cnt[w];
+                    if (rank < k) {
+                        a.sel[rank] = e;
+                        a.selv[rank] = v;
+                    }
+                }
+            }
+            grid_barrier(a.bar, ++nbar * G, a.ws.err);
+            if (tid < k) {
+                s_sel[tid] = __ldcg(a.sel + tid);
+                s_val[tid] = __ldcg(a.selv + tid);
             }
         }
         __syncthreads();
@@ -343,8 +393,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             int iss_s = rg.item0 / nt_g, iss_t = rg.item0 % nt_g, iss_b = rg.b0;
             const uint8_t* iss_w = P.w_gu + static_cast<int64_t>(s_e[iss_s]) * a.gu_bytes;
             auto issue = [&](int st) {
-                issue_panel_block<MOE_W_Q8_0>(ring_addr + st * kSlotBytes, iss_w, 2 * f, iss_t * 16, f + iss_t * 16, iss_b,
-                                              pol, 0);
+                // SwiGLU: gate rows t*16.. and up rows f + t*16..; ReLU^2: rows t*32.. and t*32 + 16..
+                const int rA = iss_t * (kSwiglu ? 16 : 32), rB = kSwiglu ? f + iss_t * 16 : iss_t * 32 + 16;
+                issue_panel_block<FMT>(ring_addr + st * kSlotBytes, iss_w, kSwiglu ? 2 * f : f, rA, rB, iss_b, pol, 0);
                 if (++iss_b == npan_g) {
                     iss_b = 0;
                     if (++iss_t == nt_g) {
@@ -368,13 +419,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                     if (i < n) {
                         cp_async_wait<kStages - 1>();
                         __syncwarp();
-                        panel_mma<MOE_W_Q8_0>(wring + st * kSlotBytes, xh, d, cur_b, 1, 0, acc, split_l, d);
+                        panel_mma<FMT>(wring + st * kSlotBytes, xh, d, cur_b, 1, 0, acc, split_l, d);
                         __syncwarp();   // every lane is done with the slot before it is refilled
                         if (i + kStages < n) issue(st);
                         cp_async_commit();
                         if (++cur_b == npan_g || i == n - 1) {
                             // this warp's share of the item, token column 0: lanes t == 0 hold rows
-                            // g and g + 8 of the gate block and of the up block
+                            // g and g + 8 of blocks A and B (gate and up, or the tile's two halves)
                             if ((lane & 3) == 0) {
                                 float* rr = cred + ((cur_item - cta_item0) * kDecWarps + warp) * 32;
                                 const int g = lane >> 2;
@@ -409,162 +460,347 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         }
         grid_barrier(a.bar, ++nbar * G, a.ws.err);
 
-        // ---------------------------------------------------------------- D ring, then H
-        // The down panel blocks do not depend on h: this warp's first ones are requested before
-        // the activations are reduced.
-        const int kf = k * f;
-        __half* hs = reinterpret_cast<__half*>(xf);   // [k][f] hi, then [k][f] lo
-        unsigned char* dring = ring + warp * kStages * kSlotBytes;
-        const uint32_t dring_addr = smem_addr(dring);
-        // the issue pointer as (slot, row tile, panel), advanced by increments: slot-major, so
-        // that a CTA's units read the activations of one or two slots only
-        int dss = rd.item0 / nrt, dsrt = rd.item0 % nrt, dsb = rd.b0;
-        const uint8_t* dsw = P.w_dn + static_cast<int64_t>(s_e[dss < k ? dss : 0]) * a.dn_bytes;
-        auto issue_d = [&](int st) {
-            issue_panel_block<MOE_W_Q8_0>(dring_addr + st * kSlotBytes, dsw, d, dsrt * 32, dsrt * 32 + 16, dsb, pol, 0);
-            if (++dsb == npan_d) {
-                dsb = 0;
-                if (++dsrt == nrt) {
-                    dsrt = 0;
-                    if (++dss < k) dsw = P.w_dn + static_cast<int64_t>(s_e[dss]) * a.dn_bytes;
+        if constexpr (kQ8) {
+            // ---------------------------------------------------------------- D ring, then H
+            // The down panel blocks do not depend on h: this warp's first ones are requested before
+            // the activations are reduced.
+            const int kf = k * f;
+            __half* hs = reinterpret_cast<__half*>(xf);   // [k][f] hi, then [k][f] lo
+            unsigned char* dring = ring + warp * kStages * kSlotBytes;
+            const uint32_t dring_addr = smem_addr(dring);
+            // the issue pointer as (slot, row tile, panel), advanced by increments: slot-major, so
+            // that a CTA's units read the activations of one or two slots only
+            int dss = rd.item0 / nrt, dsrt = rd.item0 % nrt, dsb = rd.b0;
+            const uint8_t* dsw = P.w_dn + static_cast<int64_t>(s_e[dss < k ? dss : 0]) * a.dn_bytes;
+            auto issue_d = [&](int st) {
+                issue_panel_block<MOE_W_Q8_0>(dring_addr + st * kSlotBytes, dsw, d, dsrt * 32, dsrt * 32 + 16, dsb, pol, 0);
+                if (++dsb == npan_d) {
+                    dsb = 0;
+                    if (++dsrt == nrt) {
+                        dsrt = 0;
+                        if (++dss < k) dsw = P.w_dn + static_cast<int64_t>(s_e[dss]) * a.dn_bytes;
+                    }
+                }
+            };
+#pragma unroll
+            for (int st = 0; st < kStages; ++st) {
+                if (st < rd.n) issue_d(st);
+                cp_async_commit();
+            }
+            // H: h = SiLU(gate) * up.  Each CTA sums the records (in contributor order) of the slots
+            // its down units read, into its own f16 hi + lo copy of h, and writes them as fp32 too
+            // (every slot is read by some CTA; CTAs that share a slot write the same values).
+            int h_lo_q = 0, h_hi_q = 0;   // neurons [h_lo_q, h_hi_q) of the flattened [k][f]
+            {
+                const uint32_t w0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_d));
+                const uint32_t w1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_d));
+                const uint32_t v0 = split_begin(U_d, a.warps_d, w0), v1 = split_begin(U_d, a.warps_d, w1);
+                const uint32_t per_slot = static_cast<uint32_t>(nrt * npan_d);
+                if (v1 > v0) {
+                    h_lo_q = static_cast<int>(v0 / per_slot) * f;
+                    h_hi_q = (static_cast<int>((v1 - 1) / per_slot) + 1) * f;
                 }
             }
-        };
-#pragma unroll
-        for (int st = 0; st < kStages; ++st) {
-            if (st < rd.n) issue_d(st);
-            cp_async_commit();
-        }
-        // H: h = SiLU(gate) * up.  Each CTA sums the records (in contributor order) of the slots
-        // its down units read, into its own f16 hi + lo copy of h, and writes them as fp32 too
-        // (every slot is read by some CTA; CTAs that share a slot write the same values).
-        int h_lo_q = 0, h_hi_q = 0;   // neurons [h_lo_q, h_hi_q) of the flattened [k][f]
-        {
-            const uint32_t w0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_d));
-            const uint32_t w1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_d));
-            const uint32_t v0 = split_begin(U_d, a.warps_d, w0), v1 = split_begin(U_d, a.warps_d, w1);
-            const uint32_t per_slot = static_cast<uint32_t>(nrt * npan_d);
-            if (v1 > v0) {
-                h_lo_q = static_cast<int>(v0 / per_slot) * f;
-                h_hi_q = (static_cast<int>((v1 - 1) / per_slot) + 1) * f;
+            int* gcov = reinterpret_cast<int*>(slog);     // CTAs that recorded each gate.up item (items_g <= 1024)
+            for (int i = tid; i < static_cast<int>(items_g); i += kDecThreads) {
+                const uint32_t u0 = static_cast<uint32_t>(i) * npan_g, u1 = u0 + npan_g - 1;
+                gcov[i] = static_cast<int>(split_owner(U_g, a.warps_g, u1) / kDecWarps -
+                                           split_owner(U_g, a.warps_g, u0) / kDecWarps) + 1;
             }
-        }
-        int* gcov = reinterpret_cast<int*>(slog);     // CTAs that recorded each gate.up item (items_g <= 1024)
-        for (int i = tid; i < static_cast<int>(items_g); i += kDecThreads) {
-            const uint32_t u0 = static_cast<uint32_t>(i) * npan_g, u1 = u0 + npan_g - 1;
-            gcov[i] = static_cast<int>(split_owner(U_g, a.warps_g, u1) / kDecWarps -
-                                       split_owner(U_g, a.warps_g, u0) / kDecWarps) + 1;
-        }
-        __syncthreads();
-        constexpr int kHB = 4;   // neurons per thread per batch: their first two records load together
-        for (int q0 = h_lo_q + tid; q0 < h_hi_q; q0 += kHB * kDecThreads) {   // neuron q = item * 16 + j
-            float g0[kHB], g1[kHB], u0[kHB], u1[kHB];
+            __syncthreads();
+            constexpr int kHB = 4;   // neurons per thread per batch: their first two records load together
+            for (int q0 = h_lo_q + tid; q0 < h_hi_q; q0 += kHB * kDecThreads) {   // neuron q = item * 16 + j
+                float g0[kHB], g1[kHB], u0[kHB], u1[kHB];
 #pragma unroll
-            for (int u = 0; u < kHB; ++u) {
-                const int q = q0 + u * kDecThreads;
-                g0[u] = g1[u] = u0[u] = u1[u] = 0.0f;
-                if (q < h_hi_q) {
-                    const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
-                    g0[u] = __ldcg(rec);
-                    u0[u] = __ldcg(rec + 16);
-                    if (gcov[q >> 4] > 1) {
-                        g1[u] = __ldcg(rec + 32);
-                        u1[u] = __ldcg(rec + 48);
+                for (int u = 0; u < kHB; ++u) {
+                    const int q = q0 + u * kDecThreads;
+                    g0[u] = g1[u] = u0[u] = u1[u] = 0.0f;
+                    if (q < h_hi_q) {
+                        const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
+                        g0[u] = __ldcg(rec);
+                        u0[u] = __ldcg(rec + 16);
+                        if (gcov[q >> 4] > 1) {
+                            g1[u] = __ldcg(rec + 32);
+                            u1[u] = __ldcg(rec + 48);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kHB; ++u) {
+                    const int q = q0 + u * kDecThreads;
+                    if (q < h_hi_q) {
+                        float zg = g0[u] + g1[u], zu = u0[u] + u1[u];   // records in contributor order
+                        const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
+                        for (int cc = 2; cc < gcov[q >> 4]; ++cc) {
+                            zg += __ldcg(rec + cc * 32);
+                            zu += __ldcg(rec + cc * 32 + 16);
+                        }
+                        const float h = silu(zg) * zu;
+                        const __half hi = __float2half_rn(h);
+                        hs[q] = hi;
+                        hs[kf + q] = __float2half_rn(h - __half2float(hi));
+                        a.ws.h[q] = h;
                     }
                 }
             }
-#pragma unroll
-            for (int u = 0; u < kHB; ++u) {
-                const int q = q0 + u * kDecThreads;
-                if (q < h_hi_q) {
-                    float zg = g0[u] + g1[u], zu = u0[u] + u1[u];   // records in contributor order
-                    const float* rec = a.grec + static_cast<int64_t>(q >> 4) * a.cov_g * 32 + (q & 15);
-                    for (int cc = 2; cc < gcov[q >> 4]; ++cc) {
-                        zg += __ldcg(rec + cc * 32);
-                        zu += __ldcg(rec + cc * 32 + 16);
-                    }
-                    const float h = silu(zg) * zu;
-                    const __half hi = __float2half_rn(h);
-                    hs[q] = hi;
-                    hs[kf + q] = __float2half_rn(h - __half2float(hi));
-                    a.ws.h[q] = h;
-                }
-            }
-        }
-        __syncthreads();
+            __syncthreads();
 
-        // ---------------------------------------------------------------- D: down partial sums
-        // A unit is one 32-neuron panel of a 32-row tile of one slot's down matrix (two 16-row
-        // MMA blocks, the gate.up panel product with h as the activations).
-        if (rd.n > 0) {
-            const int n = rd.n;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            int cur_item = rd.item0, cur_s = rd.item0 / nrt, cur_rt = rd.item0 % nrt, cur_b = rd.b0, cur_c = rd.c0;
-            for (int i0 = 0; i0 < n; i0 += kStages) {
+            // ---------------------------------------------------------------- D: down partial sums
+            // A unit is one 32-neuron panel of a 32-row tile of one slot's down matrix (two 16-row
+            // MMA blocks, the gate.up panel product with h as the activations).
+            if (rd.n > 0) {
+                const int n = rd.n;
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                int cur_item = rd.item0, cur_s = rd.item0 / nrt, cur_rt = rd.item0 % nrt, cur_b = rd.b0, cur_c = rd.c0;
+                for (int i0 = 0; i0 < n; i0 += kStages) {
 #pragma unroll 1   // rolled: the kernel's code stays small (no faster unrolled on GB300)
-                for (int st = 0; st < kStages; ++st) {
-                    const int i = i0 + st;
-                    if (i < n) {
-                        cp_async_wait<kStages - 1>();
-                        __syncwarp();
-                        panel_mma<MOE_W_Q8_0>(dring + st * kSlotBytes, hs + cur_s * f, f, cur_b, 1, 0, acc, true, kf);
-                        __syncwarp();   // every lane is done with the slot before it is refilled
-                        if (i + kStages < n) issue_d(st);
-                        cp_async_commit();
-                        if (++cur_b == npan_d || i == n - 1) {
-                            if ((lane & 3) == 0) {   // rows g, g + 8 of both blocks, token column 0
-                                float* rec = a.drec + (static_cast<int64_t>(cur_item) * a.cov_d + cur_c) * 32;
-                                const int g = lane >> 2;
-                                rec[g] = acc[0][0];
-                                rec[g + 8] = acc[0][2];
-                                rec[16 + g] = acc[1][0];
-                                rec[24 + g] = acc[1][2];
-                            }
+                    for (int st = 0; st < kStages; ++st) {
+                        const int i = i0 + st;
+                        if (i < n) {
+                            cp_async_wait<kStages - 1>();
+                            __syncwarp();
+                            panel_mma<MOE_W_Q8_0>(dring + st * kSlotBytes, hs + cur_s * f, f, cur_b, 1, 0, acc, true, kf);
+                            __syncwarp();   // every lane is done with the slot before it is refilled
+                            if (i + kStages < n) issue_d(st);
+                            cp_async_commit();
+                            if (++cur_b == npan_d || i == n - 1) {
+                                if ((lane & 3) == 0) {   // rows g, g + 8 of both blocks, token column 0
+                                    float* rec = a.drec + (static_cast<int64_t>(cur_item) * a.cov_d + cur_c) * 32;
+                                    const int g = lane >> 2;
+                                    rec[g] = acc[0][0];
+                                    rec[g + 8] = acc[0][2];
+                                    rec[16 + g] = acc[1][0];
+                                    rec[24 + g] = acc[1][2];
+                                }
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
-                            cur_b = 0;
-                            cur_c = 0;
-                            ++cur_item;
-                            if (++cur_rt == nrt) {
-                                cur_rt = 0;
-                                ++cur_s;
+                                for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.0f;
+                                cur_b = 0;
+                                cur_c = 0;
+                                ++cur_item;
+                                if (++cur_rt == nrt) {
+                                    cur_rt = 0;
+                                    ++cur_s;
+                                }
                             }
                         }
                     }
                 }
             }
-        }
-        cp_async_wait<0>();
-        grid_barrier(a.bar, ++nbar * G, a.ws.err);
-        if (l + 1 < a.n_layers) request_router(a.lp[l + 1].W);   // the ring is free until the next gate.up
+            cp_async_wait<0>();
+            grid_barrier(a.bar, ++nbar * G, a.ws.err);
+            if (l + 1 < a.n_layers) request_router(a.lp[l + 1].W);   // the ring is free until the next gate.up
 
-        // ---------------------------------------------------------------- C: combine
-        // Row tile rt (32 outputs) is combined by CTA rt mod G: y of each slot (its records in
-        // contributor order), then out[r] = sum over the pairs j in order of w_j * y_{slot(j)}[r].
-        float* s_y = slog;   // [k][32] (kMaxK * 32 == kMaxE floats)
-        static_assert(kMaxK * 32 <= kMaxE, "combine buffer");
-        for (int rt = c; rt < nrt; rt += G) {
-            for (int task = tid; task < k * 32; task += kDecThreads) {
-                const int s = task >> 5, r = task & 31;
-                const uint32_t item = static_cast<uint32_t>(s * nrt + rt);
-                const int nc = item_contributors(U_d, a.warps_d, npan_d, item);
-                const float* rec = a.drec + static_cast<int64_t>(item) * a.cov_d * 32 + r;
-                float v[4];
+            // ---------------------------------------------------------------- C: combine
+            // Row tile rt (32 outputs) is combined by CTA rt mod G: y of each slot (its records in
+            // contributor order), then out[r] = sum over the pairs j in order of w_j * y_{slot(j)}[r].
+            float* s_y = slog;   // [k][32] (kMaxK * 32 == kMaxE floats)
+            static_assert(kMaxK * 32 <= kMaxE, "combine buffer");
+            for (int rt = c; rt < nrt; rt += G) {
+                for (int task = tid; task < k * 32; task += kDecThreads) {
+                    const int s = task >> 5, r = task & 31;
+                    const uint32_t item = static_cast<uint32_t>(s * nrt + rt);
+                    const int nc = item_contributors(U_d, a.warps_d, npan_d, item);
+                    const float* rec = a.drec + static_cast<int64_t>(item) * a.cov_d * 32 + r;
+                    float v[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) v[q] = q < nc ? __ldcg(rec + q * 32) : 0.0f;
-                float y = ((v[0] + v[1]) + v[2]) + v[3];   // records in contributor order
-                for (int cc = 4; cc < nc; ++cc) y += __ldcg(rec + cc * 32);
-                s_y[s * 32 + r] = y;
+                    for (int q = 0; q < 4; ++q) v[q] = q < nc ? __ldcg(rec + q * 32) : 0.0f;
+                    float y = ((v[0] + v[1]) + v[2]) + v[3];   // records in contributor order
+                    for (int cc = 4; cc < nc; ++cc) y += __ldcg(rec + cc * 32);
+                    s_y[s * 32 + r] = y;
+                }
+                __syncthreads();
+                if (tid < 32) {
+                    float o = 0.0f;
+                    for (int j = 0; j < k; ++j) o = fmaf(s_w[j], s_y[s_pos[j] * 32 + tid], o);
+                    a.out[static_cast<int64_t>(l) * d + rt * 32 + tid] = o;
+                }
+                __syncthreads();
+            }
+        } else {
+            // ------------------------------------------------------------ H (NVFP4, ReLU^2)
+            // h = max(z * ts, 0)^2 for the slots this CTA's down units read (fp32, in region B),
+            // the records of each item summed in contributor order; then which 16-neuron groups
+            // hold a non-zero h (the only ones the down projection reads).
+            float* hf = xf;                                   // [cta slots][f]
+            int* gact = reinterpret_cast<int*>(slog);         // [cta slots][f/16] active flags
+            float* dred = reinterpret_cast<float*>(ring);     // [cta items][16 warps][256] down partials
+            const uint32_t dw0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_d));
+            const uint32_t dw1 = min(static_cast<uint32_t>(c * kDecWarps + kDecWarps), static_cast<uint32_t>(a.warps_d));
+            const uint32_t dv0 = split_begin(U_d, a.warps_d, dw0), dv1 = split_begin(U_d, a.warps_d, dw1);
+            const uint32_t per_slot = static_cast<uint32_t>(nrt * npan_d);
+            const int h_s0 = static_cast<int>(dv0 / per_slot);
+            const int h_ns = dv1 > dv0 ? static_cast<int>((dv1 - 1) / per_slot) - h_s0 + 1 : 0;
+            const int d_item0 = static_cast<int>(dv0 / npan_d);
+            const int d_items = dv1 > dv0 ? static_cast<int>((dv1 - 1) / npan_d) - d_item0 + 1 : 0;
+            for (int i = tid; i < d_items * kDecWarps * 256; i += kDecThreads) dred[i] = 0.0f;
+            constexpr int kHB = 8;   // neurons per thread per batch: their first two records load together
+            const int hn = h_ns * f;
+            for (int q0 = tid; q0 < hn; q0 += kHB * kDecThreads) {
+                float v0[kHB], v1[kHB];
+                int ncs[kHB];
+#pragma unroll
+                for (int u = 0; u < kHB; ++u) {
+                    const int q = q0 + u * kDecThreads;
+                    v0[u] = v1[u] = 0.0f;
+                    ncs[u] = 0;
+                    if (q < hn) {
+                        const int qq = h_s0 * f + q;          // neuron of the flattened [k][f]
+                        const uint32_t item = static_cast<uint32_t>(qq >> 5);
+                        ncs[u] = static_cast<int>(split_owner(U_g, a.warps_g, (item + 1) * npan_g - 1) / kDecWarps -
+                                                  split_owner(U_g, a.warps_g, item * npan_g) / kDecWarps) + 1;
+                        const float* rec = a.grec + static_cast<int64_t>(item) * a.cov_g * 32 + (qq & 31);
+                        v0[u] = __ldcg(rec);
+                        if (ncs[u] > 1) v1[u] = __ldcg(rec + 32);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kHB; ++u) {
+                    const int q = q0 + u * kDecThreads;
+                    if (q < hn) {
+                        const int qq = h_s0 * f + q;
+                        const float* rec = a.grec + static_cast<int64_t>(qq >> 5) * a.cov_g * 32 + (qq & 31);
+                        float z = v0[u] + v1[u];              // records in contributor order
+                        for (int cc = 2; cc < ncs[u]; ++cc) z += __ldcg(rec + cc * 32);
+                        z *= P.gu_ts[s_e[qq / f]];
+                        const float h = z > 0.0f ? z * z : 0.0f;
+                        hf[q] = h;
+                        a.ws.h[qq] = h;
+                    }
+                }
             }
             __syncthreads();
-            if (tid < 32) {
-                float o = 0.0f;
-                for (int j = 0; j < k; ++j) o = fmaf(s_w[j], s_y[s_pos[j] * 32 + tid], o);
-                a.out[static_cast<int64_t>(l) * d + rt * 32 + tid] = o;
+            for (int gi = tid; gi < h_ns * (f / 16); gi += kDecThreads) {
+                bool any = false;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) any |= hf[gi * 16 + j] != 0.0f;
+                gact[gi] = any ? 1 : 0;
             }
             __syncthreads();
-        }
 
+            // ------------------------------------------------------------ D (NVFP4)
+            // Units (slot, 256-row tile, group of 16 neurons), group fastest.  Lane l owns rows
+            // 8l .. 8l+7 of the tile: per active group 16 code words (one per neuron) and 8 row
+            // scales; the products are exact in fp32 (e2m1 x f32 h), summed over the group's
+            // neurons in order, then scaled by each row's E4M3 scale.  Inactive groups are not
+            // read.  Two active groups' loads are in flight per warp.
+            if (rd.n > 0) {
+                const int64_t grp_bytes = 16 * (d / 2) + d;     // one group record of a matrix
+                int scan_item = rd.item0, scan_g = rd.b0, left = rd.n;
+                int acc_item = -1;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                auto flush = [&]() {
+                    if (acc_item >= 0) {
+                        float* rr = dred + ((acc_item - d_item0) * kDecWarps + warp) * 256 + lane * 8;
+                        *reinterpret_cast<float4*>(rr) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                        *reinterpret_cast<float4*>(rr + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+                };
+                // the next active unit of the range (-1: none left)
+                auto next_active = [&](int& g_out) -> int {
+                    while (left > 0) {
+                        const int it = scan_item, g = scan_g;
+                        --left;
+                        if (++scan_g == npan_d) {
+                            scan_g = 0;
+                            ++scan_item;
+                        }
+                        if (gact[(it / nrt - h_s0) * npan_d + g]) {
+                            g_out = g;
+                            return it;
+                        }
+                    }
+                    return -1;
+                };
+                auto load = [&](int it, int g, uint32_t (&cw)[16], uint2& sc) {
+                    const int sl = it / nrt, rt = it % nrt;
+                    const uint8_t* base = P.w_dn + static_cast<int64_t>(s_e[sl]) * a.dn_bytes + g * grp_bytes;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) cw[j] = ldg_stream4(base + j * (d / 2) + rt * 128 + lane * 4);
+                    sc = ldg_stream8(base + 16 * (d / 2) + rt * 256 + lane * 8);
+                };
+                auto compute = [&](int it, int g, const uint32_t (&cw)[16], const uint2& sc) {
+                    if (it != acc_item) {
+                        flush();
+                        acc_item = it;
+                    }
+                    const float* hv = hf + (it / nrt - h_s0) * f + 16 * g;
+                    float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float h = hv[j];
+#pragma unroll
+                        for (int by = 0; by < 4; ++by) {
+                            const float2 v = e2m1x2_to_f32x2((cw[j] >> (8 * by)) & 0xffu);   // rows 2by, 2by+1
+                            part[2 * by] = fmaf(v.x, h, part[2 * by]);
+                            part[2 * by + 1] = fmaf(v.y, h, part[2 * by + 1]);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const float sb = e4m3_to_f32(((r < 4 ? sc.x : sc.y) >> (8 * (r & 3))) & 0xffu);
+                        acc[r] = fmaf(sb, part[r], acc[r]);
+                    }
+                };
+                uint32_t cw0[16], cw1[16];
+                uint2 sc0, sc1;
+                int g0 = 0, g1 = 0;
+                int it0 = next_active(g0);
+                if (it0 >= 0) load(it0, g0, cw0, sc0);
+                while (it0 >= 0) {
+                    const int it1 = next_active(g1);
+                    if (it1 >= 0) load(it1, g1, cw1, sc1);
+                    compute(it0, g0, cw0, sc0);
+                    if (it1 < 0) break;
+                    it0 = next_active(g0);
+                    if (it0 >= 0) load(it0, g0, cw0, sc0);
+                    compute(it1, g1, cw1, sc1);
+                }
+                flush();
+            }
+            // The CTA's record of each down item it touched: its warps' partials in warp order.
+            __syncthreads();
+            for (int i = tid; i < d_items * 256; i += kDecThreads) {
+                const int it = i >> 8, r = i & 255;
+                float v = 0.0f;
+#pragma unroll 4
+                for (int w = 0; w < kDecWarps; ++w) v += dred[(it * kDecWarps + w) * 256 + r];
+                const uint32_t item = static_cast<uint32_t>(d_item0 + it);
+                const int cidx = c - static_cast<int>(split_owner(U_d, a.warps_d, item * npan_d) / kDecWarps);
+                a.drec[(static_cast<int64_t>(item) * a.cov_d + cidx) * 256 + r] = v;
+            }
+            grid_barrier(a.bar, ++nbar * G, a.ws.err);
+            if (l + 1 < a.n_layers) request_router(a.lp[l + 1].W);   // the ring is free until the next gate.up
+
+            // ------------------------------------------------------------ C (NVFP4)
+            // 32-row chunk q of the output is combined by CTA q mod G: y of each slot (its CTA
+            // records in order, times the down tensor scale), then the pairs in order j.
+            float* s_y = slog;   // [k][32]
+            for (int q = c; q < d / 32; q += G) {
+                const int rt = q / 8, off = (q % 8) * 32;
+                for (int task = tid; task < k * 32; task += kDecThreads) {
+                    const int sl = task >> 5, r = task & 31;
+                    const uint32_t item = static_cast<uint32_t>(sl * nrt + rt);
+                    const int nc = static_cast<int>(split_owner(U_d, a.warps_d, (item + 1) * npan_d - 1) / kDecWarps -
+                                                    split_owner(U_d, a.warps_d, item * npan_d) / kDecWarps) + 1;
+                    const float* rec = a.drec + static_cast<int64_t>(item) * a.cov_d * 256 + off + r;
+                    float v[4];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) v[cc] = cc < nc ? __ldcg(rec + cc * 256) : 0.0f;
+                    float y = ((v[0] + v[1]) + v[2]) + v[3];   // records in contributor order
+                    for (int cc = 4; cc < nc; ++cc) y += __ldcg(rec + cc * 256);
+                    s_y[sl * 32 + r] = y * P.dn_ts[s_e[sl]];
+                }
+                __syncthreads();
+                if (tid < 32) {
+                    float o = 0.0f;
+                    for (int j = 0; j < k; ++j) o = fmaf(s_w[j], s_y[s_pos[j] * 32 + tid], o);
+                    a.out[static_cast<int64_t>(l) * d + q * 32 + tid] = o;
+                }
+                __syncthreads();
+            }
+        }
         // ---------------------------------------------------------------- N: the next layer's input
         // x_{l+1} = bf16(out_l / sqrt(mean(out_l^2) + eps)), the sum of squares in the order of the
         // stand-alone RMS-norm kernel (threads t < 256 take elements t, t + 256, ...; warp sums;
@@ -609,14 +845,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
 }
 
 // ------------------------------------------------------------------------------ host side
-// Largest dynamic shared memory the kernel is configured for: region B up to 64 KB
-// (k*f <= 16384, d <= 16384), region C up to 32 KB (d <= 8192, or 4096 for fp32 x), region P
-// up to 16 KB (8 items); with the static arrays, within the 227 KB of one CTA.
-size_t decode_max_smem() { return kRingBytes + 2 * 32768 + 2 * 16384 + 16384; }
+// Dynamic shared memory the kernel is configured for (with its static arrays, within the
+// 227 KB one CTA may hold).
+size_t decode_max_smem() { return 220 * 1024; }
 
 namespace {
 bool g_decode_ok[64] = {};
 int g_decode_ctas[64] = {};
+
+template <int FMT, int ACT>
+bool configure_one() {
+    const int max_smem = static_cast<int>(decode_max_smem());
+    if (cudaFuncSetAttribute(decode_layer_kernel<FMT, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
+        cudaSuccess)
+        return false;
+    int per_sm = 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel<FMT, ACT>, kDecThreads, max_smem);
+    return e == cudaSuccess && per_sm >= 1;
+}
 }  // namespace
 
 // Dynamic shared memory limit, cooperative-launch support and one-CTA-per-SM residency
@@ -627,17 +874,9 @@ cudaError_t configure_decode_kernel(int dev, int num_sms) {
     cudaError_t e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     if (e != cudaSuccess) return e;
     if (!coop) return cudaSuccess;
-    const int max_smem = static_cast<int>(decode_max_smem());
-    e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (e != cudaSuccess) {
+    if (!configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU>() || !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2>()) {
         (void)cudaGetLastError();
         return cudaSuccess;   // the separate kernels serve every shape
-    }
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel, kDecThreads, max_smem);
-    if (e != cudaSuccess || per_sm < 1) {
-        (void)cudaGetLastError();
-        return cudaSuccess;
     }
     g_decode_ok[dev] = true;
     g_decode_ctas[dev] = num_sms < kMaxDecodeCtas ? num_sms : kMaxDecodeCtas;
@@ -647,11 +886,11 @@ cudaError_t configure_decode_kernel(int dev, int num_sms) {
 // CTAs of the decode kernel on this device (0: not available).
 int decode_ctas(int dev) { return (dev >= 0 && dev < 64 && g_decode_ok[dev]) ? g_decode_ctas[dev] : 0; }
 
-cudaError_t launch_decode_layer(const DecodeArgs& a, int ctas, cudaStream_t s) {
+cudaError_t launch_decode_layer(const DecodeArgs& a, int wfmt, size_t smem, int ctas, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = decode_smem_bytes(a.d, a.f, a.k, a.xt, a.cta_items);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -660,7 +899,8 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, int ctas, cudaStream_t s) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
+    if (wfmt == MOE_W_Q8_0) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU>, a);
+    return cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2>, a);
 }
 
 }  // namespace moe

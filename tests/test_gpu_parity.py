@@ -205,9 +205,10 @@ def test_one_token_row_tile_down(k):
     assert_close(out, ref["out"])
 
 
-# One token, Q8_0 SwiGLU, routing computed: the whole layer as one cooperative kernel
-# (router, top-k, softmax, gate.up, down, combine; two grid barriers).  The shapes cover
-# k = 1 .. 8 and 32, E from 4 to 1024 (1024 experts: 8 per routing CTA), fp32 and bf16 inputs,
+# One token, routing computed: the whole layer as one cooperative kernel (router, top-k,
+# softmax, gate.up, down, combine; three grid barriers).  The shapes cover
+# k = 1 .. 8, 22 and 32, E from 4 to 1024 (1024 experts: 8 per routing CTA), Q8_0 SwiGLU and NVFP4
+# ReLU^2 with 80-92.5% zeros, fp32 and bf16 inputs,
 # panel ranges that split items across warps and warps that span several items; every case
 # is checked against the oracle and against the separate-kernel path, and the output must
 # be completely written and bitwise identical over three calls.
@@ -220,6 +221,11 @@ ONE_KERNEL = {
     "k32_e1024": synth.Workload("ok_k32", d=256, f=64, E=1024, k=32, act="swiglu", wfmt="q8_0", x_dtype="bf16",
                                 layers=1),
     "e4_k4": synth.Workload("ok_e4", d=256, f=32, E=4, k=4, act="swiglu", wfmt="q8_0", x_dtype="bf16", layers=1),
+    # NVFP4 ReLU^2 (gateless latent experts, neuron-contiguous down, all-zero groups skipped)
+    "nv_k6_e32": synth.Workload("ok_nv6", d=512, f=256, E=32, k=6, act="relu2", wfmt="nvfp4", x_dtype="bf16",
+                                layers=1, zero_fraction=0.925),
+    "nv_k22_e512_f32": synth.Workload("ok_nv22", d=256, f=128, E=512, k=22, act="relu2", wfmt="nvfp4",
+                                      x_dtype="f32", layers=1, zero_fraction=0.8),
 }
 
 
@@ -409,6 +415,8 @@ STACKS = {
     "k8_e64_bf16": (synth.Workload("st_k8", d=1024, f=192, E=64, k=8, act="swiglu", wfmt="q8_0", x_dtype="bf16",
                                    layers=4), 4),
     "tiny_f32_input": (synth.WORKLOADS["tiny"], 3),
+    "nv_relu2": (synth.Workload("st_nv", d=512, f=256, E=32, k=6, act="relu2", wfmt="nvfp4", x_dtype="bf16",
+                                layers=3, zero_fraction=0.925), 3),
 }
 
 
