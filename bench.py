@@ -542,8 +542,7 @@ def active_expert_bytes(stack, inputs, T, w):
         out = layer.forward(x, trace=tr)
         experts = torch.unique(tr["idx"]).numel()
         gu_layer.append(experts * gu_b)
-        layer_bytes.append(experts * (gu_b + dn_b) + layer.router_w.numel() * 4)
-        if w.act == "relu2":
+        if w.act == "relu2":   # the down projection reads only 16-neuron groups with a non-zero h
             h = tr["h"]
             off = tr["offsets"].cpu().numpy()
             act_groups = 0
@@ -551,9 +550,11 @@ def active_expert_bytes(stack, inputs, T, w):
                 if off[e + 1] > off[e]:
                     hh = h[off[e]:off[e + 1]].reshape(off[e + 1] - off[e], -1, 16)
                     act_groups += int((hh != 0).any(dim=2).any(dim=0).sum().item())
-            step += experts * gu_b + act_groups * (dn_b // (w.f // 16))
+            expert_bytes = experts * gu_b + act_groups * (dn_b // (w.f // 16))
         else:
-            step += experts * (gu_b + dn_b)
+            expert_bytes = experts * (gu_b + dn_b)
+        step += expert_bytes
+        layer_bytes.append(expert_bytes + layer.router_w.numel() * 4)
         x = native.rmsnorm_bf16(out)
     torch.cuda.synchronize()
     return {"step": int(step), "gate_up_per_layer": int(statistics.mean(gu_layer)),

@@ -88,10 +88,11 @@ typedef enum { MOE_LAYOUT_CANONICAL = 0, MOE_LAYOUT_DEVICE = 1, MOE_LAYOUT_NEURO
  * kernels (a few tokens per expert).  GEMM: grouped GEMMs on the tensor cores (tcgen05),
  * which need f a multiple of 64 (128 for ReLU^2); forcing GEMM on another shape returns
  * MOE_ERR_UNSUPPORTED.  AUTO takes GEMM when T*k >= 8*E and the shape allows it; for ONE
- * token with Q8_0 SwiGLU experts and routing computed by the call (d <= 8192, k*f <= 16384)
- * it runs the whole layer as a single cooperative kernel, one CTA per SM, when the device
- * supports cooperative launches (the same results within the output tolerance; routing,
- * weights and the permutation bit-identical).  GEMV keeps the separate kernels. */
+ * token with Q8_0 SwiGLU (k*f <= 16384) or NVFP4 ReLU^2 experts and routing computed by the
+ * call (d <= 8192) it runs the whole layer as a single cooperative kernel, one CTA per SM,
+ * when the device supports cooperative launches (the same results within the output
+ * tolerance; routing, weights and the permutation bit-identical).  GEMV keeps the separate
+ * kernels. */
 typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GEMM = 2 } moe_path;
 
 /* Bytes of one quantised matrix: rows*cols/32*34 (Q8_0), rows*cols/2 + rows*cols/16
@@ -244,7 +245,7 @@ moe_status moe_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uin
  * idx, w   optional device int32 / fp32 [n_layers][k]: each layer's routing, or both NULL.
  * workspace at least moe_layer_workspace_bytes(descs, 1) bytes, zero-filled before its first
  *          use (as for moe_layer_forward).
- * With Q8_0 SwiGLU layers, path AUTO, at most 64 layers and a device that supports
+ * With Q8_0 SwiGLU or NVFP4 ReLU^2 layers, path AUTO, at most 64 layers and a device that supports
  * cooperative launches, the whole stack is ONE kernel launch (one CTA per SM, the RMS-norm
  * between layers inside it, bitwise equal to the layer-by-layer result); otherwise each
  * layer is a moe_layer_forward call followed by the RMS-norm.
