@@ -1,39 +1,49 @@
-// decode.cu -- one routed MoE layer for ONE token as a single persistent kernel.
+// decode.cu -- routed MoE layers for ONE token as a single persistent kernel: one layer
+// (moe_layer_forward) or a whole stack of layers glued by the RMS-norm (moe_stack_forward).
 //
 // The same layer as route.cu + gemv.cu (router, top-k, softmax over the selected logits,
-// gate.up with SiLU(gate)*up, down projection, fixed-order combine), for the case that
+// gate.up with the activation, down projection, fixed-order combine), for the case that
 // decides decode speed: one token, where the layer moves only the routed experts' weights
 // (a few tens of MB) and the separate launches' start-up, ramp and tail cost more than the
-// bytes.  Sources of the computation:
+// bytes.  Two expert formats: Q8_0 with SwiGLU, and NVFP4 with ReLU^2 (gateless latent
+// experts).  Sources of the computation:
 //   router / top-k / softmax: "Squeezing a 26B MoE onto the cheapest Inferentia instance"
 //     (128 experts, top-8 per token), with the canonical fp32 summation order of the oracle;
 //   gate.up + SwiGLU: "Running Gemma 4 26B at 5 tokens/s on a 13-year-old Xeon", sections
 //     "A three-step fix" / "Runtime graph fallback" (fused [n_embd, 2*n_ff, n_experts]
 //     tensor, gate rows first, then SiLU(gate)*up);
-//   combine: "Running NVIDIA's new 120B Nemotron-3.5-Super on an 8GB GPU", section "How we
-//     check correctness" (per-(token, expert) results summed in a fixed order, no atomics
-//     on the values).
+//   ReLU^2 experts and the down projection over 16-neuron groups that hold a non-zero
+//     activation: "Running NVIDIA's new 120B Nemotron-3.5-Super on an 8GB GPU", section
+//     "How the engine works", step 4;
+//   combine: the same page, section "How we check correctness" (per-(token, expert) results
+//     summed in a fixed order, no atomics on the values).
 //
 // One CTA per SM (a cooperative launch: every CTA is resident, so the grid barriers below
-// cannot wait on a CTA that never runs), 16 warps each.  Three grid barriers:
+// cannot wait on a CTA that never runs), 16 warps each.  Per layer:
 //   R  CTA c < E/epc computes the logits of experts [c*epc, (c+1)*epc) in the canonical
 //      order (256 fma chains i = l (mod 256), then the halving tree); its slice of the
 //      router weights is copied into shared memory before the kernel waits for the
-//      previous one.  Barrier 1.  Every CTA then ranks all E logits itself (top-k with the
-//      lower index on ties), so no CTA waits for a selection made elsewhere.
-//   G  gate.up: the panel products of all k experts (k * f/16 items of 16 gate + 16 up
-//      rows, d/32 panels each) are one flattened range split evenly over the warps of the
-//      grid, so every warp streams the same number of panels (within one) whatever the
-//      shapes.  A CTA's warps cover a contiguous stretch of items: their partials meet in
-//      shared memory and the CTA writes one record per item it touched.  Each CTA also
-//      asks L2 for its share of the routed experts' down matrices.  Barrier 2.
-//   H  every CTA sums each item's records (in CTA order) and applies SwiGLU into its own
-//      f16 copy of h.
-//   D  down: (slot, row tile of 32, panel) units flattened the same way (the first ring
-//      stages are requested before H); each warp writes one record per item it touched.
-//      Barrier 3.
-//   C  row tile rt is combined by CTA rt mod G: y per slot (records in warp order), then the
+//      previous one (in a stack: while the previous layer finishes).  Barrier.  With up to
+//      256 experts every CTA then ranks all E logits itself (top-k, lower index on ties);
+//      with more, the routing CTAs rank their own experts and publish the winners behind
+//      one more barrier.
+//   G  gate.up: the panel products of all k experts (items of 16 gate + 16 up rows, or 32
+//      rows for ReLU^2) are one flattened range split evenly over the warps of the grid, so
+//      every warp streams the same number of panels (within one) whatever the shapes.  A
+//      CTA's warps cover a contiguous stretch of items: their partials meet in shared
+//      memory and the CTA writes one record per item it touched.  Q8_0: each CTA also asks
+//      L2 for its share of the routed experts' down matrices.  Barrier.
+//   H  each CTA sums the records of the slots its down units read (in CTA order) and applies
+//      the activation into its own copy of h (NVFP4: and flags the 16-neuron groups that
+//      hold a non-zero h).
+//   D  down, flattened the same way: Q8_0 units (slot, 32-row tile, 32-neuron panel), one
+//      record per warp and item (the first ring stages are requested before H); NVFP4
+//      units (slot, 256-row tile, 16-neuron group), only flagged groups read, one record
+//      per CTA and item.  Barrier.
+//   C  rows are combined by CTA (row chunk) mod G: y per slot (records in order), then the
 //      pairs in order j: out[r] = sum_j w_j * y_{slot(j)}[r].
+//   N  (stacks) barrier; every CTA computes the next layer's input, the RMS-norm of out in
+//      the reduction order of the stand-alone norm kernel.
 // Every per-warp quantity that depends only on the shapes is worked out before the kernel
 // waits for the previous one.  All waits are bounded (about one second, then device error 2
 // and the kernel goes on), so a barrier can never hang the GPU.  Results are bitwise
