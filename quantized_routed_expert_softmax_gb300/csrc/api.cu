@@ -206,7 +206,9 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     // staged activations: f16 (bf16 inputs) or f16 hi + lo (fp32 inputs; h always) per element
     const int64_t x_bytes = (xt == MOE_F32) ? 4 : 2;
     p.tt_gu = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tmax, kSmemBudget / (x_bytes * d->d))));
-    const int64_t dn_cap = (d->wfmt == MOE_W_NVFP4) ? 4 : 8;
+    // NVFP4 down: token tiles of at most 2 (two CTAs per SM fit in registers; a 4-token tile
+    // leaves one per SM, and a few tokens per expert is the common case)
+    const int64_t dn_cap = (d->wfmt == MOE_W_NVFP4) ? 2 : 8;
     p.tt_dn = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(std::min(tmax, dn_cap), kSmemBudget / (4 * d->f))));
     // the tile counts are powers of two up to 8 (the kernels specialise 1, 2, 4, 8)
     auto pow2 = [](int v) { return v >= 8 ? 8 : (v >= 4 ? 4 : (v >= 2 ? 2 : 1)); };
@@ -579,6 +581,12 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.rows_gu = static_cast<int>(desc->act == MOE_ACT_SWIGLU ? 2 * desc->f : desc->f);
     a.tt_gu = p.tt_gu;
     a.tt_dn = p.tt_dn;
+    {   // warps per gate.up tile: each warp should stream at least 12 K panels
+        const int npan = static_cast<int>(desc->wfmt == MOE_W_Q8_0 ? desc->d / 32 : desc->d / 64);
+        int wpt = 8;
+        while (wpt > 1 && npan / wpt < 12) wpt /= 2;
+        a.gu_wpt = wpt;
+    }
     a.gwords = p.gwords;
     a.T = static_cast<int>(T);
     a.P = static_cast<int>(p.P);

@@ -55,6 +55,7 @@ struct ExpertArgs {
     int xt;
     int d, f, k, rows_gu;
     int tt_gu, tt_dn;            // tokens per shared-memory tile
+    int gu_wpt;                  // gate.up: warps that share one tile's K panels (8, 4, 2 or 1)
     int gwords;                  // 32-bit words of group mask per slot
     int T;                       // tokens
     int P;                       // pairs T*k

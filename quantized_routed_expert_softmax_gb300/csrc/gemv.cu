@@ -192,18 +192,23 @@ __global__ void __launch_bounds__(256, 3) gate_up_gemv_kernel(ExpertArgs a) {
     unsigned char* ring = dsm + warp * kStages * kSlotBytes;
     __half* xs = reinterpret_cast<__half*>(dsm + 8 * kStages * kSlotBytes);   // [tt][d]
     __shared__ float red[8 * 256];
-    __shared__ uint32_t act_bits;
-    const int tile = blockIdx.x;
+    __shared__ uint32_t act_bits[8];
+    // wpt warps share one tile's K panels; the CTA covers 8 / wpt consecutive tiles (with a
+    // short K, each warp then streams a longer run of panels instead of a couple)
+    const int wpt = a.gu_wpt, tpc = 8 / wpt;
+    const int ntiles = (ACT == MOE_ACT_SWIGLU) ? a.f / 16 : a.f / 32;
+    const int tile = blockIdx.x * tpc + warp / wpt, part = warp % wpt;
+    const bool live = tile < ntiles;
     const int rowA = (ACT == MOE_ACT_SWIGLU) ? tile * 16 : tile * 32;
     const int rowB = (ACT == MOE_ACT_SWIGLU) ? a.f + tile * 16 : tile * 32 + 16;
     const uint8_t* W = a.w_gu + static_cast<int64_t>(e) * a.gu_bytes;
     const int npan = (FMT == MOE_W_Q8_0) ? a.d / 32 : a.d / 64;
-    const int pb = warp * npan / 8, pe = (warp + 1) * npan / 8;
+    const int pb = live ? part * npan / wpt : 0, pe = live ? (part + 1) * npan / wpt : 0;
+    if (threadIdx.x < 8) act_bits[threadIdx.x] = 0;
     if (threadIdx.x == 0) {
-        act_bits = 0;
         if (a.prefetch_down) {   // this CTA's share of the expert's down matrix, into L2
             const int64_t share = ((a.dn_bytes + gridDim.x - 1) / gridDim.x + 127) / 128 * 128;
-            const int64_t off = static_cast<int64_t>(tile) * share;
+            const int64_t off = static_cast<int64_t>(blockIdx.x) * share;
             if (off < a.dn_bytes) {
                 const int64_t n = min(share, a.dn_bytes - off);
                 prefetch_l2(a.w_dn + static_cast<int64_t>(e) * a.dn_bytes + off, static_cast<uint32_t>(n));
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(256, 3) gate_up_gemv_kernel(ExpertArgs a) {
         if (a.pf_bytes > 0) {   // this CTA's share of the caller's L2 hint (the next layer's router)
             const int64_t nct = static_cast<int64_t>(gridDim.x) * gridDim.y;
             const int64_t share = ((a.pf_bytes + nct - 1) / nct + 127) / 128 * 128;
-            const int64_t off = (static_cast<int64_t>(blockIdx.y) * gridDim.x + tile) * share;
+            const int64_t off = (static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x) * share;
             if (off < a.pf_bytes) prefetch_l2(a.pf + off, static_cast<uint32_t>(min(share, a.pf_bytes - off)));
         }
     }
@@ -228,12 +233,12 @@ __global__ void __launch_bounds__(256, 3) gate_up_gemv_kernel(ExpertArgs a) {
         });
         store_partials(red, acc);
         __syncthreads();
-        for (int it = threadIdx.x; it < 16 * 8; it += blockDim.x) {
-            const int row = it >> 3, tok = it & 7;
-            if (tok >= nt) continue;
+        for (int it = threadIdx.x; it < tpc * 16 * 8; it += blockDim.x) {
+            const int tl = it >> 7, row = (it >> 3) & 15, tok = it & 7;
+            const int tt = blockIdx.x * tpc + tl;
+            if (tok >= nt || tt >= ntiles) continue;
             float zA = 0.0f, zB = 0.0f;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
+            for (int w = tl * wpt; w < (tl + 1) * wpt; ++w) {   // the tile's warps in order
                 zA += red[w * 256 + row * 8 + tok];
                 zB += red[w * 256 + 128 + row * 8 + tok];
             }
@@ -242,22 +247,23 @@ __global__ void __launch_bounds__(256, 3) gate_up_gemv_kernel(ExpertArgs a) {
             float* hrow = a.ws.h + static_cast<int64_t>(r0 + t0 + tok) * a.f;
             if (ACT == MOE_ACT_SWIGLU) {
                 const float h = silu(zA) * zB;
-                hrow[tile * 16 + row] = h;
-                if (h != 0.0f) atomicOr(&act_bits, 1u);
+                hrow[tt * 16 + row] = h;
+                if (h != 0.0f) atomicOr(&act_bits[tl], 1u);
             } else {
                 const float hA = zA > 0.0f ? zA * zA : 0.0f;
                 const float hB = zB > 0.0f ? zB * zB : 0.0f;
-                hrow[tile * 32 + row] = hA;
-                hrow[tile * 32 + 16 + row] = hB;
-                if (hA != 0.0f) atomicOr(&act_bits, 1u);
-                if (hB != 0.0f) atomicOr(&act_bits, 2u);
+                hrow[tt * 32 + row] = hA;
+                hrow[tt * 32 + 16 + row] = hB;
+                if (hA != 0.0f) atomicOr(&act_bits[tl], 1u);
+                if (hB != 0.0f) atomicOr(&act_bits[tl], 2u);
             }
         }
         __syncthreads();   // red and xs are reused by the next token tile
     }
-    if (threadIdx.x == 0 && act_bits) {
-        const int g0 = (ACT == MOE_ACT_SWIGLU) ? tile : 2 * tile;
-        const uint32_t bits = (ACT == MOE_ACT_SWIGLU) ? 1u : act_bits;
+    if (threadIdx.x < tpc && act_bits[threadIdx.x]) {
+        const int tt = blockIdx.x * tpc + threadIdx.x;
+        const int g0 = (ACT == MOE_ACT_SWIGLU) ? tt : 2 * tt;
+        const uint32_t bits = (ACT == MOE_ACT_SWIGLU) ? 1u : act_bits[threadIdx.x];
         atomicOr(a.ws.gmask + slot * a.gwords + g0 / 32, bits << (g0 % 32));
     }
 }
@@ -604,7 +610,7 @@ __device__ __forceinline__ void dn_nv_tile(const ExpertArgs& a, const uint8_t* W
 }
 
 template <int TT>
-__global__ void __launch_bounds__(256, TT == 1 ? 3 : 1) down_nv_gemv_kernel(ExpertArgs a) {
+__global__ void __launch_bounds__(256, TT == 1 ? 3 : (TT == 2 ? 2 : 1)) down_nv_gemv_kernel(ExpertArgs a) {
     pdl_wait();
     pdl_trigger();
     const int slot = blockIdx.y;
@@ -790,10 +796,12 @@ cudaError_t configure_gemv_kernels() {
 }
 
 cudaError_t launch_gate_up_gemv(const ExpertArgs& a, int wfmt, int act, int slot_cap, cudaStream_t s) {
-    const int tiles = (act == MOE_ACT_SWIGLU) ? a.f / 16 : a.f / 32;
+    const int ntiles = (act == MOE_ACT_SWIGLU) ? a.f / 16 : a.f / 32;
+    const int tpc = 8 / a.gu_wpt;                       // tiles per CTA
+    const int ctas_x = (ntiles + tpc - 1) / tpc;
     const size_t smem = static_cast<size_t>(8) * kStages * kSlotBytes +
                         static_cast<size_t>(a.tt_gu) * a.d * 2 * (a.xt == MOE_F32 ? 2 : 1);
-    return gu_dispatch(a, wfmt, act, dim3(tiles, slot_cap), smem, s, false);
+    return gu_dispatch(a, wfmt, act, dim3(ctas_x, slot_cap), smem, s, false);
 }
 
 size_t down_gemv_smem(int wfmt, int tt_dn, int f) {
