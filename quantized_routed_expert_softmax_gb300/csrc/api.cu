@@ -202,7 +202,12 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     p.slot_cap = static_cast<int>(std::min<int64_t>(d->E, p.P));
     p.nchunk = static_cast<int>((p.P + 1023) / 1024);
     p.gwords = static_cast<int>((d->f / 16 + 31) / 32);
-    const int64_t tmax = std::max<int64_t>(1, std::min<int64_t>(8, T));
+    // Token tiles: the staged activations take shared memory per CTA, and with it CTAs per SM,
+    // so tiles are sized for twice the average pairs per routed expert (room for a skewed
+    // routing); an expert with more tokens loops over further tiles.
+    const int64_t slots = std::max<int64_t>(1, std::min<int64_t>(d->E, p.P));
+    const int64_t want = 2 * ((p.P + slots - 1) / slots);
+    const int64_t tmax = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(8, T), want));
     // staged activations: f16 (bf16 inputs) or f16 hi + lo (fp32 inputs; h always) per element
     const int64_t x_bytes = (xt == MOE_F32) ? 4 : 2;
     p.tt_gu = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tmax, kSmemBudget / (x_bytes * d->d))));
@@ -211,7 +216,7 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     const int64_t dn_cap = (d->wfmt == MOE_W_NVFP4) ? 2 : 8;
     p.tt_dn = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(std::min(tmax, dn_cap), kSmemBudget / (4 * d->f))));
     // the tile counts are powers of two up to 8 (the kernels specialise 1, 2, 4, 8)
-    auto pow2 = [](int v) { return v >= 8 ? 8 : (v >= 4 ? 4 : (v >= 2 ? 2 : 1)); };
+    auto pow2 = [](int v) { return v >= 8 ? 8 : (v >= 4 ? 4 : (v >= 2 ? 2 : 1)); };   // (rounds down)
     p.tt_gu = pow2(p.tt_gu);
     p.tt_dn = pow2(p.tt_dn);
     p.small_route = (T <= kSmallT && p.P <= kSmallPairs && T * d->E <= kFusedRouteLogits);
