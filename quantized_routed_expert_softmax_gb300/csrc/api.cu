@@ -30,7 +30,7 @@ cudaError_t launch_expert_gemm(const ExpertArgs&, int, int, int, int, int, int, 
 cudaError_t launch_gather_x_f16(const ExpertArgs&, int, cudaStream_t);
 cudaError_t configure_decode_kernel(int, int);
 int decode_ctas(int);
-size_t decode_smem_plan(int, int, int, int, int, int, int, int*, int*, int*);
+size_t decode_smem_plan(int, int, int, int, int, int, int, int*, int*);
 size_t decode_ring_bytes();
 size_t decode_max_smem();
 cudaError_t launch_decode_layer(const DecodeArgs&, int, size_t, int, cudaStream_t);
@@ -162,8 +162,8 @@ bool decode_shape_ok(const moe_layer_desc* d, int64_t T, int xt) {
     if (!q8 && !nv) return false;
     if (d->d > 8192 || d->f % 32 != 0) return false;
     if (q8 && d->k * d->f > 16384) return false;   // h of every slot in shared memory
-    if (decode_smem_plan(d->wfmt, static_cast<int>(d->d), static_cast<int>(d->f), d->k, xt, 1, 1, nullptr, nullptr,
-                         nullptr) > decode_max_smem())
+    if (decode_smem_plan(d->wfmt, static_cast<int>(d->d), static_cast<int>(d->f), d->k, xt, 1, 1, nullptr, nullptr) >
+        decode_max_smem())
         return false;
     const int epc = decode_epc(d->E, kMaxDecodeCtas);
     if (epc == 0 || static_cast<size_t>(d->d * epc * 4 + epc * 1024) > decode_ring_bytes()) return false;
@@ -175,7 +175,7 @@ bool decode_shape_ok(const moe_layer_desc* d, int64_t T, int xt) {
 // gate.up partials of one CTA's items, within what the kernel is configured for.
 bool decode_split_fits(const moe_layer_desc* d, const DecodeSplit& sp, int xt) {
     if (decode_smem_plan(d->wfmt, static_cast<int>(d->d), static_cast<int>(d->f), d->k, xt,
-                         static_cast<int>(sp.cta_items), static_cast<int>(sp.cta_slots), nullptr, nullptr,
+                         static_cast<int>(sp.cta_items), static_cast<int>(sp.cta_slots), nullptr,
                          nullptr) > decode_max_smem())
         return false;
     if (d->wfmt == MOE_W_NVFP4) {
@@ -378,7 +378,7 @@ bool fill_decode_args(const moe_layer_desc* descs, int n, const void* x, int xt,
         a->dn_bytes = static_cast<int64_t>(moe_nvfp4_bytes(desc->d, desc->f));
     }
     *smem_out = decode_smem_plan(desc->wfmt, a->d, a->f, a->k, xt, a->cta_items, static_cast<int>(sp.cta_slots),
-                                 &a->off_b, &a->off_c, &a->off_p);
+                                 &a->off_c, &a->off_p);
     a->n_layers = n;
     for (int l = 0; l < n; ++l) {
         a->lp[l].W = descs[l].router_w;

@@ -100,7 +100,7 @@ struct DecodeArgs {
     int cov_g, cov_d;            // partial records per item at most (CTAs / warps that can share one item)
     int cta_items;               // gate.up items one CTA's range touches at most
     int cta_items_d;             // NVFP4: down items (slot, 256-row tile) one CTA's range touches at most
-    int off_b, off_c, off_p;     // dynamic shared memory: x fp32 / h, x f16, gate.up partials (bytes)
+    int off_c, off_p;            // dynamic shared memory offsets of x f16 and the gate.up partials (bytes)
     int64_t gu_bytes, dn_bytes;  // bytes of one expert's gate/up and down matrices
     int n_layers;                // 1: moe_layer_forward; more: moe_stack_forward
     float eps;                   // RMS-norm between stacked layers

@@ -107,6 +107,35 @@ __device__ __forceinline__ int item_contributors(uint32_t U, uint32_t W, uint32_
 
 __device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) { return va > vb || (va == vb && ea < eb); }
 
+// Selection for many experts, by a routing CTA (all of its threads): each of its own epc
+// experts is ranked among all E logits (lg) by 512/epc threads, and an expert of rank < k is
+// published at its rank.  Only the kernels for more than 256 experts hold this code (a
+// template parameter): the extra code, and even an out-of-line call, measurably slowed the
+// kernels of the common shapes.
+__device__ __forceinline__ void rank_own_experts(const float* lg, int* cnt, int E, int k, int epc, int c, int32_t* sel,
+                                              float* selv) {
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tpx = kDecThreads / epc;
+    const int j = tid / tpx, part = tid % tpx;
+    const int e = c * epc + j;
+    const float v = lg[e];
+    int r = 0;
+#pragma unroll 1
+    for (int o = part * E / tpx; o < (part + 1) * E / tpx; ++o) r += beats(lg[o], o, v, e);
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
+    if ((tid & 31) == 0) cnt[warp] = r;
+    __syncthreads();
+    if (part == 0) {
+        int rank = 0;
+        for (int w = j * tpx / 32; w < (j + 1) * tpx / 32; ++w) rank += cnt[w];
+        if (rank < k) {
+            sel[rank] = e;
+            selv[rank] = v;
+        }
+    }
+}
+
 // A warp's share of one phase: units [u0, u0 + n) starting at panel b0 of item item0, whose
 // first record goes to contributor slot c0 of that item (later items: slot 0).
 struct WarpRange {
@@ -126,7 +155,8 @@ __device__ __forceinline__ WarpRange warp_range(uint32_t U, uint32_t W, uint32_t
 
 }  // namespace
 
-// Shared-memory plan (dynamic): [ring | B | C | P], offsets computed on the host
+// Shared-memory plan (dynamic): [ring | B | C | P]; B at the constant offset kRingBytes, the
+// offsets of C and P computed on the host
 //   ring : per-warp rings of panel blocks (16 x 6 x 1152 B), gate.up then down (Q8_0); during
 //          routing, the CTA's router-weight slice [d][epc] and the tree buffer [epc][256];
 //          NVFP4 down: the CTA's per-warp partials [items][16 warps][256]
@@ -134,14 +164,12 @@ __device__ __forceinline__ WarpRange warp_range(uint32_t U, uint32_t W, uint32_t
 //          CTA's slots [slots][f]
 //   C    : x as f16 hi [d] (+ lo [d] for fp32 inputs) (gate.up)
 //   P    : the per-warp gate.up partials of the CTA's items [cta_items][16 warps][32]
-size_t decode_smem_plan(int wfmt, int d, int f, int k, int xt, int cta_items, int cta_slots, int* off_b, int* off_c,
-                        int* off_p) {
+size_t decode_smem_plan(int wfmt, int d, int f, int k, int xt, int cta_items, int cta_slots, int* off_c, int* off_p) {
     const size_t xb = static_cast<size_t>(d) * 4;
     const size_t hb = (wfmt == MOE_W_Q8_0) ? static_cast<size_t>(k) * f * 4 : static_cast<size_t>(cta_slots) * f * 4;
     const size_t b = xb > hb ? xb : hb;
     const size_t cbytes = static_cast<size_t>(d) * 2 * (xt == MOE_F32 ? 2 : 1);
     const size_t pb = static_cast<size_t>(cta_items) * kDecWarps * 32 * sizeof(float);
-    if (off_b) *off_b = static_cast<int>(kRingBytes);
     if (off_c) *off_c = static_cast<int>(kRingBytes + b);
     if (off_p) *off_p = static_cast<int>(kRingBytes + b + cbytes);
     return kRingBytes + b + cbytes + pb;
@@ -149,7 +177,7 @@ size_t decode_smem_plan(int wfmt, int d, int f, int k, int xt, int cta_items, in
 
 size_t decode_ring_bytes() { return kRingBytes; }
 
-template <int FMT, int ACT>
+template <int FMT, int ACT, bool WIDE>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs a) {
     // Q8_0 with SwiGLU, or NVFP4 with ReLU^2 (gateless latent experts)
     constexpr bool kQ8 = FMT == MOE_W_Q8_0;
@@ -168,7 +196,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     const int d = a.d, f = a.f, E = a.E, k = a.k;
     const uint32_t gw = static_cast<uint32_t>(c * kDecWarps + warp);   // warp index in the grid
     unsigned char* ring = dsm;
-    float* xf = reinterpret_cast<float*>(dsm + a.off_b);
+    // region B starts at a constant offset: its accesses (h in the down phase above all) use
+    // immediate shared-memory addresses, measurably faster than a base passed in the arguments
+    float* xf = reinterpret_cast<float*>(dsm + kRingBytes);
     __half* xh = reinterpret_cast<__half*>(dsm + a.off_c);
     const bool split = a.xt == MOE_F32;
     // the two streaming phases: items, panels per item, units
@@ -268,7 +298,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         // comparisons would cost a CTA microseconds: each routing CTA ranks only its own
         // experts among all E logits and publishes the winners, and after one more grid barrier
         // every CTA reads the k winners.
-        const bool wide = E > kLocalRankMaxE;
+        constexpr bool wide = WIDE;   // the host launches WIDE exactly when E > kLocalRankMaxE
         if (!wide || router)
             for (int e = tid; e < E; e += kDecThreads) slog[e] = __ldcg(a.ws.logits + e);
         // gate.up items this CTA's warps touch, and their per-warp partials [items][16 warps][32]
@@ -284,7 +314,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             s_val[tid] = 0.0f;
         }
         __syncthreads();
-        if (!wide) {
+        if constexpr (!wide) {
             for (int e = tid; e < E; e += kDecThreads) {   // slot = number of experts that beat e
                 const float v = slog[e];
                 const float4* row = reinterpret_cast<const float4*>(slog);
@@ -303,26 +333,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 }
             }
         } else {
-            if (router) {   // tpx threads per own expert, each counting over a share of the E logits
-                const int tpx = kDecThreads / epc;
-                const int j = tid / tpx, part = tid % tpx;
-                const int e = c * epc + j;
-                const float v = slog[e];
-                int r = 0;
-                for (int o = part * E / tpx; o < (part + 1) * E / tpx; ++o) r += beats(slog[o], o, v, e);
-#pragma unroll
-                for (int m = 16; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
-                if (lane == 0) s_cnt[warp] = r;
-                __syncthreads();
-                if (part == 0) {
-                    int rank = 0;
-                    for (int w = j * tpx / 32; w < (j + 1) * tpx / 32; ++w) rank += s_cnt[w];
-                    if (rank < k) {
-                        a.sel[rank] = e;
-                        a.selv[rank] = v;
-                    }
-                }
-            }
+            if (router) rank_own_experts(slog, s_cnt, E, k, epc, c, a.sel, a.selv);
             grid_barrier(a.bar, ++nbar * G, a.ws.err);
             if (tid < k) {
                 s_sel[tid] = __ldcg(a.sel + tid);
@@ -863,15 +874,15 @@ namespace {
 bool g_decode_ok[64] = {};
 int g_decode_ctas[64] = {};
 
-template <int FMT, int ACT>
+template <int FMT, int ACT, bool WIDE>
 bool configure_one() {
     const int max_smem = static_cast<int>(decode_max_smem());
-    if (cudaFuncSetAttribute(decode_layer_kernel<FMT, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(decode_layer_kernel<FMT, ACT, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             max_smem) != cudaSuccess)
         return false;
     int per_sm = 0;
-    const cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel<FMT, ACT>, kDecThreads, max_smem);
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel<FMT, ACT, WIDE>,
+                                                                        kDecThreads, max_smem);
     return e == cudaSuccess && per_sm >= 1;
 }
 }  // namespace
@@ -884,7 +895,8 @@ cudaError_t configure_decode_kernel(int dev, int num_sms) {
     cudaError_t e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     if (e != cudaSuccess) return e;
     if (!coop) return cudaSuccess;
-    if (!configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU>() || !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2>()) {
+    if (!configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, false>() || !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, true>() ||
+        !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, false>() || !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, true>()) {
         (void)cudaGetLastError();
         return cudaSuccess;   // the separate kernels serve every shape
     }
@@ -909,8 +921,12 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, int wfmt, size_t smem, int 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (wfmt == MOE_W_Q8_0) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU>, a);
-    return cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2>, a);
+    const bool wide = a.E > kLocalRankMaxE;
+    if (wfmt == MOE_W_Q8_0)
+        return wide ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, true>, a)
+                    : cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, false>, a);
+    return wide ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, true>, a)
+                : cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, false>, a);
 }
 
 }  // namespace moe
