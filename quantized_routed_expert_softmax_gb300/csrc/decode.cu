@@ -24,9 +24,11 @@
 //      order (256 fma chains i = l (mod 256), then the halving tree); its slice of the
 //      router weights is copied into shared memory before the kernel waits for the
 //      previous one (in a stack: while the previous layer finishes).  Barrier.  With up to
-//      256 experts every CTA then ranks all E logits itself (top-k, lower index on ties);
-//      with more, the routing CTAs rank their own experts and publish the winners behind
-//      one more barrier.
+//      256 experts every CTA then ranks all E logits itself (top-k, lower index on ties;
+//      2 to 8 lanes per expert); with more, the routing CTAs rank their own experts and
+//      publish the winners behind one more barrier (a separate instantiation of the kernel).
+//      The softmax over the selected logits and the routing record follow the first gate.up
+//      requests, which need only the selection.
 //   G  gate.up: the panel products of all k experts (items of 16 gate + 16 up rows, or 32
 //      rows for ReLU^2) are one flattened range split evenly over the warps of the grid, so
 //      every warp streams the same number of panels (within one) whatever the shapes.  A
@@ -315,22 +317,29 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         }
         __syncthreads();
         if constexpr (!wide) {
-            for (int e = tid; e < E; e += kDecThreads) {   // slot = number of experts that beat e
-                const float v = slog[e];
-                const float4* row = reinterpret_cast<const float4*>(slog);
-                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-                for (int q = 0; q < E / 4; ++q) {
-                    const float4 o = row[q];
-                    r0 += beats(o.x, 4 * q, v, e);
-                    r1 += beats(o.y, 4 * q + 1, v, e);
-                    r2 += beats(o.z, 4 * q + 2, v, e);
-                    r3 += beats(o.w, 4 * q + 3, v, e);
-                }
-                const int r = r0 + r1 + r2 + r3;
-                if (r < k) {
-                    s_sel[r] = e;
-                    s_val[r] = v;
-                }
+            // slot = number of experts that beat e, counted by tpe adjacent lanes per expert,
+            // lane p over the float4 groups p, p + tpe, ... (a warp's loads are contiguous, free
+            // of bank conflicts; E * tpe <= 512, E a multiple of 4)
+            const int lg_tpe = E <= 64 ? 3 : (E <= 128 ? 2 : 1);
+            const int tpe = 1 << lg_tpe;
+            const int e = tid >> lg_tpe, part = tid & (tpe - 1);
+            const bool live = e < E;
+            const int nq = live ? E / 4 : 0;
+            const float v = live ? slog[e] : 0.0f;
+            const float4* row = reinterpret_cast<const float4*>(slog);
+            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+            for (int q = part; q < nq; q += tpe) {
+                const float4 o = row[q];
+                r0 += beats(o.x, 4 * q, v, e);
+                r1 += beats(o.y, 4 * q + 1, v, e);
+                r2 += beats(o.z, 4 * q + 2, v, e);
+                r3 += beats(o.w, 4 * q + 3, v, e);
+            }
+            int r = r0 + r1 + r2 + r3;
+            for (int m = 1; m < tpe; m <<= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
+            if (live && part == 0 && r < k) {
+                s_sel[r] = e;
+                s_val[r] = v;
             }
         } else {
             if (router) rank_own_experts(slog, s_cnt, E, k, epc, c, a.sel, a.selv);
@@ -341,22 +350,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             }
         }
         __syncthreads();
-        if (warp == 0) {   // softmax over the k selected logits (slot 0's subtracted, sum in slot order)
-            const int j = lane;
-            const bool live = j < k;
-            const int ej = live ? s_sel[j] : 0;
-            float wj = 0.0f;
-            if (live) {
+        if (warp == 0 && lane < k) {   // sorted slot of pair j: selected experts with a lower index
+            const int ej = s_sel[lane];
+            int r = 0;
+            for (int i = 0; i < k; ++i) r += s_sel[i] < ej;
+            s_e[r] = ej;
+            s_pos[lane] = r;
+        }
+        __syncthreads();
+        // The combine weights and the routing record need only the selection: they are worked
+        // out once the CTA's first gate.up requests are in flight (s_w is next read in the
+        // combine, several CTA barriers later).
+        auto finish_routing = [&]() {
+            if (warp == 0 && lane < k) {   // softmax over the k selected logits (slot 0's subtracted, sum in slot order)
+                const int j = lane, ej = s_sel[j], r = s_pos[j];
                 const float m0 = s_val[0];
                 float sum = 0.0f;
                 for (int i = 0; i < k; ++i) sum += expf(s_val[i] - m0);
-                wj = expf(s_val[j] - m0) / sum;
-            }
-            int r = 0;   // sorted slot: selected experts with a lower index
-            for (int i = 0; i < k; ++i) r += s_sel[i] < ej;
-            if (live) {
-                s_e[r] = ej;
-                s_pos[j] = r;
+                const float wj = expf(s_val[j] - m0) / sum;
                 s_w[j] = wj;
                 if (c == 0 && a.idx_out) {
                     a.idx_out[l * k + j] = ej;
@@ -371,16 +382,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                     a.ws.slot_info[r] = make_int4(ej, r, 1, 0);
                 }
             }
-        }
-        if (c == 0) {
-            for (int e = tid; e <= E; e += kDecThreads) {
-                int n = 0;
-                for (int i = 0; i < k; ++i) n += s_sel[i] < e;
-                a.ws.offsets[e] = n;
+            if (c == 0) {
+                for (int e = tid; e <= E; e += kDecThreads) {
+                    int n = 0;
+                    for (int i = 0; i < k; ++i) n += s_sel[i] < e;
+                    a.ws.offsets[e] = n;
+                }
+                if (tid == 0) *a.ws.n_active = k;
             }
-            if (tid == 0) *a.ws.n_active = k;
-        }
-        __syncthreads();
+        };
 
         // ---------------------------------------------------------------- G: gate.up partial sums
         const uint64_t pol = l2_evict_first_policy();
@@ -406,13 +416,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 off += n;
             }
         };
-        if (rg.n > 0) {
-            const int n = rg.n;
+        {
+            const int n = rg.n;   // 0 for a warp past the split (more warps than units)
             unsigned char* wring = ring + warp * kStages * kSlotBytes;
             const uint32_t ring_addr = smem_addr(wring);
             // the issue pointer as (slot, tile, panel), advanced by increments
             int iss_s = rg.item0 / nt_g, iss_t = rg.item0 % nt_g, iss_b = rg.b0;
-            const uint8_t* iss_w = P.w_gu + static_cast<int64_t>(s_e[iss_s]) * a.gu_bytes;
+            const uint8_t* iss_w = P.w_gu + static_cast<int64_t>(s_e[iss_s < k ? iss_s : 0]) * a.gu_bytes;
             auto issue = [&](int st) {
                 // SwiGLU: gate rows t*16.. and up rows f + t*16..; ReLU^2: rows t*32.. and t*32 + 16..
                 const int rA = iss_t * (kSwiglu ? 16 : 32), rB = kSwiglu ? f + iss_t * 16 : iss_t * 32 + 16;
@@ -431,6 +441,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 cp_async_commit();
             }
             prefetch_down();   // after this warp's first gate.up requests
+            finish_routing();   // while they are in flight
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             int cur_item = rg.item0, cur_b = rg.b0;
             for (int i0 = 0; i0 < n; i0 += kStages) {
@@ -464,8 +475,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 }
             }
             cp_async_wait<0>();
-        } else {
-            prefetch_down();
         }
         // The CTA's record of each item it touched: its warps' partials in warp order (a warp
         // that did not touch the item adds zero), at the CTA's contributor slot of the item.
