@@ -14,7 +14,11 @@ end-to-end figure with host<->device copies inside the timed region, clocks samp
 the timed region and the number of libmoe kernels launched.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload gemma|nemotron|minimax] [--tokens T]
+                  [--workload gemma|nemotron|minimax|zipf|zipf_nvfp4] [--tokens T]
+The zipf workloads are the skewed-routing sweep on the Gemma layer shape (Q8_0 or NVFP4
+experts): the routing is supplied (each token draws k distinct experts with probability
+proportional to rank^-1.1), so the router is skipped, and a stack of 4 layers with their
+own weights keeps the routed experts of one step out of L2 at the next.
 Under torchrun (N > 1) every rank runs its own replica (the layer needs no exchange on
 one GPU); value = tokens of all ranks / the slowest rank's time.
 """
@@ -33,6 +37,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; decode active-expert GB/s vs GB300 HBM roofline"
 N_ROTATE = 8          # distinct token inputs, replayed round robin (no step reuses the last one's experts)
+ZIPF_LAYERS = 4       # layers of the supplied-routing sweep's stack (4 x 50 MB of routed experts at T=1 > L2)
+
+
+def routed(w) -> bool:
+    """The workload supplies its routing (the Zipf sweep) instead of running the router."""
+    return w.name.startswith("zipf")
+
+
+def default_layers(w) -> int:
+    return ZIPF_LAYERS if routed(w) else w.layers
 
 
 def parse():
@@ -93,6 +107,9 @@ def workload_config(w, T, layers):
                     f"{w.x_dtype} activations, {'decode' if T <= 32 else 'prefill'} T={T}",
         "layers": layers, "tokens_per_step": T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "act": w.act,
         "weights": w.wfmt, "activations": w.x_dtype,
+        **({"routing": "supplied (router skipped): k distinct experts per token drawn with probability "
+                       "proportional to rank^-1.1 over a seeded permutation of the experts; weights a softmax of "
+                       "seeded normals; one draw per rotated input, the same for every layer"} if routed(w) else {}),
     }
 
 
@@ -122,7 +139,10 @@ def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0):
             return cache[layer]
         x = synth.tokens(w, tu, layer, tag="cpu")
         W = synth.router_weight(w, layer)
-        idx, _ = oracle.topk_softmax(oracle.router_logits(x, W), w.k)
+        if routed(w):
+            idx, wts = synth.zipf_routing(tu, w.E, w.k, seed_tag=f"cpu{layer}")
+        else:
+            idx, wts = oracle.topk_softmax(oracle.router_logits(x, W), w.k)[0], None
         gu, dn = [None] * w.E, [None] * w.E
         gts, dts = np.ones(w.E, np.float32), np.ones(w.E, np.float32)
         for e in sorted(set(int(v) for v in idx.ravel())):
@@ -138,16 +158,16 @@ def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0):
                 dn[e], dts[e] = oracle.nvfp4_quantize(b)
         L = oracle.Layer(w.d, w.f, w.E, w.k, act, fmt, W, gu, dn,
                          gts if w.wfmt == "nvfp4" else None, dts if w.wfmt == "nvfp4" else None)
-        cache[layer] = (L, x)
+        cache[layer] = (L, x, (idx, wts) if routed(w) else (None, None))
         return cache[layer]
 
     times = []
     units = 0
     spent = 0.0
     while units < max_units + warmup_units and (spent < time_budget_s or units < warmup_units + 1):
-        L, x = layer_obj(units % layers)
+        L, x, (ii, ww) = layer_obj(units % layers)
         t0 = time.perf_counter()
-        L.forward(x)
+        L.forward(x, idx_in=ii, w_in=ww)
         dt = time.perf_counter() - t0
         if units >= warmup_units:
             times.append(dt)
@@ -155,9 +175,10 @@ def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0):
         units += 1
     per_token_layer = statistics.mean(times) / tu
     step_s = per_token_layer * T * layers
-    desc = (f"{len(times)} oracle forwards of single layers of the stack on {tu} token(s) each (router, top-k, "
-            f"softmax, permutation, every routed expert dequantised and evaluated in fp64, combine), cycling over "
-            f"the {layers} layers; per-step time = mean per token-layer x {T} token(s) x {layers} layers")
+    what = ("supplied routing, permutation" if routed(w) else "router, top-k, softmax, permutation")
+    desc = (f"{len(times)} oracle forwards of single layers of the stack on {tu} token(s) each ({what}, every "
+            f"routed expert dequantised and evaluated in fp64, combine), cycling over the {layers} layers; "
+            f"per-step time = mean per token-layer x {T} token(s) x {layers} layers")
     return step_s, len(times), oracle.num_threads(), desc
 
 
@@ -228,9 +249,25 @@ def build_stack(w, T, layers, local_rank):
     return stack, inputs
 
 
-def capture_graphs(stack, inputs, T, w, stage_events=None, stack_obj=None):
+def build_routings(w, T):
+    """Supplied routing per rotated input (device idx [T,k] int32, w [T,k] fp32), or None
+    when the stack routes itself."""
+    import torch
+
+    from quantized_routed_expert_softmax_gb300 import synth
+    if not routed(w):
+        return None
+    out = []
+    for r in range(N_ROTATE):
+        idx, wts = synth.zipf_routing(T, w.E, w.k, seed_tag=f"bench{r}")
+        out.append((torch.from_numpy(idx).cuda(), torch.from_numpy(wts).cuda()))
+    return out
+
+
+def capture_graphs(stack, inputs, T, w, stage_events=None, stack_obj=None, routings=None):
     """One CUDA graph per rotated input; each runs the whole stack (with stack_obj: one
-    moe_stack_forward call; stage_events then holds two events per input, around it)."""
+    moe_stack_forward call; stage_events then holds two events per input, around it).
+    routings: supplied (idx, w) per rotated input, given to every layer."""
     import torch
 
     from quantized_routed_expert_softmax_gb300 import native
@@ -266,18 +303,20 @@ def capture_graphs(stack, inputs, T, w, stage_events=None, stack_obj=None):
     with torch.cuda.stream(s):
         # warm the kernels once outside capture (per-device attribute setup happens here)
         x = inputs[0]
+        ri, rw = routings[0] if routings else (None, None)
         for li, layer in enumerate(stack):
-            layer.forward(x, out=outs[li], workspace=wss[li])
+            layer.forward(x, idx_in=ri, w_in=rw, out=outs[li], workspace=wss[li])
             native.rmsnorm_bf16(outs[li], out=nxt[li])
             x = nxt[li]
         torch.cuda.current_stream().synchronize()
         for g_i, x0 in enumerate(inputs):
             g = torch.cuda.CUDAGraph()
+            ri, rw = routings[g_i] if routings else (None, None)
             with torch.cuda.graph(g, stream=s):
                 x = x0
                 for li, layer in enumerate(stack):
                     ev = None if stage_events is None else stage_events[g_i][li]
-                    layer.forward(x, out=outs[li], workspace=wss[li], stage_events=ev)
+                    layer.forward(x, idx_in=ri, w_in=rw, out=outs[li], workspace=wss[li], stage_events=ev)
                     native.rmsnorm_bf16(outs[li], out=nxt[li])
                     x = nxt[li]
             graphs.append(g)
@@ -296,14 +335,16 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     w = synth.WORKLOADS[args.workload]
     T = args.tokens
-    layers = args.layers or w.layers
+    layers = args.layers or default_layers(w)
     stack, inputs = build_stack(w, T, layers, local_rank)
+    routings = build_routings(w, T)
+    supplied = routings is not None
     # One token on layers the library runs as one kernel per layer: the whole stack as ONE
     # kernel (moe_stack_forward), the RMS-norm between layers inside it.
-    stack_obj = native.MoEStack(stack) if T == 1 else None
+    stack_obj = native.MoEStack(stack) if T == 1 and not supplied else None
     if stack_obj is not None and stack_obj.launches() != 1:
         stack_obj = None
-    graphs, outs = capture_graphs(stack, inputs, T, w, stack_obj=stack_obj)
+    graphs, outs = capture_graphs(stack, inputs, T, w, stack_obj=stack_obj, routings=routings)
 
     def barrier():
         if world > 1:
@@ -329,7 +370,7 @@ def run_ours(args, rank, world, local_rank):
     tokens_per_s = job_throughput(T * args.steps, world, ms_total)
 
     # ---- active-expert bytes of one step (from the routing the stack actually took)
-    tr_bytes = active_expert_bytes(stack, inputs, T, w)
+    tr_bytes = active_expert_bytes(stack, inputs, T, w, routings)
 
     # ---- dominant kernel (gate.up): live CUDA events recorded inside the graphs
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in stack] for _ in inputs]
@@ -377,7 +418,7 @@ def run_ours(args, rank, world, local_rank):
     try:
         if stack_obj is not None:
             raise StopIteration
-        graphs_ev, _ = capture_graphs(stack, inputs, T, w, stage_events=evs)
+        graphs_ev, _ = capture_graphs(stack, inputs, T, w, stage_events=evs, routings=routings)
         for i in range(args.warmup):
             graphs_ev[i % N_ROTATE].replay()
         torch.cuda.synchronize()
@@ -398,9 +439,10 @@ def run_ours(args, rank, world, local_rank):
         outs_e = [torch.empty((T, w.d), dtype=torch.float32, device="cuda") for _ in stack]
         for r in range(N_ROTATE):
             x = inputs[r]
+            ri, rw = routings[r] if routings else (None, None)
             for li, layer in enumerate(stack):
                 lay = evs[r][li]
-                layer.forward(x, out=outs_e[li], workspace=layer.workspace(T), stage_events=lay)
+                layer.forward(x, idx_in=ri, w_in=rw, out=outs_e[li], workspace=layer.workspace(T), stage_events=lay)
                 x = native.rmsnorm_bf16(outs_e[li])
             torch.cuda.synchronize()
             for lay in evs[r]:
@@ -411,7 +453,7 @@ def run_ours(args, rank, world, local_rank):
     # One token on Q8_0 SwiGLU layers runs as ONE kernel per layer (the library reports one
     # launch): then that kernel is the one measured, between the first two boundaries (the
     # later boundaries coincide with the second), with all the layer's bytes as its work.
-    one_kernel = stack[0].launches(T) == 1
+    one_kernel = stack[0].launches(T, supplied) == 1
     peak, peak_src = hbm_peak()
     if stack_obj is not None:   # the one-kernel stack: a launch processes every layer
         gu_ms = list(rt_ms)
@@ -439,18 +481,27 @@ def run_ours(args, rank, world, local_rank):
     tc_achieved = gu_flops / (gu_us * 1e-6) / 1e12
 
     # ---- end to end: host x in pinned memory -> device, the stack, out -> host
+    # (supplied routing is an input of the step too: idx and w are copied with x)
     x_host = [inp.cpu().pin_memory() for inp in inputs]
+    r_host = [(ri.cpu().pin_memory(), rw.cpu().pin_memory()) for ri, rw in routings] if routings else None
     out_host = torch.empty((T, w.d), dtype=torch.float32).pin_memory()
     e2e_steps = max(N_ROTATE, min(args.steps, 500))
+
+    def h2d(r):
+        inputs[r].copy_(x_host[r], non_blocking=True)
+        if r_host:
+            routings[r][0].copy_(r_host[r][0], non_blocking=True)
+            routings[r][1].copy_(r_host[r][1], non_blocking=True)
+
     for i in range(min(args.warmup, 10)):
-        inputs[i % N_ROTATE].copy_(x_host[i % N_ROTATE], non_blocking=True)
+        h2d(i % N_ROTATE)
         graphs[i % N_ROTATE].replay()
         out_host.copy_(outs[-1], non_blocking=True)
     barrier()
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record()
     for i in range(e2e_steps):
-        inputs[i % N_ROTATE].copy_(x_host[i % N_ROTATE], non_blocking=True)
+        h2d(i % N_ROTATE)
         graphs[i % N_ROTATE].replay()
         out_host.copy_(outs[-1], non_blocking=True)
     a1.record()
@@ -459,7 +510,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = job_throughput(T * e2e_steps, world, e2e_ms)
 
     launches_per_step = (1 if stack_obj is not None else
-                         sum(layer.launches(T) + 1 for layer in stack))   # + the RMS-norm glue
+                         sum(layer.launches(T, supplied) + 1 for layer in stack))   # + the RMS-norm glue
     result = None
     if rank == 0:
         step_bytes = tr_bytes["step"]
@@ -467,7 +518,7 @@ def run_ours(args, rank, world, local_rank):
         cfg.update({
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": f"per-step weight working set {step_bytes / 1e9:.2f} GB > 129 MB L2; {N_ROTATE} token inputs "
-                  f"rotate so consecutive steps route to different experts",
+                  f"{'and routings ' if supplied else ''}rotate so consecutive steps route to different experts",
             "graph": "one CUDA graph per rotated input covers the whole stack",
             "layer_us": round(ms_step * 1e3 / layers, 3),
             "layer_tokens_per_s": round(tokens_per_s * layers, 1),
@@ -516,30 +567,34 @@ def run_ours(args, rank, world, local_rank):
                          "bytes_time_us": round(gu_bytes / (peak * 1e9) * 1e6, 2),
                          "flop_time_us": round(gu_flops / (tc_peak * 1e12) * 1e6, 2)},
             "e2e": {"value": round(e2e_value, 2), "unit": f"tokens/s through the {layers}-layer stack",
-                    "h2d_bytes_per_step": int(x_host[0].numel() * x_host[0].element_size()),
+                    "h2d_bytes_per_step": int(x_host[0].numel() * x_host[0].element_size() +
+                                              (sum(t.numel() * t.element_size() for t in r_host[0]) if r_host else 0)),
                     "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()),
-                    "how": "pinned host x -> device copy, graph replay of the stack, out -> pinned host, "
-                           "all on the stream inside the timed region"},
+                    "how": ("pinned host x (and the supplied idx, w) -> device copy, " if supplied else
+                            "pinned host x -> device copy, ") +
+                           "graph replay of the stack, out -> pinned host, all on the stream inside the timed region"},
             "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
         }
     return result, (w, T, layers)
 
 
-def active_expert_bytes(stack, inputs, T, w):
+def active_expert_bytes(stack, inputs, T, w, routings=None):
     """Unique active-expert bytes of one step, from the routing each layer took
-    (gate.up bytes of every selected expert + down bytes of its active groups)."""
+    (gate.up bytes of every selected expert + down bytes of its active groups).  The router
+    weights count toward a layer's launch only when the layer runs its router."""
     import torch
 
     from quantized_routed_expert_softmax_gb300 import native
     gu_b = stack[0].gate_up.shape[1]
     dn_b = stack[0].down.shape[1]
     x = inputs[0]
+    ri, rw = routings[0] if routings else (None, None)
     step = 0
     gu_layer, layer_bytes = [], []
     for layer in stack:
         tr = {}
-        out = layer.forward(x, trace=tr)
+        out = layer.forward(x, idx_in=ri, w_in=rw, trace=tr)
         experts = torch.unique(tr["idx"]).numel()
         gu_layer.append(experts * gu_b)
         if w.act == "relu2":   # the down projection reads only 16-neuron groups with a non-zero h
@@ -554,7 +609,7 @@ def active_expert_bytes(stack, inputs, T, w):
         else:
             expert_bytes = experts * (gu_b + dn_b)
         step += expert_bytes
-        layer_bytes.append(expert_bytes + layer.router_w.numel() * 4)
+        layer_bytes.append(expert_bytes + (0 if routings else layer.router_w.numel() * 4))
         x = native.rmsnorm_bf16(out)
     torch.cuda.synchronize()
     return {"step": int(step), "gate_up_per_layer": int(statistics.mean(gu_layer)),
@@ -586,7 +641,7 @@ def run_reference(args, rank, world):
     from quantized_routed_expert_softmax_gb300 import synth
     w = synth.WORKLOADS[args.workload]
     T = args.tokens
-    layers = args.layers or w.layers
+    layers = args.layers or default_layers(w)
     budget = 120.0
     t0 = time.perf_counter()
     step_s, n, threads, desc = oracle_sample(w, T, layers, max_units=max(1, args.steps),
