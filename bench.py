@@ -538,8 +538,10 @@ def run_ours(args, rank, world, local_rank):
                                    "one cooperative launch per step (one CTA per SM)")
             cfg["graph"] = "one CUDA graph per rotated input holds the single stack launch"
         elif one_kernel:
-            cfg["layer_kernel"] = ("decode_layer_kernel: router, top-k, softmax, gate.up + SwiGLU, down and combine "
-                                   "in one cooperative launch per layer (one CTA per SM)")
+            cfg["layer_kernel"] = (("decode_layer_kernel with the supplied routing: gate.up + activation, down and "
+                                    "combine" if supplied else
+                                    "decode_layer_kernel: router, top-k, softmax, gate.up + activation, down and combine")
+                                   + " in one cooperative launch per layer (one CTA per SM)")
         result = {
             "metric": METRIC, "value": round(tokens_per_s, 2), "unit": f"tokens/s through the {layers}-layer stack",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -549,8 +551,8 @@ def run_ours(args, rank, world, local_rank):
             "roofline": {"bound": "hbm",
                          "kernel": ("decode_layer_kernel (the whole stack in one launch: every layer's routed "
                                     "experts' gate.up + down bytes and router weights)" if stack_obj is not None else
-                                    "decode_layer_kernel (the whole layer: routed experts' gate.up + down "
-                                    "bytes and the router weights)" if one_kernel else
+                                    ("decode_layer_kernel (the whole layer: routed experts' gate.up + down "
+                                     "bytes" + (")" if supplied else " and the router weights)")) if one_kernel else
                                     "expert_gemm_kernel (gate.up + activation, tcgen05)" if gemm
                                     else "gate_up_gemv (gate.up + activation + group mask)"),
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

@@ -88,11 +88,12 @@ typedef enum { MOE_LAYOUT_CANONICAL = 0, MOE_LAYOUT_DEVICE = 1, MOE_LAYOUT_NEURO
  * kernels (a few tokens per expert).  GEMM: grouped GEMMs on the tensor cores (tcgen05),
  * which need f a multiple of 64 (128 for ReLU^2); forcing GEMM on another shape returns
  * MOE_ERR_UNSUPPORTED.  AUTO takes GEMM when T*k >= 8*E and the shape allows it; for ONE
- * token with Q8_0 SwiGLU (k*f <= 16384) or NVFP4 ReLU^2 experts and routing computed by the
- * call (d <= 8192) it runs the whole layer as a single cooperative kernel, one CTA per SM,
- * when the device supports cooperative launches (the same results within the output
- * tolerance; routing, weights and the permutation bit-identical).  GEMV keeps the separate
- * kernels. */
+ * token with Q8_0 SwiGLU (k*f <= 16384) or NVFP4 ReLU^2 experts (d <= 8192) it runs the whole
+ * layer as a single cooperative kernel, one CTA per SM, when the device supports cooperative
+ * launches (the same results within the output tolerance; routing, weights and the
+ * permutation bit-identical).  With supplied routing that kernel skips the router and the
+ * selection; an expert repeated in idx_in takes one slot per pair, in pair order, as in the
+ * other paths.  GEMV keeps the separate kernels. */
 typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GEMM = 2 } moe_path;
 
 /* Bytes of one quantised matrix: rows*cols/32*34 (Q8_0), rows*cols/2 + rows*cols/16

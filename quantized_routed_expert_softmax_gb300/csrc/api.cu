@@ -547,14 +547,16 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
 
     mark(0);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    // One token, routing computed here: the whole layer as one cooperative kernel when the
-    // device and the shape allow it.
-    if (p.decode1 && !idx_in) {
+    // One token: the whole layer as one cooperative kernel when the device and the shape allow
+    // it (with supplied routing the kernel skips the router and the selection).
+    if (p.decode1) {
         DecodeArgs a{};
         int ctas = 0;
         size_t smem = 0;
         if (fill_decode_args(desc, 1, x, xt, workspace, L, ws, &a, &ctas, &smem)) {
             a.out = out;
+            a.idx_in = idx_in;
+            a.w_in = w_in;
             e = launch_decode_layer(a, desc->wfmt, smem, ctas, s);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
             for (int i = 1; i <= 4; ++i) mark(i);   // one kernel: the inner boundaries coincide
@@ -644,7 +646,7 @@ int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_
     if (validate_desc(desc) != MOE_OK || T < 0 || T > kMaxTokens) return -1;
     if (T == 0) return 0;
     const Plan p = make_plan(desc, T);
-    if (p.decode1 && !routing_supplied) {   // the one-kernel decode layer, when this device runs it
+    if (p.decode1) {   // the one-kernel decode layer, when this device runs it
         int num_sms = 0, dev = 0;
         if (ensure_configured(&num_sms) == cudaSuccess && cudaGetDevice(&dev) == cudaSuccess &&
             decode_epc(desc->E, decode_ctas(dev)) > 0 &&

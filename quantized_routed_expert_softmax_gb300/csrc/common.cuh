@@ -116,6 +116,8 @@ struct DecodeArgs {
     float* drec;                 // [k * d/32][cov_d][32] (Q8_0) or [k * d/256][cov_d][256] (NVFP4) down
                                  //   partial sums per item and contributor
     DecodeLayerPtrs lp[kMaxStackLayers];
+    const int32_t* idx_in;       // supplied routing [k] and weights [k] (one layer), or null: routed here
+    const float* w_in;
 };
 
 // Programmatic dependent launch: wait for the preceding kernel's memory, and allow the

@@ -62,6 +62,10 @@ constexpr int kDevErrTimeout = 2;
 constexpr long long kWaitLimitNs = 1000000000ll;   // bounded waits: one second
 constexpr size_t kRingBytes = static_cast<size_t>(kDecWarps) * kStages * kSlotBytes;
 constexpr int kLocalRankMaxE = 256;   // up to this many experts every CTA ranks all logits itself
+// Routing modes of the kernel (a template parameter: each kernel holds only its own code)
+constexpr int kRouteLocal = 0;      // router, then every CTA ranks all E <= 256 logits
+constexpr int kRouteWide = 1;       // router, then the routing CTAs rank their own experts (E > 256)
+constexpr int kRouteSupplied = 2;   // the caller's idx / w (one layer): no router, no selection
 
 __device__ __forceinline__ long long globaltimer() {
     long long t;
@@ -179,10 +183,11 @@ size_t decode_smem_plan(int wfmt, int d, int f, int k, int xt, int cta_items, in
 
 size_t decode_ring_bytes() { return kRingBytes; }
 
-template <int FMT, int ACT, bool WIDE>
+template <int FMT, int ACT, int ROUTE>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs a) {
     // Q8_0 with SwiGLU, or NVFP4 with ReLU^2 (gateless latent experts)
     constexpr bool kQ8 = FMT == MOE_W_Q8_0;
+    constexpr bool kSupplied = ROUTE == kRouteSupplied;
     constexpr bool kSwiglu = ACT == MOE_ACT_SWIGLU;
     constexpr int kNeur = kSwiglu ? 16 : 32;   // neurons per gate.up item (16 gate + 16 up rows, or 32 rows)
     extern __shared__ __align__(16) unsigned char dsm[];
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     float* red = wsl + d * epc;                     // [epc][256]
     // this CTA's slice of a layer's router weights, copied asynchronously into the ring region
     auto request_router = [&](const float* W) {
-        if (!router) return;
+        if (kSupplied || !router) return;
         const float* src = W + c * epc;
         const uint32_t wb = smem_addr(wsl);
         for (int it = tid; it < d * epc; it += kDecThreads) {
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         const bool split_l = l == 0 && split;   // later layers read bf16 inputs: one f16 term
         cp_async_wait<0>();
         __syncthreads();
-        if (router) {
+        if (!kSupplied && router) {
             if (tid < kRouterPartials) {   // chain l: fmaf over i = l, l + 256, ... in increasing i
                 float acc[8];
 #pragma unroll
@@ -292,7 +297,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 if (lane == 0) a.ws.logits[c * epc + warp] = v;
             }
         }
-        grid_barrier(a.bar, ++nbar * G, a.ws.err);
+        if constexpr (!kSupplied) grid_barrier(a.bar, ++nbar * G, a.ws.err);
         if (l == 0) pdl_trigger();   // every CTA is resident: the next kernel may be scheduled
 
         // ---------------------------------------------------------------- R: top-k, weights, slots
@@ -300,8 +305,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         // comparisons would cost a CTA microseconds: each routing CTA ranks only its own
         // experts among all E logits and publishes the winners, and after one more grid barrier
         // every CTA reads the k winners.
-        constexpr bool wide = WIDE;   // the host launches WIDE exactly when E > kLocalRankMaxE
-        if (!wide || router)
+        constexpr bool wide = ROUTE == kRouteWide;   // launched exactly when E > kLocalRankMaxE
+        if (!kSupplied && (!wide || router))
             for (int e = tid; e < E; e += kDecThreads) slog[e] = __ldcg(a.ws.logits + e);
         // gate.up items this CTA's warps touch, and their per-warp partials [items][16 warps][32]
         const uint32_t wc0 = min(static_cast<uint32_t>(c * kDecWarps), static_cast<uint32_t>(a.warps_g));
@@ -316,7 +321,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             s_val[tid] = 0.0f;
         }
         __syncthreads();
-        if constexpr (!wide) {
+        if constexpr (kSupplied) {
+            // the caller's selection, pair j in slot j; an index outside [0, E) is clamped and
+            // recorded as device error 1, as in the other paths
+            if (tid < k) {
+                int e = a.idx_in[tid];
+                if (e < 0 || e >= E) {
+                    if (c == 0) set_error(a.ws.err, kDevErrBadExpert);
+                    e = min(max(e, 0), E - 1);
+                }
+                s_sel[tid] = e;
+            }
+        } else if constexpr (!wide) {
             // slot = number of experts that beat e, counted by tpe adjacent lanes per expert,
             // lane p over the float4 groups p, p + tpe, ... (a warp's loads are contiguous, free
             // of bank conflicts; E * tpe <= 512, E a multiple of 4)
@@ -353,7 +369,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         if (warp == 0 && lane < k) {   // sorted slot of pair j: selected experts with a lower index
             const int ej = s_sel[lane];
             int r = 0;
-            for (int i = 0; i < k; ++i) r += s_sel[i] < ej;
+            if constexpr (kSupplied) {   // an expert the caller repeats takes one slot per pair, in pair order
+                for (int i = 0; i < k; ++i) r += s_sel[i] < ej || (s_sel[i] == ej && i < lane);
+            } else {
+                for (int i = 0; i < k; ++i) r += s_sel[i] < ej;
+            }
             s_e[r] = ej;
             s_pos[lane] = r;
         }
@@ -364,10 +384,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         auto finish_routing = [&]() {
             if (warp == 0 && lane < k) {   // softmax over the k selected logits (slot 0's subtracted, sum in slot order)
                 const int j = lane, ej = s_sel[j], r = s_pos[j];
-                const float m0 = s_val[0];
-                float sum = 0.0f;
-                for (int i = 0; i < k; ++i) sum += expf(s_val[i] - m0);
-                const float wj = expf(s_val[j] - m0) / sum;
+                float wj;
+                if constexpr (kSupplied) {
+                    wj = a.w_in[j];
+                } else {
+                    const float m0 = s_val[0];
+                    float sum = 0.0f;
+                    for (int i = 0; i < k; ++i) sum += expf(s_val[i] - m0);
+                    wj = expf(s_val[j] - m0) / sum;
+                }
                 s_w[j] = wj;
                 if (c == 0 && a.idx_out) {
                     a.idx_out[l * k + j] = ej;
@@ -883,14 +908,14 @@ namespace {
 bool g_decode_ok[64] = {};
 int g_decode_ctas[64] = {};
 
-template <int FMT, int ACT, bool WIDE>
+template <int FMT, int ACT, int ROUTE>
 bool configure_one() {
     const int max_smem = static_cast<int>(decode_max_smem());
-    if (cudaFuncSetAttribute(decode_layer_kernel<FMT, ACT, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_layer_kernel<FMT, ACT, ROUTE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              max_smem) != cudaSuccess)
         return false;
     int per_sm = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel<FMT, ACT, WIDE>,
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel<FMT, ACT, ROUTE>,
                                                                         kDecThreads, max_smem);
     return e == cudaSuccess && per_sm >= 1;
 }
@@ -904,8 +929,12 @@ cudaError_t configure_decode_kernel(int dev, int num_sms) {
     cudaError_t e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     if (e != cudaSuccess) return e;
     if (!coop) return cudaSuccess;
-    if (!configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, false>() || !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, true>() ||
-        !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, false>() || !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, true>()) {
+    if (!configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteLocal>() ||
+        !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteWide>() ||
+        !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteSupplied>() ||
+        !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteLocal>() ||
+        !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteWide>() ||
+        !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteSupplied>()) {
         (void)cudaGetLastError();
         return cudaSuccess;   // the separate kernels serve every shape
     }
@@ -930,12 +959,19 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, int wfmt, size_t smem, int 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const bool wide = a.E > kLocalRankMaxE;
-    if (wfmt == MOE_W_Q8_0)
-        return wide ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, true>, a)
-                    : cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, false>, a);
-    return wide ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, true>, a)
-                : cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, false>, a);
+    const int route = a.idx_in ? kRouteSupplied : (a.E > kLocalRankMaxE ? kRouteWide : kRouteLocal);
+    if (wfmt == MOE_W_Q8_0) {
+        if (route == kRouteSupplied)
+            return cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteSupplied>, a);
+        return route == kRouteWide
+                   ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteWide>, a)
+                   : cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteLocal>, a);
+    }
+    if (route == kRouteSupplied)
+        return cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteSupplied>, a);
+    return route == kRouteWide
+               ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteWide>, a)
+               : cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteLocal>, a);
 }
 
 }  // namespace moe

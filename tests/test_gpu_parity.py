@@ -259,6 +259,58 @@ def test_one_token_one_kernel(name):
     assert_close(L.forward(x).cpu().numpy(), ref["out"])
 
 
+# Supplied routing at one token: the same kernel without the router and the selection.  The
+# trace copies idx and w exactly; the permutation follows them bit for bit; h and out agree
+# with the oracle and with the separate kernels on the same routing.
+@pytest.mark.parametrize("name", ["tiny_f32", "k1", "k8_e64", "k32_e1024", "nv_k6_e32", "nv_k22_e512_f32"])
+def test_one_token_one_kernel_supplied_routing(name):
+    w = ONE_KERNEL[name]
+    idx, wts = synth.zipf_routing(1, w.E, w.k, seed_tag="one-kernel")
+    L, out, tr, ref = _run_small(w, 1, idx_in=idx, w_in=wts)
+    assert L.launches(1, routing_supplied=True) == 1
+    assert np.array_equal(tr["idx"].cpu().numpy(), idx)
+    assert np.array_equal(tr["w"].cpu().numpy().view(np.uint32), wts.view(np.uint32))
+    assert np.array_equal(tr["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(tr["pos"].cpu().numpy(), ref["pos"])
+    assert_close(tr["h"].cpu().numpy(), ref["h"][ref["perm"]], what="h")
+    assert_close(out, ref["out"])
+    assert L.device_status() == 0
+    x = torch.from_numpy(synth.tokens(w, 1, tag="parity")).cuda()
+    if w.x_dtype == "bf16":
+        x = x.view(torch.bfloat16)
+    ii, ww = torch.from_numpy(idx).cuda(), torch.from_numpy(wts).cuda()
+    o = torch.full((1, w.d), float("nan"), device="cuda")
+    L.forward(x, idx_in=ii, w_in=ww, out=o)
+    assert np.array_equal(o.cpu().numpy().view(np.uint32), out.view(np.uint32))   # deterministic, fully written
+    L.set_path("gemv")
+    assert L.launches(1, routing_supplied=True) > 1
+    assert_close(L.forward(x, idx_in=ii, w_in=ww).cpu().numpy(), ref["out"])
+
+
+# An expert repeated in the supplied routing takes one slot per pair (pair order), and an index
+# outside [0, E) is clamped and reported as device error 1, in the one-kernel layer as in the
+# separate kernels.
+def test_one_token_one_kernel_repeated_and_bad_experts():
+    w = ONE_KERNEL["k8_e64"]
+    rep = np.array([[5, 40, 5, 63, 0, 5, 17, 40]], dtype=np.int32)
+    wts = np.array([[0.05, 0.1, 0.15, 0.2, 0.05, 0.25, 0.1, 0.1]], dtype=np.float32)
+    L, out, tr, ref = _run_small(w, 1, idx_in=rep, w_in=wts)
+    assert L.launches(1, routing_supplied=True) == 1
+    assert np.array_equal(tr["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(tr["pos"].cpu().numpy(), ref["pos"])
+    assert_close(tr["h"].cpu().numpy(), ref["h"][ref["perm"]], what="h")
+    assert_close(out, ref["out"])
+    assert L.device_status() == 0
+    x = torch.from_numpy(synth.tokens(w, 1, tag="parity")).cuda().view(torch.bfloat16)
+    bad = np.array([[5, 40, 5, 999, -7, 5, 17, 40]], dtype=np.int32)   # 999 -> 63, -7 -> 0
+    o_bad = L.forward(x, idx_in=torch.from_numpy(bad).cuda(), w_in=torch.from_numpy(wts).cuda())
+    assert L.device_status() == 1
+    assert L.device_status() == 0
+    assert np.array_equal(o_bad.cpu().numpy().view(np.uint32), out.view(np.uint32))
+
+
 def test_one_token_repeated_expert_in_supplied_routing():
     w = SMALL["tiny_q8_swiglu"]
     idx = np.array([[3, 3]], dtype=np.int32)
