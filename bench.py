@@ -470,7 +470,7 @@ def run_ours(args, rank, world, local_rank):
         gu_bytes = tr_bytes["gate_up_per_layer"]
         gu_flops = 2 * T * w.k * w.rows_gu * w.d                # useful gate.up FLOP per layer
     achieved = gu_bytes / (gu_us * 1e-6) / 1e9
-    traffic = measured_traffic(args.workload, T)
+    traffic = measured_traffic(args.workload, T, layers) if (stack_obj is not None or not one_kernel) else None
     # Which expert kernels run (the library's AUTO rule): the tensor-core GEMMs when an expert
     # sees at least 8 tokens on average and the shape allows them, else the GEMVs.
     gemm = (T * w.k >= 8 * w.E and w.f % 64 == 0 and (w.act == "swiglu" or w.f % 128 == 0))
@@ -625,9 +625,11 @@ def kernel_source_sha(files=("gemv.cu", "gemm.cu", "common.cuh", "decode.cu", "g
     return hashlib.sha1(blob).hexdigest()[:12]
 
 
-def measured_traffic(workload, T):
+def measured_traffic(workload, T, layers):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, while the
-    kernel's own source files (the entry's "sources") are unchanged since the capture; else None."""
+    kernel's own source files (the entry's "sources") are unchanged since the capture; else None.
+    An entry for a whole-stack launch (it names its "layers") scales to this run's stack depth:
+    every layer of a stack moves the same bytes."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         entry = json.load(open(p)).get(f"{workload}_T{T}")
@@ -635,6 +637,8 @@ def measured_traffic(workload, T):
         return None
     if not entry or entry.get("source_sha1_12") != kernel_source_sha(tuple(entry.get("sources", ()))):
         return None
+    if "layers" in entry:
+        return int(round(entry["bytes"] * layers / entry["layers"]))
     return entry.get("bytes")
 
 
