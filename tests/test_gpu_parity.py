@@ -450,11 +450,13 @@ def test_minimax_layer_prefill_4096_sampled():
     _full_case("minimax", 4096, sample=[0, 2047, 4095])
 
 
-@pytest.mark.parametrize("name,T", [("zipf", 64), ("zipf", 2048), ("zipf_nvfp4", 2048)])
+# The skewed-routing sweep's sizes up to its largest, T = 8192 (65,536 pairs; the hottest
+# expert gets about a fifth of the tokens)
+@pytest.mark.parametrize("name,T", [("zipf", 64), ("zipf", 2048), ("zipf_nvfp4", 2048), ("zipf", 8192)])
 def test_zipf_routing_full_size(name, T):
     w = synth.WORKLOADS[name]
     idx, wts = synth.zipf_routing(T, w.E, w.k)
-    _full_case(name, T, sample=[0, 17, T - 1], idx_in=idx, w_in=wts)
+    _full_case(name, T, sample=[0, 17, T // 2 + 1, T - 1], idx_in=idx, w_in=wts)
 
 
 # ------------------------------------------------------------------ a stack of layers, one token
