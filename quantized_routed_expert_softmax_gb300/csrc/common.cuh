@@ -74,16 +74,17 @@ struct ExpertArgs {
     Workspace ws;
 };
 
-// Arguments of the one-kernel decode layer (decode.cu): one token, Q8_0 SwiGLU experts, one
-// layer or a stack of layers of the same shape (the next layer's input is the RMS-normalised
-// output of the previous one).  The kernel's own control words and partial sums sit in the
-// layer workspace too.
+// Arguments of the one-kernel decode layer (decode.cu): one token, Q8_0 SwiGLU or NVFP4 ReLU^2
+// experts, one layer or a stack of layers of the same shape (the next layer's input is the
+// RMS-normalised output of the previous one), routed in the kernel or (one layer) by the
+// caller's idx / w.  The kernel's own control words and partial sums sit in the layer
+// workspace too.
 constexpr int kMaxStackLayers = 64;
 
 struct DecodeLayerPtrs {
     const float* W;              // router [d][E]
-    const uint8_t* w_gu;         // gate/up matrices of the E experts (Q8_0, device layout)
-    const uint8_t* w_dn;         // down matrices
+    const uint8_t* w_gu;         // gate/up matrices of the E experts (Q8_0 device layout, or NVFP4 panels)
+    const uint8_t* w_dn;         // down matrices (Q8_0 device layout, or NVFP4 neuron-contiguous)
     const uint8_t* pf;           // L2 hint (the next layer's router weights), or null
     int64_t pf_bytes;
     const float* gu_ts;          // NVFP4 tensor scales [E] of the gate/up and down matrices
@@ -116,6 +117,7 @@ struct DecodeArgs {
     float* drec;                 // [k * d/32][cov_d][32] (Q8_0) or [k * d/256][cov_d][256] (NVFP4) down
                                  //   partial sums per item and contributor
     DecodeLayerPtrs lp[kMaxStackLayers];
+    // last, so that the offsets of the fields above (and the routed kernels' code) stay as they were
     const int32_t* idx_in;       // supplied routing [k] and weights [k] (one layer), or null: routed here
     const float* w_in;
 };
