@@ -77,6 +77,7 @@ def _declare(L: ctypes.CDLL) -> None:
         "orc_nvfp4_bytes": (_I64, [_I64, _I64]),
         "orc_q8_0_quantize": (None, [_P, _I64, _I64, _P]),
         "orc_q8_0_dequant": (None, [_P, _I64, _I64, _P]),
+        "orc_q8_0_vec_dot": (ctypes.c_double, [_P, _P, _I64]),
         "orc_q8_0_permute": (None, [_P, _I64, _I64, _I, _P]),
         "orc_nvfp4_tensor_scale": (ctypes.c_float, [_P, _I64, _I64]),
         "orc_nvfp4_quantize": (None, [_P, _I64, _I64, _P, _P]),
@@ -90,6 +91,7 @@ def _declare(L: ctypes.CDLL) -> None:
         "orc_silu": (ctypes.c_double, [ctypes.c_double]),
         "orc_fused_mul_silu": (None, [_P, _P, _I64, _P]),
         "orc_layer_forward": (_I, [_P, _P, _I, _I64, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+        "orc_layer_forward_ex": (_I, [_P, _P, _I, _I64, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "orc_layer_forward_dense_experts": (None, [_P, _P, _I, _I64, _P, _P]),
     }
     for name, (res, args) in sig.items():
@@ -164,6 +166,16 @@ def q8_0_dequant(q: np.ndarray, rows: int, cols: int) -> np.ndarray:
     out = np.empty((rows, cols), dtype=np.float64)
     lib().orc_q8_0_dequant(_ptr(q), rows, cols, _ptr(out))
     return out
+
+
+def q8_0_vec_dot(a: np.ndarray, b: np.ndarray) -> float:
+    """orc_q8_0_vec_dot: the activation-quantised dot product of two rows given as canonical
+    Q8_0 bytes (the same number of blocks each)."""
+    a = np.ascontiguousarray(a, dtype=np.uint8).ravel()
+    b = np.ascontiguousarray(b, dtype=np.uint8).ravel()
+    if a.size != b.size or a.size % 34:
+        raise ValueError("q8_0_vec_dot: two rows of whole Q8_0 blocks of equal length")
+    return float(lib().orc_q8_0_vec_dot(_ptr(a), _ptr(b), a.size // 34))
 
 
 def q8_0_to_device(canon: np.ndarray, rows: int, cols: int) -> np.ndarray:
@@ -320,9 +332,11 @@ class Layer:
                       _ptr(self.gate_up_tscale), _ptr(self.down_tscale))
         return s, (gu, dn)
 
-    def forward(self, x: np.ndarray, idx_in=None, w_in=None, sparse_down: bool = True) -> dict:
-        """orc_layer_forward: returns logits (when routed here), idx, w, offsets, perm, pos,
-        h [T*k, f] and y [T*k, d] in pair order, and out [T, d] (fp64)."""
+    def forward(self, x: np.ndarray, idx_in=None, w_in=None, sparse_down: bool = True, act_q8: bool = False) -> dict:
+        """orc_layer_forward_ex: returns logits (when routed here), idx, w, offsets, perm, pos,
+        h [T*k, f] and y [T*k, d] in pair order, and out [T, d] (fp64).  act_q8: the
+        activation-quantised expert path (each expert input quantised to Q8_0 blocks, then
+        Q8_0 x Q8_0 block dots; Q8_0 weights and f a multiple of 32 only)."""
         xa, xt = _x_arg(x)
         T = xa.shape[0]
         k, E, d, f = self.k, self.E, self.d, self.f
@@ -337,11 +351,13 @@ class Layer:
         ii = None if idx_in is None else np.ascontiguousarray(idx_in, np.int32)
         ww = None if w_in is None else np.ascontiguousarray(w_in, np.float32)
         s, keep = self._struct()
-        rc = lib().orc_layer_forward(ctypes.byref(s), _ptr(xa), xt, T, _ptr(ii), _ptr(ww), int(sparse_down),
-                                     _ptr(res["logits"]), _ptr(res["idx"]), _ptr(res["w"]), _ptr(res["offsets"]),
-                                     _ptr(res["perm"]), _ptr(res["pos"]), _ptr(res["h"]), _ptr(res["y"]),
-                                     _ptr(res["out"]))
+        rc = lib().orc_layer_forward_ex(ctypes.byref(s), _ptr(xa), xt, T, _ptr(ii), _ptr(ww), int(sparse_down),
+                                        int(act_q8), _ptr(res["logits"]), _ptr(res["idx"]), _ptr(res["w"]),
+                                        _ptr(res["offsets"]), _ptr(res["perm"]), _ptr(res["pos"]), _ptr(res["h"]),
+                                        _ptr(res["y"]), _ptr(res["out"]))
         del keep
+        if rc == -2:
+            raise ValueError("oracle: the activation-quantised path needs Q8_0 weights and f a multiple of 32")
         if rc != 0:
             raise ValueError("oracle: routing selected an expert whose weights were not supplied")
         return res

@@ -28,6 +28,10 @@
  *     a fixed order); Xeon page, section "A three-step fix", "Runtime graph fallback"
  *     (the [n_embd, 2*n_ff, n_experts] gate-first/up-second tensor split into two
  *     expert-indexed matmuls and a fused SiLU-multiply).
+ *   - The activation-quantised Q8_0 path of the CPU engines (orc_layer_forward_ex with
+ *     act_q8): each expert input quantised with the same Q8_0 codec, then Q8_0 x Q8_0
+ *     block dots with exact integer code sums (Xeon page, "A three-step fix" and
+ *     "Narrowing down the cause", which name the activation quantisers and the vector dot).
  *
  * Accumulation is fp64 throughout the expert path; quantisation decisions and router
  * logits are taken in fp32, the precision the method fixes for them.
@@ -220,6 +224,27 @@ void orc_q8_0_dequant(const uint8_t* q, int64_t rows, int64_t cols, double* out)
             for (int i = 0; i < 32; ++i) out[r * cols + b * 32 + i] = (double)(int8_t)blk[2 + i] * d;
         }
     }
+}
+
+/* Q8_0 x Q8_0 dot product of two rows of nb canonical blocks each: the CPU engines'
+ * activation-quantised path.  The Xeon page names its pieces: the Q8_0 / Q8_1 activation
+ * quantisers its non-AVX2 fix rewrites (section "A three-step fix") and the Q8_0 x Q8_0
+ * vector dot it checks (section "Narrowing down the cause").  It does not spell out the
+ * arithmetic, so the plain reading is taken.  Per block, the 32 code products are summed
+ * exactly as integers and scaled by both fp16 scales; the blocks are summed in fp64.  Each
+ * block term is exact in fp64: at most 11 + 11 + 19 significant bits. */
+double orc_q8_0_vec_dot(const uint8_t* a, const uint8_t* b, int64_t nb) {
+    double acc = 0.0;
+    for (int64_t i = 0; i < nb; ++i) {
+        const uint8_t* ba = a + i * 34;
+        const uint8_t* bb = b + i * 34;
+        int32_t s = 0;
+        for (int j = 0; j < 32; ++j) s += (int32_t)(int8_t)ba[2 + j] * (int32_t)(int8_t)bb[2 + j];
+        const double da = orc_f16_to_f64((uint16_t)(ba[0] | (ba[1] << 8)));
+        const double db = orc_f16_to_f64((uint16_t)(bb[0] | (bb[1] << 8)));
+        acc += da * db * (double)s;
+    }
+    return acc;
 }
 
 /* Device layout for Q8_0: a byte permutation of the canonical blocks, panel by panel
@@ -554,6 +579,37 @@ static void expert_down(const double* Wd, int64_t d, int64_t f, const double* h,
     free(active);
 }
 
+/* The activation-quantised expert (Q8_0 weights only).  The expert's input vector (x for
+ * gate.up; h, held in fp32, for down) is quantised with the same Q8_0 block codec as the
+ * weights.  Every weight row is then dotted with it by orc_q8_0_vec_dot.  An all-zero
+ * 16-neuron group of h quantises to zero codes, so the down projection needs no separate
+ * skip: its terms are exact zeros. */
+static void expert_q8act(int act, const uint8_t* Wgu, const uint8_t* Wd, int64_t f, int64_t d, const float* x,
+                         double* h, double* y) {
+    const int64_t nbd = d / 32, nbf = f / 32;
+    uint8_t* xq = (uint8_t*)malloc((size_t)(nbd * 34));
+    uint8_t* hq = (uint8_t*)malloc((size_t)(nbf * 34));
+    float* hf = (float*)malloc((size_t)f * sizeof(float));
+    orc_q8_0_quantize(x, 1, d, xq);
+    for (int64_t n = 0; n < f; ++n) {
+        if (act == ORC_ACT_SWIGLU) {
+            const double g = orc_q8_0_vec_dot(Wgu + n * nbd * 34, xq, nbd);
+            const double u = orc_q8_0_vec_dot(Wgu + (f + n) * nbd * 34, xq, nbd);
+            h[n] = orc_silu(g) * u;
+        } else {
+            const double z = orc_q8_0_vec_dot(Wgu + n * nbd * 34, xq, nbd);
+            const double r = z > 0.0 ? z : 0.0;
+            h[n] = r * r;
+        }
+        hf[n] = (float)h[n];
+    }
+    orc_q8_0_quantize(hf, 1, f, hq);
+    for (int64_t r = 0; r < d; ++r) y[r] = orc_q8_0_vec_dot(Wd + r * nbf * 34, hq, nbf);
+    free(xq);
+    free(hq);
+    free(hf);
+}
+
 /* ------------------------------------------------------------------------------------
  * The layer.
  * ------------------------------------------------------------------------------------ */
@@ -572,15 +628,19 @@ typedef struct {
  *   pos [T*k], h [T*k][f] in pair order, y [T*k][d] in pair order, out [T][d] double.
  * idx_in / w_in: precomputed routing (both or neither); the router is skipped.
  * sparse_down: 1 = skip all-zero 16-neuron groups, 0 = dense down.
- * Returns 0, or -1 when an expert needed by the routing has no weights. */
-int orc_layer_forward(const orc_layer* L, const void* x, int xt, int64_t T, const int32_t* idx_in,
-                      const float* w_in, int sparse_down, float* logits_out, int32_t* idx_out, double* w_out,
-                      int32_t* offsets_out, int32_t* perm_out, int32_t* pos_out, double* h_out, double* y_out,
-                      double* out) {
+ * act_q8: 1 = the activation-quantised expert path (expert_q8act; Q8_0 weights, f a
+ * multiple of 32), 0 = activations used as they are.
+ * Returns 0, -1 when an expert needed by the routing has no weights, -2 when act_q8 is
+ * asked of another format or shape. */
+int orc_layer_forward_ex(const orc_layer* L, const void* x, int xt, int64_t T, const int32_t* idx_in,
+                         const float* w_in, int sparse_down, int act_q8, float* logits_out, int32_t* idx_out,
+                         double* w_out, int32_t* offsets_out, int32_t* perm_out, int32_t* pos_out, double* h_out,
+                         double* y_out, double* out) {
     const int64_t d = L->d, f = L->f, E = L->E;
     const int k = L->k;
     const int64_t P = T * k;
     const int64_t rows_gu = (L->act == ORC_ACT_SWIGLU) ? 2 * f : f;
+    if (act_q8 && (L->wfmt != ORC_W_Q8_0 || f % 32 != 0)) return -2;
 
     int32_t* idx = idx_out ? idx_out : (int32_t*)malloc((size_t)P * sizeof(int32_t));
     double* w = w_out ? w_out : (double*)malloc((size_t)P * sizeof(double));
@@ -610,8 +670,10 @@ int orc_layer_forward(const orc_layer* L, const void* x, int xt, int64_t T, cons
     for (int64_t e = 0; e < E; ++e) {
         const int64_t r0 = offsets[e], r1 = offsets[e + 1];
         if (r0 == r1) continue;
-        dequant_matrix(L->wfmt, L->gate_up[e], rows_gu, d, L->gate_up_tscale ? L->gate_up_tscale[e] : 1.0f, Wgu);
-        dequant_matrix(L->wfmt, L->down[e], d, f, L->down_tscale ? L->down_tscale[e] : 1.0f, Wd);
+        if (!act_q8) {
+            dequant_matrix(L->wfmt, L->gate_up[e], rows_gu, d, L->gate_up_tscale ? L->gate_up_tscale[e] : 1.0f, Wgu);
+            dequant_matrix(L->wfmt, L->down[e], d, f, L->down_tscale ? L->down_tscale[e] : 1.0f, Wd);
+        }
 #pragma omp parallel
         {
             float* xrow = (float*)malloc((size_t)d * sizeof(float));
@@ -621,8 +683,12 @@ int orc_layer_forward(const orc_layer* L, const void* x, int xt, int64_t T, cons
                 const int64_t p = perm[r];
                 const int64_t t = p / k;
                 load_x_row(x, xt, d, t, xrow);
-                for (int64_t c = 0; c < d; ++c) xd[c] = (double)xrow[c];
                 double* h = hbuf + p * f;
+                if (act_q8) {
+                    expert_q8act(L->act, L->gate_up[e], L->down[e], f, d, xrow, h, y + p * d);
+                    continue;
+                }
+                for (int64_t c = 0; c < d; ++c) xd[c] = (double)xrow[c];
                 expert_gate_up(L->act, Wgu, f, d, xd, h);
                 expert_down(Wd, d, f, h, sparse_down, y + p * d);
             }
@@ -652,6 +718,14 @@ int orc_layer_forward(const orc_layer* L, const void* x, int xt, int64_t T, cons
     if (!perm_out) free(perm);
     if (!pos_out) free(pos);
     return 0;
+}
+
+int orc_layer_forward(const orc_layer* L, const void* x, int xt, int64_t T, const int32_t* idx_in,
+                      const float* w_in, int sparse_down, float* logits_out, int32_t* idx_out, double* w_out,
+                      int32_t* offsets_out, int32_t* perm_out, int32_t* pos_out, double* h_out, double* y_out,
+                      double* out) {
+    return orc_layer_forward_ex(L, x, xt, T, idx_in, w_in, sparse_down, 0, logits_out, idx_out, w_out, offsets_out,
+                                perm_out, pos_out, h_out, y_out, out);
 }
 
 /* The "DenseExperts" form (Inferentia page, "Honest caveats"): every expert is

@@ -565,3 +565,100 @@ def test_relu2_bias_channel_gives_the_page_zero_fraction():
     res = L.forward(x, idx_in=idx, w_in=np.full((16, 2), 0.5, np.float32))
     frac = float((res["h"] == 0).mean())
     assert abs(frac - 0.925) < 0.015, frac
+
+
+# ------------------------------------------------------------------ activation-quantised Q8_0
+# The CPU engines' Q8_0 x Q8_0 path (Xeon page, "A three-step fix" and "Narrowing down the
+# cause"): the expert's input vector is quantised with the same Q8_0 block codec as the
+# weights, and each weight row is dotted with it block by block: exact integer code sums,
+# both fp16 scales.  Pinned below by definitions written from the codec alone.
+def test_q8_0_vec_dot_is_the_dot_of_the_dequantised_rows():
+    g = np.random.default_rng(11)
+    for cols in (32, 256, 2816):
+        a = oracle.q8_0_quantize((g.standard_normal((1, cols)) * 0.02).astype(np.float32))
+        b = oracle.q8_0_quantize(g.standard_normal((1, cols)).astype(np.float32))
+        da, db = oracle.q8_0_dequant(a, 1, cols)[0], oracle.q8_0_dequant(b, 1, cols)[0]
+        terms = da * db                       # each exact in fp64
+        got = oracle.q8_0_vec_dot(a, b)
+        assert abs(got - math.fsum(terms)) <= 1e-13 * np.abs(terms).sum()
+
+
+def test_q8_0_vec_dot_closed_forms():
+    nb = 4
+    ones = oracle.q8_0_quantize(np.full((1, 32 * nb), 1.0, np.float32))
+    twos = oracle.q8_0_quantize(np.full((1, 32 * nb), 2.0, np.float32))
+    # constant blocks code to +127 with the fp16 of amax/127 as scale
+    s1 = oracle.f16_bits_to_f64(oracle.f32_to_f16_bits(np.float32(1.0) / np.float32(127.0)))
+    s2 = oracle.f16_bits_to_f64(oracle.f32_to_f16_bits(np.float32(2.0) / np.float32(127.0)))
+    assert oracle.q8_0_vec_dot(ones, twos) == nb * 32 * 127 * 127 * s1 * s2
+    # alternating signs against a constant: every block's integer sum is zero
+    alt = np.tile(np.array([1.0, -1.0], np.float32), 16 * nb)[None]
+    assert oracle.q8_0_vec_dot(ones, oracle.q8_0_quantize(alt)) == 0.0
+    # a zero activation block has scale 0 and codes 0
+    zero = oracle.q8_0_quantize(np.zeros((1, 32 * nb), np.float32))
+    assert oracle.q8_0_vec_dot(ones, zero) == 0.0
+    # one block of x against e_i picks the weight's code i times both scales
+    x = np.zeros((1, 32), np.float32)
+    x[0, 5] = 3.0
+    w = (np.arange(32, dtype=np.float32) - 16.0)[None] * 0.01
+    qw, qx = oracle.q8_0_quantize(w), oracle.q8_0_quantize(x)
+    sw = oracle.f16_bits_to_f64(int(qw[0]) | (int(qw[1]) << 8))
+    sx = oracle.f16_bits_to_f64(int(qx[0]) | (int(qx[1]) << 8))
+    assert oracle.q8_0_vec_dot(qw, qx) == float(np.int8(qw[2 + 5])) * 127 * sw * sx
+
+
+def test_q8_0_activation_quantisation_error_bound():
+    """|dot(Q(w), Q(x)) - dot(deq(Q(w)), x)| is bounded by the codec: each element of x is
+    off by at most d/2 (rounding with the fp32 scale d) plus 127 |d - fp16(d)| (the stored
+    scale), with d = amax(block)/127."""
+    g = np.random.default_rng(12)
+    cols = 1024
+    for trial in range(5):
+        w = (g.standard_normal((1, cols)) * 0.02).astype(np.float32)
+        x = (g.standard_normal((1, cols)) * (10.0 ** (trial - 2))).astype(np.float32)
+        qw, qx = oracle.q8_0_quantize(w), oracle.q8_0_quantize(x)
+        dw = oracle.q8_0_dequant(qw, 1, cols)[0]
+        exact = math.fsum(dw * x[0].astype(np.float64))
+        bound = 0.0
+        for b in range(cols // 32):
+            blk = x[0, 32 * b: 32 * b + 32]
+            d = np.float32(np.abs(blk).max()) / np.float32(127.0)
+            dh = oracle.f16_bits_to_f64(oracle.f32_to_f16_bits(d))
+            e = float(d) / 2 + 127 * abs(float(d) - dh) + 1e-7 * float(d)
+            bound += np.abs(dw[32 * b: 32 * b + 32]).sum() * e
+        err = abs(oracle.q8_0_vec_dot(qw, qx) - exact)
+        assert err <= bound, (trial, err, bound)
+        assert err > 0.0   # the activations really are quantised
+
+
+def test_activation_quantised_layer_composes_the_pinned_pieces():
+    """The layer with act_q8: x quantised per token, gate/up by block dots, SwiGLU in fp64,
+    h rounded to fp32 and quantised, down by block dots, the fixed-order combine.  Rebuilt
+    here from the pinned codec (quantise, dequantise) and plain numpy dots."""
+    w, L = _tiny_layer()
+    T = 6
+    x = synth.tokens(w, T)
+    idx, wts = synth.zipf_routing(T, L.E, L.k, seed_tag="q8act")
+    res = L.forward(x, idx_in=idx, w_in=wts, act_q8=True)
+    gu, dn = _dequant_all(L)
+    out = np.zeros((T, L.d))
+    for t in range(T):
+        xq = oracle.q8_0_dequant(oracle.q8_0_quantize(x[t][None].astype(np.float32)), 1, L.d)[0]
+        for j in range(L.k):
+            e = int(idx[t, j])
+            z = gu[e] @ xq
+            g_, u_ = z[: L.f], z[L.f:]
+            h = g_ / (1 + np.exp(-g_)) * u_
+            hq = oracle.q8_0_dequant(oracle.q8_0_quantize(h.astype(np.float32)[None]), 1, L.f)[0]
+            out[t] += float(wts[t, j]) * (dn[e] @ hq)
+    assert np.allclose(res["out"], out, rtol=1e-9, atol=1e-12 * np.abs(out).max())
+    # against the float-activation layer: the same routing, close but not equal
+    ref = L.forward(x, idx_in=idx, w_in=wts)
+    rel = np.abs(res["out"] - ref["out"]).max() / np.sqrt((ref["out"] ** 2).mean())
+    assert 0.0 < rel < 0.05, rel
+
+
+def test_activation_quantised_path_refuses_nvfp4():
+    w, L = _tiny_layer(act="relu2", wfmt="nvfp4")
+    with pytest.raises(ValueError):
+        L.forward(synth.tokens(w, 2), act_q8=True)
