@@ -99,6 +99,11 @@ def test_layer_validation(L):
         assert F(ctypes.byref(desc), FAKE, 0, 16, None, None, FAKE, FAKE, need, None, None) == want
     # routing supplied half-way, bad dtype, misaligned x
     assert F(ctypes.byref(ok), FAKE, 0, 16, FAKE, None, FAKE, FAKE, need, None, None) == 1
+    assert F(ctypes.byref(ok), FAKE, 0, 16, None, FAKE, FAKE, FAKE, need, None, None) == 1
+    # supplied routing must be 16-byte aligned, at one token (the one-kernel layer) and more
+    for T in (1, 16):
+        assert F(ctypes.byref(ok), FAKE, 0, T, FAKE + 4, FAKE, FAKE, FAKE, need, None, None) == 3
+        assert F(ctypes.byref(ok), FAKE, 0, T, FAKE, FAKE + 8, FAKE, FAKE, need, None, None) == 3
     assert F(ctypes.byref(ok), FAKE, 3, 16, None, None, FAKE, FAKE, need, None, None) == 1
     assert F(ctypes.byref(ok), FAKE + 2, 0, 16, None, None, FAKE, FAKE, need, None, None) == 3
     # workspace: missing, misaligned, too small
