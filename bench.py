@@ -114,13 +114,14 @@ def workload_config(w, T, layers):
 
 
 # ====================================================================== oracle timing
-def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0):
+def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0, cache=None):
     """Time the CPU oracle on a bounded sample of the workload.
 
     A unit is the oracle's forward of one layer of the stack (router, top-k, softmax,
     permutation, every routed expert: dequantise + gate.up + activation + down, combine;
     fp64) on up to 8 of the step's tokens.  Units cycle through the stack's layers; the
-    experts a layer routes to are drawn and quantised once (untimed) and cached.
+    experts a layer routes to are drawn and quantised once (untimed) and cached (in `cache`
+    when given, so that a second sample reuses them).
     Returns (seconds per stack step, units timed, threads, description)."""
     import numpy as np
     import torch
@@ -132,7 +133,7 @@ def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0):
     act = oracle.ACT_SWIGLU if w.act == "swiglu" else oracle.ACT_RELU2
     fmt = oracle.W_Q8_0 if w.wfmt == "q8_0" else oracle.W_NVFP4
     tu = min(T, 8)
-    cache = {}
+    cache = {} if cache is None else cache
 
     def layer_obj(layer):
         if layer in cache:
@@ -180,6 +181,24 @@ def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0):
             f"routed expert dequantised and evaluated in fp64, combine), cycling over the {layers} layers; "
             f"per-step time = mean per token-layer x {T} token(s) x {layers} layers")
     return step_s, len(times), oracle.num_threads(), desc
+
+
+def single_core_baseline(w, T, layers, threads_all, cache):
+    """The same oracle sample on one thread (about 8 s of timed work), then the oracle's
+    thread count restored.  A failure here is recorded, never raised: the bench line stands."""
+    import oracle
+    try:
+        oracle.set_num_threads(1)
+        step_s, n, _, _ = oracle_sample(w, T, layers, max_units=4 * layers, time_budget_s=8.0, warmup_units=1,
+                                        cache=cache)
+        return {"value": round(T / step_s, 6), "cores": 1, "units_timed": n}
+    except Exception as exc:
+        return {"error": f"{type(exc).__name__}: {exc}"}
+    finally:
+        try:
+            oracle.set_num_threads(threads_all)
+        except Exception:
+            pass
 
 
 # ====================================================================== GPU arm
@@ -686,10 +705,12 @@ def main():
     result, (w, T, layers) = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
+            cache = {}
             step_s, n, threads, desc = oracle_sample(w, T, layers, max_units=10 * layers, time_budget_s=15.0,
-                                                     warmup_units=1)
+                                                     warmup_units=1, cache=cache)
             result["cpu_baseline"] = {"value": round(T / step_s, 6), "unit": result["unit"], "cores": threads,
-                                      "kind": "oracle", "sample": desc}
+                                      "kind": "oracle", "sample": desc,
+                                      "single_core": single_core_baseline(w, T, layers, threads, cache)}
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist

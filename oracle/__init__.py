@@ -67,6 +67,7 @@ _I = ctypes.c_int
 def _declare(L: ctypes.CDLL) -> None:
     sig = {
         "orc_num_threads": (_I, []),
+        "orc_set_num_threads": (None, [_I]),
         "orc_f32_to_f16": (ctypes.c_uint16, [ctypes.c_float]),
         "orc_f16_to_f64": (ctypes.c_double, [ctypes.c_uint16]),
         "orc_f32_to_e4m3": (ctypes.c_uint8, [ctypes.c_float]),
@@ -109,6 +110,11 @@ def _ptr(a: np.ndarray | None):
 
 def num_threads() -> int:
     return int(lib().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on."""
+    lib().orc_set_num_threads(int(n))
 
 
 # ----------------------------------------------------------------------------- codecs

@@ -58,6 +58,15 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads of the parallel loops from now on (n >= 1); a no-op without OpenMP. */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------------------
  * Rounding to a small binary float format.
  *

@@ -51,3 +51,27 @@ def test_measured_traffic_is_null_once_the_kernel_changed(tmp_path, monkeypatch)
     })
     monkeypatch.setattr(bench, "kernel_source_sha", lambda files=(): "123456789abc")
     assert bench.measured_traffic("gemma", 1, 30) is None
+
+
+def test_single_core_baseline_restores_the_thread_count():
+    import oracle
+    w = synth.WORKLOADS["tiny"]
+    cache = {}
+    step_s, n, threads, _ = bench.oracle_sample(w, 16, 1, max_units=3, time_budget_s=1.0, warmup_units=1,
+                                                cache=cache)
+    assert n >= 1 and step_s > 0 and 0 in cache      # the layer's experts were quantised once
+    one = bench.single_core_baseline(w, 16, 1, threads, cache)
+    assert one["cores"] == 1 and one["value"] > 0, one
+    assert oracle.num_threads() == threads
+
+
+def test_single_core_baseline_records_a_failure(monkeypatch):
+    import oracle
+    threads = oracle.num_threads()
+
+    def boom(*a, **k):
+        raise RuntimeError("planted")
+    monkeypatch.setattr(bench, "oracle_sample", boom)
+    got = bench.single_core_baseline(synth.WORKLOADS["tiny"], 16, 1, threads, {})
+    assert got == {"error": "RuntimeError: planted"}
+    assert oracle.num_threads() == threads
