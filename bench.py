@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -215,7 +216,8 @@ class ClockSampler:
         except Exception:
             pass
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the samples only feed the summary in the JSON line: a scratch file suffices
+        self.path = os.path.join(tempfile.gettempdir(), f"moe_bench_clocks_{os.getpid()}_rank{gpu_index}.csv")
         self.fh = None
 
     def start(self):
