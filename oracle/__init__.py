@@ -25,6 +25,7 @@ ACT_SWIGLU = 0
 ACT_RELU2 = 1
 W_Q8_0 = 0
 W_NVFP4 = 1
+W_INT8PC = 2    # per-channel int8: codes row-major, then one fp32 scale per row
 
 
 def build_oracle(force: bool = False) -> str:
@@ -76,6 +77,9 @@ def _declare(L: ctypes.CDLL) -> None:
         "orc_e2m1_to_f64": (ctypes.c_double, [ctypes.c_uint8]),
         "orc_q8_0_bytes": (_I64, [_I64, _I64]),
         "orc_nvfp4_bytes": (_I64, [_I64, _I64]),
+        "orc_int8pc_bytes": (_I64, [_I64, _I64]),
+        "orc_int8pc_quantize": (None, [_P, _I64, _I64, _P]),
+        "orc_int8pc_dequant": (None, [_P, _I64, _I64, _P]),
         "orc_q8_0_quantize": (None, [_P, _I64, _I64, _P]),
         "orc_q8_0_dequant": (None, [_P, _I64, _I64, _P]),
         "orc_q8_0_vec_dot": (ctypes.c_double, [_P, _P, _I64]),
@@ -145,6 +149,26 @@ def e2m1_to_f64(c: int) -> float:
 # ----------------------------------------------------------------------------- sizes
 def q8_0_bytes(rows: int, cols: int) -> int:
     return int(lib().orc_q8_0_bytes(rows, cols))
+
+
+def int8pc_bytes(rows: int, cols: int) -> int:
+    return int(lib().orc_int8pc_bytes(rows, cols))
+
+
+def int8pc_quantize(src: np.ndarray) -> np.ndarray:
+    """orc_int8pc_quantize of one fp32 matrix [rows][cols]: per-channel int8 bytes."""
+    src = np.ascontiguousarray(src, dtype=np.float32)
+    rows, cols = src.shape
+    out = np.empty(int8pc_bytes(rows, cols), dtype=np.uint8)
+    lib().orc_int8pc_quantize(_ptr(src), rows, cols, _ptr(out))
+    return out
+
+
+def int8pc_dequant(q: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    out = np.empty((rows, cols), dtype=np.float64)
+    lib().orc_int8pc_dequant(_ptr(q), rows, cols, _ptr(out))
+    return out
 
 
 def nvfp4_bytes(rows: int, cols: int) -> int:

@@ -28,6 +28,8 @@
  *     a fixed order); Xeon page, section "A three-step fix", "Runtime graph fallback"
  *     (the [n_embd, 2*n_ff, n_experts] gate-first/up-second tensor split into two
  *     expert-indexed matmuls and a fused SiLU-multiply).
+ *   - Per-channel int8 experts (one fp32 scale per output row): Inferentia page ("Squeezing
+ *     a 26B MoE onto the cheapest Inferentia instance"), section "Wall 1: the memory math".
  *   - The activation-quantised Q8_0 path of the CPU engines (orc_layer_forward_ex with
  *     act_q8): each expert input quantised with the same Q8_0 codec, then Q8_0 x Q8_0
  *     block dots with exact integer code sums (Xeon page, "A three-step fix" and
@@ -49,6 +51,7 @@
 #define ORC_ACT_RELU2 1
 #define ORC_W_Q8_0 0
 #define ORC_W_NVFP4 1
+#define ORC_W_INT8PC 2
 
 int orc_num_threads(void) {
 #ifdef _OPENMP
@@ -189,6 +192,7 @@ static float bf16_to_f32(uint16_t b) {
  * ------------------------------------------------------------------------------------ */
 int64_t orc_q8_0_bytes(int64_t rows, int64_t cols) { return rows * (cols / 32) * 34; }
 int64_t orc_nvfp4_bytes(int64_t rows, int64_t cols) { return rows * cols / 2 + rows * cols / 16; }
+int64_t orc_int8pc_bytes(int64_t rows, int64_t cols) { return rows * cols + 4 * rows; }
 
 /* ------------------------------------------------------------------------------------
  * Q8_0.  Canonical byte layout: blocks in row-major order, each block = fp16 scale
@@ -232,6 +236,42 @@ void orc_q8_0_dequant(const uint8_t* q, int64_t rows, int64_t cols, double* out)
             double d = orc_f16_to_f64((uint16_t)(blk[0] | (blk[1] << 8)));
             for (int i = 0; i < 32; ++i) out[r * cols + b * 32 + i] = (double)(int8_t)blk[2 + i] * d;
         }
+    }
+}
+
+/* ------------------------------------------------------------------------------------
+ * Per-channel int8 (Inferentia page, "Wall 1: the memory math": the experts quantised
+ * to int8 with one scale per output channel, numerically on par with fp32 for that model).
+ * The page gives no recipe, so the plainest one is taken:
+ *   s = amax(row) / 127 (fp32, one per row); q = roundf(x / s), half away from zero;
+ *   an all-zero row has s = 0 and q = 0.
+ * Bytes: the rows x cols codes row-major, then the rows' fp32 scales (little endian).
+ * ------------------------------------------------------------------------------------ */
+void orc_int8pc_quantize(const float* src, int64_t rows, int64_t cols, uint8_t* dst) {
+    uint8_t* sb = dst + rows * cols;   /* the scales: byte offsets, no alignment assumed */
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* x = src + r * cols;
+        float amax = 0.0f;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float a = fabsf(x[c]);
+            if (a > amax) amax = a;
+        }
+        const float sc = amax / 127.0f;
+        for (int64_t c = 0; c < cols; ++c)
+            dst[r * cols + c] = (uint8_t)(int8_t)(sc != 0.0f ? roundf(x[c] / sc) : 0.0f);
+        memcpy(sb + 4 * r, &sc, sizeof(float));
+    }
+}
+
+/* Exact dequantisation: q * s in double. */
+void orc_int8pc_dequant(const uint8_t* q, int64_t rows, int64_t cols, double* out) {
+    const uint8_t* sb = q + rows * cols;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        float sc;
+        memcpy(&sc, sb + 4 * r, sizeof(float));
+        for (int64_t c = 0; c < cols; ++c) out[r * cols + c] = (double)(int8_t)q[r * cols + c] * (double)sc;
     }
 }
 
@@ -512,6 +552,7 @@ void orc_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* offse
  * ------------------------------------------------------------------------------------ */
 static void dequant_matrix(int wfmt, const uint8_t* q, int64_t rows, int64_t cols, float tscale, double* out) {
     if (wfmt == ORC_W_Q8_0) orc_q8_0_dequant(q, rows, cols, out);
+    else if (wfmt == ORC_W_INT8PC) orc_int8pc_dequant(q, rows, cols, out);
     else orc_nvfp4_dequant(q, rows, cols, tscale, out);
 }
 

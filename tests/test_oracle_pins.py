@@ -662,3 +662,71 @@ def test_activation_quantised_path_refuses_nvfp4():
     w, L = _tiny_layer(act="relu2", wfmt="nvfp4")
     with pytest.raises(ValueError):
         L.forward(synth.tokens(w, 2), act_q8=True)
+
+
+# ------------------------------------------------------------------ per-channel int8 (NEXT-4)
+# Inferentia page, 'Wall 1: the memory math': the experts quantised to int8 with one scale per
+# output channel.  The page gives no recipe; the oracle takes s = amax(row)/127 in fp32 and
+# q = round(x/s), half away from zero, and stores the codes row-major, then the fp32 scales.
+def test_int8_per_channel_bytes_match_page():
+    w = synth.WORKLOADS["gemma"]
+    params = w.layers * w.E * (w.rows_gu * w.d + w.d * w.f)
+    assert abs(params * 2 / 2 / 1e9 - page("gemma_bf16_experts_gb_per_core_tp2")) < 0.05   # bf16, two cores
+    per_expert = oracle.int8pc_bytes(w.rows_gu, w.d) + oracle.int8pc_bytes(w.d, w.f)
+    assert per_expert == (w.rows_gu * w.d + w.d * w.f) + 4 * (w.rows_gu + w.d)
+    per_rank = w.layers * w.E * per_expert / 2
+    assert abs(per_rank / 1e9 - page("gemma_int8_experts_gb_per_rank")) / page("gemma_int8_experts_gb_per_rank") < 0.01
+
+
+def test_int8_per_channel_hand_rows():
+    m = np.array([[0.0, 0.0, 0.0, 0.0],           # all zero: scale 0, codes 0
+                  [0.3, 0.3, -0.3, 0.3],          # constant magnitude: codes +-127
+                  [127.0, 2.5, -2.5, 0.5],        # scale exactly 1: half-way values round away
+                  [127.0, -0.49, 63.5, -126.5]], np.float32)
+    q = oracle.int8pc_quantize(m)
+    codes = q[:16].view(np.int8).reshape(4, 4)
+    scales = q[16:].view(np.float32)
+    assert (codes[0] == 0).all() and scales[0] == 0.0
+    assert list(codes[1]) == [127, 127, -127, 127] and scales[1] == np.float32(0.3) / np.float32(127.0)
+    assert list(codes[2]) == [127, 3, -3, 1] and scales[2] == 1.0
+    assert list(codes[3]) == [127, 0, 64, -127] and scales[3] == 1.0
+    assert np.array_equal(oracle.int8pc_dequant(q, 4, 4), codes.astype(np.float64) * scales[:, None].astype(np.float64))
+
+
+def test_int8_per_channel_scale_is_per_row_and_error_bound():
+    g = np.random.default_rng(21)
+    m = (g.standard_normal((16, 704)) * np.logspace(-3, 1, 16)[:, None]).astype(np.float32)
+    q = oracle.int8pc_quantize(m)
+    scales = q[16 * 704:].view(np.float32).astype(np.float64)
+    amax = np.abs(m).max(axis=1)
+    assert np.array_equal(scales.astype(np.float32), (amax / np.float32(127.0)).astype(np.float32))
+    err = np.abs(oracle.int8pc_dequant(q, 16, 704) - m.astype(np.float64))
+    assert (err <= scales[:, None] * (0.5 + 1e-6)).all()
+    # a per-tensor scale would leave the small rows with almost no resolution
+    assert (err.max(axis=1) <= amax / 127 * 0.5 * (1 + 1e-6)).all()
+
+
+def test_int8_per_channel_layer_brute_force():
+    """The layer over per-channel int8 experts against a numpy evaluation from the
+    dequantised weights (the same expert arithmetic as the other formats)."""
+    w = synth.Workload("int8pc", d=256, f=512, E=8, k=2, act="swiglu", wfmt="q8_0", x_dtype="f32", layers=1,
+                       rms_norm_input=False)
+    gu, dn = [], []
+    for e in range(w.E):
+        a, b = synth.expert_weights(w, 0, e)
+        gu.append(oracle.int8pc_quantize(a))
+        dn.append(oracle.int8pc_quantize(b))
+    L = oracle.Layer(w.d, w.f, w.E, w.k, oracle.ACT_SWIGLU, oracle.W_INT8PC, synth.router_weight(w), gu, dn)
+    x = synth.tokens(w, 8)
+    res = L.forward(x)
+    lg = res["logits"].astype(np.float64)
+    out = np.zeros((8, w.d))
+    for t in range(8):
+        order = np.lexsort((np.arange(w.E), -lg[t]))[: w.k]
+        sm = np.exp(lg[t, order] - lg[t, order].max())
+        sm /= sm.sum()
+        for j, e in enumerate(order):
+            z = oracle.int8pc_dequant(gu[e], 2 * w.f, w.d) @ x[t].astype(np.float64)
+            h = z[: w.f] / (1 + np.exp(-z[: w.f])) * z[w.f:]
+            out[t] += sm[j] * (oracle.int8pc_dequant(dn[e], w.d, w.f) @ h)
+    assert np.allclose(res["out"], out, rtol=1e-9, atol=1e-12 * np.abs(out).max())
