@@ -205,8 +205,10 @@ size_t moe_layer_workspace_bytes(const moe_layer_desc* desc, int64_t T_max);
  * and a fixed-order combine (no atomics: bitwise deterministic run to run).
  * x          device [T][d], fp32 or bf16 (xt).
  * idx_in     device int32 [T][k] precomputed routing, or NULL; w_in device fp32 [T][k]
- *            (both or neither).  Entries outside [0, E) are clamped to a valid expert
- *            and recorded as device error 1 (see moe_get_device_status).
+ *            (both or neither; each 16-byte aligned, else ALIGNMENT).  Entries outside
+ *            [0, E) are clamped to a valid expert and recorded as device error 1 (see
+ *            moe_get_device_status).  An expert repeated within a token's k entries is
+ *            evaluated once per entry.
  * out        device fp32 [T][d] (written).
  * workspace  device, at least moe_layer_workspace_bytes(desc, T) bytes, 256-byte
  *            aligned, zero-filled before its first use (the library leaves its control
