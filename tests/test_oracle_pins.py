@@ -730,3 +730,25 @@ def test_int8_per_channel_layer_brute_force():
             h = z[: w.f] / (1 + np.exp(-z[: w.f])) * z[w.f:]
             out[t] += sm[j] * (oracle.int8pc_dequant(dn[e], w.d, w.f) @ h)
     assert np.allclose(res["out"], out, rtol=1e-9, atol=1e-12 * np.abs(out).max())
+
+
+def test_oracle_results_do_not_depend_on_the_thread_count():
+    """Xeon page, 'Clues in the garbled output' and 'Narrowing down the cause': single- and
+    multi-thread runs are byte-identical.
+    Every oracle output is computed by one thread in a fixed order, so the thread count of
+    its parallel loops must not change a bit of the result (codecs and the layer)."""
+    threads = oracle.num_threads()
+    w, L = _tiny_layer()
+    x = synth.tokens(w, 12)
+    m = (np.random.default_rng(31).standard_normal((96, 2816)) * 0.02).astype(np.float32)
+    runs = []
+    try:
+        for n in (1, 2, max(threads, 3)):
+            oracle.set_num_threads(n)
+            r = L.forward(x)
+            q8 = oracle.q8_0_quantize(m)
+            nv, _ = oracle.nvfp4_quantize(m)
+            runs.append((r["out"].tobytes(), r["h"].tobytes(), r["idx"].tobytes(), q8.tobytes(), nv.tobytes()))
+    finally:
+        oracle.set_num_threads(threads)
+    assert runs[0] == runs[1] == runs[2]
