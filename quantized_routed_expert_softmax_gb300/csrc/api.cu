@@ -242,7 +242,9 @@ struct Layout {
 };
 
 // Workspace regions for T tokens (each 256-byte aligned).  The control words (err,
-// route_ctr, row_ctr) come first; they must be zero before a call and are left zero.
+// route_ctr, the one-kernel layer's two barrier counters, row_ctr) come first, at offsets
+// that do not depend on T: they must be zero before a call and are left zero, so one
+// workspace serves calls of any token count in any order.
 Layout layout_for(const moe_layer_desc* d, int64_t T) {
     const Plan p = make_plan(d, T);
     Layout L{};
@@ -255,6 +257,7 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     L.err = 0;
     L.route_ctr = 4;
     L.n_active = 8;
+    L.dec_bar = 16;   // [2]: grid-barrier arrivals, CTAs finished (one-kernel layer)
     off = 256;
     L.row_ctr = take(sizeof(int32_t) * (d->d / 32));
     L.logits = take(sizeof(float) * T * d->E);
@@ -282,7 +285,6 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     const bool dec = p.decode1;
     // (sized for the most CTAs any device can give the kernel: more CTAs, more records per item)
     const DecodeSplit sp = decode_split(d, kMaxDecodeCtas);
-    L.dec_bar = take(dec ? sizeof(int32_t) * 2 : 0);
     L.dec_sel = take(dec ? sizeof(int32_t) * 2 * kMaxK : 0);
     L.dec_grec = take(dec ? sizeof(float) * 32 * (sp.U_g / sp.npan_g) * sp.cov_g : 0);
     L.dec_drec = take(dec ? sizeof(float) * sp.rec_d * sp.items_d * sp.cov_d : 0);

@@ -311,6 +311,26 @@ def test_one_token_one_kernel_repeated_and_bad_experts():
     assert np.array_equal(o_bad.cpu().numpy().view(np.uint32), out.view(np.uint32))
 
 
+# One workspace serves calls of any token count in any order: its control words (the one-kernel
+# layer's barrier counters among them) sit at offsets that do not depend on T, so a one-token
+# call after a 16-token call (whose activations fill the bytes a one-token layout places later)
+# starts from clean counters.
+def test_one_workspace_serves_calls_of_any_token_count():
+    w = SMALL["tiny_q8_swiglu"]
+    L = layers.build_layer(w, source="numpy")
+    x = torch.from_numpy(synth.tokens(w, 16, tag="mixed")).cuda()
+    fresh16 = layers.build_layer(w, source="numpy").forward(x).cpu().numpy()
+    fresh1 = layers.build_layer(w, source="numpy").forward(x[:1].contiguous()).cpu().numpy()
+    assert L.launches(1) == 1
+    ws = L.workspace(16)
+    for _ in range(2):
+        o16 = L.forward(x, workspace=ws).cpu().numpy()
+        o1 = L.forward(x[:1].contiguous(), workspace=ws).cpu().numpy()
+        assert np.array_equal(o16.view(np.uint32), fresh16.view(np.uint32))
+        assert np.array_equal(o1.view(np.uint32), fresh1.view(np.uint32))
+    assert L.device_status() == 0
+
+
 def test_one_token_repeated_expert_in_supplied_routing():
     w = SMALL["tiny_q8_swiglu"]
     idx = np.array([[3, 3]], dtype=np.int32)
