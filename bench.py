@@ -14,7 +14,11 @@ end-to-end figure with host<->device copies inside the timed region, clocks samp
 the timed region and the number of libmoe kernels launched.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload gemma|nemotron|minimax|zipf|zipf_nvfp4] [--tokens T]
+                  [--workload gemma|nemotron|minimax|zipf|zipf_nvfp4] [--tokens T] [--no-secondary]
+The default run adds a "secondary" list to the line: Gemma-shaped prefill (T = 512) on the
+headline stack's weights, the 40-layer Nemotron-shaped NVFP4 stack at one token, and
+MiniMax-shaped prefill (T = 4096, 8 layers), each with its own config, roofline and oracle
+baseline (a shorter sample).
 The zipf workloads are the skewed-routing sweep on the Gemma layer shape (Q8_0 or NVFP4
 experts): the routing is supplied (each token draws k distinct experts with probability
 proportional to rank^-1.1), so the router is skipped, and a stack of 4 layers with their
@@ -60,6 +64,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false",
+                    help="time only the headline workload (the default run also times the SECONDARY list)")
     return ap.parse_args()
 
 
@@ -115,7 +121,7 @@ def workload_config(w, T, layers):
 
 
 # ====================================================================== oracle timing
-def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0, cache=None):
+def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0, cache=None, with_unit_time=False):
     """Time the CPU oracle on a bounded sample of the workload.
 
     A unit is the oracle's forward of one layer of the stack (router, top-k, softmax,
@@ -181,16 +187,18 @@ def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0, cache=
     desc = (f"{len(times)} oracle forwards of single layers of the stack on {tu} token(s) each ({what}, every "
             f"routed expert dequantised and evaluated in fp64, combine), cycling over the {layers} layers; "
             f"per-step time = mean per token-layer x {T} token(s) x {layers} layers")
+    if with_unit_time:
+        return step_s, len(times), oracle.num_threads(), desc, statistics.mean(times)
     return step_s, len(times), oracle.num_threads(), desc
 
 
-def single_core_baseline(w, T, layers, threads_all, cache):
-    """The same oracle sample on one thread (about 8 s of timed work), then the oracle's
+def single_core_baseline(w, T, layers, threads_all, cache, budget_s=8.0):
+    """The same oracle sample on one thread (about budget_s of timed work), then the oracle's
     thread count restored.  A failure here is recorded, never raised: the bench line stands."""
     import oracle
     try:
         oracle.set_num_threads(1)
-        step_s, n, _, _ = oracle_sample(w, T, layers, max_units=4 * layers, time_budget_s=8.0, warmup_units=1,
+        step_s, n, _, _ = oracle_sample(w, T, layers, max_units=4 * layers, time_budget_s=budget_s, warmup_units=1,
                                         cache=cache)
         return {"value": round(T / step_s, 6), "cores": 1, "units_timed": n}
     except Exception as exc:
@@ -346,7 +354,11 @@ def capture_graphs(stack, inputs, T, w, stage_events=None, stack_obj=None, routi
     return graphs, outs
 
 
-def run_ours(args, rank, world, local_rank):
+def run_ours(args, rank, world, local_rank, prebuilt=None):
+    """Time one workload (args.workload, args.tokens, args.layers) for args.steps steps.
+    prebuilt: layers of the same workload built earlier (a secondary line reuses the headline
+    stack's weights with other token inputs).  Returns (JSON object on rank 0, (w, T, layers),
+    the layers)."""
     import torch
     import torch.distributed as dist
 
@@ -357,7 +369,12 @@ def run_ours(args, rank, world, local_rank):
     w = synth.WORKLOADS[args.workload]
     T = args.tokens
     layers = args.layers or default_layers(w)
-    stack, inputs = build_stack(w, T, layers, local_rank)
+    if prebuilt is not None and len(prebuilt) == layers:
+        stack = prebuilt
+        inputs = [synth.tokens_cuda(w, T, layer=0, tag=f"bench{r}") for r in range(N_ROTATE)]
+        torch.cuda.synchronize()
+    else:
+        stack, inputs = build_stack(w, T, layers, local_rank)
     routings = build_routings(w, T)
     supplied = routings is not None
     # One token on layers the library runs as one kernel per layer: the whole stack as ONE
@@ -599,7 +616,7 @@ def run_ours(args, rank, world, local_rank):
             "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
         }
-    return result, (w, T, layers)
+    return result, (w, T, layers), stack
 
 
 def active_expert_bytes(stack, inputs, T, w, routings=None):
@@ -665,14 +682,20 @@ def measured_traffic(workload, T, layers):
 
 # ====================================================================== reference arm
 def run_reference(args, rank, world):
+    """The oracle as it stands on the host cores.  A step is one bounded sample of the
+    workload: one oracle forward of one layer of the stack on up to 8 of the step's tokens;
+    the line's value extrapolates those samples to tokens per second through the whole stack
+    (mean time per token and layer x tokens x layers), and ms_per_step is the measured time
+    of one such sample, so steps x ms_per_step is the time actually spent."""
     from quantized_routed_expert_softmax_gb300 import synth
     w = synth.WORKLOADS[args.workload]
     T = args.tokens
     layers = args.layers or default_layers(w)
     budget = 120.0
     t0 = time.perf_counter()
-    step_s, n, threads, desc = oracle_sample(w, T, layers, max_units=max(1, args.steps),
-                                             time_budget_s=budget, warmup_units=min(args.warmup, 1))
+    step_s, n, threads, desc, unit_s = oracle_sample(w, T, layers, max_units=max(1, args.steps),
+                                                     time_budget_s=budget, warmup_units=min(args.warmup, 1),
+                                                     with_unit_time=True)
     wall = time.perf_counter() - t0
     value = T / step_s
     cfg = workload_config(w, T, layers)
@@ -680,13 +703,34 @@ def run_reference(args, rank, world):
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6),
         "unit": f"tokens/s through the {layers}-layer stack", "n_gpus": world, "steps": n, "warmup": args.warmup,
-        "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": round(unit_s * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded; random-init weights of the workload's shapes)", "config": cfg,
+        "step_is": (f"one bounded sample: the oracle's forward of one layer of the {layers}-layer stack on "
+                    f"{min(T, 8)} token(s)"),
+        "units_timed": n, "stack_step_ms_extrapolated": round(step_s * 1e3, 3),
         "cpu_baseline": {"value": round(value, 6), "unit": f"tokens/s through the {layers}-layer stack",
                          "cores": threads, "kind": "oracle", "sample": desc, "wall_s": round(wall, 1)},
         "e2e": {"value": round(value, 6), "unit": f"tokens/s through the {layers}-layer stack",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+# Further configurations measured by the default run, each with its own workload, roofline and
+# oracle baseline: prefill on the headline stack's own weights (Gemma shape, T = 512), the
+# Nemotron-shaped NVFP4 ReLU^2 stack at one token, and MiniMax-shaped prefill (T = 4096).
+SECONDARY = [("gemma", 512, 30, 20), ("nemotron", 1, 40, 400), ("minimax", 4096, 8, 10)]
+
+
+def cpu_baseline(w, T, layers, budget_s, single_core_s=8.0, single=True):
+    import oracle
+    cache = {}
+    step_s, n, threads, desc = oracle_sample(w, T, layers, max_units=10 * layers, time_budget_s=budget_s,
+                                             warmup_units=1, cache=cache)
+    out = {"value": round(T / step_s, 6), "unit": f"tokens/s through the {layers}-layer stack", "cores": threads,
+           "kind": "oracle", "sample": desc}
+    if single:
+        out["single_core"] = single_core_baseline(w, T, layers, threads, cache, budget_s=single_core_s)
+    return out
 
 
 def main():
@@ -704,15 +748,32 @@ def main():
     if args.impl == "reference":
         print(json.dumps(run_reference(args, rank, world)), flush=True)
         return
-    result, (w, T, layers) = run_ours(args, rank, world, local_rank)
+    result, (w, T, layers), stack = run_ours(args, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, T, layers, 15.0)
+    if args.secondary and args.workload == "gemma" and args.tokens == 1 and not args.layers:
+        import torch
+        secondary = []
+        for name, t2, n2, steps2 in SECONDARY:
+            a2 = argparse.Namespace(**vars(args))
+            a2.workload, a2.tokens, a2.layers = name, t2, n2
+            a2.steps, a2.warmup = steps2, max(3, min(args.warmup, 5))
+            reuse = stack if name == w.name and n2 == layers else None
+            if reuse is None:
+                stack = None
+                torch.cuda.empty_cache()
+            r2, (w2, _, _), built = run_ours(a2, rank, world, local_rank, prebuilt=reuse)
+            if rank == 0:
+                if not args.no_cpu_baseline:
+                    r2["cpu_baseline"] = cpu_baseline(w2, t2, n2, 5.0, single=False)
+                for key in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data"):
+                    r2.pop(key, None)
+                secondary.append(r2)
+            del built, r2
+            torch.cuda.empty_cache()
+        if rank == 0:
+            result["secondary"] = secondary
     if rank == 0:
-        if not args.no_cpu_baseline:
-            cache = {}
-            step_s, n, threads, desc = oracle_sample(w, T, layers, max_units=10 * layers, time_budget_s=15.0,
-                                                     warmup_units=1, cache=cache)
-            result["cpu_baseline"] = {"value": round(T / step_s, 6), "unit": result["unit"], "cores": threads,
-                                      "kind": "oracle", "sample": desc,
-                                      "single_core": single_core_baseline(w, T, layers, threads, cache)}
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist

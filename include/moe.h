@@ -24,8 +24,8 @@
  *     nothing is launched, outputs are untouched, and the status says why.  No C++
  *     exception crosses this interface.
  *   - Faults found inside a kernel (an expert index out of range in caller-supplied
- *     routing, a tensor-core wait that ran past its time limit) never trap: the kernel
- *     clamps or stops, records a code in the workspace's error word, and
+ *     routing, a tensor-core wait or a grid barrier that ran past its time limit) never
+ *     trap: the kernel clamps or stops, records a code in the workspace's error word, and
  *     moe_get_device_status() reports it.
  *   - Shapes: row counts and column counts must be multiples of 32 (Q8_0) or 64
  *     (NVFP4); the layer needs d a multiple of 256 and f a multiple of 32 (Q8_0) or 64
@@ -285,20 +285,38 @@ int32_t moe_stack_forward_launches(const moe_layer_desc* descs, int32_t n_layers
  *   - Every call shares the one array, so calls that may overlap on the GPU (different
  *     streams without ordering between them) race and corrupt each other's results;
  *     order them on one stream.
- *   - Each call clears the array's device-error word first; out-of-range supplied expert
- *     indices are still clamped, but there is no workspace to query afterwards.
+ *   - Each call first clears the array's control region (its device-error word and the
+ *     counters the kernels use), on `stream`.  A device error of the call (1: a supplied
+ *     expert index was clamped; 2: a wait ran past its limit and the output is NOT valid;
+ *     3: an activation beyond the f16 range on the tensor-core path) stays in the array
+ *     until the next call: read it with moe_layer_forward_noalloc_status.
  * Errors: as moe_layer_forward, plus WORKSPACE when the problem does not fit.
  */
 moe_status moe_layer_forward_noalloc(const moe_layer_desc* desc, const void* x, moe_dtype xt, int64_t T,
                                      const int32_t* idx_in, const float* w_in, float* out, moe_stream_t stream);
 
 /*
+ * moe_layer_forward_noalloc_status -- moe_get_device_status for the scratch of
+ * moe_layer_forward_noalloc on the current device: synchronises `stream`, reads the device
+ * error word the last no-allocation call left (codes as for moe_get_device_status), clears
+ * it, and returns MOE_OK or MOE_ERR_DEVICE_CHECK (the code in *device_code, may be NULL).
+ * Call it on the stream of the call it reports on.  Like the entry point it allocates
+ * nothing.
+ */
+moe_status moe_layer_forward_noalloc_status(moe_stream_t stream, int32_t* device_code);
+
+/*
  * moe_get_device_status -- synchronises `stream`, reads the error word of a layer
  * workspace, clears it, and returns MOE_OK or MOE_ERR_DEVICE_CHECK (the device code in
- * *device_code, may be NULL): 1 = an expert index outside [0, E) was clamped; 2 = a
- * tensor-core (GEMM path) wait passed its one-second limit and the kernel stopped early
- * (the output is then not valid); 3 = the GEMM path met an activation (x or h) beyond the
- * f16 range +-65504 that its tensor-core operands use (the output then holds inf).
+ * *device_code, may be NULL):
+ *   1 = an expert index outside [0, E) in supplied routing was clamped;
+ *   2 = a wait passed its time limit (one second) and the kernel stopped early; the output
+ *       is then NOT valid.  Two waits can report it: a tensor-core (GEMM path) mbarrier wait,
+ *       and a grid barrier of the one-kernel decode layer (one token, moe_layer_forward or
+ *       moe_stack_forward), whose CTAs then stop at once without reading their peers' data;
+ *   3 = the GEMM path met an activation (x or h) beyond the f16 range +-65504 that its
+ *       tensor-core operands use (the output then holds inf).
+ * (The draft interface's separate timeout status is folded into code 2 here.)
  */
 moe_status moe_get_device_status(void* workspace, moe_stream_t stream, int32_t* device_code);
 

@@ -237,14 +237,24 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
 }
 
 struct Layout {
-    size_t err, route_ctr, n_active, row_ctr, logits, rpart, idx, w, offsets, perm, pos, act_e, slot_info, chunk_cnt,
+    size_t err, route_ctr, n_active, wait_limit, row_ctr, logits, rpart, idx, w, offsets, perm, pos, act_e, slot_info, chunk_cnt,
         local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, dec_bar, dec_sel, dec_grec, dec_drec, xnext, total;
 };
 
+// The control region at the start of every workspace: a 256-byte header (the error word,
+// the routing counter, the one-kernel layer's barrier counters, the test-only wait limit)
+// and the fused combine's row-tile counters, sized for the largest d.  Neither offset nor
+// size depends on the layer's shape or T, so one workspace (or the no-allocation scratch)
+// serves layers of any shape and calls of any token count in any order.
+constexpr size_t kCtrlHeaderBytes = 256;
+constexpr size_t kRowCtrBytes = sizeof(int32_t) * (kMaxDim / 32);   // 8 KiB
+constexpr size_t kCtrlBytes = kCtrlHeaderBytes + kRowCtrBytes;
+
 // Workspace regions for T tokens (each 256-byte aligned).  The control words (err,
 // route_ctr, the one-kernel layer's two barrier counters, row_ctr) come first, at offsets
-// that do not depend on T: they must be zero before a call and are left zero, so one
-// workspace serves calls of any token count in any order.
+// that depend neither on T nor on the layer's shape: they must be zero before a call and
+// are left zero, so one workspace serves calls of any token count and any layer shape in
+// any order.
 Layout layout_for(const moe_layer_desc* d, int64_t T) {
     const Plan p = make_plan(d, T);
     Layout L{};
@@ -258,8 +268,9 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     L.route_ctr = 4;
     L.n_active = 8;
     L.dec_bar = 16;   // [2]: grid-barrier arrivals, CTAs finished (one-kernel layer)
-    off = 256;
-    L.row_ctr = take(sizeof(int32_t) * (d->d / 32));
+    L.wait_limit = 32;   // int64: grid-barrier wait limit in ns, 0 = the default second
+    L.row_ctr = kCtrlHeaderBytes;
+    off = kCtrlBytes;
     L.logits = take(sizeof(float) * T * d->E);
     L.rpart = take(p.small_route ? sizeof(float) * T * d->E * 32 : 0);
     L.idx = take(sizeof(int32_t) * p.P);
@@ -292,6 +303,12 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     L.total = off;
     return L;
 }
+
+}  // namespace
+
+size_t workspace_control_bytes() { return kCtrlBytes; }
+
+namespace {
 
 Workspace bind(void* base, const Layout& L) {
     char* b = static_cast<char*>(base);

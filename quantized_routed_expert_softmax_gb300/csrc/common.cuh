@@ -15,18 +15,26 @@ namespace moe {
 // Device error codes recorded in the workspace error word.
 constexpr int kDevErrBadExpert = 1;
 
+// Bytes of a workspace's control region (its header and the row-tile counters), the same for
+// every layer shape and token count (api.cu).
+size_t workspace_control_bytes();
+
 constexpr int kRouterPartials = 256;   // partial sums of the router's canonical order
 constexpr int kMaxK = 32;              // top-k fits one warp
 constexpr int kMaxE = 1024;
 constexpr int kMaxDecodeCtas = 256;   // CTAs of the one-kernel decode layer at most (one per SM)
+// The one-kernel layer's grid-barrier wait limit in ns (int64) sits at 32-bit word 4 past its
+// barrier counters in the workspace header; zero means the default of one second.
+constexpr int kWaitLimitWord = 4;
 
 // Pointers into one layer workspace (see layout_for in api.cu).  The control words
-// (err, route_ctr, row_ctr) must be zero before a call; the kernels leave the counters
-// zero again when they finish.
+// (err, route_ctr, the one-kernel layer's counters, row_ctr) sit at fixed offsets in the
+// first workspace_control_bytes() bytes; they must be zero before a call, and the kernels
+// leave the counters zero again when they finish.
 struct Workspace {
     int32_t* err;          // [1] sticky first error
     int32_t* route_ctr;    // [1] CTAs of the routing kernel that have finished their logits
-    int32_t* row_ctr;      // [d/32] down CTAs finished per row tile (fused combine)
+    int32_t* row_ctr;      // [d/32] down CTAs finished per row tile (fused combine); room for the largest d
     int32_t* n_active;     // [1] number of experts with at least one pair
     float* logits;         // [T][E]
     float* rpart;          // [T][E][32] router partial sums by residue class (fused decode routing)
@@ -110,7 +118,8 @@ struct DecodeArgs {
     int32_t* idx_out;            // [n_layers][k] routing of each layer (stacks; may be null)
     float* w_out;                // [n_layers][k]
     Workspace ws;
-    int32_t* bar;                // [2] grid-barrier arrivals, CTAs finished (zero between calls)
+    int32_t* bar;                // [2] grid-barrier arrivals, CTAs finished (zero between calls);
+                                 //   bar[kWaitLimitWord..+1]: the barrier wait limit (int64 ns, 0 = 1 s)
     int32_t* sel;                // [k] experts selected by rank (more than 256 experts)
     float* selv;                 // [k] their logits
     float* grec;                 // [k * f/16][cov_g][32] gate.up partial sums per item and contributor

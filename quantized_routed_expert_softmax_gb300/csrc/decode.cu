@@ -80,24 +80,32 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
 }
 
 // Grid-wide barrier over a monotonically growing counter (target = n * gridDim.x for the
-// n-th barrier of a call).  Bounded: after ~1 s it records device error 2 and returns.
-__device__ __forceinline__ void grid_barrier(int32_t* ctr, int target, int32_t* err) {
+// n-th barrier of a call).  Bounded: a wait that passes `limit_ns` records device error 2 and
+// returns false, and the CTA then stops (see the end of the kernel): the data behind the
+// barrier may be incomplete, so nothing after it may be read.  A CTA that stops still counts
+// as arrived at this barrier; the others stop at their next barrier, within the same limit.
+__device__ __forceinline__ bool grid_barrier(int32_t* ctr, int target, int32_t* err, long long limit_ns,
+                                             int* s_ok) {
     __syncthreads();
     if (threadIdx.x == 0) {
         // release: the CTA's writes (ordered before this by the barrier above) are visible to
         // every CTA that acquires the counter at or past the target
         asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
+        int ok = 1;
         if (ld_acquire(ctr) < target) {
             const long long t0 = globaltimer();
             while (ld_acquire(ctr) < target) {
-                if (globaltimer() - t0 > kWaitLimitNs) {
+                if (globaltimer() - t0 > limit_ns) {
                     set_error(err, kDevErrTimeout);
+                    ok = 0;
                     break;
                 }
             }
         }
+        *s_ok = ok;
     }
     __syncthreads();
+    return *s_ok != 0;
 }
 
 
@@ -198,7 +206,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     __shared__ int s_pos[kMaxK];     // sorted slot of pair j
     __shared__ float s_w[kMaxK];     // combine weight of pair j
     __shared__ int s_cnt[kDecWarps]; // per-warp counts (ranking over many experts)
+    __shared__ int s_ok;             // the last grid barrier completed within its limit
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the grid barriers' wait limit: the workspace's limit word when set (tests), else a second
+    const long long wait_lim = *reinterpret_cast<const volatile long long*>(a.bar + kWaitLimitWord);
+    const long long wait_ns = wait_lim > 0 ? wait_lim : kWaitLimitNs;
     const int G = gridDim.x, c = blockIdx.x;
     const int d = a.d, f = a.f, E = a.E, k = a.k;
     const uint32_t gw = static_cast<uint32_t>(c * kDecWarps + warp);   // warp index in the grid
@@ -297,7 +309,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 if (lane == 0) a.ws.logits[c * epc + warp] = v;
             }
         }
-        if constexpr (!kSupplied) grid_barrier(a.bar, ++nbar * G, a.ws.err);
+        if constexpr (!kSupplied)
+            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
         if (l == 0) pdl_trigger();   // every CTA is resident: the next kernel may be scheduled
 
         // ---------------------------------------------------------------- R: top-k, weights, slots
@@ -359,7 +372,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             }
         } else {
             if (router) rank_own_experts(slog, s_cnt, E, k, epc, c, a.sel, a.selv);
-            grid_barrier(a.bar, ++nbar * G, a.ws.err);
+            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
             if (tid < k) {
                 s_sel[tid] = __ldcg(a.sel + tid);
                 s_val[tid] = __ldcg(a.selv + tid);
@@ -513,7 +526,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             const int cidx = c - static_cast<int>(split_owner(U_g, a.warps_g, item * npan_g) / kDecWarps);
             a.grec[(static_cast<int64_t>(item) * a.cov_g + cidx) * 32 + j] = v;
         }
-        grid_barrier(a.bar, ++nbar * G, a.ws.err);
+        if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
 
         if constexpr (kQ8) {
             // ---------------------------------------------------------------- D ring, then H
@@ -642,7 +655,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 }
             }
             cp_async_wait<0>();
-            grid_barrier(a.bar, ++nbar * G, a.ws.err);
+            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
             if (l + 1 < a.n_layers) request_router(a.lp[l + 1].W);   // the ring is free until the next gate.up
 
             // ---------------------------------------------------------------- C: combine
@@ -825,7 +838,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 const int cidx = c - static_cast<int>(split_owner(U_d, a.warps_d, item * npan_d) / kDecWarps);
                 a.drec[(static_cast<int64_t>(item) * a.cov_d + cidx) * 256 + r] = v;
             }
-            grid_barrier(a.bar, ++nbar * G, a.ws.err);
+            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
             if (l + 1 < a.n_layers) request_router(a.lp[l + 1].W);   // the ring is free until the next gate.up
 
             // ------------------------------------------------------------ C (NVFP4)
@@ -861,7 +874,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         // stand-alone RMS-norm kernel (threads t < 256 take elements t, t + 256, ...; warp sums;
         // the 8 warp sums in order), so a stack equals its layers glued by that kernel bitwise.
         if (l + 1 < a.n_layers || a.x_next) {
-            grid_barrier(a.bar, ++nbar * G, a.ws.err);
+            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
             const float* ol = a.out + static_cast<int64_t>(l) * d;
             float* wsum = slog;
             if (tid < 256) {
@@ -888,8 +901,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             __syncthreads();   // (slog is read again by the next layer's selection)
         }
     }
-    // The last CTA to finish resets the barrier counters for the next call (every CTA has
-    // passed all three barriers by now).
+stop:
+    // Every CTA ends here: after the last layer, or at once after a barrier wait that ran out
+    // of time (device error 2; the CTA reads nothing its peers may not have written).  No
+    // asynchronous copy into shared memory may still be in flight when the CTA exits.
+    cp_async_wait<0>();
+    // The last CTA to finish resets the barrier counters for the next call: every CTA has
+    // passed (or given up on) all of its barriers by now.
     if (tid == 0) {
         __threadfence();
         if (atomicAdd(a.bar + 1, 1) == G - 1) {

@@ -53,8 +53,18 @@ extern "C" moe_status moe_layer_forward_noalloc(const moe_layer_desc* desc, cons
     moe_status st = MOE_OK;
     void* scratch = scratch_address(&st);
     if (st != MOE_OK) return st;
-    // The workspace's first word is the sticky device-error word; it must start at zero.
+    // The scratch's control region (the error word, the barrier and row-tile counters, at the
+    // same offsets for every layer shape) must start at zero.  It is cleared on every call, so
+    // a counter left behind by an earlier call (one that overlapped this on another stream, or
+    // one whose kernel stopped at a timed-out wait) cannot carry over into this one.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, moe::workspace_control_bytes(), s) != cudaSuccess) return MOE_ERR_CUDA;
     return moe_layer_forward(desc, x, xt, T, idx_in, w_in, out, scratch, MOE_NOALLOC_SCRATCH_BYTES, nullptr, stream);
+}
+
+extern "C" moe_status moe_layer_forward_noalloc_status(moe_stream_t stream, int32_t* device_code) {
+    moe_status st = MOE_OK;
+    void* scratch = scratch_address(&st);
+    if (st != MOE_OK) return st;
+    return moe_get_device_status(scratch, stream, device_code);
 }

@@ -26,7 +26,8 @@ PATH = {"auto": 0, "gemv": 1, "gemm": 2}
 EXPORTS = ["moe_q8_0_bytes", "moe_nvfp4_bytes", "moe_quantize_q8_0", "moe_pack_nvfp4", "moe_router_workspace_bytes",
            "moe_router_topk", "moe_layer_workspace_bytes", "moe_layer_forward", "moe_rmsnorm_bf16",
            "moe_get_device_status", "moe_status_string", "moe_abi_version", "moe_layer_forward_launches",
-           "moe_layer_forward_noalloc", "moe_stack_forward", "moe_stack_forward_launches"]
+           "moe_layer_forward_noalloc", "moe_layer_forward_noalloc_status", "moe_stack_forward",
+           "moe_stack_forward_launches"]
 
 
 class MoeError(RuntimeError):
@@ -77,6 +78,7 @@ def lib() -> ctypes.CDLL:
             "moe_abi_version": (I32, []),
             "moe_layer_forward_launches": (I32, [ctypes.POINTER(LayerDesc), I64, I32]),
             "moe_layer_forward_noalloc": (I32, [ctypes.POINTER(LayerDesc), P, I32, I64, P, P, P, P]),
+            "moe_layer_forward_noalloc_status": (I32, [P, ctypes.POINTER(I32)]),
             "moe_stack_forward": (I32, [ctypes.POINTER(LayerDesc), I32, P, I32, ctypes.c_float, P, P, P, P, P, SZ, P]),
             "moe_stack_forward_launches": (I32, [ctypes.POINTER(LayerDesc), I32, I32]),
         }
@@ -168,6 +170,16 @@ def rmsnorm_bf16(x, eps: float = 1e-6, out=None, stream=None):
         out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
     _check("moe_rmsnorm_bf16", lib().moe_rmsnorm_bf16(_ptr(x), T, d, ctypes.c_float(eps), _ptr(out), _stream(stream)))
     return out
+
+
+def device_status(workspace, stream=None) -> int:
+    """moe_get_device_status: the device error code a workspace holds (0 if none); reading
+    clears it."""
+    code = ctypes.c_int32(0)
+    st = lib().moe_get_device_status(_ptr(workspace), _stream(stream), ctypes.byref(code))
+    if st not in (MOE_OK, 7):
+        raise MoeError("moe_get_device_status", st)
+    return int(code.value)
 
 
 class MoELayer:
@@ -268,11 +280,20 @@ class MoELayer:
                                                _ptr(w_in), _ptr(out), _stream(stream)))
         return out
 
-    def device_status(self, stream=None) -> int:
-        """moe_get_device_status on this layer's workspace: 0 or the device error code."""
+    @staticmethod
+    def noalloc_status(stream=None) -> int:
+        """moe_layer_forward_noalloc_status: the device error code the last no-allocation
+        call on this device left (0 if none); reading clears it."""
         code = ctypes.c_int32(0)
-        lib().moe_get_device_status(_ptr(self._ws), _stream(stream), ctypes.byref(code))
+        st = lib().moe_layer_forward_noalloc_status(_stream(stream), ctypes.byref(code))
+        if st not in (MOE_OK, 7):
+            raise MoeError("moe_layer_forward_noalloc_status", st)
         return int(code.value)
+
+    def device_status(self, stream=None, workspace=None) -> int:
+        """moe_get_device_status on this layer's workspace (or `workspace`): 0 or the device
+        error code."""
+        return device_status(self._ws if workspace is None else workspace, stream)
 
 
 class MoEStack:

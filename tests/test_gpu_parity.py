@@ -399,7 +399,33 @@ def test_rmsnorm_bf16():
 
 
 # ------------------------------------------------------------------ the layer, full shapes
-def _full_case(name, T, sample=None, idx_in=None, w_in=None, path="auto"):
+def dense_sample(tr, T, k, tile, n_min=64):
+    """Tokens to check against the oracle at a full size: the first token of every token tile
+    of the hottest expert (tiles of `tile` sorted rows) and of its last row, the last (ragged)
+    row of the 16 busiest experts whose row count is not a multiple of the tile, then evenly
+    spaced tokens up to n_min.  Every sampled token's output spans every row tile of the
+    weights."""
+    off = tr["offsets"].cpu().numpy()
+    perm = tr["perm"].cpu().numpy()
+    cnt = np.diff(off)
+    rows = set()
+    hot = int(np.argmax(cnt))
+    for i in range(0, int(cnt[hot]), tile):
+        rows.add(int(perm[off[hot] + i]) // k)
+    rows.add(int(perm[off[hot + 1] - 1]) // k)
+    ragged = [int(e) for e in np.argsort(-cnt, kind="stable") if cnt[e] % tile]
+    for e in ragged[:16]:
+        rows.add(int(perm[off[e + 1] - 1]) // k)
+    for t in np.linspace(0, T - 1, num=n_min).astype(int):
+        if len(rows) >= n_min:
+            break
+        rows.add(int(t))
+    return sorted(rows)
+
+
+def _full_case(name, T, sample=None, idx_in=None, w_in=None, path="auto", tile=None):
+    """One full-size layer against the oracle: every token (sample None), the listed tokens,
+    or (tile given) the dense_sample of the layer's own permutation."""
     w = synth.WORKLOADS[name]
     L = layers.build_layer(w, keep_fp32=True, path=path)
     x = synth.tokens_cuda(w, T, tag="parity")
@@ -407,6 +433,9 @@ def _full_case(name, T, sample=None, idx_in=None, w_in=None, path="auto"):
     ii = None if idx_in is None else torch.from_numpy(idx_in).cuda()
     ww = None if w_in is None else torch.from_numpy(w_in).cuda()
     out = L.forward(x, idx_in=ii, w_in=ww, trace=tr).cpu().numpy()
+    if tile is not None:
+        sample = dense_sample(tr, T, w.k, tile)
+        assert len(sample) >= 64
     rows = np.arange(T) if sample is None else np.asarray(sample)
     xs = to_numpy_x(x)[rows]
     W = L.router_w.cpu().numpy()
@@ -451,32 +480,68 @@ def test_gemma_layer_full_size(T):
     _full_case("gemma", T)
 
 
-@pytest.mark.parametrize("path", ["gemv", "gemm"])
-def test_gemma_layer_prefill_512_sampled(path):
-    _full_case("gemma", 512, sample=[0, 1, 255, 511], path=path)
+# Token tiles: the GEMV kernels stage up to 8 tokens of an expert, the tensor-core GEMMs 64 to
+# 192 sorted rows; sampling every 8th / 64th row of the hottest expert meets every tile of both.
+@pytest.mark.parametrize("path,tile", [("gemv", 8), ("gemm", 64)])
+def test_gemma_layer_prefill_512_sampled(path, tile):
+    _full_case("gemma", 512, path=path, tile=tile)
 
 
-@pytest.mark.parametrize("T,sample", [(1, None), (32, [0, 31])])
-def test_nemotron_layer_full_size(T, sample):
-    _full_case("nemotron", T, sample=sample)
+@pytest.mark.parametrize("T", [1, 32])
+def test_nemotron_layer_full_size(T):
+    _full_case("nemotron", T)
 
 
-@pytest.mark.parametrize("T,sample", [(1, None), (8, [0, 7])])
-def test_minimax_layer_full_size(T, sample):
-    _full_case("minimax", T, sample=sample)
+@pytest.mark.parametrize("T", [1, 8])
+def test_minimax_layer_full_size(T):
+    _full_case("minimax", T)
 
 
 def test_minimax_layer_prefill_4096_sampled():
-    _full_case("minimax", 4096, sample=[0, 2047, 4095])
+    _full_case("minimax", 4096, tile=64)
 
 
 # The skewed-routing sweep's sizes up to its largest, T = 8192 (65,536 pairs; the hottest
-# expert gets about a fifth of the tokens)
+# expert gets a pair from most tokens, over a hundred 64-row tiles)
 @pytest.mark.parametrize("name,T", [("zipf", 64), ("zipf", 2048), ("zipf_nvfp4", 2048), ("zipf", 8192)])
 def test_zipf_routing_full_size(name, T):
     w = synth.WORKLOADS[name]
     idx, wts = synth.zipf_routing(T, w.E, w.k)
-    _full_case(name, T, sample=[0, 17, T // 2 + 1, T - 1], idx_in=idx, w_in=wts)
+    _full_case(name, T, idx_in=idx, w_in=wts, tile=8 if T * w.k < 8 * w.E else 64)
+
+
+# ------------------------------------------------------------------ the benchmarked stacks, full shape
+# The call bench.py times at one token: moe_stack_forward over the Gemma-shaped (Q8_0 SwiGLU)
+# and Nemotron-shaped (NVFP4 ReLU^2, 92.5% zeros) stacks, built by the bench's own builder
+# (device-drawn weights, each layer warming L2 with the next one's router).  Each layer's
+# routing must match the oracle's bit for bit and its output to the tolerance, on the bf16
+# input that layer consumed; a second call must be bitwise identical (Nemotron page, "How we
+# check correctness": compared against a reference, the same input run repeatedly).
+@pytest.mark.parametrize("name,n", [("gemma", 4), ("nemotron", 4)])
+def test_benchmarked_stack_full_shape(name, n):
+    import bench
+    w = synth.WORKLOADS[name]
+    stack_layers, inputs = bench.build_stack(w, 1, n, 0)
+    st = native.MoEStack(stack_layers)
+    assert st.launches() == 1
+    x0 = inputs[0]
+    xn = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
+    routing = {}
+    outs = st.forward(x0, x_next=xn, routing=routing).clone()
+    for l in range(n):
+        xs = to_numpy_x(x0 if l == 0 else xn[l - 1:l])
+        W = stack_layers[l].router_w.cpu().numpy()
+        need, _ = oracle.topk_softmax(oracle.router_logits(xs, W), w.k)
+        ol = oracle_layer(w, W, lambda e: synth.expert_stack_cuda(w, l, "gate_up", [e])[0].cpu().numpy(),
+                          lambda e: synth.expert_stack_cuda(w, l, "down", [e])[0].cpu().numpy(), need.ravel())
+        ref = ol.forward(xs)
+        assert np.array_equal(routing["idx"][l:l + 1].cpu().numpy(), ref["idx"]), l
+        assert np.allclose(routing["w"][l:l + 1].cpu().numpy(), ref["w"], rtol=1e-6, atol=0), l
+        assert_close(outs[l:l + 1].cpu().numpy(), ref["out"], what=f"layer {l}")
+    again = st.forward(x0)
+    assert torch.equal(outs.view(torch.int32), again.view(torch.int32))
+    del stack_layers, st
+    torch.cuda.empty_cache()
 
 
 # ------------------------------------------------------------------ a stack of layers, one token
