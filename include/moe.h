@@ -310,10 +310,12 @@ moe_status moe_layer_forward_noalloc_status(moe_stream_t stream, int32_t* device
  * workspace, clears it, and returns MOE_OK or MOE_ERR_DEVICE_CHECK (the device code in
  * *device_code, may be NULL):
  *   1 = an expert index outside [0, E) in supplied routing was clamped;
- *   2 = a wait passed its time limit (one second) and the kernel stopped early; the output
- *       is then NOT valid.  Two waits can report it: a tensor-core (GEMM path) mbarrier wait,
- *       and a grid barrier of the one-kernel decode layer (one token, moe_layer_forward or
- *       moe_stack_forward), whose CTAs then stop at once without reading their peers' data;
+ *   2 = a wait passed its time limit (one second) and the kernel gave up; the output is then
+ *       NOT valid.  Two waits can report it: a tensor-core (GEMM path) mbarrier wait (that
+ *       kernel stops early), and a grid barrier of the one-kernel decode layer (one token,
+ *       moe_layer_forward or moe_stack_forward), after which no CTA of the launch waits again
+ *       and the kernel runs to its end at once (every index it reads from the workspace is
+ *       clamped, so stale data cannot send an access out of its buffer);
  *   3 = the GEMM path met an activation (x or h) beyond the f16 range +-65504 that its
  *       tensor-core operands use (the output then holds inf).
  * (The draft interface's separate timeout status is folded into code 2 here.)

@@ -81,31 +81,31 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
 
 // Grid-wide barrier over a monotonically growing counter (target = n * gridDim.x for the
 // n-th barrier of a call).  Bounded: a wait that passes `limit_ns` records device error 2 and
-// returns false, and the CTA then stops (see the end of the kernel): the data behind the
-// barrier may be incomplete, so nothing after it may be read.  A CTA that stops still counts
-// as arrived at this barrier; the others stop at their next barrier, within the same limit.
-__device__ __forceinline__ bool grid_barrier(int32_t* ctr, int target, int32_t* err, long long limit_ns,
-                                             int* s_ok) {
+// raises the counter past every target of the call, so that no CTA waits again: the kernel
+// then runs to its end at once.  The data behind a barrier that was given up on may be stale;
+// every index the kernel reads from the workspace is clamped to its range, so the stale values
+// can make the output wrong (error 2 declares it invalid) but cannot make an access leave its
+// buffer.  The normal path costs nothing extra: no flag is read outside the spin.
+constexpr int32_t kBarrierGiveUp = 1 << 30;   // above every target: 64 layers x 5 barriers x 256 CTAs
+
+__device__ __forceinline__ void grid_barrier(int32_t* ctr, int target, int32_t* err, long long limit_ns) {
     __syncthreads();
     if (threadIdx.x == 0) {
         // release: the CTA's writes (ordered before this by the barrier above) are visible to
         // every CTA that acquires the counter at or past the target
         asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
-        int ok = 1;
         if (ld_acquire(ctr) < target) {
             const long long t0 = globaltimer();
             while (ld_acquire(ctr) < target) {
                 if (globaltimer() - t0 > limit_ns) {
                     set_error(err, kDevErrTimeout);
-                    ok = 0;
+                    atomicMax(ctr, kBarrierGiveUp);
                     break;
                 }
             }
         }
-        *s_ok = ok;
     }
     __syncthreads();
-    return *s_ok != 0;
 }
 
 
@@ -206,7 +206,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     __shared__ int s_pos[kMaxK];     // sorted slot of pair j
     __shared__ float s_w[kMaxK];     // combine weight of pair j
     __shared__ int s_cnt[kDecWarps]; // per-warp counts (ranking over many experts)
-    __shared__ int s_ok;             // the last grid barrier completed within its limit
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // the grid barriers' wait limit: the workspace's limit word when set (tests), else a second
     const long long wait_lim = *reinterpret_cast<const volatile long long*>(a.bar + kWaitLimitWord);
@@ -309,8 +308,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 if (lane == 0) a.ws.logits[c * epc + warp] = v;
             }
         }
-        if constexpr (!kSupplied)
-            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
+        if constexpr (!kSupplied) grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns);
         if (l == 0) pdl_trigger();   // every CTA is resident: the next kernel may be scheduled
 
         // ---------------------------------------------------------------- R: top-k, weights, slots
@@ -372,9 +370,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             }
         } else {
             if (router) rank_own_experts(slog, s_cnt, E, k, epc, c, a.sel, a.selv);
-            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
-            if (tid < k) {
-                s_sel[tid] = __ldcg(a.sel + tid);
+            grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns);
+            if (tid < k) {   // (clamped: after a given-up barrier the word may be stale)
+                s_sel[tid] = min(max(__ldcg(a.sel + tid), 0), E - 1);
                 s_val[tid] = __ldcg(a.selv + tid);
             }
         }
@@ -454,6 +452,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 off += n;
             }
         };
+        // Q8_0 down: the issue pointer as (slot, row tile, panel), advanced by increments:
+        // slot-major, so that a CTA's units read the activations of one or two slots only.  The
+        // first stages are requested as soon as the warp's gate.up units are done (they do not
+        // depend on h), so they are in flight across the barrier.
+        const uint32_t dring_addr = smem_addr(ring + warp * kStages * kSlotBytes);
+        int dss = rd.item0 / nrt, dsrt = rd.item0 % nrt, dsb = rd.b0;
+        const uint8_t* dsw = P.w_dn + static_cast<int64_t>(s_e[dss < k ? dss : 0]) * a.dn_bytes;
+        auto issue_d = [&](int st) {
+            issue_panel_block<MOE_W_Q8_0>(dring_addr + st * kSlotBytes, dsw, d, dsrt * 32, dsrt * 32 + 16, dsb, pol, 0);
+            if (++dsb == npan_d) {
+                dsb = 0;
+                if (++dsrt == nrt) {
+                    dsrt = 0;
+                    if (++dss < k) dsw = P.w_dn + static_cast<int64_t>(s_e[dss]) * a.dn_bytes;
+                }
+            }
+        };
         {
             const int n = rg.n;   // 0 for a warp past the split (more warps than units)
             unsigned char* wring = ring + warp * kStages * kSlotBytes;
@@ -513,6 +528,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 }
             }
             cp_async_wait<0>();
+            if constexpr (kQ8) {
+#pragma unroll
+                for (int st = 0; st < kStages; ++st) {
+                    if (st < rd.n) issue_d(st);
+                    cp_async_commit();
+                }
+            }
         }
         // The CTA's record of each item it touched: its warps' partials in warp order (a warp
         // that did not touch the item adds zero), at the CTA's contributor slot of the item.
@@ -526,7 +548,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             const int cidx = c - static_cast<int>(split_owner(U_g, a.warps_g, item * npan_g) / kDecWarps);
             a.grec[(static_cast<int64_t>(item) * a.cov_g + cidx) * 32 + j] = v;
         }
-        if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
+        grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns);
 
         if constexpr (kQ8) {
             // ---------------------------------------------------------------- D ring, then H
@@ -535,26 +557,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             const int kf = k * f;
             __half* hs = reinterpret_cast<__half*>(xf);   // [k][f] hi, then [k][f] lo
             unsigned char* dring = ring + warp * kStages * kSlotBytes;
-            const uint32_t dring_addr = smem_addr(dring);
-            // the issue pointer as (slot, row tile, panel), advanced by increments: slot-major, so
-            // that a CTA's units read the activations of one or two slots only
-            int dss = rd.item0 / nrt, dsrt = rd.item0 % nrt, dsb = rd.b0;
-            const uint8_t* dsw = P.w_dn + static_cast<int64_t>(s_e[dss < k ? dss : 0]) * a.dn_bytes;
-            auto issue_d = [&](int st) {
-                issue_panel_block<MOE_W_Q8_0>(dring_addr + st * kSlotBytes, dsw, d, dsrt * 32, dsrt * 32 + 16, dsb, pol, 0);
-                if (++dsb == npan_d) {
-                    dsb = 0;
-                    if (++dsrt == nrt) {
-                        dsrt = 0;
-                        if (++dss < k) dsw = P.w_dn + static_cast<int64_t>(s_e[dss]) * a.dn_bytes;
-                    }
-                }
-            };
-#pragma unroll
-            for (int st = 0; st < kStages; ++st) {
-                if (st < rd.n) issue_d(st);
-                cp_async_commit();
-            }
             // H: h = SiLU(gate) * up.  Each CTA sums the records (in contributor order) of the slots
             // its down units read, into its own f16 hi + lo copy of h, and writes them as fp32 too
             // (every slot is read by some CTA; CTAs that share a slot write the same values).
@@ -655,7 +657,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 }
             }
             cp_async_wait<0>();
-            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
+            grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns);
             if (l + 1 < a.n_layers) request_router(a.lp[l + 1].W);   // the ring is free until the next gate.up
 
             // ---------------------------------------------------------------- C: combine
@@ -838,7 +840,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 const int cidx = c - static_cast<int>(split_owner(U_d, a.warps_d, item * npan_d) / kDecWarps);
                 a.drec[(static_cast<int64_t>(item) * a.cov_d + cidx) * 256 + r] = v;
             }
-            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
+            grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns);
             if (l + 1 < a.n_layers) request_router(a.lp[l + 1].W);   // the ring is free until the next gate.up
 
             // ------------------------------------------------------------ C (NVFP4)
@@ -874,15 +876,28 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         // stand-alone RMS-norm kernel (threads t < 256 take elements t, t + 256, ...; warp sums;
         // the 8 warp sums in order), so a stack equals its layers glued by that kernel bitwise.
         if (l + 1 < a.n_layers || a.x_next) {
-            if (!grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns, &s_ok)) goto stop;
+            grid_barrier(a.bar, ++nbar * G, a.ws.err, wait_ns);
             const float* ol = a.out + static_cast<int64_t>(l) * d;
             float* wsum = slog;
+            // out_l into shared memory, loaded in batches of 8 per thread (one L2 round trip per
+            // batch instead of one per element)
+            for (int base = 0; base < d; base += 8 * kDecThreads) {
+                float v[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int i = base + m * kDecThreads + tid;
+                    v[m] = i < d ? __ldcg(ol + i) : 0.0f;
+                }
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int i = base + m * kDecThreads + tid;
+                    if (i < d) xf[i] = v[m];
+                }
+            }
+            __syncthreads();
             if (tid < 256) {
                 float ss = 0.0f;
-                for (int i = tid; i < 32 * 256; i += 256) {
-                    const float v = i < d ? __ldcg(ol + i) : 0.0f;
-                    ss = fmaf(v, v, ss);
-                }
+                for (int i = tid; i < d; i += 256) ss = fmaf(xf[i], xf[i], ss);
                 ss = warp_sum(ss);
                 if (lane == 0) wsum[warp] = ss;
             }
@@ -892,7 +907,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             for (int i = 0; i < 8; ++i) tot += wsum[i];
             const float inv = rsqrtf(tot / static_cast<float>(d) + a.eps);
             for (int i = tid; i < d; i += kDecThreads) {
-                const __nv_bfloat16 xb = __float2bfloat16_rn(__ldcg(ol + i) * inv);
+                const __nv_bfloat16 xb = __float2bfloat16_rn(xf[i] * inv);
                 const float xv = __bfloat162float(xb);
                 xf[i] = xv;
                 xh[i] = __float2half_rn(xv);
@@ -901,11 +916,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             __syncthreads();   // (slog is read again by the next layer's selection)
         }
     }
-stop:
-    // Every CTA ends here: after the last layer, or at once after a barrier wait that ran out
-    // of time (device error 2; the CTA reads nothing its peers may not have written).  No
-    // asynchronous copy into shared memory may still be in flight when the CTA exits.
-    cp_async_wait<0>();
     // The last CTA to finish resets the barrier counters for the next call: every CTA has
     // passed (or given up on) all of its barriers by now.
     if (tid == 0) {

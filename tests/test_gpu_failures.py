@@ -4,9 +4,10 @@ Every wait in libmoe's kernels is bounded.  The one-kernel decode layer's grid b
 normally wait at most a second; a test can shorten that limit through the workspace header
 (the int64 at byte 32, in ns) and make every barrier wait run out by setting the barrier's
 arrival counter (the int32 at byte 16) to a value its targets never reach.  The kernel must
-then record device error 2, stop without reading data its peers never wrote, leave its
-counters zero for the next call, and return within the limit; the next call on the same
-workspace must give the normal result bit for bit.  Error 3 (an activation beyond the f16
+then record device error 2, give up waiting for the rest of the launch (it raises the counter
+past every target, so no later barrier waits), leave its counters zero for the next call, and
+return within the limit; the next call on the same workspace must give the normal result bit
+for bit.  Error 3 (an activation beyond the f16
 range of the tensor-core operands) needs no wait at all: a host-made input of 1e5 on the
 GEMM path triggers it.  The pages have no counterpart to these checks: they guard the GPU
 and the caller, not the method.
