@@ -671,11 +671,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                     const uint32_t item = static_cast<uint32_t>(s * nrt + rt);
                     const int nc = item_contributors(U_d, a.warps_d, npan_d, item);
                     const float* rec = a.drec + static_cast<int64_t>(item) * a.cov_d * 32 + r;
-                    float v[4];
+                    float v[8];   // the first 8 records in one batch (one L2 round trip)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = q < nc ? __ldcg(rec + q * 32) : 0.0f;
-                    float y = ((v[0] + v[1]) + v[2]) + v[3];   // records in contributor order
-                    for (int cc = 4; cc < nc; ++cc) y += __ldcg(rec + cc * 32);
+                    for (int q = 0; q < 8; ++q) v[q] = q < nc ? __ldcg(rec + q * 32) : 0.0f;
+                    float y = v[0];   // records in contributor order
+#pragma unroll
+                    for (int q = 1; q < 8; ++q) y += v[q];
+                    for (int cc = 8; cc < nc; ++cc) y += __ldcg(rec + cc * 32);
                     s_y[s * 32 + r] = y;
                 }
                 __syncthreads();
