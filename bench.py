@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--act-quant", choices=["none", "q8_0"], default="none",
+                    help="q8_0: the activation-quantised expert path (Q8_0 weights only)")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false",
                     help="time only the headline workload (the default run also times the SECONDARY list)")
     return ap.parse_args()
@@ -107,11 +109,13 @@ def hbm_peak():
     return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
-def workload_config(w, T, layers):
+def workload_config(w, T, layers, act_quant="none"):
     return {
         "workload": f"{w.name}-shaped MoE stack: {layers} layers, d={w.d}, E={w.E}, top-{w.k}, f={w.f}, "
                     f"{'SwiGLU' if w.act == 'swiglu' else 'ReLU^2'}, {w.wfmt.upper()} experts, "
-                    f"{w.x_dtype} activations, {'decode' if T <= 32 else 'prefill'} T={T}",
+                    f"{w.x_dtype} activations{', Q8_0-coded expert inputs' if act_quant == 'q8_0' else ''}, "
+                    f"{'decode' if T <= 32 else 'prefill'} T={T}",
+        "act_quant": act_quant,
         "layers": layers, "tokens_per_step": T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "act": w.act,
         "weights": w.wfmt, "activations": w.x_dtype,
         **({"routing": "supplied (router skipped): k distinct experts per token drawn with probability "
@@ -121,7 +125,8 @@ def workload_config(w, T, layers):
 
 
 # ====================================================================== oracle timing
-def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0, cache=None, with_unit_time=False):
+def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0, cache=None, with_unit_time=False,
+                  act_q8=False):
     """Time the CPU oracle on a bounded sample of the workload.
 
     A unit is the oracle's forward of one layer of the stack (router, top-k, softmax,
@@ -175,7 +180,7 @@ def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0, cache=
     while units < max_units + warmup_units and (spent < time_budget_s or units < warmup_units + 1):
         L, x, (ii, ww) = layer_obj(units % layers)
         t0 = time.perf_counter()
-        L.forward(x, idx_in=ii, w_in=ww)
+        L.forward(x, idx_in=ii, w_in=ww, act_q8=act_q8)
         dt = time.perf_counter() - t0
         if units >= warmup_units:
             times.append(dt)
@@ -375,6 +380,9 @@ def run_ours(args, rank, world, local_rank, prebuilt=None):
         torch.cuda.synchronize()
     else:
         stack, inputs = build_stack(w, T, layers, local_rank)
+    aq = getattr(args, "act_quant", "none")
+    for layer in stack:   # the activation-quantised path is a flag of the same weights
+        layer.desc.act_quant = native.ACT_QUANT[aq]
     routings = build_routings(w, T)
     supplied = routings is not None
     # One token on layers the library runs as one kernel per layer: the whole stack as ONE
@@ -552,7 +560,7 @@ def run_ours(args, rank, world, local_rank, prebuilt=None):
     result = None
     if rank == 0:
         step_bytes = tr_bytes["step"]
-        cfg = workload_config(w, T, layers)
+        cfg = workload_config(w, T, layers, aq)
         cfg.update({
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": f"per-step weight working set {step_bytes / 1e9:.2f} GB > 129 MB L2; {N_ROTATE} token inputs "
@@ -718,14 +726,15 @@ def run_reference(args, rank, world):
 # Further configurations measured by the default run, each with its own workload, roofline and
 # oracle baseline: prefill on the headline stack's own weights (Gemma shape, T = 512), the
 # Nemotron-shaped NVFP4 ReLU^2 stack at one token, and MiniMax-shaped prefill (T = 4096).
-SECONDARY = [("gemma", 512, 30, 20), ("nemotron", 1, 40, 400), ("minimax", 4096, 8, 10)]
+SECONDARY = [("gemma", 512, 30, 20, "none"), ("gemma", 1, 30, 400, "q8_0"), ("nemotron", 1, 40, 400, "none"),
+             ("minimax", 4096, 8, 10, "none"), ("minimax", 4096, 8, 10, "q8_0")]
 
 
-def cpu_baseline(w, T, layers, budget_s, single_core_s=8.0, single=True):
+def cpu_baseline(w, T, layers, budget_s, single_core_s=8.0, single=True, act_q8=False):
     import oracle
     cache = {}
     step_s, n, threads, desc = oracle_sample(w, T, layers, max_units=10 * layers, time_budget_s=budget_s,
-                                             warmup_units=1, cache=cache)
+                                             warmup_units=1, cache=cache, act_q8=act_q8)
     out = {"value": round(T / step_s, 6), "unit": f"tokens/s through the {layers}-layer stack", "cores": threads,
            "kind": "oracle", "sample": desc}
     if single:
@@ -750,25 +759,28 @@ def main():
         return
     result, (w, T, layers), stack = run_ours(args, rank, world, local_rank)
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, T, layers, 15.0)
+        result["cpu_baseline"] = cpu_baseline(w, T, layers, 15.0, act_q8=args.act_quant == "q8_0")
     if args.secondary and args.workload == "gemma" and args.tokens == 1 and not args.layers:
         import torch
         secondary = []
-        for name, t2, n2, steps2 in SECONDARY:
+        w_prev = w
+        for name, t2, n2, steps2, aq2 in SECONDARY:
             a2 = argparse.Namespace(**vars(args))
-            a2.workload, a2.tokens, a2.layers = name, t2, n2
+            a2.workload, a2.tokens, a2.layers, a2.act_quant = name, t2, n2, aq2
             a2.steps, a2.warmup = steps2, max(3, min(args.warmup, 5))
-            reuse = stack if name == w.name and n2 == layers else None
+            reuse = stack if stack is not None and name == w_prev.name and n2 == len(stack) else None
             if reuse is None:
                 stack = None
                 torch.cuda.empty_cache()
             r2, (w2, _, _), built = run_ours(a2, rank, world, local_rank, prebuilt=reuse)
+            stack = built
             if rank == 0:
                 if not args.no_cpu_baseline:
-                    r2["cpu_baseline"] = cpu_baseline(w2, t2, n2, 5.0, single=False)
+                    r2["cpu_baseline"] = cpu_baseline(w2, t2, n2, 5.0, single=False, act_q8=aq2 == "q8_0")
                 for key in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data"):
                     r2.pop(key, None)
                 secondary.append(r2)
+            w_prev = w2
             del built, r2
             torch.cuda.empty_cache()
         if rank == 0:

@@ -96,6 +96,16 @@ typedef enum { MOE_LAYOUT_CANONICAL = 0, MOE_LAYOUT_DEVICE = 1, MOE_LAYOUT_NEURO
  * other paths.  GEMV keeps the separate kernels. */
 typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GEMM = 2 } moe_path;
 
+/* How the experts see their inputs.  NONE: as given (fp32 or bf16 x; h in fp32).  Q8_0: the
+ * activation-quantised path of the CPU engines ("Running Gemma 4 26B at 5 tokens/s on a
+ * 13-year-old Xeon without a GPU", sections "A three-step fix" and "Narrowing down the
+ * cause": Q8_0 activation quantisers feeding Q8_0 x Q8_0 block dots).  Each expert input (x
+ * for gate.up; h, held in fp32, for down) is coded per block of 32 with the weight packer's
+ * Q8_0 codec (see moe_quantize_act_q8_0), and every weight row meets the coded values: per
+ * block, the 32 code products summed exactly, times both fp16 scales, the blocks summed in
+ * fp32.  Routing still reads the unquantised x.  Q8_0 weights only. */
+typedef enum { MOE_ACTQ_NONE = 0, MOE_ACTQ_Q8_0 = 1 } moe_act_quant;
+
 /* Bytes of one quantised matrix: rows*cols/32*34 (Q8_0), rows*cols/2 + rows*cols/16
  * (NVFP4).  Returns 0 for non-positive or non-multiple sizes. */
 size_t moe_q8_0_bytes(int64_t rows, int64_t cols);
@@ -130,6 +140,17 @@ moe_status moe_quantize_q8_0(const float* src, int64_t n_mat, int64_t rows, int6
  */
 moe_status moe_pack_nvfp4(const float* src, int64_t n_mat, int64_t rows, int64_t cols, moe_layout layout,
                           void* dst, float* tensor_scale, moe_stream_t stream);
+
+/*
+ * moe_quantize_act_q8_0 -- the activation quantiser of MOE_ACTQ_Q8_0, as values: every block
+ * of 32 along a row of x is coded exactly as moe_quantize_q8_0 codes weights (d = amax/127 in
+ * fp32, q = round-half-away(x * (1/d)), stored scale fp16(d)) and out holds q * fp16(d), the
+ * value the code stands for (exact in fp32).
+ * x     device [rows][cols], fp32 or bf16 (xt).   out  device fp32 [rows][cols] (written).
+ * Errors: INVALID_ARG, SHAPE (cols a positive multiple of 32), ALIGNMENT, CUDA.
+ */
+moe_status moe_quantize_act_q8_0(const void* x, moe_dtype xt, int64_t rows, int64_t cols, float* out,
+                                 moe_stream_t stream);
 
 /*
  * moe_router_topk -- router projection, top-k and softmax over the selected logits
@@ -173,6 +194,8 @@ typedef struct {
                                      router weights, so its routing does not wait on HBM.  A hint:
                                      never read by the layer's arithmetic; 16-byte aligned */
     int64_t l2_prefetch_bytes;    /* bytes at l2_prefetch (rounded down to a multiple of 16) */
+    int32_t act_quant;            /* moe_act_quant (MOE_ACTQ_Q8_0 needs Q8_0 weights) */
+    int32_t reserved;             /* zero */
 } moe_layer_desc;
 
 /* Optional copies of intermediate results (device pointers, each may be NULL), and
@@ -187,7 +210,8 @@ typedef struct {
     int32_t* offsets;  /* [E+1]: expert e owns sorted rows offsets[e]..offsets[e+1]-1 */
     int32_t* perm;     /* [T*k]: pair id (t*k+j) at each sorted row */
     int32_t* pos;      /* [T*k]: sorted row of each pair */
-    float* h;          /* [T*k][f] activations in sorted-row order */
+    float* h;          /* [T*k][f] activations in sorted-row order (MOE_ACTQ_Q8_0: the coded values
+                          the down projection read) */
     void* stage_events[5];
 } moe_trace;
 
@@ -325,7 +349,8 @@ moe_status moe_get_device_status(void* workspace, moe_stream_t stream, int32_t* 
 /* A static string naming a status. */
 const char* moe_status_string(moe_status status);
 
-/* Version of this interface (major*10000 + minor*100 + patch). */
+/* Version of this interface (major*10000 + minor*100 + patch): 10300 adds act_quant to
+ * moe_layer_desc, moe_quantize_act_q8_0 and moe_layer_forward_noalloc_status. */
 int32_t moe_abi_version(void);
 
 #ifdef __cplusplus

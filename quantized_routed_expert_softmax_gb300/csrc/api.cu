@@ -10,6 +10,7 @@ namespace moe {
 // launchers (pack.cu, route.cu, gemv.cu)
 cudaError_t launch_q8_0_quantize(const float*, int64_t, int64_t, int64_t, int, void*, cudaStream_t);
 cudaError_t launch_nvfp4_pack(const float*, int64_t, int64_t, int64_t, int, void*, float*, cudaStream_t);
+cudaError_t launch_act_q8_0(const void*, int, int64_t, int64_t, float*, uint16_t*, uint16_t*, int, cudaStream_t);
 cudaError_t launch_router_logits(const void*, int, const float*, int64_t, int64_t, int64_t, float*, cudaStream_t);
 cudaError_t launch_topk_softmax(const float*, int64_t, int64_t, int, int32_t*, float*, cudaStream_t);
 cudaError_t launch_route_small(const float*, const int32_t*, const float*, int64_t, int64_t, int, int,
@@ -232,13 +233,13 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
                 (d->k == 1 || d->k == 2 || d->k == 4 || d->k == 8) && d->f / 32 >= 8 / d->k && d->d % 16 == 0;
     if (p.down_t1) p.fuse_combine = true;   // the down kernel writes the output rows
     p.nv_split = (!p.gemm && d->wfmt == MOE_W_NVFP4 && p.fuse_combine && T == 1 && (d->f / 16) >= 4 * 8) ? 4 : 1;
-    p.decode1 = !p.gemm && decode_shape_ok(d, T, xt);
+    p.decode1 = !p.gemm && d->act_quant == MOE_ACTQ_NONE && decode_shape_ok(d, T, xt);
     return p;
 }
 
 struct Layout {
     size_t err, route_ctr, n_active, wait_limit, row_ctr, logits, rpart, idx, w, offsets, perm, pos, act_e, slot_info, chunk_cnt,
-        local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, dec_bar, dec_sel, dec_grec, dec_drec, xnext, total;
+        local_rank, gmask, h, y, xs_hi, xs_lo, h_hi, h_lo, dec_bar, dec_sel, dec_grec, dec_drec, xnext, xq, total;
 };
 
 // The control region at the start of every workspace: a 256-byte header (the error word,
@@ -300,6 +301,7 @@ Layout layout_for(const moe_layer_desc* d, int64_t T) {
     L.dec_grec = take(dec ? sizeof(float) * 32 * (sp.U_g / sp.npan_g) * sp.cov_g : 0);
     L.dec_drec = take(dec ? sizeof(float) * sp.rec_d * sp.items_d * sp.cov_d : 0);
     L.xnext = take(T == 1 ? sizeof(uint16_t) * d->d : 0);   // a stack's next input (one token)
+    L.xq = take(d->act_quant ? sizeof(float) * T * d->d : 0);   // the coded expert input (MOE_ACTQ_Q8_0)
     L.total = off;
     return L;
 }
@@ -353,6 +355,8 @@ moe_status validate_desc(const moe_layer_desc* d) {
     if (d->wfmt == MOE_W_NVFP4 && (!d->gate_up_tscale || !d->down_tscale)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(d->router_w) || !aligned16(d->w_gate_up) || !aligned16(d->w_down)) return MOE_ERR_ALIGNMENT;
     if (d->l2_prefetch && (d->l2_prefetch_bytes < 0 || !aligned16(d->l2_prefetch))) return MOE_ERR_ALIGNMENT;
+    if (d->act_quant != MOE_ACTQ_NONE && d->act_quant != MOE_ACTQ_Q8_0) return MOE_ERR_INVALID_ARG;
+    if (d->act_quant == MOE_ACTQ_Q8_0 && d->wfmt != MOE_W_Q8_0) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -425,7 +429,7 @@ using namespace moe;
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 10200; }
+int32_t moe_abi_version(void) { return 10300; }
 
 const char* moe_status_string(moe_status s) {
     switch (s) {
@@ -473,6 +477,19 @@ moe_status moe_pack_nvfp4(const float* src, int64_t n_mat, int64_t rows, int64_t
     if (!aligned16(src) || !aligned16(dst) || (reinterpret_cast<uintptr_t>(tensor_scale) & 3u)) return MOE_ERR_ALIGNMENT;
     if (n_mat == 0) return MOE_OK;
     return cuda_status(launch_nvfp4_pack(src, n_mat, rows, cols, layout, dst, tensor_scale, stream));
+}
+
+moe_status moe_quantize_act_q8_0(const void* x, moe_dtype xt, int64_t rows, int64_t cols, float* out,
+                                 moe_stream_t stream) {
+    if (!x || !out) return MOE_ERR_INVALID_ARG;
+    if (xt != MOE_F32 && xt != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (rows < 0 || cols <= 0 || cols % 32 != 0 || rows > kMaxTokens * kMaxK || cols > kMaxF * 2) return MOE_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
+    if (rows == 0) return MOE_OK;
+    int num_sms = 0;
+    if (ensure_configured(&num_sms) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(launch_act_q8_0(x, xt, rows, cols, out, nullptr, nullptr, num_sms,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_router_workspace_bytes(int64_t T, int64_t E) {
@@ -539,7 +556,10 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     cudaError_t e = ensure_configured(&num_sms);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const Plan p = make_plan(desc, T, xt);
+    // the experts read fp32 coded values on the activation-quantised path
+    const bool actq = desc->act_quant == MOE_ACTQ_Q8_0;
+    const int xt_exp = actq ? MOE_F32 : xt;
+    const Plan p = make_plan(desc, T, xt_exp);
     const Workspace ws = bind(workspace, L);
     const int k = desc->k;
 
@@ -601,6 +621,13 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     ExpertArgs a{};
     a.x = x;
     a.xt = xt;
+    if (actq) {   // the experts' input: x coded per block of 32 (Q8_0), as the values the codes stand for
+        float* xq = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.xq);
+        if ((e = launch_act_q8_0(x, xt, T, desc->d, xq, nullptr, nullptr, num_sms, s)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        a.x = xq;
+        a.xt = MOE_F32;
+    }
     a.d = static_cast<int>(desc->d);
     a.f = static_cast<int>(desc->f);
     a.k = k;
@@ -643,6 +670,11 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
         e = launch_gate_up_gemv(a, desc->wfmt, desc->act, p.slot_cap, s);
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (actq) {   // h coded in place, and its f16 planes on the tensor-core path
+        e = launch_act_q8_0(ws.h, MOE_F32, p.P, desc->f, ws.h, p.gemm ? ws.h_hi : nullptr, p.gemm ? ws.h_lo : nullptr,
+                            num_sms, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
     mark(2);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (p.gemm) e = launch_expert_gemm(a, 1, desc->wfmt, desc->act, p.slot_cap, static_cast<int>(desc->E), num_sms, s);
@@ -678,6 +710,7 @@ int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_
     n += 2;                                                 // gate.up, down
     if (p.gemm) n += 1;                                     // sorted f16 copy of x
     if (!p.fuse_combine) n += 1;                            // combine
+    if (desc->act_quant) n += 2;                            // the coded x and h
     return n;
 }
 

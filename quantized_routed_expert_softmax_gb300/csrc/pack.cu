@@ -51,6 +51,44 @@ __global__ void __launch_bounds__(256) q8_0_quantize_kernel(const float* __restr
     }
 }
 
+// --------------------------------------------------------------- Q8_0 activations (quantise-dequantise)
+// The expert inputs of the activation-quantised path (the CPU engines' Q8_0 activation
+// quantiser before their Q8_0 x Q8_0 block dots: "Running Gemma 4 26B at 5 tokens/s on a
+// 13-year-old Xeon without a GPU", sections "A three-step fix" and "Narrowing down the cause"):
+// every block of 32 along a row is coded with the weight packer's arithmetic above, and the
+// kernel writes the value each code stands for, q * fp16(d), which is exact in fp32 (8 x 11
+// significant bits).  The expert kernels then meet these values exactly (their f16 hi + lo
+// operands carry 22 bits), so every block's code products are summed as the integers they are
+// and scaled by both fp16 scales, up to fp32 rounding.  Optionally also the f16 hi / lo planes
+// of the tensor-core path.  One warp per block, grid-stride.
+__global__ void __launch_bounds__(256) act_q8_0_kernel(const void* __restrict__ src, int xt, int64_t n_blocks,
+                                                        int64_t cols, float* __restrict__ dst,
+                                                        uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t blk = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; blk < n_blocks;
+         blk += warps) {
+        const int64_t nb = cols / 32;
+        const int64_t o = (blk / nb) * cols + (blk % nb) * 32 + lane;
+        const float x = xt == MOE_F32 ? static_cast<const float*>(src)[o]
+                                      : bf16_bits_to_f32(static_cast<const uint16_t*>(src)[o]);
+        const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x)));
+        const float amax = __uint_as_float(amax_bits);
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+        const int q = static_cast<int>(roundf(__fmul_rn(x, id)));
+        const float v = static_cast<float>(q) * __half2float(__float2half_rn(d));
+        dst[o] = v;
+        if (hi) {
+            const __half h = __float2half_rn(v);
+            hi[o] = __half_as_ushort(h);
+            lo[o] = __half_as_ushort(__float2half_rn(v - __half2float(h)));
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------- NVFP4
 // Per-matrix amax as uint bits (non-negative floats order like their bit patterns).
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const float* __restrict__ src, int64_t per_mat,
@@ -205,6 +243,15 @@ cudaError_t launch_q8_0_quantize(const float* src, int64_t n_mat, int64_t rows, 
     q8_0_quantize_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(src, n_blocks, rows, cols, layout,
                                                                      static_cast<uint8_t*>(dst));
     return cudaGetLastError();
+}
+
+cudaError_t launch_act_q8_0(const void* src, int xt, int64_t rows, int64_t cols, float* dst, uint16_t* hi,
+                            uint16_t* lo, int num_sms, cudaStream_t s) {
+    const int64_t n_blocks = rows * (cols / 32);
+    const int64_t want = (n_blocks * 32 + 255) / 256;
+    const int64_t grid = want < 8ll * num_sms ? want : 8ll * num_sms;   // grid-stride beyond 8 CTAs per SM
+    return launch_pdl(act_q8_0_kernel, dim3(static_cast<unsigned>(grid > 0 ? grid : 1)), dim3(256), 0, s, src, xt,
+                      n_blocks, cols, dst, hi, lo);
 }
 
 cudaError_t launch_nvfp4_pack(const float* src, int64_t n_mat, int64_t rows, int64_t cols, int layout, void* dst,

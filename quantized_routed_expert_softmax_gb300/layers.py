@@ -11,13 +11,14 @@ from . import native, synth
 
 
 def build_layer(w: synth.Workload, layer: int = 0, source: str = "cuda", keep_fp32: bool = False,
-                path: str = "auto", E_chunk: int = 16):
+                path: str = "auto", E_chunk: int = 16, act_quant: str = "none"):
     """A native.MoELayer for `w`, layer `layer`.
 
     source = "cuda": fp32 weights drawn on the device, E_chunk experts at a time;
     source = "numpy": drawn on the host with the numpy generator (small shapes), the
     same numbers the oracle tests draw.  keep_fp32 keeps the fp32 stacks on the layer
-    (attributes gate_up_f32 / down_f32) for tests that hand them to the oracle.
+    (attributes gate_up_f32 / down_f32) for tests that hand them to the oracle.  act_quant
+    "q8_0" selects the activation-quantised expert path (Q8_0 weights only).
     """
     dev = torch.device("cuda")
     router_w = torch.from_numpy(synth.router_weight(w, layer)).to(dev)
@@ -52,7 +53,8 @@ def build_layer(w: synth.Workload, layer: int = 0, source: str = "cuda", keep_fp
             keep_dn.append(b)
         else:
             del a, b
-    layer_obj = native.MoELayer(w.d, w.f, w.E, w.k, w.act, w.wfmt, router_w, gu, dn, gts, dts, path=path)
+    layer_obj = native.MoELayer(w.d, w.f, w.E, w.k, w.act, w.wfmt, router_w, gu, dn, gts, dts, path=path,
+                                act_quant=act_quant)
     if keep_fp32:
         layer_obj.gate_up_f32 = torch.cat(keep_gu)
         layer_obj.down_f32 = torch.cat(keep_dn)

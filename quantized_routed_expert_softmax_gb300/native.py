@@ -21,9 +21,11 @@ WFMT = {"q8_0": 0, "nvfp4": 1}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 LAYOUT = {"canonical": 0, "device": 1, "neuron": 2}
 PATH = {"auto": 0, "gemv": 1, "gemm": 2}
+ACT_QUANT = {"none": 0, "q8_0": 1}
 
 # Every symbol include/moe.h declares.
-EXPORTS = ["moe_q8_0_bytes", "moe_nvfp4_bytes", "moe_quantize_q8_0", "moe_pack_nvfp4", "moe_router_workspace_bytes",
+EXPORTS = ["moe_q8_0_bytes", "moe_nvfp4_bytes", "moe_quantize_q8_0", "moe_pack_nvfp4", "moe_quantize_act_q8_0",
+           "moe_router_workspace_bytes",
            "moe_router_topk", "moe_layer_workspace_bytes", "moe_layer_forward", "moe_rmsnorm_bf16",
            "moe_get_device_status", "moe_status_string", "moe_abi_version", "moe_layer_forward_launches",
            "moe_layer_forward_noalloc", "moe_layer_forward_noalloc_status", "moe_stack_forward",
@@ -43,6 +45,7 @@ class LayerDesc(ctypes.Structure):
         ("router_w", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
         ("gate_up_tscale", ctypes.c_void_p), ("down_tscale", ctypes.c_void_p),
         ("l2_prefetch", ctypes.c_void_p), ("l2_prefetch_bytes", ctypes.c_int64),
+        ("act_quant", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -67,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "moe_nvfp4_bytes": (SZ, [I64, I64]),
             "moe_quantize_q8_0": (I32, [P, I64, I64, I64, I32, P, P]),
             "moe_pack_nvfp4": (I32, [P, I64, I64, I64, I32, P, P, P]),
+            "moe_quantize_act_q8_0": (I32, [P, I32, I64, I64, P, P]),
             "moe_router_workspace_bytes": (SZ, [I64, I64]),
             "moe_router_topk": (I32, [P, I32, P, I64, I64, I64, I32, P, P, P, P, SZ, P]),
             "moe_layer_workspace_bytes": (SZ, [ctypes.POINTER(LayerDesc), I64]),
@@ -141,6 +145,16 @@ def pack_nvfp4(src, layout: str = "device", out=None, tscale=None, stream=None):
     return out, tscale
 
 
+def quantize_act_q8_0(x, out=None, stream=None):
+    """moe_quantize_act_q8_0: x [rows, cols] fp32 or bf16 -> the Q8_0-coded values, fp32."""
+    import torch
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    _check("moe_quantize_act_q8_0", lib().moe_quantize_act_q8_0(_ptr(x), _x_dtype(x), x.shape[0], x.shape[1],
+                                                                 _ptr(out), _stream(stream)))
+    return out
+
+
 def _x_dtype(x) -> int:
     import torch
     if x.dtype == torch.float32:
@@ -191,12 +205,13 @@ class MoELayer:
     """
 
     def __init__(self, d, f, E, k, act, wfmt, router_w, gate_up, down, gate_up_tscale=None, down_tscale=None,
-                 path: str = "auto"):
+                 path: str = "auto", act_quant: str = "none"):
         self.d, self.f, self.E, self.k, self.act, self.wfmt = d, f, E, k, act, wfmt
         self.router_w, self.gate_up, self.down = router_w, gate_up, down
         self.gate_up_tscale, self.down_tscale = gate_up_tscale, down_tscale
         self.desc = LayerDesc(d, f, E, k, ACT[act], WFMT[wfmt], PATH[path], _ptr(router_w), _ptr(gate_up), _ptr(down),
                               _ptr(gate_up_tscale), _ptr(down_tscale))
+        self.desc.act_quant = ACT_QUANT[act_quant]
         self._ws = None
         self._ws_tokens = 0
 
@@ -217,10 +232,12 @@ class MoELayer:
         return n
 
     def workspace(self, T: int):
-        """A zero-filled workspace for up to T tokens (kept and reused)."""
+        """A zero-filled workspace for up to T tokens with the current descriptor (kept, and
+        replaced by a larger one when T or the descriptor needs more)."""
         import torch
-        if self._ws is None or self._ws_tokens < T:
-            self._ws = torch.zeros(self.workspace_bytes(T), dtype=torch.uint8, device=self.router_w.device)
+        need = self.workspace_bytes(T)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.zeros(need, dtype=torch.uint8, device=self.router_w.device)
             self._ws_tokens = T
         return self._ws
 

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.moe_abi_version() == 10200
+    assert L.moe_abi_version() == 10300
     for s in range(8):
         assert L.moe_status_string(s).decode().startswith(native.STATUS_NAMES[s])
 
@@ -67,6 +67,22 @@ def test_packer_validation(L):
     assert P(FAKE, 1, 32, 64, 9, FAKE, FAKE, None) == 1
 
 
+def test_activation_quantiser_validation(L):
+    Q = L.moe_quantize_act_q8_0
+    assert Q(None, 0, 4, 64, FAKE, None) == 1
+    assert Q(FAKE, 2, 4, 64, FAKE, None) == 1       # bad dtype
+    assert Q(FAKE, 0, 4, 48, FAKE, None) == 2       # cols a multiple of 32
+    assert Q(FAKE + 4, 0, 4, 64, FAKE, None) == 3
+    assert Q(FAKE, 1, 0, 64, FAKE, None) == 0       # nothing to do, nothing launched
+
+
+def test_activation_quantised_layer_workspace(L):
+    # the coded expert input takes T * d fp32 more
+    plain = L.moe_layer_workspace_bytes(ctypes.byref(_desc()), 64)
+    coded = L.moe_layer_workspace_bytes(ctypes.byref(_desc(act_quant=1)), 64)
+    assert coded >= plain + 64 * 256 * 4
+
+
 def test_router_validation(L):
     R = L.moe_router_topk
     assert R(FAKE, 0, FAKE, 4, 256, 8, 0, FAKE, FAKE, None, None, 0, None) == 1    # k = 0
@@ -94,6 +110,8 @@ def test_layer_validation(L):
         (_desc(d=200), 2), (_desc(f=500), 2), (_desc(E=6), 2), (_desc(E=2048), 2), (_desc(router_w=None), 1),
         (_desc(wfmt=1), 1),                       # NVFP4 needs tensor scales
         (_desc(w_down=FAKE + 8), 3),
+        (_desc(act_quant=2), 1),                  # unknown activation quantiser
+        (_desc(act_quant=1, wfmt=1, gate_up_tscale=FAKE, down_tscale=FAKE), 5),   # Q8_0 activations need Q8_0 weights
     ]
     for desc, want in cases:
         assert F(ctypes.byref(desc), FAKE, 0, 16, None, None, FAKE, FAKE, need, None, None) == want

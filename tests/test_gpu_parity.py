@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from oracle_bridge import TOL, assert_close, oracle_layer, to_numpy_x
+from oracle_bridge import TOL, assert_close, check_act_quant, oracle_layer, to_numpy_x
 from quantized_routed_expert_softmax_gb300 import layers, native, synth
 
 pytestmark = pytest.mark.gpu
@@ -423,11 +423,12 @@ def dense_sample(tr, T, k, tile, n_min=64):
     return sorted(rows)
 
 
-def _full_case(name, T, sample=None, idx_in=None, w_in=None, path="auto", tile=None):
+def _full_case(name, T, sample=None, idx_in=None, w_in=None, path="auto", tile=None, act_quant="none"):
     """One full-size layer against the oracle: every token (sample None), the listed tokens,
-    or (tile given) the dense_sample of the layer's own permutation."""
+    or (tile given) the dense_sample of the layer's own permutation.  act_quant "q8_0": the
+    activation-quantised expert path on both sides."""
     w = synth.WORKLOADS[name]
-    L = layers.build_layer(w, keep_fp32=True, path=path)
+    L = layers.build_layer(w, keep_fp32=True, path=path, act_quant=act_quant)
     x = synth.tokens_cuda(w, T, tag="parity")
     tr = {}
     ii = None if idx_in is None else torch.from_numpy(idx_in).cuda()
@@ -447,7 +448,7 @@ def _full_case(name, T, sample=None, idx_in=None, w_in=None, path="auto", tile=N
     ol = oracle_layer(w, W, lambda e: L.gate_up_f32[e].cpu().numpy(), lambda e: L.down_f32[e].cpu().numpy(),
                       need.ravel())
     ref = ol.forward(xs, idx_in=None if idx_in is None else idx_in[rows],
-                     w_in=None if w_in is None else w_in[rows])
+                     w_in=None if w_in is None else w_in[rows], act_q8=act_quant == "q8_0")
     # the packed bytes of the experts used, bit for bit
     for e in sorted(set(int(v) for v in need.ravel()))[:3]:
         if w.wfmt == "q8_0":
@@ -460,7 +461,11 @@ def _full_case(name, T, sample=None, idx_in=None, w_in=None, path="auto", tile=N
         assert np.array_equal(tr["logits"].cpu().numpy()[rows].view(np.uint32), ref["logits"].view(np.uint32))
     assert np.array_equal(tr["idx"].cpu().numpy()[rows], ref["idx"])
     assert np.allclose(tr["w"].cpu().numpy()[rows], ref["w"], rtol=1e-6, atol=0)
-    ratio = assert_close(out[rows], ref["out"])
+    if act_quant == "q8_0":
+        check_act_quant(w, ol, rows, out[rows], tr, ref)
+        ratio = None
+    else:
+        ratio = assert_close(out[rows], ref["out"])
     # invariants of the full-size permutation
     off = tr["offsets"].cpu().numpy()
     perm = tr["perm"].cpu().numpy()
