@@ -143,7 +143,7 @@ def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0, cache=
 
     have_cuda = torch.cuda.is_available()
     act = oracle.ACT_SWIGLU if w.act == "swiglu" else oracle.ACT_RELU2
-    fmt = oracle.W_Q8_0 if w.wfmt == "q8_0" else oracle.W_NVFP4
+    fmt = {"q8_0": oracle.W_Q8_0, "nvfp4": oracle.W_NVFP4, "int8pc": oracle.W_INT8PC}[w.wfmt]
     tu = min(T, 8)
     cache = {} if cache is None else cache
 
@@ -166,6 +166,8 @@ def oracle_sample(w, T, layers, max_units, time_budget_s, warmup_units=0, cache=
                 a, b = synth.expert_weights(w, layer, e)
             if w.wfmt == "q8_0":
                 gu[e], dn[e] = oracle.q8_0_quantize(a), oracle.q8_0_quantize(b)
+            elif w.wfmt == "int8pc":
+                gu[e], dn[e] = oracle.int8pc_quantize(a), oracle.int8pc_quantize(b)
             else:
                 gu[e], gts[e] = oracle.nvfp4_quantize(a)
                 dn[e], dts[e] = oracle.nvfp4_quantize(b)
@@ -724,9 +726,12 @@ def run_reference(args, rank, world):
 
 
 # Further configurations measured by the default run, each with its own workload, roofline and
-# oracle baseline: prefill on the headline stack's own weights (Gemma shape, T = 512), the
-# Nemotron-shaped NVFP4 ReLU^2 stack at one token, and MiniMax-shaped prefill (T = 4096).
-SECONDARY = [("gemma", 512, 30, 20, "none"), ("gemma", 1, 30, 400, "q8_0"), ("nemotron", 1, 40, 400, "none"),
+# oracle baseline: prefill on the headline stack's own weights (Gemma shape, T = 512) and its
+# activation-quantised decode, per-channel int8 experts on the Gemma shape (T = 1 and 64), the
+# Nemotron-shaped NVFP4 ReLU^2 stack at one token, and MiniMax-shaped prefill (T = 4096), plain
+# and activation-quantised.
+SECONDARY = [("gemma", 512, 30, 20, "none"), ("gemma", 1, 30, 400, "q8_0"), ("gemma_int8pc", 1, 8, 400, "none"),
+             ("gemma_int8pc", 64, 8, 100, "none"), ("nemotron", 1, 40, 400, "none"),
              ("minimax", 4096, 8, 10, "none"), ("minimax", 4096, 8, 10, "q8_0")]
 
 

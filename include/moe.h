@@ -57,7 +57,10 @@ typedef enum {
 } moe_status;
 
 typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_RELU2 = 1 } moe_act;
-typedef enum { MOE_W_Q8_0 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
+/* Expert weight formats.  INT8PC: per-channel int8 (the Inferentia page, "Squeezing a 26B MoE
+ * onto the cheapest Inferentia instance", section "Wall 1: the memory math": experts in int8
+ * with one scale per output channel): per row s = amax/127 (fp32), q = round-half-away(x / s). */
+typedef enum { MOE_W_Q8_0 = 0, MOE_W_NVFP4 = 1, MOE_W_INT8PC = 2 } moe_wfmt;
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
 /*
@@ -68,26 +71,31 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  *          fp16 scale (little endian) then 32 int8 codes: 34 bytes per 32 values.
  *   NVFP4: all E2M1 codes row-major, two per byte (even element in the low nibble),
  *          then all E4M3 block scales row-major (one per 16 values).
+ *   INT8PC: all int8 codes row-major, then one fp32 scale per row (little endian).
  * MOE_LAYOUT_DEVICE  (what moe_layer_forward reads for gate/up matrices, and for the
  *                     down matrix in Q8_0)
  *   Q8_0 : panel b = columns 32b..32b+31: the 32 codes of every row (rows in order),
  *          then the fp16 scale of every row.  Panel size rows*34 bytes.
  *   NVFP4: panel P = columns 64P..64P+63: the 32 code bytes of every row, then the 4
  *          scale bytes of every row.  Panel size rows*36 bytes.
+ *   INT8PC: the fp32 scale of every row first, then panel b = columns 32b..32b+31: the 32
+ *          codes of every row (rows in order).  Panel size rows*32 bytes.
  * MOE_LAYOUT_NEURON  (NVFP4 down matrices [d, f] only; what moe_layer_forward reads)
  *   Nemotron page, "How the engine works", step 4: for each group g of 16 neurons
  *   (columns), each neuron's codes for rows 0..rows-1 contiguous (rows/2 bytes, row r
  *   in the low nibble of byte r/2 when r is even), then the rows scale bytes of the
  *   group.  A pure byte permutation of the canonical layout, same size.
- * Every layout of a matrix has the same size (moe_q8_0_bytes / moe_nvfp4_bytes); a
+ * Every layout of a matrix has the same size (moe_q8_0_bytes / moe_nvfp4_bytes /
+ * moe_int8pc_bytes); a
  * stack of n_mat matrices is the matrices back to back.
  */
 typedef enum { MOE_LAYOUT_CANONICAL = 0, MOE_LAYOUT_DEVICE = 1, MOE_LAYOUT_NEURON = 2 } moe_layout;
 
 /* Which expert kernels moe_layer_forward uses.  GEMV: weight-streaming matrix-vector
  * kernels (a few tokens per expert).  GEMM: grouped GEMMs on the tensor cores (tcgen05),
- * which need f a multiple of 64 (128 for ReLU^2); forcing GEMM on another shape returns
- * MOE_ERR_UNSUPPORTED.  AUTO takes GEMM when T*k >= 8*E and the shape allows it; for ONE
+ * which need f a multiple of 64 (128 for ReLU^2) and Q8_0 or NVFP4 weights; forcing GEMM on
+ * another shape or format returns MOE_ERR_UNSUPPORTED (AUTO runs INT8PC weights on the GEMV
+ * kernels at every T).  AUTO takes GEMM when T*k >= 8*E and the shape allows it; for ONE
  * token with Q8_0 SwiGLU (k*f <= 16384) or NVFP4 ReLU^2 experts (d <= 8192) it runs the whole
  * layer as a single cooperative kernel, one CTA per SM, when the device supports cooperative
  * launches (the same results within the output tolerance; routing, weights and the
@@ -110,6 +118,7 @@ typedef enum { MOE_ACTQ_NONE = 0, MOE_ACTQ_Q8_0 = 1 } moe_act_quant;
  * (NVFP4).  Returns 0 for non-positive or non-multiple sizes. */
 size_t moe_q8_0_bytes(int64_t rows, int64_t cols);
 size_t moe_nvfp4_bytes(int64_t rows, int64_t cols);
+size_t moe_int8pc_bytes(int64_t rows, int64_t cols);   /* rows*cols + 4*rows (cols a multiple of 32) */
 
 /*
  * moe_quantize_q8_0 -- Q8_0 weight packer (the Xeon page's Q8_0 experts; block of 32
@@ -140,6 +149,18 @@ moe_status moe_quantize_q8_0(const float* src, int64_t n_mat, int64_t rows, int6
  */
 moe_status moe_pack_nvfp4(const float* src, int64_t n_mat, int64_t rows, int64_t cols, moe_layout layout,
                           void* dst, float* tensor_scale, moe_stream_t stream);
+
+/*
+ * moe_quantize_int8pc -- per-channel int8 weight packer (MOE_W_INT8PC; Inferentia page, "Wall
+ * 1: the memory math", whose page gives sizes and quality but no recipe).  Per row:
+ *   s = amax/127 (fp32 IEEE divide); q = round-half-away(x / s) (fp32 IEEE divide), 0 when
+ *   s = 0; codes int8, the scale stored as fp32.
+ * src device fp32 [n_mat][rows][cols]; dst device n_mat * moe_int8pc_bytes(rows, cols) bytes in
+ * `layout` (CANONICAL or DEVICE).
+ * Errors: INVALID_ARG, SHAPE (rows and cols positive multiples of 32), ALIGNMENT, CUDA.
+ */
+moe_status moe_quantize_int8pc(const float* src, int64_t n_mat, int64_t rows, int64_t cols, moe_layout layout,
+                               void* dst, moe_stream_t stream);
 
 /*
  * moe_quantize_act_q8_0 -- the activation quantiser of MOE_ACTQ_Q8_0, as values: every block
@@ -186,7 +207,7 @@ typedef struct {
     const float* router_w;        /* fp32 [d][E] */
     const void* w_gate_up;        /* E matrices [rows_gu][d], MOE_LAYOUT_DEVICE, back to back;
                                      SwiGLU: rows 0..f-1 gate, f..2f-1 up */
-    const void* w_down;           /* E matrices [d][f]: Q8_0 MOE_LAYOUT_DEVICE, NVFP4 MOE_LAYOUT_NEURON */
+    const void* w_down;           /* E matrices [d][f]: Q8_0 / INT8PC MOE_LAYOUT_DEVICE, NVFP4 MOE_LAYOUT_NEURON */
     const float* gate_up_tscale;  /* NVFP4: fp32 [E] tensor scales of the gate/up matrices */
     const float* down_tscale;     /* NVFP4: fp32 [E] tensor scales of the down matrices */
     const void* l2_prefetch;      /* optional, may be NULL: device bytes to pull into L2 while this

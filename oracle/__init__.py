@@ -84,6 +84,7 @@ def _declare(L: ctypes.CDLL) -> None:
         "orc_q8_0_dequant": (None, [_P, _I64, _I64, _P]),
         "orc_q8_0_vec_dot": (ctypes.c_double, [_P, _P, _I64]),
         "orc_q8_0_permute": (None, [_P, _I64, _I64, _I, _P]),
+        "orc_int8pc_permute": (None, [_P, _I64, _I64, _I, _P]),
         "orc_nvfp4_tensor_scale": (ctypes.c_float, [_P, _I64, _I64]),
         "orc_nvfp4_quantize": (None, [_P, _I64, _I64, _P, _P]),
         "orc_nvfp4_dequant": (None, [_P, _I64, _I64, ctypes.c_float, _P]),
@@ -168,6 +169,22 @@ def int8pc_dequant(q: np.ndarray, rows: int, cols: int) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.uint8)
     out = np.empty((rows, cols), dtype=np.float64)
     lib().orc_int8pc_dequant(_ptr(q), rows, cols, _ptr(out))
+    return out
+
+
+def int8pc_to_device(canon: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """orc_int8pc_permute(+1): canonical per-channel int8 bytes -> the device layout (the row
+    scales first, then panels of 32 columns)."""
+    canon = np.ascontiguousarray(canon, dtype=np.uint8)
+    out = np.empty_like(canon)
+    lib().orc_int8pc_permute(_ptr(canon), rows, cols, 1, _ptr(out))
+    return out
+
+
+def int8pc_from_device(dev: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    dev = np.ascontiguousarray(dev, dtype=np.uint8)
+    out = np.empty_like(dev)
+    lib().orc_int8pc_permute(_ptr(dev), rows, cols, -1, _ptr(out))
     return out
 
 

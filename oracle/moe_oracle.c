@@ -296,6 +296,26 @@ double orc_q8_0_vec_dot(const uint8_t* a, const uint8_t* b, int64_t nb) {
     return acc;
 }
 
+/* Device layout for per-channel int8: a byte permutation of the canonical bytes.  First the
+ * rows' fp32 scales (4 bytes each, rows in order), then panel b (columns 32b..32b+31): the 32
+ * codes of every row (rows in order, 32 bytes each).  dir = +1 maps canonical -> device,
+ * dir = -1 maps device -> canonical. */
+void orc_int8pc_permute(const uint8_t* src, int64_t rows, int64_t cols, int dir, uint8_t* dst) {
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            const int64_t canon = r * cols + c;
+            const int64_t dev = 4 * rows + (c / 32) * (rows * 32) + r * 32 + (c % 32);
+            if (dir > 0) dst[dev] = src[canon];
+            else dst[canon] = src[dev];
+        }
+        for (int64_t i = 0; i < 4; ++i) {
+            const int64_t canon = rows * cols + 4 * r + i, dev = 4 * r + i;
+            if (dir > 0) dst[dev] = src[canon];
+            else dst[canon] = src[dev];
+        }
+    }
+}
+
 /* Device layout for Q8_0: a byte permutation of the canonical blocks, panel by panel
  * along K.  Panel b (columns 32b..32b+31): the 32 codes of every row (rows in order,
  * 32 bytes each), then the fp16 scales of every row (2 bytes each).  dir = +1 maps

@@ -11,6 +11,7 @@ namespace moe {
 cudaError_t launch_q8_0_quantize(const float*, int64_t, int64_t, int64_t, int, void*, cudaStream_t);
 cudaError_t launch_nvfp4_pack(const float*, int64_t, int64_t, int64_t, int, void*, float*, cudaStream_t);
 cudaError_t launch_act_q8_0(const void*, int, int64_t, int64_t, float*, uint16_t*, uint16_t*, int, cudaStream_t);
+cudaError_t launch_int8pc_quantize(const float*, int64_t, int64_t, int64_t, int, void*, cudaStream_t);
 cudaError_t launch_router_logits(const void*, int, const float*, int64_t, int64_t, int64_t, float*, cudaStream_t);
 cudaError_t launch_topk_softmax(const float*, int64_t, int64_t, int, int32_t*, float*, cudaStream_t);
 cudaError_t launch_route_small(const float*, const int32_t*, const float*, int64_t, int64_t, int, int,
@@ -49,6 +50,13 @@ constexpr size_t kSmemBudget = 96 * 1024;        // token rows staged per expert
 constexpr int64_t kPrefetchBudget = 64ll << 20;   // down weights prefetched into L2 (of 126 MB)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Bytes of one quantised matrix [rows, cols] in the format (every layout of a format has them).
+int64_t matrix_bytes(int wfmt, int64_t rows, int64_t cols) {
+    if (wfmt == MOE_W_Q8_0) return static_cast<int64_t>(moe_q8_0_bytes(rows, cols));
+    if (wfmt == MOE_W_NVFP4) return static_cast<int64_t>(moe_nvfp4_bytes(rows, cols));
+    return static_cast<int64_t>(moe_int8pc_bytes(rows, cols));
+}
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -191,6 +199,7 @@ bool decode_split_fits(const moe_layer_desc* d, const DecodeSplit& sp, int xt) {
 
 // The GEMM path tiles rows by 128 (SwiGLU gate.up: 64 neurons' gate and up rows) and K by 64.
 bool gemm_shape_ok(const moe_layer_desc* d) {
+    if (d->wfmt == MOE_W_INT8PC) return false;   // per-channel int8 runs on the GEMV kernels
     if (d->f % 64 != 0 || d->d % 64 != 0) return false;
     if (d->act == MOE_ACT_RELU2 && d->f % 128 != 0) return false;
     return true;
@@ -221,10 +230,9 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     p.tt_gu = pow2(p.tt_gu);
     p.tt_dn = pow2(p.tt_dn);
     p.small_route = (T <= kSmallT && p.P <= kSmallPairs && T * d->E <= kFusedRouteLogits);
-    const int64_t rows_per_tile = (d->wfmt == MOE_W_Q8_0) ? 32 : 256;
+    const int64_t rows_per_tile = (d->wfmt == MOE_W_NVFP4) ? 256 : 32;
     p.fuse_combine = T * rows_per_tile <= 256;
-    const int64_t dn_bytes = static_cast<int64_t>(d->wfmt == MOE_W_Q8_0 ? moe_q8_0_bytes(d->d, d->f)
-                                                                          : moe_nvfp4_bytes(d->d, d->f));
+    const int64_t dn_bytes = matrix_bytes(d->wfmt, d->d, d->f);
     p.prefetch_down = static_cast<int64_t>(p.slot_cap) * dn_bytes <= kPrefetchBudget;
     // many tokens per expert (at least 8 on average): tensor-core GEMMs
     p.gemm = gemm_shape_ok(d) && (d->path == MOE_PATH_GEMM || (d->path == MOE_PATH_AUTO && p.P >= 8 * d->E));
@@ -343,12 +351,12 @@ Workspace bind(void* base, const Layout& L) {
 moe_status validate_desc(const moe_layer_desc* d) {
     if (!d) return MOE_ERR_INVALID_ARG;
     if (d->act != MOE_ACT_SWIGLU && d->act != MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
-    if (d->wfmt != MOE_W_Q8_0 && d->wfmt != MOE_W_NVFP4) return MOE_ERR_INVALID_ARG;
+    if (d->wfmt != MOE_W_Q8_0 && d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_INT8PC) return MOE_ERR_INVALID_ARG;
     if (d->path != MOE_PATH_AUTO && d->path != MOE_PATH_GEMV && d->path != MOE_PATH_GEMM) return MOE_ERR_INVALID_ARG;
     if (d->E < 1 || d->E > kMaxE || d->E % 4 != 0) return MOE_ERR_SHAPE;
     if (d->k < 1 || d->k > kMaxK || d->k > d->E) return MOE_ERR_INVALID_ARG;
     if (d->d < 256 || d->d > kMaxDim || d->d % 256 != 0) return MOE_ERR_SHAPE;
-    const int64_t fq = (d->wfmt == MOE_W_Q8_0) ? 32 : 64;
+    const int64_t fq = (d->wfmt == MOE_W_NVFP4) ? 64 : 32;
     if (d->f < fq || d->f > kMaxF || d->f % fq != 0) return MOE_ERR_SHAPE;
     if (d->act == MOE_ACT_RELU2 && d->f % 32 != 0) return MOE_ERR_SHAPE;
     if (!d->router_w || !d->w_gate_up || !d->w_down) return MOE_ERR_INVALID_ARG;
@@ -450,6 +458,11 @@ size_t moe_q8_0_bytes(int64_t rows, int64_t cols) {
     return static_cast<size_t>(rows) * static_cast<size_t>(cols / 32) * 34;
 }
 
+size_t moe_int8pc_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0 || cols % 32 != 0) return 0;
+    return static_cast<size_t>(rows) * static_cast<size_t>(cols) + 4 * static_cast<size_t>(rows);
+}
+
 size_t moe_nvfp4_bytes(int64_t rows, int64_t cols) {
     if (rows <= 0 || cols <= 0 || cols % 16 != 0) return 0;
     return static_cast<size_t>(rows) * static_cast<size_t>(cols) / 2 + static_cast<size_t>(rows) * cols / 16;
@@ -464,6 +477,18 @@ moe_status moe_quantize_q8_0(const float* src, int64_t n_mat, int64_t rows, int6
     if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_ALIGNMENT;
     if (n_mat == 0) return MOE_OK;
     return cuda_status(launch_q8_0_quantize(src, n_mat, rows, cols, layout, dst, stream));
+}
+
+moe_status moe_quantize_int8pc(const float* src, int64_t n_mat, int64_t rows, int64_t cols, moe_layout layout,
+                               void* dst, moe_stream_t stream) {
+    if (!src || !dst || n_mat < 0) return MOE_ERR_INVALID_ARG;
+    if (layout != MOE_LAYOUT_CANONICAL && layout != MOE_LAYOUT_DEVICE) return MOE_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 32 != 0 || rows > kMaxTokens || cols > kMaxDim)
+        return MOE_ERR_SHAPE;
+    if (n_mat > 65535) return MOE_ERR_SHAPE;
+    if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_ALIGNMENT;
+    if (n_mat == 0) return MOE_OK;
+    return cuda_status(launch_int8pc_quantize(src, n_mat, rows, cols, layout, dst, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_pack_nvfp4(const float* src, int64_t n_mat, int64_t rows, int64_t cols, moe_layout layout, void* dst,
@@ -635,7 +660,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.tt_gu = p.tt_gu;
     a.tt_dn = p.tt_dn;
     {   // warps per gate.up tile: each warp should stream at least 12 K panels
-        const int npan = static_cast<int>(desc->wfmt == MOE_W_Q8_0 ? desc->d / 32 : desc->d / 64);
+        const int npan = static_cast<int>(desc->wfmt == MOE_W_NVFP4 ? desc->d / 64 : desc->d / 32);
         int wpt = 8;
         while (wpt > 1 && npan / wpt < 12) wpt /= 2;
         a.gu_wpt = wpt;
@@ -649,13 +674,8 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.out = out;
     a.w_gu = static_cast<const uint8_t*>(desc->w_gate_up);
     a.w_dn = static_cast<const uint8_t*>(desc->w_down);
-    if (desc->wfmt == MOE_W_Q8_0) {
-        a.gu_bytes = static_cast<int64_t>(moe_q8_0_bytes(a.rows_gu, desc->d));
-        a.dn_bytes = static_cast<int64_t>(moe_q8_0_bytes(desc->d, desc->f));
-    } else {
-        a.gu_bytes = static_cast<int64_t>(moe_nvfp4_bytes(a.rows_gu, desc->d));
-        a.dn_bytes = static_cast<int64_t>(moe_nvfp4_bytes(desc->d, desc->f));
-    }
+    a.gu_bytes = matrix_bytes(desc->wfmt, a.rows_gu, desc->d);
+    a.dn_bytes = matrix_bytes(desc->wfmt, desc->d, desc->f);
     a.pf = static_cast<const uint8_t*>(desc->l2_prefetch);
     a.pf_bytes = desc->l2_prefetch ? (desc->l2_prefetch_bytes & ~static_cast<int64_t>(15)) : 0;
     a.gu_ts = desc->gate_up_tscale;

@@ -79,13 +79,17 @@ __device__ __forceinline__ void stream_panels_dense(const uint8_t* W, int rows, 
     const uint64_t pol = l2_evict_first_policy();
     constexpr int kScb = (FMT == MOE_W_Q8_0) ? 2 : 4;       // scale bytes per row
     constexpr int kScLanes = kScb;                           // lanes copying one block's 16 rows of scales
-    const int64_t stride = static_cast<int64_t>(rows) * (32 + kScb);
-    const uint8_t* P = W + static_cast<int64_t>(pb) * stride;
+    // per-channel int8: panels of codes only, after the rows' fp32 scales (read again per panel)
+    constexpr bool kPc = FMT == MOE_W_INT8PC;
+    const int64_t stride = static_cast<int64_t>(rows) * (kPc ? 32 : 32 + kScb);
+    const uint8_t* P = W + (kPc ? static_cast<int64_t>(rows) * 4 : 0) + static_cast<int64_t>(pb) * stride;
     const uint8_t* srcA = P + rowA * 32 + lane * 16;
     const uint8_t* srcB = P + rowB * 32 + lane * 16;
     const bool copies_scales = lane < 2 * kScLanes;
     const int sl = lane < kScLanes ? lane : lane - kScLanes;
-    const uint8_t* srcS = P + static_cast<int64_t>(rows) * 32 + (lane < kScLanes ? rowA : rowB) * kScb + sl * 16;
+    const uint8_t* srcS = (kPc ? W : P + static_cast<int64_t>(rows) * 32) + (lane < kScLanes ? rowA : rowB) * kScb +
+                          sl * 16;
+    const int64_t strideS = kPc ? 0 : stride;
     const uint32_t offS = 1024 + (lane < kScLanes ? 0 : 16 * kScb) + sl * 16;
     const uint32_t ring_addr = smem_addr(ring);
     const int n = pe - pb;
@@ -96,7 +100,7 @@ __device__ __forceinline__ void stream_panels_dense(const uint8_t* W, int rows, 
         if (copies_scales) cp_async16(slot + offS, srcS);
         srcA += stride;
         srcB += stride;
-        srcS += stride;
+        srcS += strideS;
     };
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(256, 3) gate_up_gemv_kernel(ExpertArgs a) {
     const int rowA = (ACT == MOE_ACT_SWIGLU) ? tile * 16 : tile * 32;
     const int rowB = (ACT == MOE_ACT_SWIGLU) ? a.f + tile * 16 : tile * 32 + 16;
     const uint8_t* W = a.w_gu + static_cast<int64_t>(e) * a.gu_bytes;
-    const int npan = (FMT == MOE_W_Q8_0) ? a.d / 32 : a.d / 64;
+    const int npan = (FMT == MOE_W_NVFP4) ? a.d / 64 : a.d / 32;
     const int pb = live ? part * npan / wpt : 0, pe = live ? (part + 1) * npan / wpt : 0;
     if (threadIdx.x < 8) act_bits[threadIdx.x] = 0;
     if (threadIdx.x == 0) {
@@ -321,6 +325,7 @@ __device__ __forceinline__ void combine_rows_if_last(const ExpertArgs& a, int ti
 // groups are inactive are skipped.  grid: (d/32, slot capacity).
 constexpr int kDnWarps = 4;
 
+template <int FMT>   // Q8_0 or per-channel int8
 __global__ void __launch_bounds__(kDnWarps * 32, 6) down_q8_gemv_kernel(ExpertArgs a) {
     const int slot = blockIdx.y;
     const int warp = threadIdx.x >> 5;
@@ -345,7 +350,7 @@ __global__ void __launch_bounds__(kDnWarps * 32, 6) down_q8_gemv_kernel(ExpertAr
     const int npre = cnt > 0 ? min(kStages, pe - pb) : 0;
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
-        if (s < npre) issue_panel_block<MOE_W_Q8_0>(smem_addr(ring + s * kSlotBytes), W, a.d, rowA, rowB, pb + s, pol, 0);
+        if (s < npre) issue_panel_block<FMT>(smem_addr(ring + s * kSlotBytes), W, a.d, rowA, rowB, pb + s, pol, 0);
         cp_async_commit();
     }
     pdl_wait();
@@ -366,7 +371,7 @@ __global__ void __launch_bounds__(kDnWarps * 32, 6) down_q8_gemv_kernel(ExpertAr
 #pragma unroll
             for (int s = 0; s < kStages; ++s) {
                 if (s < npre)
-                    issue_panel_block<MOE_W_Q8_0>(smem_addr(ring + s * kSlotBytes), W, a.d, rowA, rowB, pb + s, pol,
+                    issue_panel_block<FMT>(smem_addr(ring + s * kSlotBytes), W, a.d, rowA, rowB, pb + s, pol,
                                                   skip_of(pb + s));
                 cp_async_commit();
             }
@@ -377,11 +382,11 @@ __global__ void __launch_bounds__(kDnWarps * 32, 6) down_q8_gemv_kernel(ExpertAr
             cp_async_wait<kStages - 1>();
             __syncwarp();
             const int s = i % kStages;
-            panel_mma<MOE_W_Q8_0>(ring + s * kSlotBytes, hs, a.f, pb + i, nt, skip_of(pb + i), acc, true, lo_off);
+            panel_mma<FMT>(ring + s * kSlotBytes, hs, a.f, pb + i, nt, skip_of(pb + i), acc, true, lo_off);
             __syncwarp();
             const int bn = pb + i + kStages;
             if (bn < pe)
-                issue_panel_block<MOE_W_Q8_0>(smem_addr(ring + s * kSlotBytes), W, a.d, rowA, rowB, bn, pol, skip_of(bn));
+                issue_panel_block<FMT>(smem_addr(ring + s * kSlotBytes), W, a.d, rowA, rowB, bn, pol, skip_of(bn));
             cp_async_commit();
         }
         store_partials(red, acc);
@@ -748,6 +753,9 @@ static cudaError_t gu_dispatch(const ExpertArgs& a, int wfmt, int act, dim3 grid
                                bool configure) {
     if (wfmt == MOE_W_Q8_0 && act == MOE_ACT_SWIGLU) return gu_launch<MOE_W_Q8_0, MOE_ACT_SWIGLU>(a, grid, smem, s, configure);
     if (wfmt == MOE_W_Q8_0) return gu_launch<MOE_W_Q8_0, MOE_ACT_RELU2>(a, grid, smem, s, configure);
+    if (wfmt == MOE_W_INT8PC && act == MOE_ACT_SWIGLU)
+        return gu_launch<MOE_W_INT8PC, MOE_ACT_SWIGLU>(a, grid, smem, s, configure);
+    if (wfmt == MOE_W_INT8PC) return gu_launch<MOE_W_INT8PC, MOE_ACT_RELU2>(a, grid, smem, s, configure);
     if (act == MOE_ACT_SWIGLU) return gu_launch<MOE_W_NVFP4, MOE_ACT_SWIGLU>(a, grid, smem, s, configure);
     return gu_launch<MOE_W_NVFP4, MOE_ACT_RELU2>(a, grid, smem, s, configure);
 }
@@ -761,8 +769,13 @@ static cudaError_t dn_nv_launch(const ExpertArgs& a, int slot_cap, size_t smem, 
 static cudaError_t dn_dispatch(const ExpertArgs& a, int wfmt, int slot_cap, size_t smem, cudaStream_t s,
                                bool configure) {
     if (wfmt == MOE_W_Q8_0) {
-        if (configure) return allow_smem(down_q8_gemv_kernel, 200 * 1024);
-        return launch_pdl(down_q8_gemv_kernel, dim3(a.d / 32, slot_cap), dim3(kDnWarps * 32), smem, s, a);
+        if (configure) return allow_smem(down_q8_gemv_kernel<MOE_W_Q8_0>, 200 * 1024);
+        return launch_pdl(down_q8_gemv_kernel<MOE_W_Q8_0>, dim3(a.d / 32, slot_cap), dim3(kDnWarps * 32), smem, s, a);
+    }
+    if (wfmt == MOE_W_INT8PC) {
+        if (configure) return allow_smem(down_q8_gemv_kernel<MOE_W_INT8PC>, 200 * 1024);
+        return launch_pdl(down_q8_gemv_kernel<MOE_W_INT8PC>, dim3(a.d / 32, slot_cap), dim3(kDnWarps * 32), smem, s,
+                          a);
     }
     switch (a.tt_dn) {
         case 1: return dn_nv_launch<1>(a, slot_cap, smem, s, configure);
@@ -775,7 +788,7 @@ static cudaError_t dn_dispatch(const ExpertArgs& a, int wfmt, int slot_cap, size
 // device).
 cudaError_t configure_gemv_kernels() {
     ExpertArgs a{};
-    const int wf[2] = {MOE_W_Q8_0, MOE_W_NVFP4};
+    const int wf[3] = {MOE_W_Q8_0, MOE_W_NVFP4, MOE_W_INT8PC};
     const int ac[2] = {MOE_ACT_SWIGLU, MOE_ACT_RELU2};
     for (int w : wf)
         for (int c : ac) {

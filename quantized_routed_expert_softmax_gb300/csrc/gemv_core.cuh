@@ -184,10 +184,22 @@ __device__ __forceinline__ __half2 e4m3_to_h2(uint32_t byte) {
 // Copy one panel's codes of rows [rowA, rowA+16) and [rowB, rowB+16) and their scales into
 // a slot.  Chunk c (16 bytes) of a 512-byte block is row c/2, columns 16*(c%2)..; `skip`
 // bit 0 / 1 drops the first / second 16 columns (inactive neuron groups, Q8_0 down).
+// Per-channel int8 (MOE_W_INT8PC, device layout): the rows' fp32 scales first, then panels
+// of 32 codes per row; every panel of a row tile copies the same 2 x 64 bytes of scales.
 template <int FMT>
 __device__ __forceinline__ void issue_panel_block(uint32_t slot, const uint8_t* W, int rows, int rowA, int rowB,
                                                   int b, uint64_t pol, int skip) {
     const int lane = threadIdx.x & 31;
+    if (FMT == MOE_W_INT8PC) {
+        const uint8_t* P = W + static_cast<int64_t>(rows) * 4 + static_cast<int64_t>(b) * rows * 32;
+        if (!((skip >> (lane & 1)) & 1)) {
+            cp_async16_ef(slot + lane * 16, P + rowA * 32 + lane * 16, pol);
+            cp_async16_ef(slot + 512 + lane * 16, P + rowB * 32 + lane * 16, pol);
+        }
+        if (lane < 4) cp_async16(slot + 1024 + lane * 16, W + rowA * 4 + lane * 16);
+        else if (lane < 8) cp_async16(slot + 1024 + 64 + (lane - 4) * 16, W + rowB * 4 + (lane - 4) * 16);
+        return;
+    }
     const int64_t pbytes = static_cast<int64_t>(rows) * (FMT == MOE_W_Q8_0 ? 34 : 36);
     const uint8_t* P = W + b * pbytes;
     const bool keep = !((skip >> (lane & 1)) & 1);
@@ -215,7 +227,7 @@ __device__ __forceinline__ void panel_mma(const unsigned char* slot, const __hal
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const bool has_tok = g < nt;
-    if (FMT == MOE_W_Q8_0) {
+    if (FMT == MOE_W_Q8_0 || FMT == MOE_W_INT8PC) {
         uint4 xv = make_uint4(0, 0, 0, 0), xl = make_uint4(0, 0, 0, 0);
         if (has_tok) {
             xv = *reinterpret_cast<const uint4*>(xs + g * ld + b * 32 + 8 * t);
@@ -228,9 +240,16 @@ __device__ __forceinline__ void panel_mma(const unsigned char* slot, const __hal
             uint2 r0 = *reinterpret_cast<const uint2*>(cb + g * 32 + 8 * t);
             uint2 r8 = *reinterpret_cast<const uint2*>(cb + (g + 8) * 32 + 8 * t);
             if (dead) r0 = r8 = make_uint2(0u, 0u);   // a skipped group: its bytes were not copied
-            const unsigned short* sc = reinterpret_cast<const unsigned short*>(slot + 1024 + blk * 32);
-            const float s0 = __half2float(__ushort_as_half(sc[g]));
-            const float s8 = __half2float(__ushort_as_half(sc[g + 8]));
+            float s0, s8;   // Q8_0: the block's fp16 scales; per-channel int8: the rows' fp32 scales
+            if (FMT == MOE_W_Q8_0) {
+                const unsigned short* sc = reinterpret_cast<const unsigned short*>(slot + 1024 + blk * 32);
+                s0 = __half2float(__ushort_as_half(sc[g]));
+                s8 = __half2float(__ushort_as_half(sc[g + 8]));
+            } else {
+                const float* sc = reinterpret_cast<const float*>(slot + 1024 + blk * 64);
+                s0 = sc[g];
+                s8 = sc[g + 8];
+            }
             uint32_t a0, a2, a1, a3, c0, c2, c1, c3;
             s8x4_to_f16x2x2(r0.x, a0, a2);
             s8x4_to_f16x2x2(r8.x, a1, a3);

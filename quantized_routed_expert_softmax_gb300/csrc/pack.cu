@@ -51,6 +51,43 @@ __global__ void __launch_bounds__(256) q8_0_quantize_kernel(const float* __restr
     }
 }
 
+// ------------------------------------------------------------------------- per-channel int8
+// One CTA per row: s = amax/127 and q = round-half-away(x / s), both fp32 IEEE divides (the
+// per-channel int8 experts of "Squeezing a 26B MoE onto the cheapest Inferentia instance",
+// section "Wall 1: the memory math"; the page gives no recipe, this is the plainest one).
+// CANONICAL: codes row-major, then the fp32 row scales; DEVICE: the fp32 row scales first,
+// then panels of 32 columns, each the 32 codes of every row.  grid (rows, n_mat).
+__global__ void __launch_bounds__(256) int8pc_quantize_kernel(const float* __restrict__ src, int64_t rows,
+                                                               int64_t cols, int layout, uint8_t* __restrict__ dst) {
+    const int64_t r = blockIdx.x, m = blockIdx.y;
+    const float* x = src + (m * rows + r) * cols;
+    uint32_t mx = 0;
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) mx = max(mx, __float_as_uint(fabsf(x[c])));
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    __shared__ uint32_t wmax[8];
+    __shared__ float s_sc;
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = 0;
+        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) b = max(b, wmax[i]);
+        s_sc = __fdiv_rn(__uint_as_float(b), 127.0f);
+    }
+    __syncthreads();
+    const float sc = s_sc;
+    uint8_t* mat = dst + m * (rows * cols + 4 * rows);
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) {
+        const int q = sc != 0.0f ? static_cast<int>(roundf(__fdiv_rn(x[c], sc))) : 0;
+        const int64_t o = layout == MOE_LAYOUT_CANONICAL ? r * cols + c : 4 * rows + (c / 32) * rows * 32 + r * 32 + c % 32;
+        mat[o] = static_cast<uint8_t>(static_cast<int8_t>(q));
+    }
+    if (threadIdx.x == 0) {
+        const uint32_t bits = __float_as_uint(sc);
+        uint8_t* sp = mat + (layout == MOE_LAYOUT_CANONICAL ? rows * cols + 4 * r : 4 * r);
+        for (int i = 0; i < 4; ++i) sp[i] = static_cast<uint8_t>((bits >> (8 * i)) & 0xffu);
+    }
+}
+
 // --------------------------------------------------------------- Q8_0 activations (quantise-dequantise)
 // The expert inputs of the activation-quantised path (the CPU engines' Q8_0 activation
 // quantiser before their Q8_0 x Q8_0 block dots: "Running Gemma 4 26B at 5 tokens/s on a
@@ -242,6 +279,13 @@ cudaError_t launch_q8_0_quantize(const float* src, int64_t n_mat, int64_t rows, 
     const int64_t grid = (threads + 255) / 256;
     q8_0_quantize_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(src, n_blocks, rows, cols, layout,
                                                                      static_cast<uint8_t*>(dst));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_int8pc_quantize(const float* src, int64_t n_mat, int64_t rows, int64_t cols, int layout, void* dst,
+                                   cudaStream_t s) {
+    int8pc_quantize_kernel<<<dim3(static_cast<unsigned>(rows), static_cast<unsigned>(n_mat)), 256, 0, s>>>(
+        src, rows, cols, layout, static_cast<uint8_t*>(dst));
     return cudaGetLastError();
 }
 

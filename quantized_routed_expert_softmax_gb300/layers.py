@@ -26,6 +26,9 @@ def build_layer(w: synth.Workload, layer: int = 0, source: str = "cuda", keep_fp
     if w.wfmt == "q8_0":
         gu = torch.empty((w.E, native.q8_0_bytes(rows, w.d)), dtype=torch.uint8, device=dev)
         dn = torch.empty((w.E, native.q8_0_bytes(w.d, w.f)), dtype=torch.uint8, device=dev)
+    elif w.wfmt == "int8pc":
+        gu = torch.empty((w.E, native.int8pc_bytes(rows, w.d)), dtype=torch.uint8, device=dev)
+        dn = torch.empty((w.E, native.int8pc_bytes(w.d, w.f)), dtype=torch.uint8, device=dev)
     else:
         gu = torch.empty((w.E, native.nvfp4_bytes(rows, w.d)), dtype=torch.uint8, device=dev)
         dn = torch.empty((w.E, native.nvfp4_bytes(w.d, w.f)), dtype=torch.uint8, device=dev)
@@ -45,6 +48,9 @@ def build_layer(w: synth.Workload, layer: int = 0, source: str = "cuda", keep_fp
         if w.wfmt == "q8_0":
             native.quantize_q8_0(a, "device", out=gu[sl])
             native.quantize_q8_0(b, "device", out=dn[sl])
+        elif w.wfmt == "int8pc":
+            native.quantize_int8pc(a, "device", out=gu[sl])
+            native.quantize_int8pc(b, "device", out=dn[sl])
         else:
             native.pack_nvfp4(a, "device", out=gu[sl], tscale=gts[sl])
             native.pack_nvfp4(b, "neuron", out=dn[sl], tscale=dts[sl])

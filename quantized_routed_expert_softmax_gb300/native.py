@@ -17,14 +17,15 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_ALIGNMENT",
                 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_UNSUPPORTED", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_DEVICE_CHECK"}
 ACT = {"swiglu": 0, "relu2": 1}
-WFMT = {"q8_0": 0, "nvfp4": 1}
+WFMT = {"q8_0": 0, "nvfp4": 1, "int8pc": 2}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 LAYOUT = {"canonical": 0, "device": 1, "neuron": 2}
 PATH = {"auto": 0, "gemv": 1, "gemm": 2}
 ACT_QUANT = {"none": 0, "q8_0": 1}
 
 # Every symbol include/moe.h declares.
-EXPORTS = ["moe_q8_0_bytes", "moe_nvfp4_bytes", "moe_quantize_q8_0", "moe_pack_nvfp4", "moe_quantize_act_q8_0",
+EXPORTS = ["moe_q8_0_bytes", "moe_nvfp4_bytes", "moe_int8pc_bytes", "moe_quantize_q8_0", "moe_pack_nvfp4",
+           "moe_quantize_int8pc", "moe_quantize_act_q8_0",
            "moe_router_workspace_bytes",
            "moe_router_topk", "moe_layer_workspace_bytes", "moe_layer_forward", "moe_rmsnorm_bf16",
            "moe_get_device_status", "moe_status_string", "moe_abi_version", "moe_layer_forward_launches",
@@ -68,6 +69,8 @@ def lib() -> ctypes.CDLL:
         sig = {
             "moe_q8_0_bytes": (SZ, [I64, I64]),
             "moe_nvfp4_bytes": (SZ, [I64, I64]),
+            "moe_int8pc_bytes": (SZ, [I64, I64]),
+            "moe_quantize_int8pc": (I32, [P, I64, I64, I64, I32, P, P]),
             "moe_quantize_q8_0": (I32, [P, I64, I64, I64, I32, P, P]),
             "moe_pack_nvfp4": (I32, [P, I64, I64, I64, I32, P, P, P]),
             "moe_quantize_act_q8_0": (I32, [P, I32, I64, I64, P, P]),
@@ -143,6 +146,22 @@ def pack_nvfp4(src, layout: str = "device", out=None, tscale=None, stream=None):
     _check("moe_pack_nvfp4", lib().moe_pack_nvfp4(_ptr(src), n, rows, cols, LAYOUT[layout], _ptr(out),
                                                    _ptr(tscale), _stream(stream)))
     return out, tscale
+
+
+def int8pc_bytes(rows: int, cols: int) -> int:
+    return int(lib().moe_int8pc_bytes(rows, cols))
+
+
+def quantize_int8pc(src, layout: str = "device", out=None, stream=None):
+    """moe_quantize_int8pc: src fp32 [n, rows, cols] (or [rows, cols]) -> uint8 [n, bytes]."""
+    import torch
+    s3 = src if src.dim() == 3 else src.unsqueeze(0)
+    n, rows, cols = s3.shape
+    if out is None:
+        out = torch.empty((n, int8pc_bytes(rows, cols)), dtype=torch.uint8, device=src.device)
+    _check("moe_quantize_int8pc", lib().moe_quantize_int8pc(_ptr(s3), n, rows, cols, LAYOUT[layout], _ptr(out),
+                                                             _stream(stream)))
+    return out
 
 
 def quantize_act_q8_0(x, out=None, stream=None):

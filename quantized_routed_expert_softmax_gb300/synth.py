@@ -16,6 +16,7 @@ Workload shapes follow the models the pages run:
   minimax   d=6144, E=128, k=4,  f=3072, SwiGLU, Q8_0, 8 resident layers (MiniMax-M3:
             "Why can super-large MoE be distributed for inference", section 1)
   zipf      the gemma shape with Zipf(s=1.1) routing supplied by the caller
+  gemma_int8pc  the gemma shape with per-channel int8 experts
 """
 from __future__ import annotations
 
@@ -64,6 +65,10 @@ WORKLOADS = {
                      tokens=(1, 8, 64, 512, 2048, 8192)),
     "zipf_nvfp4": Workload("zipf_nvfp4", d=2816, f=704, E=128, k=8, act="swiglu", wfmt="nvfp4", x_dtype="bf16",
                            layers=1, tokens=(1, 8, 64, 512, 2048, 8192)),
+    # the Gemma layer shape with per-channel int8 experts (Inferentia page, "Wall 1": about
+    # 11.4 GB of int8 experts per rank of two)
+    "gemma_int8pc": Workload("gemma_int8pc", d=2816, f=704, E=128, k=8, act="swiglu", wfmt="int8pc", x_dtype="bf16",
+                             layers=30, tokens=(1, 4, 64)),
 }
 
 

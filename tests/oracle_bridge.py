@@ -34,11 +34,14 @@ def oracle_layer(w: synth.Workload, router_w: np.ndarray, gu_f32, dn_f32, expert
         if w.wfmt == "q8_0":
             gu[e] = oracle.q8_0_quantize(a)
             dn[e] = oracle.q8_0_quantize(b)
+        elif w.wfmt == "int8pc":
+            gu[e] = oracle.int8pc_quantize(a)
+            dn[e] = oracle.int8pc_quantize(b)
         else:
             gu[e], gts[e] = oracle.nvfp4_quantize(a)
             dn[e], dts[e] = oracle.nvfp4_quantize(b)
     act = oracle.ACT_SWIGLU if w.act == "swiglu" else oracle.ACT_RELU2
-    fmt = oracle.W_Q8_0 if w.wfmt == "q8_0" else oracle.W_NVFP4
+    fmt = {"q8_0": oracle.W_Q8_0, "nvfp4": oracle.W_NVFP4, "int8pc": oracle.W_INT8PC}[w.wfmt]
     return oracle.Layer(w.d, w.f, w.E, w.k, act, fmt, router_w, gu, dn,
                         gts if w.wfmt == "nvfp4" else None, dts if w.wfmt == "nvfp4" else None)
 

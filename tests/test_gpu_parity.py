@@ -454,6 +454,9 @@ def _full_case(name, T, sample=None, idx_in=None, w_in=None, path="auto", tile=N
         if w.wfmt == "q8_0":
             assert np.array_equal(L.gate_up[e].cpu().numpy(), oracle.q8_0_to_device(ol.gate_up[e], w.rows_gu, w.d))
             assert np.array_equal(L.down[e].cpu().numpy(), oracle.q8_0_to_device(ol.down[e], w.d, w.f))
+        elif w.wfmt == "int8pc":
+            assert np.array_equal(L.gate_up[e].cpu().numpy(), oracle.int8pc_to_device(ol.gate_up[e], w.rows_gu, w.d))
+            assert np.array_equal(L.down[e].cpu().numpy(), oracle.int8pc_to_device(ol.down[e], w.d, w.f))
         else:
             assert np.array_equal(L.gate_up[e].cpu().numpy(), oracle.nvfp4_to_panels(ol.gate_up[e], w.rows_gu, w.d))
             assert np.array_equal(L.down[e].cpu().numpy(), oracle.nvfp4_to_neuron(ol.down[e], w.d, w.f))

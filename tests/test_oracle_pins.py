@@ -208,6 +208,27 @@ def test_q8_0_device_layout_is_a_byte_permutation():
     assert np.array_equal(d[rows * 34 + rows * 32 + 10: rows * 34 + rows * 32 + 12], blk[:2])
 
 
+def test_int8pc_device_layout_is_a_byte_permutation():
+    # per-channel int8 (Inferentia page, "Wall 1: the memory math"): the device layout the
+    # weight-streaming kernels read holds the same bytes in another order
+    g = np.random.default_rng(5)
+    rows, cols = 40, 96
+    x = (g.standard_normal((rows, cols)) * 0.02).astype(np.float32)
+    c = oracle.int8pc_quantize(x)
+    d = oracle.int8pc_to_device(c, rows, cols)
+    assert np.array_equal(oracle.int8pc_from_device(d, rows, cols), c)
+    assert np.array_equal(np.sort(c), np.sort(d))
+    # hand check: row 7's fp32 scale is bytes 28..31; panel 2 (columns 64..95) starts at
+    # 4*rows + 2*rows*32 and row 7's 32 codes there are the canonical codes (7, 64..95)
+    assert np.array_equal(d[28:32], c[rows * cols + 28: rows * cols + 32])
+    p2 = 4 * rows + 2 * rows * 32
+    assert np.array_equal(d[p2 + 7 * 32: p2 + 8 * 32], c[7 * cols + 64: 7 * cols + 96])
+    # a planted mistake fails it: swapping two rows of a panel
+    bad = d.copy()
+    bad[p2: p2 + 32], bad[p2 + 32: p2 + 64] = d[p2 + 32: p2 + 64], d[p2: p2 + 32]
+    assert not np.array_equal(oracle.int8pc_from_device(bad, rows, cols), c)
+
+
 # ------------------------------------------------------------------ NVFP4
 def test_nvfp4_hand_worked_block():
     # Row 0 holds 10.5, so s_t = 10.5 / 2688 = 2^-8 exactly.  Row 1's first block has
