@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-weights", choices=["none", "down", "all"], default="none",
+                    help="expert stacks in page-locked host memory, read in place (NVLink-C2C on GB300): "
+                         "the down stack, or both")
     ap.add_argument("--act-quant", choices=["none", "q8_0"], default="none",
                     help="q8_0: the activation-quantised expert path (Q8_0 weights only)")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false",
@@ -93,6 +96,25 @@ def max_over_ranks(value: float, world: int, device="cuda") -> float:
 def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
     """Units per second of the whole job: every rank's units over the slowest rank's time."""
     return world * units_per_rank / (ms / 1e3)
+
+
+def host_link_peak():
+    """GB/s of a 2 GiB page-locked host -> device copy (best of 3, CUDA events): the host link's
+    read rate (NVLink-C2C on GB300), the bound of weights read in place from host memory."""
+    import torch
+    n = 2 << 30
+    src = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best = max(best, n / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del src, dst
+    return round(best, 1), "measured in this run: page-locked host -> device copy of 2 GiB (best of 3)"
 
 
 def peaks():
@@ -272,12 +294,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def build_stack(w, T, layers, local_rank):
+def build_stack(w, T, layers, local_rank, host_weights="none"):
     import torch
 
     from quantized_routed_expert_softmax_gb300 import layers as L
     from quantized_routed_expert_softmax_gb300 import synth
-    stack = [L.build_layer(w, layer=l) for l in range(layers)]
+    stack = [L.build_layer(w, layer=l, host_weights=host_weights) for l in range(layers)]
     for l, layer in enumerate(stack):   # each layer warms L2 with the next one's router weights
         layer.set_l2_prefetch(stack[(l + 1) % layers].router_w)
     inputs = [synth.tokens_cuda(w, T, layer=0, tag=f"bench{r}") for r in range(N_ROTATE)]
@@ -381,7 +403,7 @@ def run_ours(args, rank, world, local_rank, prebuilt=None):
         inputs = [synth.tokens_cuda(w, T, layer=0, tag=f"bench{r}") for r in range(N_ROTATE)]
         torch.cuda.synchronize()
     else:
-        stack, inputs = build_stack(w, T, layers, local_rank)
+        stack, inputs = build_stack(w, T, layers, local_rank, host_weights=getattr(args, "host_weights", "none"))
     aq = getattr(args, "act_quant", "none")
     for layer in stack:   # the activation-quantised path is a flag of the same weights
         layer.desc.act_quant = native.ACT_QUANT[aq]
@@ -503,6 +525,18 @@ def run_ours(args, rank, world, local_rank, prebuilt=None):
     # later boundaries coincide with the second), with all the layer's bytes as its work.
     one_kernel = stack[0].launches(T, supplied) == 1
     peak, peak_src = hbm_peak()
+    host_w = getattr(args, "host_weights", "none")
+    host_w = None if host_w in (False, None, "none") else host_w
+    if host_w == "all":   # every weight byte crosses the host link: its measured copy rate is the bound
+        peak, peak_src = host_link_peak()
+    elif host_w == "down":   # gate.up (and the router) from HBM, then the down bytes over the link
+        link, link_src = host_link_peak()
+        per_layer = tr_bytes["layer_per_launch"]
+        dn_b = tr_bytes["step"] / layers - tr_bytes["gate_up_per_layer"]
+        t_bound = (per_layer - dn_b) / (peak * 1e9) + dn_b / (link * 1e9)
+        peak_src = (f"derived: the layer's HBM bytes at {peak} GB/s, then its down bytes at the host link's "
+                    f"{link} GB/s ({link_src}); peak = all bytes / that time")
+        peak = round(per_layer / t_bound / 1e9, 1)
     if stack_obj is not None:   # the one-kernel stack: a launch processes every layer
         gu_ms = list(rt_ms)
         gu_us = statistics.mean(gu_ms) * 1e3
@@ -563,6 +597,11 @@ def run_ours(args, rank, world, local_rank, prebuilt=None):
     if rank == 0:
         step_bytes = tr_bytes["step"]
         cfg = workload_config(w, T, layers, aq)
+        if host_w:
+            cfg["workload"] += (", down experts" if host_w == "down" else ", all expert weights") + \
+                " in page-locked host memory read in place"
+            cfg["weights_location"] = ("down stack" if host_w == "down" else "both stacks") + \
+                " in host memory (page-locked; read in place over the host link)"
         cfg.update({
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": f"per-step weight working set {step_bytes / 1e9:.2f} GB > 129 MB L2; {N_ROTATE} token inputs "
@@ -596,7 +635,7 @@ def run_ours(args, rank, world, local_rank, prebuilt=None):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; random-init weights of the workload's shapes)",
             "config": cfg,
-            "roofline": {"bound": "hbm",
+            "roofline": {"bound": "host-link" if host_w else "hbm",
                          "kernel": ("decode_layer_kernel (the whole stack in one launch: every layer's routed "
                                     "experts' gate.up + down bytes and router weights)" if stack_obj is not None else
                                     ("decode_layer_kernel (the whole layer: routed experts' gate.up + down "
@@ -728,11 +767,14 @@ def run_reference(args, rank, world):
 # Further configurations measured by the default run, each with its own workload, roofline and
 # oracle baseline: prefill on the headline stack's own weights (Gemma shape, T = 512) and its
 # activation-quantised decode, per-channel int8 experts on the Gemma shape (T = 1 and 64), the
-# Nemotron-shaped NVFP4 ReLU^2 stack at one token, and MiniMax-shaped prefill (T = 4096), plain
-# and activation-quantised.
-SECONDARY = [("gemma", 512, 30, 20, "none"), ("gemma", 1, 30, 400, "q8_0"), ("gemma_int8pc", 1, 8, 400, "none"),
-             ("gemma_int8pc", 64, 8, 100, "none"), ("nemotron", 1, 40, 400, "none"),
-             ("minimax", 4096, 8, 10, "none"), ("minimax", 4096, 8, 10, "q8_0")]
+# Nemotron-shaped NVFP4 ReLU^2 stack at one token (and, 8 layers deep, with its experts in
+# page-locked host memory read in place), and MiniMax-shaped prefill (T = 4096), plain and
+# activation-quantised.
+SECONDARY = [("gemma", 512, 30, 20, "none", "none"), ("gemma", 1, 30, 400, "q8_0", "none"),
+             ("gemma_int8pc", 1, 8, 400, "none", "none"), ("gemma_int8pc", 64, 8, 100, "none", "none"),
+             ("nemotron", 1, 40, 400, "none", "none"), ("nemotron", 1, 8, 200, "none", "down"),
+             ("nemotron", 1, 8, 200, "none", "all"),
+             ("minimax", 4096, 8, 10, "none", "none"), ("minimax", 4096, 8, 10, "q8_0", "none")]
 
 
 def cpu_baseline(w, T, layers, budget_s, single_core_s=8.0, single=True, act_q8=False):
@@ -769,11 +811,12 @@ def main():
         import torch
         secondary = []
         w_prev = w
-        for name, t2, n2, steps2, aq2 in SECONDARY:
+        for name, t2, n2, steps2, aq2, hw2 in SECONDARY:
             a2 = argparse.Namespace(**vars(args))
-            a2.workload, a2.tokens, a2.layers, a2.act_quant = name, t2, n2, aq2
+            a2.workload, a2.tokens, a2.layers, a2.act_quant, a2.host_weights = name, t2, n2, aq2, hw2
             a2.steps, a2.warmup = steps2, max(3, min(args.warmup, 5))
-            reuse = stack if stack is not None and name == w_prev.name and n2 == len(stack) else None
+            reuse = (stack if stack is not None and name == w_prev.name and n2 == len(stack) and
+                     hw2 == getattr(stack[0], "host_resident", "none") else None)
             if reuse is None:
                 stack = None
                 torch.cuda.empty_cache()

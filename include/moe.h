@@ -216,8 +216,24 @@ typedef struct {
                                      never read by the layer's arithmetic; 16-byte aligned */
     int64_t l2_prefetch_bytes;    /* bytes at l2_prefetch (rounded down to a multiple of 16) */
     int32_t act_quant;            /* moe_act_quant (MOE_ACTQ_Q8_0 needs Q8_0 weights) */
-    int32_t reserved;             /* zero */
+    int32_t flags;                /* MOE_FLAG_* bits, 0 for the default */
 } moe_layer_desc;
+
+/* Expert weight stacks in page-locked host memory, read by the GPU in place (on GB300 from the
+ * Grace memory over NVLink-C2C): the GB300 form of the Nemotron page's experts kept in host RAM
+ * ("Running NVIDIA's new 120B Nemotron-3.5-Super on an 8GB GPU", "How the engine works", step 4:
+ * the up projection brought to the GPU, the down projection read over the bus in place, only its
+ * active 16-neuron groups).  MOE_FLAG_HOST_DOWN: w_down lives in host memory (gate.up stays in
+ * device memory, as the page stages it); MOE_FLAG_HOST_GATE_UP: w_gate_up too.
+ * moe_layer_forward checks that each such pointer is a host allocation the device addresses at the
+ * same pointer (else MOE_ERR_INVALID_ARG), runs the weight-streaming kernels (the tensor-core path,
+ * which loads by TMA, returns MOE_ERR_UNSUPPORTED when forced) and issues no L2 bulk prefetch of
+ * host weights.  Routing weights and tensor scales stay device memory.  Results are bitwise those
+ * of the same weights in device memory on the same kernels (with many tokens per expert AUTO
+ * would take the tensor-core path for device weights). */
+#define MOE_FLAG_HOST_GATE_UP 1
+#define MOE_FLAG_HOST_DOWN 2
+#define MOE_FLAG_HOST_WEIGHTS (MOE_FLAG_HOST_GATE_UP | MOE_FLAG_HOST_DOWN)
 
 /* Optional copies of intermediate results (device pointers, each may be NULL), and
  * optional stage-boundary events for timing: each non-NULL stage_events[i] must be a

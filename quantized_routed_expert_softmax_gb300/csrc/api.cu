@@ -200,6 +200,7 @@ bool decode_split_fits(const moe_layer_desc* d, const DecodeSplit& sp, int xt) {
 // The GEMM path tiles rows by 128 (SwiGLU gate.up: 64 neurons' gate and up rows) and K by 64.
 bool gemm_shape_ok(const moe_layer_desc* d) {
     if (d->wfmt == MOE_W_INT8PC) return false;   // per-channel int8 runs on the GEMV kernels
+    if (d->flags & MOE_FLAG_HOST_WEIGHTS) return false;   // TMA loads device memory only
     if (d->f % 64 != 0 || d->d % 64 != 0) return false;
     if (d->act == MOE_ACT_RELU2 && d->f % 128 != 0) return false;
     return true;
@@ -233,7 +234,8 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     const int64_t rows_per_tile = (d->wfmt == MOE_W_NVFP4) ? 256 : 32;
     p.fuse_combine = T * rows_per_tile <= 256;
     const int64_t dn_bytes = matrix_bytes(d->wfmt, d->d, d->f);
-    p.prefetch_down = static_cast<int64_t>(p.slot_cap) * dn_bytes <= kPrefetchBudget;
+    p.prefetch_down = static_cast<int64_t>(p.slot_cap) * dn_bytes <= kPrefetchBudget &&
+                      !(d->flags & MOE_FLAG_HOST_DOWN);   // no bulk L2 prefetch of host memory
     // many tokens per expert (at least 8 on average): tensor-core GEMMs
     p.gemm = gemm_shape_ok(d) && (d->path == MOE_PATH_GEMM || (d->path == MOE_PATH_AUTO && p.P >= 8 * d->E));
     if (p.gemm) p.fuse_combine = false;
@@ -365,7 +367,25 @@ moe_status validate_desc(const moe_layer_desc* d) {
     if (d->l2_prefetch && (d->l2_prefetch_bytes < 0 || !aligned16(d->l2_prefetch))) return MOE_ERR_ALIGNMENT;
     if (d->act_quant != MOE_ACTQ_NONE && d->act_quant != MOE_ACTQ_Q8_0) return MOE_ERR_INVALID_ARG;
     if (d->act_quant == MOE_ACTQ_Q8_0 && d->wfmt != MOE_W_Q8_0) return MOE_ERR_UNSUPPORTED;
+    if (d->flags & ~MOE_FLAG_HOST_WEIGHTS) return MOE_ERR_INVALID_ARG;   // unknown bits
+    if ((d->flags & MOE_FLAG_HOST_WEIGHTS) && d->path == MOE_PATH_GEMM) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
+}
+
+// Every expert stack a MOE_FLAG_HOST_* bit names is a host allocation (page-locked, mapped) that
+// the device reads at the same pointer.
+bool host_weights_ok(const moe_layer_desc* d) {
+    for (int bit : {MOE_FLAG_HOST_GATE_UP, MOE_FLAG_HOST_DOWN}) {
+        if (!(d->flags & bit)) continue;
+        const void* p = bit == MOE_FLAG_HOST_GATE_UP ? d->w_gate_up : d->w_down;
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        if (at.type != cudaMemoryTypeHost || at.devicePointer != p) return false;
+    }
+    return true;
 }
 
 // The one-kernel decode arguments for n layers of descs[0]'s shape (pointers per layer), on
@@ -576,6 +596,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     const Layout L = layout_for(desc, T);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     if (desc->path == MOE_PATH_GEMM && !gemm_shape_ok(desc)) return MOE_ERR_UNSUPPORTED;
+    if (!host_weights_ok(desc)) return MOE_ERR_INVALID_ARG;
 
     int num_sms = 0;
     cudaError_t e = ensure_configured(&num_sms);
@@ -763,6 +784,8 @@ moe_status moe_stack_forward(const moe_layer_desc* descs, int32_t n_layers, cons
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_ALIGNMENT;
     const Layout L = layout_for(descs, 1);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    for (int32_t l = 0; l < n_layers; ++l)
+        if (!host_weights_ok(descs + l)) return MOE_ERR_INVALID_ARG;
     int num_sms = 0;
     if (ensure_configured(&num_sms) != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -11,14 +11,16 @@ from . import native, synth
 
 
 def build_layer(w: synth.Workload, layer: int = 0, source: str = "cuda", keep_fp32: bool = False,
-                path: str = "auto", E_chunk: int = 16, act_quant: str = "none"):
+                path: str = "auto", E_chunk: int = 16, act_quant: str = "none", host_weights: str = "none"):
     """A native.MoELayer for `w`, layer `layer`.
 
     source = "cuda": fp32 weights drawn on the device, E_chunk experts at a time;
     source = "numpy": drawn on the host with the numpy generator (small shapes), the
     same numbers the oracle tests draw.  keep_fp32 keeps the fp32 stacks on the layer
     (attributes gate_up_f32 / down_f32) for tests that hand them to the oracle.  act_quant
-    "q8_0" selects the activation-quantised expert path (Q8_0 weights only).
+    "q8_0" selects the activation-quantised expert path (Q8_0 weights only).  host_weights "down"
+    moves the packed down stack, "all" both stacks, to page-locked host memory that the kernels
+    read in place.
     """
     dev = torch.device("cuda")
     router_w = torch.from_numpy(synth.router_weight(w, layer)).to(dev)
@@ -59,8 +61,16 @@ def build_layer(w: synth.Workload, layer: int = 0, source: str = "cuda", keep_fp
             keep_dn.append(b)
         else:
             del a, b
+    def to_host(t):   # packed on the device, then moved to page-locked host memory
+        h = torch.empty(t.shape, dtype=torch.uint8, pin_memory=True)
+        h.copy_(t)
+        return h
+    if host_weights in ("down", "all"):
+        dn = to_host(dn)
+    if host_weights == "all":
+        gu = to_host(gu)
     layer_obj = native.MoELayer(w.d, w.f, w.E, w.k, w.act, w.wfmt, router_w, gu, dn, gts, dts, path=path,
-                                act_quant=act_quant)
+                                act_quant=act_quant, host_weights=host_weights)
     if keep_fp32:
         layer_obj.gate_up_f32 = torch.cat(keep_gu)
         layer_obj.down_f32 = torch.cat(keep_dn)

@@ -22,6 +22,7 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 LAYOUT = {"canonical": 0, "device": 1, "neuron": 2}
 PATH = {"auto": 0, "gemv": 1, "gemm": 2}
 ACT_QUANT = {"none": 0, "q8_0": 1}
+FLAG_HOST_GATE_UP, FLAG_HOST_DOWN = 1, 2
 
 # Every symbol include/moe.h declares.
 EXPORTS = ["moe_q8_0_bytes", "moe_nvfp4_bytes", "moe_int8pc_bytes", "moe_quantize_q8_0", "moe_pack_nvfp4",
@@ -46,7 +47,7 @@ class LayerDesc(ctypes.Structure):
         ("router_w", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
         ("gate_up_tscale", ctypes.c_void_p), ("down_tscale", ctypes.c_void_p),
         ("l2_prefetch", ctypes.c_void_p), ("l2_prefetch_bytes", ctypes.c_int64),
-        ("act_quant", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("act_quant", ctypes.c_int32), ("flags", ctypes.c_int32),
     ]
 
 
@@ -224,13 +225,16 @@ class MoELayer:
     """
 
     def __init__(self, d, f, E, k, act, wfmt, router_w, gate_up, down, gate_up_tscale=None, down_tscale=None,
-                 path: str = "auto", act_quant: str = "none"):
+                 path: str = "auto", act_quant: str = "none", host_weights: str = "none"):
         self.d, self.f, self.E, self.k, self.act, self.wfmt = d, f, E, k, act, wfmt
         self.router_w, self.gate_up, self.down = router_w, gate_up, down
         self.gate_up_tscale, self.down_tscale = gate_up_tscale, down_tscale
         self.desc = LayerDesc(d, f, E, k, ACT[act], WFMT[wfmt], PATH[path], _ptr(router_w), _ptr(gate_up), _ptr(down),
                               _ptr(gate_up_tscale), _ptr(down_tscale))
         self.desc.act_quant = ACT_QUANT[act_quant]
+        # host_weights: "none", "down" (the down stack in page-locked host memory) or "all"
+        self.desc.flags = {"none": 0, "down": FLAG_HOST_DOWN, "all": FLAG_HOST_GATE_UP | FLAG_HOST_DOWN}[host_weights]
+        self.host_resident = host_weights
         self._ws = None
         self._ws_tokens = 0
 

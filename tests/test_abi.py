@@ -111,6 +111,9 @@ def test_layer_validation(L):
         (_desc(wfmt=1), 1),                       # NVFP4 needs tensor scales
         (_desc(w_down=FAKE + 8), 3),
         (_desc(act_quant=2), 1),                  # unknown activation quantiser
+        (_desc(flags=4), 1),                      # unknown flag
+        (_desc(flags=1, path=2), 5),              # host-resident weights cannot take the TMA path
+        (_desc(flags=1), 1),                      # not host allocations the device can address
         (_desc(act_quant=1, wfmt=1, gate_up_tscale=FAKE, down_tscale=FAKE), 5),   # Q8_0 activations need Q8_0 weights
     ]
     for desc, want in cases:
