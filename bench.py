@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--workload", default="gemma")
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = the workload's)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count (0 = the workload's): small cases of a shape for profiling")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-weights", choices=["none", "down", "all"], default="none",
                     help="expert stacks in page-locked host memory, read in place (NVLink-C2C on GB300): "
@@ -396,6 +398,9 @@ def run_ours(args, rank, world, local_rank, prebuilt=None):
     B.build()
     torch.cuda.set_device(local_rank)
     w = synth.WORKLOADS[args.workload]
+    if getattr(args, "experts", 0):
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}_e{args.experts}", E=args.experts)
     T = args.tokens
     layers = args.layers or default_layers(w)
     if prebuilt is not None and len(prebuilt) == layers:
@@ -807,7 +812,7 @@ def main():
     result, (w, T, layers), stack = run_ours(args, rank, world, local_rank)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, T, layers, 15.0, act_q8=args.act_quant == "q8_0")
-    if args.secondary and args.workload == "gemma" and args.tokens == 1 and not args.layers:
+    if args.secondary and args.workload == "gemma" and args.tokens == 1 and not args.layers and not args.experts:
         import torch
         secondary = []
         w_prev = w

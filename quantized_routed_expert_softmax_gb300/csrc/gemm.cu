@@ -927,8 +927,11 @@ cudaError_t launch_expert_gemm(const ExpertArgs& a, int kind, int wfmt, int act,
     const bool large = a.P >= static_cast<int64_t>(kLargeAverage) * slot_cap;
     g.nt_max = std::min(large ? kLargeTile : kSmallTile, kBRows / g.planes);
     g.acc_stride = (g.nt_max + 31) & ~31;
-    g.a_stages = large ? 2 : 4;
     g.acc_bufs = large ? 1 : 2;
+    // as many A stages (2 or 4) as tensor memory holds beside the accumulators: with 4, each
+    // issuer's next K step can be dequantised while its current one is multiplied
+    g.a_stages = (4 * static_cast<int>(kAColsPerStage) + g.acc_bufs * 2 * g.acc_stride <= static_cast<int>(kTmemCols))
+                     ? 4 : 2;
     g.nbh = 0;
     for (int i = 0; i < kNumBoxHeights && kBoxHeights[i] < g.nt_max; ++i) g.bh[g.nbh++] = kBoxHeights[i];
     static_assert(kNumBoxHeights + 1 <= 4, "box height table");
