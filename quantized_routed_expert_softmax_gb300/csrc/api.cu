@@ -23,6 +23,7 @@ cudaError_t launch_route_decode(const void*, int, const float*, int64_t, int64_t
 cudaError_t configure_gemv_kernels();
 cudaError_t launch_gate_up_gemv(const ExpertArgs&, int, int, int, cudaStream_t);
 cudaError_t launch_down_gemv(const ExpertArgs&, int, int, cudaStream_t);
+size_t down_nv_mma_smem(int, int);
 cudaError_t launch_down_q8_t1(const ExpertArgs&, cudaStream_t);
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int64_t, int, int64_t, float*, cudaStream_t);
 cudaError_t launch_rmsnorm_bf16(const float*, int64_t, int64_t, float, uint16_t*, cudaStream_t);
@@ -48,6 +49,7 @@ constexpr int kSmallPairs = 1024;    // ... and up to 1024 pairs
 constexpr int64_t kFusedRouteLogits = 4096;   // ... and up to 4096 logits (the routing CTA keeps them on chip)
 constexpr size_t kSmemBudget = 96 * 1024;        // token rows staged per expert CTA (plus the 55 KB ring)
 constexpr int64_t kPrefetchBudget = 64ll << 20;   // down weights prefetched into L2 (of 126 MB)
+constexpr size_t kNvMmaSmem = 112 * 1024;         // NVFP4 tensor-core down: stage ring + h planes + group lists (2 CTAs per SM)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -99,6 +101,7 @@ struct Plan {
     bool gemm;          // expert GEMMs on the tensor cores instead of the GEMVs
     bool down_t1;       // one token, Q8_0 SwiGLU, k in {1,2,4,8}: the row-tile down kernel combines
     int nv_split;       // NVFP4 down with fused combine: group splits per (row tile, slot)
+    bool nv_mma;        // NVFP4 down on the tensor cores (tt_dn tokens per pass)
     bool decode1;       // one token, Q8_0 SwiGLU: the shape fits the one-kernel decode layer
 };
 
@@ -243,6 +246,15 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
                 (d->k == 1 || d->k == 2 || d->k == 4 || d->k == 8) && d->f / 32 >= 8 / d->k && d->d % 16 == 0;
     if (p.down_t1) p.fuse_combine = true;   // the down kernel writes the output rows
     p.nv_split = (!p.gemm && d->wfmt == MOE_W_NVFP4 && p.fuse_combine && T == 1 && (d->f / 16) >= 4 * 8) ? 4 : 1;
+    // NVFP4 down at two or more tokens: tensor cores, tokens in passes of 8, 16 or 32 (as many
+    // as T asks for and the f16 h planes leave room for in shared memory)
+    p.nv_mma = !p.gemm && d->wfmt == MOE_W_NVFP4 && !p.fuse_combine && T >= 2 &&
+               down_nv_mma_smem(8, static_cast<int>(d->f)) <= kNvMmaSmem;
+    if (p.nv_mma) {
+        int tt = 8;
+        while (tt < 32 && tt < T && down_nv_mma_smem(2 * tt, static_cast<int>(d->f)) <= kNvMmaSmem) tt *= 2;
+        p.tt_dn = tt;
+    }
     p.decode1 = !p.gemm && d->act_quant == MOE_ACTQ_NONE && decode_shape_ok(d, T, xt);
     return p;
 }
@@ -692,6 +704,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.fuse_combine = p.fuse_combine ? 1 : 0;
     a.prefetch_down = p.prefetch_down ? 1 : 0;
     a.nv_split = p.nv_split;
+    a.nv_mma = p.nv_mma ? 1 : 0;
     a.out = out;
     a.w_gu = static_cast<const uint8_t*>(desc->w_gate_up);
     a.w_dn = static_cast<const uint8_t*>(desc->w_down);

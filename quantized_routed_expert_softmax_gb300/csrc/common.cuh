@@ -70,6 +70,7 @@ struct ExpertArgs {
     int fuse_combine;            // the down kernel's last CTA per row tile also combines
     int prefetch_down;           // gate.up CTAs prefetch the routed experts' down weights into L2
     int nv_split;                // NVFP4 down, fused combine: CTAs per (row tile, slot), each a share of the groups
+    int nv_mma;                  // NVFP4 down on the tensor cores (two or more tokens; tt_dn = 8, 16 or 32)
     float* out;                  // [T][d] layer output (fused combine)
     const uint8_t* w_gu;
     int64_t gu_bytes;            // bytes of one expert's gate/up matrix

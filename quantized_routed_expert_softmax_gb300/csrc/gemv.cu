@@ -670,6 +670,186 @@ __global__ void __launch_bounds__(256, TT == 1 ? 3 : (TT == 2 ? 2 : 1)) down_nv_
     if (a.fuse_combine) combine_rows_if_last(a, rt, rt * 256, 256, spos, sw, nz);
 }
 
+// ------------------------------------------------------------------------------ down, NVFP4, tensor cores
+// Two or more tokens: the neuron-layout matrices on mma.sync.  An E2M1 code times its E4M3
+// block scale is exact in f16 (2 x 4 significant bits, magnitudes 2^-10 .. 2688), so each
+// 16-neuron group is one K step of an m16n8k16 MMA with the scale folded into the weight
+// fragment, the f32 accumulators run over all groups, and h rides as f16 hi + lo.
+//   A warp covers 64 rows.  Lane (g, q) takes, of neurons 4q .. 4q+3, the code word of rows
+// 8g .. 8g+7 (4 bytes each); MMA block mb (0..3) puts row 8g+2mb at M index g and row
+// 8g+2mb+1 at g+8 (the low and high nibble of byte mb); K indices 2q, 2q+1 are neurons 4q,
+// 4q+1 and 2q+8, 2q+9 are 4q+2, 4q+3, and the activations follow the same assignment.
+//   A CTA covers 256 rows: warp w takes rows 64 (w & 3) .. and half w >> 2 of the slot's
+// active groups; the two halves meet in shared memory in a fixed order.  Each warp streams
+// its groups through a ring of cp.async stages: the 16 neurons' 32 code bytes at 32-byte
+// slots n + n/4 (so that the four lanes of a quad read different banks), then 64 scale bytes.
+// Tokens go in passes of 8 * NT (the h planes in shared memory); a slot's unused N tiles
+// are skipped.  grid: (d/256, slots).
+constexpr int kNvStages = 8;
+constexpr int kNvStageBytes = 19 * 32 + 64;
+
+__host__ __device__ constexpr int nv_h_ld(int f) { return f + ((16 - f % 64) + 64) % 64; }   // = 16 mod 64
+
+size_t down_nv_mma_smem(int tt, int f) {
+    const size_t h = static_cast<size_t>(2) * tt * nv_h_ld(f) * sizeof(__half);
+    const size_t red = static_cast<size_t>(2) * tt * 257 * sizeof(float);
+    return static_cast<size_t>(8) * kNvStages * kNvStageBytes + std::max(h, red) +
+           static_cast<size_t>(f / 16) * sizeof(int);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(256, NT <= 2 ? 2 : 1) down_nv_mma_kernel(ExpertArgs a) {
+    constexpr int TT = 8 * NT;
+    const int slot = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int wq = warp & 3, half = warp >> 2;
+    extern __shared__ __align__(16) unsigned char nsm[];
+    unsigned char* ring = nsm + warp * kNvStages * kNvStageBytes;
+    unsigned char* uni = nsm + 8 * kNvStages * kNvStageBytes;           // h planes, then the partial sums
+    const int d = a.d, f = a.f, ng = f / 16, ld = nv_h_ld(f);
+    __half* hs = reinterpret_cast<__half*>(uni);                       // [TT][ld] hi, then [TT][ld] lo
+    float* red = reinterpret_cast<float*>(uni);                        // [2 halves][TT][257]
+    const size_t h_bytes = static_cast<size_t>(2) * TT * ld * sizeof(__half);
+    const size_t red_bytes = static_cast<size_t>(2) * TT * 257 * sizeof(float);
+    const size_t uni_bytes = h_bytes > red_bytes ? h_bytes : red_bytes;
+    int* glist = reinterpret_cast<int*>(uni + uni_bytes);               // active groups: half 0, then half 1
+    __shared__ int s_na[2];
+    pdl_wait();
+    pdl_trigger();
+    const int4 si = __ldcg(a.ws.slot_info + slot);
+    const int e = si.x, r0 = si.y, cnt = si.z;
+    if (cnt == 0) return;
+    const int rt = blockIdx.x;
+    const int R = rt * 256 + wq * 64;                                   // this warp's first row
+    const uint8_t* W = a.w_dn + static_cast<int64_t>(e) * a.dn_bytes;
+    const int64_t rec = 16 * static_cast<int64_t>(d / 2) + d;          // bytes of one group
+    const float ts = a.dn_ts[e];
+    const uint64_t pol = l2_evict_first_policy();
+    // the active groups of each half, compacted by warps 0 and 4 (ballot + prefix count)
+    if ((warp & 3) == 0) {
+        const int gb = half ? ng / 2 : 0, ge = half ? ng : ng / 2;
+        const uint32_t* gm = a.ws.gmask + static_cast<int64_t>(slot) * a.gwords;
+        int n = 0;
+        for (int c = gb; c < ge; c += 32) {
+            const int gi = c + lane;
+            const bool act = gi < ge && ((__ldcg(gm + (gi >> 5)) >> (gi & 31)) & 1u);
+            const uint32_t bal = __ballot_sync(0xffffffffu, act);
+            if (act) glist[gb + n + __popc(bal & ((1u << lane) - 1u))] = gi;
+            n += __popc(bal);
+        }
+        if (lane == 0) s_na[half] = n;
+    }
+    __syncthreads();
+    const int na = s_na[half];
+    const int* mylist = glist + (half ? ng / 2 : 0);
+    auto issue = [&](int st, int grp) {
+        const uint32_t dst = smem_addr(ring + st * kNvStageBytes);
+        const uint8_t* base = W + grp * rec;
+        const int n = lane >> 1, h = lane & 1;
+        cp_async16_ef(dst + (n + (n >> 2)) * 32 + h * 16, base + static_cast<int64_t>(n) * (d / 2) + R / 2 + h * 16,
+                      pol);
+        if (lane < 4) cp_async16(dst + 19 * 32 + lane * 16, base + 16 * static_cast<int64_t>(d / 2) + R + lane * 16);
+    };
+    for (int t0 = 0; t0 < cnt; t0 += TT) {
+        const int nt = min(TT, cnt - t0);
+#pragma unroll
+        for (int s = 0; s < kNvStages; ++s) {
+            if (s < na) issue(s, mylist[s]);
+            cp_async_commit();
+        }
+        {   // h of this pass's tokens as f16 hi + lo planes
+            const int f4 = f / 4;
+            const float4* src = reinterpret_cast<const float4*>(a.ws.h + static_cast<int64_t>(r0 + t0) * f);
+            for (int i = threadIdx.x; i < nt * f4; i += blockDim.x) {
+                const int t = i / f4, c = (i % f4) * 4;
+                const float4 v = __ldcg(src + i);
+                __half2 h0, l0, h1, l1;
+                split_f16(v.x, v.y, h0, l0);
+                split_f16(v.z, v.w, h1, l1);
+                __half2* hp = reinterpret_cast<__half2*>(hs + t * ld + c);
+                __half2* lp = reinterpret_cast<__half2*>(hs + TT * ld + t * ld + c);
+                hp[0] = h0;
+                hp[1] = h1;
+                lp[0] = l0;
+                lp[1] = l1;
+            }
+        }
+        __syncthreads();
+        float acc[4][NT][4];
+#pragma unroll
+        for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) acc[mb][n][0] = acc[mb][n][1] = acc[mb][n][2] = acc[mb][n][3] = 0.0f;
+        for (int i = 0; i < na; ++i) {
+            cp_async_wait<kNvStages - 1>();
+            __syncwarp();
+            const int st = i % kNvStages;
+            const int grp = mylist[i];
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(ring + st * kNvStageBytes);
+            const uint32_t c0 = sw[(4 * q + 0 + q) * 8 + g], c1 = sw[(4 * q + 1 + q) * 8 + g];
+            const uint32_t c2 = sw[(4 * q + 2 + q) * 8 + g], c3 = sw[(4 * q + 3 + q) * 8 + g];
+            const uint2 sc = *reinterpret_cast<const uint2*>(ring + st * kNvStageBytes + 19 * 32 + 8 * g);
+            constexpr uint32_t m = 0x0f0f0f0fu;
+            const uint32_t lo01 = (c0 & m) | ((c1 << 4) & ~m);   // byte b: row 8g+2b of neurons 4q | 4q+1
+            const uint32_t hi01 = ((c0 >> 4) & m) | (c1 & ~m);   // row 8g+2b+1
+            const uint32_t lo23 = (c2 & m) | ((c3 << 4) & ~m);
+            const uint32_t hi23 = ((c2 >> 4) & m) | (c3 & ~m);
+            // B fragments: token n*8+g, neurons 16 grp + 4q .. 4q+3 (hi and lo planes)
+            uint2 bh[NT], bl[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const __half* hp = hs + (n * 8 + g) * ld + 16 * grp + 4 * q;
+                bh[n] = *reinterpret_cast<const uint2*>(hp);
+                bl[n] = *reinterpret_cast<const uint2*>(hp + TT * ld);
+            }
+#pragma unroll
+            for (int mb = 0; mb < 4; ++mb) {
+                const uint32_t pair = ((mb < 2 ? sc.x : sc.y) >> (16 * (mb & 1))) & 0xffffu;   // rows 8g+2mb, +1
+                uint32_t s2;
+                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(static_cast<uint16_t>(pair)));
+                const __half2 sA = __low2half2(*reinterpret_cast<const __half2*>(&s2));
+                const __half2 sB = __high2half2(*reinterpret_cast<const __half2*>(&s2));
+                const int sh = 8 * mb;
+                const uint32_t a0 = e2m1x2_scaled((lo01 >> sh) & 0xffu, sA);
+                const uint32_t a1 = e2m1x2_scaled((hi01 >> sh) & 0xffu, sB);
+                const uint32_t a2 = e2m1x2_scaled((lo23 >> sh) & 0xffu, sA);
+                const uint32_t a3 = e2m1x2_scaled((hi23 >> sh) & 0xffu, sB);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    if (n * 8 < nt) {
+                        mma16816(acc[mb][n], a0, a1, a2, a3, bh[n].x, bh[n].y);
+                        mma16816(acc[mb][n], a0, a1, a2, a3, bl[n].x, bl[n].y);
+                    }
+                }
+            }
+            __syncwarp();
+            if (i + kNvStages < na) issue(st, mylist[i + kNvStages]);
+            cp_async_commit();
+        }
+        cp_async_wait<0>();
+        __syncthreads();   // every warp is done with the h planes: the partial sums take their place
+#pragma unroll
+        for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int row = wq * 64 + 8 * g + 2 * mb, tok = n * 8 + 2 * q;
+                float* rp = red + (half * TT + tok) * 257 + row;
+                rp[0] = acc[mb][n][0];
+                rp[257] = acc[mb][n][1];
+                rp[1] = acc[mb][n][2];
+                rp[258] = acc[mb][n][3];
+            }
+        __syncthreads();
+        for (int it = threadIdx.x; it < nt * 256; it += blockDim.x) {
+            const int t = it >> 8, r = it & 255;
+            const float v = red[t * 257 + r] + red[(TT + t) * 257 + r];
+            a.ws.y[static_cast<int64_t>(r0 + t0 + t) * d + rt * 256 + r] = v * ts;
+        }
+        __syncthreads();
+    }
+}
+
 // ------------------------------------------------------------------------------ combine
 // out[t] = sum_{j<k} w[t][j] * y[pos(t,j)], in slot order.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pos,
@@ -766,6 +946,13 @@ static cudaError_t dn_nv_launch(const ExpertArgs& a, int slot_cap, size_t smem, 
     return launch_pdl(down_nv_gemv_kernel<TT>, dim3(a.d / 256, slot_cap, a.nv_split), dim3(256), smem, s, a);
 }
 
+template <int NT>
+static cudaError_t nv_mma_launch(const ExpertArgs& a, int slot_cap, cudaStream_t s, bool configure) {
+    if (configure) return allow_smem(down_nv_mma_kernel<NT>, 200 * 1024);
+    return launch_pdl(down_nv_mma_kernel<NT>, dim3(a.d / 256, slot_cap), dim3(256), down_nv_mma_smem(8 * NT, a.f), s,
+                      a);
+}
+
 static cudaError_t dn_dispatch(const ExpertArgs& a, int wfmt, int slot_cap, size_t smem, cudaStream_t s,
                                bool configure) {
     if (wfmt == MOE_W_Q8_0) {
@@ -776,6 +963,15 @@ static cudaError_t dn_dispatch(const ExpertArgs& a, int wfmt, int slot_cap, size
         if (configure) return allow_smem(down_q8_gemv_kernel<MOE_W_INT8PC>, 200 * 1024);
         return launch_pdl(down_q8_gemv_kernel<MOE_W_INT8PC>, dim3(a.d / 32, slot_cap), dim3(kDnWarps * 32), smem, s,
                           a);
+    }
+    if (a.nv_mma || configure) {
+        cudaError_t e = cudaSuccess;
+        switch (a.tt_dn) {
+            case 32: e = nv_mma_launch<4>(a, slot_cap, s, configure); break;
+            case 16: e = nv_mma_launch<2>(a, slot_cap, s, configure); break;
+            default: e = nv_mma_launch<1>(a, slot_cap, s, configure); break;
+        }
+        if (!configure || e != cudaSuccess) return e;
     }
     switch (a.tt_dn) {
         case 1: return dn_nv_launch<1>(a, slot_cap, smem, s, configure);
@@ -797,7 +993,7 @@ cudaError_t configure_gemv_kernels() {
         }
     cudaError_t e0 = allow_smem(down_q8_t1_kernel, 200 * 1024);
     if (e0 != cudaSuccess) return e0;
-    const int tts[3] = {1, 2, 4};
+    const int tts[6] = {1, 2, 4, 8, 16, 32};
     for (int tt : tts) {
         a.tt_dn = tt;
         for (int w : wf) {

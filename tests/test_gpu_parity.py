@@ -165,6 +165,20 @@ def test_layer_small_parity(name, T):
     assert_close(out, ref["out"])
 
 
+# NVFP4 down on the tensor cores at two or more tokens, the GEMV path forced: passes of 8, 16
+# and 32 tokens with ragged last passes (T = 300 puts about 75 rows on each of the 8 experts),
+# ReLU^2 with 92.5% zeros (inactive groups skipped, uneven halves) and SwiGLU with 20 groups.
+@pytest.mark.parametrize("name", ["small_nvfp4_relu2", "small_nvfp4_swiglu"])
+@pytest.mark.parametrize("T", [2, 9, 40, 300])
+def test_nvfp4_down_tensor_core_parity(name, T):
+    w = SMALL[name]
+    L, out, tr, ref = _run_small(w, T, path="gemv")
+    assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
+    assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
+    assert_close(tr["h"].cpu().numpy(), ref["h"][ref["perm"]], what="h")
+    assert_close(out, ref["out"])
+
+
 # The tensor-core GEMM path forced on the same layers: token tiles of 128 with ragged tails
 # (T=700 puts about 175 rows on each expert of the 8-expert layers), fp32 inputs split hi/lo.
 @pytest.mark.parametrize("name", list(SMALL))
@@ -511,7 +525,8 @@ def test_minimax_layer_prefill_4096_sampled():
 
 # The skewed-routing sweep's sizes up to its largest, T = 8192 (65,536 pairs; the hottest
 # expert gets a pair from most tokens, over a hundred 64-row tiles)
-@pytest.mark.parametrize("name,T", [("zipf", 64), ("zipf", 2048), ("zipf_nvfp4", 2048), ("zipf", 8192)])
+@pytest.mark.parametrize("name,T", [("zipf", 64), ("zipf_nvfp4", 64), ("zipf", 2048), ("zipf_nvfp4", 2048),
+                                    ("zipf", 8192)])
 def test_zipf_routing_full_size(name, T):
     w = synth.WORKLOADS[name]
     idx, wts = synth.zipf_routing(T, w.E, w.k)
