@@ -36,7 +36,7 @@ int decode_ctas(int);
 size_t decode_smem_plan(int, int, int, int, int, int, int, int*, int*);
 size_t decode_ring_bytes();
 size_t decode_max_smem();
-cudaError_t launch_decode_layer(const DecodeArgs&, int, size_t, int, cudaStream_t);
+cudaError_t launch_decode_layer(const DecodeArgs&, int, int, size_t, int, cudaStream_t);
 
 
 namespace {
@@ -139,14 +139,15 @@ int64_t cta_max_items(int64_t U, int64_t W, int64_t npan) {
 }
 
 // Q8_0 SwiGLU: gate.up units (slot, 16-neuron tile, 32-column panel), down units (slot,
-// 32-row tile, 32-neuron panel).  NVFP4 ReLU^2: gate.up units (slot, 32-neuron tile,
-// 64-column panel), down units (slot, 256-row tile, 16-neuron group).
+// 32-row tile, 32-neuron panel).  NVFP4: gate.up units (slot, 32-neuron tile (ReLU^2) or
+// 16-neuron tile of gate and up rows (SwiGLU), 64-column panel), down units (slot, 256-row
+// tile, 16-neuron group).
 DecodeSplit decode_split(const moe_layer_desc* d, int64_t ctas) {
     DecodeSplit sp{};
     const bool q8 = d->wfmt == MOE_W_Q8_0;
     sp.npan_g = q8 ? d->d / 32 : d->d / 64;
     sp.npan_d = q8 ? d->f / 32 : d->f / 16;
-    const int64_t items_g = static_cast<int64_t>(d->k) * (q8 ? d->f / 16 : d->f / 32);
+    const int64_t items_g = static_cast<int64_t>(d->k) * (d->act == MOE_ACT_SWIGLU ? d->f / 16 : d->f / 32);
     sp.items_d = static_cast<int64_t>(d->k) * (q8 ? d->d / 32 : d->d / 256);
     sp.rec_d = q8 ? 32 : 256;
     sp.U_g = items_g * sp.npan_g;
@@ -165,12 +166,12 @@ DecodeSplit decode_split(const moe_layer_desc* d, int64_t ctas) {
 }
 
 // The one-kernel decode layer's shape limits (any device): one token, Q8_0 SwiGLU or NVFP4
-// ReLU^2, the router-weight slice of a routing CTA and x within its shared memory, and 32-bit
+// (ReLU^2 or SwiGLU), the router-weight slice of a routing CTA and x within its shared memory, and 32-bit
 // unit arithmetic.
 bool decode_shape_ok(const moe_layer_desc* d, int64_t T, int xt) {
     if (T != 1 || d->path != MOE_PATH_AUTO) return false;
     const bool q8 = d->wfmt == MOE_W_Q8_0 && d->act == MOE_ACT_SWIGLU;
-    const bool nv = d->wfmt == MOE_W_NVFP4 && d->act == MOE_ACT_RELU2;
+    const bool nv = d->wfmt == MOE_W_NVFP4;   // ReLU^2 (latent experts) or SwiGLU
     if (!q8 && !nv) return false;
     if (d->d > 8192 || d->f % 32 != 0) return false;
     if (q8 && d->k * d->f > 16384) return false;   // h of every slot in shared memory
@@ -422,9 +423,10 @@ bool fill_decode_args(const moe_layer_desc* descs, int n, const void* x, int xt,
     a->E = static_cast<int>(desc->E);
     a->k = desc->k;
     a->epc = epc;
-    // the routed experts' whole down matrices into L2 (Q8_0: every byte is read; NVFP4 reads
-    // only the active groups, so a whole-matrix prefetch would fetch bytes that are skipped)
-    a->prefetch_down = (p.prefetch_down && desc->wfmt == MOE_W_Q8_0) ? 1 : 0;
+    // the routed experts' whole down matrices into L2 (Q8_0 and SwiGLU: every byte is read;
+    // NVFP4 ReLU^2 reads only the active groups, so a whole-matrix prefetch would fetch bytes
+    // that are skipped)
+    a->prefetch_down = (p.prefetch_down && (desc->wfmt == MOE_W_Q8_0 || desc->act == MOE_ACT_SWIGLU)) ? 1 : 0;
     // warps that share each phase's panel range: all of them, or one per unit
     a->warps_g = static_cast<int>(sp.warps_g);
     a->warps_d = static_cast<int>(sp.warps_d);
@@ -654,7 +656,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
             a.out = out;
             a.idx_in = idx_in;
             a.w_in = w_in;
-            e = launch_decode_layer(a, desc->wfmt, smem, ctas, s);
+            e = launch_decode_layer(a, desc->wfmt, desc->act, smem, ctas, s);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
             for (int i = 1; i <= 4; ++i) mark(i);   // one kernel: the inner boundaries coincide
             if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -814,7 +816,7 @@ moe_status moe_stack_forward(const moe_layer_desc* descs, int32_t n_layers, cons
             a.x_next = x_next;
             a.idx_out = idx;
             a.w_out = w;
-            return cuda_status(launch_decode_layer(a, descs->wfmt, smem, ctas, s));
+            return cuda_status(launch_decode_layer(a, descs->wfmt, descs->act, smem, ctas, s));
         }
     }
     // otherwise layer by layer, the RMS-norm glue between them

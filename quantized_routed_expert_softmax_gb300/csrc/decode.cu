@@ -689,10 +689,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                 __syncthreads();
             }
         } else {
-            // ------------------------------------------------------------ H (NVFP4, ReLU^2)
-            // h = max(z * ts, 0)^2 for the slots this CTA's down units read (fp32, in region B),
-            // the records of each item summed in contributor order; then which 16-neuron groups
-            // hold a non-zero h (the only ones the down projection reads).
+            // ------------------------------------------------------------ H (NVFP4)
+            // h = max(z * ts, 0)^2 (ReLU^2, 32-neuron items) or SiLU(zg * ts) * (zu * ts) (SwiGLU,
+            // items of 16 gate + 16 up rows) for the slots this CTA's down units read (fp32, in
+            // region B), the records of each item summed in contributor order; then which
+            // 16-neuron groups hold a non-zero h (the only ones the down projection reads).
             float* hf = xf;                                   // [cta slots][f]
             int* gact = reinterpret_cast<int*>(slog);         // [cta slots][f/16] active flags
             float* dred = reinterpret_cast<float*>(ring);     // [cta items][16 warps][256] down partials
@@ -705,24 +706,33 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             const int d_item0 = static_cast<int>(dv0 / npan_d);
             const int d_items = dv1 > dv0 ? static_cast<int>((dv1 - 1) / npan_d) - d_item0 + 1 : 0;
             for (int i = tid; i < d_items * kDecWarps * 256; i += kDecThreads) dred[i] = 0.0f;
-            constexpr int kHB = 8;   // neurons per thread per batch: their first two records load together
+            constexpr int kHB = kSwiglu ? 4 : 8;   // neurons per thread per batch: their first two records load together
+            constexpr int kLg = kSwiglu ? 4 : 5;   // log2 of the neurons per gate.up item
+            // the record word of neuron qq within its item (SwiGLU: the gate row; the up row is 16 later)
+            auto rec_of = [&](int qq) {
+                return a.grec + static_cast<int64_t>(qq >> kLg) * a.cov_g * 32 + (qq & ((1 << kLg) - 1));
+            };
             const int hn = h_ns * f;
             for (int q0 = tid; q0 < hn; q0 += kHB * kDecThreads) {
-                float v0[kHB], v1[kHB];
+                float v0[kHB], v1[kHB], w0[kHB], w1[kHB];   // (gate or z) and up, first two records
                 int ncs[kHB];
 #pragma unroll
                 for (int u = 0; u < kHB; ++u) {
                     const int q = q0 + u * kDecThreads;
-                    v0[u] = v1[u] = 0.0f;
+                    v0[u] = v1[u] = w0[u] = w1[u] = 0.0f;
                     ncs[u] = 0;
                     if (q < hn) {
                         const int qq = h_s0 * f + q;          // neuron of the flattened [k][f]
-                        const uint32_t item = static_cast<uint32_t>(qq >> 5);
+                        const uint32_t item = static_cast<uint32_t>(qq >> kLg);
                         ncs[u] = static_cast<int>(split_owner(U_g, a.warps_g, (item + 1) * npan_g - 1) / kDecWarps -
                                                   split_owner(U_g, a.warps_g, item * npan_g) / kDecWarps) + 1;
-                        const float* rec = a.grec + static_cast<int64_t>(item) * a.cov_g * 32 + (qq & 31);
+                        const float* rec = rec_of(qq);
                         v0[u] = __ldcg(rec);
-                        if (ncs[u] > 1) v1[u] = __ldcg(rec + 32);
+                        if (kSwiglu) w0[u] = __ldcg(rec + 16);
+                        if (ncs[u] > 1) {
+                            v1[u] = __ldcg(rec + 32);
+                            if (kSwiglu) w1[u] = __ldcg(rec + 48);
+                        }
                     }
                 }
 #pragma unroll
@@ -730,11 +740,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                     const int q = q0 + u * kDecThreads;
                     if (q < hn) {
                         const int qq = h_s0 * f + q;
-                        const float* rec = a.grec + static_cast<int64_t>(qq >> 5) * a.cov_g * 32 + (qq & 31);
-                        float z = v0[u] + v1[u];              // records in contributor order
-                        for (int cc = 2; cc < ncs[u]; ++cc) z += __ldcg(rec + cc * 32);
-                        z *= P.gu_ts[s_e[qq / f]];
-                        const float h = z > 0.0f ? z * z : 0.0f;
+                        const float* rec = rec_of(qq);
+                        float z = v0[u] + v1[u], zu = w0[u] + w1[u];   // records in contributor order
+                        for (int cc = 2; cc < ncs[u]; ++cc) {
+                            z += __ldcg(rec + cc * 32);
+                            if (kSwiglu) zu += __ldcg(rec + cc * 32 + 16);
+                        }
+                        const float ts = P.gu_ts[s_e[qq / f]];
+                        float h;
+                        if constexpr (kSwiglu) {
+                            h = silu(z * ts) * (zu * ts);
+                        } else {
+                            z *= ts;
+                            h = z > 0.0f ? z * z : 0.0f;
+                        }
                         hf[q] = h;
                         a.ws.h[qq] = h;
                     }
@@ -964,7 +983,10 @@ cudaError_t configure_decode_kernel(int dev, int num_sms) {
         !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteSupplied>() ||
         !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteLocal>() ||
         !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteWide>() ||
-        !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteSupplied>()) {
+        !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteSupplied>() ||
+        !configure_one<MOE_W_NVFP4, MOE_ACT_SWIGLU, kRouteLocal>() ||
+        !configure_one<MOE_W_NVFP4, MOE_ACT_SWIGLU, kRouteWide>() ||
+        !configure_one<MOE_W_NVFP4, MOE_ACT_SWIGLU, kRouteSupplied>()) {
         (void)cudaGetLastError();
         return cudaSuccess;   // the separate kernels serve every shape
     }
@@ -976,7 +998,14 @@ cudaError_t configure_decode_kernel(int dev, int num_sms) {
 // CTAs of the decode kernel on this device (0: not available).
 int decode_ctas(int dev) { return (dev >= 0 && dev < 64 && g_decode_ok[dev]) ? g_decode_ctas[dev] : 0; }
 
-cudaError_t launch_decode_layer(const DecodeArgs& a, int wfmt, size_t smem, int ctas, cudaStream_t s) {
+template <int FMT, int ACT>
+static cudaError_t launch_decode_route(const cudaLaunchConfig_t& cfg, const DecodeArgs& a, int route) {
+    if (route == kRouteSupplied) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<FMT, ACT, kRouteSupplied>, a);
+    if (route == kRouteWide) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<FMT, ACT, kRouteWide>, a);
+    return cudaLaunchKernelEx(&cfg, decode_layer_kernel<FMT, ACT, kRouteLocal>, a);
+}
+
+cudaError_t launch_decode_layer(const DecodeArgs& a, int wfmt, int act, size_t smem, int ctas, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kDecThreads);
@@ -990,18 +1019,9 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, int wfmt, size_t smem, int 
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     const int route = a.idx_in ? kRouteSupplied : (a.E > kLocalRankMaxE ? kRouteWide : kRouteLocal);
-    if (wfmt == MOE_W_Q8_0) {
-        if (route == kRouteSupplied)
-            return cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteSupplied>, a);
-        return route == kRouteWide
-                   ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteWide>, a)
-                   : cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteLocal>, a);
-    }
-    if (route == kRouteSupplied)
-        return cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteSupplied>, a);
-    return route == kRouteWide
-               ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteWide>, a)
-               : cudaLaunchKernelEx(&cfg, decode_layer_kernel<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteLocal>, a);
+    if (wfmt == MOE_W_Q8_0) return launch_decode_route<MOE_W_Q8_0, MOE_ACT_SWIGLU>(cfg, a, route);
+    if (act == MOE_ACT_SWIGLU) return launch_decode_route<MOE_W_NVFP4, MOE_ACT_SWIGLU>(cfg, a, route);
+    return launch_decode_route<MOE_W_NVFP4, MOE_ACT_RELU2>(cfg, a, route);
 }
 
 }  // namespace moe

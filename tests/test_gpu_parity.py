@@ -240,6 +240,11 @@ ONE_KERNEL = {
                                 layers=1, zero_fraction=0.925),
     "nv_k22_e512_f32": synth.Workload("ok_nv22", d=256, f=128, E=512, k=22, act="relu2", wfmt="nvfp4",
                                       x_dtype="f32", layers=1, zero_fraction=0.8),
+    # NVFP4 SwiGLU (16-neuron gate + up items, every down group active, down prefetched)
+    "nv_swiglu_k4": synth.Workload("ok_nvsw4", d=512, f=320, E=16, k=4, act="swiglu", wfmt="nvfp4",
+                                   x_dtype="bf16", layers=1),
+    "nv_swiglu_k8_f32": synth.Workload("ok_nvsw8", d=1024, f=192, E=64, k=8, act="swiglu", wfmt="nvfp4",
+                                       x_dtype="f32", layers=1),
 }
 
 
@@ -276,7 +281,8 @@ def test_one_token_one_kernel(name):
 # Supplied routing at one token: the same kernel without the router and the selection.  The
 # trace copies idx and w exactly; the permutation follows them bit for bit; h and out agree
 # with the oracle and with the separate kernels on the same routing.
-@pytest.mark.parametrize("name", ["tiny_f32", "k1", "k8_e64", "k32_e1024", "nv_k6_e32", "nv_k22_e512_f32"])
+@pytest.mark.parametrize("name", ["tiny_f32", "k1", "k8_e64", "k32_e1024", "nv_k6_e32", "nv_k22_e512_f32",
+                                  "nv_swiglu_k4"])
 def test_one_token_one_kernel_supplied_routing(name):
     w = ONE_KERNEL[name]
     idx, wts = synth.zipf_routing(1, w.E, w.k, seed_tag="one-kernel")
@@ -533,6 +539,19 @@ def test_zipf_routing_full_size(name, T):
     _full_case(name, T, idx_in=idx, w_in=wts, tile=8 if T * w.k < 8 * w.E else 64)
 
 
+# One token of the sweep's layer shape with supplied routing: the one-kernel layer for Q8_0
+# and for NVFP4 SwiGLU (every token of the call checked)
+@pytest.mark.parametrize("name", ["zipf", "zipf_nvfp4"])
+def test_zipf_one_token_full_size(name):
+    w = synth.WORKLOADS[name]
+    idx, wts = synth.zipf_routing(1, w.E, w.k)
+    _full_case(name, 1, idx_in=idx, w_in=wts)
+    L = layers.build_layer(w)
+    assert L.launches(1, routing_supplied=True) == 1
+    del L
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ the benchmarked stacks, full shape
 # The call bench.py times at one token: moe_stack_forward over the Gemma-shaped (Q8_0 SwiGLU)
 # and Nemotron-shaped (NVFP4 ReLU^2, 92.5% zeros) stacks, built by the bench's own builder
@@ -579,6 +598,8 @@ STACKS = {
     "tiny_f32_input": (synth.WORKLOADS["tiny"], 3),
     "nv_relu2": (synth.Workload("st_nv", d=512, f=256, E=32, k=6, act="relu2", wfmt="nvfp4", x_dtype="bf16",
                                 layers=3, zero_fraction=0.925), 3),
+    "nv_swiglu": (synth.Workload("st_nvsw", d=768, f=256, E=32, k=8, act="swiglu", wfmt="nvfp4",
+                                 x_dtype="bf16", layers=3), 3),
 }
 
 
