@@ -73,82 +73,92 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const void* __restri
 }
 
 // Many tokens: thread l keeps partial sum l of an 8-token x 8-expert block of logits in
-// registers (each x value meets 8 weights and each weight 8 x values).  The 256-wide slices
-// of x and W that a step needs (i = 256 m + l) are staged into shared memory by a 3-deep
-// cp.async ring, so the next slices stream in while this one is multiplied; then the block's
-// partials go through the fixed halving tree, 32 logits at a time.
-constexpr int kRtT = 8, kRtE = 8, kRtStages = 3;
+// registers (each x value meets 8 weights and each weight 8 x values).
+constexpr int kRtT = 8, kRtE = 8;
 
 __device__ __forceinline__ void rt_cp16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Many tokens, without block barriers in the main loop: warp w owns partial sums
+// l = 32w .. 32w+31 and stages its own 32-wide slices of x (8 tokens) and W (8 experts) through a
+// private cp.async ring, so a warp waits only for its own copies (__syncwarp).  The W rows of
+// a stage are stored with their two 16-byte halves swapped on every other group of 4 rows,
+// so that the 128-bit reads of 8 consecutive lanes hit all 32 banks.  The block's partials
+// then go through the same halving tree as the one-expert kernel above.
 template <bool XF32>
-__global__ void __launch_bounds__(256, 2) router_logits_staged_kernel(const void* __restrict__ x,
-                                                                       const float* __restrict__ W, int T, int d,
-                                                                       int E, float* __restrict__ logits) {
-    constexpr int kXB = XF32 ? 4 : 2;                         // bytes per x element
-    constexpr int kXStage = kRtT * kRouterPartials * kXB;     // x slice: [8 tokens][256]
-    constexpr int kWStage = kRouterPartials * kRtE * 4;       // W slice: [256 rows][8 experts]
+__global__ void __launch_bounds__(256, 2) router_logits_warp_kernel(const void* __restrict__ x,
+                                                                     const float* __restrict__ W, int T, int d,
+                                                                     int E, float* __restrict__ logits) {
+    constexpr int kXB = XF32 ? 4 : 2;                     // bytes per x element
+    constexpr int kStages = XF32 ? 3 : 4;
+    constexpr int kXStage = kRtT * 32 * kXB;              // x slice: [8 tokens][32]
+    constexpr int kWStage = 32 * kRtE * 4;                // W slice: [32 rows][8 experts]
     constexpr int kStage = kXStage + kWStage;
-    __shared__ __align__(16) unsigned char sm[kRtStages * kStage];
-    static_assert(kRtStages * kStage >= 32 * kRouterPartials * 4, "tree buffer reuse");
+    __shared__ __align__(16) unsigned char sm[8 * kStages * kStage];
+    static_assert(8 * kStages * kStage >= 32 * kRouterPartials * 4, "tree buffer reuse");
+    static_assert(8 * kStages * kStage <= 48 * 1024, "static shared memory");
     pdl_wait();
-    const int l = threadIdx.x;
+    const int l = threadIdx.x, warp = l >> 5, lane = l & 31;
     const int e0 = blockIdx.x * kRtE;
     const int t0 = blockIdx.y * kRtT;
     const int nt = min(kRtT, T - t0);
     const int M = d / kRouterPartials;
-    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
-    // this thread's 16-byte chunks of a stage: x rows (tokens past T repeat the last one) and
-    // W rows i = 256 m + row, 2 chunks of 4 experts each
+    unsigned char* ring = sm + warp * kStages * kStage;
+    const uint32_t rbase = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
     auto issue = [&](int m, int st) {
-        const uint32_t dst = sbase + st * kStage;
-        constexpr int kXChunks = kXStage / 16;                // 256 (bf16) or 512 (fp32)
-        for (int c = l; c < kXChunks; c += 256) {
-            const int t = c / (kXChunks / kRtT), q = c % (kXChunks / kRtT);
+        const uint32_t dst = rbase + st * kStage;
+        const int64_t col = static_cast<int64_t>(m) * kRouterPartials + warp * 32;   // first x column / W row
+#pragma unroll
+        for (int u = 0; u < kXStage / 16 / 32; ++u) {    // x: per token kXB * 32 bytes
+            const int c = lane + 32 * u;
+            const int t = c / (kXB * 2), q = c % (kXB * 2);
             const int tt = min(t0 + t, T - 1);
-            const unsigned char* src = static_cast<const unsigned char*>(x) +
-                                       (static_cast<int64_t>(tt) * d + static_cast<int64_t>(m) * kRouterPartials) * kXB +
-                                       q * 16;
-            rt_cp16(dst + c * 16, src);
+            rt_cp16(dst + c * 16, static_cast<const unsigned char*>(x) + (static_cast<int64_t>(tt) * d + col) * kXB + q * 16);
         }
-        for (int c = l; c < kRouterPartials * 2; c += 256) {
-            const int row = c >> 1, h = c & 1;
-            rt_cp16(dst + kXStage + c * 16,
-                    W + (static_cast<int64_t>(m) * kRouterPartials + row) * E + e0 + 4 * h);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {                    // W: 32 rows x 2 halves
+            const int c = lane + 32 * u;
+            const int r = c >> 1, h = c & 1;
+            const int hs = h ^ ((r >> 2) & 1);
+            rt_cp16(dst + kXStage + (2 * r + hs) * 16, W + (col + r) * E + e0 + 4 * h);
         }
     };
 #pragma unroll
-    for (int st = 0; st < kRtStages; ++st) {
+    for (int st = 0; st < kStages; ++st) {
         if (st < M) issue(st, st);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     float acc[kRtT * kRtE];
 #pragma unroll
     for (int v = 0; v < kRtT * kRtE; ++v) acc[v] = 0.0f;
+    const int sw = (lane >> 2) & 1;
     for (int m = 0; m < M; ++m) {
-        const int st = m % kRtStages;
-        asm volatile("cp.async.wait_group %0;" ::"n"(kRtStages - 1) : "memory");
-        __syncthreads();
-        const unsigned char* xs = sm + st * kStage;
-        const float4* wr = reinterpret_cast<const float4*>(sm + st * kStage + kXStage + l * kRtE * 4);
-        const float4 wa = wr[0], wb = wr[1];
+        const int st = m % kStages;
+        asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+        __syncwarp();
+        const unsigned char* xs = ring + st * kStage;
+        const float4* wr = reinterpret_cast<const float4*>(ring + st * kStage + kXStage) + 2 * lane;
+        const float4 wa = wr[sw], wb = wr[sw ^ 1];
         const float wv[kRtE] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
         for (int t = 0; t < kRtT; ++t) {
             float xv;
-            if (XF32) xv = reinterpret_cast<const float*>(xs)[t * kRouterPartials + l];
-            else xv = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xs)[t * kRouterPartials + l]);
+            if (XF32) xv = reinterpret_cast<const float*>(xs)[t * 32 + lane];
+            else xv = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xs)[t * 32 + lane]);
 #pragma unroll
             for (int c = 0; c < kRtE; ++c) acc[t * kRtE + c] = fmaf(xv, wv[c], acc[t * kRtE + c]);
         }
-        __syncthreads();   // every thread is done with the stage before it is refilled
-        if (m + kRtStages < M) issue(m + kRtStages, st);
+        __syncwarp();   // every lane is done with the stage before it is refilled
+        if (m + kStages < M) issue(m + kStages, st);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
+    // The tree: all 256 partials of 32 logits at a time in shared memory, then warp w takes
+    // logits 4w .. 4w+3 of the pass: lane j holds partials j + 32 q (q = 0..7), so levels 128,
+    // 64 and 32 are additions in registers and levels 16 .. 1 shuffles (lane j adds lane j + h),
+    // the same pairs s_l += s_{l+h} in the same order.
     constexpr int kPass = 32;
     float (*red)[kRouterPartials] = reinterpret_cast<float (*)[kRouterPartials]>(sm);
 #pragma unroll
@@ -157,24 +167,21 @@ __global__ void __launch_bounds__(256, 2) router_logits_staged_kernel(const void
         for (int v = 0; v < kPass; ++v) red[v][l] = acc[pass * kPass + v];
         __syncthreads();
 #pragma unroll
-        for (int h = kRouterPartials / 2; h >= 32; h >>= 1) {
-            if (l < h) {
+        for (int u = 0; u < kPass / 8; ++u) {
+            const int v = warp * (kPass / 8) + u;
+            float sq[8];
 #pragma unroll
-                for (int v = 0; v < kPass; ++v) red[v][l] = red[v][l] + red[v][l + h];
-            }
-            __syncthreads();
-        }
-        if (l < kPass) {   // levels 16 .. 1: thread v takes logit v's 32 partials, same pairs
-            float sv[32];
+            for (int q = 0; q < 8; ++q) sq[q] = red[v][lane + 32 * q];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sv[j] = red[l][j];
+            for (int q = 0; q < 4; ++q) sq[q] = sq[q] + sq[q + 4];   // h = 128
+            sq[0] = sq[0] + sq[2];                                    // h = 64
+            sq[1] = sq[1] + sq[3];
+            float sv = sq[0] + sq[1];                                 // h = 32
 #pragma unroll
-            for (int h = 16; h >= 1; h >>= 1)
-#pragma unroll
-                for (int j = 0; j < h; ++j) sv[j] = sv[j] + sv[j + h];
-            const int vv = pass * kPass + l;
+            for (int h = 16; h >= 1; h >>= 1) sv = sv + __shfl_down_sync(0xffffffffu, sv, h);
+            const int vv = pass * kPass + v;
             const int t = vv / kRtE;
-            if (t < nt) logits[static_cast<int64_t>(t0 + t) * E + e0 + (vv % kRtE)] = sv[0];
+            if (lane == 0 && t < nt) logits[static_cast<int64_t>(t0 + t) * E + e0 + (vv % kRtE)] = sv;
         }
         __syncthreads();
     }
@@ -190,8 +197,8 @@ cudaError_t launch_router_logits(const void* x, int xt, const float* W, int64_t 
     if (T <= 4) return launch_pdl(router_logits_kernel<4>, dim3(E / 4, 1), block, 0, s, x, xt, W, Ti, di, Ei, logits);
     if (E % 8 == 0) {
         const dim3 grid(static_cast<unsigned>(E / 8), static_cast<unsigned>((T + 7) / 8));
-        if (xt == MOE_F32) return launch_pdl(router_logits_staged_kernel<true>, grid, block, 0, s, x, W, Ti, di, Ei, logits);
-        return launch_pdl(router_logits_staged_kernel<false>, grid, block, 0, s, x, W, Ti, di, Ei, logits);
+        if (xt == MOE_F32) return launch_pdl(router_logits_warp_kernel<true>, grid, block, 0, s, x, W, Ti, di, Ei, logits);
+        return launch_pdl(router_logits_warp_kernel<false>, grid, block, 0, s, x, W, Ti, di, Ei, logits);
     }
     return launch_pdl(router_logits_kernel<8>, dim3(E / 4, (unsigned)((T + 7) / 8)), block, 0, s, x, xt, W, Ti, di, Ei,
                       logits);

@@ -72,7 +72,7 @@ def test_nvfp4_packer_bitexact(rows, cols):
 
 # ------------------------------------------------------------------ router
 @pytest.mark.parametrize("name", ["tiny", "gemma", "nemotron"])
-@pytest.mark.parametrize("T", [1, 3, 16, 37])
+@pytest.mark.parametrize("T", [1, 3, 16, 37, 512, 4096])
 def test_router_topk_bitexact(name, T):
     w = synth.WORKLOADS[name]
     x = synth.tokens(w, T, tag="router")
