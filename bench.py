@@ -779,7 +779,8 @@ SECONDARY = [("gemma", 512, 30, 20, "none", "none"), ("gemma", 1, 30, 400, "q8_0
              ("gemma_int8pc", 1, 8, 400, "none", "none"), ("gemma_int8pc", 64, 8, 100, "none", "none"),
              ("nemotron", 1, 40, 400, "none", "none"), ("nemotron", 1, 8, 200, "none", "down"),
              ("nemotron", 1, 8, 200, "none", "all"),
-             ("minimax", 4096, 8, 10, "none", "none"), ("minimax", 4096, 8, 10, "q8_0", "none")]
+             ("minimax", 4096, 8, 10, "none", "none"), ("minimax", 4096, 8, 10, "q8_0", "none"),
+             ("zipf_nvfp4", 1, 4, 400, "none", "none"), ("zipf_nvfp4", 64, 4, 100, "none", "none")]
 
 
 def cpu_baseline(w, T, layers, budget_s, single_core_s=8.0, single=True, act_q8=False):
