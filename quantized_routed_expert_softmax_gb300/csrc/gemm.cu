@@ -247,6 +247,21 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float v[8]) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 columns of each of the two issuers' accumulators, one wait for both loads.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t a0, uint32_t a1, uint32_t r[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+        "[%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(a0), "r"(a1)
+        : "memory");
+}
+
 // Offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
@@ -636,42 +651,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + acc_col0 + static_cast<uint32_t>(2 * buf * g.acc_stride);
             bool range_ok = true;
-            for (int c0 = 0; c0 < n16; c0 += 8) {
-                float v[8], v1[8];
-                if (has0) tmem_ld8(tbase + static_cast<uint32_t>(c0), v);
-                if (has1) tmem_ld8(tbase + static_cast<uint32_t>(g.acc_stride + c0), v1);
+            for (int c0 = 0; c0 < n16; c0 += 16) {   // 16 tokens: both accumulators' columns, one wait
+                float v[16];
+                if (has0 && has1) {
+                    uint32_t r[32];
+                    tmem_ld16x2(tbase + static_cast<uint32_t>(c0), tbase + static_cast<uint32_t>(g.acc_stride + c0), r);
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) v[jj] = has0 ? (has1 ? v[jj] + v1[jj] : v[jj]) : v1[jj];
+                    for (int jj = 0; jj < 16; ++jj) v[jj] = __uint_as_float(r[jj]) + __uint_as_float(r[16 + jj]);
+                } else {
+                    tmem_ld16(tbase + static_cast<uint32_t>(has0 ? c0 : g.acc_stride + c0), v);
+                }
+                // in groups of 8 tokens, each step for all 8 at once (the shuffles, then the
+                // activations, then the stores), so the tokens' latency chains overlap
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int n = c0 + j;
-                    const int64_t prow = static_cast<int64_t>(it.r_first + n);
-                    const float z = v[j] * ts;
+                for (int jb = 0; jb < 16; jb += 8) {
+                    float z[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) z[j] = v[jb + j] * ts;
                     if (g.kind == kGateUp) {
-                        float hv;
+                        float hv[8];
                         int64_t col;
-                        bool store;
+                        bool lane_stores;
                         if (g.act == MOE_ACT_SWIGLU) {
-                            const float u = __shfl_xor_sync(0xffffffffu, z, 1);   // odd lanes hold the up rows
-                            hv = silu(z) * u;
+                            float u[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) u[j] = __shfl_xor_sync(0xffffffffu, z[j], 1);   // odd lanes: up rows
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) hv[j] = silu(z[j]) * u[j];
                             col = it.mtile * 64 + (row >> 1);
-                            store = !(lane & 1) && n < it.nt;
+                            lane_stores = !(lane & 1);
                         } else {
-                            hv = z > 0.0f ? z * z : 0.0f;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) hv[j] = z[j] > 0.0f ? z[j] * z[j] : 0.0f;
                             col = it.mtile * kTileM + row;
-                            store = n < it.nt;
+                            lane_stores = true;
                         }
-                        if (store) {
-                            const int64_t o = prow * a.f + col;
-                            a.ws.h[o] = hv;
-                            __half hh, hl;
-                            split_f16(hv, &hh, &hl);
-                            range_ok &= fabsf(hv) <= 65504.0f;
-                            a.ws.h_hi[o] = __half_as_ushort(hh);
-                            a.ws.h_lo[o] = __half_as_ushort(hl);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int n = c0 + jb + j;
+                            if (lane_stores && n < it.nt) {
+                                const int64_t o = static_cast<int64_t>(it.r_first + n) * a.f + col;
+                                a.ws.h[o] = hv[j];
+                                __half hh, hl;
+                                split_f16(hv[j], &hh, &hl);
+                                range_ok &= fabsf(hv[j]) <= 65504.0f;
+                                a.ws.h_hi[o] = __half_as_ushort(hh);
+                                a.ws.h_lo[o] = __half_as_ushort(hl);
+                            }
                         }
-                    } else if (n < it.nt) {
-                        a.ws.y[prow * a.d + it.mtile * kTileM + row] = z;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int n = c0 + jb + j;
+                            if (n < it.nt) a.ws.y[static_cast<int64_t>(it.r_first + n) * a.d + it.mtile * kTileM + row] = z[j];
+                        }
                     }
                 }
             }
