@@ -328,16 +328,17 @@ __device__ __forceinline__ Item decode_item(const GemmArgs& g, const int* tile_p
 //     two per byte], then scales [8 groups][128 B] at byte 8192.
 // SwiGLU gate.up tiles stage gate rows of 64 neurons as rows 0..63 and the same neurons' up
 // rows as 64..127 (the gate/up half is a dimension of the tensor maps).
+template <int KIND>
 __device__ __forceinline__ void load_slot(const GemmArgs& g, uint32_t dst, int e, int mtile, int ks0, uint64_t* bar) {
     const bool q8 = (g.fmt == MOE_W_Q8_0);
     const uint32_t scales_at = q8 ? 16384u : 8192u;
-    if (g.kind == kDown && !q8) {
+    if (KIND == kDown && !q8) {
         tma_4d(dst, &g.tw_codes, mtile * 64, 0, ks0 * 4, e, bar);
         tma_3d(dst + scales_at, &g.tw_scales, mtile * kTileM, ks0 * 4, e, bar);
         return;
     }
     const int p0 = ks0 * (q8 ? 2 : 1);   // first K panel
-    if (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU) {
+    if (KIND == kGateUp && g.act == MOE_ACT_SWIGLU) {
         tma_5d(dst, &g.tw_codes, 0, mtile * 8, 0, p0, e, bar);
         tma_4d(dst + scales_at, &g.tw_scales, mtile * 64, 0, p0, e, bar);
     } else {
@@ -348,9 +349,10 @@ __device__ __forceinline__ void load_slot(const GemmArgs& g, uint32_t dst, int e
 
 // Dequantise 16 columns (chunk c16 of K step js of a raw slot) of tile row r into the A hi
 // (and, for Q8_0, lo) columns of tensor memory at ta (this warp's lane quadrant).
+template <int KIND>
 __device__ __forceinline__ void dequant_step(const GemmArgs& g, const unsigned char* raw, int js, uint32_t ta, int r,
                                              int c16) {
-    const bool swiglu = (g.kind == kGateUp && g.act == MOE_ACT_SWIGLU);
+    const bool swiglu = (KIND == kGateUp && g.act == MOE_ACT_SWIGLU);
     {
         const int sr = swiglu ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;   // staged row
         uint32_t h[8];
@@ -379,7 +381,7 @@ __device__ __forceinline__ void dequant_step(const GemmArgs& g, const unsigned c
                 hl[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&l23);
             }
             tmem_st8(ta + 32 + c16 * 8, hl);
-        } else if (g.kind == kDown) {
+        } else if (KIND == kDown) {
             // NVFP4 neuron layout: columns 16*c16 .. +15 are group c16; row sr is nibble
             // (sr & 1) of byte sr/2 in each neuron's run
             const int gg = 4 * js + c16;
@@ -421,6 +423,9 @@ __device__ __forceinline__ void dequant_step(const GemmArgs& g, const unsigned c
 }
 
 // ------------------------------------------------------------------------------ the kernel
+// KIND (gate.up or down) is a template parameter: each launch's code and register allocation
+// hold only its own epilogue and conversions.
+template <int KIND>
 __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __grid_constant__ GemmArgs g) {
     pdl_wait();
     const ExpertArgs& a = g.a;
@@ -470,7 +475,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
         s_fail = 0;
     }
     // the work list: per slot, (token tiles) x (row tiles); exclusive prefix over the slots
-    const int rows_out = (g.kind == kGateUp) ? a.rows_gu : a.d;
+    const int rows_out = (KIND == kGateUp) ? a.rows_gu : a.d;
     const int mtiles = rows_out / kTileM;
     {
         const int per = (g.slot_cap + kGemmThreads - 1) / kGemmThreads;   // <= 2 (slot_cap <= 1024)
@@ -507,8 +512,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
     tc_fence_after();
     const uint32_t tmem = tmem_base;
     const int total = tile_prefix[g.slot_cap];
-    const int ksteps = ((g.kind == kGateUp) ? a.d : a.f) / kStepK;
-    const int rows_w = (g.kind == kGateUp) ? a.rows_gu : a.d;
+    const int ksteps = ((KIND == kGateUp) ? a.d : a.f) / kStepK;
+    const int rows_w = (KIND == kGateUp) ? a.rows_gu : a.d;
     // a_stages (2 or 4) and acc_bufs (1 or 2) are powers of two: shifts and masks
     const uint32_t a_shift = (g.a_stages == 4) ? 2u : 1u, a_mask = (1u << a_shift) - 1u;
     const uint32_t b_shift = (g.acc_bufs == 2) ? 1u : 0u, b_mask = (1u << b_shift) - 1u;
@@ -530,7 +535,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
                     }
                     mbar_arrive_expect_tx(&raw_full[slot], g.slot_bytes);
                     raw_issued[slot] = use + 1;
-                    load_slot(g, s_addr(raws + slot * kRawSlot), it.e, it.mtile, ks0, &raw_full[slot]);
+                    load_slot<KIND>(g, s_addr(raws + slot * kRawSlot), it.e, it.mtile, ks0, &raw_full[slot]);
                 }
             }
             if (!ok) {
@@ -631,7 +636,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
         // ---------------------------------------------------------------- epilogue
         const int q = warp & 3;
         const int row = q * 32 + lane;                 // accumulator lane = tile row
-        const float* ts_arr = (g.kind == kGateUp) ? a.gu_ts : a.dn_ts;
+        const float* ts_arr = (KIND == kGateUp) ? a.gu_ts : a.dn_ts;
         uint32_t n_item = 0, gs0 = 0;   // gs0: global index of the item's first K step
         bool ok = true;
         for (int item = blockIdx.x; item < total; item += gridDim.x, ++n_item, gs0 += ksteps) {
@@ -661,49 +666,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
                 } else {
                     tmem_ld16(tbase + static_cast<uint32_t>(has0 ? c0 : g.acc_stride + c0), v);
                 }
-                // in groups of 8 tokens, each step for all 8 at once (the shuffles, then the
-                // activations, then the stores), so the tokens' latency chains overlap
+                if (KIND == kGateUp && g.act == MOE_ACT_SWIGLU) {
+                    // lane pairs (2i: gate row i, 2i+1: up row i) split the 16 tokens: the even
+                    // lane takes tokens 0..7 and the odd lane 8..15, each receiving the partner's
+                    // half in one shuffle per token; the 8 tokens' steps run side by side
+                    const bool odd = lane & 1;
+                    float mine[8], u[8];   // this lane's row and the partner's row, of this lane's tokens
 #pragma unroll
-                for (int jb = 0; jb < 16; jb += 8) {
-                    float z[8];
+                    for (int j = 0; j < 8; ++j) {
+                        mine[j] = (odd ? v[8 + j] : v[j]) * ts;
+                        u[j] = __shfl_xor_sync(0xffffffffu, (odd ? v[j] : v[8 + j]) * ts, 1);
+                    }
+                    float hv[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) z[j] = v[jb + j] * ts;
-                    if (g.kind == kGateUp) {
-                        float hv[8];
-                        int64_t col;
-                        bool lane_stores;
-                        if (g.act == MOE_ACT_SWIGLU) {
-                            float u[8];
+                    for (int j = 0; j < 8; ++j) hv[j] = odd ? silu(u[j]) * mine[j] : silu(mine[j]) * u[j];
+                    const int64_t col = it.mtile * 64 + (row >> 1);
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) u[j] = __shfl_xor_sync(0xffffffffu, z[j], 1);   // odd lanes: up rows
+                    for (int j = 0; j < 8; ++j) {
+                        const int n = c0 + (odd ? 8 : 0) + j;
+                        if (n < it.nt) {
+                            const int64_t o = static_cast<int64_t>(it.r_first + n) * a.f + col;
+                            a.ws.h[o] = hv[j];
+                            __half hh, hl;
+                            split_f16(hv[j], &hh, &hl);
+                            range_ok &= fabsf(hv[j]) <= 65504.0f;
+                            a.ws.h_hi[o] = __half_as_ushort(hh);
+                            a.ws.h_lo[o] = __half_as_ushort(hl);
+                        }
+                    }
+                } else {
+                    // in groups of 8 tokens, each step for all 8 at once, so the tokens' latency
+                    // chains overlap
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) hv[j] = silu(z[j]) * u[j];
-                            col = it.mtile * 64 + (row >> 1);
-                            lane_stores = !(lane & 1);
+                    for (int jb = 0; jb < 16; jb += 8) {
+                        float z[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) z[j] = v[jb + j] * ts;
+                        if (KIND == kGateUp) {   // ReLU^2
+                            const int64_t col = it.mtile * kTileM + row;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int n = c0 + jb + j;
+                                const float hv = z[j] > 0.0f ? z[j] * z[j] : 0.0f;
+                                if (n < it.nt) {
+                                    const int64_t o = static_cast<int64_t>(it.r_first + n) * a.f + col;
+                                    a.ws.h[o] = hv;
+                                    __half hh, hl;
+                                    split_f16(hv, &hh, &hl);
+                                    range_ok &= fabsf(hv) <= 65504.0f;
+                                    a.ws.h_hi[o] = __half_as_ushort(hh);
+                                    a.ws.h_lo[o] = __half_as_ushort(hl);
+                                }
+                            }
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) hv[j] = z[j] > 0.0f ? z[j] * z[j] : 0.0f;
-                            col = it.mtile * kTileM + row;
-                            lane_stores = true;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int n = c0 + jb + j;
-                            if (lane_stores && n < it.nt) {
-                                const int64_t o = static_cast<int64_t>(it.r_first + n) * a.f + col;
-                                a.ws.h[o] = hv[j];
-                                __half hh, hl;
-                                split_f16(hv[j], &hh, &hl);
-                                range_ok &= fabsf(hv[j]) <= 65504.0f;
-                                a.ws.h_hi[o] = __half_as_ushort(hh);
-                                a.ws.h_lo[o] = __half_as_ushort(hl);
+                            for (int j = 0; j < 8; ++j) {
+                                const int n = c0 + jb + j;
+                                if (n < it.nt)
+                                    a.ws.y[static_cast<int64_t>(it.r_first + n) * a.d + it.mtile * kTileM + row] = z[j];
                             }
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int n = c0 + jb + j;
-                            if (n < it.nt) a.ws.y[static_cast<int64_t>(it.r_first + n) * a.d + it.mtile * kTileM + row] = z[j];
                         }
                     }
                 }
@@ -751,8 +772,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
                 tc_fence_after();
                 const unsigned char* raw = raws + slot * kRawSlot;
                 const uint32_t ta = tq + static_cast<uint32_t>(sa) * kAColsPerStage;
-                dequant_step(g, raw, j, ta, r, 2 * cpair);
-                dequant_step(g, raw, j, ta, r, 2 * cpair + 1);
+                dequant_step<KIND>(g, raw, j, ta, r, 2 * cpair);
+                dequant_step<KIND>(g, raw, j, ta, r, 2 * cpair + 1);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
@@ -929,10 +950,14 @@ cudaError_t weight_maps(GemmArgs* g, const uint8_t* W, int64_t E, int64_t mat_by
 cudaError_t configure_gemm_kernels() {
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kGemmSmem));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    for (int kind = 0; kind < 2; ++kind) {
+        const void* fn = kind == 0 ? reinterpret_cast<const void*>(expert_gemm_kernel<kGateUp>)
+                                   : reinterpret_cast<const void*>(expert_gemm_kernel<kDown>);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kGemmSmem));
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 size_t gemm_smem_bytes() { return kGemmSmem; }
@@ -984,7 +1009,8 @@ cudaError_t launch_expert_gemm(const ExpertArgs& a, int kind, int wfmt, int act,
     const int rows_out = (kind == kGateUp) ? a.rows_gu : a.d;
     const int64_t bound = static_cast<int64_t>(rows_out / kTileM) * (slot_cap + (a.P + g.nt_max - 1) / g.nt_max);
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms, bound)));
-    return launch_pdl(expert_gemm_kernel, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, g);
+    if (kind == kGateUp) return launch_pdl(expert_gemm_kernel<kGateUp>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, g);
+    return launch_pdl(expert_gemm_kernel<kDown>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, g);
 }
 
 }  // namespace moe
