@@ -694,9 +694,11 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, moe_dtyp
     a.rows_gu = static_cast<int>(desc->act == MOE_ACT_SWIGLU ? 2 * desc->f : desc->f);
     a.tt_gu = p.tt_gu;
     a.tt_dn = p.tt_dn;
-    {   // warps per gate.up tile: each warp should stream at least 12 K panels
+    {   // warps per gate.up tile: at most 4, and each warp should stream at least 12 K panels
+        // (fewer, longer panel runs per warp cost parallelism at d = 2816, and 8 warps of 24
+        // panels were slower than 4 of 48 at d = 6144)
         const int npan = static_cast<int>(desc->wfmt == MOE_W_NVFP4 ? desc->d / 64 : desc->d / 32);
-        int wpt = 8;
+        int wpt = 4;
         while (wpt > 1 && npan / wpt < 12) wpt /= 2;
         a.gu_wpt = wpt;
     }
