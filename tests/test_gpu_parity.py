@@ -165,13 +165,24 @@ def test_layer_small_parity(name, T):
     assert_close(out, ref["out"])
 
 
-# NVFP4 down on the tensor cores at two or more tokens, the GEMV path forced: passes of 8, 16
-# and 32 tokens with ragged last passes (T = 300 puts about 75 rows on each of the 8 experts),
-# ReLU^2 with 92.5% zeros (inactive groups skipped, uneven halves) and SwiGLU with 20 groups.
-@pytest.mark.parametrize("name", ["small_nvfp4_relu2", "small_nvfp4_swiglu"])
+# NVFP4 down at two or more tokens, the GEMV path forced: on the tensor cores in passes of 8,
+# 16 and 32 tokens with ragged last passes (T = 300 puts about 75 rows on each of the 8
+# experts), ReLU^2 with 92.5% zeros (inactive groups skipped, uneven halves) and SwiGLU with 20
+# groups; and the CUDA-core kernel for a wide f.
+NV_DOWN = {
+    "small_nvfp4_relu2": SMALL["small_nvfp4_relu2"],
+    "small_nvfp4_swiglu": SMALL["small_nvfp4_swiglu"],
+    # f = 2688: the h planes of 8 tokens would leave one CTA per SM, so the CUDA-core kernel
+    # (2-token tiles) runs the down projection at every T here
+    "wide_f_relu2": synth.Workload("nv_wide_f", d=256, f=2688, E=16, k=4, act="relu2", wfmt="nvfp4", x_dtype="bf16",
+                                   layers=1, zero_fraction=0.925),
+}
+
+
+@pytest.mark.parametrize("name", list(NV_DOWN))
 @pytest.mark.parametrize("T", [2, 9, 40, 300])
 def test_nvfp4_down_tensor_core_parity(name, T):
-    w = SMALL[name]
+    w = NV_DOWN[name]
     L, out, tr, ref = _run_small(w, T, path="gemv")
     assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
     assert np.array_equal(tr["perm"].cpu().numpy(), ref["perm"])
