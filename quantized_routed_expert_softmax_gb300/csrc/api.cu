@@ -20,6 +20,7 @@ cudaError_t launch_permute_large(const int32_t*, const float*, int64_t, int64_t,
                                  cudaStream_t);
 cudaError_t launch_route_decode(const void*, int, const float*, int64_t, int64_t, int64_t, int, int, const Workspace&,
                                 cudaStream_t);
+bool route_decode_fits(int64_t, int64_t, int64_t);
 cudaError_t configure_gemv_kernels();
 cudaError_t launch_gate_up_gemv(const ExpertArgs&, int, int, int, cudaStream_t);
 cudaError_t launch_down_gemv(const ExpertArgs&, int, int, cudaStream_t);
@@ -234,7 +235,8 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
     auto pow2 = [](int v) { return v >= 8 ? 8 : (v >= 4 ? 4 : (v >= 2 ? 2 : 1)); };   // (rounds down)
     p.tt_gu = pow2(p.tt_gu);
     p.tt_dn = pow2(p.tt_dn);
-    p.small_route = (T <= kSmallT && p.P <= kSmallPairs && T * d->E <= kFusedRouteLogits);
+    p.small_route = (T <= kSmallT && p.P <= kSmallPairs && T * d->E <= kFusedRouteLogits) &&
+                    route_decode_fits(T, d->d, d->E);
     const int64_t rows_per_tile = (d->wfmt == MOE_W_NVFP4) ? 256 : 32;
     p.fuse_combine = T * rows_per_tile <= 256;
     const int64_t dn_bytes = matrix_bytes(d->wfmt, d->d, d->f);

@@ -720,30 +720,17 @@ __device__ void permute_block_256(const int* sidx, int T, int k, int E, int gwor
 // Router + top-k + softmax + permutation for small batches (T * E <= 4096, T * k <= 1024)
 // in one launch.  grid: (32 residue classes, E / (32 * EPL) expert chunks) x 256 threads.
 // Warp j of CTA (c, chunk) owns the canonical partial sum l = c + 32 j for the chunk's
-// 32 * EPL experts (lane = EPL experts): it reads rows i = l, l + 256, ... of W, coalesced
-// across the warp.  Narrow chunks spread the router weights over 128-256 CTAs: a CTA can keep
-// only so many loads in flight, and the weights come from HBM.  Tree levels h = 128, 64, 32
+// 32 * EPL experts (lane = EPL experts): rows i = l, l + 256, ... of W, staged in shared
+// memory with 16-byte asynchronous copies.  Narrow chunks spread the router weights over
+// 128-256 CTAs, and the weights come from HBM.  Tree levels h = 128, 64, 32
 // combine partials of the same residue c, inside the CTA; the CTA writes its result to
 // part[t][e][c].  The last CTA to finish (atomic counter, no waiting) applies levels
 // h = 16 .. 1 across the 32 residues, then selects, weights and permutes, and resets the
 // counter.
 constexpr int kResidues = 32;
-constexpr int kChainBatch = 12;
 constexpr int kFusedRouteLogits = 4096;
 constexpr int kRankTopkMaxE = 256;   // above this, top-k goes through segment candidates
-
-template <int EPL>
-__device__ __forceinline__ void load_w_row(const float* __restrict__ W, int64_t off, float (&w)[EPL]) {
-    if constexpr (EPL == 4) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(W + off));
-        w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
-    } else if constexpr (EPL == 2) {
-        const float2 v = __ldg(reinterpret_cast<const float2*>(W + off));
-        w[0] = v.x, w[1] = v.y;
-    } else {
-        w[0] = __ldg(W + off);
-    }
-}
+constexpr size_t kRouteDecodeMaxSmem = 160 * 1024;   // route_decode_kernel's weight rows and x values (beside 43 KB static)
 
 // a beats b: larger logit, or equal logit and lower expert index
 __device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) { return va > vb || (va == vb && ea < eb); }
@@ -887,7 +874,6 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
     constexpr int kChunk = 32 * EPL;
     const int c = blockIdx.x, chunk = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int l = c + kResidues * warp;
     const int e0 = chunk * kChunk + lane * EPL;
     const bool on = e0 < E;
     const int nchain = d / kRouterPartials;     // d is a multiple of 256
@@ -898,16 +884,41 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
     float (*red)[4][kChunk] = reinterpret_cast<float (*)[4][kChunk]>(buf);
     float* slog = buf;
     __shared__ int s_last;
-    // The router weights do not depend on the previous kernel: the first batch of rows is
-    // loaded before waiting for it.
-    float w0[kChainBatch][EPL];
-#pragma unroll
-    for (int u = 0; u < kChainBatch; ++u)
-        if (on && u < nchain) load_w_row<EPL>(W, static_cast<int64_t>(l + u * kRouterPartials) * E + e0, w0[u]);
+    // The CTA's rows of the router weights (warp j: rows l + 256 m, m < nchain, the chunk's
+    // experts) are copied into shared memory before waiting for the previous kernel; then the
+    // x values the CTA's chains read ([T][8 warps][nchain]).  The products read both from
+    // shared memory, so no chain step waits on a global load.
+    extern __shared__ __align__(16) float rdyn[];
+    float* wsm = rdyn;                                   // [8][nchain][kChunk]
+    float* xsm = rdyn + 8 * nchain * kChunk;             // [T][8][nchain]
+    {
+        const uint32_t wbase = static_cast<uint32_t>(__cvta_generic_to_shared(wsm));
+        constexpr int kQ = kChunk / 4;                   // 16-byte pieces of a row segment
+        for (int it = threadIdx.x; it < 8 * nchain * kQ; it += blockDim.x) {
+            const int ww = it / (nchain * kQ), rem = it % (nchain * kQ);
+            const int m = rem / kQ, q4 = rem % kQ;
+            const int e = chunk * kChunk + q4 * 4;
+            if (e < E) {
+                const int64_t i = c + 32 * ww + static_cast<int64_t>(kRouterPartials) * m;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(wbase + static_cast<uint32_t>(it) * 16),
+                             "l"(W + i * E + e)
+                             : "memory");
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
     pdl_wait();
     // No early trigger: the expert kernel that follows is launched once the partial-sum CTAs
     // have exited (and the last one triggers below), so its CTAs spread over every SM
     // instead of piling onto the few SMs the routing CTAs leave free.
+    for (int it = threadIdx.x; it < T * 8 * nchain; it += blockDim.x) {
+        const int t = it / (8 * nchain), rem = it % (8 * nchain);
+        const int ww = rem / nchain, m = rem % nchain;
+        xsm[it] = load_x(x, xt, static_cast<int64_t>(t) * d + c + 32 * ww + static_cast<int64_t>(kRouterPartials) * m);
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const float* wrow = wsm + warp * nchain * kChunk + lane * EPL;
     for (int t0 = 0; t0 < T; t0 += 4) {
         const int nt = min(4, T - t0);
         float acc[4][EPL];
@@ -915,35 +926,17 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int q = 0; q < EPL; ++q) acc[t][q] = 0.0f;
-        for (int m0 = 0; m0 < nchain; m0 += kChainBatch) {
-            float wv[kChainBatch][EPL];
-            float xv[4][kChainBatch];
+        if (on) {
+            const float* xr = xsm + (t0 * 8 + warp) * nchain;
+            for (int m = 0; m < nchain; ++m) {   // chain l: fmaf over i = l, l + 256, ... in increasing i
+                float wv[EPL];
 #pragma unroll
-            for (int u = 0; u < kChainBatch; ++u) {
-                if (m0 + u < nchain) {
-                    const int i = l + (m0 + u) * kRouterPartials;
-                    if (on) {
-                        if (m0 == 0) {
+                for (int q = 0; q < EPL; ++q) wv[q] = wrow[m * kChunk + q];
 #pragma unroll
-                            for (int q = 0; q < EPL; ++q) wv[u][q] = w0[u][q];
-                        } else {
-                            load_w_row<EPL>(W, static_cast<int64_t>(i) * E + e0, wv[u]);
-                        }
-                    }
+                for (int t = 0; t < 4; ++t) {
+                    const float xv = (t < nt) ? xr[t * 8 * nchain + m] : 0.0f;
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        xv[t][u] = (t < nt) ? load_x(x, xt, static_cast<int64_t>(t0 + t) * d + i) : 0.0f;
-                }
-            }
-            if (on) {
-#pragma unroll
-                for (int u = 0; u < kChainBatch; ++u) {
-                    if (m0 + u < nchain) {
-#pragma unroll
-                        for (int t = 0; t < 4; ++t)
-#pragma unroll
-                            for (int q = 0; q < EPL; ++q) acc[t][q] = fmaf(xv[t][u], wv[u][q], acc[t][q]);
-                    }
+                    for (int q = 0; q < EPL; ++q) acc[t][q] = fmaf(xv, wv[q], acc[t][q]);
                 }
             }
         }
@@ -1206,6 +1199,15 @@ cudaError_t configure_route_cluster() {
 // Enables the cluster router when a 16-CTA cluster with the largest shared-memory request
 // can be resident; otherwise every shape keeps the partial-sum router.
 cudaError_t configure_route_kernels() {
+    // route_decode_kernel: its weight rows and x values, up to kRouteDecodeMaxSmem (larger
+    // shapes take the many-token routing kernels)
+    for (const void* fn : {reinterpret_cast<const void*>(route_decode_kernel<1>),
+                           reinterpret_cast<const void*>(route_decode_kernel<2>),
+                           reinterpret_cast<const void*>(route_decode_kernel<4>)}) {
+        const cudaError_t ea = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    static_cast<int>(kRouteDecodeMaxSmem));
+        if (ea != cudaSuccess) return ea;
+    }
     cudaError_t e = configure_route_cluster<4>();
     if (e == cudaSuccess) e = configure_route_cluster<8>();
     if (e == cudaSuccess) e = configure_route_cluster<16>();
@@ -1254,6 +1256,22 @@ cudaError_t launch_route_cluster(const void* x, int xt, const float* W, int T, i
     return cudaLaunchKernelEx(&cfg, route_cluster_kernel<EPC>, x, xt, W, T, d, E, k, gwords, ws);
 }
 
+// Dynamic shared memory of route_decode_kernel: the CTA's router-weight rows and x values.
+size_t route_decode_smem(int64_t T, int64_t d, int epl) {
+    const int64_t nchain = d / kRouterPartials;
+    return static_cast<size_t>(8 * nchain * 32 * epl + T * 8 * nchain) * sizeof(float);
+}
+
+int route_decode_epl(int64_t E) { return (E <= 128) ? 1 : (E <= 512 ? 2 : 4); }
+
+// Whether the one-launch routing serves T tokens of this shape (the cluster kernel, or the
+// partial-sum kernel whose shared memory holds its weight rows and x values).
+bool route_decode_fits(int64_t T, int64_t d, int64_t E) {
+    const int epc = route_cluster_epc(E);
+    if (epc > 0 && T * epc <= kClusterMaxAcc && route_cluster_smem(T, d, E, epc) <= kClusterMaxDynSmem) return true;
+    return route_decode_smem(T, d, route_decode_epl(E)) <= kRouteDecodeMaxSmem;
+}
+
 cudaError_t launch_route_decode(const void* x, int xt, const float* W, int64_t T, int64_t d, int64_t E, int k,
                                 int gwords, const Workspace& ws, cudaStream_t s) {
     const int epc = route_cluster_epc(E);
@@ -1270,12 +1288,13 @@ cudaError_t launch_route_decode(const void* x, int xt, const float* W, int64_t T
         }
     }
     // experts per lane: chunks narrow enough that the router weights spread over >= 128 CTAs
-    const int epl = (E <= 128) ? 1 : (E <= 512 ? 2 : 4);
+    const int epl = route_decode_epl(E);
     const dim3 grid(kResidues, static_cast<unsigned>((E + 32 * epl - 1) / (32 * epl)));
     const int Ti = static_cast<int>(T), di = static_cast<int>(d), Ei = static_cast<int>(E);
-    if (epl == 1) return launch_pdl(route_decode_kernel<1>, grid, dim3(256), 0, s, x, xt, W, Ti, di, Ei, k, gwords, ws);
-    if (epl == 2) return launch_pdl(route_decode_kernel<2>, grid, dim3(256), 0, s, x, xt, W, Ti, di, Ei, k, gwords, ws);
-    return launch_pdl(route_decode_kernel<4>, grid, dim3(256), 0, s, x, xt, W, Ti, di, Ei, k, gwords, ws);
+    const size_t smem = route_decode_smem(T, d, epl);
+    if (epl == 1) return launch_pdl(route_decode_kernel<1>, grid, dim3(256), smem, s, x, xt, W, Ti, di, Ei, k, gwords, ws);
+    if (epl == 2) return launch_pdl(route_decode_kernel<2>, grid, dim3(256), smem, s, x, xt, W, Ti, di, Ei, k, gwords, ws);
+    return launch_pdl(route_decode_kernel<4>, grid, dim3(256), smem, s, x, xt, W, Ti, di, Ei, k, gwords, ws);
 }
 
 }  // namespace moe
