@@ -738,12 +738,57 @@ __device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) { retu
 // Selection, weights and permutation from the logits slog[T][E] in shared memory (every
 // thread of the block): top-k with larger first and the lower index on ties, softmax over the
 // k selected logits, then the permutation by expert.
+// kWarpTopk: the warp-argmax top-k may be chosen (the partial-sum kernel's last CTA; the
+// cluster kernel keeps the smaller code of the ranking alone).
+template <bool kWarpTopk>
 __device__ __forceinline__ void route_select(const float* slog, int T, int E, int k, int gwords, const Workspace& ws) {
     // Top-k: expert e's slot is the number of experts that beat it -- the order repeated
     // selection would produce, computed for all (token, expert) at once.
     __shared__ int sidx[1024];
     __shared__ float stop[1024];
-    if (E <= kRankTopkMaxE && 2 * T * E <= static_cast<int>(blockDim.x) && E % 8 == 0) {
+    const int nwarps = static_cast<int>(blockDim.x) >> 5;
+    // (measured: a round of the warp argmax costs about a third of one rank item per thread at
+    // E = 128, so the warp path is taken when k rounds cost less than the ranking's share)
+    const int rank_items = (T * E + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+    if (kWarpTopk && E <= kRankTopkMaxE && E % 32 == 0 && 2 * T * E > static_cast<int>(blockDim.x) &&
+        T <= 4 * nwarps && 2 * 128 * k < 7 * rank_items * E) {
+        // one warp per token: k rounds of a warp-wide argmax (larger logit, then lower index),
+        // each round's winner taken out -- the order the ranks below give, in k * 5 shuffle steps
+        const int lane = threadIdx.x & 31;
+        const int per = E / 32;   // logits per lane: experts lane, lane + 32, ...
+        for (int t = threadIdx.x >> 5; t < T; t += nwarps) {
+            float v[kRankTopkMaxE / 32];
+            uint32_t taken = 0;
+#pragma unroll
+            for (int j = 0; j < kRankTopkMaxE / 32; ++j) v[j] = j < per ? slog[t * E + lane + 32 * j] : 0.0f;
+            for (int r = 0; r < k; ++r) {
+                float bv = -INFINITY;
+                int be = 0x7fffffff;
+#pragma unroll
+                for (int j = 0; j < kRankTopkMaxE / 32; ++j) {
+                    const int e = lane + 32 * j;
+                    if (j < per && !((taken >> j) & 1u) && (be == 0x7fffffff || beats(v[j], e, bv, be))) {
+                        bv = v[j];
+                        be = e;
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                    if (oe != 0x7fffffff && (be == 0x7fffffff || beats(ov, oe, bv, be))) {
+                        bv = ov;
+                        be = oe;
+                    }
+                }
+                if ((be & 31) == lane) taken |= 1u << (be >> 5);
+                if (lane == 0) {
+                    sidx[t * k + r] = be;
+                    stop[t * k + r] = bv;
+                }
+            }
+        }
+    } else if (E <= kRankTopkMaxE && 2 * T * E <= static_cast<int>(blockDim.x) && E % 8 == 0) {
         // two threads per (token, expert), each counting over half the experts
         const int it = threadIdx.x >> 1, half = threadIdx.x & 1;
         const bool live = it < T * E;
@@ -1000,7 +1045,7 @@ __global__ void __launch_bounds__(256) route_decode_kernel(const void* __restric
         }
     }
     __syncthreads();
-    route_select(slog, T, E, k, gwords, ws);
+    route_select<true>(slog, T, E, k, gwords, ws);
     if (threadIdx.x == 0) *ws.route_ctr = 0;
 }
 
@@ -1170,7 +1215,7 @@ __global__ void __launch_bounds__(256, 1) route_cluster_kernel(const void* __res
     if (g != 0) return;
     pdl_trigger();   // the expert kernel's launch overlaps the selection and permutation
     for (int it = l; it < T * E; it += blockDim.x) ws.logits[it] = slog[it];
-    route_select(slog, T, E, k, gwords, ws);
+    route_select<false>(slog, T, E, k, gwords, ws);
 }
 
 // Experts per CTA of the cluster kernel for E experts (0: not eligible).
