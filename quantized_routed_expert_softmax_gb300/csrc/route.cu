@@ -80,12 +80,36 @@ __device__ __forceinline__ void rt_cp16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Two fp32 fused multiply-adds in one instruction, each half rounded as fmaf:
+// acc.lo = fma(a.lo, b.lo, acc.lo), acc.hi = fma(a.hi, b.hi, acc.hi).
+__device__ __forceinline__ void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+// Two fp32 additions in one instruction, each half rounded as an fp32 add.
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
 // Many tokens, without block barriers in the main loop: warp w owns partial sums
 // l = 32w .. 32w+31 and stages its own 32-wide slices of x (8 tokens) and W (8 experts) through a
 // private cp.async ring, so a warp waits only for its own copies (__syncwarp).  The W rows of
 // a stage are stored with their two 16-byte halves swapped on every other group of 4 rows,
-// so that the 128-bit reads of 8 consecutive lanes hit all 32 banks.  The block's partials
-// then go through the same halving tree as the one-expert kernel above.
+// so that the 128-bit reads of 8 consecutive lanes hit all 32 banks.  The multiply-adds of an
+// expert pair go in one packed instruction (x broadcast to both halves, W rows read as pairs):
+// each half is the same fmaf step of its own chain.  The block's partials then go through the
+// same halving tree as the one-expert kernel above.
 template <bool XF32>
 __global__ void __launch_bounds__(256, 2) router_logits_warp_kernel(const void* __restrict__ x,
                                                                      const float* __restrict__ W, int T, int d,
@@ -95,6 +119,7 @@ __global__ void __launch_bounds__(256, 2) router_logits_warp_kernel(const void* 
     constexpr int kXStage = kRtT * 32 * kXB;              // x slice: [8 tokens][32]
     constexpr int kWStage = 32 * kRtE * 4;                // W slice: [32 rows][8 experts]
     constexpr int kStage = kXStage + kWStage;
+    constexpr int kXU = kXStage / 16 / 32;                // 16-byte x copies per lane and stage
     __shared__ __align__(16) unsigned char sm[8 * kStages * kStage];
     static_assert(8 * kStages * kStage >= 32 * kRouterPartials * 4, "tree buffer reuse");
     static_assert(8 * kStages * kStage <= 48 * 1024, "static shared memory");
@@ -106,82 +131,126 @@ __global__ void __launch_bounds__(256, 2) router_logits_warp_kernel(const void* 
     const int M = d / kRouterPartials;
     unsigned char* ring = sm + warp * kStages * kStage;
     const uint32_t rbase = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-    auto issue = [&](int m, int st) {
-        const uint32_t dst = rbase + st * kStage;
-        const int64_t col = static_cast<int64_t>(m) * kRouterPartials + warp * 32;   // first x column / W row
+    // this lane's copies of a step: their sources advance by 256 columns (x) or rows (W) a step
+    const unsigned char* xsrc[kXU];
+    uint32_t xdst[kXU];
 #pragma unroll
-        for (int u = 0; u < kXStage / 16 / 32; ++u) {    // x: per token kXB * 32 bytes
-            const int c = lane + 32 * u;
-            const int t = c / (kXB * 2), q = c % (kXB * 2);
-            const int tt = min(t0 + t, T - 1);
-            rt_cp16(dst + c * 16, static_cast<const unsigned char*>(x) + (static_cast<int64_t>(tt) * d + col) * kXB + q * 16);
+    for (int u = 0; u < kXU; ++u) {
+        const int c = lane + 32 * u;
+        const int t = c / (kXB * 2), q = c % (kXB * 2);
+        const int tt = min(t0 + t, T - 1);
+        xsrc[u] = static_cast<const unsigned char*>(x) + (static_cast<int64_t>(tt) * d + warp * 32) * kXB + q * 16;
+        xdst[u] = c * 16;
+    }
+    const float* wsrc[2];
+    uint32_t wdst[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {                        // W: 32 rows x 2 halves
+        const int c = lane + 32 * u;
+        const int r = c >> 1, h = c & 1;
+        const int hs = h ^ ((r >> 2) & 1);
+        wsrc[u] = W + static_cast<int64_t>(warp * 32 + r) * E + e0 + 4 * h;
+        wdst[u] = kXStage + (2 * r + hs) * 16;
+    }
+    const int64_t wstep = static_cast<int64_t>(kRouterPartials) * E;
+    auto issue = [&](int st) {   // the next step's slices into stage st
+        const uint32_t dst = rbase + st * kStage;
+#pragma unroll
+        for (int u = 0; u < kXU; ++u) {
+            rt_cp16(dst + xdst[u], xsrc[u]);
+            xsrc[u] += kRouterPartials * kXB;
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {                    // W: 32 rows x 2 halves
-            const int c = lane + 32 * u;
-            const int r = c >> 1, h = c & 1;
-            const int hs = h ^ ((r >> 2) & 1);
-            rt_cp16(dst + kXStage + (2 * r + hs) * 16, W + (col + r) * E + e0 + 4 * h);
+        for (int u = 0; u < 2; ++u) {
+            rt_cp16(dst + wdst[u], wsrc[u]);
+            wsrc[u] += wstep;
         }
     };
 #pragma unroll
     for (int st = 0; st < kStages; ++st) {
-        if (st < M) issue(st, st);
+        if (st < M) issue(st);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    float acc[kRtT * kRtE];
+    uint64_t acc[kRtT][kRtE / 2];   // (expert 2p, expert 2p + 1) of token t
 #pragma unroll
-    for (int v = 0; v < kRtT * kRtE; ++v) acc[v] = 0.0f;
+    for (int t = 0; t < kRtT; ++t)
+#pragma unroll
+        for (int p = 0; p < kRtE / 2; ++p) acc[t][p] = 0;
     const int sw = (lane >> 2) & 1;
-    for (int m = 0; m < M; ++m) {
-        const int st = m % kStages;
-        asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
-        __syncwarp();
-        const unsigned char* xs = ring + st * kStage;
-        const float4* wr = reinterpret_cast<const float4*>(ring + st * kStage + kXStage) + 2 * lane;
-        const float4 wa = wr[sw], wb = wr[sw ^ 1];
-        const float wv[kRtE] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    for (int m0 = 0; m0 < M; m0 += kStages) {
 #pragma unroll
-        for (int t = 0; t < kRtT; ++t) {
-            float xv;
-            if (XF32) xv = reinterpret_cast<const float*>(xs)[t * 32 + lane];
-            else xv = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xs)[t * 32 + lane]);
+        for (int st = 0; st < kStages; ++st) {
+            const int m = m0 + st;
+            if (m < M) {
+                asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+                __syncwarp();
+                const unsigned char* xs = ring + st * kStage;
+                const ulonglong2* wr = reinterpret_cast<const ulonglong2*>(ring + st * kStage + kXStage) + 2 * lane;
+                const ulonglong2 wa = wr[sw], wb = wr[sw ^ 1];
+                const uint64_t wp[kRtE / 2] = {wa.x, wa.y, wb.x, wb.y};
 #pragma unroll
-            for (int c = 0; c < kRtE; ++c) acc[t * kRtE + c] = fmaf(xv, wv[c], acc[t * kRtE + c]);
+                for (int t = 0; t < kRtT; ++t) {
+                    float xv;
+                    if (XF32) xv = reinterpret_cast<const float*>(xs)[t * 32 + lane];
+                    else xv = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xs)[t * 32 + lane]);
+                    const uint64_t xx = pack_f32x2(xv, xv);
+#pragma unroll
+                    for (int p = 0; p < kRtE / 2; ++p) fma_f32x2(acc[t][p], xx, wp[p]);
+                }
+                __syncwarp();   // every lane is done with the stage before it is refilled
+                if (m + kStages < M) issue(st);
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            }
         }
-        __syncwarp();   // every lane is done with the stage before it is refilled
-        if (m + kStages < M) issue(m + kStages, st);
-        asm volatile("cp.async.commit_group;" ::: "memory");
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    // The tree: all 256 partials of 32 logits at a time in shared memory, then warp w takes
-    // logits 4w .. 4w+3 of the pass: lane j holds partials j + 32 q (q = 0..7), so levels 128,
-    // 64 and 32 are additions in registers and levels 16 .. 1 shuffles (lane j adds lane j + h),
-    // the same pairs s_l += s_{l+h} in the same order.
+    // The tree, 32 logits (4 tokens x 8 experts) a pass: thread l stores its 32 partials as 8
+    // chunks of 4 logits, chunk u at position u ^ (l & 7) of its 32-float row (16-byte stores
+    // and loads without bank conflicts).  Warp w then takes chunk w: lane j loads partials
+    // j + 32q (q = 0..7) of its 4 logits, adds levels 128, 64 and 32 in registers (two logits
+    // per packed add) and 16 .. 1 with shuffles (lane j adds lane j + h): the same pairs
+    // s_l += s_{l+h} in the same order.
     constexpr int kPass = 32;
-    float (*red)[kRouterPartials] = reinterpret_cast<float (*)[kRouterPartials]>(sm);
+    float* red = reinterpret_cast<float*>(sm);   // [256 partials][32 logits], chunks swizzled
 #pragma unroll
     for (int pass = 0; pass < kRtT * kRtE / kPass; ++pass) {
 #pragma unroll
-        for (int v = 0; v < kPass; ++v) red[v][l] = acc[pass * kPass + v];
+        for (int u = 0; u < kPass / 4; ++u) {   // logits 4u .. 4u+3 of the pass: token t, experts 4(u&1)..
+            const int t = pass * (kPass / kRtE) + (u >> 1), p = 2 * (u & 1);
+            const float2 a = unpack_f32x2(acc[t][p]), b = unpack_f32x2(acc[t][p + 1]);
+            *reinterpret_cast<float4*>(red + l * kPass + 4 * (u ^ (l & 7))) = make_float4(a.x, a.y, b.x, b.y);
+        }
         __syncthreads();
+        uint64_t sq[8][2];   // partial j + 32q: logits (0, 1) and (2, 3) of the warp's chunk
 #pragma unroll
-        for (int u = 0; u < kPass / 8; ++u) {
-            const int v = warp * (kPass / 8) + u;
-            float sq[8];
+        for (int q = 0; q < 8; ++q) {
+            const int pl = lane + 32 * q;
+            const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(red + pl * kPass + 4 * (warp ^ (pl & 7)));
+            sq[q][0] = v.x;
+            sq[q][1] = v.y;
+        }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) sq[q] = red[v][lane + 32 * q];
+        for (int i = 0; i < 2; ++i) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) sq[q] = sq[q] + sq[q + 4];   // h = 128
-            sq[0] = sq[0] + sq[2];                                    // h = 64
-            sq[1] = sq[1] + sq[3];
-            float sv = sq[0] + sq[1];                                 // h = 32
+            for (int q = 0; q < 4; ++q) sq[q][i] = add_f32x2(sq[q][i], sq[q + 4][i]);   // h = 128
+            sq[0][i] = add_f32x2(sq[0][i], sq[2][i]);                                    // h = 64
+            sq[1][i] = add_f32x2(sq[1][i], sq[3][i]);
+            sq[0][i] = add_f32x2(sq[0][i], sq[1][i]);                                    // h = 32
 #pragma unroll
-            for (int h = 16; h >= 1; h >>= 1) sv = sv + __shfl_down_sync(0xffffffffu, sv, h);
-            const int vv = pass * kPass + v;
-            const int t = vv / kRtE;
-            if (lane == 0 && t < nt) logits[static_cast<int64_t>(t0 + t) * E + e0 + (vv % kRtE)] = sv;
+            for (int h = 16; h >= 1; h >>= 1) {
+                const uint64_t o = __shfl_down_sync(0xffffffffu, sq[0][i], h);
+                sq[0][i] = add_f32x2(sq[0][i], o);
+            }
+        }
+        const int t = pass * (kPass / kRtE) + (warp >> 1);
+        if (lane == 0 && t < nt) {
+            const float2 a = unpack_f32x2(sq[0][0]), b = unpack_f32x2(sq[0][1]);
+            float* o = logits + static_cast<int64_t>(t0 + t) * E + e0 + 4 * (warp & 1);
+            o[0] = a.x;
+            o[1] = a.y;
+            o[2] = b.x;
+            o[3] = b.y;
         }
         __syncthreads();
     }
