@@ -817,21 +817,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                         acc_item = it;
                     }
                     const float* hv = hf + (it / nrt - h_s0) * f + 16 * g;
-                    float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    uint64_t part[4] = {0, 0, 0, 0};   // rows (2by, 2by+1): one packed fmaf pair per code byte
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float h = hv[j];
+                        const uint64_t hh = pack_f32x2(h, h);
 #pragma unroll
                         for (int by = 0; by < 4; ++by) {
                             const float2 v = e2m1x2_to_f32x2((cw[j] >> (8 * by)) & 0xffu);   // rows 2by, 2by+1
-                            part[2 * by] = fmaf(v.x, h, part[2 * by]);
-                            part[2 * by + 1] = fmaf(v.y, h, part[2 * by + 1]);
+                            fma_f32x2(part[by], pack_f32x2(v.x, v.y), hh);
                         }
                     }
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const float sb = e4m3_to_f32(((r < 4 ? sc.x : sc.y) >> (8 * (r & 3))) & 0xffu);
-                        acc[r] = fmaf(sb, part[r], acc[r]);
+                    for (int by = 0; by < 4; ++by) {
+                        const float2 pv = unpack_f32x2(part[by]);
+                        const uint32_t sw = by < 2 ? sc.x : sc.y;
+                        const int r = 2 * by;
+                        acc[r] = fmaf(e4m3_to_f32((sw >> (8 * (r & 3))) & 0xffu), pv.x, acc[r]);
+                        acc[r + 1] = fmaf(e4m3_to_f32((sw >> (8 * ((r + 1) & 3))) & 0xffu), pv.y, acc[r + 1]);
                     }
                 };
                 uint32_t cw0[16], cw1[16];

@@ -85,7 +85,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAColsPerStage = 64;
 
 constexpr int kWarpLoadA = 0, kWarpLoadB = 1, kWarpMma = 2, kWarpEpi0 = 4, kWarpConv0 = 8;
-constexpr int kConvWarps = 16, kConvThreads = kConvWarps * 32;
+constexpr int kConvWarps = 16;
 
 // ------------------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t s_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -513,7 +513,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
     const uint32_t tmem = tmem_base;
     const int total = tile_prefix[g.slot_cap];
     const int ksteps = ((KIND == kGateUp) ? a.d : a.f) / kStepK;
-    const int rows_w = (KIND == kGateUp) ? a.rows_gu : a.d;
     // a_stages (2 or 4) and acc_bufs (1 or 2) are powers of two: shifts and masks
     const uint32_t a_shift = (g.a_stages == 4) ? 2u : 1u, a_mask = (1u << a_shift) - 1u;
     const uint32_t b_shift = (g.acc_bufs == 2) ? 1u : 0u, b_mask = (1u << b_shift) - 1u;

@@ -582,31 +582,35 @@ __device__ __forceinline__ void dn_nv_tile(const ExpertArgs& a, const uint8_t* W
 #pragma unroll
         for (int u = 0; u < kGif; ++u) {
             if (u < n) {
-                float part[N][8];
+                uint64_t part[N][4];   // rows (2by, 2by+1): one packed fmaf pair per code byte and token
 #pragma unroll
                 for (int t = 0; t < N; ++t)
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) part[t][r] = 0.0f;
+                    for (int by = 0; by < 4; ++by) part[t][by] = 0;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    float hv[N];
+                    uint64_t hh[N];
 #pragma unroll
-                    for (int t = 0; t < N; ++t) hv[t] = hs[t * f + 16 * gid[u] + j];
+                    for (int t = 0; t < N; ++t) {
+                        const float hv = hs[t * f + 16 * gid[u] + j];
+                        hh[t] = pack_f32x2(hv, hv);
+                    }
 #pragma unroll
                     for (int by = 0; by < 4; ++by) {
                         const float2 v = e2m1x2_to_f32x2((codes[u][j] >> (8 * by)) & 0xffu);   // rows 2by, 2by+1
+                        const uint64_t vv = pack_f32x2(v.x, v.y);
 #pragma unroll
-                        for (int t = 0; t < N; ++t) {
-                            part[t][2 * by] = fmaf(v.x, hv[t], part[t][2 * by]);
-                            part[t][2 * by + 1] = fmaf(v.y, hv[t], part[t][2 * by + 1]);
-                        }
+                        for (int t = 0; t < N; ++t) fma_f32x2(part[t][by], vv, hh[t]);
                     }
                 }
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const float sb = e4m3_to_f32(((r < 4 ? sc[u].x : sc[u].y) >> (8 * (r & 3))) & 0xffu);
 #pragma unroll
-                    for (int t = 0; t < N; ++t) acc[t][r] = fmaf(sb, part[t][r], acc[t][r]);
+                    for (int t = 0; t < N; ++t) {
+                        const float2 pv = unpack_f32x2(part[t][r >> 1]);
+                        acc[t][r] = fmaf(sb, (r & 1) ? pv.y : pv.x, acc[t][r]);
+                    }
                 }
             }
         }
