@@ -145,7 +145,7 @@ int64_t cta_max_items(int64_t U, int64_t W, int64_t npan) {
 // tile, 16-neuron group).
 DecodeSplit decode_split(const moe_layer_desc* d, int64_t ctas) {
     DecodeSplit sp{};
-    const bool q8 = d->wfmt == MOE_W_Q8_0;
+    const bool q8 = d->wfmt != MOE_W_NVFP4;   // 32-column int8 panels (Q8_0, per-channel int8)
     sp.npan_g = q8 ? d->d / 32 : d->d / 64;
     sp.npan_d = q8 ? d->f / 32 : d->f / 16;
     const int64_t items_g = static_cast<int64_t>(d->k) * (d->act == MOE_ACT_SWIGLU ? d->f / 16 : d->f / 32);
@@ -166,12 +166,12 @@ DecodeSplit decode_split(const moe_layer_desc* d, int64_t ctas) {
     return sp;
 }
 
-// The one-kernel decode layer's shape limits (any device): one token, Q8_0 SwiGLU or NVFP4
-// (ReLU^2 or SwiGLU), the router-weight slice of a routing CTA and x within its shared memory, and 32-bit
+// The one-kernel decode layer's shape limits (any device): one token, Q8_0 or per-channel int8
+// SwiGLU, or NVFP4 (ReLU^2 or SwiGLU), the router-weight slice of a routing CTA and x within its shared memory, and 32-bit
 // unit arithmetic.
 bool decode_shape_ok(const moe_layer_desc* d, int64_t T, int xt) {
     if (T != 1 || d->path != MOE_PATH_AUTO) return false;
-    const bool q8 = d->wfmt == MOE_W_Q8_0 && d->act == MOE_ACT_SWIGLU;
+    const bool q8 = (d->wfmt == MOE_W_Q8_0 || d->wfmt == MOE_W_INT8PC) && d->act == MOE_ACT_SWIGLU;
     const bool nv = d->wfmt == MOE_W_NVFP4;   // ReLU^2 (latent experts) or SwiGLU
     if (!q8 && !nv) return false;
     if (d->d > 8192 || d->f % 32 != 0) return false;
@@ -437,13 +437,8 @@ bool fill_decode_args(const moe_layer_desc* descs, int n, const void* x, int xt,
     a->cta_items = static_cast<int>(sp.cta_items);
     a->cta_items_d = static_cast<int>(sp.cta_items_d);
     const int64_t rows_gu = desc->act == MOE_ACT_SWIGLU ? 2 * desc->f : desc->f;
-    if (desc->wfmt == MOE_W_Q8_0) {
-        a->gu_bytes = static_cast<int64_t>(moe_q8_0_bytes(rows_gu, desc->d));
-        a->dn_bytes = static_cast<int64_t>(moe_q8_0_bytes(desc->d, desc->f));
-    } else {
-        a->gu_bytes = static_cast<int64_t>(moe_nvfp4_bytes(rows_gu, desc->d));
-        a->dn_bytes = static_cast<int64_t>(moe_nvfp4_bytes(desc->d, desc->f));
-    }
+    a->gu_bytes = matrix_bytes(desc->wfmt, rows_gu, desc->d);
+    a->dn_bytes = matrix_bytes(desc->wfmt, desc->d, desc->f);
     *smem_out = decode_smem_plan(desc->wfmt, a->d, a->f, a->k, xt, a->cta_items, static_cast<int>(sp.cta_slots),
                                  &a->off_c, &a->off_p);
     a->n_layers = n;

@@ -5,8 +5,8 @@
 // gate.up with the activation, down projection, fixed-order combine), for the case that
 // decides decode speed: one token, where the layer moves only the routed experts' weights
 // (a few tens of MB) and the separate launches' start-up, ramp and tail cost more than the
-// bytes.  Two expert formats: Q8_0 with SwiGLU, and NVFP4 with ReLU^2 (gateless latent
-// experts).  Sources of the computation:
+// bytes.  Expert formats: Q8_0 or per-channel int8 with SwiGLU, and NVFP4 with ReLU^2
+// (gateless latent experts) or SwiGLU.  Sources of the computation:
 //   router / top-k / softmax: "Squeezing a 26B MoE onto the cheapest Inferentia instance"
 //     (128 experts, top-8 per token), with the canonical fp32 summation order of the oracle;
 //   gate.up + SwiGLU: "Running Gemma 4 26B at 5 tokens/s on a 13-year-old Xeon", sections
@@ -180,7 +180,7 @@ __device__ __forceinline__ WarpRange warp_range(uint32_t U, uint32_t W, uint32_t
 //   P    : the per-warp gate.up partials of the CTA's items [cta_items][16 warps][32]
 size_t decode_smem_plan(int wfmt, int d, int f, int k, int xt, int cta_items, int cta_slots, int* off_c, int* off_p) {
     const size_t xb = static_cast<size_t>(d) * 4;
-    const size_t hb = (wfmt == MOE_W_Q8_0) ? static_cast<size_t>(k) * f * 4 : static_cast<size_t>(cta_slots) * f * 4;
+    const size_t hb = (wfmt != MOE_W_NVFP4) ? static_cast<size_t>(k) * f * 4 : static_cast<size_t>(cta_slots) * f * 4;
     const size_t b = xb > hb ? xb : hb;
     const size_t cbytes = static_cast<size_t>(d) * 2 * (xt == MOE_F32 ? 2 : 1);
     const size_t pb = static_cast<size_t>(cta_items) * kDecWarps * 32 * sizeof(float);
@@ -193,8 +193,9 @@ size_t decode_ring_bytes() { return kRingBytes; }
 
 template <int FMT, int ACT, int ROUTE>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs a) {
-    // Q8_0 with SwiGLU, or NVFP4 with ReLU^2 (gateless latent experts)
-    constexpr bool kQ8 = FMT == MOE_W_Q8_0;
+    // Q8_0 or per-channel int8 with SwiGLU (32-column int8 panels with block or row scales),
+    // or NVFP4 with ReLU^2 (gateless latent experts) or SwiGLU
+    constexpr bool kQ8 = FMT == MOE_W_Q8_0 || FMT == MOE_W_INT8PC;
     constexpr bool kSupplied = ROUTE == kRouteSupplied;
     constexpr bool kSwiglu = ACT == MOE_ACT_SWIGLU;
     constexpr int kNeur = kSwiglu ? 16 : 32;   // neurons per gate.up item (16 gate + 16 up rows, or 32 rows)
@@ -460,7 +461,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         int dss = rd.item0 / nrt, dsrt = rd.item0 % nrt, dsb = rd.b0;
         const uint8_t* dsw = P.w_dn + static_cast<int64_t>(s_e[dss < k ? dss : 0]) * a.dn_bytes;
         auto issue_d = [&](int st) {
-            issue_panel_block<MOE_W_Q8_0>(dring_addr + st * kSlotBytes, dsw, d, dsrt * 32, dsrt * 32 + 16, dsb, pol, 0);
+            issue_panel_block<FMT>(dring_addr + st * kSlotBytes, dsw, d, dsrt * 32, dsrt * 32 + 16, dsb, pol, 0);
             if (++dsb == npan_d) {
                 dsb = 0;
                 if (++dsrt == nrt) {
@@ -629,7 +630,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                         if (i < n) {
                             cp_async_wait<kStages - 1>();
                             __syncwarp();
-                            panel_mma<MOE_W_Q8_0>(dring + st * kSlotBytes, hs + cur_s * f, f, cur_b, 1, 0, acc, true, kf);
+                            panel_mma<FMT>(dring + st * kSlotBytes, hs + cur_s * f, f, cur_b, 1, 0, acc, true, kf);
                             __syncwarp();   // every lane is done with the slot before it is refilled
                             if (i + kStages < n) issue_d(st);
                             cp_async_commit();
@@ -984,6 +985,9 @@ cudaError_t configure_decode_kernel(int dev, int num_sms) {
     if (!configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteLocal>() ||
         !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteWide>() ||
         !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteSupplied>() ||
+        !configure_one<MOE_W_INT8PC, MOE_ACT_SWIGLU, kRouteLocal>() ||
+        !configure_one<MOE_W_INT8PC, MOE_ACT_SWIGLU, kRouteWide>() ||
+        !configure_one<MOE_W_INT8PC, MOE_ACT_SWIGLU, kRouteSupplied>() ||
         !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteLocal>() ||
         !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteWide>() ||
         !configure_one<MOE_W_NVFP4, MOE_ACT_RELU2, kRouteSupplied>() ||
@@ -1023,6 +1027,7 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, int wfmt, int act, size_t s
     cfg.numAttrs = 2;
     const int route = a.idx_in ? kRouteSupplied : (a.E > kLocalRankMaxE ? kRouteWide : kRouteLocal);
     if (wfmt == MOE_W_Q8_0) return launch_decode_route<MOE_W_Q8_0, MOE_ACT_SWIGLU>(cfg, a, route);
+    if (wfmt == MOE_W_INT8PC) return launch_decode_route<MOE_W_INT8PC, MOE_ACT_SWIGLU>(cfg, a, route);
     if (act == MOE_ACT_SWIGLU) return launch_decode_route<MOE_W_NVFP4, MOE_ACT_SWIGLU>(cfg, a, route);
     return launch_decode_route<MOE_W_NVFP4, MOE_ACT_RELU2>(cfg, a, route);
 }

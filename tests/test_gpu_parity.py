@@ -256,6 +256,13 @@ ONE_KERNEL = {
                                    x_dtype="bf16", layers=1),
     "nv_swiglu_k8_f32": synth.Workload("ok_nvsw8", d=1024, f=192, E=64, k=8, act="swiglu", wfmt="nvfp4",
                                        x_dtype="f32", layers=1),
+    # per-channel int8 SwiGLU (the Q8_0 panels with one fp32 scale per row)
+    "pc_k8_e64": synth.Workload("ok_pc8", d=1024, f=192, E=64, k=8, act="swiglu", wfmt="int8pc", x_dtype="bf16",
+                                layers=1),
+    "pc_k3_e12_f32": synth.Workload("ok_pc3", d=768, f=96, E=12, k=3, act="swiglu", wfmt="int8pc", x_dtype="f32",
+                                    layers=1),
+    "pc_k22_e512": synth.Workload("ok_pc22", d=256, f=64, E=512, k=22, act="swiglu", wfmt="int8pc",
+                                  x_dtype="bf16", layers=1),
 }
 
 
@@ -293,7 +300,7 @@ def test_one_token_one_kernel(name):
 # trace copies idx and w exactly; the permutation follows them bit for bit; h and out agree
 # with the oracle and with the separate kernels on the same routing.
 @pytest.mark.parametrize("name", ["tiny_f32", "k1", "k8_e64", "k32_e1024", "nv_k6_e32", "nv_k22_e512_f32",
-                                  "nv_swiglu_k4"])
+                                  "nv_swiglu_k4", "pc_k8_e64"])
 def test_one_token_one_kernel_supplied_routing(name):
     w = ONE_KERNEL[name]
     idx, wts = synth.zipf_routing(1, w.E, w.k, seed_tag="one-kernel")
@@ -611,6 +618,8 @@ STACKS = {
                                 layers=3, zero_fraction=0.925), 3),
     "nv_swiglu": (synth.Workload("st_nvsw", d=768, f=256, E=32, k=8, act="swiglu", wfmt="nvfp4",
                                  x_dtype="bf16", layers=3), 3),
+    "int8pc": (synth.Workload("st_pc", d=1024, f=192, E=64, k=8, act="swiglu", wfmt="int8pc", x_dtype="bf16",
+                              layers=3), 3),
 }
 
 
