@@ -169,6 +169,10 @@ DecodeSplit decode_split(const moe_layer_desc* d, int64_t ctas) {
 // The one-kernel decode layer's shape limits (any device): one token, Q8_0 or per-channel int8
 // SwiGLU, or NVFP4 (ReLU^2 or SwiGLU), the router-weight slice of a routing CTA and x within its shared memory, and 32-bit
 // unit arithmetic.
+// The input type the one-kernel layer's shared-memory plan takes: coded activations (Q8_0
+// values need about 19 significant bits) travel as two f16 planes, like an fp32 input.
+int decode_xt(const moe_layer_desc* d, int xt) { return d->act_quant == MOE_ACTQ_Q8_0 ? MOE_F32 : xt; }
+
 bool decode_shape_ok(const moe_layer_desc* d, int64_t T, int xt) {
     if (T != 1 || d->path != MOE_PATH_AUTO) return false;
     const bool q8 = (d->wfmt == MOE_W_Q8_0 || d->wfmt == MOE_W_INT8PC) && d->act == MOE_ACT_SWIGLU;
@@ -258,7 +262,10 @@ Plan make_plan(const moe_layer_desc* d, int64_t T, int xt = MOE_BF16) {
         while (tt < 32 && tt < T && down_nv_mma_smem(2 * tt, static_cast<int>(d->f)) <= kNvMmaSmem) tt *= 2;
         p.tt_dn = tt;
     }
-    p.decode1 = !p.gemm && d->act_quant == MOE_ACTQ_NONE && decode_shape_ok(d, T, xt);
+    // (coded activations: Q8_0 SwiGLU, with x carried as two f16 planes like an fp32 input)
+    p.decode1 = !p.gemm &&
+                (d->act_quant == MOE_ACTQ_NONE || (d->wfmt == MOE_W_Q8_0 && d->act == MOE_ACT_SWIGLU)) &&
+                decode_shape_ok(d, T, decode_xt(d, xt));
     return p;
 }
 
@@ -415,11 +422,15 @@ bool fill_decode_args(const moe_layer_desc* descs, int n, const void* x, int xt,
     const int ctas = decode_ctas(dev);
     const int epc = decode_epc(desc->E, ctas);
     const DecodeSplit sp = decode_split(desc, std::max(1, ctas));
-    if (ctas <= 0 || epc <= 0 || !decode_split_fits(desc, sp, xt)) return false;
+    const int xt_planes = decode_xt(desc, xt);   // the shared-memory plan's input type: fp32 = two f16 planes
+    if (ctas <= 0 || epc <= 0 || !decode_split_fits(desc, sp, xt_planes)) return false;
+    for (int l = 1; l < n; ++l)   // one kernel serves the stack only if every layer codes (or not) and reads alike
+        if (descs[l].act_quant != desc->act_quant || descs[l].flags != desc->flags) return false;
     char* base = static_cast<char*>(workspace);
     *a = DecodeArgs{};
     a->x = x;
     a->xt = xt;
+    a->act_q = desc->act_quant == MOE_ACTQ_Q8_0 ? 1 : 0;
     a->d = static_cast<int>(desc->d);
     a->f = static_cast<int>(desc->f);
     a->E = static_cast<int>(desc->E);
@@ -439,7 +450,7 @@ bool fill_decode_args(const moe_layer_desc* descs, int n, const void* x, int xt,
     const int64_t rows_gu = desc->act == MOE_ACT_SWIGLU ? 2 * desc->f : desc->f;
     a->gu_bytes = matrix_bytes(desc->wfmt, rows_gu, desc->d);
     a->dn_bytes = matrix_bytes(desc->wfmt, desc->d, desc->f);
-    *smem_out = decode_smem_plan(desc->wfmt, a->d, a->f, a->k, xt, a->cta_items, static_cast<int>(sp.cta_slots),
+    *smem_out = decode_smem_plan(desc->wfmt, a->d, a->f, a->k, xt_planes, a->cta_items, static_cast<int>(sp.cta_slots),
                                  &a->off_c, &a->off_p);
     a->n_layers = n;
     for (int l = 0; l < n; ++l) {
@@ -756,7 +767,7 @@ int32_t moe_layer_forward_launches(const moe_layer_desc* desc, int64_t T, int32_
         int num_sms = 0, dev = 0;
         if (ensure_configured(&num_sms) == cudaSuccess && cudaGetDevice(&dev) == cudaSuccess &&
             decode_epc(desc->E, decode_ctas(dev)) > 0 &&
-            decode_split_fits(desc, decode_split(desc, std::max(1, decode_ctas(dev))), MOE_BF16))
+            decode_split_fits(desc, decode_split(desc, std::max(1, decode_ctas(dev))), decode_xt(desc, MOE_BF16)))
             return 1;
     }
     int n = 0;
@@ -841,9 +852,14 @@ moe_status moe_stack_forward(const moe_layer_desc* descs, int32_t n_layers, cons
 
 int32_t moe_stack_forward_launches(const moe_layer_desc* descs, int32_t n_layers, int32_t with_x_next) {
     if (validate_stack(descs, n_layers) != MOE_OK) return -1;
-    int32_t one = moe_layer_forward_launches(descs, 1, 0);
-    if (one == 1 && n_layers <= kMaxStackLayers) return 1;
-    return n_layers * (one + 1) - (with_x_next ? 0 : 1);
+    bool uniform = true;   // (the one-kernel stack needs every layer to code, and read its weights, alike)
+    for (int32_t l = 1; l < n_layers; ++l)
+        uniform = uniform && descs[l].act_quant == descs[0].act_quant && descs[l].flags == descs[0].flags;
+    const int32_t one = moe_layer_forward_launches(descs, 1, 0);
+    if (one == 1 && uniform && n_layers <= kMaxStackLayers) return 1;
+    int32_t n = 0;   // layer by layer, the RMS-norm after each
+    for (int32_t l = 0; l < n_layers; ++l) n += moe_layer_forward_launches(descs + l, 1, 0) + 1;
+    return n - (with_x_next ? 0 : 1);
 }
 
 moe_status moe_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uint16_t* xo, moe_stream_t stream) {

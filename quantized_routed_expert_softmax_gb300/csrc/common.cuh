@@ -130,6 +130,7 @@ struct DecodeArgs {
     // last, so that the offsets of the fields above (and the routed kernels' code) stay as they were
     const int32_t* idx_in;       // supplied routing [k] and weights [k] (one layer), or null: routed here
     const float* w_in;
+    int act_q;                   // 1: the experts read Q8_0-coded x and h (the AQ instantiation; host-side dispatch)
 };
 
 // Programmatic dependent launch: wait for the preceding kernel's memory, and allow the
@@ -203,6 +204,16 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// The Q8_0 activation coder for one value of a block of 32 whose largest magnitude is amax:
+// d = amax / 127, the code round(x * (1 / d)) (both correctly rounded, as the weight packer),
+// and the value the code stands for, q * fp16(d), which is exact in fp32.
+__device__ __forceinline__ float q8_0_coded_value(float x, float amax) {
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+    const int q = static_cast<int>(roundf(__fmul_rn(x, id)));
+    return static_cast<float>(q) * __half2float(__float2half_rn(d));
+}
 
 // Two fp32 fused multiply-adds in one instruction, each half rounded as fmaf:
 // acc.lo = fma(a.lo, b.lo, acc.lo), acc.hi = fma(a.hi, b.hi, acc.hi).

@@ -191,11 +191,14 @@ size_t decode_smem_plan(int wfmt, int d, int f, int k, int xt, int cta_items, in
 
 size_t decode_ring_bytes() { return kRingBytes; }
 
-template <int FMT, int ACT, int ROUTE>
+template <int FMT, int ACT, int ROUTE, bool AQ>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs a) {
     // Q8_0 or per-channel int8 with SwiGLU (32-column int8 panels with block or row scales),
     // or NVFP4 with ReLU^2 (gateless latent experts) or SwiGLU
     constexpr bool kQ8 = FMT == MOE_W_Q8_0 || FMT == MOE_W_INT8PC;
+    // AQ (Q8_0 only): the experts read x and h through the Q8_0 activation coder (blocks of 32,
+    // the values the codes stand for, carried as f16 hi + lo); the router reads x as it is
+    static_assert(!AQ || (FMT == MOE_W_Q8_0 && ACT == MOE_ACT_SWIGLU), "coded activations: Q8_0 SwiGLU");
     constexpr bool kSupplied = ROUTE == kRouteSupplied;
     constexpr bool kSwiglu = ACT == MOE_ACT_SWIGLU;
     constexpr int kNeur = kSwiglu ? 16 : 32;   // neurons per gate.up item (16 gate + 16 up rows, or 32 rows)
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     // immediate shared-memory addresses, measurably faster than a base passed in the arguments
     float* xf = reinterpret_cast<float*>(dsm + kRingBytes);
     __half* xh = reinterpret_cast<__half*>(dsm + a.off_c);
-    const bool split = a.xt == MOE_F32;
+    const bool split = a.xt == MOE_F32 || AQ;   // x for the experts as f16 hi + lo (fp32 input, or coded)
     // the two streaming phases: items, panels per item, units
     // gate.up: items (slot, tile of kNeur neurons), panels of 32 (Q8_0) or 64 (NVFP4) columns
     const int nt_g = f / kNeur, npan_g = kQ8 ? d / 32 : d / 64;
@@ -251,9 +254,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     };
     request_router(a.lp[0].W);   // does not depend on the previous kernel: before waiting for it
     pdl_wait();
-    for (int i = tid; i < d / 4; i += kDecThreads) {
+    for (int i = tid; i < d / 4; i += kDecThreads) {   // (whole warps: d / 4 is a multiple of 64)
         float4 v;
-        if (split) {
+        if (AQ ? a.xt == MOE_F32 : split) {   // (split: an fp32 input, unless coded)
             v = __ldcg(reinterpret_cast<const float4*>(a.x) + i);
         } else {
             const uint2 b = __ldcg(reinterpret_cast<const uint2*>(a.x) + i);
@@ -261,6 +264,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                             __uint_as_float(b.y & 0xffff0000u));
         }
         reinterpret_cast<float4*>(xf)[i] = v;
+        if constexpr (AQ) {   // the experts' x: each block of 32 (8 threads) through the coder
+            uint32_t mb = max(max(__float_as_uint(fabsf(v.x)), __float_as_uint(fabsf(v.y))),
+                              max(__float_as_uint(fabsf(v.z)), __float_as_uint(fabsf(v.w))));
+#pragma unroll
+            for (int m = 1; m < 8; m <<= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, m));
+            const float amax = __uint_as_float(mb);
+            v = make_float4(q8_0_coded_value(v.x, amax), q8_0_coded_value(v.y, amax), q8_0_coded_value(v.z, amax),
+                            q8_0_coded_value(v.w, amax));
+        }
         __half2 h01, h23, l01, l23;
         split_f16(v.x, v.y, h01, l01);
         split_f16(v.z, v.w, h23, l23);
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     int nbar = 0;   // grid barriers passed (the counter target of the next is (nbar + 1) * G)
     for (int l = 0; l < a.n_layers; ++l) {
         const DecodeLayerPtrs P = a.lp[l];
-        const bool split_l = l == 0 && split;   // later layers read bf16 inputs: one f16 term
+        const bool split_l = (l == 0 && split) || AQ;   // later layers read bf16 inputs: one f16 term, unless coded
         cp_async_wait<0>();
         __syncthreads();
         if (!kSupplied && router) {
@@ -606,7 +618,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
                             zg += __ldcg(rec + cc * 32);
                             zu += __ldcg(rec + cc * 32 + 16);
                         }
-                        const float h = silu(zg) * zu;
+                        float h = silu(zg) * zu;
+                        if constexpr (AQ) {   // the down projection's input through the coder (a warp: one block of 32)
+                            const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
+                            h = q8_0_coded_value(h, amax);
+                        }
                         const __half hi = __float2half_rn(h);
                         hs[q] = hi;
                         hs[kf + q] = __float2half_rn(h - __half2float(hi));
@@ -931,11 +947,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
 #pragma unroll
             for (int i = 0; i < 8; ++i) tot += wsum[i];
             const float inv = rsqrtf(tot / static_cast<float>(d) + a.eps);
-            for (int i = tid; i < d; i += kDecThreads) {
+            for (int i = tid; i < d; i += kDecThreads) {   // (whole warps: d is a multiple of 256)
                 const __nv_bfloat16 xb = __float2bfloat16_rn(xf[i] * inv);
                 const float xv = __bfloat162float(xb);
                 xf[i] = xv;
-                xh[i] = __float2half_rn(xv);
+                if constexpr (AQ) {   // the experts' x through the coder (a warp: one block of 32), hi + lo
+                    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(xv))));
+                    const float cv = q8_0_coded_value(xv, amax);
+                    const __half hi = __float2half_rn(cv);
+                    xh[i] = hi;
+                    xh[d + i] = __float2half_rn(cv - __half2float(hi));
+                } else {
+                    xh[i] = __float2half_rn(xv);
+                }
                 if (c == 0 && a.x_next) a.x_next[static_cast<int64_t>(l) * d + i] = __bfloat16_as_ushort(xb);
             }
             __syncthreads();   // (slog is read again by the next layer's selection)
@@ -961,14 +985,14 @@ namespace {
 bool g_decode_ok[64] = {};
 int g_decode_ctas[64] = {};
 
-template <int FMT, int ACT, int ROUTE>
+template <int FMT, int ACT, int ROUTE, bool AQ = false>
 bool configure_one() {
     const int max_smem = static_cast<int>(decode_max_smem());
-    if (cudaFuncSetAttribute(decode_layer_kernel<FMT, ACT, ROUTE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_layer_kernel<FMT, ACT, ROUTE, AQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              max_smem) != cudaSuccess)
         return false;
     int per_sm = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel<FMT, ACT, ROUTE>,
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel<FMT, ACT, ROUTE, AQ>,
                                                                         kDecThreads, max_smem);
     return e == cudaSuccess && per_sm >= 1;
 }
@@ -985,6 +1009,9 @@ cudaError_t configure_decode_kernel(int dev, int num_sms) {
     if (!configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteLocal>() ||
         !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteWide>() ||
         !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteSupplied>() ||
+        !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteLocal, true>() ||
+        !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteWide, true>() ||
+        !configure_one<MOE_W_Q8_0, MOE_ACT_SWIGLU, kRouteSupplied, true>() ||
         !configure_one<MOE_W_INT8PC, MOE_ACT_SWIGLU, kRouteLocal>() ||
         !configure_one<MOE_W_INT8PC, MOE_ACT_SWIGLU, kRouteWide>() ||
         !configure_one<MOE_W_INT8PC, MOE_ACT_SWIGLU, kRouteSupplied>() ||
@@ -1005,11 +1032,11 @@ cudaError_t configure_decode_kernel(int dev, int num_sms) {
 // CTAs of the decode kernel on this device (0: not available).
 int decode_ctas(int dev) { return (dev >= 0 && dev < 64 && g_decode_ok[dev]) ? g_decode_ctas[dev] : 0; }
 
-template <int FMT, int ACT>
+template <int FMT, int ACT, bool AQ = false>
 static cudaError_t launch_decode_route(const cudaLaunchConfig_t& cfg, const DecodeArgs& a, int route) {
-    if (route == kRouteSupplied) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<FMT, ACT, kRouteSupplied>, a);
-    if (route == kRouteWide) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<FMT, ACT, kRouteWide>, a);
-    return cudaLaunchKernelEx(&cfg, decode_layer_kernel<FMT, ACT, kRouteLocal>, a);
+    if (route == kRouteSupplied) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<FMT, ACT, kRouteSupplied, AQ>, a);
+    if (route == kRouteWide) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<FMT, ACT, kRouteWide, AQ>, a);
+    return cudaLaunchKernelEx(&cfg, decode_layer_kernel<FMT, ACT, kRouteLocal, AQ>, a);
 }
 
 cudaError_t launch_decode_layer(const DecodeArgs& a, int wfmt, int act, size_t smem, int ctas, cudaStream_t s) {
@@ -1026,6 +1053,7 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, int wfmt, int act, size_t s
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     const int route = a.idx_in ? kRouteSupplied : (a.E > kLocalRankMaxE ? kRouteWide : kRouteLocal);
+    if (wfmt == MOE_W_Q8_0 && a.act_q) return launch_decode_route<MOE_W_Q8_0, MOE_ACT_SWIGLU, true>(cfg, a, route);
     if (wfmt == MOE_W_Q8_0) return launch_decode_route<MOE_W_Q8_0, MOE_ACT_SWIGLU>(cfg, a, route);
     if (wfmt == MOE_W_INT8PC) return launch_decode_route<MOE_W_INT8PC, MOE_ACT_SWIGLU>(cfg, a, route);
     if (act == MOE_ACT_SWIGLU) return launch_decode_route<MOE_W_NVFP4, MOE_ACT_SWIGLU>(cfg, a, route);

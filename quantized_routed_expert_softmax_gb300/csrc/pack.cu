@@ -112,11 +112,7 @@ __global__ void __launch_bounds__(256) act_q8_0_kernel(const void* __restrict__ 
         const float x = xt == MOE_F32 ? static_cast<const float*>(src)[o]
                                       : bf16_bits_to_f32(static_cast<const uint16_t*>(src)[o]);
         const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x)));
-        const float amax = __uint_as_float(amax_bits);
-        const float d = __fdiv_rn(amax, 127.0f);
-        const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
-        const int q = static_cast<int>(roundf(__fmul_rn(x, id)));
-        const float v = static_cast<float>(q) * __half2float(__float2half_rn(d));
+        const float v = q8_0_coded_value(x, __uint_as_float(amax_bits));
         dst[o] = v;
         if (hi) {
             const __half h = __float2half_rn(v);

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from oracle_bridge import assert_close, check_act_quant, coded_q8_0, oracle_layer
+from oracle_bridge import assert_close, check_act_quant, coded_q8_0, oracle_layer, to_numpy_x
 from quantized_routed_expert_softmax_gb300 import layers, native, synth
 
 pytestmark = pytest.mark.gpu
@@ -87,10 +87,12 @@ def test_layer_activation_quantised_parity(name, T, path):
     check_act_quant(w, ol, np.arange(T), out, tr, ref)
     # deterministic: a second call is bit-identical
     assert np.array_equal(L.forward(xt).cpu().numpy().view(np.uint32), out.view(np.uint32))
-    # two more launches than the unquantised path on the same kernels (one token: not the one-kernel layer)
-    plain = native.MoELayer(w.d, w.f, w.E, w.k, w.act, w.wfmt, L.router_w, L.gate_up, L.down,
-                            path="gemv" if (T == 1 and path == "auto") else path)
-    assert L.launches(T) == plain.launches(T) + 2
+    if T == 1 and path == "auto" and w.act == "swiglu":
+        assert L.launches(T) == 1   # the one-kernel layer codes x and h itself
+    else:   # two more launches than the unquantised path on the same kernels
+        plain = native.MoELayer(w.d, w.f, w.E, w.k, w.act, w.wfmt, L.router_w, L.gate_up, L.down,
+                                path="gemv" if (T == 1 and path == "auto") else path)
+        assert L.launches(T) == plain.launches(T) + 2
 
 
 def test_activation_quantised_differs_from_plain():
@@ -110,8 +112,57 @@ def test_activation_quantised_noalloc_and_stack():
     a = L.forward(x)
     assert np.array_equal(L.forward_noalloc(x).cpu().numpy().view(np.uint32), a.cpu().numpy().view(np.uint32))
     st = native.MoEStack([L])
-    assert st.launches() > 1                    # layer by layer: the one-kernel layer reads unquantised inputs
+    assert st.launches() == 1                   # the one-kernel layer codes x and h itself
     assert np.array_equal(st.forward(x).cpu().numpy().view(np.uint32), a.cpu().numpy().view(np.uint32))
+    # the separate kernels on the same layer: the same codes and routing, outputs within tolerance
+    tr1, tr2 = {}, {}
+    a1 = L.forward(x, trace=tr1).cpu().numpy()
+    L.set_path("gemv")
+    assert L.launches(1) > 1
+    a2 = L.forward(x, trace=tr2).cpu().numpy()
+    assert np.array_equal(tr1["idx"].cpu().numpy(), tr2["idx"].cpu().numpy())
+    assert_close(a1, a2.astype(np.float64), what="one kernel vs separate kernels")
+
+
+# A stack of coded layers as one kernel: bitwise equal to its layers glued by the stand-alone
+# RMS-norm, each layer against the oracle's coded path on its own input.  A stack whose layers
+# code differently runs layer by layer.
+def test_activation_quantised_stack_one_kernel():
+    w = synth.Workload("aq_st", d=1024, f=192, E=64, k=8, act="swiglu", wfmt="q8_0", x_dtype="bf16", layers=3)
+    n = 3
+    ls = [layers.build_layer(w, layer=l, source="numpy", act_quant="q8_0") for l in range(n)]
+    st = native.MoEStack(ls)
+    assert st.launches(True) == 1
+    x0 = synth.tokens_cuda(w, 1, tag="aq_stack")
+    xn = torch.zeros((n, w.d), dtype=torch.bfloat16, device="cuda")
+    outs = torch.full((n, w.d), float("nan"), device="cuda")
+    routing = {}
+    st.forward(x0, outs=outs, x_next=xn, routing=routing)
+    x = x0
+    for l, L in enumerate(ls):
+        tr = {}
+        o = L.forward(x, trace=tr)
+        assert np.array_equal(o.cpu().numpy().view(np.uint32), outs[l:l + 1].cpu().numpy().view(np.uint32)), l
+        assert np.array_equal(tr["idx"].cpu().numpy(), routing["idx"][l:l + 1].cpu().numpy())
+        ol = oracle_layer(w, synth.router_weight(w, l), lambda e, l=l: synth.expert_weights(w, l, e)[0],
+                          lambda e, l=l: synth.expert_weights(w, l, e)[1], range(w.E))
+        ref = ol.forward(to_numpy_x(x), act_q8=True)
+        assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
+        check_act_quant(w, ol, np.arange(1), o.cpu().numpy(), tr, ref)
+        x = native.rmsnorm_bf16(o)
+        assert torch.equal(x.view(torch.int16), xn[l:l + 1].view(torch.int16)), l
+    assert torch.equal(st.forward(x0).view(torch.int32), outs.view(torch.int32))
+    # mixed: the first layer coded, the others not
+    plain = [layers.build_layer(w, layer=l, source="numpy") for l in range(1, n)]
+    mixed = native.MoEStack([ls[0]] + plain)
+    assert mixed.launches(True) == 1 + 1 + 2 * 2   # one kernel per layer, a norm after each
+    mo = torch.full((n, w.d), float("nan"), device="cuda")
+    mixed.forward(x0, outs=mo)
+    x = x0
+    for l, L in enumerate([ls[0]] + plain):
+        o = L.forward(x)
+        assert np.array_equal(o.cpu().numpy().view(np.uint32), mo[l:l + 1].cpu().numpy().view(np.uint32)), l
+        x = native.rmsnorm_bf16(o)
 
 
 @pytest.mark.parametrize("name,T,tile", [("gemma", 1, None), ("gemma", 4, None), ("minimax", 4096, 64)])
