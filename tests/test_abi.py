@@ -167,3 +167,17 @@ def test_stack_validation(L):
     assert call(two, 2, x=FAKE + 2) == 3           # misaligned x
     assert call(two, 2, ws=0) == 4                 # no workspace
     assert call(two, 2, nbytes=need1 - 1) == 4     # workspace too small
+
+
+def test_stack_launch_count_sums_its_layers(L):
+    # without a GPU no layer takes the one-kernel path: the stack runs layer by layer, each
+    # layer's own launches and a norm after each; a coded layer (two coding launches more) and
+    # a plain one count their own launches
+    one = L.moe_layer_forward_launches(ctypes.byref(_desc()), 1, 0)
+    coded = L.moe_layer_forward_launches(ctypes.byref(_desc(act_quant=1)), 1, 0)
+    assert one > 1 and coded == one + 2
+    mixed = (native.LayerDesc * 3)(_desc(act_quant=1), _desc(), _desc())
+    assert L.moe_stack_forward_launches(mixed, 3, 1) == (coded + 1) + 2 * (one + 1)
+    assert L.moe_stack_forward_launches(mixed, 3, 0) == (coded + 1) + 2 * (one + 1) - 1
+    same = (native.LayerDesc * 3)(_desc(), _desc(), _desc())
+    assert L.moe_stack_forward_launches(same, 3, 1) == 3 * (one + 1)
