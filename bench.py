@@ -525,7 +525,7 @@ def run_ours(args, rank, world, local_rank, prebuilt=None):
                 gu_ms.append(lay[1].elapsed_time(lay[2]))
                 dn_ms.append(lay[2].elapsed_time(lay[3]))
                 cb_ms.append(lay[3].elapsed_time(lay[4]))
-    # One token on Q8_0 SwiGLU layers runs as ONE kernel per layer (the library reports one
+    # One token on the one-kernel formats runs as ONE kernel per layer (the library reports one
     # launch): then that kernel is the one measured, between the first two boundaries (the
     # later boundaries coincide with the second), with all the layer's bytes as its work.
     one_kernel = stack[0].launches(T, supplied) == 1
@@ -557,7 +557,10 @@ def run_ours(args, rank, world, local_rank, prebuilt=None):
         gu_bytes = tr_bytes["gate_up_per_layer"]
         gu_flops = 2 * T * w.k * w.rows_gu * w.d                # useful gate.up FLOP per layer
     achieved = gu_bytes / (gu_us * 1e-6) / 1e9
-    traffic = measured_traffic(args.workload, T, layers) if (stack_obj is not None or not one_kernel) else None
+    # (the captures cover the plain configurations only: uncoded inputs, device-resident weights)
+    captured = aq == "none" and not host_w
+    traffic = measured_traffic(args.workload, T, layers) if captured and (stack_obj is not None or not one_kernel) \
+        else None
     # Which expert kernels run (the library's AUTO rule): the tensor-core GEMMs when an expert
     # sees at least 8 tokens on average and the shape allows them, else the GEMVs.
     gemm = (T * w.k >= 8 * w.E and w.f % 64 == 0 and (w.act == "swiglu" or w.f % 128 == 0))
