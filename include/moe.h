@@ -309,10 +309,11 @@ moe_status moe_rmsnorm_bf16(const float* x, int64_t T, int64_t d, float eps, uin
  * idx, w   optional device int32 / fp32 [n_layers][k]: each layer's routing, or both NULL.
  * workspace at least moe_layer_workspace_bytes(descs, 1) bytes, zero-filled before its first
  *          use (as for moe_layer_forward).
- * With Q8_0 SwiGLU or NVFP4 ReLU^2 layers, path AUTO, at most 64 layers and a device that supports
- * cooperative launches, the whole stack is ONE kernel launch (one CTA per SM, the RMS-norm
- * between layers inside it, bitwise equal to the layer-by-layer result); otherwise each
- * layer is a moe_layer_forward call followed by the RMS-norm.
+ * With Q8_0 or INT8PC SwiGLU layers (also with act_quant = MOE_ACTQ_Q8_0) or NVFP4 ReLU^2 or
+ * SwiGLU layers, path AUTO, at most 64 layers that share act_quant and flags, and a device that
+ * supports cooperative launches, the whole stack is ONE kernel launch (one CTA per SM, the
+ * RMS-norm between layers inside it, bitwise equal to the layer-by-layer result); otherwise
+ * each layer is a moe_layer_forward call followed by the RMS-norm.
  * Errors: those of moe_layer_forward, and SHAPE when the descriptors differ in shape.
  */
 moe_status moe_stack_forward(const moe_layer_desc* descs, int32_t n_layers, const void* x, moe_dtype xt, float eps,
